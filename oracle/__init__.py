@@ -1,0 +1,166 @@
+"""CPU oracle for C = alpha*op(A)*op(B) + beta*C (FP16/BF16 in, FP64 reference).
+
+TEST INFRASTRUCTURE ONLY.  Only the test-suite, ``__graft_entry__.smoke()`` and
+the ``cpu_baseline`` / ``--impl reference`` legs of ``bench.py`` may import this
+package.  The CUDA library never imports, links or calls it, and this package
+imports nothing from the CUDA library; the two share only the input bit
+patterns made by the seeded workload generator.
+
+The arithmetic lives in ``oracle.c`` (plain C, binary64; its header names the
+page passages each step follows).  This module builds it with gcc and wraps it
+with ctypes.  Inputs are numpy arrays of raw bit patterns (uint16 for FP16/BF16,
+uint32 or float32 for FP32).
+
+Parity status: every entry point is pinned by ``tests/test_oracle_*.py``
+(exhaustive decode, IEEE rounding tables and exhaustive midpoints, exact
+rational brute force, closed forms and invariants).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+F16, BF16, F32 = 0, 1, 2
+_HERE = os.path.dirname(os.path.abspath(__file__))
+SRC = os.path.join(_HERE, "oracle.c")
+LIB_PATH = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_default = None
+
+
+def compile_source(src: str, out: str) -> str:
+    """gcc -O2 -ffp-contract=off (OpenMP when available) -> shared library."""
+    base = ["gcc", "-O2", "-ffp-contract=off", "-fno-fast-math", "-std=gnu11",
+            "-shared", "-fPIC", src, "-o", out + ".tmp", "-lm"]
+    try:
+        subprocess.run(base[:1] + ["-fopenmp"] + base[1:], check=True, capture_output=True)
+    except subprocess.CalledProcessError:
+        subprocess.run(base, check=True, capture_output=True)   # no OpenMP: 1 thread
+    os.replace(out + ".tmp", out)
+    return out
+
+
+def build(force: bool = False) -> str:
+    if not force and os.path.exists(LIB_PATH) and \
+            os.path.getmtime(LIB_PATH) >= os.path.getmtime(SRC):
+        return LIB_PATH
+    return compile_source(SRC, LIB_PATH)
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data
+
+
+def _prep(x, c=False):
+    if x is None:
+        return None
+    x = np.ascontiguousarray(x)
+    if c and x.dtype == np.float32:
+        return x.view(np.uint32)
+    return x
+
+
+class Oracle:
+    """ctypes wrapper around one build of oracle.c."""
+
+    def __init__(self, path: str):
+        lib = ctypes.CDLL(path)
+        i64, vp, dp = ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p
+        lib.oracle_decode_f16.restype = ctypes.c_double
+        lib.oracle_decode_f16.argtypes = [ctypes.c_uint16]
+        lib.oracle_decode_bf16.restype = ctypes.c_double
+        lib.oracle_decode_bf16.argtypes = [ctypes.c_uint16]
+        lib.oracle_round_f16.restype = ctypes.c_uint16
+        lib.oracle_round_f16.argtypes = [ctypes.c_double]
+        lib.oracle_round_bf16.restype = ctypes.c_uint16
+        lib.oracle_round_bf16.argtypes = [ctypes.c_double]
+        lib.oracle_round_f32.restype = ctypes.c_float
+        lib.oracle_round_f32.argtypes = [ctypes.c_double]
+        common = [ctypes.c_char, ctypes.c_char, i64, i64, i64,
+                  ctypes.c_float, vp, i64, vp, i64, ctypes.c_float, vp, i64,
+                  ctypes.c_int, ctypes.c_int]
+        lib.oracle_gemm.restype = ctypes.c_int
+        lib.oracle_gemm.argtypes = common + [dp, dp, ctypes.c_int]
+        lib.oracle_gemm_sampled.restype = ctypes.c_int
+        lib.oracle_gemm_sampled.argtypes = common + [i64, vp, vp, dp, dp, ctypes.c_int]
+        lib.oracle_round_output.restype = ctypes.c_int
+        lib.oracle_round_output.argtypes = [ctypes.c_int, i64, dp, vp]
+        lib.oracle_max_threads.restype = ctypes.c_int
+        lib.oracle_max_threads.argtypes = []
+        self.lib = lib
+        self.path = path
+
+    def max_threads(self) -> int:
+        return int(self.lib.oracle_max_threads())
+
+    def decode_scalar(self, code: int, dtype: int) -> float:
+        fn = self.lib.oracle_decode_f16 if dtype == F16 else self.lib.oracle_decode_bf16
+        return float(fn(int(code)))
+
+    def decode(self, codes, dtype: int) -> np.ndarray:
+        """Decode uint16 bit patterns (FP16 or BF16) to float64, one at a time."""
+        fn = self.lib.oracle_decode_f16 if dtype == F16 else self.lib.oracle_decode_bf16
+        flat = np.asarray(codes, dtype=np.uint16).ravel()
+        return np.array([fn(int(c)) for c in flat], dtype=np.float64)
+
+    def round_scalar(self, x: float, dtype: int) -> int:
+        if dtype == F16:
+            return int(self.lib.oracle_round_f16(float(x)))
+        if dtype == BF16:
+            return int(self.lib.oracle_round_bf16(float(x)))
+        raise ValueError("round_scalar: F16 or BF16 only")
+
+    def round_output(self, r, c_dtype: int) -> np.ndarray:
+        """Round binary64 results to the output format: float32 values for F32,
+        uint16 bit patterns for F16/BF16."""
+        r = np.ascontiguousarray(r, dtype=np.float64)
+        out = np.empty(r.shape, dtype=np.float32 if c_dtype == F32 else np.uint16)
+        st = self.lib.oracle_round_output(c_dtype, r.size, r.ctypes.data, out.ctypes.data)
+        if st != 0:
+            raise ValueError(f"oracle_round_output failed ({st})")
+        return out
+
+    def gemm(self, transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc,
+             ab_dtype, c_dtype, nthreads: int = 0):
+        """Full oracle.  A, B: uint16 codes in their stored layout (row pitch
+        lda/ldb); C: stored M x ldc codes / float32, or None when beta == 0.
+        Returns (R, S), float64 M x N arrays."""
+        A, B, C = _prep(A), _prep(B), _prep(C, c=True)
+        R = np.empty((M, N), dtype=np.float64)
+        S = np.empty((M, N), dtype=np.float64)
+        st = self.lib.oracle_gemm(transA.encode(), transB.encode(), M, N, K, float(alpha),
+                                  _ptr(A), lda, _ptr(B), ldb, float(beta), _ptr(C), ldc,
+                                  ab_dtype, c_dtype, R.ctypes.data, S.ctypes.data, nthreads)
+        if st != 0:
+            raise ValueError(f"oracle_gemm failed ({st})")
+        return R, S
+
+    def gemm_sampled(self, transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc,
+                     ab_dtype, c_dtype, rows, cols, nthreads: int = 0):
+        """The oracle evaluated at (rows[s], cols[s]) only.  Returns (R, S), 1-D."""
+        A, B, C = _prep(A), _prep(B), _prep(C, c=True)
+        rows = np.ascontiguousarray(rows, dtype=np.int64)
+        cols = np.ascontiguousarray(cols, dtype=np.int64)
+        R = np.empty(rows.shape, dtype=np.float64)
+        S = np.empty(rows.shape, dtype=np.float64)
+        st = self.lib.oracle_gemm_sampled(
+            transA.encode(), transB.encode(), M, N, K, float(alpha),
+            _ptr(A), lda, _ptr(B), ldb, float(beta), _ptr(C), ldc,
+            ab_dtype, c_dtype, rows.size, rows.ctypes.data, cols.ctypes.data,
+            R.ctypes.data, S.ctypes.data, nthreads)
+        if st != 0:
+            raise ValueError(f"oracle_gemm_sampled failed ({st})")
+        return R, S
+
+
+def get() -> Oracle:
+    """The oracle built from oracle.c (compiled on first use)."""
+    global _default
+    with _lock:
+        if _default is None:
+            _default = Oracle(build())
+        return _default

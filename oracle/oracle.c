@@ -1,0 +1,324 @@
+/*
+ * oracle.c -- plain, slow, obviously-correct CPU oracle for the mixed-precision
+ * dense GEMM   C = alpha * op(A) * op(B) + beta * C.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product path may include, link or
+ * call this file: only the test-suite, the smoke check and the CPU-baseline leg
+ * of the benchmark use it.  It shares no code with the CUDA library; the two
+ * meet only in the 16-bit input bit patterns produced by the seeded workload
+ * generator.
+ *
+ * What it computes, and the passage each step follows:
+ *
+ *   - Semantics.  "C[i][j] accumulates A[i][k] * B[k][j]" -- the naive i-j-k
+ *     triple loop of the SGEMM tutorial page (section 3.1), and "C = A * B + C"
+ *     of the CATLASS page (section 2.1).  alpha/beta scaling and op() are the
+ *     BLAS reading of that formula (the pages never name alpha or beta):
+ *       r_ij = alpha * sum_k op(A)_ik op(B)_kj + beta * C_ij.
+ *   - Precision.  Inputs are FP16 or BF16; accumulation must be wider than the
+ *     inputs (DeepGEMM page, section 6.2; CATLASS page, section 3.4).  The
+ *     oracle decodes every input exactly to binary64 and accumulates in
+ *     binary64, so it is strictly more accurate than any FP32-accumulating
+ *     kernel.  An FP16 x FP16 (or BF16 x BF16) product has at most 22
+ *     significant bits and is exact in binary64.
+ *   - Formats.  FP16 = 1 sign, 5 exponent, 10 mantissa bits (max 65504, min
+ *     normal 2^-14 ~ 6e-5, min subnormal 2^-24 ~ 6e-8); BF16 = 1 sign, 8
+ *     exponent, 7 mantissa bits (max ~3.4e38, min normal 2^-126 ~ 1e-38)
+ *     (CATLASS page, section 3.2).  The decoders below follow these field
+ *     splits and the IEEE-754 interpretation of each field.
+ *   - Layout.  Row-major with a leading dimension: element (m, n) of a stored
+ *     matrix sits at offset m * ld + n (CATLASS page, section 1.3).
+ *     op(X) = X for 'N'/'n', X^T for 'T'/'t'.  A with 'N' is stored M x K,
+ *     with 'T' it is stored K x M; B with 'N' is stored K x N, with 'T' it is
+ *     stored N x K.  C is M x N.
+ *   - Output rounding.  FP32 output is the binary64 result converted by the C
+ *     language's own double -> float conversion (round to nearest even).
+ *     FP16/BF16 output is rounded directly from binary64 to the 16-bit format
+ *     with round-to-nearest, ties-to-even, written out below from the format
+ *     definition (one rounding, never through FP32).  The pages do not state a
+ *     rounding mode; round-to-nearest-even is the IEEE-754 default.
+ *   - Quick returns (BLAS convention, pages silent): with K == 0 or
+ *     alpha == 0 the result is beta * C and A, B are not read; with
+ *     beta == 0, C is not read, so NaN/Inf already in C does not propagate.
+ *
+ * Alongside r_ij the oracle returns S_ij = sum_k |op(A)_ik * op(B)_kj|, the
+ * scale the acceptance tolerance is expressed in.
+ *
+ * Build: gcc -O2 -ffp-contract=off -fopenmp -shared -fPIC (no fast-math, no FMA
+ * contraction, so every multiply and add is a separately rounded binary64 op).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+enum { OR_F16 = 0, OR_BF16 = 1, OR_F32 = 2 };
+enum { OR_OK = 0, OR_BAD_ARG = 1, OR_NO_MEM = 2 };
+
+/* ---------------------------------------------------------------- decoders */
+
+/* binary16: value = (-1)^s * 2^(e-15) * 1.m  (e in 1..30),
+ *                   (-1)^s * 2^-14 * 0.m     (e == 0, subnormal),
+ *                   +-inf / NaN              (e == 31). */
+double oracle_decode_f16(uint16_t h) {
+    int s = (h >> 15) & 1;
+    int e = (h >> 10) & 0x1F;
+    int m = h & 0x3FF;
+    double v;
+    if (e == 0) {
+        v = ldexp((double)m, -24);           /* m * 2^-10 * 2^-14 */
+    } else if (e == 31) {
+        v = (m == 0) ? INFINITY : NAN;
+    } else {
+        v = ldexp((double)(1024 + m), e - 25); /* (1 + m/2^10) * 2^(e-15) */
+    }
+    return s ? -v : v;
+}
+
+/* bfloat16: the upper half of a binary32: value = (-1)^s * 2^(e-127) * 1.m
+ * (e in 1..254), (-1)^s * 2^-126 * 0.m (e == 0), +-inf / NaN (e == 255). */
+double oracle_decode_bf16(uint16_t h) {
+    int s = (h >> 15) & 1;
+    int e = (h >> 7) & 0xFF;
+    int m = h & 0x7F;
+    double v;
+    if (e == 0) {
+        v = ldexp((double)m, -133);           /* m * 2^-7 * 2^-126 */
+    } else if (e == 255) {
+        v = (m == 0) ? INFINITY : NAN;
+    } else {
+        v = ldexp((double)(128 + m), e - 134); /* (1 + m/2^7) * 2^(e-127) */
+    }
+    return s ? -v : v;
+}
+
+double oracle_decode_f32(uint32_t u) {
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+/* --------------------------------------------------------------- rounders */
+
+/* Round a non-negative finite q (q < 2^53) to the nearest integer, ties to
+ * even.  q - floor(q) is exact for such q. */
+static double rne_integer(double q) {
+    double fl = floor(q);
+    double frac = q - fl;
+    if (frac > 0.5) return fl + 1.0;
+    if (frac < 0.5) return fl;
+    return (fmod(fl, 2.0) == 0.0) ? fl : fl + 1.0;
+}
+
+/*
+ * Generic direct binary64 -> small binary format rounding, round to nearest,
+ * ties to even.  A format with `mbits` stored mantissa bits and exponent bias
+ * `bias` (exponent field width `ebits`) has, for |x| in the binade
+ * [2^e, 2^(e+1)), a grid spacing of 2^(e - mbits); below the smallest normal
+ * 2^(1-bias) the spacing stays 2^(1 - bias - mbits) (subnormals).  The value is
+ * scaled onto that grid (an exact power-of-two scaling), rounded to an integer
+ * n, and re-encoded; a carry to n == 2^(mbits+1) moves to the next binade, and
+ * an exponent field that reaches all-ones means overflow to infinity.
+ */
+static uint16_t round_to_small(double x, int ebits, int mbits, int bias) {
+    const uint16_t sign = signbit(x) ? (uint16_t)(1u << (ebits + mbits)) : 0;
+    const uint16_t exp_all_ones = (uint16_t)(((1u << ebits) - 1u) << mbits);
+    if (isnan(x)) return (uint16_t)(exp_all_ones | (1u << (mbits - 1)));  /* quiet NaN */
+    double a = fabs(x);
+    if (isinf(a)) return sign | exp_all_ones;
+    if (a == 0.0) return sign;
+
+    int E;
+    (void)frexp(a, &E);           /* a = f * 2^E, f in [0.5, 1) -> binade exponent E-1 */
+    int e = E - 1;
+    const int emin = 1 - bias;    /* exponent of the smallest normal */
+    int ulp_exp = (e < emin ? emin : e) - mbits;
+    double n = rne_integer(ldexp(a, -ulp_exp));
+    const double hidden = ldexp(1.0, mbits);      /* 2^mbits */
+    if (n < hidden) {
+        /* subnormal (only reachable when ulp_exp is the subnormal spacing) */
+        return sign | (uint16_t)n;
+    }
+    if (n >= 2.0 * hidden) {      /* carried into the next binade */
+        n = n / 2.0;
+        ulp_exp += 1;
+    }
+    int efield = ulp_exp + mbits + bias;
+    if (efield >= (1 << ebits) - 1) return sign | exp_all_ones;   /* overflow -> inf */
+    return sign | (uint16_t)((unsigned)efield << mbits) | (uint16_t)(n - hidden);
+}
+
+uint16_t oracle_round_f16(double x) { return round_to_small(x, 5, 10, 15); }
+uint16_t oracle_round_bf16(double x) { return round_to_small(x, 8, 7, 127); }
+
+/* FP32 output: the C language's double -> float conversion (round to nearest
+ * even under the default floating-point environment, overflow to +-inf). */
+float oracle_round_f32(double x) { return (float)x; }
+
+/* ------------------------------------------------------------------- GEMM */
+
+static double decode_in(int dt, const void* p, int64_t idx) {
+    const uint16_t* h = (const uint16_t*)p;
+    return dt == OR_F16 ? oracle_decode_f16(h[idx]) : oracle_decode_bf16(h[idx]);
+}
+
+static double decode_c(int dt, const void* p, int64_t idx) {
+    if (dt == OR_F32) return oracle_decode_f32(((const uint32_t*)p)[idx]);
+    return decode_in(dt, p, idx);
+}
+
+static int is_n(char t) { return t == 'N' || t == 'n'; }
+static int is_t(char t) { return t == 'T' || t == 't'; }
+
+static int check_args(char transA, char transB, int64_t M, int64_t N, int64_t K,
+                      int64_t lda, int64_t ldb, int64_t ldc, int ab_dtype, int c_dtype) {
+    if (!(is_n(transA) || is_t(transA)) || !(is_n(transB) || is_t(transB))) return OR_BAD_ARG;
+    if (M < 0 || N < 0 || K < 0) return OR_BAD_ARG;
+    if (ab_dtype != OR_F16 && ab_dtype != OR_BF16) return OR_BAD_ARG;
+    if (c_dtype != OR_F16 && c_dtype != OR_BF16 && c_dtype != OR_F32) return OR_BAD_ARG;
+    int64_t a_cols = is_n(transA) ? K : M;
+    int64_t b_cols = is_n(transB) ? N : K;
+    if (lda < (a_cols > 1 ? a_cols : 1)) return OR_BAD_ARG;
+    if (ldb < (b_cols > 1 ? b_cols : 1)) return OR_BAD_ARG;
+    if (ldc < (N > 1 ? N : 1)) return OR_BAD_ARG;
+    return OR_OK;
+}
+
+/* op(A)_ik and op(B)_kj as stored-matrix offsets (row-major, offset = row*ld+col). */
+static int64_t a_off(char transA, int64_t i, int64_t k, int64_t lda) {
+    return is_n(transA) ? i * lda + k : k * lda + i;
+}
+static int64_t b_off(char transB, int64_t k, int64_t j, int64_t ldb) {
+    return is_n(transB) ? k * ldb + j : j * ldb + k;
+}
+
+/*
+ * Full oracle.  R and S are dense M x N row-major binary64 outputs.
+ * A is decoded once into opA (M x K), B once into opB (K x N); then
+ *   for i: for k: for j: acc[j] += opA[i][k] * opB[k][j]
+ * which, for every (i, j), adds the K products in increasing k -- the same
+ * sum, in the same order, as the i-j-k loop of the definition.
+ */
+int oracle_gemm(char transA, char transB, int64_t M, int64_t N, int64_t K,
+                float alpha, const void* A, int64_t lda,
+                const void* B, int64_t ldb,
+                float beta, const void* C, int64_t ldc,
+                int ab_dtype, int c_dtype,
+                double* R, double* S, int nthreads) {
+    int st = check_args(transA, transB, M, N, K, lda, ldb, ldc, ab_dtype, c_dtype);
+    if (st != OR_OK) return st;
+    if (M == 0 || N == 0) return OR_OK;
+    const double al = (double)alpha, be = (double)beta;
+    const int use_ab = (K > 0 && alpha != 0.0f);
+    double* opA = NULL;
+    double* opB = NULL;
+    if (use_ab) {
+        opA = (double*)malloc(sizeof(double) * (size_t)M * (size_t)K);
+        opB = (double*)malloc(sizeof(double) * (size_t)K * (size_t)N);
+        if (!opA || !opB) { free(opA); free(opB); return OR_NO_MEM; }
+        for (int64_t i = 0; i < M; ++i)
+            for (int64_t k = 0; k < K; ++k)
+                opA[i * K + k] = decode_in(ab_dtype, A, a_off(transA, i, k, lda));
+        for (int64_t k = 0; k < K; ++k)
+            for (int64_t j = 0; j < N; ++j)
+                opB[k * N + j] = decode_in(ab_dtype, B, b_off(transB, k, j, ldb));
+    }
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#pragma omp parallel for schedule(dynamic, 1)
+#endif
+    for (int64_t i = 0; i < M; ++i) {
+        double* acc = R + i * N;
+        double* sabs = S + i * N;
+        for (int64_t j = 0; j < N; ++j) { acc[j] = 0.0; sabs[j] = 0.0; }
+        if (use_ab) {
+            for (int64_t k = 0; k < K; ++k) {
+                const double a = opA[i * K + k];
+                const double* brow = opB + k * N;
+                for (int64_t j = 0; j < N; ++j) {
+                    double p = a * brow[j];          /* exact for 16-bit inputs */
+                    acc[j] = acc[j] + p;
+                    sabs[j] = sabs[j] + fabs(p);
+                }
+            }
+        }
+        for (int64_t j = 0; j < N; ++j) {
+            double r = use_ab ? al * acc[j] : 0.0;
+            if (be != 0.0) r = r + be * decode_c(c_dtype, C, i * ldc + j);
+            acc[j] = r;
+        }
+    }
+    free(opA);
+    free(opB);
+    return OR_OK;
+}
+
+/*
+ * Sampled oracle: the same definition evaluated only at the listed (row, col)
+ * positions, one K-long dot product each, for shapes too large for the full
+ * triple loop.  R[s], S[s] receive r and S at (rows[s], cols[s]).
+ */
+int oracle_gemm_sampled(char transA, char transB, int64_t M, int64_t N, int64_t K,
+                        float alpha, const void* A, int64_t lda,
+                        const void* B, int64_t ldb,
+                        float beta, const void* C, int64_t ldc,
+                        int ab_dtype, int c_dtype,
+                        int64_t nsamp, const int64_t* rows, const int64_t* cols,
+                        double* R, double* S, int nthreads) {
+    int st = check_args(transA, transB, M, N, K, lda, ldb, ldc, ab_dtype, c_dtype);
+    if (st != OR_OK) return st;
+    for (int64_t s = 0; s < nsamp; ++s)
+        if (rows[s] < 0 || rows[s] >= M || cols[s] < 0 || cols[s] >= N) return OR_BAD_ARG;
+    const double al = (double)alpha, be = (double)beta;
+    const int use_ab = (K > 0 && alpha != 0.0f);
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#pragma omp parallel for schedule(dynamic, 16)
+#endif
+    for (int64_t s = 0; s < nsamp; ++s) {
+        const int64_t i = rows[s], j = cols[s];
+        double acc = 0.0, sabs = 0.0;
+        if (use_ab) {
+            for (int64_t k = 0; k < K; ++k) {
+                double p = decode_in(ab_dtype, A, a_off(transA, i, k, lda)) *
+                           decode_in(ab_dtype, B, b_off(transB, k, j, ldb));
+                acc = acc + p;
+                sabs = sabs + fabs(p);
+            }
+        }
+        double r = use_ab ? al * acc : 0.0;
+        if (be != 0.0) r = r + be * decode_c(c_dtype, C, i * ldc + j);
+        R[s] = r;
+        S[s] = sabs;
+    }
+    return OR_OK;
+}
+
+/* Round `count` binary64 results to the output type: FP32 (float, written as
+ * its 32-bit pattern) or FP16/BF16 (16-bit patterns). */
+int oracle_round_output(int c_dtype, int64_t count, const double* R, void* out) {
+    if (c_dtype == OR_F32) {
+        float* o = (float*)out;
+        for (int64_t s = 0; s < count; ++s) o[s] = oracle_round_f32(R[s]);
+    } else if (c_dtype == OR_F16) {
+        uint16_t* o = (uint16_t*)out;
+        for (int64_t s = 0; s < count; ++s) o[s] = oracle_round_f16(R[s]);
+    } else if (c_dtype == OR_BF16) {
+        uint16_t* o = (uint16_t*)out;
+        for (int64_t s = 0; s < count; ++s) o[s] = oracle_round_bf16(R[s]);
+    } else {
+        return OR_BAD_ARG;
+    }
+    return OR_OK;
+}
+
+int oracle_max_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}

@@ -1,0 +1,383 @@
+"""The battery of checks that pins the CPU oracle to things other than itself.
+
+Each ``pin_*`` function takes an ``oracle.Oracle`` and raises AssertionError
+when the oracle disagrees with what the pages, the IEEE-754 format definitions
+or plain mathematics fix.  ``test_oracle_pins.py`` runs every pin against the
+real oracle (all must pass); ``test_oracle_mutants.py`` runs the battery against
+builds of oracle.c with one planted mistake each (at least one pin must fail).
+"""
+from __future__ import annotations
+
+import math
+import os
+from fractions import Fraction
+
+import numpy as np
+
+import exact
+from exact import F16, BF16, F32
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def _rng(seed):
+    return np.random.default_rng(seed)
+
+
+def _to_codes(values, dtype):
+    """float64 values that are exactly representable -> uint16 codes (torch)."""
+    import torch
+    tdt = torch.float16 if dtype == F16 else torch.bfloat16
+    t = torch.tensor(np.asarray(values, dtype=np.float64)).to(tdt)
+    back = t.to(torch.float64).numpy()
+    ok = (back == np.asarray(values)) | (np.isnan(back) & np.isnan(values))
+    assert ok.all(), "test input not representable"
+    return t.view(torch.int16).numpy().view(np.uint16).copy()
+
+
+def _random_codes(rng, shape, dtype, scale=1.0):
+    import torch
+    tdt = torch.float16 if dtype == F16 else torch.bfloat16
+    v = torch.from_numpy(rng.standard_normal(shape).astype(np.float32) * scale).to(tdt)
+    return v.view(torch.int16).numpy().view(np.uint16).copy()
+
+
+def _stored(rng, rows, cols, ld, dtype, maker):
+    """A rows x ld buffer with the logical block from `maker` and NaN padding."""
+    buf = np.full((rows, ld), 0x7E00 if dtype == F16 else 0x7FC0, dtype=np.uint16)
+    buf[:, :cols] = maker(rows, cols)
+    return buf
+
+
+# ----------------------------------------------------------------- formats
+
+def pin_decode_exhaustive(o):
+    """Every one of the 65536 FP16 and BF16 codes decodes to the value the
+    library's own conversion gives (NaN codes to NaN)."""
+    codes = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    for dt in (F16, BF16):
+        mine = o.decode(codes, dt)
+        lib = exact.codes_to_float64(codes, dt)
+        same = (mine == lib) | (np.isnan(mine) & np.isnan(lib))
+        assert same.all(), f"decode mismatch dtype={dt} at codes {np.flatnonzero(~same)[:5]}"
+        # signed zeros keep their sign
+        assert math.copysign(1.0, o.decode_scalar(0x8000, dt)) == -1.0
+
+
+def pin_page_format_limits(o):
+    """The printed format limits (CATLASS page, section 3.2)."""
+    path = os.path.join(GOLDEN, "format_limits.txt")
+    rows = [ln.split() for ln in open(path) if ln.strip() and not ln.startswith("#")]
+    assert len(rows) == 5
+    for fmt, qty, printed, code, tol in rows:
+        dt = F16 if fmt == "f16" else BF16
+        v = o.decode_scalar(int(code, 16), dt)
+        assert abs(v - float(printed)) <= float(tol) * float(printed), (fmt, qty, v)
+        if qty == "max":
+            # the next code up is infinity: values past the maximum overflow
+            assert math.isinf(o.decode_scalar(int(code, 16) + 1, dt))
+            assert o.round_scalar(v, dt) == int(code, 16)
+    # FP16: 65504 is the largest finite value; rounding past it goes to infinity
+    assert o.round_scalar(65504.0, F16) == 0x7BFF
+    assert o.round_scalar(1e6, F16) == 0x7C00
+
+
+def pin_round_ieee_table(o):
+    """Round-to-nearest-even facts that follow from the binary16/bfloat16
+    definitions (ties go to the code with an even last bit)."""
+    cases = [
+        (65504.0, F16, 0x7BFF),
+        (65519.99, F16, 0x7BFF),            # below the overflow midpoint
+        (65520.0, F16, 0x7C00),             # the midpoint 65504..65536 ties to even -> inf
+        (-65520.0, F16, 0xFC00),
+        (2.0 ** -25, F16, 0x0000),          # half of the smallest subnormal ties to 0
+        (3 * 2.0 ** -25, F16, 0x0002),      # 1.5 subnormal ulps ties up to 2 (even)
+        (2.0 ** -24, F16, 0x0001),
+        (1.0 + 2.0 ** -11, F16, 0x3C00),    # tie between 1 and 1+2^-10 -> 1 (even)
+        (1.0 + 3 * 2.0 ** -11, F16, 0x3C02),
+        (1.0, BF16, 0x3F80),
+        (1.0 + 2.0 ** -8, BF16, 0x3F80),    # tie -> 1 (even)
+        (1.0 + 3 * 2.0 ** -8, BF16, 0x3F82),  # tie -> 1 + 2^-6 (even)
+        (-0.0, F16, 0x8000),
+        (float("inf"), BF16, 0x7F80),
+        (3.3961775292304455e38, BF16, 0x7F7F),  # bf16 max
+        (3.4e38, BF16, 0x7F80),             # past max + half ulp -> inf
+        (2.0 ** -133, BF16, 0x0001),        # smallest bf16 subnormal
+        (2.0 ** -134, BF16, 0x0000),        # tie -> 0
+    ]
+    for x, dt, want in cases:
+        got = o.round_scalar(x, dt)
+        assert got == want, f"round({x!r}, {dt}) = {got:#06x}, want {want:#06x}"
+    for dt in (F16, BF16):
+        assert (o.round_scalar(float("nan"), dt) & 0x7FFF) > (0x7C00 if dt == F16 else 0x7F80)
+
+
+def pin_round_roundtrip_exhaustive(o):
+    """Every finite code, decoded by the library, rounds back to itself."""
+    for dt in (F16, BF16):
+        codes = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+        vals = exact.codes_to_float64(codes, dt)
+        fin = np.isfinite(vals)
+        out = o.round_output(vals[fin], dt)
+        # -0 and +0 both exist; the round trip keeps the sign bit
+        assert (out == codes[fin]).all(), f"roundtrip mismatch dtype={dt}"
+
+
+def pin_round_midpoints(o):
+    """Exhaustive over adjacent positive codes: the exact midpoint ties to the
+    even code, one double below it rounds down, one above rounds up."""
+    for dt in (F16, BF16):
+        tb = exact.table(dt)
+        vals = [float(v) for v in tb.vals]
+        lo = np.array(vals[:-1])
+        hi = np.array(vals[1:])
+        mid = (lo + hi) / 2.0          # exact: both are on a grid far coarser than binary64
+        below = np.nextafter(mid, 0.0)
+        above = np.nextafter(mid, np.inf)
+        codes_lo = np.array(tb.codes[:-1], dtype=np.uint16)
+        codes_hi = np.array(tb.codes[1:], dtype=np.uint16)
+        even = np.where(codes_lo % 2 == 0, codes_lo, codes_hi)
+        assert (o.round_output(mid, dt) == even).all(), f"midpoint ties dtype={dt}"
+        assert (o.round_output(below, dt) == codes_lo).all(), f"below-midpoint dtype={dt}"
+        assert (o.round_output(above, dt) == codes_hi).all(), f"above-midpoint dtype={dt}"
+        assert (o.round_output(-above, dt) == (codes_hi | 0x8000)).all()
+
+
+def pin_round_random_exact(o):
+    """Random doubles over the whole range vs exact rational round-to-nearest-even."""
+    rng = _rng(7)
+    for dt, lo_e, hi_e in ((F16, -30, 18), (BF16, -140, 130)):
+        e = rng.integers(lo_e, hi_e, 1500)
+        x = rng.uniform(1.0, 2.0, 1500) * np.ldexp(1.0, e) * rng.choice([-1.0, 1.0], 1500)
+        got = o.round_output(x, dt)
+        want = np.array([exact.exact_round(Fraction(float(v)), dt) for v in x], dtype=np.uint16)
+        assert (got == want).all(), f"random rounding dtype={dt}"
+
+
+def pin_f32_output(o):
+    """FP32 output is the IEEE double -> float conversion (numpy's cast)."""
+    rng = _rng(8)
+    x = rng.standard_normal(4000) * np.ldexp(1.0, rng.integers(-160, 140, 4000))
+    x = np.concatenate([x, [3.5e38, -3.5e38, 1e-46, np.nan]])
+    got = o.round_output(x, F32)
+    want = x.astype(np.float32)
+    same = (got.view(np.uint32) == want.view(np.uint32)) | (np.isnan(got) & np.isnan(want))
+    assert same.all()
+
+
+# -------------------------------------------------------------------- GEMM
+
+def _gemm_case(o, rng, M, N, K, ta, tb, dt, cdt, alpha, beta, pad, integer, sampled=False):
+    a_rows, a_cols = (M, K) if ta == "N" else (K, M)
+    b_rows, b_cols = (K, N) if tb == "N" else (N, K)
+    lda, ldb, ldc = max(a_cols, 1) + pad, max(b_cols, 1) + pad, max(N, 1) + pad
+
+    if integer:
+        mk = lambda r, c: _to_codes(rng.integers(-8, 9, (r, c)).astype(np.float64), dt)
+    else:
+        mk = lambda r, c: _random_codes(rng, (r, c), dt)
+    A = _stored(rng, a_rows, a_cols, lda, dt, mk)
+    B = _stored(rng, b_rows, b_cols, ldb, dt, mk)
+    C = None
+    if beta != 0:
+        if cdt == F32:
+            C = np.full((M, ldc), np.nan, dtype=np.float32)
+            cv = rng.integers(-8, 9, (M, N)) if integer else rng.standard_normal((M, N))
+            C[:, :N] = cv.astype(np.float32)
+        else:
+            C = _stored(rng, M, N, ldc, cdt, mk)
+
+    opA = exact.op_matrix(exact.codes_to_float64(A, dt), a_rows, a_cols, ta)
+    opB = exact.op_matrix(exact.codes_to_float64(B, dt), b_rows, b_cols, tb)
+    if C is None:
+        Cv = np.zeros((M, N))
+    elif cdt == F32:
+        Cv = C[:, :N].astype(np.float64)
+    else:
+        Cv = exact.codes_to_float64(C, cdt)[:, :N]
+    r_ex, s_ex = exact.exact_gemm(opA, opB, alpha, beta, Cv)
+
+    if sampled:
+        rows = np.array([i for i in range(M) for _ in range(N)], dtype=np.int64)
+        cols = np.array([j for _ in range(M) for j in range(N)], dtype=np.int64)
+        R, S = o.gemm_sampled(ta, tb, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc,
+                              dt, cdt, rows, cols)
+        R, S = R.reshape(M, N), S.reshape(M, N)
+    else:
+        R, S = o.gemm(ta, tb, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, dt, cdt)
+
+    for i in range(M):
+        for j in range(N):
+            ex, sx = r_ex[i][j], s_ex[i][j]
+            scale = abs(Fraction(float(np.float32(alpha)))) * sx + \
+                abs(Fraction(float(np.float32(beta))) * Fraction(float(Cv[i][j])))
+            err = abs(Fraction(float(R[i, j])) - ex)
+            if integer:
+                assert err == 0, (i, j, float(ex), R[i, j])
+            else:
+                assert err <= Fraction(2) ** -48 * scale + Fraction(1, 2 ** 1000), \
+                    (M, N, K, ta, tb, i, j, float(ex), R[i, j])
+            assert abs(Fraction(float(S[i, j])) - sx) <= Fraction(2) ** -48 * sx, (i, j)
+    if integer and cdt != F32:
+        got = o.round_output(R, cdt)
+        want = np.array([[exact.exact_round(r_ex[i][j], cdt) for j in range(N)]
+                         for i in range(M)], dtype=np.uint16).reshape(M, N)
+        assert (got == want).all()
+
+
+def pin_gemm_bruteforce(o):
+    """Tiny shapes against exact rational arithmetic: every transpose pair,
+    both input formats, all output formats, alpha/beta, padded leading
+    dimensions, full and sampled entry points."""
+    rng = _rng(11)
+    shapes = [(1, 1, 1), (2, 3, 5), (3, 2, 4), (5, 7, 3), (8, 8, 8), (4, 1, 7), (1, 6, 2)]
+    n = 0
+    for (M, N, K) in shapes:
+        for ta in "NT":
+            for tb in "NT":
+                dt = (F16, BF16)[n % 2]
+                cdt = (F32, F16, BF16)[n % 3]
+                alpha = (1.0, -0.5, 3.0, 0.3)[n % 4]
+                beta = (0.0, 1.0, -2.0, 0.7)[(n // 2) % 4]
+                pad = (0, 3)[(n // 3) % 2]
+                _gemm_case(o, rng, M, N, K, ta, tb, dt, cdt, alpha, beta, pad,
+                           integer=False, sampled=(n % 5 == 4))
+                n += 1
+
+
+def pin_gemm_integer_exact(o):
+    """Integer inputs make every sum exact: the oracle must equal the exact
+    rational result bit for bit, and its FP16/BF16 outputs must be the exact
+    round-to-nearest-even of it."""
+    rng = _rng(12)
+    n = 0
+    for (M, N, K) in [(3, 4, 5), (6, 5, 8), (2, 9, 1)]:
+        for ta in "NT":
+            for tb in "NT":
+                cdt = (F16, BF16, F32)[n % 3]
+                _gemm_case(o, rng, M, N, K, ta, tb, (F16, BF16)[n % 2], cdt,
+                           (1.0, 2.0, -1.0)[n % 3], (0.0, 1.0, -3.0)[(n + 1) % 3],
+                           (0, 2)[n % 2], integer=True, sampled=(n % 4 == 1))
+                n += 1
+
+
+def pin_identity_and_permutation(o):
+    """A * I = A and I * B = B exactly; A * P permutes columns exactly."""
+    rng = _rng(13)
+    for dt in (F16, BF16):
+        M, K = 9, 12
+        A = _random_codes(rng, (M, K), dt)
+        Av = exact.codes_to_float64(A, dt)
+        I = _to_codes(np.eye(K), dt)
+        for tb in "NT":
+            R, _ = o.gemm("N", tb, M, K, K, 1.0, A, K, I, K, 0.0, None, K, dt, dt)
+            assert (R == Av).all()
+            out = o.round_output(R, dt)
+            assert (exact.codes_to_float64(out, dt) == Av).all()
+        R, _ = o.gemm("N", "N", K, M, K, 1.0, I, K, A.T.copy(), M, 0.0, None, M, dt, dt)
+        assert (R == Av.T).all()
+        perm = rng.permutation(K)
+        P = np.zeros((K, K))
+        P[perm, np.arange(K)] = 1.0           # (A P)[:, j] = A[:, perm[j]]
+        R, _ = o.gemm("N", "N", M, K, K, 1.0, A, K, _to_codes(P, dt), K, 0.0, None, K, dt, F32)
+        assert (R == Av[:, perm]).all()
+
+
+def pin_all_ones(o):
+    """All-ones inputs: every entry equals K (and S equals K)."""
+    for dt in (F16, BF16):
+        for (M, N, K) in [(5, 7, 1), (4, 3, 257), (2, 2, 1000)]:
+            A = _to_codes(np.ones((M, K)), dt)
+            B = _to_codes(np.ones((N, K)), dt)
+            R, S = o.gemm("N", "T", M, N, K, 1.0, A, K, B, K, 0.0, None, N, dt, F32)
+            assert (R == K).all() and (S == K).all()
+
+
+def pin_rank1_closed_form(o):
+    """A_ik = x_i y_k, B_kj = y'_k z_j gives C_ij = x_i z_j sum_k y_k y'_k."""
+    rng = _rng(14)
+    vals = np.array([1.0, -1.0, 2.0, -2.0, 0.5, -0.5, 4.0, 0.25])
+    for dt in (F16, BF16):
+        M, N, K = 6, 5, 33
+        x, z = rng.choice(vals, M), rng.choice(vals, N)
+        y, yp = rng.choice(vals, K), rng.choice(vals, K)
+        A = _to_codes(np.outer(x, y), dt)
+        B = _to_codes(np.outer(yp, z), dt)
+        dot = sum(Fraction(float(a)) * Fraction(float(b)) for a, b in zip(y, yp))
+        R, _ = o.gemm("N", "N", M, N, K, 1.0, A, K, B, N, 0.0, None, N, dt, F32)
+        want = np.array([[float(Fraction(float(xi)) * Fraction(float(zj)) * dot)
+                          for zj in z] for xi in x])
+        assert (R == want).all()
+
+
+def pin_linearity(o):
+    """A (B1 + B2) = A B1 + A B2 with integer entries (all sums exact)."""
+    rng = _rng(15)
+    for dt in (F16, BF16):
+        M, N, K = 7, 6, 40
+        A = _to_codes(rng.integers(-16, 17, (M, K)).astype(np.float64), dt)
+        b1 = rng.integers(-16, 17, (K, N)).astype(np.float64)
+        b2 = rng.integers(-16, 17, (K, N)).astype(np.float64)
+        R1, _ = o.gemm("N", "N", M, N, K, 1.0, A, K, _to_codes(b1, dt), N, 0.0, None, N, dt, F32)
+        R2, _ = o.gemm("N", "N", M, N, K, 1.0, A, K, _to_codes(b2, dt), N, 0.0, None, N, dt, F32)
+        R12, _ = o.gemm("N", "N", M, N, K, 1.0, A, K, _to_codes(b1 + b2, dt), N, 0.0, None, N,
+                        dt, F32)
+        assert (R12 == R1 + R2).all()
+        assert not (R1 == 0).all()
+
+
+def pin_quick_returns(o):
+    """K == 0 or alpha == 0 gives beta*C without reading A or B; beta == 0 never
+    reads C (NaN in C does not propagate); M == 0 / N == 0 is a no-op."""
+    rng = _rng(16)
+    M, N = 4, 5
+    C = rng.standard_normal((M, N)).astype(np.float32)
+    R, S = o.gemm("N", "N", M, N, 0, 1.0, None, 1, None, N, 2.0, C, N, F16, F32)
+    assert (R == 2.0 * C.astype(np.float64)).all() and (S == 0).all()
+    A = _random_codes(rng, (M, 3), F16)
+    B = _random_codes(rng, (3, N), F16)
+    R, _ = o.gemm("N", "N", M, N, 3, 0.0, None, 3, None, N, -1.0, C, N, F16, F32)
+    assert (R == -C.astype(np.float64)).all()
+    Cnan = np.full((M, N), np.nan, dtype=np.float32)
+    R, _ = o.gemm("N", "N", M, N, 3, 1.0, A, 3, B, N, 0.0, Cnan, N, F16, F32)
+    assert np.isfinite(R).all()
+    R, _ = o.gemm("N", "N", 0, N, 3, 1.0, A, 3, B, N, 0.0, None, N, F16, F32)
+    assert R.shape == (0, N)
+
+
+def pin_bad_arguments(o):
+    """Invalid arguments are rejected, not computed."""
+    A = np.zeros((4, 4), dtype=np.uint16)
+    bad = [
+        dict(ta="X"), dict(M=-1), dict(lda=3), dict(ldb=3), dict(ldc=3),
+        dict(dt=F32), dict(cdt=7),
+    ]
+    for b in bad:
+        kw = dict(ta="N", tb="N", M=4, N=4, K=4, lda=4, ldb=4, ldc=4, dt=F16, cdt=F32)
+        kw.update(b)
+        try:
+            o.gemm(kw["ta"], kw["tb"], kw["M"], kw["N"], kw["K"], 1.0, A, kw["lda"], A,
+                   kw["ldb"], 0.0, None, kw["ldc"], kw["dt"], kw["cdt"])
+        except ValueError:
+            continue
+        raise AssertionError(f"accepted bad arguments {b}")
+
+
+def pin_threads_deterministic(o):
+    """The result does not depend on the number of host threads."""
+    rng = _rng(17)
+    M, N, K = 37, 29, 65
+    A = _random_codes(rng, (M, K), BF16)
+    B = _random_codes(rng, (K, N), BF16)
+    R1, S1 = o.gemm("N", "N", M, N, K, 1.0, A, K, B, N, 0.0, None, N, BF16, F32, nthreads=1)
+    R4, S4 = o.gemm("N", "N", M, N, K, 1.0, A, K, B, N, 0.0, None, N, BF16, F32, nthreads=4)
+    assert (R1 == R4).all() and (S1 == S4).all()
+
+
+ALL_PINS = [
+    pin_decode_exhaustive, pin_page_format_limits, pin_round_ieee_table,
+    pin_round_roundtrip_exhaustive, pin_round_midpoints, pin_round_random_exact,
+    pin_f32_output, pin_gemm_bruteforce, pin_gemm_integer_exact,
+    pin_identity_and_permutation, pin_all_ones, pin_rank1_closed_form, pin_linearity,
+    pin_quick_returns, pin_bad_arguments, pin_threads_deterministic,
+]

@@ -1,0 +1,80 @@
+"""The pins are strong enough: a copy of oracle.c with one plausible mistake
+planted in it (on the CPU, in a temporary build) must fail at least one pin."""
+import os
+import subprocess
+import sys
+import tempfile
+
+import pytest
+
+import oracle
+import oracle_pins
+
+# (name, original text, mutated text) -- each original occurs exactly once.
+MUTANTS = [
+    ("dropped_beta_term", "r = r + be * decode_c(c_dtype, C, i * ldc + j);\n            acc[j] = r;",
+     "r = r + 0.0 * decode_c(c_dtype, C, i * ldc + j);\n            acc[j] = r;"),
+    ("sampled_dropped_beta", "r = r + be * decode_c(c_dtype, C, i * ldc + j);\n        R[s] = r;",
+     "r = r + 0.0 * decode_c(c_dtype, C, i * ldc + j);\n        R[s] = r;"),
+    ("dropped_alpha", "double r = use_ab ? al * acc[j] : 0.0;",
+     "double r = use_ab ? acc[j] : 0.0;"),
+    ("sign_of_product", "acc[j] = acc[j] + p;", "acc[j] = acc[j] - p;"),
+    ("k_loop_short", "for (int64_t k = 0; k < K; ++k) {\n                const double a",
+     "for (int64_t k = 0; k < K - 1; ++k) {\n                const double a"),
+    ("transA_swapped", "return is_n(transA) ? i * lda + k : k * lda + i;",
+     "return is_n(transA) ? k * lda + i : i * lda + k;"),
+    ("transB_swapped", "return is_n(transB) ? k * ldb + j : j * ldb + k;",
+     "return is_n(transB) ? j * ldb + k : k * ldb + j;"),
+    ("ldb_used_for_a", "decode_in(ab_dtype, A, a_off(transA, i, k, lda));",
+     "decode_in(ab_dtype, A, a_off(transA, i, k, ldb));"),
+    ("ldc_ignored", "decode_c(c_dtype, C, i * ldc + j);\n            acc[j] = r;",
+     "decode_c(c_dtype, C, i * N + j);\n            acc[j] = r;"),
+    ("f16_bias_off_by_one", "v = ldexp((double)(1024 + m), e - 25);",
+     "v = ldexp((double)(1024 + m), e - 24);"),
+    ("f16_subnormal_scale", "v = ldexp((double)m, -24);", "v = ldexp((double)m, -25);"),
+    ("bf16_mantissa_width", "v = ldexp((double)(128 + m), e - 134);",
+     "v = ldexp((double)(256 + m), e - 135);"),
+    ("ties_away_from_zero", "return (fmod(fl, 2.0) == 0.0) ? fl : fl + 1.0;",
+     "return fl + 1.0;"),
+    ("truncating_rounder", "if (frac > 0.5) return fl + 1.0;", "if (frac > 2.0) return fl + 1.0;"),
+    ("overflow_threshold", "if (efield >= (1 << ebits) - 1) return sign | exp_all_ones;",
+     "if (efield > (1 << ebits) - 1) return sign | exp_all_ones;"),
+    ("subnormal_floor", "int ulp_exp = (e < emin ? emin : e) - mbits;",
+     "int ulp_exp = e - mbits;"),
+    ("abs_sum_signed", "sabs[j] = sabs[j] + fabs(p);", "sabs[j] = sabs[j] + p;"),
+    ("sampled_transB", "decode_in(ab_dtype, B, b_off(transB, k, j, ldb));\n                acc = acc + p;",
+     "decode_in(ab_dtype, B, b_off('N', k, j, ldb));\n                acc = acc + p;"),
+    ("beta_read_when_zero", "if (be != 0.0) r = r + be * decode_c(c_dtype, C, i * ldc + j);\n            acc[j] = r;",
+     "r = r + be * decode_c(c_dtype, C, i * ldc + j);\n            acc[j] = r;"),
+]
+
+
+@pytest.fixture(scope="module")
+def source():
+    return open(oracle.SRC).read()
+
+
+@pytest.mark.parametrize("name,old,new", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_mutant_is_caught(source, name, old, new):
+    assert source.count(old) == 1, f"mutation site for {name} not unique/found"
+    with tempfile.TemporaryDirectory() as d:
+        src = os.path.join(d, "mutant.c")
+        with open(src, "w") as f:
+            f.write(source.replace(old, new))
+        lib = oracle.compile_source(src, os.path.join(d, "libmutant.so"))
+        # The battery runs in a child process: a mutant may crash (e.g. read
+        # through a NULL C), which counts as caught.
+        here = os.path.dirname(os.path.abspath(__file__))
+        code = (
+            "import sys; sys.path[:0] = [%r, %r]\n"
+            "import oracle, oracle_pins\n"
+            "o = oracle.Oracle(%r)\n"
+            "for pin in oracle_pins.ALL_PINS:\n"
+            "    try:\n"
+            "        pin(o)\n"
+            "    except (AssertionError, ValueError):\n"
+            "        print('caught by', pin.__name__); sys.exit(3)\n"
+            "sys.exit(0)\n" % (here, os.path.dirname(here), lib))
+        res = subprocess.run([sys.executable, "-c", code], capture_output=True,
+                             text=True, timeout=600)
+        assert res.returncode != 0, f"mutant {name} passed every pin"

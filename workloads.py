@@ -1,0 +1,150 @@
+"""Seeded synthetic GEMM workloads shared by the tests, the smoke check and the
+benchmark.
+
+This module holds no GEMM arithmetic: it only draws random numbers and stores
+them in the 16-bit (or 32-bit) formats the GEMM consumes.  Both the CUDA path
+and the CPU oracle receive exactly these bit patterns.
+
+Recipe (one generator per workload, seed 0, draws in the order A, B, C):
+  * U(-1, 1)   : 2 * torch.rand - 1 in FP32,
+  * N(0, 1)    : torch.randn in FP32,
+  * N(0, 0.02) : 0.02 * torch.randn in FP32 (0.02 read as the standard
+                 deviation, the usual weight-initialisation convention),
+then converted to FP16/BF16 by torch (round to nearest even).  Matrices are
+drawn in their stored shape: A is M x K for 'N' and K x M for 'T'; B is K x N
+for 'N' and N x K for 'T' ("weights stored N x K, K-contiguous"); C is M x N.
+When a leading dimension exceeds the logical row length, the padding columns
+are filled with NaN so that any read outside the logical matrix shows up in the
+result.
+
+The named workloads are the five shapes of the mixed-precision GEMM study: a
+256^3 FP16 GEMM with FP32 output; a 1024^3 FP16 GEMM with B stored column-major
+and FP16 output; a ragged 1000 x 1023 x 777 BF16 GEMM with C = A*B + C in FP32;
+three transformer linear layers (8192 tokens, 4096 -> 4096, 4096 -> 14336,
+14336 -> 4096, BF16); and a skinny decode GEMM (64 tokens, 8192 -> 16384, FP16).
+"""
+from __future__ import annotations
+
+import dataclasses
+from typing import Optional
+
+import torch
+
+DT_F16, DT_BF16, DT_F32 = 0, 1, 2
+TORCH_DTYPE = {DT_F16: torch.float16, DT_BF16: torch.bfloat16, DT_F32: torch.float32}
+DT_NAME = {DT_F16: "f16", DT_BF16: "bf16", DT_F32: "f32"}
+
+
+@dataclasses.dataclass(frozen=True)
+class Workload:
+    name: str
+    M: int
+    N: int
+    K: int
+    transA: str
+    transB: str
+    ab_dtype: int
+    c_dtype: int
+    alpha: float
+    beta: float
+    a_dist: str          # "U", "N1" or "N002"
+    b_dist: str
+    c_dist: Optional[str] = None   # None: C is not an input (beta == 0)
+    lda: Optional[int] = None      # None: tight (the stored row length)
+    ldb: Optional[int] = None
+    ldc: Optional[int] = None
+    seed: int = 0
+
+    def a_shape(self):
+        return (self.M, self.K) if self.transA in "Nn" else (self.K, self.M)
+
+    def b_shape(self):
+        return (self.K, self.N) if self.transB in "Nn" else (self.N, self.K)
+
+    def lds(self):
+        return (self.lda or self.a_shape()[1], self.ldb or self.b_shape()[1],
+                self.ldc or self.N)
+
+    def flops(self) -> float:
+        return 2.0 * self.M * self.N * self.K
+
+    def algorithmic_bytes(self) -> int:
+        """A and B read once, C written once, C also read when beta != 0."""
+        e_ab = 2
+        e_c = 4 if self.c_dtype == DT_F32 else 2
+        b = (self.M * self.K + self.K * self.N) * e_ab + self.M * self.N * e_c
+        if self.beta != 0:
+            b += self.M * self.N * e_c
+        return b
+
+
+WORKLOADS = {
+    w.name: w for w in [
+        Workload("square256_f16_f32out", 256, 256, 256, "N", "N", DT_F16, DT_F32,
+                 1.0, 0.0, "U", "U"),
+        Workload("square1024_f16_nt_f16out", 1024, 1024, 1024, "N", "T", DT_F16, DT_F16,
+                 1.0, 0.0, "U", "U"),
+        Workload("ragged1000x1023x777_bf16_beta1", 1000, 1023, 777, "N", "N", DT_BF16,
+                 DT_F32, 1.0, 1.0, "N1", "N1", "N1"),
+        Workload("linear_8192x4096x4096_bf16", 8192, 4096, 4096, "N", "T", DT_BF16,
+                 DT_BF16, 1.0, 0.0, "N1", "N002"),
+        Workload("linear_8192x14336x4096_bf16", 8192, 14336, 4096, "N", "T", DT_BF16,
+                 DT_BF16, 1.0, 0.0, "N1", "N002"),
+        Workload("linear_8192x4096x14336_bf16", 8192, 4096, 14336, "N", "T", DT_BF16,
+                 DT_BF16, 1.0, 0.0, "N1", "N002"),
+        Workload("skinny_64x16384x8192_f16", 64, 16384, 8192, "N", "T", DT_F16, DT_F16,
+                 1.0, 0.0, "N1", "N002"),
+    ]
+}
+
+
+def _draw(gen: torch.Generator, dist: str, shape) -> torch.Tensor:
+    if dist == "U":
+        return torch.rand(shape, generator=gen, dtype=torch.float32) * 2.0 - 1.0
+    if dist == "N1":
+        return torch.randn(shape, generator=gen, dtype=torch.float32)
+    if dist == "N002":
+        return torch.randn(shape, generator=gen, dtype=torch.float32) * 0.02
+    raise ValueError(f"unknown distribution {dist!r}")
+
+
+def _stored(values: torch.Tensor, ld: int, dtype: torch.dtype) -> torch.Tensor:
+    rows, cols = values.shape
+    if ld == cols:
+        return values.to(dtype).contiguous()
+    buf = torch.full((rows, ld), float("nan"), dtype=dtype)
+    buf[:, :cols] = values.to(dtype)
+    return buf
+
+
+@dataclasses.dataclass
+class Inputs:
+    A: torch.Tensor   # stored (rows x lda), CPU, FP16/BF16
+    B: torch.Tensor   # stored (rows x ldb)
+    C: Optional[torch.Tensor]   # stored (M x ldc) in the output dtype, or None
+    lda: int
+    ldb: int
+    ldc: int
+
+
+def make_inputs(w: Workload) -> Inputs:
+    """Draw A, then B, then C (if beta != 0) from one seeded CPU generator."""
+    gen = torch.Generator(device="cpu")
+    gen.manual_seed(w.seed)
+    lda, ldb, ldc = w.lds()
+    ab_t = TORCH_DTYPE[w.ab_dtype]
+    A = _stored(_draw(gen, w.a_dist, w.a_shape()), lda, ab_t)
+    B = _stored(_draw(gen, w.b_dist, w.b_shape()), ldb, ab_t)
+    C = None
+    if w.c_dist is not None:
+        C = _stored(_draw(gen, w.c_dist, (w.M, w.N)), ldc, TORCH_DTYPE[w.c_dtype])
+    return Inputs(A, B, C, lda, ldb, ldc)
+
+
+def as_codes(t: torch.Tensor):
+    """Raw bit patterns of a CPU tensor as a numpy array (uint16 or uint32)."""
+    if t.dtype in (torch.float16, torch.bfloat16):
+        return t.contiguous().view(torch.int16).numpy().view("uint16")
+    if t.dtype == torch.float32:
+        return t.contiguous().numpy().view("uint32")
+    raise TypeError(t.dtype)
