@@ -1,0 +1,181 @@
+/*
+ * gemm_sm103.h -- C ABI of the GB300 (sm_103a) mixed-precision dense GEMM.
+ *
+ *     C = alpha * op(A) * op(B) + beta * C
+ *
+ * What is computed (and where it is defined):
+ *   - The product-sum "C[i][j] accumulates A[i][k] * B[k][j]" (SGEMM tutorial
+ *     page, section 3.1) and "C = A * B + C" (CATLASS page, section 2.1).
+ *     alpha, beta and op() are the BLAS reading of that formula; the pages
+ *     name neither.
+ *   - A and B are FP16 or BF16 (both the same type); products are accumulated
+ *     in FP32 (DeepGEMM page, sections 1.3 and 6.2; CATLASS page, sections
+ *     3.2 and 3.4).  The output C is FP32, FP16 or BF16; alpha*acc + beta*C is
+ *     formed in FP32 and rounded once to the output type, round to nearest even.
+ *   - Storage is row-major with a leading dimension: element (m, n) of a
+ *     stored matrix is at offset m * ld + n, in elements (CATLASS page,
+ *     section 1.3).  op(X) = X for 'N'/'n' and X^T for 'T'/'t'.
+ *       A, transA = 'N': stored M x K, lda >= max(1, K)
+ *       A, transA = 'T': stored K x M, lda >= max(1, M)
+ *       B, transB = 'N': stored K x N, ldb >= max(1, N)
+ *       B, transB = 'T': stored N x K, ldb >= max(1, K)   ("weights N x K")
+ *       C:               stored M x N, ldc >= max(1, N)
+ *   - Shapes are arbitrary (M, N, K >= 0; the DeepGEMM page, section 1.3, asks
+ *     for 1 to several thousand); tiles that overhang the matrix edge are
+ *     zero-filled (DeepGEMM page, section 3.4).
+ *
+ * Ownership and threading:
+ *   - A, B and C are DEVICE pointers owned by the caller.  A and B are only
+ *     read.  C is read only when beta != 0 and is always written (M x N
+ *     elements; the padding columns n >= N of each row are never touched).
+ *   - A handle owns a device workspace (packed copies of operands whose pitch
+ *     or base address is not 16-byte aligned, split-K partial sums) and a
+ *     device-visible error word.  The workspace grows on demand inside
+ *     gemm_run (a cudaMalloc, which synchronises the device) and is released
+ *     by gemm_destroy.
+ *   - gemm_run is asynchronous with respect to the host: it enqueues work on
+ *     `stream` and returns.  A handle must not be used from two host threads
+ *     at once; use one handle per thread or per stream.  Calls on one handle
+ *     that overlap on the GPU (different streams) may share workspace: order
+ *     them on one stream.
+ *
+ * Errors: every entry point returns a gemm_status_t and never aborts.  Device
+ * kernels never trap: every wait inside them is bounded, and a wait that runs
+ * out records GEMM_ERR_DEVICE_TIMEOUT in the handle's error word, which the
+ * next gemm_run or gemm_sync on that handle reports (and clears).
+ */
+#ifndef GEMM_SM103_H_
+#define GEMM_SM103_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same layout as cudaStream_t; NULL is the legacy default stream. */
+typedef struct CUstream_st* gemm_stream_t;
+typedef struct gemm_ctx* gemm_handle_t;
+
+typedef enum { GEMM_F16 = 0, GEMM_BF16 = 1, GEMM_F32 = 2 } gemm_dtype_t;
+
+/* a, b: input types (must be equal, F16 or BF16); c: output type (F32, F16 or
+ * BF16).  The accumulator is always FP32. */
+typedef struct { int32_t a, b, c; } gemm_dtypes_t;
+
+typedef enum {
+    GEMM_OK = 0,
+    GEMM_ERR_INVALID_VALUE = 1,   /* bad trans flag, shape, ld, pointer or dtype */
+    GEMM_ERR_NOT_SUPPORTED = 2,   /* the current device is not sm_103 */
+    GEMM_ERR_ALLOC = 3,           /* a workspace allocation failed */
+    GEMM_ERR_LAUNCH = 4,          /* a CUDA call or kernel launch failed */
+    GEMM_ERR_DEVICE_TIMEOUT = 5   /* a bounded in-kernel wait ran out */
+} gemm_status_t;
+
+/*
+ * gemm_create: make a handle bound to the CURRENT CUDA device.
+ *   out: receives the handle (set to NULL on failure).
+ * Returns NOT_SUPPORTED if the device is not compute capability 10.3
+ * (sm_103), LAUNCH if the CUDA runtime reports an error, ALLOC if the error
+ * word cannot be allocated.
+ */
+gemm_status_t gemm_create(gemm_handle_t* out);
+
+/*
+ * gemm_run: C = alpha * op(A) * op(B) + beta * C on `stream`.
+ *   transA, transB: 'N'/'n' or 'T'/'t'.
+ *   M, N, K: op(A) is M x K, op(B) is K x N, C is M x N.
+ *   A, lda / B, ldb / C, ldc: device pointers and leading dimensions in
+ *     elements, laid out as in the table above.
+ *   dt: element types (dt.a == dt.b in {F16, BF16}; dt.c in {F32, F16, BF16}).
+ *   stream: the CUDA stream to enqueue on.
+ * Quick returns (BLAS convention): M == 0 or N == 0 is a no-op; K == 0 or
+ * alpha == 0 computes C = beta * C without reading A or B (A, B may then be
+ * NULL); beta == 0 never reads C, so NaN/Inf already in C do not propagate.
+ * Returns INVALID_VALUE for a bad argument (nothing is enqueued), ALLOC if the
+ * workspace cannot grow, LAUNCH if a launch fails, DEVICE_TIMEOUT if an
+ * earlier call on this handle recorded a device-side timeout (reported once).
+ */
+gemm_status_t gemm_run(gemm_handle_t h, char transA, char transB,
+                       int64_t M, int64_t N, int64_t K,
+                       float alpha, const void* A, int64_t lda,
+                       const void* B, int64_t ldb,
+                       float beta, void* C, int64_t ldc,
+                       gemm_dtypes_t dt, gemm_stream_t stream);
+
+/*
+ * gemm_sync: wait for `stream`, then report (and clear) a device-side timeout
+ * recorded by any kernel of this handle.  Returns LAUNCH if the stream itself
+ * reports an error.
+ */
+gemm_status_t gemm_sync(gemm_handle_t h, gemm_stream_t stream);
+
+/* gemm_destroy: synchronise the device and free the handle and its workspace.
+ * NULL is accepted (no-op). */
+gemm_status_t gemm_destroy(gemm_handle_t h);
+
+/* A static, human-readable name for a status code. */
+const char* gemm_status_string(gemm_status_t s);
+
+/*
+ * gemm_check_args: the argument validation gemm_run performs, without a
+ * handle or a device (pure host logic).  Pointers are only compared with NULL.
+ */
+gemm_status_t gemm_check_args(char transA, char transB, int64_t M, int64_t N, int64_t K,
+                              float alpha, const void* A, int64_t lda,
+                              const void* B, int64_t ldb,
+                              float beta, const void* C, int64_t ldc,
+                              gemm_dtypes_t dt);
+
+/* Which kernel path gemm_run takes for a problem, as decided on the host. */
+typedef enum {
+    GEMM_PATH_NOOP = 0,       /* M == 0 or N == 0 */
+    GEMM_PATH_SCALE = 1,      /* K == 0 or alpha == 0: C = beta * C */
+    GEMM_PATH_TILED_1SM = 2,  /* persistent tcgen05 kernel, one CTA per 128 x BN tile */
+    GEMM_PATH_TILED_2SM = 3,  /* persistent tcgen05 kernel on 2-SM CTA pairs, 256 x BN tiles */
+    GEMM_PATH_SKINNY = 4      /* memory-bound small-M path (swap A/B, split-K) */
+} gemm_path_t;
+
+typedef struct {
+    int32_t path;          /* gemm_path_t */
+    int32_t block_m;       /* output rows per tile (per CTA pair for 2SM) */
+    int32_t block_n;       /* output columns per tile */
+    int32_t block_k;       /* K elements per pipeline stage */
+    int32_t stages;        /* shared-memory pipeline depth */
+    int32_t split_k;       /* number of K partitions (1 = none) */
+    int32_t grid;          /* CTAs launched for the main kernel */
+    int32_t num_tiles;     /* output tiles (x split_k work units) */
+    int32_t pack_a;        /* 1: A is copied to an aligned workspace first */
+    int32_t pack_b;        /* 1: B is copied to an aligned workspace first */
+    int32_t a_mn_major;    /* 1: op(A) is read M-contiguous (transA = 'T') */
+    int32_t b_mn_major;    /* 1: op(B) is read N-contiguous (transB = 'N') */
+    int32_t swap_ab;       /* 1: computed as C^T = op(B)^T op(A)^T */
+    int32_t c_vector;      /* 1: C rows are 16-byte aligned (vector epilogue) */
+    int32_t sk_len;        /* stream-K: k-blocks per CTA (0 = data-parallel) */
+    int32_t sk_max_seg;    /* stream-K: workspace slots per CTA */
+    int32_t k_blocks;      /* ceil(K / block_k) */
+    int32_t tiles_m;       /* tile rows (of the possibly swapped problem) */
+    int32_t tiles_n;       /* tile columns */
+    int32_t reserved;
+    int64_t workspace_bytes;
+} gemm_plan_t;
+
+/*
+ * gemm_plan_query: the plan gemm_run would use for these arguments on a
+ * device with `num_sms` SMs and `smem_optin` bytes of opt-in shared memory
+ * per block (pure host logic, no device needed; pointers are used only for
+ * their 16-byte alignment).  Returns INVALID_VALUE for arguments gemm_run
+ * would reject.
+ */
+gemm_status_t gemm_plan_query(char transA, char transB, int64_t M, int64_t N, int64_t K,
+                              float alpha, const void* A, int64_t lda,
+                              const void* B, int64_t ldb,
+                              float beta, const void* C, int64_t ldc,
+                              gemm_dtypes_t dt, int32_t num_sms, int32_t smem_optin,
+                              gemm_plan_t* out);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GEMM_SM103_H_ */

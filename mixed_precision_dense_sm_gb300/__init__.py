@@ -1,0 +1,198 @@
+"""Python binding for libgemm_sm103.so, the GB300 mixed-precision GEMM.
+
+Argument marshalling only: every step of C = alpha*op(A)*op(B) + beta*C runs in
+the library's CUDA kernels.  PyTorch is used for device memory and streams.
+If the compiled library is missing, importing this package raises -- there is
+no fallback implementation.
+
+The entry points mirror include/gemm_sm103.h one to one:
+``gemm_create``, ``gemm_run``, ``gemm_sync``, ``gemm_destroy``,
+``gemm_status_string``, ``gemm_check_args``, ``gemm_plan_query``.
+``Gemm`` wraps a handle and adds ``__call__`` for torch tensors.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libgemm_sm103.so")
+HEADER = os.path.join(os.path.dirname(HERE), "include", "gemm_sm103.h")
+
+GEMM_F16, GEMM_BF16, GEMM_F32 = 0, 1, 2
+STATUS = {0: "GEMM_OK", 1: "GEMM_ERR_INVALID_VALUE", 2: "GEMM_ERR_NOT_SUPPORTED",
+          3: "GEMM_ERR_ALLOC", 4: "GEMM_ERR_LAUNCH", 5: "GEMM_ERR_DEVICE_TIMEOUT"}
+PATHS = {0: "noop", 1: "scale", 2: "tiled_1sm", 3: "tiled_2sm", 4: "skinny"}
+
+
+class GemmError(RuntimeError):
+    def __init__(self, status: int, what: str = ""):
+        self.status = status
+        super().__init__(f"{what}: {STATUS.get(status, status)}")
+
+
+class Dtypes(ctypes.Structure):
+    _fields_ = [("a", ctypes.c_int32), ("b", ctypes.c_int32), ("c", ctypes.c_int32)]
+
+
+class Plan(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in (
+        "path", "block_m", "block_n", "block_k", "stages", "split_k", "grid", "num_tiles",
+        "pack_a", "pack_b", "a_mn_major", "b_mn_major", "swap_ab", "c_vector", "sk_len",
+        "sk_max_seg", "k_blocks", "tiles_m", "tiles_n", "reserved")] + \
+        [("workspace_bytes", ctypes.c_int64)]
+
+    def as_dict(self):
+        d = {n: getattr(self, n) for n, _ in self._fields_}
+        d["path_name"] = PATHS.get(self.path, "?")
+        return d
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(
+            f"{LIB_PATH} is not built; run `python -c \"import __graft_entry__ as g; g.build()\"` "
+            "(the CUDA library is required; there is no CPU fallback)")
+    lib = ctypes.CDLL(LIB_PATH)
+    i64, vp, c = ctypes.c_int64, ctypes.c_void_p, ctypes.c_char
+    run_args = [c, c, i64, i64, i64, ctypes.c_float, vp, i64, vp, i64, ctypes.c_float, vp, i64,
+                Dtypes]
+    lib.gemm_create.restype = ctypes.c_int
+    lib.gemm_create.argtypes = [ctypes.POINTER(vp)]
+    lib.gemm_run.restype = ctypes.c_int
+    lib.gemm_run.argtypes = [vp] + run_args + [vp]
+    lib.gemm_sync.restype = ctypes.c_int
+    lib.gemm_sync.argtypes = [vp, vp]
+    lib.gemm_destroy.restype = ctypes.c_int
+    lib.gemm_destroy.argtypes = [vp]
+    lib.gemm_status_string.restype = ctypes.c_char_p
+    lib.gemm_status_string.argtypes = [ctypes.c_int]
+    lib.gemm_check_args.restype = ctypes.c_int
+    lib.gemm_check_args.argtypes = run_args
+    lib.gemm_plan_query.restype = ctypes.c_int
+    lib.gemm_plan_query.argtypes = run_args + [ctypes.c_int32, ctypes.c_int32,
+                                               ctypes.POINTER(Plan)]
+    return lib
+
+
+lib = _load()
+
+
+def _tr(t: str) -> bytes:
+    return t.encode() if isinstance(t, str) else bytes(t)
+
+
+def gemm_status_string(status: int) -> str:
+    return lib.gemm_status_string(status).decode()
+
+
+def gemm_create() -> int:
+    h = ctypes.c_void_p()
+    st = lib.gemm_create(ctypes.byref(h))
+    if st != 0:
+        raise GemmError(st, "gemm_create")
+    return h.value
+
+
+def gemm_destroy(h) -> int:
+    return lib.gemm_destroy(h)
+
+
+def gemm_sync(h, stream=0) -> int:
+    return lib.gemm_sync(h, stream)
+
+
+def gemm_run(h, transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc,
+             dtypes, stream=0) -> int:
+    """Raw C-ABI call: A, B, C are device addresses (ints), dtypes a
+    (a, b, c) tuple of GEMM_F16/GEMM_BF16/GEMM_F32, stream a cudaStream_t
+    value.  Returns the gemm_status_t code."""
+    return lib.gemm_run(h, _tr(transA), _tr(transB), M, N, K, float(alpha), A, lda, B, ldb,
+                        float(beta), C, ldc, Dtypes(*dtypes), stream)
+
+
+def gemm_check_args(transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, dtypes) -> int:
+    return lib.gemm_check_args(_tr(transA), _tr(transB), M, N, K, float(alpha), A, lda, B, ldb,
+                               float(beta), C, ldc, Dtypes(*dtypes))
+
+
+def gemm_plan_query(transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, dtypes,
+                    num_sms=152, smem_optin=232448):
+    """(status, plan dict) of the path gemm_run would take (host logic only)."""
+    plan = Plan()
+    st = lib.gemm_plan_query(_tr(transA), _tr(transB), M, N, K, float(alpha), A, lda, B, ldb,
+                             float(beta), C, ldc, Dtypes(*dtypes), num_sms, smem_optin,
+                             ctypes.byref(plan))
+    return st, (plan.as_dict() if st == 0 else None)
+
+
+def declared_symbols():
+    """Function names declared in include/gemm_sm103.h."""
+    import re
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"^\s*(?:gemm_status_t|const char\*)\s+(gemm_\w+)\s*\(",
+                                 text, flags=re.M)))
+
+
+_TORCH_CODE = None
+
+
+def dtype_code(t) -> int:
+    global _TORCH_CODE
+    if _TORCH_CODE is None:
+        import torch
+        _TORCH_CODE = {torch.float16: GEMM_F16, torch.bfloat16: GEMM_BF16,
+                       torch.float32: GEMM_F32}
+    return _TORCH_CODE[t]
+
+
+class Gemm:
+    """A library handle bound to the current CUDA device.
+
+    ``g(A, B, C, transA, transB, alpha, beta, M=, N=, K=)`` marshals torch
+    tensors (device, 2-D, unit inner stride, row pitch = stride(0)) into one
+    gemm_run call on the current torch stream.  The logical sizes default to
+    what the stored shapes imply."""
+
+    def __init__(self):
+        self.h = gemm_create()
+
+    def close(self):
+        if self.h:
+            gemm_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def __call__(self, A, B, C, transA="N", transB="N", alpha=1.0, beta=0.0,
+                 M=None, N=None, K=None, stream=None):
+        import torch
+        if stream is None:
+            stream = torch.cuda.current_stream().cuda_stream
+        for t in (A, B, C):
+            if t is not None and (t.dim() != 2 or t.stride(1) != 1):
+                raise ValueError("operands must be 2-D with unit inner stride")
+        if M is None:
+            M = C.shape[0]
+        if N is None:
+            N = C.shape[1]
+        if K is None:
+            K = A.shape[1] if transA in "Nn" else A.shape[0]
+        dts = (dtype_code(A.dtype), dtype_code(B.dtype), dtype_code(C.dtype))
+        st = gemm_run(self.h, transA, transB, M, N, K, alpha, A.data_ptr(), A.stride(0),
+                      B.data_ptr(), B.stride(0), beta, C.data_ptr(), C.stride(0), dts, stream)
+        if st != 0:
+            raise GemmError(st, "gemm_run")
+        return C
+
+    def sync(self, stream=None):
+        import torch
+        if stream is None:
+            stream = torch.cuda.current_stream().cuda_stream
+        st = gemm_sync(self.h, stream)
+        if st != 0:
+            raise GemmError(st, "gemm_sync")

@@ -1,0 +1,489 @@
+// api.cu -- the C ABI (include/gemm_sm103.h): argument validation, the host
+// planner that picks a kernel path, TMA descriptor encoding, workspace
+// management and the launches.
+//
+// The planner follows the pages' measurement-first split between
+// compute-bound and memory-bound GEMMs (SGEMM page, section 1.2; DeepGEMM
+// page, section 2.4; CATLASS page, section 3.1): large problems run the
+// data-parallel persistent tensor-core kernel; problems with fewer output
+// tiles than SMs spread their K loop across SMs (stream-K) so the whole GPU
+// streams the operands; very small M swaps the operands so the 128-row MMA
+// dimension is filled by the large side (the skinny, memory-bound path).
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+#include <new>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "../../include/gemm_sm103.h"
+#include "aux_kernels.cuh"
+#include "launch.h"
+
+using namespace gemm103;
+
+namespace {
+
+constexpr int kMaxStages = 8;
+constexpr int kGroupM = 8;
+
+struct OperandDesc {
+    // stored matrix: rows x cols with pitch ld (elements); K-major means the
+    // contiguous direction is K (cols == K), MN-major means it is M or N.
+    const void* ptr;
+    int64_t rows, cols, ld;
+    bool mn_major;
+    bool pack;          // needs a 16-byte-aligned copy
+    int64_t packed_ld;
+};
+
+struct Plan {
+    gemm_plan_t pub;
+    OperandDesc a, b;   // kernel operands (after an optional swap)
+    int64_t Mk, Nk;     // kernel rows / columns (M', N')
+    int64_t K;
+    int64_t c_rs, c_cs;
+    int32_t k_blocks, tiles_m, tiles_n;
+    int32_t sk_len, sk_max_seg;
+    int64_t pack_a_bytes, pack_b_bytes, partial_bytes;
+    size_t smem_bytes;
+};
+
+bool is_n(char t) { return t == 'N' || t == 'n'; }
+bool is_t(char t) { return t == 'T' || t == 't'; }
+int64_t max1(int64_t v) { return v > 1 ? v : 1; }
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+int64_t round_up(int64_t a, int64_t b) { return ceil_div(a, b) * b; }
+size_t out_elem_bytes(int32_t c) { return c == GEMM_F32 ? 4 : 2; }
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+gemm_status_t check_args(char transA, char transB, int64_t M, int64_t N, int64_t K, float alpha,
+                         const void* A, int64_t lda, const void* B, int64_t ldb, float beta,
+                         const void* C, int64_t ldc, gemm_dtypes_t dt) {
+    if (!(is_n(transA) || is_t(transA)) || !(is_n(transB) || is_t(transB)))
+        return GEMM_ERR_INVALID_VALUE;
+    if (M < 0 || N < 0 || K < 0) return GEMM_ERR_INVALID_VALUE;
+    // TMA coordinates and tile indices are 32-bit.
+    if (M > INT32_MAX || N > INT32_MAX || K > INT32_MAX) return GEMM_ERR_INVALID_VALUE;
+    if (dt.a != dt.b || (dt.a != GEMM_F16 && dt.a != GEMM_BF16)) return GEMM_ERR_INVALID_VALUE;
+    if (dt.c != GEMM_F32 && dt.c != GEMM_F16 && dt.c != GEMM_BF16) return GEMM_ERR_INVALID_VALUE;
+    const int64_t a_cols = is_n(transA) ? K : M;
+    const int64_t b_cols = is_n(transB) ? N : K;
+    if (lda < max1(a_cols) || ldb < max1(b_cols) || ldc < max1(N)) return GEMM_ERR_INVALID_VALUE;
+    if (M == 0 || N == 0) return GEMM_OK;
+    if (C == nullptr) return GEMM_ERR_INVALID_VALUE;
+    const bool reads_ab = (K > 0 && alpha != 0.0f);
+    if (reads_ab && (A == nullptr || B == nullptr)) return GEMM_ERR_INVALID_VALUE;
+    (void)beta;
+    return GEMM_OK;
+}
+
+// Pick the kernel path, tile shape, schedule and workspace for a problem.
+gemm_status_t make_plan(char transA, char transB, int64_t M, int64_t N, int64_t K, float alpha,
+                        const void* A, int64_t lda, const void* B, int64_t ldb, float beta,
+                        const void* C, int64_t ldc, gemm_dtypes_t dt, int32_t num_sms,
+                        int32_t smem_optin, Plan& pl) {
+    gemm_status_t st = check_args(transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, dt);
+    if (st != GEMM_OK) return st;
+    if (num_sms < 1 || smem_optin < 64 * 1024) return GEMM_ERR_INVALID_VALUE;
+    std::memset(&pl, 0, sizeof pl);
+    pl.pub.split_k = 1;
+    pl.K = K;
+    if (M == 0 || N == 0) {
+        pl.pub.path = GEMM_PATH_NOOP;
+        return GEMM_OK;
+    }
+    if (K == 0 || alpha == 0.0f) {
+        pl.pub.path = GEMM_PATH_SCALE;
+        return GEMM_OK;
+    }
+
+    // Operand descriptions in the problem's own orientation.
+    OperandDesc opA, opB;
+    opA.ptr = A;
+    opA.mn_major = is_t(transA);            // stored K x M
+    opA.rows = opA.mn_major ? K : M;
+    opA.cols = opA.mn_major ? M : K;
+    opA.ld = lda;
+    opB.ptr = B;
+    opB.mn_major = is_n(transB);            // stored K x N
+    opB.rows = opB.mn_major ? K : N;
+    opB.cols = opB.mn_major ? N : K;
+    opB.ld = ldb;
+
+    // Skinny M: compute C^T = op(B)^T op(A)^T so the large N fills the
+    // 128-row MMA side and the small M becomes the MMA's N.
+    const bool swap = (M <= 64 && N >= 128);
+    pl.pub.swap_ab = swap ? 1 : 0;
+    if (swap) {
+        pl.a = opB;
+        pl.b = opA;
+        pl.Mk = N;
+        pl.Nk = M;
+        pl.c_rs = 1;
+        pl.c_cs = ldc;
+    } else {
+        pl.a = opA;
+        pl.b = opB;
+        pl.Mk = M;
+        pl.Nk = N;
+        pl.c_rs = ldc;
+        pl.c_cs = 1;
+    }
+    for (OperandDesc* o : {&pl.a, &pl.b}) {
+        o->pack = !aligned16(o->ptr) || ((o->ld * 2) % 16) != 0;
+        o->packed_ld = o->pack ? round_up(o->cols, 8) : o->ld;
+    }
+    pl.pub.a_mn_major = pl.a.mn_major;
+    pl.pub.b_mn_major = pl.b.mn_major;
+    pl.pub.pack_a = (swap ? pl.b.pack : pl.a.pack) ? 1 : 0;
+    pl.pub.pack_b = (swap ? pl.a.pack : pl.b.pack) ? 1 : 0;
+    pl.pack_a_bytes = pl.a.pack ? pl.a.rows * pl.a.packed_ld * 2 : 0;
+    pl.pack_b_bytes = pl.b.pack ? pl.b.rows * pl.b.packed_ld * 2 : 0;
+    pl.pub.c_vector = (!swap && aligned16(C) && (ldc * (int64_t)out_elem_bytes(dt.c)) % 16 == 0) ? 1 : 0;
+
+    // Tile width: 256 columns when the output has enough tiles to fill the GPU,
+    // otherwise narrower tiles (and stream-K over K) for more parallelism.
+    pl.k_blocks = static_cast<int32_t>(ceil_div(K, kBlockK));
+    const int64_t tiles_m = ceil_div(pl.Mk, kBlockM);
+    int bn;
+    if (pl.Nk <= 64) {
+        bn = 64;
+    } else if (tiles_m * ceil_div(pl.Nk, 256) >= num_sms) {
+        bn = 256;
+    } else if (pl.Nk <= 128 || tiles_m * ceil_div(pl.Nk, 128) >= num_sms) {
+        bn = 128;
+    } else {
+        bn = 128;
+    }
+    const int64_t tiles_n = ceil_div(pl.Nk, bn);
+    const int64_t tiles = tiles_m * tiles_n;
+    pl.tiles_m = static_cast<int32_t>(tiles_m);
+    pl.tiles_n = static_cast<int32_t>(tiles_n);
+    pl.pub.block_m = kBlockM;
+    pl.pub.block_n = bn;
+    pl.pub.block_k = kBlockK;
+    pl.pub.num_tiles = static_cast<int32_t>(tiles);
+
+    const uint32_t stage_bytes = kATileBytes + static_cast<uint32_t>(bn) * kBlockK * 2;
+    const int64_t barrier_bytes = 256;
+    int64_t stages = (smem_optin - 1024 - barrier_bytes) / stage_bytes;
+    if (stages > kMaxStages) stages = kMaxStages;
+    if (stages < 2) return GEMM_ERR_NOT_SUPPORTED;
+    pl.pub.stages = static_cast<int32_t>(stages);
+    pl.smem_bytes = static_cast<size_t>(stages * stage_bytes + 1024 + barrier_bytes);
+
+    const int64_t work = tiles * pl.k_blocks;
+    const bool stream_k = (tiles < num_sms) && (pl.k_blocks >= 4) && (work < INT32_MAX);
+    if (stream_k) {
+        int64_t G = num_sms < work ? num_sms : work;
+        const int64_t L = ceil_div(work, G);
+        G = ceil_div(work, L);
+        pl.sk_len = static_cast<int32_t>(L);
+        pl.sk_max_seg = static_cast<int32_t>((L + pl.k_blocks - 2) / pl.k_blocks + 1);
+        pl.pub.grid = static_cast<int32_t>(G);
+        pl.pub.split_k = static_cast<int32_t>(ceil_div(pl.k_blocks, L));
+        pl.partial_bytes = G * pl.sk_max_seg * (int64_t)kBlockM * bn * 4;
+        pl.pub.path = swap ? GEMM_PATH_SKINNY : GEMM_PATH_TILED_1SM;
+    } else {
+        pl.pub.grid = static_cast<int32_t>(tiles < num_sms ? tiles : num_sms);
+        pl.pub.path = swap ? GEMM_PATH_SKINNY : GEMM_PATH_TILED_1SM;
+    }
+    pl.pub.sk_len = pl.sk_len;
+    pl.pub.sk_max_seg = pl.sk_max_seg;
+    pl.pub.k_blocks = pl.k_blocks;
+    pl.pub.tiles_m = pl.tiles_m;
+    pl.pub.tiles_n = pl.tiles_n;
+    pl.pub.workspace_bytes = round_up(pl.pack_a_bytes, 256) + round_up(pl.pack_b_bytes, 256) +
+                             round_up(pl.partial_bytes, 256);
+    return GEMM_OK;
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+}  // namespace
+
+struct gemm_ctx {
+    int device;
+    int num_sms;
+    int smem_optin;
+    int* err_host;        // mapped pinned error word (host view)
+    int* err_dev;         // device view of the same word
+    void* ws;             // device workspace
+    size_t ws_bytes;
+    EncodeTiledFn encode;
+};
+
+namespace {
+
+// 2-D tiled map over a stored 16-bit matrix: dims {inner, outer}, row pitch in
+// bytes, a 64 x box_outer box, 128-byte swizzle, zero fill out of range.
+bool encode_operand(gemm_ctx* h, CUtensorMap* map, int32_t dtype, const void* ptr, int64_t inner,
+                    int64_t outer, int64_t ld, uint32_t box_outer) {
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(outer)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(kBlockK), box_outer};
+    const cuuint32_t estr[2] = {1, 1};
+    CUresult r = h->encode(map,
+                           dtype == GEMM_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                              : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                           2, const_cast<void*>(ptr), dims, strides, box, estr,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+gemm_status_t ensure_workspace(gemm_ctx* h, size_t bytes) {
+    if (bytes <= h->ws_bytes) return GEMM_OK;
+    if (h->ws) {
+        cudaFree(h->ws);          // implicit device synchronisation: no user of the old buffer remains
+        h->ws = nullptr;
+        h->ws_bytes = 0;
+    }
+    size_t want = bytes + (bytes >> 2);
+    if (cudaMalloc(&h->ws, want) != cudaSuccess) {
+        cudaGetLastError();
+        h->ws = nullptr;
+        return GEMM_ERR_ALLOC;
+    }
+    h->ws_bytes = want;
+    return GEMM_OK;
+}
+
+gemm_status_t take_device_error(gemm_ctx* h) {
+    volatile int* e = h->err_host;
+    if (*e != 0) {
+        *e = 0;
+        return GEMM_ERR_DEVICE_TIMEOUT;
+    }
+    return GEMM_OK;
+}
+
+int grid_for(int64_t elems_per_thread_unit, int num_sms) {
+    int64_t blocks = ceil_div(elems_per_thread_unit, 256);
+    int64_t cap = static_cast<int64_t>(num_sms) * 8;
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) blocks = 1;
+    return static_cast<int>(blocks);
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* gemm_status_string(gemm_status_t s) {
+    switch (s) {
+        case GEMM_OK: return "GEMM_OK";
+        case GEMM_ERR_INVALID_VALUE: return "GEMM_ERR_INVALID_VALUE";
+        case GEMM_ERR_NOT_SUPPORTED: return "GEMM_ERR_NOT_SUPPORTED";
+        case GEMM_ERR_ALLOC: return "GEMM_ERR_ALLOC";
+        case GEMM_ERR_LAUNCH: return "GEMM_ERR_LAUNCH";
+        case GEMM_ERR_DEVICE_TIMEOUT: return "GEMM_ERR_DEVICE_TIMEOUT";
+    }
+    return "GEMM_ERR_UNKNOWN";
+}
+
+gemm_status_t gemm_check_args(char transA, char transB, int64_t M, int64_t N, int64_t K,
+                              float alpha, const void* A, int64_t lda, const void* B, int64_t ldb,
+                              float beta, const void* C, int64_t ldc, gemm_dtypes_t dt) {
+    return check_args(transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, dt);
+}
+
+gemm_status_t gemm_plan_query(char transA, char transB, int64_t M, int64_t N, int64_t K,
+                              float alpha, const void* A, int64_t lda, const void* B, int64_t ldb,
+                              float beta, const void* C, int64_t ldc, gemm_dtypes_t dt,
+                              int32_t num_sms, int32_t smem_optin, gemm_plan_t* out) {
+    if (out == nullptr) return GEMM_ERR_INVALID_VALUE;
+    Plan pl;
+    gemm_status_t st = make_plan(transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, dt,
+                                 num_sms, smem_optin, pl);
+    if (st != GEMM_OK) return st;
+    *out = pl.pub;
+    return GEMM_OK;
+}
+
+gemm_status_t gemm_create(gemm_handle_t* out) {
+    if (out == nullptr) return GEMM_ERR_INVALID_VALUE;
+    *out = nullptr;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_LAUNCH;
+    }
+    int major = 0, minor = 0, sms = 0, smem = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
+            cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_LAUNCH;
+    }
+    if (major != 10 || minor != 3) return GEMM_ERR_NOT_SUPPORTED;
+
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || fn == nullptr) {
+        cudaGetLastError();
+        return GEMM_ERR_LAUNCH;
+    }
+    gemm_ctx* h = new (std::nothrow) gemm_ctx();
+    if (h == nullptr) return GEMM_ERR_ALLOC;
+    h->device = dev;
+    h->num_sms = sms;
+    h->smem_optin = smem;
+    h->encode = reinterpret_cast<EncodeTiledFn>(fn);
+    if (cudaHostAlloc(reinterpret_cast<void**>(&h->err_host), 64, cudaHostAllocMapped) !=
+            cudaSuccess ||
+        cudaHostGetDevicePointer(reinterpret_cast<void**>(&h->err_dev), h->err_host, 0) !=
+            cudaSuccess) {
+        cudaGetLastError();
+        if (h->err_host) cudaFreeHost(h->err_host);
+        delete h;
+        return GEMM_ERR_ALLOC;
+    }
+    *h->err_host = 0;
+    *out = h;
+    return GEMM_OK;
+}
+
+gemm_status_t gemm_destroy(gemm_handle_t h) {
+    if (h == nullptr) return GEMM_OK;
+    cudaDeviceSynchronize();
+    if (h->ws) cudaFree(h->ws);
+    if (h->err_host) cudaFreeHost(h->err_host);
+    delete h;
+    cudaGetLastError();
+    return GEMM_OK;
+}
+
+gemm_status_t gemm_sync(gemm_handle_t h, gemm_stream_t stream) {
+    if (h == nullptr) return GEMM_ERR_INVALID_VALUE;
+    cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
+    gemm_status_t st = take_device_error(h);
+    if (st != GEMM_OK) return st;
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_LAUNCH;
+    }
+    return GEMM_OK;
+}
+
+gemm_status_t gemm_run(gemm_handle_t h, char transA, char transB, int64_t M, int64_t N, int64_t K,
+                       float alpha, const void* A, int64_t lda, const void* B, int64_t ldb,
+                       float beta, void* C, int64_t ldc, gemm_dtypes_t dt, gemm_stream_t stream_) {
+    if (h == nullptr) return GEMM_ERR_INVALID_VALUE;
+    gemm_status_t st = take_device_error(h);
+    if (st != GEMM_OK) return st;
+    Plan pl;
+    st = make_plan(transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, dt, h->num_sms,
+                   h->smem_optin, pl);
+    if (st != GEMM_OK) return st;
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+
+    if (pl.pub.path == GEMM_PATH_NOOP) return GEMM_OK;
+    if (pl.pub.path == GEMM_PATH_SCALE) {
+        const int grid = grid_for(M * N, h->num_sms);
+        if (dt.c == GEMM_F32)
+            scale_c_kernel<float><<<grid, 256, 0, stream>>>(static_cast<float*>(C), M, N, ldc, beta);
+        else if (dt.c == GEMM_F16)
+            scale_c_kernel<__half><<<grid, 256, 0, stream>>>(static_cast<__half*>(C), M, N, ldc, beta);
+        else
+            scale_c_kernel<__nv_bfloat16>
+                <<<grid, 256, 0, stream>>>(static_cast<__nv_bfloat16*>(C), M, N, ldc, beta);
+        return cudaGetLastError() == cudaSuccess ? GEMM_OK : GEMM_ERR_LAUNCH;
+    }
+
+    st = ensure_workspace(h, static_cast<size_t>(pl.pub.workspace_bytes));
+    if (st != GEMM_OK) return st;
+    uint8_t* ws = static_cast<uint8_t*>(h->ws);
+    uint8_t* ws_a = ws;
+    uint8_t* ws_b = ws_a + round_up(pl.pack_a_bytes, 256);
+    float* ws_part = reinterpret_cast<float*>(ws_b + round_up(pl.pack_b_bytes, 256));
+
+    // Pack operands whose rows TMA cannot address (pitch or base not 16-byte aligned).
+    const void* a_ptr = pl.a.ptr;
+    const void* b_ptr = pl.b.ptr;
+    if (pl.a.pack) {
+        const int grid = grid_for(pl.a.rows * pl.a.packed_ld / 8, h->num_sms);
+        pack_rows_kernel<<<grid, 256, 0, stream>>>(static_cast<const uint16_t*>(pl.a.ptr), pl.a.ld,
+                                                   pl.a.rows, pl.a.cols,
+                                                   reinterpret_cast<uint16_t*>(ws_a), pl.a.packed_ld);
+        a_ptr = ws_a;
+    }
+    if (pl.b.pack) {
+        const int grid = grid_for(pl.b.rows * pl.b.packed_ld / 8, h->num_sms);
+        pack_rows_kernel<<<grid, 256, 0, stream>>>(static_cast<const uint16_t*>(pl.b.ptr), pl.b.ld,
+                                                   pl.b.rows, pl.b.cols,
+                                                   reinterpret_cast<uint16_t*>(ws_b), pl.b.packed_ld);
+        b_ptr = ws_b;
+    }
+    if ((pl.a.pack || pl.b.pack) && cudaGetLastError() != cudaSuccess) return GEMM_ERR_LAUNCH;
+
+    TcLaunch l;
+    std::memset(&l, 0, sizeof l);
+    const int bn = pl.pub.block_n;
+    bool ok = encode_operand(h, &l.tmA, dt.a, a_ptr, pl.a.cols, pl.a.rows, pl.a.packed_ld,
+                             pl.a.mn_major ? 64u : static_cast<uint32_t>(kBlockM));
+    ok = ok && encode_operand(h, &l.tmB, dt.b, b_ptr, pl.b.cols, pl.b.rows, pl.b.packed_ld,
+                              pl.b.mn_major ? 64u : static_cast<uint32_t>(bn));
+    if (!ok) return GEMM_ERR_LAUNCH;
+
+    TcParams& p = l.p;
+    p.M = static_cast<int32_t>(pl.Mk);
+    p.N = static_cast<int32_t>(pl.Nk);
+    p.k_blocks = pl.k_blocks;
+    p.tiles_m = pl.tiles_m;
+    p.tiles_n = pl.tiles_n;
+    p.num_tiles = pl.pub.num_tiles;
+    p.group_m = kGroupM;
+    p.stages = pl.pub.stages;
+    p.a_mn_major = pl.a.mn_major ? 1 : 0;
+    p.b_mn_major = pl.b.mn_major ? 1 : 0;
+    p.idesc = instr_desc_f16(dt.a == GEMM_BF16, pl.a.mn_major, pl.b.mn_major, kBlockM,
+                             static_cast<uint32_t>(bn));
+    p.stream_k = pl.sk_len > 0 ? 1 : 0;
+    p.sk_len = pl.sk_len;
+    p.sk_max_seg = pl.sk_max_seg;
+    p.alpha = alpha;
+    p.beta = beta;
+    p.C = C;
+    p.c_rs = pl.c_rs;
+    p.c_cs = pl.c_cs;
+    p.c_vector = pl.pub.c_vector;
+    p.partials = pl.partial_bytes > 0 ? ws_part : nullptr;
+    p.err = h->err_dev;
+    l.grid = pl.pub.grid;
+    l.block_n = bn;
+    l.smem_bytes = pl.smem_bytes;
+    l.stream = stream;
+
+    cudaError_t e;
+    if (dt.c == GEMM_F32) e = launch_tc_f32(l);
+    else if (dt.c == GEMM_F16) e = launch_tc_f16(l);
+    else e = launch_tc_bf16(l);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_LAUNCH;
+    }
+    if (p.stream_k) {
+        const int grid = grid_for(static_cast<int64_t>(p.num_tiles) * kBlockM * (bn / 4),
+                                  h->num_sms);
+        if (dt.c == GEMM_F32) e = launch_fixup_f32(l, grid);
+        else if (dt.c == GEMM_F16) e = launch_fixup_f16(l, grid);
+        else e = launch_fixup_bf16(l, grid);
+        if (e != cudaSuccess) {
+            cudaGetLastError();
+            return GEMM_ERR_LAUNCH;
+        }
+    }
+    return GEMM_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,4 @@
+// kern_bf16.cu -- tcgen05 GEMM kernels with bf16 output.
+#define KERN_OUT_T __nv_bfloat16
+#define KERN_SUFFIX bf16
+#include "kern_inst.cuh"

@@ -1,0 +1,4 @@
+// kern_f16.cu -- tcgen05 GEMM kernels with f16 output.
+#define KERN_OUT_T __half
+#define KERN_SUFFIX f16
+#include "kern_inst.cuh"

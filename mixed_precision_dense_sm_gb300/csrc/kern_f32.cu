@@ -1,0 +1,4 @@
+// kern_f32.cu -- tcgen05 GEMM kernels with f32 output.
+#define KERN_OUT_T float
+#define KERN_SUFFIX f32
+#include "kern_inst.cuh"

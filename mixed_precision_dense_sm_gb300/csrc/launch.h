@@ -1,0 +1,29 @@
+// launch.h -- internal interface between the host planner (api.cu) and the
+// translation units that instantiate the kernels for each output type.
+#pragma once
+#include <cstddef>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "gemm_tc.cuh"
+
+namespace gemm103 {
+
+struct TcLaunch {
+    CUtensorMap tmA, tmB;
+    TcParams p;
+    int grid;
+    int block_n;
+    size_t smem_bytes;
+    cudaStream_t stream;
+};
+
+// Output type codes follow gemm_dtype_t: 0 = F16, 1 = BF16, 2 = F32.
+cudaError_t launch_tc_f32(const TcLaunch& l);
+cudaError_t launch_tc_f16(const TcLaunch& l);
+cudaError_t launch_tc_bf16(const TcLaunch& l);
+cudaError_t launch_fixup_f32(const TcLaunch& l, int grid);
+cudaError_t launch_fixup_f16(const TcLaunch& l, int grid);
+cudaError_t launch_fixup_bf16(const TcLaunch& l, int grid);
+
+}  // namespace gemm103

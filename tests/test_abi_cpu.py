@@ -1,0 +1,168 @@
+"""The C ABI library on the CPU: it loads, exports every symbol the header
+declares, validates arguments and plans paths (host logic only, no GPU)."""
+import ctypes
+import itertools
+import subprocess
+
+import pytest
+import torch
+
+import mixed_precision_dense_sm_gb300 as lib
+import workloads
+from workloads import DT_BF16, DT_F16, DT_F32
+
+F16F32 = (DT_F16, DT_F16, DT_F32)
+
+
+def test_exports_every_declared_symbol():
+    declared = lib.declared_symbols()
+    assert declared == sorted(["gemm_check_args", "gemm_create", "gemm_destroy",
+                               "gemm_plan_query", "gemm_run", "gemm_status_string",
+                               "gemm_sync"]) or set(declared) >= {"gemm_create", "gemm_run"}
+    out = subprocess.run(["nm", "-D", "--defined-only", lib.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = {ln.split()[-1] for ln in out.splitlines() if " T " in ln}
+    for name in declared:
+        assert name in exported, name
+        assert hasattr(lib.lib, name)
+
+
+def test_status_strings():
+    for code, name in lib.STATUS.items():
+        assert lib.gemm_status_string(code) == name
+    assert lib.gemm_status_string(99) == "GEMM_ERR_UNKNOWN"
+
+
+def test_check_args():
+    ok = dict(ta="N", tb="N", M=8, N=8, K=8, alpha=1.0, A=16, lda=8, B=16, ldb=8, beta=0.0,
+              C=16, ldc=8, dt=F16F32)
+
+    def call(**kw):
+        a = dict(ok)
+        a.update(kw)
+        return lib.gemm_check_args(a["ta"], a["tb"], a["M"], a["N"], a["K"], a["alpha"], a["A"],
+                                   a["lda"], a["B"], a["ldb"], a["beta"], a["C"], a["ldc"],
+                                   a["dt"])
+
+    assert call() == 0
+    assert call(ta="t", tb="n") == 0
+    for bad in [dict(ta="X"), dict(tb="?"), dict(M=-1), dict(N=-2), dict(K=-3),
+                dict(lda=7), dict(ldb=7), dict(ldc=7), dict(ta="T", lda=7, M=8),
+                dict(tb="T", ldb=7), dict(dt=(DT_F16, DT_BF16, DT_F32)),
+                dict(dt=(DT_F32, DT_F32, DT_F32)), dict(dt=(DT_F16, DT_F16, 5)),
+                dict(A=0), dict(B=0), dict(C=0), dict(M=2 ** 31)]:
+        assert call(**bad) == 1, bad
+    # quick-return forms
+    assert call(M=0, C=0, A=0, B=0) == 0
+    assert call(K=0, A=0, B=0) == 0
+    assert call(alpha=0.0, A=0, B=0) == 0
+    assert call(K=0, lda=1) == 0
+
+
+def plan(w: workloads.Workload, ptr=256, **kw):
+    lda, ldb, ldc = w.lds()
+    st, p = lib.gemm_plan_query(w.transA, w.transB, w.M, w.N, w.K, w.alpha, ptr, lda, ptr, ldb,
+                                w.beta, ptr, ldc, (w.ab_dtype, w.ab_dtype, w.c_dtype), **kw)
+    assert st == 0
+    return p
+
+
+def test_plans_of_named_workloads():
+    P = {n: plan(w) for n, w in workloads.WORKLOADS.items()}
+    big = P["linear_8192x4096x4096_bf16"]
+    assert big["path_name"] == "tiled_1sm" and big["block_n"] == 256 and big["sk_len"] == 0
+    assert big["grid"] == 152 and big["num_tiles"] == 64 * 16
+    sk = P["skinny_64x16384x8192_f16"]
+    assert sk["path_name"] == "skinny" and sk["swap_ab"] == 1 and sk["block_n"] == 64
+    rag = P["ragged1000x1023x777_bf16_beta1"]
+    assert rag["pack_a"] == 1 and rag["pack_b"] == 1 and rag["c_vector"] == 0
+    assert rag["b_mn_major"] == 1 and rag["a_mn_major"] == 0
+    sq = P["square1024_f16_nt_f16out"]
+    assert sq["pack_a"] == 0 and sq["pack_b"] == 0 and sq["b_mn_major"] == 0
+    for p in P.values():
+        assert 2 <= p["stages"] <= 8
+        stage = 128 * 64 * 2 + p["block_n"] * 64 * 2
+        assert p["stages"] * stage + 1024 + 256 <= 232448
+
+
+def test_quick_paths_and_swap_rule():
+    w = workloads.Workload("q", 0, 5, 5, "N", "N", DT_F16, DT_F32, 1.0, 0.0, "U", "U")
+    assert plan(w)["path_name"] == "noop"
+    w = workloads.Workload("q", 5, 5, 0, "N", "N", DT_F16, DT_F32, 1.0, 1.0, "U", "U", "U")
+    assert plan(w)["path_name"] == "scale"
+    w = workloads.Workload("q", 5, 5, 5, "N", "N", DT_F16, DT_F32, 0.0, 1.0, "U", "U", "U")
+    assert plan(w)["path_name"] == "scale"
+    w = workloads.Workload("q", 64, 128, 64, "N", "N", DT_F16, DT_F32, 1.0, 0.0, "U", "U")
+    assert plan(w)["swap_ab"] == 1
+    w = workloads.Workload("q", 65, 128, 64, "N", "N", DT_F16, DT_F32, 1.0, 0.0, "U", "U")
+    assert plan(w)["swap_ab"] == 0
+
+
+def test_pack_rule_follows_16_byte_alignment():
+    w = workloads.Workload("p", 100, 100, 100, "N", "N", DT_F16, DT_F32, 1.0, 0.0, "U", "U",
+                           lda=104, ldb=100 + 3)
+    p = plan(w)
+    assert p["pack_a"] == 0 and p["pack_b"] == 1
+    p = plan(w, ptr=258)          # misaligned base: everything packs, C scalar path
+    assert p["pack_a"] == 1 and p["pack_b"] == 1 and p["c_vector"] == 0
+
+
+def simulate_stream_k(p):
+    """Replays the device-side segment iteration for every CTA and checks the
+    schedule: each (tile, k-block) is covered exactly once, partial slots are
+    unique and in range, and the fixup's slot lookup finds the same slots."""
+    T, KB, L, G, S = p["num_tiles"], p["k_blocks"], p["sk_len"], p["grid"], p["sk_max_seg"]
+    total = T * KB
+    covered = [0] * total
+    slots = {}
+    for g in range(G):
+        pos, end = min(g * L, total), min(g * L + L, total)
+        assert pos < end, "a CTA without work"
+        while pos < end:
+            tile = pos // KB
+            kb0 = pos - tile * KB
+            take = min(KB - kb0, end - pos)
+            for k in range(kb0, kb0 + take):
+                covered[tile * KB + k] += 1
+            pos += take
+            if not (kb0 == 0 and take == KB):
+                first_tile = (g * L) // KB
+                slot = g * S + (tile - first_tile)
+                assert 0 <= tile - first_tile < S
+                assert slot not in slots
+                slots[slot] = (tile, g)
+    assert all(c == 1 for c in covered)
+    for tile in range(T):
+        g_first, g_last = (tile * KB) // L, ((tile + 1) * KB - 1) // L
+        if g_first == g_last:
+            continue
+        for g in range(g_first, g_last + 1):
+            slot = g * S + tile - (g * L) // KB
+            assert slots.get(slot) == (tile, g)
+    assert len(slots) * 128 * p["block_n"] * 4 <= p["workspace_bytes"]
+
+
+@pytest.mark.parametrize("shape", [(256, 256, 256), (1024, 1024, 1024), (1000, 1023, 777),
+                                   (64, 16384, 8192), (5, 300, 700), (129, 300, 777),
+                                   (257, 129, 4096), (33, 128, 2048), (1, 1, 100000)])
+@pytest.mark.parametrize("sms", [148, 152, 7])
+def test_stream_k_schedule_covers_every_block_once(shape, sms):
+    M, N, K = shape
+    w = workloads.Workload("s", M, N, K, "N", "T", DT_BF16, DT_BF16, 1.0, 0.0, "U", "U")
+    p = plan(w, num_sms=sms)
+    if p["sk_len"] == 0:
+        assert p["num_tiles"] >= sms or p["k_blocks"] < 4
+        return
+    assert p["grid"] <= sms
+    simulate_stream_k(p)
+
+
+def test_create_fails_cleanly_without_gpu():
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    h = ctypes.c_void_p(1234)
+    st = lib.lib.gemm_create(ctypes.byref(h))
+    assert st in (2, 4) and h.value is None
+    assert lib.gemm_destroy(None) == 0
+    assert lib.gemm_sync(None, None) == 1
+    assert lib.gemm_run(None, "N", "N", 1, 1, 1, 1.0, 16, 1, 16, 1, 0.0, 16, 1, F16F32) == 1

@@ -1,0 +1,196 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle."""
+import itertools
+
+import numpy as np
+import pytest
+import torch
+
+import gpu_cases as gc
+import workloads
+from workloads import DT_BF16, DT_F16, DT_F32, Workload
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def g():
+    import mixed_precision_dense_sm_gb300 as lib
+    h = lib.Gemm()
+    yield h
+    h.close()
+
+
+def W(M, N, K, ta="N", tb="N", ab=DT_F16, c=DT_F32, alpha=1.0, beta=0.0, lda=None, ldb=None,
+      ldc=None, dist="N1", seed=0, name=None):
+    return Workload(name or f"{M}x{N}x{K}_{ta}{tb}", M, N, K, ta, tb, ab, c, alpha, beta,
+                    dist, dist, dist if beta != 0 else None, lda, ldb, ldc, seed)
+
+
+def test_layout_4x4_block(g, orc):
+    """A 4 x 4 block first (DeepGEMM page, section 4.4): distinct small integers
+    in every position, every transpose pair, both input types, exact."""
+    for ta, tb, ab in itertools.product("NT", "NT", (DT_F16, DT_BF16)):
+        w = W(4, 4, 4, ta, tb, ab, DT_F32)
+        A = torch.arange(16, dtype=torch.float32).view(4, 4) - 7
+        B = (torch.arange(16, dtype=torch.float32).view(4, 4) * 3) % 11 - 5
+        t = workloads.TORCH_DTYPE[ab]
+        inp = workloads.Inputs(A.to(t), B.to(t), None, 4, 4, 4)
+        C = gc.run_gpu(g, w, inp)
+        gc.check_full(orc, w, inp, C, exact=True)
+
+
+SIZES = [1, 2, 3, 15, 16, 17, 63, 64, 65, 127, 128, 129]
+
+
+def _tiny_cases():
+    rng = np.random.default_rng(5)
+    cases = []
+    for n in range(72):
+        M, N, K = (int(rng.choice(SIZES)) for _ in range(3))
+        ta, tb = "NT"[n % 2], "NT"[(n // 2) % 2]
+        ab = (DT_F16, DT_BF16)[(n // 4) % 2]
+        c = (DT_F32, DT_F16, DT_BF16)[n % 3]
+        cases.append((M, N, K, ta, tb, ab, c))
+    return cases
+
+
+@pytest.mark.parametrize("integer", [True, False], ids=["integer_exact", "random_tol"])
+def test_tiny_shapes(g, orc, integer):
+    """Tiny ragged shapes across every transpose pair and type combination.
+    Integer inputs keep every FP32 partial sum exact, so the result must be
+    bit-identical to the oracle's correctly rounded value."""
+    for (M, N, K, ta, tb, ab, c) in _tiny_cases():
+        beta = 0.0 if (M + N) % 2 else 1.0
+        w = W(M, N, K, ta, tb, ab, c, alpha=1.0 if integer else 0.75, beta=beta, seed=M * N + K)
+        inp = gc.integer_inputs(w) if integer else workloads.make_inputs(w)
+        C = gc.run_gpu(g, w, inp)
+        gc.check_full(orc, w, inp, C, exact=integer)
+
+
+MEDIUM = [
+    (300, 520, 1000), (257, 129, 4096), (129, 300, 777), (1000, 1023, 777),
+    (5, 300, 700), (64, 1000, 513), (33, 128, 2048), (640, 768, 320),
+]
+
+
+@pytest.mark.parametrize("M,N,K", MEDIUM, ids=[f"{m}x{n}x{k}" for m, n, k in MEDIUM])
+def test_medium_integer_exact(g, orc, M, N, K):
+    """Several tiles with ragged tails (data-parallel, stream-K and skinny
+    paths); integer inputs, bit-exact against the oracle."""
+    for ta, tb in itertools.product("NT", "NT"):
+        c = (DT_F32, DT_BF16, DT_F16)[(M + N + K) % 3]
+        w = W(M, N, K, ta, tb, DT_BF16 if K % 2 else DT_F16, c, beta=1.0 if K % 3 == 0 else 0.0)
+        inp = gc.integer_inputs(w)
+        C = gc.run_gpu(g, w, inp)
+        gc.check_full(orc, w, inp, C, exact=True)
+
+
+@pytest.mark.parametrize("name", ["square256_f16_f32out", "square1024_f16_nt_f16out",
+                                  "ragged1000x1023x777_bf16_beta1", "skinny_64x16384x8192_f16"])
+def test_workload_full(g, orc, name):
+    """The named workloads at full size, every output element checked."""
+    w = workloads.WORKLOADS[name]
+    inp = workloads.make_inputs(w)
+    C = gc.run_gpu(g, w, inp)
+    stats = gc.check_full(orc, w, inp, C)
+    print(name, stats)
+
+
+@pytest.mark.parametrize("name", ["linear_8192x4096x4096_bf16", "linear_8192x14336x4096_bf16",
+                                  "linear_8192x4096x14336_bf16"])
+def test_workload_sampled(g, orc, name):
+    """The transformer-layer shapes at full size, sampled outputs."""
+    w = workloads.WORKLOADS[name]
+    inp = workloads.make_inputs(w)
+    C = gc.run_gpu(g, w, inp)
+    stats = gc.check_sampled(orc, w, inp, C)
+    print(name, stats)
+
+
+def test_padded_leading_dimensions(g, orc):
+    """lda/ldb/ldc larger than the rows: NaN in the operand padding must not be
+    read, the C padding (canary) must not be written."""
+    for ta, tb in itertools.product("NT", "NT"):
+        for (M, N, K) in [(200, 300, 150), (64, 256, 96)]:
+            a_cols = K if ta == "N" else M
+            b_cols = N if tb == "N" else K
+            w = W(M, N, K, ta, tb, DT_BF16, DT_BF16, beta=1.0, lda=a_cols + 8,
+                  ldb=b_cols + 16, ldc=N + 8)
+            inp = workloads.make_inputs(w)
+            C = gc.run_gpu(g, w, inp)
+            gc.check_full(orc, w, inp, C)
+
+
+def test_unaligned_pitch_and_base(g, orc):
+    """Leading dimensions that are not a multiple of 8 elements and base
+    addresses that are not 16-byte aligned go through the pack pre-pass."""
+    for ta, tb in itertools.product("NT", "NT"):
+        M, N, K = 150, 201, 333
+        a_cols = K if ta == "N" else M
+        b_cols = N if tb == "N" else K
+        w = W(M, N, K, ta, tb, DT_F16, DT_F32, beta=1.0, lda=a_cols + 1, ldb=b_cols + 3,
+              ldc=N + 1)
+        inp = gc.integer_inputs(w)
+        C = gc.run_gpu(g, w, inp, misalign=True)
+        gc.check_full(orc, w, inp, C, exact=True)
+
+
+def test_quick_returns(g, orc):
+    import mixed_precision_dense_sm_gb300 as lib
+    # M == 0 / N == 0: nothing touched
+    C = torch.full((4, 4), 7.0, device="cuda")
+    A = torch.ones((4, 4), dtype=torch.float16, device="cuda")
+    g(A, A, C, M=0, N=4, K=4)
+    g(A, A, C, M=4, N=0, K=4)
+    g.sync()
+    assert torch.all(C == 7.0)
+    # K == 0: C = beta * C, A and B not read (NULL allowed)
+    s = torch.cuda.current_stream().cuda_stream
+    st = lib.gemm_run(g.h, "N", "N", 4, 4, 0, 1.0, 0, 1, 0, 4, 0.5, C.data_ptr(), 4,
+                      (DT_F16, DT_F16, DT_F32), s)
+    assert st == 0
+    g.sync()
+    assert torch.all(C == 3.5)
+    # alpha == 0, beta == 0: zeros even when C held NaN
+    C.fill_(float("nan"))
+    st = lib.gemm_run(g.h, "N", "N", 4, 4, 4, 0.0, 0, 4, 0, 4, 0.0, C.data_ptr(), 4,
+                      (DT_F16, DT_F16, DT_F32), s)
+    assert st == 0
+    g.sync()
+    assert torch.all(C == 0.0)
+
+
+def test_invalid_arguments_enqueue_nothing(g):
+    import mixed_precision_dense_sm_gb300 as lib
+    C = torch.full((8, 8), 3.0, device="cuda")
+    A = torch.ones((8, 8), dtype=torch.float16, device="cuda")
+    s = torch.cuda.current_stream().cuda_stream
+    bad = [
+        dict(ta="X"), dict(M=-1), dict(lda=7), dict(ldb=7), dict(ldc=7),
+        dict(dts=(DT_F16, DT_BF16, DT_F32)), dict(dts=(DT_F32, DT_F32, DT_F32)),
+        dict(dts=(DT_F16, DT_F16, 9)), dict(a=0), dict(c=0),
+    ]
+    for b in bad:
+        kw = dict(ta="N", M=8, lda=8, ldb=8, ldc=8, dts=(DT_F16, DT_F16, DT_F32),
+                  a=A.data_ptr(), c=C.data_ptr())
+        kw.update(b)
+        st = lib.gemm_run(g.h, kw["ta"], "N", kw["M"], 8, 8, 1.0, kw["a"], kw["lda"],
+                          A.data_ptr(), kw["ldb"], 0.0, kw["c"], kw["ldc"], kw["dts"], s)
+        assert st == 1, (b, st)
+    g.sync()
+    assert torch.all(C == 3.0)
+
+
+def test_deterministic_and_stream(g, orc):
+    """Bitwise-identical results on repeated calls (the stream-K fixup adds
+    partial sums in a fixed order), on a non-default stream."""
+    w = W(1000, 1023, 777, "N", "N", DT_BF16, DT_F32, beta=1.0)
+    inp = workloads.make_inputs(w)
+    s = torch.cuda.Stream()
+    outs = []
+    for _ in range(5):
+        with torch.cuda.stream(s):
+            outs.append(gc.run_gpu(g, w, inp, stream=s.cuda_stream).cpu())
+    for o in outs[1:]:
+        assert torch.equal(o.view(torch.int32), outs[0].view(torch.int32))
+    gc.check_full(orc, w, inp, outs[0].cuda())

@@ -62,8 +62,8 @@ class Workload:
         return (self.K, self.N) if self.transB in "Nn" else (self.N, self.K)
 
     def lds(self):
-        return (self.lda or self.a_shape()[1], self.ldb or self.b_shape()[1],
-                self.ldc or self.N)
+        return (self.lda or max(1, self.a_shape()[1]), self.ldb or max(1, self.b_shape()[1]),
+                self.ldc or max(1, self.N))
 
     def flops(self) -> float:
         return 2.0 * self.M * self.N * self.K
