@@ -1,0 +1,468 @@
+"""Throughput benchmark of the GB300 mixed-precision GEMM (one JSON line).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME]
+
+A step is one pass of the hot path over one batch of synthetic input: by
+default the three GEMMs of a transformer layer at 8192 tokens (BF16 inputs,
+weights stored N x K, FP32 accumulation, BF16 output):
+    8192 x 4096 x 4096, 8192 x 14336 x 4096, 8192 x 4096 x 14336.
+Throughput is 2*M*N*K per GEMM summed over the step, divided by the
+device-timed step (CUDA events on the launching stream, W warm-up steps,
+barrier + synchronize around K timed steps, max over ranks).  Every step
+touches about 1 GB of operands, far more than the 129 MB L2, so no L2 flush is
+needed between steps.
+
+Also reported:
+  roofline     -- the dominant kernel's achieved TFLOP/s (algorithmic flops per
+                  launch / mean launch duration from events around each launch)
+                  against the measured dense BF16 peak in MEASURED_PEAKS.json;
+                  `traffic` is the DRAM bytes per launch from the committed ncu
+                  summary when it was taken on the current kernel sources;
+  e2e          -- the same metric through the C ABI with host (pinned) buffers:
+                  each step copies its inputs host->device and the outputs back;
+  cpu_baseline -- the CPU oracle (plain FP64 triple loop, all host cores) timed
+                  on a bounded sample of the same workload (rank 0, N = 1);
+  clocks       -- nvidia-smi SM clocks and throttle reasons sampled during the
+                  timed region.
+--impl reference times the CPU oracle as the comparison arm (the pages ship
+no runnable implementation); it runs on rank 0 only.
+With N > 1 (torchrun, one rank per GPU) every rank runs the same step on its
+own GPU: replicas, no collective on the data path (weak scaling).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import workloads  # noqa: E402
+
+METRIC = "GEMM TFLOP/s (2MNK/t) at 1 GB300; % of dense tensor peak or HBM roofline"
+LAYER = ["linear_8192x4096x4096_bf16", "linear_8192x14336x4096_bf16",
+         "linear_8192x4096x14336_bf16"]
+FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+KERNEL_SOURCES = ["mixed_precision_dense_sm_gb300/csrc/gemm_tc.cuh",
+                  "mixed_precision_dense_sm_gb300/csrc/ptx.cuh",
+                  "mixed_precision_dense_sm_gb300/csrc/kern_inst.cuh"]
+
+
+def kernel_hash() -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK), "fallback"
+
+
+def committed_traffic(workload: str):
+    """DRAM bytes per launch from profiles/traffic.json, if taken on these sources."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f)
+    e = d.get(workload)
+    if not e or e.get("kernel_hash") != kernel_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi SM clock / throttle-reason samples during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def _read(self):
+        for ln in self.proc.stdout:
+            self.lines.append(ln.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def workload_list(name: str):
+    if name == "transformer_layer":
+        return [workloads.WORKLOADS[n] for n in LAYER]
+    return [workloads.WORKLOADS[name]]
+
+
+def describe(name: str, ws):
+    if name == "transformer_layer":
+        return ("transformer linear layers at 8192 tokens, BF16 activations N(0,1) and "
+                "N x K weights N(0,0.02), FP32 accumulate, BF16 out: "
+                "8192x4096x4096 + 8192x14336x4096 + 8192x4096x14336 (M x N x K) per step")
+    w = ws[0]
+    return f"{w.name}: {w.M}x{w.N}x{w.K} {w.transA}{w.transB}"
+
+
+# ------------------------------------------------------------------ CPU oracle
+
+def oracle_sample(ws, target_s: float = 12.0):
+    """Time the CPU oracle on the first rows of each GEMM of the step (the
+    full triple loop restricted to those rows).  The row count is calibrated
+    so the sample takes about target_s seconds; returns
+    (flops, seconds, rows, threads)."""
+    import numpy as np
+    import oracle
+    orc = oracle.get()
+    threads = orc.max_threads()
+
+    def timed(rows):
+        total_t, flops = 0.0, 0.0
+        for w in ws:
+            inp = workloads.make_inputs(w)
+            r = min(rows, w.M)
+            A = workloads.as_codes(inp.A)
+            if w.transA in "Nn":
+                a_rows, a_ld = A[:r], inp.lda
+            else:
+                a_rows, a_ld = np.ascontiguousarray(A[:, :r]), r
+            Bc = workloads.as_codes(inp.B)
+            t = time.perf_counter()
+            orc.gemm(w.transA, w.transB, r, w.N, w.K, w.alpha, a_rows, a_ld, Bc, inp.ldb, 0.0,
+                     None, w.N, w.ab_dtype, w.c_dtype)
+            total_t += time.perf_counter() - t
+            flops += 2.0 * r * w.N * w.K
+        return flops, total_t
+
+    f1, t1 = timed(4)
+    rows = max(4, int(4 * target_s / max(t1, 1e-3)))
+    rows = min(rows, min(w.M for w in ws))
+    f, t = timed(rows)
+    return f, t, rows, threads
+
+
+# ------------------------------------------------------------------ GPU arm
+
+def run_ours(args):
+    import mixed_precision_dense_sm_gb300 as lib
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    ws = workload_list(args.workload)
+    g = lib.Gemm()
+    stream = torch.cuda.current_stream()
+    sh = stream.cuda_stream
+
+    bufs = []
+    for w in ws:
+        inp = workloads.make_inputs(w)
+        A, B = inp.A.cuda(), inp.B.cuda()
+        cdt = workloads.TORCH_DTYPE[w.c_dtype]
+        C = (inp.C.cuda() if inp.C is not None
+             else torch.zeros((w.M, inp.ldc), dtype=cdt, device="cuda"))
+        bufs.append((w, inp, A, B, C))
+    del inp
+
+    plans = []
+    for (w, inp, A, B, C) in bufs:
+        st, p = lib.gemm_plan_query(w.transA, w.transB, w.M, w.N, w.K, w.alpha, A.data_ptr(),
+                                    inp.lda, B.data_ptr(), inp.ldb, w.beta, C.data_ptr(), inp.ldc,
+                                    (w.ab_dtype, w.ab_dtype, w.c_dtype),
+                                    num_sms=torch.cuda.get_device_properties(local).multi_processor_count)
+        plans.append(p)
+    launches_per_step = sum(1 + p["pack_a"] + p["pack_b"] + (1 if p["sk_len"] else 0)
+                            for p in plans)
+
+    def step(events=None):
+        for i, (w, inp, A, B, C) in enumerate(bufs):
+            if events is not None:
+                events[i][0].record(stream)
+            st = lib.gemm_run(g.h, w.transA, w.transB, w.M, w.N, w.K, w.alpha, A.data_ptr(),
+                              inp.lda, B.data_ptr(), inp.ldb, w.beta, C.data_ptr(), inp.ldc,
+                              (w.ab_dtype, w.ab_dtype, w.c_dtype), sh)
+            if st != 0:
+                raise lib.GemmError(st, "gemm_run")
+            if events is not None:
+                events[i][1].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    g.sync()
+
+    # timed region: K steps; per-launch events give the roofline figures
+    ev = [[[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)]
+           for _ in bufs] for _ in range(args.steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local)
+    barrier(world)
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.25)
+    t_start.record(stream)
+    for k in range(args.steps):
+        step(ev[k])
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    barrier(world)
+    g.sync()
+    ms_total = t_start.elapsed_time(t_end)
+    ms_total = max_over_ranks(ms_total, world)
+    ms_step = ms_total / args.steps
+    flops_step = sum(w.flops() for w in ws)
+    value = world * flops_step * args.steps / (ms_total * 1e-3) / 1e12
+
+    # dominant kernel: the main GEMM launch of each call
+    launch_ms = [statistics.fmean(ev[k][i][0].elapsed_time(ev[k][i][1])
+                                  for k in range(args.steps)) for i in range(len(bufs))]
+    dom = max(range(len(bufs)), key=lambda i: launch_ms[i])
+    achieved = sum(w.flops() for w in ws) / (sum(launch_ms) * 1e-3) / 1e12
+    peaks, peak_src = load_peaks()
+    bound = "tensor"
+    peak = peaks["bf16_tflops"]
+    ws_names = [w.name for w in ws]
+    if all(w.M <= 64 for w in ws):       # skinny: HBM-bound
+        bound = "hbm"
+        gbs = sum(w.algorithmic_bytes() for w in ws) / (sum(launch_ms) * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "frac": round(gbs / peaks["hbm_gbs"], 4)}
+    else:
+        roof = {"bound": bound, "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
+                "frac": round(achieved / peak, 4),
+                "frac_of_sustained": round(achieved / peaks["bf16_tflops_sustained"], 4)}
+    traffic = [committed_traffic(n) for n in ws_names]
+    roof["traffic"] = (sum(traffic) / len(traffic)) if all(t is not None for t in traffic) else None
+    roof["peak_source"] = f"{peak_src} ({'MEASURED_PEAKS.json' if peak_src == 'measured' else 'recipe fallback'})"
+    roof["kernel"] = "gemm_tc_kernel"
+    roof["launch_ms"] = [round(x, 4) for x in launch_ms]
+    roof["per_launch_tflops"] = [round(w.flops() / (t * 1e-3) / 1e12, 1)
+                                 for w, t in zip(ws, launch_ms)]
+
+    # e2e: host buffers through the C ABI; copies inside the timed region
+    e2e = run_e2e(lib, g, bufs, stream, args, world)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        f, t, rows, threads = oracle_sample(ws)
+        cpu = {"value": round(f / t / 1e12, 6), "unit": "TFLOP/s", "cores": threads,
+               "kind": "oracle",
+               "sample": f"first {rows} rows of each GEMM of the step (full N and K), "
+                         f"{f / 1e9:.1f} GFLOP in {t:.1f} s"}
+
+    out = {
+        "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": describe(args.workload, ws), "shapes": ws_names,
+                   "l2": "no flush: each step touches "
+                         f"{sum(w.algorithmic_bytes() for w in ws) / 1e9:.2f} GB > 129 MB L2",
+                   "parallelism": "replicas" if world > 1 else "single GPU",
+                   "paths": [p["path_name"] for p in plans]},
+        "roofline": roof, "e2e": e2e, "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk,
+    }
+    if cpu is not None:
+        out["cpu_baseline"] = cpu
+    g.close()
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def run_e2e(lib, g, bufs, stream, args, world):
+    """Same step with inputs in pinned host memory: H2D copies, the GEMMs,
+    D2H of every output, all inside the timed region."""
+    host = []
+    h2d = d2h = 0
+    for (w, inp, A, B, C) in bufs:
+        hA, hB = inp.A.pin_memory(), inp.B.pin_memory()
+        hC = torch.empty(C.shape, dtype=C.dtype).pin_memory()
+        host.append((hA, hB, hC))
+        h2d += hA.numel() * hA.element_size() + hB.numel() * hB.element_size()
+        if w.beta != 0:
+            h2d += C.numel() * C.element_size()
+        d2h += hC.numel() * hC.element_size()
+    sh = stream.cuda_stream
+
+    def step():
+        for (w, inp, A, B, C), (hA, hB, hC) in zip(bufs, host):
+            A.copy_(hA, non_blocking=True)
+            B.copy_(hB, non_blocking=True)
+            st = lib.gemm_run(g.h, w.transA, w.transB, w.M, w.N, w.K, w.alpha, A.data_ptr(),
+                              inp.lda, B.data_ptr(), inp.ldb, w.beta, C.data_ptr(), inp.ldc,
+                              (w.ab_dtype, w.ab_dtype, w.c_dtype), sh)
+            if st != 0:
+                raise lib.GemmError(st, "gemm_run")
+            hC.copy_(C, non_blocking=True)
+
+    for _ in range(min(args.warmup, 3)):
+        step()
+    steps = max(3, min(args.steps, 20))
+    barrier(world)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = max_over_ranks(e0.elapsed_time(e1), world)
+    flops = sum(w.flops() for (w, *_rest) in bufs)
+    return {"value": round(world * flops * steps / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
+            "ms_per_step": round(ms / steps, 4)}
+
+
+# ------------------------------------------------------------ reference arm
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    ws = workload_list(args.workload)
+    # each step: the oracle on a bounded sample (first rows of each GEMM)
+    f0, t0, rows, threads = oracle_sample(ws, target_s=4.0)
+    times = []
+    for k in range(args.warmup + args.steps):
+        f, t, _, _ = _oracle_rows(ws, rows)
+        if k >= args.warmup:
+            times.append(t)
+    t = sum(times)
+    value = f * len(times) / t / 1e12
+    sample = (f"first {rows} rows of each GEMM of the step (full N and K): "
+              f"{f / 1e9:.1f} GFLOP per step")
+    out = {"metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": world,
+           "steps": args.steps, "warmup": args.warmup,
+           "ms_per_step": round(1e3 * t / len(times), 2), "higher_is_better": True,
+           "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+           "impl": "reference",
+           "config": {"workload": describe(args.workload, ws), "shapes": [w.name for w in ws]},
+           "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": threads,
+                            "kind": "oracle", "sample": sample},
+           "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                   "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+
+
+def _oracle_rows(ws, rows):
+    import numpy as np
+    import oracle
+    orc = oracle.get()
+    total_t, flops = 0.0, 0.0
+    for w in ws:
+        inp = workloads.make_inputs(w)
+        r = min(rows, w.M)
+        A = workloads.as_codes(inp.A)
+        if w.transA in "Nn":
+            a_rows, a_ld = A[:r], inp.lda
+        else:
+            a_rows, a_ld = np.ascontiguousarray(A[:, :r]), r
+        Bc = workloads.as_codes(inp.B)
+        t = time.perf_counter()
+        orc.gemm(w.transA, w.transB, r, w.N, w.K, w.alpha, a_rows, a_ld, Bc, inp.ldb, 0.0, None,
+                 w.N, w.ab_dtype, w.c_dtype)
+        total_t += time.perf_counter() - t
+        flops += 2.0 * r * w.N * w.K
+    return flops, total_t, rows, orc.max_threads()
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="transformer_layer",
+                    choices=["transformer_layer"] + list(workloads.WORKLOADS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -137,4 +137,5 @@ def check_canary(w, Cdev):
     ldc = Cdev.shape[1]
     if ldc > w.N:
         pad = Cdev[:, w.N:].float().cpu()
-        assert torch.all(pad == CANARY), f"{w.name}: C padding columns were written"
+        want = torch.tensor(CANARY, dtype=Cdev.dtype).float()
+        assert torch.all(pad == want), f"{w.name}: C padding columns were written"
