@@ -174,6 +174,42 @@ gemm_status_t gemm_plan_query(char transA, char transB, int64_t M, int64_t N, in
                               gemm_dtypes_t dt, int32_t num_sms, int32_t smem_optin,
                               gemm_plan_t* out);
 
+/* Size of the static device scratch used by gemm_run_noalloc (32 MiB). */
+#define GEMM_NOALLOC_SCRATCH_BYTES (32u << 20)
+
+/*
+ * gemm_run_noalloc: gemm_run for callers that cannot allocate device memory.
+ * There is no counterpart on the pages; it exists because some callers may not
+ * call cudaMalloc at all -- code running inside a memory pool or allocator
+ * that must not re-enter the CUDA allocator, code that has handed all device
+ * memory to another owner, or code that must not trigger the implicit device
+ * synchronisation a first cudaMalloc brings.  It takes no handle, calls no
+ * cudaMalloc, cudaFree or other allocating routine, and computes exactly what
+ * gemm_run computes, with the same arguments, conventions and argument errors.
+ *
+ * Scratch: packed operand copies and split-K partial sums go to one file-scope
+ * device array of GEMM_NOALLOC_SCRATCH_BYTES, which every GPU that loads this
+ * library holds until the process exits.  A problem that needs more scratch
+ * than that (see gemm_plan_t.workspace_bytes) is rejected with
+ * GEMM_ERR_INVALID_VALUE and nothing is enqueued.  All calls on a device share
+ * the array and it keeps the last call's contents (nothing in it needs to start
+ * at zero); calls that overlap on the GPU -- on different streams, or from
+ * different host threads without ordering -- race on it, so order them on one
+ * stream.
+ *
+ * Set-up: the first call on each device (with that device current) resolves
+ * the array's device address and loads the kernels; make that first call
+ * before any stream capture.  Device-side timeouts still wind the kernel down
+ * cleanly but are not reported, since there is no handle error word.
+ * Returns NOT_SUPPORTED off sm_103 and LAUNCH if a CUDA call fails.
+ */
+gemm_status_t gemm_run_noalloc(char transA, char transB,
+                               int64_t M, int64_t N, int64_t K,
+                               float alpha, const void* A, int64_t lda,
+                               const void* B, int64_t ldb,
+                               float beta, void* C, int64_t ldc,
+                               gemm_dtypes_t dt, gemm_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

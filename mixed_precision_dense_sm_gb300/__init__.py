@@ -7,7 +7,8 @@ no fallback implementation.
 
 The entry points mirror include/gemm_sm103.h one to one:
 ``gemm_create``, ``gemm_run``, ``gemm_sync``, ``gemm_destroy``,
-``gemm_status_string``, ``gemm_check_args``, ``gemm_plan_query``.
+``gemm_status_string``, ``gemm_check_args``, ``gemm_plan_query`` and
+``gemm_run_noalloc``.
 ``Gemm`` wraps a handle and adds ``__call__`` for torch tensors.
 """
 from __future__ import annotations
@@ -61,6 +62,8 @@ def _load():
     lib.gemm_create.argtypes = [ctypes.POINTER(vp)]
     lib.gemm_run.restype = ctypes.c_int
     lib.gemm_run.argtypes = [vp] + run_args + [vp]
+    lib.gemm_run_noalloc.restype = ctypes.c_int
+    lib.gemm_run_noalloc.argtypes = run_args + [vp]
     lib.gemm_sync.restype = ctypes.c_int
     lib.gemm_sync.argtypes = [vp, vp]
     lib.gemm_destroy.restype = ctypes.c_int
@@ -109,6 +112,15 @@ def gemm_run(h, transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc,
     value.  Returns the gemm_status_t code."""
     return lib.gemm_run(h, _tr(transA), _tr(transB), M, N, K, float(alpha), A, lda, B, ldb,
                         float(beta), C, ldc, Dtypes(*dtypes), stream)
+
+
+def gemm_run_noalloc(transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc,
+                     dtypes, stream=0) -> int:
+    """Raw C-ABI call of the entry point that allocates nothing (no handle):
+    for callers that cannot call cudaMalloc.  Same arguments as gemm_run
+    without the handle; returns the gemm_status_t code."""
+    return lib.gemm_run_noalloc(_tr(transA), _tr(transB), M, N, K, float(alpha), A, lda, B, ldb,
+                                float(beta), C, ldc, Dtypes(*dtypes), stream)
 
 
 def gemm_check_args(transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, dtypes) -> int:

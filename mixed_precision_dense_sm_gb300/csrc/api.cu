@@ -487,3 +487,189 @@ gemm_status_t gemm_run(gemm_handle_t h, char transA, char transB, int64_t M, int
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// gemm_run_noalloc: the same GEMM for callers that cannot allocate device
+// memory.  Its scratch (packed operand copies and stream-K partial sums) lives
+// in the file-scope array below instead of a handle's cudaMalloc'd workspace.
+// ---------------------------------------------------------------------------
+#include <functional>
+#include <mutex>
+
+namespace {
+
+constexpr int kNoAllocMaxDevices = 64;
+
+// Scratch for gemm_run_noalloc.  Every GPU that loads this library holds it
+// until the process exits.  In host code `g_noalloc_scratch` is only a
+// stand-in symbol, never a device address: the device address comes from
+// cudaGetSymbolAddress during the per-device set-up below.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[GEMM_NOALLOC_SCRATCH_BYTES];
+
+struct NoAllocDevice {
+    std::once_flag once;
+    gemm_status_t status;      // outcome of the set-up
+    void* scratch;             // device address of g_noalloc_scratch on this device
+    int num_sms, smem_optin;
+    EncodeTiledFn encode;
+};
+NoAllocDevice g_noalloc_dev[kNoAllocMaxDevices];
+
+// Runs once per device, with that device current.
+void noalloc_setup(NoAllocDevice& d, int dev) {
+    d.status = GEMM_ERR_LAUNCH;
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
+            cudaSuccess) {
+        cudaGetLastError();
+        return;
+    }
+    if (major != 10 || minor != 3) {
+        d.status = GEMM_ERR_NOT_SUPPORTED;
+        return;
+    }
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || fn == nullptr) {
+        cudaGetLastError();
+        return;
+    }
+    d.encode = reinterpret_cast<EncodeTiledFn>(fn);
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || ptr == nullptr) {
+        cudaGetLastError();
+        return;
+    }
+    d.scratch = ptr;
+    d.status = GEMM_OK;
+}
+
+}  // namespace
+
+extern "C" gemm_status_t gemm_run_noalloc(char transA, char transB, int64_t M, int64_t N,
+                                          int64_t K, float alpha, const void* A, int64_t lda,
+                                          const void* B, int64_t ldb, float beta, void* C,
+                                          int64_t ldc, gemm_dtypes_t dt, gemm_stream_t stream_) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_LAUNCH;
+    }
+    if (dev < 0 || dev >= kNoAllocMaxDevices) return GEMM_ERR_NOT_SUPPORTED;
+    NoAllocDevice& d = g_noalloc_dev[dev];
+    std::call_once(d.once, noalloc_setup, std::ref(d), dev);
+    if (d.status != GEMM_OK) return d.status;
+
+    Plan pl;
+    gemm_status_t st = make_plan(transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, dt,
+                                 d.num_sms, d.smem_optin, pl);
+    if (st != GEMM_OK) return st;
+    if (pl.pub.workspace_bytes > static_cast<int64_t>(GEMM_NOALLOC_SCRATCH_BYTES))
+        return GEMM_ERR_INVALID_VALUE;      // needs more scratch than the static array holds
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+
+    if (pl.pub.path == GEMM_PATH_NOOP) return GEMM_OK;
+    if (pl.pub.path == GEMM_PATH_SCALE) {
+        const int grid = grid_for(M * N, d.num_sms);
+        if (dt.c == GEMM_F32)
+            scale_c_kernel<float><<<grid, 256, 0, stream>>>(static_cast<float*>(C), M, N, ldc, beta);
+        else if (dt.c == GEMM_F16)
+            scale_c_kernel<__half><<<grid, 256, 0, stream>>>(static_cast<__half*>(C), M, N, ldc, beta);
+        else
+            scale_c_kernel<__nv_bfloat16>
+                <<<grid, 256, 0, stream>>>(static_cast<__nv_bfloat16*>(C), M, N, ldc, beta);
+        return cudaGetLastError() == cudaSuccess ? GEMM_OK : GEMM_ERR_LAUNCH;
+    }
+
+    // Scratch layout (same as a handle's workspace).  Nothing in it has to
+    // start at zero: the packed copies and every partial-sum slot are fully
+    // written before they are read within this call.
+    uint8_t* ws_a = static_cast<uint8_t*>(d.scratch);
+    uint8_t* ws_b = ws_a + round_up(pl.pack_a_bytes, 256);
+    float* ws_part = reinterpret_cast<float*>(ws_b + round_up(pl.pack_b_bytes, 256));
+
+    const void* a_ptr = pl.a.ptr;
+    const void* b_ptr = pl.b.ptr;
+    if (pl.a.pack) {
+        const int grid = grid_for(pl.a.rows * pl.a.packed_ld / 8, d.num_sms);
+        pack_rows_kernel<<<grid, 256, 0, stream>>>(static_cast<const uint16_t*>(pl.a.ptr), pl.a.ld,
+                                                   pl.a.rows, pl.a.cols,
+                                                   reinterpret_cast<uint16_t*>(ws_a), pl.a.packed_ld);
+        a_ptr = ws_a;
+    }
+    if (pl.b.pack) {
+        const int grid = grid_for(pl.b.rows * pl.b.packed_ld / 8, d.num_sms);
+        pack_rows_kernel<<<grid, 256, 0, stream>>>(static_cast<const uint16_t*>(pl.b.ptr), pl.b.ld,
+                                                   pl.b.rows, pl.b.cols,
+                                                   reinterpret_cast<uint16_t*>(ws_b), pl.b.packed_ld);
+        b_ptr = ws_b;
+    }
+    if ((pl.a.pack || pl.b.pack) && cudaGetLastError() != cudaSuccess) return GEMM_ERR_LAUNCH;
+
+    gemm_ctx enc_ctx;                       // only its encoder is used; nothing allocated
+    std::memset(&enc_ctx, 0, sizeof enc_ctx);
+    enc_ctx.encode = d.encode;
+    TcLaunch l;
+    std::memset(&l, 0, sizeof l);
+    const int bn = pl.pub.block_n;
+    bool ok = encode_operand(&enc_ctx, &l.tmA, dt.a, a_ptr, pl.a.cols, pl.a.rows, pl.a.packed_ld,
+                             pl.a.mn_major ? 64u : static_cast<uint32_t>(kBlockM));
+    ok = ok && encode_operand(&enc_ctx, &l.tmB, dt.b, b_ptr, pl.b.cols, pl.b.rows, pl.b.packed_ld,
+                              pl.b.mn_major ? 64u : static_cast<uint32_t>(bn));
+    if (!ok) return GEMM_ERR_LAUNCH;
+
+    TcParams& p = l.p;
+    p.M = static_cast<int32_t>(pl.Mk);
+    p.N = static_cast<int32_t>(pl.Nk);
+    p.k_blocks = pl.k_blocks;
+    p.tiles_m = pl.tiles_m;
+    p.tiles_n = pl.tiles_n;
+    p.num_tiles = pl.pub.num_tiles;
+    p.group_m = kGroupM;
+    p.stages = pl.pub.stages;
+    p.a_mn_major = pl.a.mn_major ? 1 : 0;
+    p.b_mn_major = pl.b.mn_major ? 1 : 0;
+    p.idesc = instr_desc_f16(dt.a == GEMM_BF16, pl.a.mn_major, pl.b.mn_major, kBlockM,
+                             static_cast<uint32_t>(bn));
+    p.stream_k = pl.sk_len > 0 ? 1 : 0;
+    p.sk_len = pl.sk_len;
+    p.sk_max_seg = pl.sk_max_seg;
+    p.alpha = alpha;
+    p.beta = beta;
+    p.C = C;
+    p.c_rs = pl.c_rs;
+    p.c_cs = pl.c_cs;
+    p.c_vector = pl.pub.c_vector;
+    p.partials = pl.partial_bytes > 0 ? ws_part : nullptr;
+    p.err = nullptr;                        // no host-visible error word without an allocation
+    l.grid = pl.pub.grid;
+    l.block_n = bn;
+    l.smem_bytes = pl.smem_bytes;
+    l.stream = stream;
+
+    cudaError_t e;
+    if (dt.c == GEMM_F32) e = launch_tc_f32(l);
+    else if (dt.c == GEMM_F16) e = launch_tc_f16(l);
+    else e = launch_tc_bf16(l);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_LAUNCH;
+    }
+    if (p.stream_k) {
+        const int grid = grid_for(static_cast<int64_t>(p.num_tiles) * kBlockM * (bn / 4),
+                                  d.num_sms);
+        if (dt.c == GEMM_F32) e = launch_fixup_f32(l, grid);
+        else if (dt.c == GEMM_F16) e = launch_fixup_f16(l, grid);
+        else e = launch_fixup_bf16(l, grid);
+        if (e != cudaSuccess) {
+            cudaGetLastError();
+            return GEMM_ERR_LAUNCH;
+        }
+    }
+    return GEMM_OK;
+}
