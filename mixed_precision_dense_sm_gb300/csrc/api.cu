@@ -45,6 +45,7 @@ struct Plan {
     int64_t K;
     int64_t c_rs, c_cs;
     int32_t k_blocks, tiles_m, tiles_n;
+    int32_t cta_group;
     int32_t sk_len, sk_max_seg;
     int64_t pack_a_bytes, pack_b_bytes, partial_bytes;
     size_t smem_bytes;
@@ -143,30 +144,36 @@ gemm_status_t make_plan(char transA, char transB, int64_t M, int64_t N, int64_t 
     pl.pack_b_bytes = pl.b.pack ? pl.b.rows * pl.b.packed_ld * 2 : 0;
     pl.pub.c_vector = (!swap && aligned16(C) && (ldc * (int64_t)out_elem_bytes(dt.c)) % 16 == 0) ? 1 : 0;
 
-    // Tile width: 256 columns when the output has enough tiles to fill the GPU,
-    // otherwise narrower tiles (and stream-K over K) for more parallelism.
+    // Tile shape.  Enough 256 x 256 tiles to give every SM pair one: CTA-pair
+    // tiles (tcgen05 cta_group::2).  Otherwise single-CTA 128-row tiles, 256
+    // columns wide when that still fills the GPU, else narrower ones with
+    // stream-K over K for more parallelism.
     pl.k_blocks = static_cast<int32_t>(ceil_div(K, kBlockK));
-    const int64_t tiles_m = ceil_div(pl.Mk, kBlockM);
+    const int64_t pair_tiles = ceil_div(pl.Mk, 2 * kBlockM) * ceil_div(pl.Nk, 256);
+    const bool pairs = !swap && pl.Mk >= 2 * kBlockM && pl.Nk >= 256 && num_sms >= 2 &&
+                       pair_tiles >= num_sms / 2;
+    const int cg = pairs ? 2 : 1;
+    const int64_t block_m = static_cast<int64_t>(kBlockM) * cg;
+    const int64_t tiles_m = ceil_div(pl.Mk, block_m);
     int bn;
-    if (pl.Nk <= 64) {
-        bn = 64;
-    } else if (tiles_m * ceil_div(pl.Nk, 256) >= num_sms) {
+    if (pairs || (pl.Nk > 128 && tiles_m * ceil_div(pl.Nk, 256) >= num_sms)) {
         bn = 256;
-    } else if (pl.Nk <= 128 || tiles_m * ceil_div(pl.Nk, 128) >= num_sms) {
-        bn = 128;
+    } else if (pl.Nk <= 64) {
+        bn = 64;
     } else {
         bn = 128;
     }
     const int64_t tiles_n = ceil_div(pl.Nk, bn);
     const int64_t tiles = tiles_m * tiles_n;
+    pl.cta_group = cg;
     pl.tiles_m = static_cast<int32_t>(tiles_m);
     pl.tiles_n = static_cast<int32_t>(tiles_n);
-    pl.pub.block_m = kBlockM;
+    pl.pub.block_m = static_cast<int32_t>(block_m);
     pl.pub.block_n = bn;
     pl.pub.block_k = kBlockK;
     pl.pub.num_tiles = static_cast<int32_t>(tiles);
 
-    const uint32_t stage_bytes = kATileBytes + static_cast<uint32_t>(bn) * kBlockK * 2;
+    const uint32_t stage_bytes = kATileBytes + static_cast<uint32_t>(bn / cg) * kBlockK * 2;
     const int64_t barrier_bytes = 256;
     int64_t stages = (smem_optin - 1024 - barrier_bytes) / stage_bytes;
     if (stages > kMaxStages) stages = kMaxStages;
@@ -175,7 +182,7 @@ gemm_status_t make_plan(char transA, char transB, int64_t M, int64_t N, int64_t 
     pl.smem_bytes = static_cast<size_t>(stages * stage_bytes + 1024 + barrier_bytes);
 
     const int64_t work = tiles * pl.k_blocks;
-    const bool stream_k = (tiles < num_sms) && (pl.k_blocks >= 4) && (work < INT32_MAX);
+    const bool stream_k = !pairs && (tiles < num_sms) && (pl.k_blocks >= 4) && (work < INT32_MAX);
     if (stream_k) {
         int64_t G = num_sms < work ? num_sms : work;
         const int64_t L = ceil_div(work, G);
@@ -185,11 +192,11 @@ gemm_status_t make_plan(char transA, char transB, int64_t M, int64_t N, int64_t 
         pl.pub.grid = static_cast<int32_t>(G);
         pl.pub.split_k = static_cast<int32_t>(ceil_div(pl.k_blocks, L));
         pl.partial_bytes = G * pl.sk_max_seg * (int64_t)kBlockM * bn * 4;
-        pl.pub.path = swap ? GEMM_PATH_SKINNY : GEMM_PATH_TILED_1SM;
     } else {
-        pl.pub.grid = static_cast<int32_t>(tiles < num_sms ? tiles : num_sms);
-        pl.pub.path = swap ? GEMM_PATH_SKINNY : GEMM_PATH_TILED_1SM;
+        const int64_t units = num_sms / cg;
+        pl.pub.grid = static_cast<int32_t>(cg * (tiles < units ? tiles : units));
     }
+    pl.pub.path = swap ? GEMM_PATH_SKINNY : (pairs ? GEMM_PATH_TILED_2SM : GEMM_PATH_TILED_1SM);
     pl.pub.sk_len = pl.sk_len;
     pl.pub.sk_max_seg = pl.sk_max_seg;
     pl.pub.k_blocks = pl.k_blocks;
@@ -222,13 +229,13 @@ namespace {
 
 // 2-D tiled map over a stored 16-bit matrix: dims {inner, outer}, row pitch in
 // bytes, a 64 x box_outer box, 128-byte swizzle, zero fill out of range.
-bool encode_operand(gemm_ctx* h, CUtensorMap* map, int32_t dtype, const void* ptr, int64_t inner,
-                    int64_t outer, int64_t ld, uint32_t box_outer) {
+bool encode_operand(EncodeTiledFn encode, CUtensorMap* map, int32_t dtype, const void* ptr,
+                    int64_t inner, int64_t outer, int64_t ld, uint32_t box_outer) {
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(outer)};
     const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2};
     const cuuint32_t box[2] = {static_cast<cuuint32_t>(kBlockK), box_outer};
     const cuuint32_t estr[2] = {1, 1};
-    CUresult r = h->encode(map,
+    CUresult r = encode(map,
                            dtype == GEMM_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
                                               : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
                            2, const_cast<void*>(ptr), dims, strides, box, estr,
@@ -269,6 +276,110 @@ int grid_for(int64_t elems_per_thread_unit, int num_sms) {
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
     return static_cast<int>(blocks);
+}
+
+
+// Everything gemm_run enqueues after planning: the optional pack pre-passes,
+// the TMA descriptors, the GEMM kernel and the stream-K fixup.  `ws` is the
+// workspace laid out as [packed A][packed B][partial slots].
+gemm_status_t enqueue_plan(const Plan& pl, EncodeTiledFn encode, int num_sms, uint8_t* ws,
+                           int* err_dev, float alpha, float beta, void* C, gemm_dtypes_t dt,
+                           cudaStream_t stream) {
+    uint8_t* ws_a = ws;
+    uint8_t* ws_b = ws_a + round_up(pl.pack_a_bytes, 256);
+    float* ws_part = reinterpret_cast<float*>(ws_b + round_up(pl.pack_b_bytes, 256));
+
+    // Pack operands whose rows TMA cannot address (pitch or base not 16-byte aligned).
+    const void* a_ptr = pl.a.ptr;
+    const void* b_ptr = pl.b.ptr;
+    if (pl.a.pack) {
+        const int grid = grid_for(pl.a.rows * pl.a.packed_ld / 8, num_sms);
+        pack_rows_kernel<<<grid, 256, 0, stream>>>(static_cast<const uint16_t*>(pl.a.ptr), pl.a.ld,
+                                                   pl.a.rows, pl.a.cols,
+                                                   reinterpret_cast<uint16_t*>(ws_a), pl.a.packed_ld);
+        a_ptr = ws_a;
+    }
+    if (pl.b.pack) {
+        const int grid = grid_for(pl.b.rows * pl.b.packed_ld / 8, num_sms);
+        pack_rows_kernel<<<grid, 256, 0, stream>>>(static_cast<const uint16_t*>(pl.b.ptr), pl.b.ld,
+                                                   pl.b.rows, pl.b.cols,
+                                                   reinterpret_cast<uint16_t*>(ws_b), pl.b.packed_ld);
+        b_ptr = ws_b;
+    }
+    if ((pl.a.pack || pl.b.pack) && cudaGetLastError() != cudaSuccess) return GEMM_ERR_LAUNCH;
+
+    TcLaunch l;
+    std::memset(&l, 0, sizeof l);
+    const int bn = pl.pub.block_n;
+    const int cg = pl.cta_group;
+    bool ok = encode_operand(encode, &l.tmA, dt.a, a_ptr, pl.a.cols, pl.a.rows, pl.a.packed_ld,
+                             pl.a.mn_major ? 64u : static_cast<uint32_t>(kBlockM));
+    ok = ok && encode_operand(encode, &l.tmB, dt.b, b_ptr, pl.b.cols, pl.b.rows, pl.b.packed_ld,
+                              pl.b.mn_major ? 64u : static_cast<uint32_t>(bn / cg));
+    if (!ok) return GEMM_ERR_LAUNCH;
+
+    TcParams& p = l.p;
+    p.M = static_cast<int32_t>(pl.Mk);
+    p.N = static_cast<int32_t>(pl.Nk);
+    p.k_blocks = pl.k_blocks;
+    p.tiles_m = pl.tiles_m;
+    p.tiles_n = pl.tiles_n;
+    p.num_tiles = pl.pub.num_tiles;
+    p.group_m = kGroupM;
+    p.stages = pl.pub.stages;
+    p.a_mn_major = pl.a.mn_major ? 1 : 0;
+    p.b_mn_major = pl.b.mn_major ? 1 : 0;
+    p.idesc = instr_desc_f16(dt.a == GEMM_BF16, pl.a.mn_major, pl.b.mn_major,
+                             static_cast<uint32_t>(kBlockM * cg), static_cast<uint32_t>(bn));
+    p.stream_k = pl.sk_len > 0 ? 1 : 0;
+    p.sk_len = pl.sk_len;
+    p.sk_max_seg = pl.sk_max_seg;
+    p.alpha = alpha;
+    p.beta = beta;
+    p.C = C;
+    p.c_rs = pl.c_rs;
+    p.c_cs = pl.c_cs;
+    p.c_vector = pl.pub.c_vector;
+    p.partials = pl.partial_bytes > 0 ? ws_part : nullptr;
+    p.err = err_dev;
+    l.grid = pl.pub.grid;
+    l.cta_group = cg;
+    l.block_n = bn;
+    l.smem_bytes = pl.smem_bytes;
+    l.stream = stream;
+
+    cudaError_t e;
+    if (dt.c == GEMM_F32) e = launch_tc_f32(l);
+    else if (dt.c == GEMM_F16) e = launch_tc_f16(l);
+    else e = launch_tc_bf16(l);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_LAUNCH;
+    }
+    if (p.stream_k) {
+        const int grid = grid_for(static_cast<int64_t>(p.num_tiles) * kBlockM * (bn / 4), num_sms);
+        if (dt.c == GEMM_F32) e = launch_fixup_f32(l, grid);
+        else if (dt.c == GEMM_F16) e = launch_fixup_f16(l, grid);
+        else e = launch_fixup_bf16(l, grid);
+        if (e != cudaSuccess) {
+            cudaGetLastError();
+            return GEMM_ERR_LAUNCH;
+        }
+    }
+    return GEMM_OK;
+}
+
+gemm_status_t enqueue_scale(int64_t M, int64_t N, void* C, int64_t ldc, float beta,
+                            gemm_dtypes_t dt, int num_sms, cudaStream_t stream) {
+    const int grid = grid_for(M * N, num_sms);
+    if (dt.c == GEMM_F32)
+        scale_c_kernel<float><<<grid, 256, 0, stream>>>(static_cast<float*>(C), M, N, ldc, beta);
+    else if (dt.c == GEMM_F16)
+        scale_c_kernel<__half><<<grid, 256, 0, stream>>>(static_cast<__half*>(C), M, N, ldc, beta);
+    else
+        scale_c_kernel<__nv_bfloat16>
+            <<<grid, 256, 0, stream>>>(static_cast<__nv_bfloat16*>(C), M, N, ldc, beta);
+    return cudaGetLastError() == cudaSuccess ? GEMM_OK : GEMM_ERR_LAUNCH;
 }
 
 }  // namespace
@@ -388,102 +499,12 @@ gemm_status_t gemm_run(gemm_handle_t h, char transA, char transB, int64_t M, int
     cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
 
     if (pl.pub.path == GEMM_PATH_NOOP) return GEMM_OK;
-    if (pl.pub.path == GEMM_PATH_SCALE) {
-        const int grid = grid_for(M * N, h->num_sms);
-        if (dt.c == GEMM_F32)
-            scale_c_kernel<float><<<grid, 256, 0, stream>>>(static_cast<float*>(C), M, N, ldc, beta);
-        else if (dt.c == GEMM_F16)
-            scale_c_kernel<__half><<<grid, 256, 0, stream>>>(static_cast<__half*>(C), M, N, ldc, beta);
-        else
-            scale_c_kernel<__nv_bfloat16>
-                <<<grid, 256, 0, stream>>>(static_cast<__nv_bfloat16*>(C), M, N, ldc, beta);
-        return cudaGetLastError() == cudaSuccess ? GEMM_OK : GEMM_ERR_LAUNCH;
-    }
-
+    if (pl.pub.path == GEMM_PATH_SCALE)
+        return enqueue_scale(M, N, C, ldc, beta, dt, h->num_sms, stream);
     st = ensure_workspace(h, static_cast<size_t>(pl.pub.workspace_bytes));
     if (st != GEMM_OK) return st;
-    uint8_t* ws = static_cast<uint8_t*>(h->ws);
-    uint8_t* ws_a = ws;
-    uint8_t* ws_b = ws_a + round_up(pl.pack_a_bytes, 256);
-    float* ws_part = reinterpret_cast<float*>(ws_b + round_up(pl.pack_b_bytes, 256));
-
-    // Pack operands whose rows TMA cannot address (pitch or base not 16-byte aligned).
-    const void* a_ptr = pl.a.ptr;
-    const void* b_ptr = pl.b.ptr;
-    if (pl.a.pack) {
-        const int grid = grid_for(pl.a.rows * pl.a.packed_ld / 8, h->num_sms);
-        pack_rows_kernel<<<grid, 256, 0, stream>>>(static_cast<const uint16_t*>(pl.a.ptr), pl.a.ld,
-                                                   pl.a.rows, pl.a.cols,
-                                                   reinterpret_cast<uint16_t*>(ws_a), pl.a.packed_ld);
-        a_ptr = ws_a;
-    }
-    if (pl.b.pack) {
-        const int grid = grid_for(pl.b.rows * pl.b.packed_ld / 8, h->num_sms);
-        pack_rows_kernel<<<grid, 256, 0, stream>>>(static_cast<const uint16_t*>(pl.b.ptr), pl.b.ld,
-                                                   pl.b.rows, pl.b.cols,
-                                                   reinterpret_cast<uint16_t*>(ws_b), pl.b.packed_ld);
-        b_ptr = ws_b;
-    }
-    if ((pl.a.pack || pl.b.pack) && cudaGetLastError() != cudaSuccess) return GEMM_ERR_LAUNCH;
-
-    TcLaunch l;
-    std::memset(&l, 0, sizeof l);
-    const int bn = pl.pub.block_n;
-    bool ok = encode_operand(h, &l.tmA, dt.a, a_ptr, pl.a.cols, pl.a.rows, pl.a.packed_ld,
-                             pl.a.mn_major ? 64u : static_cast<uint32_t>(kBlockM));
-    ok = ok && encode_operand(h, &l.tmB, dt.b, b_ptr, pl.b.cols, pl.b.rows, pl.b.packed_ld,
-                              pl.b.mn_major ? 64u : static_cast<uint32_t>(bn));
-    if (!ok) return GEMM_ERR_LAUNCH;
-
-    TcParams& p = l.p;
-    p.M = static_cast<int32_t>(pl.Mk);
-    p.N = static_cast<int32_t>(pl.Nk);
-    p.k_blocks = pl.k_blocks;
-    p.tiles_m = pl.tiles_m;
-    p.tiles_n = pl.tiles_n;
-    p.num_tiles = pl.pub.num_tiles;
-    p.group_m = kGroupM;
-    p.stages = pl.pub.stages;
-    p.a_mn_major = pl.a.mn_major ? 1 : 0;
-    p.b_mn_major = pl.b.mn_major ? 1 : 0;
-    p.idesc = instr_desc_f16(dt.a == GEMM_BF16, pl.a.mn_major, pl.b.mn_major, kBlockM,
-                             static_cast<uint32_t>(bn));
-    p.stream_k = pl.sk_len > 0 ? 1 : 0;
-    p.sk_len = pl.sk_len;
-    p.sk_max_seg = pl.sk_max_seg;
-    p.alpha = alpha;
-    p.beta = beta;
-    p.C = C;
-    p.c_rs = pl.c_rs;
-    p.c_cs = pl.c_cs;
-    p.c_vector = pl.pub.c_vector;
-    p.partials = pl.partial_bytes > 0 ? ws_part : nullptr;
-    p.err = h->err_dev;
-    l.grid = pl.pub.grid;
-    l.block_n = bn;
-    l.smem_bytes = pl.smem_bytes;
-    l.stream = stream;
-
-    cudaError_t e;
-    if (dt.c == GEMM_F32) e = launch_tc_f32(l);
-    else if (dt.c == GEMM_F16) e = launch_tc_f16(l);
-    else e = launch_tc_bf16(l);
-    if (e != cudaSuccess) {
-        cudaGetLastError();
-        return GEMM_ERR_LAUNCH;
-    }
-    if (p.stream_k) {
-        const int grid = grid_for(static_cast<int64_t>(p.num_tiles) * kBlockM * (bn / 4),
-                                  h->num_sms);
-        if (dt.c == GEMM_F32) e = launch_fixup_f32(l, grid);
-        else if (dt.c == GEMM_F16) e = launch_fixup_f16(l, grid);
-        else e = launch_fixup_bf16(l, grid);
-        if (e != cudaSuccess) {
-            cudaGetLastError();
-            return GEMM_ERR_LAUNCH;
-        }
-    }
-    return GEMM_OK;
+    return enqueue_plan(pl, h->encode, h->num_sms, static_cast<uint8_t*>(h->ws), h->err_dev, alpha,
+                        beta, C, dt, stream);
 }
 
 }  // extern "C"
@@ -574,102 +595,12 @@ extern "C" gemm_status_t gemm_run_noalloc(char transA, char transB, int64_t M, i
     cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
 
     if (pl.pub.path == GEMM_PATH_NOOP) return GEMM_OK;
-    if (pl.pub.path == GEMM_PATH_SCALE) {
-        const int grid = grid_for(M * N, d.num_sms);
-        if (dt.c == GEMM_F32)
-            scale_c_kernel<float><<<grid, 256, 0, stream>>>(static_cast<float*>(C), M, N, ldc, beta);
-        else if (dt.c == GEMM_F16)
-            scale_c_kernel<__half><<<grid, 256, 0, stream>>>(static_cast<__half*>(C), M, N, ldc, beta);
-        else
-            scale_c_kernel<__nv_bfloat16>
-                <<<grid, 256, 0, stream>>>(static_cast<__nv_bfloat16*>(C), M, N, ldc, beta);
-        return cudaGetLastError() == cudaSuccess ? GEMM_OK : GEMM_ERR_LAUNCH;
-    }
-
-    // Scratch layout (same as a handle's workspace).  Nothing in it has to
-    // start at zero: the packed copies and every partial-sum slot are fully
-    // written before they are read within this call.
-    uint8_t* ws_a = static_cast<uint8_t*>(d.scratch);
-    uint8_t* ws_b = ws_a + round_up(pl.pack_a_bytes, 256);
-    float* ws_part = reinterpret_cast<float*>(ws_b + round_up(pl.pack_b_bytes, 256));
-
-    const void* a_ptr = pl.a.ptr;
-    const void* b_ptr = pl.b.ptr;
-    if (pl.a.pack) {
-        const int grid = grid_for(pl.a.rows * pl.a.packed_ld / 8, d.num_sms);
-        pack_rows_kernel<<<grid, 256, 0, stream>>>(static_cast<const uint16_t*>(pl.a.ptr), pl.a.ld,
-                                                   pl.a.rows, pl.a.cols,
-                                                   reinterpret_cast<uint16_t*>(ws_a), pl.a.packed_ld);
-        a_ptr = ws_a;
-    }
-    if (pl.b.pack) {
-        const int grid = grid_for(pl.b.rows * pl.b.packed_ld / 8, d.num_sms);
-        pack_rows_kernel<<<grid, 256, 0, stream>>>(static_cast<const uint16_t*>(pl.b.ptr), pl.b.ld,
-                                                   pl.b.rows, pl.b.cols,
-                                                   reinterpret_cast<uint16_t*>(ws_b), pl.b.packed_ld);
-        b_ptr = ws_b;
-    }
-    if ((pl.a.pack || pl.b.pack) && cudaGetLastError() != cudaSuccess) return GEMM_ERR_LAUNCH;
-
-    gemm_ctx enc_ctx;                       // only its encoder is used; nothing allocated
-    std::memset(&enc_ctx, 0, sizeof enc_ctx);
-    enc_ctx.encode = d.encode;
-    TcLaunch l;
-    std::memset(&l, 0, sizeof l);
-    const int bn = pl.pub.block_n;
-    bool ok = encode_operand(&enc_ctx, &l.tmA, dt.a, a_ptr, pl.a.cols, pl.a.rows, pl.a.packed_ld,
-                             pl.a.mn_major ? 64u : static_cast<uint32_t>(kBlockM));
-    ok = ok && encode_operand(&enc_ctx, &l.tmB, dt.b, b_ptr, pl.b.cols, pl.b.rows, pl.b.packed_ld,
-                              pl.b.mn_major ? 64u : static_cast<uint32_t>(bn));
-    if (!ok) return GEMM_ERR_LAUNCH;
-
-    TcParams& p = l.p;
-    p.M = static_cast<int32_t>(pl.Mk);
-    p.N = static_cast<int32_t>(pl.Nk);
-    p.k_blocks = pl.k_blocks;
-    p.tiles_m = pl.tiles_m;
-    p.tiles_n = pl.tiles_n;
-    p.num_tiles = pl.pub.num_tiles;
-    p.group_m = kGroupM;
-    p.stages = pl.pub.stages;
-    p.a_mn_major = pl.a.mn_major ? 1 : 0;
-    p.b_mn_major = pl.b.mn_major ? 1 : 0;
-    p.idesc = instr_desc_f16(dt.a == GEMM_BF16, pl.a.mn_major, pl.b.mn_major, kBlockM,
-                             static_cast<uint32_t>(bn));
-    p.stream_k = pl.sk_len > 0 ? 1 : 0;
-    p.sk_len = pl.sk_len;
-    p.sk_max_seg = pl.sk_max_seg;
-    p.alpha = alpha;
-    p.beta = beta;
-    p.C = C;
-    p.c_rs = pl.c_rs;
-    p.c_cs = pl.c_cs;
-    p.c_vector = pl.pub.c_vector;
-    p.partials = pl.partial_bytes > 0 ? ws_part : nullptr;
-    p.err = nullptr;                        // no host-visible error word without an allocation
-    l.grid = pl.pub.grid;
-    l.block_n = bn;
-    l.smem_bytes = pl.smem_bytes;
-    l.stream = stream;
-
-    cudaError_t e;
-    if (dt.c == GEMM_F32) e = launch_tc_f32(l);
-    else if (dt.c == GEMM_F16) e = launch_tc_f16(l);
-    else e = launch_tc_bf16(l);
-    if (e != cudaSuccess) {
-        cudaGetLastError();
-        return GEMM_ERR_LAUNCH;
-    }
-    if (p.stream_k) {
-        const int grid = grid_for(static_cast<int64_t>(p.num_tiles) * kBlockM * (bn / 4),
-                                  d.num_sms);
-        if (dt.c == GEMM_F32) e = launch_fixup_f32(l, grid);
-        else if (dt.c == GEMM_F16) e = launch_fixup_f16(l, grid);
-        else e = launch_fixup_bf16(l, grid);
-        if (e != cudaSuccess) {
-            cudaGetLastError();
-            return GEMM_ERR_LAUNCH;
-        }
-    }
-    return GEMM_OK;
+    if (pl.pub.path == GEMM_PATH_SCALE)
+        return enqueue_scale(M, N, C, ldc, beta, dt, d.num_sms, stream);
+    // The scratch takes the place of a handle's workspace.  Nothing in it has
+    // to start at zero: the packed copies and every partial-sum slot are fully
+    // written before they are read within this call.  No host-visible error
+    // word exists without an allocation, so device timeouts are not reported.
+    return enqueue_plan(pl, d.encode, d.num_sms, static_cast<uint8_t*>(d.scratch), nullptr, alpha,
+                        beta, C, dt, stream);
 }

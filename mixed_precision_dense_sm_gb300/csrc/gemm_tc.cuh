@@ -35,6 +35,10 @@
 //    FP32 sums to a workspace slot, and a separate fixup kernel adds a tile's
 //    slots in increasing CTA order (deterministic) and applies the epilogue.
 //
+// CTA pairs.  For large problems two CTAs of a cluster share one 256 x BN
+// tile through tcgen05's cta_group::2 form (see gemm_tc_kernel below): each SM
+// reads half of B, which halves the B traffic and shared-memory reads per SM.
+//
 // Swap-A/B.  For small M the host passes A' = op(B)^T and B' = op(A)^T, so the
 // kernel computes D' = C^T and the epilogue stores D'(i, j) at C[j][i]
 // (c_rs = 1, c_cs = ldc).  The kernel itself only sees "rows" M' and "columns"
@@ -210,14 +214,48 @@ __device__ __forceinline__ void store_row32_vec(OutT* dst, const float (&v)[32],
     }
 }
 
-template <int BN, typename OutT>
+// Wait on a barrier that receives plain arrivals from the peer CTA (the odd
+// CTA's epilogue releasing the accumulator): cluster-scope acquire, so the
+// peer's TMEM reads are ordered before the MMAs that overwrite them.  Barriers
+// completed by TMA transactions or tcgen05.commit are waited on at CTA scope.
+template <int CG>
+__device__ __forceinline__ bool wait_role(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
+    if constexpr (CG == 1) {
+        return wait_or_abort(bar, parity, abort_flag);
+    } else {
+        const uint32_t a = smem_addr(bar);
+        if (mbar_try_wait_cluster(a, parity)) return true;
+        const uint64_t t0 = global_timer_ns();
+        for (uint32_t i = 1;; ++i) {
+            if (mbar_try_wait_cluster(a, parity)) return true;
+            if ((i & 63u) == 0) {
+                if (*abort_flag) return false;
+                if (global_timer_ns() - t0 > kWaitTimeoutNs) return false;
+            }
+        }
+    }
+}
+
+// CG = 1: one CTA per 128 x BN tile (tcgen05 cta_group::1, M = 128).
+// CG = 2: a cluster of two CTAs per 256 x BN tile (cta_group::2, M = 256).
+//   Each CTA loads its own 128 rows of A and BN/2 rows of B; both CTAs'
+//   loads count their bytes on the even CTA's "full" barrier, which the even
+//   CTA alone arms with the pair's total (no cluster-scope arrive, and so no
+//   memory barrier, on the per-k-block path); the even CTA
+//   alone issues the MMAs, whose commits arrive on the "empty" / "acc_full"
+//   barriers of both CTAs; both CTAs drain their own TMEM half (128 rows x BN)
+//   and release the accumulator on the even CTA's "acc_empty" barrier.
+template <int CG, int BN, typename OutT>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ TcParams p) {
     static_assert(BN == 64 || BN == 128 || BN == 256, "BN");
-    constexpr uint32_t kBTileBytes = BN * kBlockK * 2;
+    static_assert(CG == 1 || (CG == 2 && BN >= 128), "CG");
+    constexpr int BM = kBlockM * CG;                      // rows per (pair) tile
+    constexpr uint32_t kBRows = BN / CG;                  // B rows this CTA loads
+    constexpr uint32_t kBTileBytes = kBRows * kBlockK * 2;
     constexpr uint32_t kStageBytes = kATileBytes + kBTileBytes;
-    constexpr uint32_t kTmemCols = 2 * BN;         // double-buffered accumulator
+    constexpr uint32_t kTmemCols = 2 * BN;               // double-buffered accumulator
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -233,16 +271,19 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    const uint32_t rank = (CG == 2) ? cluster_ctarank() : 0u;
+    const int32_t unit = blockIdx.x / CG;                 // CTA (pair) index
+    const int32_t units = gridDim.x / CG;
 
     if (threadIdx.x == 0) {
         abort_flag = 0;
         for (int s = 0; s < S; ++s) {
-            mbar_init(&full[s], 1);
+            mbar_init(&full[s], 1);                      // the even CTA's producer arms it
             mbar_init(&empty[s], 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&acc_full[b], 1);
-            mbar_init(&acc_empty[b], kEpiWarps);
+            mbar_init(&acc_empty[b], kEpiWarps * CG);
         }
         mbar_init(drain, 1);
         fence_barrier_init();
@@ -250,11 +291,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_prefetch_desc(&tmB);
     }
     if (warp == 1) {
-        tmem_alloc(tmem_slot, kTmemCols);
-        tmem_relinquish();
+        if constexpr (CG == 1) {
+            tmem_alloc(tmem_slot, kTmemCols);
+            tmem_relinquish();
+        } else {
+            tmem_alloc_pair(tmem_slot, kTmemCols);
+            tmem_relinquish_pair();
+        }
     }
     tc_fence_before_sync();
     __syncthreads();
+    if constexpr (CG == 2) cluster_sync_all();            // peer barriers initialised
     tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_slot;
 
@@ -264,13 +311,43 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t policy = l2_policy_evict_last();
             uint32_t stage = 0, phase = 0;
             uint32_t armed = 0;                   // number of slot armings so far
-            SegmentIter it(p, blockIdx.x, gridDim.x);
+            SegmentIter it(p, unit, units);
             Segment sg;
             bool ok = true;
             while (ok && it.next(p, sg)) {
                 int32_t tm, tn;
                 tile_coords(p, sg.tile, tm, tn);
-                const int32_t m0 = tm * kBlockM, n0 = tn * BN;
+                // Parts of a CTA's A / B tiles that lie wholly outside the
+                // matrix only feed outputs that are never stored: not loaded.
+                // tile_bytes(r) is what CTA r of the pair loads per k-block.
+                auto a_parts = [&](int32_t m_first) {
+                    if (!p.a_mn_major) return (m_first < p.M) ? 1 : 0;
+                    int n = 0;
+                    for (int c = 0; c < kBlockM / 64; ++c) n += (m_first + 64 * c < p.M);
+                    return n;
+                };
+                auto b_parts = [&](int32_t n_first) {
+                    if (!p.b_mn_major) return (n_first < p.N) ? 1 : 0;
+                    int n = 0;
+                    for (int c = 0; c < static_cast<int>(kBRows) / 64; ++c) n += (n_first + 64 * c < p.N);
+                    return n;
+                };
+                auto tile_bytes = [&](uint32_t r) {
+                    const int32_t mf = tm * BM + static_cast<int32_t>(r) * kBlockM;
+                    const int32_t nf = tn * BN + static_cast<int32_t>(r * kBRows);
+                    return static_cast<uint32_t>(a_parts(mf)) *
+                               (p.a_mn_major ? kChunkBytes : kATileBytes) +
+                           static_cast<uint32_t>(b_parts(nf)) *
+                               (p.b_mn_major ? kChunkBytes : kBTileBytes);
+                };
+                const int32_t m0 = tm * BM + static_cast<int32_t>(rank) * kBlockM;
+                const int32_t n0 = tn * BN + static_cast<int32_t>(rank * kBRows);
+                const int na = a_parts(m0), nb = b_parts(n0);
+                // The even CTA's "full" barrier counts the bytes of both CTAs;
+                // the odd CTA's loads may land before it is armed (the
+                // transaction count may go transiently negative).
+                const uint32_t bytes = (CG == 1) ? tile_bytes(0)
+                                                 : (rank == 0 ? tile_bytes(0) + tile_bytes(1) : 0u);
                 for (int32_t kb = sg.kb0; kb < sg.kb1; ++kb) {
                     if (!wait_or_abort(&empty[stage], phase ^ 1u, &abort_flag)) {
                         record_error(p, kErrTimeoutProducer, &abort_flag);
@@ -280,38 +357,39 @@ __global__ void __launch_bounds__(kThreads, 1)
                     uint8_t* sa = smem + stage * kStageBytes;
                     uint8_t* sb = sa + kATileBytes;
                     const int32_t k0 = kb * kBlockK;
-                    // bytes this slot will receive (fully out-of-range 64-wide
-                    // MN chunks are skipped: they only feed unstored outputs)
-                    uint32_t bytes = 0;
-                    int na = 1, nb = 1;
-                    if (p.a_mn_major) {
-                        na = 0;
-                        for (int c = 0; c < kBlockM / 64; ++c) na += (m0 + 64 * c < p.M);
-                        bytes += na * kChunkBytes;
+                    if constexpr (CG == 1) {
+                        mbar_arrive_expect_tx(&full[stage], bytes);
+                        if (p.a_mn_major) {
+                            for (int c = 0; c < na; ++c)
+                                tma_load_2d(sa + c * kChunkBytes, &tmA, &full[stage], m0 + 64 * c,
+                                            k0, policy);
+                        } else if (na) {
+                            tma_load_2d(sa, &tmA, &full[stage], k0, m0, policy);
+                        }
+                        if (p.b_mn_major) {
+                            for (int c = 0; c < nb; ++c)
+                                tma_load_2d(sb + c * kChunkBytes, &tmB, &full[stage], n0 + 64 * c,
+                                            k0, policy);
+                        } else if (nb) {
+                            tma_load_2d(sb, &tmB, &full[stage], k0, n0, policy);
+                        }
                     } else {
-                        bytes += kATileBytes;
-                    }
-                    if (p.b_mn_major) {
-                        nb = 0;
-                        for (int c = 0; c < BN / 64; ++c) nb += (n0 + 64 * c < p.N);
-                        bytes += nb * kChunkBytes;
-                    } else {
-                        bytes += kBTileBytes;
-                    }
-                    mbar_arrive_expect_tx(&full[stage], bytes);
-                    if (p.a_mn_major) {
-                        for (int c = 0; c < na; ++c)
-                            tma_load_2d(sa + c * kChunkBytes, &tmA, &full[stage], m0 + 64 * c, k0,
-                                        policy);
-                    } else {
-                        tma_load_2d(sa, &tmA, &full[stage], k0, m0, policy);
-                    }
-                    if (p.b_mn_major) {
-                        for (int c = 0; c < nb; ++c)
-                            tma_load_2d(sb + c * kChunkBytes, &tmB, &full[stage], n0 + 64 * c, k0,
-                                        policy);
-                    } else {
-                        tma_load_2d(sb, &tmB, &full[stage], k0, n0, policy);
+                        const uint32_t fb = map_to_rank(smem_addr(&full[stage]), 0);
+                        if (rank == 0) mbar_arrive_expect_tx(&full[stage], bytes);
+                        if (p.a_mn_major) {
+                            for (int c = 0; c < na; ++c)
+                                tma_load_2d_pair(sa + c * kChunkBytes, &tmA, fb, m0 + 64 * c, k0,
+                                                 policy);
+                        } else if (na) {
+                            tma_load_2d_pair(sa, &tmA, fb, k0, m0, policy);
+                        }
+                        if (p.b_mn_major) {
+                            for (int c = 0; c < nb; ++c)
+                                tma_load_2d_pair(sb + c * kChunkBytes, &tmB, fb, n0 + 64 * c, k0,
+                                                 policy);
+                        } else if (nb) {
+                            tma_load_2d_pair(sb, &tmB, fb, k0, n0, policy);
+                        }
                     }
                     ++armed;
                     if (++stage == static_cast<uint32_t>(S)) {
@@ -320,22 +398,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             }
-            // Wind-down: wait (bounded) until every TMA load this thread issued
-            // has landed, so no copy is in flight when the CTA exits.
-            for (int s = 0; s < S; ++s) {
-                if (armed <= static_cast<uint32_t>(s)) break;
-                const uint32_t last = ((armed - 1 - s) / S) * S + s;   // last arming of slot s
-                if (!mbar_wait(&full[s], (last / S) & 1u)) {
-                    record_error(p, kErrTimeoutProducer, &abort_flag);
-                    break;
+            // Wind-down: wait (bounded) until every TMA load issued into this
+            // CTA pair has landed.  The even CTA's "full" barriers count the
+            // bytes of both CTAs, so only the even CTA waits; the odd CTA is
+            // held by the cluster barrier before exit until then.
+            if (rank == 0) {
+                for (int s = 0; s < S; ++s) {
+                    if (armed <= static_cast<uint32_t>(s)) break;
+                    const uint32_t last = ((armed - 1 - s) / S) * S + s;   // last arming of slot s
+                    if (!mbar_wait(&full[s], (last / S) & 1u)) {
+                        record_error(p, kErrTimeoutProducer, &abort_flag);
+                        break;
+                    }
                 }
             }
         }
     } else if (warp == 1) {
         // ------------------------------------------------------- MMA issuer
-        if (lane == 0) {
+        if (lane == 0 && rank == 0) {
             uint32_t stage = 0, phase = 0, acc_i = 0;
-            SegmentIter it(p, blockIdx.x, gridDim.x);
+            SegmentIter it(p, unit, units);
             Segment sg;
             bool ok = true;
             const uint32_t a_lbo = p.a_mn_major ? kChunkBytes : 16u;
@@ -345,7 +427,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t smem_base = smem_addr(smem);
             while (ok && it.next(p, sg)) {
                 const uint32_t buf = acc_i & 1u;
-                if (!wait_or_abort(&acc_empty[buf], ((acc_i >> 1) & 1u) ^ 1u, &abort_flag)) {
+                if (!wait_role<CG>(&acc_empty[buf], ((acc_i >> 1) & 1u) ^ 1u, &abort_flag)) {
                     record_error(p, kErrTimeoutMma, &abort_flag);
                     break;
                 }
@@ -364,29 +446,35 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int kk = 0; kk < kBlockK / kUmmaK; ++kk) {
                         const uint64_t ad = smem_desc_sw128(sa + kk * a_kstep, a_lbo, 1024);
                         const uint64_t bd = smem_desc_sw128(sb + kk * b_kstep, b_lbo, 1024);
-                        tc_mma_f16(d_tmem, ad, bd, p.idesc, (kb > sg.kb0 || kk > 0) ? 1u : 0u);
+                        const uint32_t acc = (kb > sg.kb0 || kk > 0) ? 1u : 0u;
+                        if constexpr (CG == 1) tc_mma_f16(d_tmem, ad, bd, p.idesc, acc);
+                        else tc_mma_f16_pair(d_tmem, ad, bd, p.idesc, acc);
                     }
-                    tc_commit(&empty[stage]);
+                    if constexpr (CG == 1) tc_commit(&empty[stage]);
+                    else tc_commit_pair_multicast(&empty[stage], 0x3);
                     if (++stage == static_cast<uint32_t>(S)) {
                         stage = 0;
                         phase ^= 1u;
                     }
                 }
                 if (!ok) break;
-                tc_commit(&acc_full[buf]);
+                if constexpr (CG == 1) tc_commit(&acc_full[buf]);
+                else tc_commit_pair_multicast(&acc_full[buf], 0x3);
                 ++acc_i;
             }
             // Wind-down: every MMA issued has completed before TMEM is freed.
-            tc_commit(drain);
+            if constexpr (CG == 1) tc_commit(drain);
+            else tc_commit_pair(drain);
             if (!mbar_wait(drain, 0)) record_error(p, kErrTimeoutMma, &abort_flag);
         }
     } else {
         // --------------------------------------------------------- epilogue
         const int quarter = warp & 3;                   // TMEM lanes 32*quarter..+31
-        const int row_in_tile = quarter * 32 + lane;
+        const int row_in_cta = quarter * 32 + lane;
+        const int row_in_tile = static_cast<int>(rank) * kBlockM + row_in_cta;
         OutT* C = reinterpret_cast<OutT*>(p.C);
         uint32_t acc_i = 0;
-        SegmentIter it(p, blockIdx.x, gridDim.x);
+        SegmentIter it(p, unit, units);
         Segment sg;
         while (it.next(p, sg)) {
             const uint32_t buf = acc_i & 1u;
@@ -397,8 +485,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after_sync();
             int32_t tm, tn;
             tile_coords(p, sg.tile, tm, tn);
-            const int32_t row = tm * kBlockM + row_in_tile;        // D' row
-            const int32_t col0 = tn * BN;                          // D' first column
+            const int32_t row = tm * BM + row_in_tile;              // D' row
+            const int32_t col0 = tn * BN;                           // D' first column
             const uint32_t t_row = tmem_base + buf * BN + (static_cast<uint32_t>(quarter * 32) << 16);
             #pragma unroll 1
             for (int ch = 0; ch < BN / 32; ++ch) {
@@ -413,7 +501,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (sg.slot >= 0) {
                     // stream-K partial: raw FP32 sums, [slot][row_in_tile][BN]
                     float4* dst = reinterpret_cast<float4*>(
-                        p.partials + (static_cast<int64_t>(sg.slot) * kBlockM + row_in_tile) * BN +
+                        p.partials + (static_cast<int64_t>(sg.slot) * BM + row_in_tile) * BN +
                         ch * 32);
                     #pragma unroll
                     for (int q = 0; q < 8; ++q)
@@ -441,24 +529,31 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             tc_fence_before_sync();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&acc_empty[buf]);
+            if (lane == 0) {
+                if constexpr (CG == 1) mbar_arrive(&acc_empty[buf]);
+                else mbar_arrive_cluster(map_to_rank(smem_addr(&acc_empty[buf]), 0));
+            }
             ++acc_i;
         }
     }
 
     tc_fence_before_sync();
     __syncthreads();
+    if constexpr (CG == 2) cluster_sync_all();            // peer done with our smem / TMEM
     tc_fence_after_sync();
-    if (warp == 1) tmem_dealloc(tmem_base, kTmemCols);
+    if (warp == 1) {
+        if constexpr (CG == 1) tmem_dealloc(tmem_base, kTmemCols);
+        else tmem_dealloc_pair(tmem_base, kTmemCols);
+    }
 }
 
 // Stream-K fixup: for every tile that was split across CTAs, add its partial
 // slots in increasing CTA order, then apply alpha/beta and the output cast.
 // One thread per (tile, row, 4 columns).
-template <int BN, typename OutT>
+template <int BM, int BN, typename OutT>
 __global__ void __launch_bounds__(256)
     streamk_fixup_kernel(const __grid_constant__ TcParams p) {
-    const int64_t per_tile = static_cast<int64_t>(kBlockM) * (BN / 4);
+    const int64_t per_tile = static_cast<int64_t>(BM) * (BN / 4);
     const int64_t total = per_tile * p.num_tiles;
     OutT* C = reinterpret_cast<OutT*>(p.C);
     const int32_t KB = p.k_blocks, L = p.sk_len;
@@ -473,14 +568,14 @@ __global__ void __launch_bounds__(256)
         if (g_first == g_last) continue;           // stored whole by one CTA
         int32_t tm, tn;
         tile_coords(p, tile, tm, tn);
-        const int32_t row = tm * kBlockM + r;
+        const int32_t row = tm * BM + r;
         if (row >= p.M) continue;
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
         for (int32_t g = g_first; g <= g_last; ++g) {
             const int32_t first_tile = static_cast<int32_t>((static_cast<int64_t>(g) * L) / KB);
             const int64_t slot = static_cast<int64_t>(g) * p.sk_max_seg + (tile - first_tile);
             const float4 v = *reinterpret_cast<const float4*>(
-                p.partials + (slot * kBlockM + r) * BN + c4);
+                p.partials + (slot * BM + r) * BN + c4);
             acc.x += v.x;
             acc.y += v.y;
             acc.z += v.z;

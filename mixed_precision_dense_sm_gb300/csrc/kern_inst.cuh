@@ -1,6 +1,9 @@
 // kern_inst.cuh -- instantiates the tcgen05 GEMM and its stream-K fixup for one
-// output type (KERN_OUT_T) and the three tile widths, behind plain launchers.
+// output type (KERN_OUT_T): single-CTA tiles of width 64/128/256 and CTA-pair
+// tiles of width 256, behind plain launchers.
 #pragma once
+#include <mutex>
+
 #include "launch.h"
 
 #define GEMM103_CAT2(a, b) a##b
@@ -8,30 +11,76 @@
 
 namespace gemm103 {
 
-template <int BN>
-static cudaError_t launch_tc_bn(const TcLaunch& l) {
-    auto kern = gemm_tc_kernel<BN, KERN_OUT_T>;
+template <int CG, int BN>
+static cudaError_t launch_tc_cfg(const TcLaunch& l) {
+    auto kern = gemm_tc_kernel<CG, BN, KERN_OUT_T>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(l.smem_bytes));
     if (e != cudaSuccess) return e;
-    kern<<<l.grid, kThreads, l.smem_bytes, l.stream>>>(l.tmA, l.tmB, l.p);
-    return cudaGetLastError();
+    if constexpr (CG == 1) {
+        kern<<<l.grid, kThreads, l.smem_bytes, l.stream>>>(l.tmA, l.tmB, l.p);
+        return cudaGetLastError();
+    } else {
+        cudaLaunchConfig_t cfg = {};
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.blockDim = dim3(kThreads, 1, 1);
+        cfg.dynamicSmemBytes = l.smem_bytes;
+        cfg.stream = l.stream;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int grid = l.grid;
+        if (!l.p.stream_k) {
+            // A data-parallel schedule adapts to the grid: launch no more
+            // pairs than can be resident at once (persistent CTAs).
+            static std::mutex mu;
+            static size_t cached_smem = 0;
+            static int cached_clusters = 0;
+            int clusters = 0;
+            {
+                std::lock_guard<std::mutex> g(mu);
+                if (cached_smem != l.smem_bytes) {
+                    cfg.gridDim = dim3(grid, 1, 1);
+                    if (cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg) != cudaSuccess) {
+                        cudaGetLastError();
+                        clusters = 0;
+                    }
+                    cached_smem = l.smem_bytes;
+                    cached_clusters = clusters;
+                }
+                clusters = cached_clusters;
+            }
+            if (clusters > 0 && grid > 2 * clusters) grid = 2 * clusters;
+        }
+        cfg.gridDim = dim3(grid, 1, 1);
+        return cudaLaunchKernelEx(&cfg, kern, l.tmA, l.tmB, l.p);
+    }
 }
 
 cudaError_t GEMM103_CAT(launch_tc_, KERN_SUFFIX)(const TcLaunch& l) {
+    if (l.cta_group == 2) {
+        switch (l.block_n) {
+            case 256: return launch_tc_cfg<2, 256>(l);
+            default: return cudaErrorInvalidValue;
+        }
+    }
     switch (l.block_n) {
-        case 64: return launch_tc_bn<64>(l);
-        case 128: return launch_tc_bn<128>(l);
-        case 256: return launch_tc_bn<256>(l);
+        case 64: return launch_tc_cfg<1, 64>(l);
+        case 128: return launch_tc_cfg<1, 128>(l);
+        case 256: return launch_tc_cfg<1, 256>(l);
         default: return cudaErrorInvalidValue;
     }
 }
 
 cudaError_t GEMM103_CAT(launch_fixup_, KERN_SUFFIX)(const TcLaunch& l, int grid) {
+    if (l.cta_group != 1) return cudaErrorInvalidValue;
     switch (l.block_n) {
-        case 64: streamk_fixup_kernel<64, KERN_OUT_T><<<grid, 256, 0, l.stream>>>(l.p); break;
-        case 128: streamk_fixup_kernel<128, KERN_OUT_T><<<grid, 256, 0, l.stream>>>(l.p); break;
-        case 256: streamk_fixup_kernel<256, KERN_OUT_T><<<grid, 256, 0, l.stream>>>(l.p); break;
+        case 64: streamk_fixup_kernel<128, 64, KERN_OUT_T><<<grid, 256, 0, l.stream>>>(l.p); break;
+        case 128: streamk_fixup_kernel<128, 128, KERN_OUT_T><<<grid, 256, 0, l.stream>>>(l.p); break;
+        case 256: streamk_fixup_kernel<128, 256, KERN_OUT_T><<<grid, 256, 0, l.stream>>>(l.p); break;
         default: return cudaErrorInvalidValue;
     }
     return cudaGetLastError();

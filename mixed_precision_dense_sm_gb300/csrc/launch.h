@@ -13,6 +13,7 @@ struct TcLaunch {
     CUtensorMap tmA, tmB;
     TcParams p;
     int grid;
+    int cta_group;      // 1: single-CTA tiles, 2: CTA-pair tiles
     int block_n;
     size_t smem_bytes;
     cudaStream_t stream;

@@ -70,8 +70,10 @@ def plan(w: workloads.Workload, ptr=256, **kw):
 def test_plans_of_named_workloads():
     P = {n: plan(w) for n, w in workloads.WORKLOADS.items()}
     big = P["linear_8192x4096x4096_bf16"]
-    assert big["path_name"] == "tiled_1sm" and big["block_n"] == 256 and big["sk_len"] == 0
-    assert big["grid"] == 152 and big["num_tiles"] == 64 * 16
+    assert big["path_name"] == "tiled_2sm" and big["block_n"] == 256 and big["sk_len"] == 0
+    assert big["block_m"] == 256 and big["grid"] == 152 and big["num_tiles"] == 32 * 16
+    for n in ("linear_8192x14336x4096_bf16", "linear_8192x4096x14336_bf16"):
+        assert P[n]["path_name"] == "tiled_2sm" and P[n]["grid"] % 2 == 0
     sk = P["skinny_64x16384x8192_f16"]
     assert sk["path_name"] == "skinny" and sk["swap_ab"] == 1 and sk["block_n"] == 64
     rag = P["ragged1000x1023x777_bf16_beta1"]
@@ -81,7 +83,8 @@ def test_plans_of_named_workloads():
     assert sq["pack_a"] == 0 and sq["pack_b"] == 0 and sq["b_mn_major"] == 0
     for p in P.values():
         assert 2 <= p["stages"] <= 8
-        stage = 128 * 64 * 2 + p["block_n"] * 64 * 2
+        cg = p["block_m"] // 128
+        stage = 128 * 64 * 2 + (p["block_n"] // cg) * 64 * 2
         assert p["stages"] * stage + 1024 + 256 <= 232448
 
 
@@ -96,6 +99,18 @@ def test_quick_paths_and_swap_rule():
     assert plan(w)["swap_ab"] == 1
     w = workloads.Workload("q", 65, 128, 64, "N", "N", DT_F16, DT_F32, 1.0, 0.0, "U", "U")
     assert plan(w)["swap_ab"] == 0
+
+
+def test_pair_tiles_only_when_they_fill_the_gpu():
+    def path(M, N, K, sms=152):
+        w = workloads.Workload("p", M, N, K, "N", "T", DT_BF16, DT_BF16, 1.0, 0.0, "U", "U")
+        return plan(w, num_sms=sms)
+    assert path(4096, 4096, 4096)["path_name"] == "tiled_2sm"     # 256 pair tiles
+    assert path(2048, 2048, 4096)["path_name"] == "tiled_1sm"     # 64 pair tiles < 76 pairs
+    p = path(2048, 4864, 1024)                                    # 8 x 19 = 152 >= 76
+    assert p["path_name"] == "tiled_2sm" and p["grid"] == 152
+    p = path(300, 100000, 64, sms=8)
+    assert p["path_name"] == "tiled_2sm" and p["grid"] == 8
 
 
 def test_pack_rule_follows_16_byte_alignment():

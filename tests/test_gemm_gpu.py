@@ -194,3 +194,27 @@ def test_deterministic_and_stream(g, orc):
     for o in outs[1:]:
         assert torch.equal(o.view(torch.int32), outs[0].view(torch.int32))
     gc.check_full(orc, w, inp, outs[0].cuda())
+
+
+PAIR_SHAPES = [(1900, 4736, 200), (2048, 4864, 136), (4096, 4096, 64)]
+
+
+@pytest.mark.parametrize("M,N,K", PAIR_SHAPES, ids=[f"{m}x{n}x{k}" for m, n, k in PAIR_SHAPES])
+def test_cta_pair_tiles_integer_exact(g, orc, M, N, K):
+    """Shapes large enough for 256 x 256 CTA-pair tiles, every transpose pair,
+    bit-exact with integer inputs.  1900 x 4736 puts the odd CTA's half of the
+    last tile row (rows 1920+) and of the last tile column (columns 4736+)
+    wholly outside the matrix."""
+    import mixed_precision_dense_sm_gb300 as lib
+    for ta, tb in itertools.product("NT", "NT"):
+        c = (DT_BF16, DT_F32, DT_F16, DT_BF16)["NT".index(ta) * 2 + "NT".index(tb)]
+        w = W(M, N, K, ta, tb, DT_BF16 if ta == tb else DT_F16, c,
+              beta=1.0 if ta == "T" else 0.0)
+        lda, ldb, ldc = w.lds()
+        st, plan = lib.gemm_plan_query(ta, tb, M, N, K, 1.0, 256, lda, 256, ldb, w.beta, 256, ldc,
+                                       (w.ab_dtype, w.ab_dtype, w.c_dtype),
+                                       num_sms=torch.cuda.get_device_properties(0).multi_processor_count)
+        assert st == 0 and plan["path_name"] == "tiled_2sm", plan
+        inp = gc.integer_inputs(w)
+        C = gc.run_gpu(g, w, inp)
+        gc.check_full(orc, w, inp, C, exact=True)
