@@ -192,8 +192,9 @@ gemm_status_t gemm_plan_query(char transA, char transB, int64_t M, int64_t N, in
  * library holds until the process exits.  A problem that needs more scratch
  * than that (see gemm_plan_t.workspace_bytes) is rejected with
  * GEMM_ERR_INVALID_VALUE and nothing is enqueued.  All calls on a device share
- * the array and it keeps the last call's contents (nothing in it needs to start
- * at zero); calls that overlap on the GPU -- on different streams, or from
+ * the array and it keeps the last call's contents; the part that must start at
+ * zero (split-K tile counters) is cleared on the stream by each call that uses
+ * it.  Calls that overlap on the GPU -- on different streams, or from
  * different host threads without ordering -- race on it, so order them on one
  * stream.
  *

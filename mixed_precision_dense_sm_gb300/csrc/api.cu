@@ -17,7 +17,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
-#include "../../include/gemm_sm103.h"
+#include "gemm_sm103.h"
 #include "aux_kernels.cuh"
 #include "launch.h"
 
@@ -27,6 +27,11 @@ namespace {
 
 constexpr int kMaxStages = 8;
 constexpr int kGroupM = 8;
+// Workspace header: two stream-K counters (int32: arrived, written) per output
+// tile.  Stream-K is only planned with fewer tiles than SMs, so 512 tiles'
+// worth always suffices.
+constexpr int64_t kWsHeaderBytes = 4096;
+constexpr int64_t kMaxCounterTiles = kWsHeaderBytes / 8;
 
 struct OperandDesc {
     // stored matrix: rows x cols with pitch ld (elements); K-major means the
@@ -155,13 +160,18 @@ gemm_status_t make_plan(char transA, char transB, int64_t M, int64_t N, int64_t 
     const int cg = pairs ? 2 : 1;
     const int64_t block_m = static_cast<int64_t>(kBlockM) * cg;
     const int64_t tiles_m = ceil_div(pl.Mk, block_m);
+    // Single-CTA tiles: the widest of 256 / 128 / 64 columns that still gives
+    // every SM a tile (256) or at least half a wave (128, 64).
     int bn;
+    const int64_t half_wave = (num_sms + 1) / 2;
     if (pairs || (pl.Nk > 128 && tiles_m * ceil_div(pl.Nk, 256) >= num_sms)) {
         bn = 256;
-    } else if (pl.Nk <= 64) {
-        bn = 64;
-    } else {
+    } else if (pl.Nk > 64 && tiles_m * ceil_div(pl.Nk, 128) >= half_wave) {
         bn = 128;
+    } else if (pl.Nk > 64 && tiles_m * ceil_div(pl.Nk, 64) < half_wave) {
+        bn = 128;                           // too few tiles either way: stream-K below
+    } else {
+        bn = 64;
     }
     const int64_t tiles_n = ceil_div(pl.Nk, bn);
     const int64_t tiles = tiles_m * tiles_n;
@@ -182,7 +192,12 @@ gemm_status_t make_plan(char transA, char transB, int64_t M, int64_t N, int64_t 
     pl.smem_bytes = static_cast<size_t>(stages * stage_bytes + 1024 + barrier_bytes);
 
     const int64_t work = tiles * pl.k_blocks;
-    const bool stream_k = !pairs && (tiles < num_sms) && (pl.k_blocks >= 4) && (work < INT32_MAX);
+    // Stream-K spreads the K loop of too few tiles over all SMs.  It pays for
+    // itself only when the tiles are long in K; the swapped skinny path
+    // (a weight-streaming GEMM) always uses it.
+    const bool stream_k = !pairs && (tiles < num_sms) && (tiles <= kMaxCounterTiles) &&
+                          (work < INT32_MAX) &&
+                          (swap ? pl.k_blocks >= 4 : (tiles < half_wave && pl.k_blocks >= 32));
     if (stream_k) {
         int64_t G = num_sms < work ? num_sms : work;
         const int64_t L = ceil_div(work, G);
@@ -202,8 +217,9 @@ gemm_status_t make_plan(char transA, char transB, int64_t M, int64_t N, int64_t 
     pl.pub.k_blocks = pl.k_blocks;
     pl.pub.tiles_m = pl.tiles_m;
     pl.pub.tiles_n = pl.tiles_n;
-    pl.pub.workspace_bytes = round_up(pl.pack_a_bytes, 256) + round_up(pl.pack_b_bytes, 256) +
-                             round_up(pl.partial_bytes, 256);
+    const int64_t body = round_up(pl.pack_a_bytes, 256) + round_up(pl.pack_b_bytes, 256) +
+                         round_up(pl.partial_bytes, 256);
+    pl.pub.workspace_bytes = body > 0 ? kWsHeaderBytes + body : 0;
     return GEMM_OK;
 }
 
@@ -257,6 +273,14 @@ gemm_status_t ensure_workspace(gemm_ctx* h, size_t bytes) {
         h->ws = nullptr;
         return GEMM_ERR_ALLOC;
     }
+    // The stream-K tile counters must start at zero; every call leaves them
+    // at zero again.
+    if (cudaMemset(h->ws, 0, kWsHeaderBytes) != cudaSuccess) {
+        cudaGetLastError();
+        cudaFree(h->ws);
+        h->ws = nullptr;
+        return GEMM_ERR_ALLOC;
+    }
     h->ws_bytes = want;
     return GEMM_OK;
 }
@@ -264,6 +288,11 @@ gemm_status_t ensure_workspace(gemm_ctx* h, size_t bytes) {
 gemm_status_t take_device_error(gemm_ctx* h) {
     volatile int* e = h->err_host;
     if (*e != 0) {
+        // A kernel that gave up may have left stream-K tile counters
+        // half-counted: clear them before the handle is used again.
+        cudaDeviceSynchronize();
+        if (h->ws) cudaMemset(h->ws, 0, kWsHeaderBytes);
+        cudaGetLastError();
         *e = 0;
         return GEMM_ERR_DEVICE_TIMEOUT;
     }
@@ -280,12 +309,19 @@ int grid_for(int64_t elems_per_thread_unit, int num_sms) {
 
 
 // Everything gemm_run enqueues after planning: the optional pack pre-passes,
-// the TMA descriptors, the GEMM kernel and the stream-K fixup.  `ws` is the
-// workspace laid out as [packed A][packed B][partial slots].
+// the TMA descriptors and the GEMM kernel.  `ws` is the workspace laid out as
+// [tile counters (4 KB)][packed A][packed B][partial slots]; with
+// clear_counters the counters are zeroed on the stream first.
 gemm_status_t enqueue_plan(const Plan& pl, EncodeTiledFn encode, int num_sms, uint8_t* ws,
                            int* err_dev, float alpha, float beta, void* C, gemm_dtypes_t dt,
-                           cudaStream_t stream) {
-    uint8_t* ws_a = ws;
+                           cudaStream_t stream, bool clear_counters) {
+    int* counters = reinterpret_cast<int*>(ws);
+    if (clear_counters && pl.sk_len > 0 &&
+        cudaMemsetAsync(counters, 0, kWsHeaderBytes, stream) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_LAUNCH;
+    }
+    uint8_t* ws_a = ws + kWsHeaderBytes;
     uint8_t* ws_b = ws_a + round_up(pl.pack_a_bytes, 256);
     float* ws_part = reinterpret_cast<float*>(ws_b + round_up(pl.pack_b_bytes, 256));
 
@@ -341,7 +377,13 @@ gemm_status_t enqueue_plan(const Plan& pl, EncodeTiledFn encode, int num_sms, ui
     p.c_cs = pl.c_cs;
     p.c_vector = pl.pub.c_vector;
     p.partials = pl.partial_bytes > 0 ? ws_part : nullptr;
+    p.tile_counters = pl.partial_bytes > 0 ? counters : nullptr;
     p.err = err_dev;
+    // In the swapped skinny path each tile of A' (the large operand) is read
+    // by exactly one CTA while B' (the few rows of the original A) is re-read
+    // by every CTA.
+    p.a_stream_once = pl.pub.swap_ab ? 1 : 0;
+    p.b_stream_once = 0;
     l.grid = pl.pub.grid;
     l.cta_group = cg;
     l.block_n = bn;
@@ -355,16 +397,6 @@ gemm_status_t enqueue_plan(const Plan& pl, EncodeTiledFn encode, int num_sms, ui
     if (e != cudaSuccess) {
         cudaGetLastError();
         return GEMM_ERR_LAUNCH;
-    }
-    if (p.stream_k) {
-        const int grid = grid_for(static_cast<int64_t>(p.num_tiles) * kBlockM * (bn / 4), num_sms);
-        if (dt.c == GEMM_F32) e = launch_fixup_f32(l, grid);
-        else if (dt.c == GEMM_F16) e = launch_fixup_f16(l, grid);
-        else e = launch_fixup_bf16(l, grid);
-        if (e != cudaSuccess) {
-            cudaGetLastError();
-            return GEMM_ERR_LAUNCH;
-        }
     }
     return GEMM_OK;
 }
@@ -504,7 +536,7 @@ gemm_status_t gemm_run(gemm_handle_t h, char transA, char transB, int64_t M, int
     st = ensure_workspace(h, static_cast<size_t>(pl.pub.workspace_bytes));
     if (st != GEMM_OK) return st;
     return enqueue_plan(pl, h->encode, h->num_sms, static_cast<uint8_t*>(h->ws), h->err_dev, alpha,
-                        beta, C, dt, stream);
+                        beta, C, dt, stream, false);
 }
 
 }  // extern "C"
@@ -597,10 +629,12 @@ extern "C" gemm_status_t gemm_run_noalloc(char transA, char transB, int64_t M, i
     if (pl.pub.path == GEMM_PATH_NOOP) return GEMM_OK;
     if (pl.pub.path == GEMM_PATH_SCALE)
         return enqueue_scale(M, N, C, ldc, beta, dt, d.num_sms, stream);
-    // The scratch takes the place of a handle's workspace.  Nothing in it has
-    // to start at zero: the packed copies and every partial-sum slot are fully
-    // written before they are read within this call.  No host-visible error
-    // word exists without an allocation, so device timeouts are not reported.
+    // The scratch takes the place of a handle's workspace.  Its stream-K tile
+    // counters must start at zero, so they are cleared on the stream at the
+    // start of every call that uses them; the packed copies and every
+    // partial-sum slot are fully written before they are read within the
+    // call.  No host-visible error word exists without an allocation, so
+    // device timeouts are not reported.
     return enqueue_plan(pl, d.encode, d.num_sms, static_cast<uint8_t*>(d.scratch), nullptr, alpha,
-                        beta, C, dt, stream);
+                        beta, C, dt, stream, true);
 }

@@ -31,9 +31,10 @@
 //  * Data-parallel mode: CTA g takes tiles g, g + G, g + 2G, ... whole.
 //  * Stream-K mode (fewer tiles than SMs): the (tile, k-block) space is cut
 //    into G contiguous ranges of L k-blocks, one per CTA.  A segment that
-//    covers a whole tile is stored directly; a partial one writes its raw
-//    FP32 sums to a workspace slot, and a separate fixup kernel adds a tile's
-//    slots in increasing CTA order (deterministic) and applies the epilogue.
+//    covers a whole tile is stored directly; for a split tile the last CTA to
+//    finish its part adds every contribution in increasing CTA order
+//    (deterministic) -- its own from registers, the others' from workspace
+//    slots -- and applies the epilogue.
 //
 // CTA pairs.  For large problems two CTAs of a cluster share one 256 x BN
 // tile through tcgen05's cta_group::2 form (see gemm_tc_kernel below): each SM
@@ -80,9 +81,11 @@ struct TcParams {
     void* C;
     int64_t c_rs, c_cs;         // D'(i, j) -> C[i * c_rs + j * c_cs]
     int32_t c_vector;           // c_cs == 1 and rows 16-byte aligned
-    float* partials;            // stream-K slots: [G * sk_max_seg][128][BN] FP32
+    float* partials;            // stream-K slots: [G * sk_max_seg][BM][BN] FP32
+    int* tile_counters;         // stream-K: per tile {arrived, written} (self-resetting)
     int* err;                   // device-visible error word (0 = ok)
-    uint64_t ab_policy;         // unused placeholder for cache-policy selection
+    int32_t a_stream_once;      // 1: A is read once (evict-first in L2), 0: reused
+    int32_t b_stream_once;
 };
 
 struct Segment {
@@ -195,14 +198,22 @@ __device__ __forceinline__ float load_out<__nv_bfloat16>(const __nv_bfloat16* p)
 template <typename OutT>
 __device__ __forceinline__ void store_row32_vec(OutT* dst, const float (&v)[32], float beta) {
     constexpr int kPer16 = 16 / sizeof(OutT);      // elements per 16-byte vector
+    constexpr int kVecs = 32 / kPer16;
+    // Read every old value before the first store: a load that follows a
+    // store to the same array cannot be hoisted, and each would cost a full
+    // memory round trip.
+    uint4 old[kVecs];
+    if (beta != 0.0f) {
+        #pragma unroll
+        for (int q = 0; q < kVecs; ++q) old[q] = *reinterpret_cast<const uint4*>(dst + q * kPer16);
+    }
     #pragma unroll
-    for (int q = 0; q < 32 / kPer16; ++q) {
+    for (int q = 0; q < kVecs; ++q) {
         float x[kPer16];
         #pragma unroll
         for (int e = 0; e < kPer16; ++e) x[e] = v[q * kPer16 + e];
         if (beta != 0.0f) {
-            uint4 old = *reinterpret_cast<const uint4*>(dst + q * kPer16);
-            const OutT* o = reinterpret_cast<const OutT*>(&old);
+            const OutT* o = reinterpret_cast<const OutT*>(&old[q]);
             #pragma unroll
             for (int e = 0; e < kPer16; ++e) x[e] = fmaf(beta, load_out<OutT>(o + e), x[e]);
         }
@@ -245,6 +256,71 @@ __device__ __forceinline__ bool wait_role(uint64_t* bar, uint32_t parity, volati
 //   alone issues the MMAs, whose commits arrive on the "empty" / "acc_full"
 //   barriers of both CTAs; both CTAs drain their own TMEM half (128 rows x BN)
 //   and release the accumulator on the even CTA's "acc_empty" barrier.
+// r = alpha * v + beta * C for one row of 32 columns starting at D' column c0,
+// cast and stored (vector stores when C rows are 16-byte aligned and the chunk
+// is whole, element stores otherwise).
+template <typename OutT>
+__device__ __forceinline__ void store_chunk(const TcParams& p, int32_t row, int32_t c0,
+                                            float (&v)[32]) {
+    OutT* C = reinterpret_cast<OutT*>(p.C);
+    #pragma unroll
+    for (int j = 0; j < 32; ++j) v[j] *= p.alpha;
+    if (row >= p.M) return;
+    if (p.c_vector && c0 + 32 <= p.N) {
+        store_row32_vec<OutT>(C + static_cast<int64_t>(row) * p.c_rs + c0, v, p.beta);
+    } else {
+        OutT* base = C + static_cast<int64_t>(row) * p.c_rs;
+        if (p.beta != 0.0f) {
+            float old[32];
+            #pragma unroll
+            for (int j = 0; j < 32; ++j)
+                old[j] = (c0 + j < p.N) ? load_out<OutT>(base + static_cast<int64_t>(c0 + j) * p.c_cs)
+                                        : 0.0f;
+            #pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] = fmaf(p.beta, old[j], v[j]);
+        }
+        #pragma unroll
+        for (int j = 0; j < 32; ++j)
+            if (c0 + j < p.N) base[static_cast<int64_t>(c0 + j) * p.c_cs] = cvt_out<OutT>(v[j]);
+    }
+}
+
+// Spin (bounded) until the global counter reaches `target`.
+__device__ __forceinline__ bool wait_counter(const int* ctr, int target, volatile int* abort_flag) {
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t i = 0;; ++i) {
+        int v;
+        asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(ctr) : "memory");
+        if (v >= target) return true;
+        if ((i & 63u) == 63u) {
+            if (*abort_flag) return false;
+            if (global_timer_ns() - t0 > kWaitTimeoutNs) return false;
+        }
+        __nanosleep(32);
+    }
+}
+
+// Named barrier 1 among the four epilogue warps.
+__device__ __forceinline__ void epilogue_bar_sync() {
+    asm volatile("bar.sync 1, %0;" ::"n"(kEpiWarps * 32) : "memory");
+}
+
+// All four epilogue warps agree on `ok` (logical AND), so that after a
+// bounded wait either every epilogue warp carries on or every one stops --
+// none is left behind at a later named barrier.
+__device__ __forceinline__ bool epilogue_all(bool ok) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 q, %1, 0;\n\t"
+        "bar.red.and.pred p, 1, %2, q;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(r)
+        : "r"(ok ? 1u : 0u), "n"(kEpiWarps * 32)
+        : "memory");
+    return r != 0;
+}
+
 template <int CG, int BN, typename OutT>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -308,7 +384,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0) {
         // ------------------------------------------------------ TMA producer
         if (lane == 0) {
-            const uint64_t policy = l2_policy_evict_last();
+            // Operands that every tile re-reads stay in L2 (evict-last); an
+            // operand streamed once (the weights of a skinny GEMM) is marked
+            // evict-first so it does not push the reused one out.
+            const uint64_t pol_a = p.a_stream_once ? l2_policy_evict_first() : l2_policy_evict_last();
+            const uint64_t pol_b = p.b_stream_once ? l2_policy_evict_first() : l2_policy_evict_last();
             uint32_t stage = 0, phase = 0;
             uint32_t armed = 0;                   // number of slot armings so far
             SegmentIter it(p, unit, units);
@@ -362,16 +442,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (p.a_mn_major) {
                             for (int c = 0; c < na; ++c)
                                 tma_load_2d(sa + c * kChunkBytes, &tmA, &full[stage], m0 + 64 * c,
-                                            k0, policy);
+                                            k0, pol_a);
                         } else if (na) {
-                            tma_load_2d(sa, &tmA, &full[stage], k0, m0, policy);
+                            tma_load_2d(sa, &tmA, &full[stage], k0, m0, pol_a);
                         }
                         if (p.b_mn_major) {
                             for (int c = 0; c < nb; ++c)
                                 tma_load_2d(sb + c * kChunkBytes, &tmB, &full[stage], n0 + 64 * c,
-                                            k0, policy);
+                                            k0, pol_b);
                         } else if (nb) {
-                            tma_load_2d(sb, &tmB, &full[stage], k0, n0, policy);
+                            tma_load_2d(sb, &tmB, &full[stage], k0, n0, pol_b);
                         }
                     } else {
                         const uint32_t fb = map_to_rank(smem_addr(&full[stage]), 0);
@@ -379,16 +459,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (p.a_mn_major) {
                             for (int c = 0; c < na; ++c)
                                 tma_load_2d_pair(sa + c * kChunkBytes, &tmA, fb, m0 + 64 * c, k0,
-                                                 policy);
+                                                 pol_a);
                         } else if (na) {
-                            tma_load_2d_pair(sa, &tmA, fb, k0, m0, policy);
+                            tma_load_2d_pair(sa, &tmA, fb, k0, m0, pol_a);
                         }
                         if (p.b_mn_major) {
                             for (int c = 0; c < nb; ++c)
                                 tma_load_2d_pair(sb + c * kChunkBytes, &tmB, fb, n0 + 64 * c, k0,
-                                                 policy);
+                                                 pol_b);
                         } else if (nb) {
-                            tma_load_2d_pair(sb, &tmB, fb, k0, n0, policy);
+                            tma_load_2d_pair(sb, &tmB, fb, k0, n0, pol_b);
                         }
                     }
                     ++armed;
@@ -472,13 +552,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int quarter = warp & 3;                   // TMEM lanes 32*quarter..+31
         const int row_in_cta = quarter * 32 + lane;
         const int row_in_tile = static_cast<int>(rank) * kBlockM + row_in_cta;
-        OutT* C = reinterpret_cast<OutT*>(p.C);
         uint32_t acc_i = 0;
         SegmentIter it(p, unit, units);
         Segment sg;
         while (it.next(p, sg)) {
             const uint32_t buf = acc_i & 1u;
-            if (!wait_or_abort(&acc_full[buf], (acc_i >> 1) & 1u, &abort_flag)) {
+            bool ok = wait_or_abort(&acc_full[buf], (acc_i >> 1) & 1u, &abort_flag);
+            if (p.stream_k) ok = epilogue_all(ok);        // stream-K uses named barriers below
+            if (!ok) {
                 record_error(p, kErrTimeoutEpilogue, &abort_flag);
                 break;
             }
@@ -488,8 +569,95 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int32_t row = tm * BM + row_in_tile;              // D' row
             const int32_t col0 = tn * BN;                           // D' first column
             const uint32_t t_row = tmem_base + buf * BN + (static_cast<uint32_t>(quarter * 32) << 16);
+
+            // Stream-K tile split across CTAs g_first..g_last.  Each
+            // contributor counts itself on the tile's "arrive" counter as soon
+            // as its sums are in TMEM.  The last to arrive is the finisher: it
+            // keeps its own sums in registers, waits (bounded) until the others
+            // have stored theirs and counted them on the "written" counter,
+            // then adds all contributions in increasing CTA order -- the same
+            // order whichever CTA finishes -- applies the epilogue and resets
+            // both counters.  The others store their sums to their slot.
+            const int32_t KB = p.k_blocks, L = p.sk_len;
+            int32_t g_first = 0, g_last = -1;
+            bool finisher = false;
+            __shared__ int role_flag;
+            if (sg.slot >= 0) {
+                g_first = static_cast<int32_t>((static_cast<int64_t>(sg.tile) * KB) / L);
+                g_last = static_cast<int32_t>((static_cast<int64_t>(sg.tile + 1) * KB - 1) / L);
+                int* arrive = p.tile_counters + 2 * sg.tile;
+                if (warp == 2 && lane == 0) {
+                    const int old = atomicAdd(arrive, 1);
+                    const int last = (old == g_last - g_first) ? 1 : 0;
+                    if (last) *arrive = 0;
+                    role_flag = last;
+                }
+                epilogue_bar_sync();
+                finisher = (role_flag != 0);
+                if (finisher) {
+                    epilogue_bar_sync();                   // everyone has read role_flag
+                    if (warp == 2 && lane == 0) {
+                        const bool ok_w = wait_counter(arrive + 1, g_last - g_first, &abort_flag);
+                        if (ok_w) arrive[1] = 0;
+                        else record_error(p, kErrTimeoutEpilogue, &abort_flag);
+                    }
+                    epilogue_bar_sync();
+                    __threadfence();
+                }
+            }
+            float* my_slot = (sg.slot >= 0 && !finisher)
+                                 ? p.partials + static_cast<int64_t>(sg.slot) * BM * BN
+                                 : nullptr;
+            if constexpr (BN == 64) {
+                if (finisher) {
+                    // 64-column tiles: one batch of loads per contribution (the
+                    // whole row at once), own sums re-read from TMEM in turn.
+                    float acc[64];
+                    #pragma unroll
+                    for (int j = 0; j < 64; ++j) acc[j] = 0.0f;
+                    for (int32_t g = g_first; g <= g_last; ++g) {
+                        float x[64];
+                        if (g == unit) {
+                            uint32_t r0[32], r1[32];
+                            __syncwarp();
+                            tmem_ld_32x32b_x32(t_row, r0);
+                            tmem_ld_32x32b_x32(t_row + 32, r1);
+                            tmem_ld_wait();
+                            #pragma unroll
+                            for (int j = 0; j < 32; ++j) {
+                                x[j] = __uint_as_float(r0[j]);
+                                x[32 + j] = __uint_as_float(r1[j]);
+                            }
+                        } else {
+                            const int32_t first_tile =
+                                static_cast<int32_t>((static_cast<int64_t>(g) * L) / KB);
+                            const float* src = p.partials +
+                                               (static_cast<int64_t>(g) * p.sk_max_seg +
+                                                (sg.tile - first_tile)) * BM * BN;
+                            if (p.c_cs == 1) {
+                                const float4* s4 = reinterpret_cast<const float4*>(src + row_in_tile * BN);
+                                #pragma unroll
+                                for (int q = 0; q < 16; ++q) {
+                                    const float4 t = __ldcg(s4 + q);
+                                    x[4 * q] = t.x;
+                                    x[4 * q + 1] = t.y;
+                                    x[4 * q + 2] = t.z;
+                                    x[4 * q + 3] = t.w;
+                                }
+                            } else {
+                                #pragma unroll
+                                for (int j = 0; j < 64; ++j) x[j] = __ldcg(src + j * BM + row_in_tile);
+                            }
+                        }
+                        #pragma unroll
+                        for (int j = 0; j < 64; ++j) acc[j] += x[j];
+                    }
+                    store_chunk<OutT>(p, row, col0, *reinterpret_cast<float(*)[32]>(acc));
+                    store_chunk<OutT>(p, row, col0 + 32, *reinterpret_cast<float(*)[32]>(acc + 32));
+                }
+            }
             #pragma unroll 1
-            for (int ch = 0; ch < BN / 32; ++ch) {
+            for (int ch = 0; ch < ((BN == 64 && finisher) ? 0 : BN / 32); ++ch) {
                 uint32_t r[32];
                 __syncwarp();                      // tcgen05.ld is warp-collective
                 tmem_ld_32x32b_x32(t_row + ch * 32, r);
@@ -498,33 +666,70 @@ __global__ void __launch_bounds__(kThreads, 1)
                 #pragma unroll
                 for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
                 const int32_t c0 = col0 + ch * 32;
-                if (sg.slot >= 0) {
-                    // stream-K partial: raw FP32 sums, [slot][row_in_tile][BN]
-                    float4* dst = reinterpret_cast<float4*>(
-                        p.partials + (static_cast<int64_t>(sg.slot) * BM + row_in_tile) * BN +
-                        ch * 32);
+                if (sg.slot < 0) {
+                    store_chunk<OutT>(p, row, c0, v);
+                } else if (my_slot != nullptr) {
+                    // raw FP32 sums, laid out along C's contiguous direction:
+                    // [row][col] when C rows are contiguous (c_cs == 1),
+                    // [col][row] otherwise, so every warp store is coalesced
+                    if (p.c_cs == 1) {
+                        float4* dst = reinterpret_cast<float4*>(my_slot + row_in_tile * BN + ch * 32);
+                        #pragma unroll
+                        for (int q = 0; q < 8; ++q)
+                            dst[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+                    } else {
+                        #pragma unroll
+                        for (int j = 0; j < 32; ++j) my_slot[(ch * 32 + j) * BM + row_in_tile] = v[j];
+                    }
+                } else if constexpr (BN != 64) {
+                    // finisher: acc = sum of contributions g_first..g_last in
+                    // that order, its own (g == unit) from registers.  Loads of
+                    // up to four slots are issued together, 16 columns at a
+                    // time, so their memory latencies overlap.
+                    float acc[32];
                     #pragma unroll
-                    for (int q = 0; q < 8; ++q)
-                        dst[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-                    continue;
-                }
-                #pragma unroll
-                for (int j = 0; j < 32; ++j) v[j] *= p.alpha;
-                if (row >= p.M) continue;
-                if (p.c_vector && c0 + 32 <= p.N) {
-                    store_row32_vec<OutT>(C + static_cast<int64_t>(row) * p.c_rs + c0, v, p.beta);
-                } else {
+                    for (int j = 0; j < 32; ++j) acc[j] = 0.0f;
                     #pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        const int32_t col = c0 + j;
-                        if (col < p.N) {
-                            OutT* dst = C + static_cast<int64_t>(row) * p.c_rs +
-                                        static_cast<int64_t>(col) * p.c_cs;
-                            float x = v[j];
-                            if (p.beta != 0.0f) x = fmaf(p.beta, load_out<OutT>(dst), x);
-                            *dst = cvt_out<OutT>(x);
+                    for (int h = 0; h < 2; ++h) {
+                        for (int32_t g0 = g_first; g0 <= g_last; g0 += 4) {
+                            float x[4][16];
+                            #pragma unroll
+                            for (int u = 0; u < 4; ++u) {
+                                const int32_t g = g0 + u;
+                                if (g > g_last || g == unit) continue;
+                                const int32_t first_tile =
+                                    static_cast<int32_t>((static_cast<int64_t>(g) * L) / KB);
+                                const float* src = p.partials +
+                                                   (static_cast<int64_t>(g) * p.sk_max_seg +
+                                                    (sg.tile - first_tile)) * BM * BN;
+                                if (p.c_cs == 1) {
+                                    const float4* s4 = reinterpret_cast<const float4*>(
+                                        src + row_in_tile * BN + ch * 32 + h * 16);
+                                    #pragma unroll
+                                    for (int q = 0; q < 4; ++q) {
+                                        const float4 t = __ldcg(s4 + q);
+                                        x[u][4 * q] = t.x;
+                                        x[u][4 * q + 1] = t.y;
+                                        x[u][4 * q + 2] = t.z;
+                                        x[u][4 * q + 3] = t.w;
+                                    }
+                                } else {
+                                    #pragma unroll
+                                    for (int j = 0; j < 16; ++j)
+                                        x[u][j] = __ldcg(src + (ch * 32 + h * 16 + j) * BM + row_in_tile);
+                                }
+                            }
+                            #pragma unroll
+                            for (int u = 0; u < 4; ++u) {
+                                const int32_t g = g0 + u;
+                                if (g > g_last) break;
+                                #pragma unroll
+                                for (int j = 0; j < 16; ++j)
+                                    acc[h * 16 + j] += (g == unit) ? v[h * 16 + j] : x[u][j];
+                            }
                         }
                     }
+                    store_chunk<OutT>(p, row, c0, acc);
                 }
             }
             tc_fence_before_sync();
@@ -534,6 +739,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 else mbar_arrive_cluster(map_to_rank(smem_addr(&acc_empty[buf]), 0));
             }
             ++acc_i;
+            if (sg.slot >= 0) {
+                if (!finisher) {
+                    __threadfence();                       // this thread's slot stores
+                    epilogue_bar_sync();
+                    if (warp == 2 && lane == 0) atomicAdd(p.tile_counters + 2 * sg.tile + 1, 1);
+                }
+                epilogue_bar_sync();                       // role_flag is reused by the next tile
+            }
         }
     }
 
@@ -544,53 +757,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 1) {
         if constexpr (CG == 1) tmem_dealloc(tmem_base, kTmemCols);
         else tmem_dealloc_pair(tmem_base, kTmemCols);
-    }
-}
-
-// Stream-K fixup: for every tile that was split across CTAs, add its partial
-// slots in increasing CTA order, then apply alpha/beta and the output cast.
-// One thread per (tile, row, 4 columns).
-template <int BM, int BN, typename OutT>
-__global__ void __launch_bounds__(256)
-    streamk_fixup_kernel(const __grid_constant__ TcParams p) {
-    const int64_t per_tile = static_cast<int64_t>(BM) * (BN / 4);
-    const int64_t total = per_tile * p.num_tiles;
-    OutT* C = reinterpret_cast<OutT*>(p.C);
-    const int32_t KB = p.k_blocks, L = p.sk_len;
-    for (int64_t idx = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; idx < total;
-         idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-        const int32_t tile = static_cast<int32_t>(idx / per_tile);
-        const int32_t rem = static_cast<int32_t>(idx - static_cast<int64_t>(tile) * per_tile);
-        const int32_t r = rem / (BN / 4);
-        const int32_t c4 = (rem - r * (BN / 4)) * 4;
-        const int32_t g_first = static_cast<int32_t>((static_cast<int64_t>(tile) * KB) / L);
-        const int32_t g_last = static_cast<int32_t>((static_cast<int64_t>(tile + 1) * KB - 1) / L);
-        if (g_first == g_last) continue;           // stored whole by one CTA
-        int32_t tm, tn;
-        tile_coords(p, tile, tm, tn);
-        const int32_t row = tm * BM + r;
-        if (row >= p.M) continue;
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int32_t g = g_first; g <= g_last; ++g) {
-            const int32_t first_tile = static_cast<int32_t>((static_cast<int64_t>(g) * L) / KB);
-            const int64_t slot = static_cast<int64_t>(g) * p.sk_max_seg + (tile - first_tile);
-            const float4 v = *reinterpret_cast<const float4*>(
-                p.partials + (slot * BM + r) * BN + c4);
-            acc.x += v.x;
-            acc.y += v.y;
-            acc.z += v.z;
-            acc.w += v.w;
-        }
-        const float vals[4] = {acc.x, acc.y, acc.z, acc.w};
-        #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const int32_t col = tn * BN + c4 + e;
-            if (col >= p.N) break;
-            OutT* dst = C + static_cast<int64_t>(row) * p.c_rs + static_cast<int64_t>(col) * p.c_cs;
-            float x = p.alpha * vals[e];
-            if (p.beta != 0.0f) x = fmaf(p.beta, load_out<OutT>(dst), x);
-            *dst = cvt_out<OutT>(x);
-        }
     }
 }
 

@@ -1,6 +1,6 @@
-// kern_inst.cuh -- instantiates the tcgen05 GEMM and its stream-K fixup for one
-// output type (KERN_OUT_T): single-CTA tiles of width 64/128/256 and CTA-pair
-// tiles of width 256, behind plain launchers.
+// kern_inst.cuh -- instantiates the tcgen05 GEMM for one output type
+// (KERN_OUT_T): single-CTA tiles of width 64/128/256 and CTA-pair tiles of
+// width 256, behind a plain launcher.
 #pragma once
 #include <mutex>
 
@@ -73,17 +73,6 @@ cudaError_t GEMM103_CAT(launch_tc_, KERN_SUFFIX)(const TcLaunch& l) {
         case 256: return launch_tc_cfg<1, 256>(l);
         default: return cudaErrorInvalidValue;
     }
-}
-
-cudaError_t GEMM103_CAT(launch_fixup_, KERN_SUFFIX)(const TcLaunch& l, int grid) {
-    if (l.cta_group != 1) return cudaErrorInvalidValue;
-    switch (l.block_n) {
-        case 64: streamk_fixup_kernel<128, 64, KERN_OUT_T><<<grid, 256, 0, l.stream>>>(l.p); break;
-        case 128: streamk_fixup_kernel<128, 128, KERN_OUT_T><<<grid, 256, 0, l.stream>>>(l.p); break;
-        case 256: streamk_fixup_kernel<128, 256, KERN_OUT_T><<<grid, 256, 0, l.stream>>>(l.p); break;
-        default: return cudaErrorInvalidValue;
-    }
-    return cudaGetLastError();
 }
 
 }  // namespace gemm103

@@ -23,8 +23,5 @@ struct TcLaunch {
 cudaError_t launch_tc_f32(const TcLaunch& l);
 cudaError_t launch_tc_f16(const TcLaunch& l);
 cudaError_t launch_tc_bf16(const TcLaunch& l);
-cudaError_t launch_fixup_f32(const TcLaunch& l, int grid);
-cudaError_t launch_fixup_f16(const TcLaunch& l, int grid);
-cudaError_t launch_fixup_bf16(const TcLaunch& l, int grid);
 
 }  // namespace gemm103
