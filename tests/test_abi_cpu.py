@@ -166,10 +166,22 @@ def test_stream_k_schedule_covers_every_block_once(shape, sms):
     w = workloads.Workload("s", M, N, K, "N", "T", DT_BF16, DT_BF16, 1.0, 0.0, "U", "U")
     p = plan(w, num_sms=sms)
     if p["sk_len"] == 0:
-        assert p["num_tiles"] >= sms or p["k_blocks"] < 4
-        return
-    assert p["grid"] <= sms
+        return                      # data-parallel plan: nothing to replay
+    assert p["grid"] <= sms and p["num_tiles"] < sms
     simulate_stream_k(p)
+
+
+def test_stream_k_only_for_skinny_or_tile_starved_long_k():
+    def P(M, N, K, sms=152):
+        w = workloads.Workload("s", M, N, K, "N", "T", DT_BF16, DT_BF16, 1.0, 0.0, "U", "U")
+        return plan(w, num_sms=sms)
+    assert P(64, 16384, 8192)["sk_len"] > 0          # swapped weight-streaming GEMM
+    assert P(257, 129, 4096)["sk_len"] > 0           # 6 tiles, 64 k-blocks each
+    assert P(1, 1, 100000)["sk_len"] > 0
+    for shape in [(1024, 1024, 1024), (1000, 1023, 777), (256, 256, 256), (300, 520, 1000)]:
+        assert P(*shape)["sk_len"] == 0, shape
+    assert P(1024, 1024, 1024)["block_n"] == 64      # 128 tiles of 128 x 64
+    assert P(256, 256, 256)["num_tiles"] >= 4
 
 
 def test_create_fails_cleanly_without_gpu():
