@@ -14,9 +14,19 @@ namespace gemm103 {
 template <int CG, int BN>
 static cudaError_t launch_tc_cfg(const TcLaunch& l) {
     auto kern = gemm_tc_kernel<CG, BN, KERN_OUT_T>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(l.smem_bytes));
-    if (e != cudaSuccess) return e;
+    {
+        // The dynamic shared-memory limit is raised once per size (a host
+        // call worth avoiding on every launch of a microsecond-scale GEMM).
+        static std::mutex mu;
+        static size_t raised_to = 0;
+        std::lock_guard<std::mutex> g(mu);
+        if (l.smem_bytes > raised_to) {
+            cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 static_cast<int>(l.smem_bytes));
+            if (e != cudaSuccess) return e;
+            raised_to = l.smem_bytes;
+        }
+    }
     if constexpr (CG == 1) {
         kern<<<l.grid, kThreads, l.smem_bytes, l.stream>>>(l.tmA, l.tmB, l.p);
         return cudaGetLastError();
