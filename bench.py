@@ -209,7 +209,7 @@ class OracleSampler:
             inp = workloads.make_inputs(w)
             codes = (workloads.as_codes(inp.A), workloads.as_codes(inp.B),
                      None if inp.C is None else workloads.as_codes(inp.C))
-            pos = (rng.integers(0, w.M, 1 << 16), rng.integers(0, w.N, 1 << 16))
+            pos = (rng.integers(0, w.M, 1 << 20), rng.integers(0, w.N, 1 << 20))
             self.inputs.append((inp, codes, pos))
 
     def run(self, n):
@@ -246,14 +246,27 @@ class OracleSampler:
     def calibrate(self, target_s):
         """Sample size (per GEMM) that takes about target_s seconds."""
         n, t = 64, 0.0
-        while n < (1 << 16):
+        while n < (1 << 20):
             _, t = self.run(n)
             if t >= target_s / 8:
                 break
-            n = min(n * 4, 1 << 16)
+            n = min(n * 4, 1 << 20)
         if t > 0:
-            n = int(min(1 << 16, max(16, n * target_s / t)))
+            n = int(min(1 << 20, max(16, n * target_s / t)))
         return n
+
+    def calibrate_rows(self, target_s):
+        """Row count for run_rows that takes about target_s seconds."""
+        max_rows = min(w.M for w in self.ws)
+        rows, t = 4, 0.0
+        while rows < max_rows:
+            _, t = self.run_rows(rows)
+            if t >= target_s / 4:
+                break
+            rows = min(rows * 4, max_rows)
+        if t > 0 and rows < max_rows:
+            rows = int(min(max_rows, max(4, rows * target_s / t)))
+        return rows
 
 
 # ------------------------------------------------------------------ GPU arm
@@ -371,7 +384,7 @@ def run_ours(args):
         smp = OracleSampler(ws)
         n = smp.calibrate(12.0)
         f, t = smp.run(n)
-        rows = 16
+        rows = smp.calibrate_rows(8.0)
         fr, tr = smp.run_rows(rows)
         cpu = {"value": round(f / t / 1e12, 6), "unit": "TFLOP/s", "cores": smp.threads,
                "kind": "oracle",
