@@ -114,6 +114,21 @@ gemm_status_t gemm_sync(gemm_handle_t h, gemm_stream_t stream);
  * NULL is accepted (no-op). */
 gemm_status_t gemm_destroy(gemm_handle_t h);
 
+/*
+ * gemm_debug_set: test hook for the failure path (no counterpart on the
+ * pages).  wait_limit_ns bounds every in-kernel wait of later calls on this
+ * handle (0 restores the default of 2 s).  With flags =
+ * GEMM_DEBUG_SKIP_FIRST_LOAD, the first CTA's producer arms its first
+ * pipeline slot but issues no load into it: the MMA's bounded wait on that slot
+ * runs out, the kernel records GEMM_ERR_DEVICE_TIMEOUT and winds down (no trap,
+ * no fault; the CUDA context stays usable), and the next gemm_sync or gemm_run
+ * on the handle reports it.  The results of such a call are undefined.
+ * flags = 0 restores normal operation.  Returns INVALID_VALUE for a NULL
+ * handle or an unknown flag.
+ */
+#define GEMM_DEBUG_SKIP_FIRST_LOAD 1u
+gemm_status_t gemm_debug_set(gemm_handle_t h, uint32_t flags, uint64_t wait_limit_ns);
+
 /* A static, human-readable name for a status code. */
 const char* gemm_status_string(gemm_status_t s);
 

@@ -64,6 +64,8 @@ def _load():
     lib.gemm_run.argtypes = [vp] + run_args + [vp]
     lib.gemm_run_noalloc.restype = ctypes.c_int
     lib.gemm_run_noalloc.argtypes = run_args + [vp]
+    lib.gemm_debug_set.restype = ctypes.c_int
+    lib.gemm_debug_set.argtypes = [vp, ctypes.c_uint32, ctypes.c_uint64]
     lib.gemm_sync.restype = ctypes.c_int
     lib.gemm_sync.argtypes = [vp, vp]
     lib.gemm_destroy.restype = ctypes.c_int
@@ -99,6 +101,14 @@ def gemm_create() -> int:
 
 def gemm_destroy(h) -> int:
     return lib.gemm_destroy(h)
+
+
+GEMM_DEBUG_SKIP_FIRST_LOAD = 1
+
+
+def gemm_debug_set(h, flags: int, wait_limit_ns: int = 0) -> int:
+    """Test hook of the failure path (see include/gemm_sm103.h)."""
+    return lib.gemm_debug_set(h, flags, wait_limit_ns)
 
 
 def gemm_sync(h, stream=0) -> int:

@@ -231,6 +231,8 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
 }  // namespace
 
 struct gemm_ctx {
+    uint32_t debug_flags;     // test hook (gemm_debug_set)
+    uint64_t wait_limit_ns;   // 0: the default bound
     int device;
     int num_sms;
     int smem_optin;
@@ -314,7 +316,8 @@ int grid_for(int64_t elems_per_thread_unit, int num_sms) {
 // clear_counters the counters are zeroed on the stream first.
 gemm_status_t enqueue_plan(const Plan& pl, EncodeTiledFn encode, int num_sms, uint8_t* ws,
                            int* err_dev, float alpha, float beta, void* C, gemm_dtypes_t dt,
-                           cudaStream_t stream, bool clear_counters) {
+                           cudaStream_t stream, bool clear_counters, uint32_t debug_flags = 0,
+                           uint64_t wait_limit_ns = 0) {
     int* counters = reinterpret_cast<int*>(ws);
     if (clear_counters && pl.sk_len > 0 &&
         cudaMemsetAsync(counters, 0, kWsHeaderBytes, stream) != cudaSuccess) {
@@ -384,6 +387,8 @@ gemm_status_t enqueue_plan(const Plan& pl, EncodeTiledFn encode, int num_sms, ui
     // by every CTA.
     p.a_stream_once = pl.pub.swap_ab ? 1 : 0;
     p.b_stream_once = 0;
+    p.wait_limit_ns = wait_limit_ns ? wait_limit_ns : kWaitTimeoutNs;
+    p.debug_flags = debug_flags;
     l.grid = pl.pub.grid;
     l.cta_group = cg;
     l.block_n = bn;
@@ -496,6 +501,14 @@ gemm_status_t gemm_create(gemm_handle_t* out) {
     return GEMM_OK;
 }
 
+gemm_status_t gemm_debug_set(gemm_handle_t h, uint32_t flags, uint64_t wait_limit_ns) {
+    if (h == nullptr || (flags & ~static_cast<uint32_t>(GEMM_DEBUG_SKIP_FIRST_LOAD)) != 0)
+        return GEMM_ERR_INVALID_VALUE;
+    h->debug_flags = flags;
+    h->wait_limit_ns = wait_limit_ns;
+    return GEMM_OK;
+}
+
 gemm_status_t gemm_destroy(gemm_handle_t h) {
     if (h == nullptr) return GEMM_OK;
     cudaDeviceSynchronize();
@@ -536,7 +549,7 @@ gemm_status_t gemm_run(gemm_handle_t h, char transA, char transB, int64_t M, int
     st = ensure_workspace(h, static_cast<size_t>(pl.pub.workspace_bytes));
     if (st != GEMM_OK) return st;
     return enqueue_plan(pl, h->encode, h->num_sms, static_cast<uint8_t*>(h->ws), h->err_dev, alpha,
-                        beta, C, dt, stream, false);
+                        beta, C, dt, stream, false, h->debug_flags, h->wait_limit_ns);
 }
 
 }  // extern "C"

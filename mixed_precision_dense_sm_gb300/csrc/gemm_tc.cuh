@@ -86,7 +86,13 @@ struct TcParams {
     int* err;                   // device-visible error word (0 = ok)
     int32_t a_stream_once;      // 1: A is read once (evict-first in L2), 0: reused
     int32_t b_stream_once;
+    uint64_t wait_limit_ns;     // bound on every in-kernel wait
+    uint32_t debug_flags;       // test hook (kDebugSkipFirstLoad), 0 in normal use
 };
+
+// Test hook: CTA 0's producer arms its first pipeline slot but issues no load
+// into it, so the MMA's bounded wait on that slot runs out.
+constexpr uint32_t kDebugSkipFirstLoad = 1u;
 
 struct Segment {
     int32_t tile, kb0, kb1;
@@ -158,7 +164,7 @@ __device__ __forceinline__ void record_error(const TcParams& p, int code, volati
 
 // Bounded wait that also gives up early once another role has aborted.
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity,
-                                              volatile int* abort_flag) {
+                                              volatile int* abort_flag, uint64_t limit_ns) {
     const uint32_t a = smem_addr(bar);
     if (mbar_try_wait(a, parity)) return true;
     const uint64_t t0 = global_timer_ns();
@@ -166,7 +172,7 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity,
         if (mbar_try_wait(a, parity)) return true;
         if ((i & 63u) == 0) {
             if (*abort_flag) return false;
-            if (global_timer_ns() - t0 > kWaitTimeoutNs) return false;
+            if (global_timer_ns() - t0 > limit_ns) return false;
         }
     }
 }
@@ -230,9 +236,10 @@ __device__ __forceinline__ void store_row32_vec(OutT* dst, const float (&v)[32],
 // peer's TMEM reads are ordered before the MMAs that overwrite them.  Barriers
 // completed by TMA transactions or tcgen05.commit are waited on at CTA scope.
 template <int CG>
-__device__ __forceinline__ bool wait_role(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
+__device__ __forceinline__ bool wait_role(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                          uint64_t limit_ns) {
     if constexpr (CG == 1) {
-        return wait_or_abort(bar, parity, abort_flag);
+        return wait_or_abort(bar, parity, abort_flag, limit_ns);
     } else {
         const uint32_t a = smem_addr(bar);
         if (mbar_try_wait_cluster(a, parity)) return true;
@@ -241,7 +248,7 @@ __device__ __forceinline__ bool wait_role(uint64_t* bar, uint32_t parity, volati
             if (mbar_try_wait_cluster(a, parity)) return true;
             if ((i & 63u) == 0) {
                 if (*abort_flag) return false;
-                if (global_timer_ns() - t0 > kWaitTimeoutNs) return false;
+                if (global_timer_ns() - t0 > limit_ns) return false;
             }
         }
     }
@@ -286,7 +293,8 @@ __device__ __forceinline__ void store_chunk(const TcParams& p, int32_t row, int3
 }
 
 // Spin (bounded) until the global counter reaches `target`.
-__device__ __forceinline__ bool wait_counter(const int* ctr, int target, volatile int* abort_flag) {
+__device__ __forceinline__ bool wait_counter(const int* ctr, int target, volatile int* abort_flag,
+                                             uint64_t limit_ns) {
     const uint64_t t0 = global_timer_ns();
     for (uint32_t i = 0;; ++i) {
         int v;
@@ -294,7 +302,7 @@ __device__ __forceinline__ bool wait_counter(const int* ctr, int target, volatil
         if (v >= target) return true;
         if ((i & 63u) == 63u) {
             if (*abort_flag) return false;
-            if (global_timer_ns() - t0 > kWaitTimeoutNs) return false;
+            if (global_timer_ns() - t0 > limit_ns) return false;
         }
         __nanosleep(32);
     }
@@ -429,7 +437,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t bytes = (CG == 1) ? tile_bytes(0)
                                                  : (rank == 0 ? tile_bytes(0) + tile_bytes(1) : 0u);
                 for (int32_t kb = sg.kb0; kb < sg.kb1; ++kb) {
-                    if (!wait_or_abort(&empty[stage], phase ^ 1u, &abort_flag)) {
+                    if (!wait_or_abort(&empty[stage], phase ^ 1u, &abort_flag, p.wait_limit_ns)) {
                         record_error(p, kErrTimeoutProducer, &abort_flag);
                         ok = false;
                         break;
@@ -437,6 +445,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                     uint8_t* sa = smem + stage * kStageBytes;
                     uint8_t* sb = sa + kATileBytes;
                     const int32_t k0 = kb * kBlockK;
+                    if ((p.debug_flags & kDebugSkipFirstLoad) && armed == 0 && blockIdx.x == 0) {
+                        // test hook: arm the slot, load nothing into it
+                        if (rank == 0) mbar_arrive_expect_tx(&full[stage], bytes > 0 ? bytes : 16u);
+                        ++armed;
+                        if (++stage == static_cast<uint32_t>(S)) {
+                            stage = 0;
+                            phase ^= 1u;
+                        }
+                        continue;
+                    }
                     if constexpr (CG == 1) {
                         mbar_arrive_expect_tx(&full[stage], bytes);
                         if (p.a_mn_major) {
@@ -486,10 +504,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int s = 0; s < S; ++s) {
                     if (armed <= static_cast<uint32_t>(s)) break;
                     const uint32_t last = ((armed - 1 - s) / S) * S + s;   // last arming of slot s
-                    if (!mbar_wait(&full[s], (last / S) & 1u)) {
+                    if (!mbar_wait(&full[s], (last / S) & 1u, p.wait_limit_ns))
                         record_error(p, kErrTimeoutProducer, &abort_flag);
-                        break;
-                    }
                 }
             }
         }
@@ -507,14 +523,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t smem_base = smem_addr(smem);
             while (ok && it.next(p, sg)) {
                 const uint32_t buf = acc_i & 1u;
-                if (!wait_role<CG>(&acc_empty[buf], ((acc_i >> 1) & 1u) ^ 1u, &abort_flag)) {
+                if (!wait_role<CG>(&acc_empty[buf], ((acc_i >> 1) & 1u) ^ 1u, &abort_flag, p.wait_limit_ns)) {
                     record_error(p, kErrTimeoutMma, &abort_flag);
                     break;
                 }
                 tc_fence_after_sync();
                 const uint32_t d_tmem = tmem_base + buf * BN;
                 for (int32_t kb = sg.kb0; kb < sg.kb1; ++kb) {
-                    if (!wait_or_abort(&full[stage], phase, &abort_flag)) {
+                    if (!wait_or_abort(&full[stage], phase, &abort_flag, p.wait_limit_ns)) {
                         record_error(p, kErrTimeoutMma, &abort_flag);
                         ok = false;
                         break;
@@ -545,7 +561,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // Wind-down: every MMA issued has completed before TMEM is freed.
             if constexpr (CG == 1) tc_commit(drain);
             else tc_commit_pair(drain);
-            if (!mbar_wait(drain, 0)) record_error(p, kErrTimeoutMma, &abort_flag);
+            if (!mbar_wait(drain, 0, p.wait_limit_ns)) record_error(p, kErrTimeoutMma, &abort_flag);
         }
     } else {
         // --------------------------------------------------------- epilogue
@@ -557,7 +573,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         Segment sg;
         while (it.next(p, sg)) {
             const uint32_t buf = acc_i & 1u;
-            bool ok = wait_or_abort(&acc_full[buf], (acc_i >> 1) & 1u, &abort_flag);
+            bool ok = wait_or_abort(&acc_full[buf], (acc_i >> 1) & 1u, &abort_flag, p.wait_limit_ns);
             if (p.stream_k) ok = epilogue_all(ok);        // stream-K uses named barriers below
             if (!ok) {
                 record_error(p, kErrTimeoutEpilogue, &abort_flag);
@@ -597,7 +613,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (finisher) {
                     epilogue_bar_sync();                   // everyone has read role_flag
                     if (warp == 2 && lane == 0) {
-                        const bool ok_w = wait_counter(arrive + 1, g_last - g_first, &abort_flag);
+                        const bool ok_w = wait_counter(arrive + 1, g_last - g_first, &abort_flag, p.wait_limit_ns);
                         if (ok_w) arrive[1] = 0;
                         else record_error(p, kErrTimeoutEpilogue, &abort_flag);
                     }

@@ -14,8 +14,8 @@
 
 namespace gemm103 {
 
-// Longest any single in-kernel wait may take before the kernel gives up,
-// records a timeout and winds down (nanoseconds of %globaltimer).
+// Default longest time any single in-kernel wait may take before the kernel
+// gives up, records a timeout and winds down (nanoseconds of %globaltimer).
 constexpr uint64_t kWaitTimeoutNs = 2000000000ull;   // 2 s
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
@@ -65,14 +65,14 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Wait until the phase with the given parity has completed.  Bounded: returns
-// false after kWaitTimeoutNs instead of spinning forever.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+// false after limit_ns instead of spinning forever.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
     const uint32_t a = smem_addr(bar);
     if (mbar_try_wait(a, parity)) return true;
     const uint64_t t0 = global_timer_ns();
     for (uint32_t i = 1;; ++i) {
         if (mbar_try_wait(a, parity)) return true;
-        if ((i & 255u) == 0 && global_timer_ns() - t0 > kWaitTimeoutNs) return false;
+        if ((i & 255u) == 0 && global_timer_ns() - t0 > limit_ns) return false;
     }
 }
 

@@ -27,6 +27,12 @@ def test_exports_every_declared_symbol():
         assert hasattr(lib.lib, name)
 
 
+def test_debug_hook_validates_arguments():
+    assert lib.gemm_debug_set(None, 0, 0) == 1
+    assert lib.GEMM_DEBUG_SKIP_FIRST_LOAD == 1
+    assert "gemm_debug_set" in lib.declared_symbols()
+
+
 def test_status_strings():
     for code, name in lib.STATUS.items():
         assert lib.gemm_status_string(code) == name
