@@ -167,12 +167,20 @@ def barrier(world):
 
 
 def max_over_ranks(x: float, world: int) -> float:
+    """The largest of every rank's x (the slowest rank's time decides)."""
     if world == 1:
         return x
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def whole_job_tflops(flops_per_step: float, steps: int, world: int, max_ms: float) -> float:
+    """Replicas: every rank runs the same step, so the job does world x the
+    work in the slowest rank's time."""
+    return world * flops_per_step * steps / (max_ms * 1e-3) / 1e12
 
 
 def workload_list(name: str):
@@ -342,7 +350,7 @@ def run_ours(args):
     ms_total = max_over_ranks(ms_total, world)
     ms_step = ms_total / args.steps
     flops_step = sum(w.flops() for w in ws)
-    value = world * flops_step * args.steps / (ms_total * 1e-3) / 1e12
+    value = whole_job_tflops(flops_step, args.steps, world, ms_total)
 
     # dominant kernel: the main GEMM launch of each call
     launch_ms = [statistics.fmean(ev[k][i][0].elapsed_time(ev[k][i][1])
