@@ -91,6 +91,13 @@ class Oracle:
         lib.oracle_round_output.argtypes = [ctypes.c_int, i64, dp, vp]
         lib.oracle_max_threads.restype = ctypes.c_int
         lib.oracle_max_threads.argtypes = []
+        lib.oracle_activation.restype = ctypes.c_double
+        lib.oracle_activation.argtypes = [ctypes.c_int, ctypes.c_double]
+        ep = [vp, ctypes.c_int, ctypes.c_int]
+        lib.oracle_gemm_ex.restype = ctypes.c_int
+        lib.oracle_gemm_ex.argtypes = common + ep + [dp, dp, ctypes.c_int]
+        lib.oracle_gemm_sampled_ex.restype = ctypes.c_int
+        lib.oracle_gemm_sampled_ex.argtypes = common + ep + [i64, vp, vp, dp, dp, ctypes.c_int]
         self.lib = lib
         self.path = path
 
@@ -155,6 +162,55 @@ class Oracle:
         if st != 0:
             raise ValueError(f"oracle_gemm_sampled failed ({st})")
         return R, S
+
+
+ACT_NONE, ACT_RELU, ACT_GELU, ACT_SILU = 0, 1, 2, 3
+
+
+def _oracle_ex_methods():
+    def activation(self, act: int, x: float) -> float:
+        return float(self.lib.oracle_activation(act, float(x)))
+
+    def gemm_ex(self, transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc,
+                ab_dtype, c_dtype, bias=None, bias_dtype=F32, act=ACT_NONE, nthreads: int = 0):
+        """Fused-epilogue oracle: act(alpha*AB + beta*C + bias[col]).  bias is
+        a length-N array of codes (uint16) or float32, or None."""
+        A, B, C = _prep(A), _prep(B), _prep(C, c=True)
+        bias = _prep(bias, c=True)
+        R = np.empty((M, N), dtype=np.float64)
+        S = np.empty((M, N), dtype=np.float64)
+        st = self.lib.oracle_gemm_ex(transA.encode(), transB.encode(), M, N, K, float(alpha),
+                                     _ptr(A), lda, _ptr(B), ldb, float(beta), _ptr(C), ldc,
+                                     ab_dtype, c_dtype, _ptr(bias), bias_dtype, act,
+                                     R.ctypes.data, S.ctypes.data, nthreads)
+        if st != 0:
+            raise ValueError(f"oracle_gemm_ex failed ({st})")
+        return R, S
+
+    def gemm_sampled_ex(self, transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc,
+                        ab_dtype, c_dtype, rows, cols, bias=None, bias_dtype=F32,
+                        act=ACT_NONE, nthreads: int = 0):
+        A, B, C = _prep(A), _prep(B), _prep(C, c=True)
+        bias = _prep(bias, c=True)
+        rows = np.ascontiguousarray(rows, dtype=np.int64)
+        cols = np.ascontiguousarray(cols, dtype=np.int64)
+        R = np.empty(rows.shape, dtype=np.float64)
+        S = np.empty(rows.shape, dtype=np.float64)
+        st = self.lib.oracle_gemm_sampled_ex(
+            transA.encode(), transB.encode(), M, N, K, float(alpha),
+            _ptr(A), lda, _ptr(B), ldb, float(beta), _ptr(C), ldc, ab_dtype, c_dtype,
+            _ptr(bias), bias_dtype, act, rows.size, rows.ctypes.data, cols.ctypes.data,
+            R.ctypes.data, S.ctypes.data, nthreads)
+        if st != 0:
+            raise ValueError(f"oracle_gemm_sampled_ex failed ({st})")
+        return R, S
+
+    Oracle.activation = activation
+    Oracle.gemm_ex = gemm_ex
+    Oracle.gemm_sampled_ex = gemm_sampled_ex
+
+
+_oracle_ex_methods()
 
 
 def get() -> Oracle:

@@ -322,3 +322,78 @@ int oracle_max_threads(void) {
     return 1;
 #endif
 }
+
+/* --------------------------------------------------- fused epilogue oracle */
+
+/*
+ * Fused epilogue ("keep the GEMM mainloop, replace the epilogue": CATLASS
+ * page, section 5.2, which names residual add and activations next to the
+ * linear layer; the page gives no formula).  Read as the usual linear-layer
+ * form
+ *     r_ij = act(alpha * sum_k op(A)_ik op(B)_kj + beta * C_ij + bias_j)
+ * with act one of: none, ReLU (x if x > 0, else 0; NaN stays NaN),
+ * GELU in its erf form x * Phi(x) = 0.5 x (1 + erf(x / sqrt 2)), and
+ * SiLU x / (1 + exp(-x)).  bias (length N, indexed by the output column) may
+ * be NULL.  The sums are the plain oracle's; the epilogue is applied to each
+ * binary64 result.
+ */
+enum { OR_ACT_NONE = 0, OR_ACT_RELU = 1, OR_ACT_GELU = 2, OR_ACT_SILU = 3 };
+
+double oracle_activation(int act, double x) {
+    switch (act) {
+        case OR_ACT_NONE: return x;
+        case OR_ACT_RELU: return isnan(x) ? x : (x > 0.0 ? x : 0.0);
+        case OR_ACT_GELU: return 0.5 * x * (1.0 + erf(x / sqrt(2.0)));
+        case OR_ACT_SILU: return x / (1.0 + exp(-x));
+    }
+    return NAN;
+}
+
+static int check_epilogue(const void* bias, int bias_dtype, int act) {
+    if (act < OR_ACT_NONE || act > OR_ACT_SILU) return OR_BAD_ARG;
+    if (bias != NULL && bias_dtype != OR_F16 && bias_dtype != OR_BF16 && bias_dtype != OR_F32)
+        return OR_BAD_ARG;
+    return OR_OK;
+}
+
+int oracle_gemm_ex(char transA, char transB, int64_t M, int64_t N, int64_t K,
+                   float alpha, const void* A, int64_t lda,
+                   const void* B, int64_t ldb,
+                   float beta, const void* C, int64_t ldc,
+                   int ab_dtype, int c_dtype,
+                   const void* bias, int bias_dtype, int act,
+                   double* R, double* S, int nthreads) {
+    int st = check_epilogue(bias, bias_dtype, act);
+    if (st != OR_OK) return st;
+    st = oracle_gemm(transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc,
+                     ab_dtype, c_dtype, R, S, nthreads);
+    if (st != OR_OK) return st;
+    for (int64_t i = 0; i < M; ++i)
+        for (int64_t j = 0; j < N; ++j) {
+            double x = R[i * N + j];
+            if (bias != NULL) x = x + decode_c(bias_dtype, bias, j);
+            R[i * N + j] = oracle_activation(act, x);
+        }
+    return OR_OK;
+}
+
+int oracle_gemm_sampled_ex(char transA, char transB, int64_t M, int64_t N, int64_t K,
+                           float alpha, const void* A, int64_t lda,
+                           const void* B, int64_t ldb,
+                           float beta, const void* C, int64_t ldc,
+                           int ab_dtype, int c_dtype,
+                           const void* bias, int bias_dtype, int act,
+                           int64_t nsamp, const int64_t* rows, const int64_t* cols,
+                           double* R, double* S, int nthreads) {
+    int st = check_epilogue(bias, bias_dtype, act);
+    if (st != OR_OK) return st;
+    st = oracle_gemm_sampled(transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc,
+                             ab_dtype, c_dtype, nsamp, rows, cols, R, S, nthreads);
+    if (st != OR_OK) return st;
+    for (int64_t s = 0; s < nsamp; ++s) {
+        double x = R[s];
+        if (bias != NULL) x = x + decode_c(bias_dtype, bias, cols[s]);
+        R[s] = oracle_activation(act, x);
+    }
+    return OR_OK;
+}

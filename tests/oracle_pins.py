@@ -374,10 +374,101 @@ def pin_threads_deterministic(o):
     assert (R1 == R4).all() and (S1 == S4).all()
 
 
+# ----------------------------------------------------------- fused epilogue
+
+ACT_NONE, ACT_RELU, ACT_GELU, ACT_SILU = 0, 1, 2, 3
+
+
+def pin_activation_values(o):
+    """GELU = x * Phi(x) and SiLU = x * sigmoid(x) against scipy's own normal
+    CDF and logistic routines; ReLU exactly; the odd-part identities
+    act(x) - act(-x) = x that both GELU and SiLU satisfy."""
+    from scipy.special import expit, ndtr
+    rng = _rng(21)
+    xs = np.concatenate([rng.standard_normal(500) * 4.0, [0.0, 1.0, -1.0, 8.0, -8.0, 30.0, -30.0]])
+    for x in xs:
+        g = o.activation(ACT_GELU, x)
+        assert abs(g - x * ndtr(x)) <= 1e-14 * max(1.0, abs(x)), x
+        s = o.activation(ACT_SILU, x)
+        assert abs(s - x * expit(x)) <= 1e-14 * max(1.0, abs(x)), x
+        assert abs((o.activation(ACT_GELU, x) - o.activation(ACT_GELU, -x)) - x) <= 1e-14 * max(1.0, abs(x))
+        assert abs((o.activation(ACT_SILU, x) - o.activation(ACT_SILU, -x)) - x) <= 1e-14 * max(1.0, abs(x))
+        assert o.activation(ACT_RELU, x) == (x if x > 0 else 0.0)
+        assert o.activation(ACT_NONE, x) == x
+    assert math.isnan(o.activation(ACT_RELU, float("nan")))
+    assert o.activation(ACT_GELU, 0.0) == 0.0 and o.activation(ACT_SILU, 0.0) == 0.0
+
+
+def pin_epilogue_bruteforce(o):
+    """act(alpha*AB + beta*C + bias) on tiny shapes: the GEMM part in exact
+    rationals, the activation by scipy, every transpose pair."""
+    from scipy.special import expit, ndtr
+    ref_act = {ACT_NONE: lambda x: x, ACT_RELU: lambda x: max(x, 0.0),
+               ACT_GELU: lambda x: x * ndtr(x), ACT_SILU: lambda x: x * expit(x)}
+    rng = _rng(22)
+    n = 0
+    for (M, N, K) in [(3, 5, 4), (6, 2, 7), (1, 8, 3)]:
+        for ta in "NT":
+            for tb in "NT":
+                dt = (F16, BF16)[n % 2]
+                act = n % 4
+                a_rows, a_cols = (M, K) if ta == "N" else (K, M)
+                b_rows, b_cols = (K, N) if tb == "N" else (N, K)
+                A = _random_codes(rng, (a_rows, a_cols), dt)
+                B = _random_codes(rng, (b_rows, b_cols), dt)
+                C = rng.standard_normal((M, N)).astype(np.float32)
+                bias = _random_codes(rng, (N,), BF16)
+                alpha, beta = (1.0, -0.5)[n % 2], (0.0, 1.0)[(n // 2) % 2]
+                R, _ = o.gemm_ex(ta, tb, M, N, K, alpha, A, a_cols, B, b_cols, beta, C, N, dt,
+                                 F32, bias, BF16, act)
+                opA = exact.op_matrix(exact.codes_to_float64(A, dt), a_rows, a_cols, ta)
+                opB = exact.op_matrix(exact.codes_to_float64(B, dt), b_rows, b_cols, tb)
+                r_ex, _ = exact.exact_gemm(opA, opB, alpha, beta, C.astype(np.float64))
+                bv = exact.codes_to_float64(bias, BF16)
+                for i in range(M):
+                    for j in range(N):
+                        x = float(r_ex[i][j] + Fraction(float(bv[j])))
+                        want = ref_act[act](x)
+                        assert abs(R[i, j] - want) <= 1e-12 * max(1.0, abs(want)), (i, j, act)
+                n += 1
+
+
+def pin_epilogue_exact_and_sampled(o):
+    """Integer inputs and bias with ReLU are exact; the sampled entry point
+    agrees with the full one element by element; a NULL bias is no bias."""
+    rng = _rng(23)
+    M, N, K = 9, 11, 13
+    A = _to_codes(rng.integers(-4, 5, (M, K)).astype(np.float64), F16)
+    B = _to_codes(rng.integers(-4, 5, (K, N)).astype(np.float64), F16)
+    bias = rng.integers(-20, 21, N).astype(np.float32)
+    R, _ = o.gemm_ex("N", "N", M, N, K, 1.0, A, K, B, N, 0.0, None, N, F16, F32, bias, F32,
+                     ACT_RELU)
+    plain, _ = o.gemm("N", "N", M, N, K, 1.0, A, K, B, N, 0.0, None, N, F16, F32)
+    assert (R == np.maximum(plain + bias[None, :].astype(np.float64), 0.0)).all()
+    R0, _ = o.gemm_ex("N", "N", M, N, K, 1.0, A, K, B, N, 0.0, None, N, F16, F32, None, F32,
+                      ACT_NONE)
+    assert (R0 == plain).all()
+    rows = rng.integers(0, M, 40)
+    cols = rng.integers(0, N, 40)
+    for act in range(4):
+        Rf, _ = o.gemm_ex("N", "N", M, N, K, 0.5, A, K, B, N, 0.0, None, N, F16, F32, bias, F32,
+                          act)
+        Rs, _ = o.gemm_sampled_ex("N", "N", M, N, K, 0.5, A, K, B, N, 0.0, None, N, F16, F32,
+                                  rows, cols, bias, F32, act)
+        assert (Rs == Rf[rows, cols]).all()
+    try:
+        o.gemm_ex("N", "N", M, N, K, 1.0, A, K, B, N, 0.0, None, N, F16, F32, bias, F32, 9)
+    except ValueError:
+        pass
+    else:
+        raise AssertionError("unknown activation accepted")
+
+
 ALL_PINS = [
     pin_decode_exhaustive, pin_page_format_limits, pin_round_ieee_table,
     pin_round_roundtrip_exhaustive, pin_round_midpoints, pin_round_random_exact,
     pin_f32_output, pin_gemm_bruteforce, pin_gemm_integer_exact,
     pin_identity_and_permutation, pin_all_ones, pin_rank1_closed_form, pin_linearity,
     pin_quick_returns, pin_bad_arguments, pin_threads_deterministic,
+    pin_activation_values, pin_epilogue_bruteforce, pin_epilogue_exact_and_sampled,
 ]

@@ -44,6 +44,21 @@ MUTANTS = [
     ("abs_sum_signed", "sabs[j] = sabs[j] + fabs(p);", "sabs[j] = sabs[j] + p;"),
     ("sampled_transB", "decode_in(ab_dtype, B, b_off(transB, k, j, ldb));\n                acc = acc + p;",
      "decode_in(ab_dtype, B, b_off('N', k, j, ldb));\n                acc = acc + p;"),
+    ("epilogue_bias_dropped", "if (bias != NULL) x = x + decode_c(bias_dtype, bias, j);",
+     "if (bias != NULL) x = x + 0.0 * decode_c(bias_dtype, bias, j);"),
+    ("epilogue_bias_by_row", "if (bias != NULL) x = x + decode_c(bias_dtype, bias, j);",
+     "if (bias != NULL) x = x + decode_c(bias_dtype, bias, i);"),
+    ("sampled_bias_by_row", "if (bias != NULL) x = x + decode_c(bias_dtype, bias, cols[s]);",
+     "if (bias != NULL) x = x + decode_c(bias_dtype, bias, rows[s]);"),
+    ("gelu_missing_half", "return 0.5 * x * (1.0 + erf(x / sqrt(2.0)));",
+     "return x * (1.0 + erf(x / sqrt(2.0)));"),
+    ("gelu_wrong_scale", "return 0.5 * x * (1.0 + erf(x / sqrt(2.0)));",
+     "return 0.5 * x * (1.0 + erf(x / 2.0));"),
+    ("silu_sign", "return x / (1.0 + exp(-x));", "return x / (1.0 + exp(x));"),
+    ("relu_leaky", "return isnan(x) ? x : (x > 0.0 ? x : 0.0);",
+     "return isnan(x) ? x : (x > 0.0 ? x : 0.01 * x);"),
+    ("activation_after_bias_skipped", "        R[i * N + j] = oracle_activation(act, x);",
+     "        R[i * N + j] = x;"),
     ("beta_read_when_zero", "if (be != 0.0) r = r + be * decode_c(c_dtype, C, i * ldc + j);\n            acc[j] = r;",
      "r = r + be * decode_c(c_dtype, C, i * ldc + j);\n            acc[j] = r;"),
 ]
