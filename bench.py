@@ -33,6 +33,7 @@ own GPU: replicas, no collective on the data path (weak scaling).
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import os
@@ -287,18 +288,33 @@ def run_ours(args):
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     ws = workload_list(args.workload)
+    if args.epilogue and args.workload != "transformer_layer":
+        raise SystemExit("--epilogue applies to the transformer_layer workload")
     g = lib.Gemm()
     stream = torch.cuda.current_stream()
     sh = stream.cuda_stream
 
     bufs = []
-    for w in ws:
+    epis = []
+    for j, w in enumerate(ws):
+        if args.epilogue:
+            # transformer MLP block: bias on every GEMM, GELU after the
+            # up-projection, the residual added (beta = 1) after the down one
+            w = dataclasses.replace(w, beta=1.0, c_dist="N1") if j == 2 else w
+            ws[j] = w
         inp = workloads.make_inputs(w)
         A, B = inp.A.cuda(), inp.B.cuda()
         cdt = workloads.TORCH_DTYPE[w.c_dtype]
         C = (inp.C.cuda() if inp.C is not None
              else torch.zeros((w.M, inp.ldc), dtype=cdt, device="cuda"))
         bufs.append((w, inp, A, B, C))
+        if args.epilogue:
+            gen = torch.Generator().manual_seed(100 + j)
+            bias = (0.02 * torch.randn(w.N, generator=gen)).to(cdt).cuda()
+            act = lib.ACT_GELU if j == 1 else lib.ACT_NONE
+            epis.append((bias, lib.dtype_code(bias.dtype), act))
+        else:
+            epis.append(None)
     del inp
 
     plans = []
@@ -315,9 +331,16 @@ def run_ours(args):
         for i, (w, inp, A, B, C) in enumerate(bufs):
             if events is not None:
                 events[i][0].record(stream)
-            st = lib.gemm_run(g.h, w.transA, w.transB, w.M, w.N, w.K, w.alpha, A.data_ptr(),
-                              inp.lda, B.data_ptr(), inp.ldb, w.beta, C.data_ptr(), inp.ldc,
-                              (w.ab_dtype, w.ab_dtype, w.c_dtype), sh)
+            if epis[i] is None:
+                st = lib.gemm_run(g.h, w.transA, w.transB, w.M, w.N, w.K, w.alpha, A.data_ptr(),
+                                  inp.lda, B.data_ptr(), inp.ldb, w.beta, C.data_ptr(), inp.ldc,
+                                  (w.ab_dtype, w.ab_dtype, w.c_dtype), sh)
+            else:
+                bias, bdt, act = epis[i]
+                st = lib.gemm_run_ex(g.h, w.transA, w.transB, w.M, w.N, w.K, w.alpha,
+                                     A.data_ptr(), inp.lda, B.data_ptr(), inp.ldb, w.beta,
+                                     C.data_ptr(), inp.ldc, (w.ab_dtype, w.ab_dtype, w.c_dtype),
+                                     bias.data_ptr(), bdt, act, sh)
             if st != 0:
                 raise lib.GemmError(st, "gemm_run")
             if events is not None:
@@ -408,7 +431,9 @@ def run_ours(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": describe(args.workload, ws), "shapes": ws_names,
+        "config": {"workload": describe(args.workload, ws) + (
+                       "; fused epilogues: bias, bias + GELU, bias + residual (beta = 1)"
+                       if args.epilogue else ""), "shapes": ws_names,
                    "l2": "no flush: each step touches "
                          f"{sum(w.algorithmic_bytes() for w in ws) / 1e9:.2f} GB > 129 MB L2",
                    "parallelism": "replicas" if world > 1 else "single GPU",
@@ -541,6 +566,9 @@ def main():
     ap.add_argument("--workload", default="transformer_layer",
                     choices=["transformer_layer"] + list(workloads.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--epilogue", action="store_true",
+                    help="fused epilogues of a transformer MLP block: bias on every GEMM, "
+                         "GELU after the up-projection, residual add after the down-projection")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         ap.error("--warmup must be >= 3")

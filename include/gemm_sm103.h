@@ -104,6 +104,41 @@ gemm_status_t gemm_run(gemm_handle_t h, char transA, char transB,
                        gemm_dtypes_t dt, gemm_stream_t stream);
 
 /*
+ * Fused epilogue ("keep the GEMM mainloop, replace the epilogue", CATLASS page,
+ * section 5.2, read in the usual linear-layer form):
+ *     C = act(alpha * op(A) * op(B) + beta * C + bias[n])
+ * evaluated in FP32 before the single cast to C's type.  bias has N elements
+ * (one per output column n), is read only, and may be NULL.  A residual add
+ * is beta = 1 with the residual in C.
+ */
+typedef enum {
+    GEMM_ACT_NONE = 0,
+    GEMM_ACT_RELU = 1,   /* x > 0 ? x : 0 (NaN stays NaN) */
+    GEMM_ACT_GELU = 2,   /* x * Phi(x) = 0.5 x (1 + erf(x / sqrt 2)) */
+    GEMM_ACT_SILU = 3    /* x / (1 + exp(-x)) */
+} gemm_activation_t;
+
+typedef struct {
+    const void* bias;    /* device pointer to N elements, or NULL */
+    int32_t bias_dtype;  /* GEMM_F16, GEMM_BF16 or GEMM_F32 (ignored if bias is NULL) */
+    int32_t activation;  /* gemm_activation_t */
+} gemm_epilogue_t;
+
+/*
+ * gemm_run_ex: gemm_run with a fused epilogue.  ep == NULL is plain gemm_run.
+ * The quick returns keep their shape: K == 0 or alpha == 0 gives
+ * C = act(beta * C + bias) without reading A or B.  Returns INVALID_VALUE for
+ * an unknown activation or bias type, otherwise as gemm_run.
+ */
+gemm_status_t gemm_run_ex(gemm_handle_t h, char transA, char transB,
+                          int64_t M, int64_t N, int64_t K,
+                          float alpha, const void* A, int64_t lda,
+                          const void* B, int64_t ldb,
+                          float beta, void* C, int64_t ldc,
+                          gemm_dtypes_t dt, const gemm_epilogue_t* ep,
+                          gemm_stream_t stream);
+
+/*
  * gemm_sync: wait for `stream`, then report (and clear) a device-side timeout
  * recorded by any kernel of this handle.  Returns LAUNCH if the stream itself
  * reports an error.

@@ -7,7 +7,8 @@ no fallback implementation.
 
 The entry points mirror include/gemm_sm103.h one to one:
 ``gemm_create``, ``gemm_run``, ``gemm_sync``, ``gemm_destroy``,
-``gemm_status_string``, ``gemm_check_args``, ``gemm_plan_query`` and
+``gemm_status_string``, ``gemm_check_args``, ``gemm_plan_query``,
+``gemm_run_ex`` (fused bias/activation epilogue), ``gemm_debug_set`` and
 ``gemm_run_noalloc``.
 ``Gemm`` wraps a handle and adds ``__call__`` for torch tensors.
 """
@@ -36,6 +37,16 @@ class Dtypes(ctypes.Structure):
     _fields_ = [("a", ctypes.c_int32), ("b", ctypes.c_int32), ("c", ctypes.c_int32)]
 
 
+class Epilogue(ctypes.Structure):
+    _fields_ = [("bias", ctypes.c_void_p), ("bias_dtype", ctypes.c_int32),
+                ("activation", ctypes.c_int32)]
+
+
+ACT_NONE, ACT_RELU, ACT_GELU, ACT_SILU = 0, 1, 2, 3
+ACTIVATIONS = {None: ACT_NONE, "none": ACT_NONE, "relu": ACT_RELU, "gelu": ACT_GELU,
+               "silu": ACT_SILU}
+
+
 class Plan(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "path", "block_m", "block_n", "block_k", "stages", "split_k", "grid", "num_tiles",
@@ -62,6 +73,8 @@ def _load():
     lib.gemm_create.argtypes = [ctypes.POINTER(vp)]
     lib.gemm_run.restype = ctypes.c_int
     lib.gemm_run.argtypes = [vp] + run_args + [vp]
+    lib.gemm_run_ex.restype = ctypes.c_int
+    lib.gemm_run_ex.argtypes = [vp] + run_args + [ctypes.POINTER(Epilogue), vp]
     lib.gemm_run_noalloc.restype = ctypes.c_int
     lib.gemm_run_noalloc.argtypes = run_args + [vp]
     lib.gemm_debug_set.restype = ctypes.c_int
@@ -122,6 +135,15 @@ def gemm_run(h, transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc,
     value.  Returns the gemm_status_t code."""
     return lib.gemm_run(h, _tr(transA), _tr(transB), M, N, K, float(alpha), A, lda, B, ldb,
                         float(beta), C, ldc, Dtypes(*dtypes), stream)
+
+
+def gemm_run_ex(h, transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, dtypes,
+                bias=0, bias_dtype=GEMM_F32, act=ACT_NONE, stream=0) -> int:
+    """Raw C-ABI call with a fused epilogue: act(alpha*AB + beta*C + bias[n]).
+    bias is a device address (0 for none)."""
+    ep = Epilogue(bias or None, bias_dtype, act)
+    return lib.gemm_run_ex(h, _tr(transA), _tr(transB), M, N, K, float(alpha), A, lda, B, ldb,
+                           float(beta), C, ldc, Dtypes(*dtypes), ctypes.byref(ep), stream)
 
 
 def gemm_run_noalloc(transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc,
@@ -191,7 +213,7 @@ class Gemm:
             pass
 
     def __call__(self, A, B, C, transA="N", transB="N", alpha=1.0, beta=0.0,
-                 M=None, N=None, K=None, stream=None):
+                 M=None, N=None, K=None, stream=None, bias=None, act=None):
         import torch
         if stream is None:
             stream = torch.cuda.current_stream().cuda_stream
@@ -205,8 +227,15 @@ class Gemm:
         if K is None:
             K = A.shape[1] if transA in "Nn" else A.shape[0]
         dts = (dtype_code(A.dtype), dtype_code(B.dtype), dtype_code(C.dtype))
-        st = gemm_run(self.h, transA, transB, M, N, K, alpha, A.data_ptr(), A.stride(0),
-                      B.data_ptr(), B.stride(0), beta, C.data_ptr(), C.stride(0), dts, stream)
+        if bias is None and act is None:
+            st = gemm_run(self.h, transA, transB, M, N, K, alpha, A.data_ptr(), A.stride(0),
+                          B.data_ptr(), B.stride(0), beta, C.data_ptr(), C.stride(0), dts, stream)
+        else:
+            st = gemm_run_ex(self.h, transA, transB, M, N, K, alpha, A.data_ptr(), A.stride(0),
+                             B.data_ptr(), B.stride(0), beta, C.data_ptr(), C.stride(0), dts,
+                             bias.data_ptr() if bias is not None else 0,
+                             dtype_code(bias.dtype) if bias is not None else GEMM_F32,
+                             ACTIVATIONS[act] if not isinstance(act, int) else act, stream)
         if st != 0:
             raise GemmError(st, "gemm_run")
         return C

@@ -317,7 +317,7 @@ int grid_for(int64_t elems_per_thread_unit, int num_sms) {
 gemm_status_t enqueue_plan(const Plan& pl, EncodeTiledFn encode, int num_sms, uint8_t* ws,
                            int* err_dev, float alpha, float beta, void* C, gemm_dtypes_t dt,
                            cudaStream_t stream, bool clear_counters, uint32_t debug_flags = 0,
-                           uint64_t wait_limit_ns = 0) {
+                           uint64_t wait_limit_ns = 0, const gemm_epilogue_t* ep = nullptr) {
     int* counters = reinterpret_cast<int*>(ws);
     if (clear_counters && pl.sk_len > 0 &&
         cudaMemsetAsync(counters, 0, kWsHeaderBytes, stream) != cudaSuccess) {
@@ -389,6 +389,10 @@ gemm_status_t enqueue_plan(const Plan& pl, EncodeTiledFn encode, int num_sms, ui
     p.b_stream_once = 0;
     p.wait_limit_ns = wait_limit_ns ? wait_limit_ns : kWaitTimeoutNs;
     p.debug_flags = debug_flags;
+    p.bias = ep ? ep->bias : nullptr;
+    p.bias_dtype = (ep && ep->bias) ? ep->bias_dtype : GEMM_F32;
+    p.bias_on_rows = pl.pub.swap_ab ? 1 : 0;      // swapped: C columns are D' rows
+    p.act = ep ? ep->activation : GEMM_ACT_NONE;
     l.grid = pl.pub.grid;
     l.cta_group = cg;
     l.block_n = bn;
@@ -407,16 +411,31 @@ gemm_status_t enqueue_plan(const Plan& pl, EncodeTiledFn encode, int num_sms, ui
 }
 
 gemm_status_t enqueue_scale(int64_t M, int64_t N, void* C, int64_t ldc, float beta,
-                            gemm_dtypes_t dt, int num_sms, cudaStream_t stream) {
+                            gemm_dtypes_t dt, int num_sms, cudaStream_t stream,
+                            const gemm_epilogue_t* ep = nullptr) {
     const int grid = grid_for(M * N, num_sms);
+    const void* bias = ep ? ep->bias : nullptr;
+    const int32_t bdt = (ep && ep->bias) ? ep->bias_dtype : GEMM_F32;
+    const int32_t act = ep ? ep->activation : GEMM_ACT_NONE;
     if (dt.c == GEMM_F32)
-        scale_c_kernel<float><<<grid, 256, 0, stream>>>(static_cast<float*>(C), M, N, ldc, beta);
+        scale_c_kernel<float><<<grid, 256, 0, stream>>>(static_cast<float*>(C), M, N, ldc, beta,
+                                                        bias, bdt, act);
     else if (dt.c == GEMM_F16)
-        scale_c_kernel<__half><<<grid, 256, 0, stream>>>(static_cast<__half*>(C), M, N, ldc, beta);
+        scale_c_kernel<__half><<<grid, 256, 0, stream>>>(static_cast<__half*>(C), M, N, ldc, beta,
+                                                         bias, bdt, act);
     else
-        scale_c_kernel<__nv_bfloat16>
-            <<<grid, 256, 0, stream>>>(static_cast<__nv_bfloat16*>(C), M, N, ldc, beta);
+        scale_c_kernel<__nv_bfloat16><<<grid, 256, 0, stream>>>(
+            static_cast<__nv_bfloat16*>(C), M, N, ldc, beta, bias, bdt, act);
     return cudaGetLastError() == cudaSuccess ? GEMM_OK : GEMM_ERR_LAUNCH;
+}
+
+bool epilogue_ok(const gemm_epilogue_t* ep) {
+    if (ep == nullptr) return true;
+    if (ep->activation < GEMM_ACT_NONE || ep->activation > GEMM_ACT_SILU) return false;
+    if (ep->bias != nullptr && ep->bias_dtype != GEMM_F16 && ep->bias_dtype != GEMM_BF16 &&
+        ep->bias_dtype != GEMM_F32)
+        return false;
+    return true;
 }
 
 }  // namespace
@@ -531,12 +550,14 @@ gemm_status_t gemm_sync(gemm_handle_t h, gemm_stream_t stream) {
     return GEMM_OK;
 }
 
-gemm_status_t gemm_run(gemm_handle_t h, char transA, char transB, int64_t M, int64_t N, int64_t K,
-                       float alpha, const void* A, int64_t lda, const void* B, int64_t ldb,
-                       float beta, void* C, int64_t ldc, gemm_dtypes_t dt, gemm_stream_t stream_) {
+gemm_status_t gemm_run_ex(gemm_handle_t h, char transA, char transB, int64_t M, int64_t N,
+                          int64_t K, float alpha, const void* A, int64_t lda, const void* B,
+                          int64_t ldb, float beta, void* C, int64_t ldc, gemm_dtypes_t dt,
+                          const gemm_epilogue_t* ep, gemm_stream_t stream_) {
     if (h == nullptr) return GEMM_ERR_INVALID_VALUE;
     gemm_status_t st = take_device_error(h);
     if (st != GEMM_OK) return st;
+    if (!epilogue_ok(ep)) return GEMM_ERR_INVALID_VALUE;
     Plan pl;
     st = make_plan(transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, dt, h->num_sms,
                    h->smem_optin, pl);
@@ -545,11 +566,18 @@ gemm_status_t gemm_run(gemm_handle_t h, char transA, char transB, int64_t M, int
 
     if (pl.pub.path == GEMM_PATH_NOOP) return GEMM_OK;
     if (pl.pub.path == GEMM_PATH_SCALE)
-        return enqueue_scale(M, N, C, ldc, beta, dt, h->num_sms, stream);
+        return enqueue_scale(M, N, C, ldc, beta, dt, h->num_sms, stream, ep);
     st = ensure_workspace(h, static_cast<size_t>(pl.pub.workspace_bytes));
     if (st != GEMM_OK) return st;
     return enqueue_plan(pl, h->encode, h->num_sms, static_cast<uint8_t*>(h->ws), h->err_dev, alpha,
-                        beta, C, dt, stream, false, h->debug_flags, h->wait_limit_ns);
+                        beta, C, dt, stream, false, h->debug_flags, h->wait_limit_ns, ep);
+}
+
+gemm_status_t gemm_run(gemm_handle_t h, char transA, char transB, int64_t M, int64_t N, int64_t K,
+                       float alpha, const void* A, int64_t lda, const void* B, int64_t ldb,
+                       float beta, void* C, int64_t ldc, gemm_dtypes_t dt, gemm_stream_t stream) {
+    return gemm_run_ex(h, transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, dt,
+                       nullptr, stream);
 }
 
 }  // extern "C"

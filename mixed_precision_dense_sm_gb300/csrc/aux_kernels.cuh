@@ -6,12 +6,14 @@
 //    is the GB300 form of the pages' "pad to the tile and zero-fill" edge
 //    handling (DeepGEMM page, section 3.4) for operands the caller laid out
 //    with an odd leading dimension.
-//  * scale_c_kernel: C = beta * C for the quick-return cases (K == 0 or
-//    alpha == 0); beta == 0 writes zeros without reading C.
+//  * scale_c_kernel: C = act(beta * C + bias) for the quick-return cases
+//    (K == 0 or alpha == 0); beta == 0 never reads C.
 #pragma once
 #include <cstdint>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+
+#include "epilogue_ops.cuh"
 
 namespace gemm103 {
 
@@ -63,13 +65,16 @@ __device__ __forceinline__ __nv_bfloat16 scale_store<__nv_bfloat16>(float v) {
 
 template <typename OutT>
 __global__ void __launch_bounds__(256)
-    scale_c_kernel(OutT* __restrict__ C, int64_t M, int64_t N, int64_t ldc, float beta) {
+    scale_c_kernel(OutT* __restrict__ C, int64_t M, int64_t N, int64_t ldc, float beta,
+                   const void* bias, int32_t bias_dtype, int32_t act) {
     const int64_t total = M * N;
     for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
          i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
         const int64_t r = i / N, c = i - r * N;
         OutT* p = C + r * ldc + c;
-        *p = scale_store<OutT>(beta == 0.0f ? 0.0f : beta * scale_load<OutT>(p));
+        float x = beta == 0.0f ? 0.0f : beta * scale_load<OutT>(p);
+        if (bias != nullptr) x += load_bias_elem(bias, bias_dtype, c);
+        *p = scale_store<OutT>(activate(act, x));
     }
 }
 

@@ -50,6 +50,7 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include "epilogue_ops.cuh"
 #include "ptx.cuh"
 
 namespace gemm103 {
@@ -57,8 +58,9 @@ namespace gemm103 {
 constexpr int kBlockM = 128;      // tcgen05 M (cta_group::1)
 constexpr int kBlockK = 64;       // 64 16-bit elements = one 128-byte swizzle row
 constexpr int kUmmaK = 16;        // K per tcgen05.mma kind::f16
-constexpr int kThreads = 192;     // warp 0 producer, warp 1 MMA, warps 2-5 epilogue
-constexpr int kEpiWarps = 4;
+constexpr int kThreads = 320;     // warp 0 producer, warp 1 MMA, warps 2-9 epilogue
+constexpr int kEpiWarps = 8;      // two per TMEM lane quarter, splitting the columns
+constexpr int kFinBatch = 2;      // stream-K finisher: partial slots loaded per batch
 constexpr uint32_t kATileBytes = kBlockM * kBlockK * 2;   // 16 KB
 constexpr uint32_t kChunkBytes = 64 * kBlockK * 2;        // one 64 x 64 MN-major box, 8 KB
 
@@ -88,6 +90,11 @@ struct TcParams {
     int32_t b_stream_once;
     uint64_t wait_limit_ns;     // bound on every in-kernel wait
     uint32_t debug_flags;       // test hook (kDebugSkipFirstLoad), 0 in normal use
+    // fused epilogue: r = act(alpha * acc + beta * C + bias)
+    const void* bias;           // N elements or nullptr
+    int32_t bias_dtype;         // 0 F16, 1 BF16, 2 F32
+    int32_t bias_on_rows;       // 1: bias indexed by D' row (swapped problem), 0: by column
+    int32_t act;                // 0 none, 1 ReLU, 2 GELU (erf), 3 SiLU
 };
 
 // Test hook: CTA 0's producer arms its first pipeline slot but issues no load
@@ -199,38 +206,6 @@ __device__ __forceinline__ float load_out<__nv_bfloat16>(const __nv_bfloat16* p)
     return __bfloat162float(*p);
 }
 
-// Store 32 consecutive values v[0..31] of one C row at `dst` (16-byte aligned,
-// all in range), with optional beta * C read.
-template <typename OutT>
-__device__ __forceinline__ void store_row32_vec(OutT* dst, const float (&v)[32], float beta) {
-    constexpr int kPer16 = 16 / sizeof(OutT);      // elements per 16-byte vector
-    constexpr int kVecs = 32 / kPer16;
-    // Read every old value before the first store: a load that follows a
-    // store to the same array cannot be hoisted, and each would cost a full
-    // memory round trip.
-    uint4 old[kVecs];
-    if (beta != 0.0f) {
-        #pragma unroll
-        for (int q = 0; q < kVecs; ++q) old[q] = *reinterpret_cast<const uint4*>(dst + q * kPer16);
-    }
-    #pragma unroll
-    for (int q = 0; q < kVecs; ++q) {
-        float x[kPer16];
-        #pragma unroll
-        for (int e = 0; e < kPer16; ++e) x[e] = v[q * kPer16 + e];
-        if (beta != 0.0f) {
-            const OutT* o = reinterpret_cast<const OutT*>(&old[q]);
-            #pragma unroll
-            for (int e = 0; e < kPer16; ++e) x[e] = fmaf(beta, load_out<OutT>(o + e), x[e]);
-        }
-        uint4 pack;
-        OutT* pk = reinterpret_cast<OutT*>(&pack);
-        #pragma unroll
-        for (int e = 0; e < kPer16; ++e) pk[e] = cvt_out<OutT>(x[e]);
-        *reinterpret_cast<uint4*>(dst + q * kPer16) = pack;
-    }
-}
-
 // Wait on a barrier that receives plain arrivals from the peer CTA (the odd
 // CTA's epilogue releasing the accumulator): cluster-scope acquire, so the
 // peer's TMEM reads are ordered before the MMAs that overwrite them.  Barriers
@@ -263,18 +238,116 @@ __device__ __forceinline__ bool wait_role(uint64_t* bar, uint32_t parity, volati
 //   alone issues the MMAs, whose commits arrive on the "empty" / "acc_full"
 //   barriers of both CTAs; both CTAs drain their own TMEM half (128 rows x BN)
 //   and release the accumulator on the even CTA's "acc_empty" barrier.
-// r = alpha * v + beta * C for one row of 32 columns starting at D' column c0,
-// cast and stored (vector stores when C rows are 16-byte aligned and the chunk
-// is whole, element stores otherwise).
+__device__ __forceinline__ float load_bias(const TcParams& p, int64_t idx) {
+    return load_bias_elem(p.bias, p.bias_dtype, idx);
+}
+
+// Adds the bias and applies the activation to one row's 32 values at D'
+// columns c0..c0+31 (in place); the beta * C term is already in v.
+__device__ __forceinline__ void bias_act(const TcParams& p, int32_t row, int32_t c0,
+                                         float (&v)[32]) {
+    if (p.bias != nullptr) {
+        if (p.bias_on_rows) {
+            const float b = load_bias(p, row);
+            #pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] += b;
+        } else {
+            float b[32];
+            const int esize = p.bias_dtype == 2 ? 4 : 2;
+            const uintptr_t addr = reinterpret_cast<uintptr_t>(p.bias) + static_cast<uintptr_t>(c0) * esize;
+            if (c0 + 32 <= p.N && (addr & 15u) == 0) {
+                // 16-byte loads (every thread of the warp reads the same
+                // columns: one L1 line serves the warp)
+                const uint4* src = reinterpret_cast<const uint4*>(addr);
+                if (p.bias_dtype == 2) {
+                    #pragma unroll
+                    for (int q = 0; q < 8; ++q) {
+                        const uint4 t = __ldg(src + q);
+                        b[4 * q] = __uint_as_float(t.x);
+                        b[4 * q + 1] = __uint_as_float(t.y);
+                        b[4 * q + 2] = __uint_as_float(t.z);
+                        b[4 * q + 3] = __uint_as_float(t.w);
+                    }
+                } else {
+                    #pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const uint4 t = __ldg(src + q);
+                        const uint32_t w[4] = {t.x, t.y, t.z, t.w};
+                        #pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const uint16_t lo = static_cast<uint16_t>(w[e] & 0xFFFFu);
+                            const uint16_t hi = static_cast<uint16_t>(w[e] >> 16);
+                            if (p.bias_dtype == 1) {
+                                b[8 * q + 2 * e] = __bfloat162float(__ushort_as_bfloat16(lo));
+                                b[8 * q + 2 * e + 1] = __bfloat162float(__ushort_as_bfloat16(hi));
+                            } else {
+                                b[8 * q + 2 * e] = __half2float(__ushort_as_half(lo));
+                                b[8 * q + 2 * e + 1] = __half2float(__ushort_as_half(hi));
+                            }
+                        }
+                    }
+                }
+            } else {
+                #pragma unroll
+                for (int j = 0; j < 32; ++j) b[j] = (c0 + j < p.N) ? load_bias(p, c0 + j) : 0.0f;
+            }
+            #pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] += b[j];
+        }
+    }
+    if (p.act != 0) {
+        #pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = activate(p.act, v[j]);
+    }
+}
+
+// Store 32 consecutive values v[0..31] of one C row at `dst` (16-byte aligned,
+// all in range): r = act(v + beta * C + bias).
+template <typename OutT>
+__device__ __forceinline__ void store_row32_vec(const TcParams& p, OutT* dst, int32_t row,
+                                                int32_t c0, float (&v)[32]) {
+    constexpr int kPer16 = 16 / sizeof(OutT);      // elements per 16-byte vector
+    constexpr int kVecs = 32 / kPer16;
+    // Read every old value before the first store: a load that follows a
+    // store to the same array cannot be hoisted, and each would cost a full
+    // memory round trip.
+    if (p.beta != 0.0f) {
+        uint4 old[kVecs];
+        #pragma unroll
+        for (int q = 0; q < kVecs; ++q) old[q] = *reinterpret_cast<const uint4*>(dst + q * kPer16);
+        #pragma unroll
+        for (int q = 0; q < kVecs; ++q) {
+            const OutT* o = reinterpret_cast<const OutT*>(&old[q]);
+            #pragma unroll
+            for (int e = 0; e < kPer16; ++e)
+                v[q * kPer16 + e] = fmaf(p.beta, load_out<OutT>(o + e), v[q * kPer16 + e]);
+        }
+    }
+    bias_act(p, row, c0, v);
+    #pragma unroll
+    for (int q = 0; q < kVecs; ++q) {
+        uint4 pack;
+        OutT* pk = reinterpret_cast<OutT*>(&pack);
+        #pragma unroll
+        for (int e = 0; e < kPer16; ++e) pk[e] = cvt_out<OutT>(v[q * kPer16 + e]);
+        *reinterpret_cast<uint4*>(dst + q * kPer16) = pack;
+    }
+}
+
+// r = act(alpha * v + beta * C + bias) for one row of 32 columns starting at
+// D' column c0, cast and stored (vector stores when C rows are 16-byte aligned
+// and the chunk is whole, element stores otherwise).
 template <typename OutT>
 __device__ __forceinline__ void store_chunk(const TcParams& p, int32_t row, int32_t c0,
                                             float (&v)[32]) {
     OutT* C = reinterpret_cast<OutT*>(p.C);
-    #pragma unroll
-    for (int j = 0; j < 32; ++j) v[j] *= p.alpha;
+    if (p.alpha != 1.0f) {
+        #pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] *= p.alpha;
+    }
     if (row >= p.M) return;
     if (p.c_vector && c0 + 32 <= p.N) {
-        store_row32_vec<OutT>(C + static_cast<int64_t>(row) * p.c_rs + c0, v, p.beta);
+        store_row32_vec<OutT>(p, C + static_cast<int64_t>(row) * p.c_rs + c0, row, c0, v);
     } else {
         OutT* base = C + static_cast<int64_t>(row) * p.c_rs;
         if (p.beta != 0.0f) {
@@ -286,6 +359,7 @@ __device__ __forceinline__ void store_chunk(const TcParams& p, int32_t row, int3
             #pragma unroll
             for (int j = 0; j < 32; ++j) v[j] = fmaf(p.beta, old[j], v[j]);
         }
+        bias_act(p, row, c0, v);
         #pragma unroll
         for (int j = 0; j < 32; ++j)
             if (c0 + j < p.N) base[static_cast<int64_t>(c0 + j) * p.c_cs] = cvt_out<OutT>(v[j]);
@@ -565,7 +639,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {
         // --------------------------------------------------------- epilogue
+        // Warp w may read TMEM lanes 32*(w%4)..+31: two epilogue warps share each
+        // lane quarter and take alternate 32-column chunks of the tile.
         const int quarter = warp & 3;                   // TMEM lanes 32*quarter..+31
+        const int half = (warp - 2) >> 2;               // 0: even chunks, 1: odd chunks
         const int row_in_cta = quarter * 32 + lane;
         const int row_in_tile = static_cast<int>(rank) * kBlockM + row_in_cta;
         uint32_t acc_i = 0;
@@ -624,56 +701,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             float* my_slot = (sg.slot >= 0 && !finisher)
                                  ? p.partials + static_cast<int64_t>(sg.slot) * BM * BN
                                  : nullptr;
-            if constexpr (BN == 64) {
-                if (finisher) {
-                    // 64-column tiles: one batch of loads per contribution (the
-                    // whole row at once), own sums re-read from TMEM in turn.
-                    float acc[64];
-                    #pragma unroll
-                    for (int j = 0; j < 64; ++j) acc[j] = 0.0f;
-                    for (int32_t g = g_first; g <= g_last; ++g) {
-                        float x[64];
-                        if (g == unit) {
-                            uint32_t r0[32], r1[32];
-                            __syncwarp();
-                            tmem_ld_32x32b_x32(t_row, r0);
-                            tmem_ld_32x32b_x32(t_row + 32, r1);
-                            tmem_ld_wait();
-                            #pragma unroll
-                            for (int j = 0; j < 32; ++j) {
-                                x[j] = __uint_as_float(r0[j]);
-                                x[32 + j] = __uint_as_float(r1[j]);
-                            }
-                        } else {
-                            const int32_t first_tile =
-                                static_cast<int32_t>((static_cast<int64_t>(g) * L) / KB);
-                            const float* src = p.partials +
-                                               (static_cast<int64_t>(g) * p.sk_max_seg +
-                                                (sg.tile - first_tile)) * BM * BN;
-                            if (p.c_cs == 1) {
-                                const float4* s4 = reinterpret_cast<const float4*>(src + row_in_tile * BN);
-                                #pragma unroll
-                                for (int q = 0; q < 16; ++q) {
-                                    const float4 t = __ldcg(s4 + q);
-                                    x[4 * q] = t.x;
-                                    x[4 * q + 1] = t.y;
-                                    x[4 * q + 2] = t.z;
-                                    x[4 * q + 3] = t.w;
-                                }
-                            } else {
-                                #pragma unroll
-                                for (int j = 0; j < 64; ++j) x[j] = __ldcg(src + j * BM + row_in_tile);
-                            }
-                        }
-                        #pragma unroll
-                        for (int j = 0; j < 64; ++j) acc[j] += x[j];
-                    }
-                    store_chunk<OutT>(p, row, col0, *reinterpret_cast<float(*)[32]>(acc));
-                    store_chunk<OutT>(p, row, col0 + 32, *reinterpret_cast<float(*)[32]>(acc + 32));
-                }
-            }
             #pragma unroll 1
-            for (int ch = 0; ch < ((BN == 64 && finisher) ? 0 : BN / 32); ++ch) {
+            for (int ch = half; ch < BN / 32; ch += 2) {
                 uint32_t r[32];
                 __syncwarp();                      // tcgen05.ld is warp-collective
                 tmem_ld_32x32b_x32(t_row + ch * 32, r);
@@ -697,20 +726,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                         #pragma unroll
                         for (int j = 0; j < 32; ++j) my_slot[(ch * 32 + j) * BM + row_in_tile] = v[j];
                     }
-                } else if constexpr (BN != 64) {
+                } else {
                     // finisher: acc = sum of contributions g_first..g_last in
                     // that order, its own (g == unit) from registers.  Loads of
-                    // up to four slots are issued together, 16 columns at a
+                    // up to kFinBatch slots are issued together, 16 columns at a
                     // time, so their memory latencies overlap.
                     float acc[32];
                     #pragma unroll
                     for (int j = 0; j < 32; ++j) acc[j] = 0.0f;
                     #pragma unroll
                     for (int h = 0; h < 2; ++h) {
-                        for (int32_t g0 = g_first; g0 <= g_last; g0 += 4) {
-                            float x[4][16];
+                        for (int32_t g0 = g_first; g0 <= g_last; g0 += kFinBatch) {
+                            float x[kFinBatch][16];
                             #pragma unroll
-                            for (int u = 0; u < 4; ++u) {
+                            for (int u = 0; u < kFinBatch; ++u) {
                                 const int32_t g = g0 + u;
                                 if (g > g_last || g == unit) continue;
                                 const int32_t first_tile =
@@ -736,7 +765,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 }
                             }
                             #pragma unroll
-                            for (int u = 0; u < 4; ++u) {
+                            for (int u = 0; u < kFinBatch; ++u) {
                                 const int32_t g = g0 + u;
                                 if (g > g_last) break;
                                 #pragma unroll

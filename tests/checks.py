@@ -71,3 +71,30 @@ def compare(gpu_vals, gpu_codes, R, S, Cin_vals, alpha, beta, c_dtype, oracle_co
     stats["n"] = int(ok.size)
     stats["fail"] = int((~ok).sum())
     return stats, ~ok
+
+
+def compare_epilogue(gpu_vals, gpu_codes, R, S, Cin_vals, bias_vals, alpha, beta, c_dtype,
+                     oracle_codes=None, slope=1.2, rel=2e-6):
+    """Acceptance for act(alpha*AB + beta*C + bias): the pre-activation bound
+    (the same FP32 rule, with |bias| added to the scale) times the largest
+    slope of the activations (ReLU 1, SiLU ~1.1, GELU ~1.13), plus a relative
+    term for the FP32 evaluation of erf/exp and the extra roundings."""
+    scale = abs(alpha) * S
+    if beta != 0 and Cin_vals is not None:
+        scale = scale + np.abs(beta * Cin_vals)
+    if bias_vals is not None:
+        scale = scale + np.abs(bias_vals)
+    bound = slope * (REL * scale + ABS) + rel * np.abs(R)
+    err = np.abs(gpu_vals - R)
+    nan_ok = np.isnan(gpu_vals) & np.isnan(R)
+    if c_dtype == F32:
+        ok = (err <= bound) | nan_ok
+        stats = {}
+    else:
+        dist = np.abs(_ordered(gpu_codes) - _ordered(oracle_codes))
+        strict = dist <= 1
+        ok = strict | (err <= ulp_of(R, c_dtype) + bound) | nan_ok
+        stats = {"strict_1ulp_frac": float(strict.mean()) if strict.size else 1.0}
+    stats["n"] = int(ok.size)
+    stats["fail"] = int((~ok).sum())
+    return stats, ~ok
