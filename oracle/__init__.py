@@ -91,6 +91,8 @@ class Oracle:
         lib.oracle_round_output.argtypes = [ctypes.c_int, i64, dp, vp]
         lib.oracle_max_threads.restype = ctypes.c_int
         lib.oracle_max_threads.argtypes = []
+        lib.oracle_decode_tf32.restype = ctypes.c_double
+        lib.oracle_decode_tf32.argtypes = [ctypes.c_uint32]
         lib.oracle_activation.restype = ctypes.c_double
         lib.oracle_activation.argtypes = [ctypes.c_int, ctypes.c_double]
         ep = [vp, ctypes.c_int, ctypes.c_int]
@@ -103,6 +105,10 @@ class Oracle:
 
     def max_threads(self) -> int:
         return int(self.lib.oracle_max_threads())
+
+    def decode_tf32(self, bits: int) -> float:
+        """Value an FP32 bit pattern has as a TF32 tensor-core input."""
+        return float(self.lib.oracle_decode_tf32(int(bits) & 0xFFFFFFFF))
 
     def decode_scalar(self, code: int, dtype: int) -> float:
         fn = self.lib.oracle_decode_f16 if dtype == F16 else self.lib.oracle_decode_bf16

@@ -15,7 +15,9 @@
  *     of the CATLASS page (section 2.1).  alpha/beta scaling and op() are the
  *     BLAS reading of that formula (the pages never name alpha or beta):
  *       r_ij = alpha * sum_k op(A)_ik op(B)_kj + beta * C_ij.
- *   - Precision.  Inputs are FP16 or BF16; accumulation must be wider than the
+ *   - Precision.  Inputs are FP16 or BF16 -- or FP32 used as TF32 (the third
+ *     format of the CATLASS page, section 3.2: the mantissa is truncated to 10
+ *     bits, see oracle_decode_tf32); accumulation must be wider than the
  *     inputs (DeepGEMM page, section 6.2; CATLASS page, section 3.4).  The
  *     oracle decodes every input exactly to binary64 and accumulates in
  *     binary64, so it is strictly more accurate than any FP32-accumulating
@@ -160,7 +162,19 @@ float oracle_round_f32(double x) { return (float)x; }
 
 /* ------------------------------------------------------------------- GEMM */
 
+/* TF32 inputs: FP32 storage whose value enters the product with its mantissa
+ * cut to the 10 bits TF32 keeps -- "TF32 truncates the FP32 data to a 10-bit
+ * mantissa inside the tensor core; inputs and outputs stay FP32 in memory"
+ * (CATLASS page, section 3.2).  The low 13 mantissa bits are dropped (round
+ * toward zero); the sign, the 8-bit exponent and infinities/NaNs are kept. */
+double oracle_decode_tf32(uint32_t u) {
+    const uint32_t e = (u >> 23) & 0xFFu;
+    if (e == 0xFFu) return oracle_decode_f32(u);          /* inf / NaN unchanged */
+    return oracle_decode_f32(u & 0xFFFFE000u);
+}
+
 static double decode_in(int dt, const void* p, int64_t idx) {
+    if (dt == OR_F32) return oracle_decode_tf32(((const uint32_t*)p)[idx]);
     const uint16_t* h = (const uint16_t*)p;
     return dt == OR_F16 ? oracle_decode_f16(h[idx]) : oracle_decode_bf16(h[idx]);
 }
@@ -177,7 +191,7 @@ static int check_args(char transA, char transB, int64_t M, int64_t N, int64_t K,
                       int64_t lda, int64_t ldb, int64_t ldc, int ab_dtype, int c_dtype) {
     if (!(is_n(transA) || is_t(transA)) || !(is_n(transB) || is_t(transB))) return OR_BAD_ARG;
     if (M < 0 || N < 0 || K < 0) return OR_BAD_ARG;
-    if (ab_dtype != OR_F16 && ab_dtype != OR_BF16) return OR_BAD_ARG;
+    if (ab_dtype != OR_F16 && ab_dtype != OR_BF16 && ab_dtype != OR_F32) return OR_BAD_ARG;
     if (c_dtype != OR_F16 && c_dtype != OR_BF16 && c_dtype != OR_F32) return OR_BAD_ARG;
     int64_t a_cols = is_n(transA) ? K : M;
     int64_t b_cols = is_n(transB) ? N : K;

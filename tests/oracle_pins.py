@@ -350,7 +350,7 @@ def pin_bad_arguments(o):
     A = np.zeros((4, 4), dtype=np.uint16)
     bad = [
         dict(ta="X"), dict(M=-1), dict(lda=3), dict(ldb=3), dict(ldc=3),
-        dict(dt=F32), dict(cdt=7),
+        dict(dt=5), dict(cdt=7),
     ]
     for b in bad:
         kw = dict(ta="N", tb="N", M=4, N=4, K=4, lda=4, ldb=4, ldc=4, dt=F16, cdt=F32)
@@ -464,6 +464,69 @@ def pin_epilogue_exact_and_sampled(o):
         raise AssertionError("unknown activation accepted")
 
 
+# -------------------------------------------------------------------- TF32
+
+def _tf32_numpy(x32):
+    """TF32 value of float32 inputs by a numpy bit mask (independent of C)."""
+    u = np.ascontiguousarray(x32, dtype=np.float32).view(np.uint32)
+    special = ((u >> 23) & 0xFF) == 0xFF
+    t = np.where(special, u, u & np.uint32(0xFFFFE000)).astype(np.uint32)
+    return t.view(np.float32).astype(np.float64)
+
+
+def pin_tf32_truncation(o):
+    """FP32 used as TF32 keeps 10 mantissa bits, dropping the rest toward zero
+    (CATLASS page, section 3.2): page facts and random bit patterns."""
+    import struct
+    bits = lambda f: struct.unpack("<I", struct.pack("<f", f))[0]
+    facts = [(1.0 + 2.0 ** -10, 1.0 + 2.0 ** -10), (1.0 + 2.0 ** -11, 1.0),
+             (1.0 + 2.0 ** -10 + 2.0 ** -11, 1.0 + 2.0 ** -10), (-(1.0 + 3 * 2.0 ** -12), -1.0),
+             (3.0e38, float(_tf32_numpy(np.float32([3.0e38]))[0])), (0.0, 0.0)]
+    for x, want in facts:
+        assert o.decode_tf32(bits(x)) == want, (x, o.decode_tf32(bits(x)), want)
+    assert math.isinf(o.decode_tf32(bits(float("inf"))))
+    assert math.isnan(o.decode_tf32(0x7FC00001))
+    rng = _rng(31)
+    u = rng.integers(0, 2 ** 32, 20000, dtype=np.uint64).astype(np.uint32)
+    x = u.view(np.float32)
+    mine = np.array([o.decode_tf32(int(v)) for v in u])
+    lib = _tf32_numpy(x)
+    same = (mine == lib) | (np.isnan(mine) & np.isnan(lib))
+    assert same.all()
+    fin = np.isfinite(lib) & (lib != 0)
+    assert (np.abs(lib[fin]) <= np.abs(x[fin].astype(np.float64))).all()     # toward zero
+
+
+def pin_gemm_tf32_bruteforce(o):
+    """FP32 inputs as TF32 against exact rationals (every transpose pair), and
+    integer inputs exactly."""
+    rng = _rng(32)
+    n = 0
+    for (M, N, K) in [(3, 4, 5), (5, 2, 7), (1, 6, 3)]:
+        for ta in "NT":
+            for tb in "NT":
+                a_rows, a_cols = (M, K) if ta == "N" else (K, M)
+                b_rows, b_cols = (K, N) if tb == "N" else (N, K)
+                A = rng.standard_normal((a_rows, a_cols)).astype(np.float32)
+                B = rng.standard_normal((b_rows, b_cols)).astype(np.float32)
+                alpha = (1.0, 0.5)[n % 2]
+                R, S = o.gemm(ta, tb, M, N, K, alpha, A.view(np.uint32), a_cols,
+                              B.view(np.uint32), b_cols, 0.0, None, N, F32, F32)
+                opA = exact.op_matrix(_tf32_numpy(A), a_rows, a_cols, ta)
+                opB = exact.op_matrix(_tf32_numpy(B), b_rows, b_cols, tb)
+                r_ex, s_ex = exact.exact_gemm(opA, opB, alpha, 0.0, np.zeros((M, N)))
+                for i in range(M):
+                    for j in range(N):
+                        assert abs(Fraction(float(R[i, j])) - r_ex[i][j]) <= \
+                            Fraction(2) ** -48 * s_ex[i][j] + Fraction(1, 2 ** 1000)
+                n += 1
+    Ai = rng.integers(-1000, 1001, (6, 9)).astype(np.float32)
+    Bi = rng.integers(-1000, 1001, (9, 7)).astype(np.float32)
+    R, _ = o.gemm("N", "N", 6, 7, 9, 1.0, Ai.view(np.uint32), 9, Bi.view(np.uint32), 7, 0.0,
+                  None, 7, F32, F32)
+    assert (R == Ai.astype(np.float64) @ Bi.astype(np.float64)).all()   # 10-bit integers are exact
+
+
 ALL_PINS = [
     pin_decode_exhaustive, pin_page_format_limits, pin_round_ieee_table,
     pin_round_roundtrip_exhaustive, pin_round_midpoints, pin_round_random_exact,
@@ -471,4 +534,5 @@ ALL_PINS = [
     pin_identity_and_permutation, pin_all_ones, pin_rank1_closed_form, pin_linearity,
     pin_quick_returns, pin_bad_arguments, pin_threads_deterministic,
     pin_activation_values, pin_epilogue_bruteforce, pin_epilogue_exact_and_sampled,
+    pin_tf32_truncation, pin_gemm_tf32_bruteforce,
 ]

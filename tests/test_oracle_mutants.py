@@ -59,6 +59,12 @@ MUTANTS = [
      "return isnan(x) ? x : (x > 0.0 ? x : 0.01 * x);"),
     ("activation_after_bias_skipped", "        R[i * N + j] = oracle_activation(act, x);",
      "        R[i * N + j] = x;"),
+    ("tf32_keeps_11_bits", "return oracle_decode_f32(u & 0xFFFFE000u);",
+     "return oracle_decode_f32(u & 0xFFFFF000u);"),
+    ("tf32_rounds_up", "return oracle_decode_f32(u & 0xFFFFE000u);",
+     "return oracle_decode_f32((u + 0x1000u) & 0xFFFFE000u);"),
+    ("tf32_not_truncated", "if (dt == OR_F32) return oracle_decode_tf32(((const uint32_t*)p)[idx]);",
+     "if (dt == OR_F32) return oracle_decode_f32(((const uint32_t*)p)[idx]);"),
     ("beta_read_when_zero", "if (be != 0.0) r = r + be * decode_c(c_dtype, C, i * ldc + j);\n            acc[j] = r;",
      "r = r + be * decode_c(c_dtype, C, i * ldc + j);\n            acc[j] = r;"),
 ]
