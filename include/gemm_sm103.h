@@ -4,14 +4,18 @@
  *     C = alpha * op(A) * op(B) + beta * C
  *
  * What is computed (and where it is defined):
- *   - The product-sum "C[i][j] accumulates A[i][k] * B[k][j]" (SGEMM tutorial
- *     page, section 3.1) and "C = A * B + C" (CATLASS page, section 2.1).
+ *   - Each C[i][j] sums A[i][k] * B[k][j] over k (SGEMM tutorial page,
+ *     section 3.1), and the formula C = A * B + C (CATLASS page, section 2.1).
  *     alpha, beta and op() are the BLAS reading of that formula; the pages
  *     name neither.
  *   - A and B are FP16 or BF16 (both the same type); products are accumulated
  *     in FP32 (DeepGEMM page, sections 1.3 and 6.2; CATLASS page, sections
  *     3.2 and 3.4).  The output C is FP32, FP16 or BF16; alpha*acc + beta*C is
  *     formed in FP32 and rounded once to the output type, round to nearest even.
+ *   - A and B may also both be FP32, used as TF32 (the third format of the
+ *     CATLASS page, section 3.2): they stay FP32 in memory and the tensor core
+ *     keeps only the top 10 of each element's 23 mantissa bits (the low 13 are
+ *     dropped, i.e. rounded toward zero); the accumulator is FP32 as above.
  *   - Storage is row-major with a leading dimension: element (m, n) of a
  *     stored matrix is at offset m * ld + n, in elements (CATLASS page,
  *     section 1.3).  op(X) = X for 'N'/'n' and X^T for 'T'/'t'.
@@ -23,6 +27,8 @@
  *   - Shapes are arbitrary (M, N, K >= 0; the DeepGEMM page, section 1.3, asks
  *     for 1 to several thousand); tiles that overhang the matrix edge are
  *     zero-filled (DeepGEMM page, section 3.4).
+ *   - Each of A, B and C must be aligned to its own element size (2 or 4
+ *     bytes); any leading dimension and any further offset are accepted.
  *
  * Ownership and threading:
  *   - A, B and C are DEVICE pointers owned by the caller.  A and B are only
@@ -59,8 +65,8 @@ typedef struct gemm_ctx* gemm_handle_t;
 
 typedef enum { GEMM_F16 = 0, GEMM_BF16 = 1, GEMM_F32 = 2 } gemm_dtype_t;
 
-/* a, b: input types (must be equal, F16 or BF16); c: output type (F32, F16 or
- * BF16).  The accumulator is always FP32. */
+/* a, b: input types (must be equal: F16, BF16, or F32 computed as TF32); c:
+ * output type (F32, F16 or BF16).  The accumulator is always FP32. */
 typedef struct { int32_t a, b, c; } gemm_dtypes_t;
 
 typedef enum {
@@ -87,7 +93,8 @@ gemm_status_t gemm_create(gemm_handle_t* out);
  *   M, N, K: op(A) is M x K, op(B) is K x N, C is M x N.
  *   A, lda / B, ldb / C, ldc: device pointers and leading dimensions in
  *     elements, laid out as in the table above.
- *   dt: element types (dt.a == dt.b in {F16, BF16}; dt.c in {F32, F16, BF16}).
+ *   dt: element types (dt.a == dt.b in {F16, BF16, F32 as TF32}; dt.c in
+ *     {F32, F16, BF16}).
  *   stream: the CUDA stream to enqueue on.
  * Quick returns (BLAS convention): M == 0 or N == 0 is a no-op; K == 0 or
  * alpha == 0 computes C = beta * C without reading A or B (A, B may then be
@@ -104,8 +111,8 @@ gemm_status_t gemm_run(gemm_handle_t h, char transA, char transB,
                        gemm_dtypes_t dt, gemm_stream_t stream);
 
 /*
- * Fused epilogue ("keep the GEMM mainloop, replace the epilogue", CATLASS page,
- * section 5.2, read in the usual linear-layer form):
+ * Fused epilogue (CATLASS page, section 5.2: an unchanged mainloop followed by
+ * a replaced epilogue, read in the usual linear-layer form):
  *     C = act(alpha * op(A) * op(B) + beta * C + bias[n])
  * evaluated in FP32 before the single cast to C's type.  bias has N elements
  * (one per output column n), is read only, and may be NULL.  A residual add
@@ -197,6 +204,7 @@ typedef struct {
     int32_t num_tiles;     /* output tiles (x split_k work units) */
     int32_t pack_a;        /* 1: A is copied to an aligned workspace first */
     int32_t pack_b;        /* 1: B is copied to an aligned workspace first */
+                           /* (the copy is a transposition when transpose_ab says so) */
     int32_t a_mn_major;    /* 1: op(A) is read M-contiguous (transA = 'T') */
     int32_t b_mn_major;    /* 1: op(B) is read N-contiguous (transB = 'N') */
     int32_t swap_ab;       /* 1: computed as C^T = op(B)^T op(A)^T */
@@ -206,7 +214,10 @@ typedef struct {
     int32_t k_blocks;      /* ceil(K / block_k) */
     int32_t tiles_m;       /* tile rows (of the possibly swapped problem) */
     int32_t tiles_n;       /* tile columns */
-    int32_t reserved;
+    int32_t transpose_ab;  /* FP32 (TF32) inputs only: bit 0 (A), bit 1 (B) set when that
+                              operand is stored M/N-contiguous and a pre-pass rewrites it
+                              K-contiguous into the workspace (kind::tf32 reads K-major
+                              operands only) */
     int64_t workspace_bytes;
 } gemm_plan_t;
 

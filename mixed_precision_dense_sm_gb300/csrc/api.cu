@@ -40,6 +40,7 @@ struct OperandDesc {
     int64_t rows, cols, ld;
     bool mn_major;
     bool pack;          // needs a 16-byte-aligned copy
+    bool transpose;     // the copy also transposes (FP32 MN-major -> K-major)
     int64_t packed_ld;
 };
 
@@ -51,6 +52,7 @@ struct Plan {
     int64_t c_rs, c_cs;
     int32_t k_blocks, tiles_m, tiles_n;
     int32_t cta_group;
+    int32_t esize;      // input element bytes: 2 (FP16/BF16) or 4 (FP32 as TF32)
     int32_t sk_len, sk_max_seg;
     int64_t pack_a_bytes, pack_b_bytes, partial_bytes;
     size_t smem_bytes;
@@ -62,7 +64,9 @@ int64_t max1(int64_t v) { return v > 1 ? v : 1; }
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 int64_t round_up(int64_t a, int64_t b) { return ceil_div(a, b) * b; }
 size_t out_elem_bytes(int32_t c) { return c == GEMM_F32 ? 4 : 2; }
+int32_t in_elem_bytes(int32_t ab) { return ab == GEMM_F32 ? 4 : 2; }
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned_to(const void* p, size_t n) { return (reinterpret_cast<uintptr_t>(p) % n) == 0; }
 
 gemm_status_t check_args(char transA, char transB, int64_t M, int64_t N, int64_t K, float alpha,
                          const void* A, int64_t lda, const void* B, int64_t ldb, float beta,
@@ -72,15 +76,20 @@ gemm_status_t check_args(char transA, char transB, int64_t M, int64_t N, int64_t
     if (M < 0 || N < 0 || K < 0) return GEMM_ERR_INVALID_VALUE;
     // TMA coordinates and tile indices are 32-bit.
     if (M > INT32_MAX || N > INT32_MAX || K > INT32_MAX) return GEMM_ERR_INVALID_VALUE;
-    if (dt.a != dt.b || (dt.a != GEMM_F16 && dt.a != GEMM_BF16)) return GEMM_ERR_INVALID_VALUE;
+    if (dt.a != dt.b || (dt.a != GEMM_F16 && dt.a != GEMM_BF16 && dt.a != GEMM_F32))
+        return GEMM_ERR_INVALID_VALUE;
     if (dt.c != GEMM_F32 && dt.c != GEMM_F16 && dt.c != GEMM_BF16) return GEMM_ERR_INVALID_VALUE;
     const int64_t a_cols = is_n(transA) ? K : M;
     const int64_t b_cols = is_n(transB) ? N : K;
     if (lda < max1(a_cols) || ldb < max1(b_cols) || ldc < max1(N)) return GEMM_ERR_INVALID_VALUE;
     if (M == 0 || N == 0) return GEMM_OK;
-    if (C == nullptr) return GEMM_ERR_INVALID_VALUE;
+    if (C == nullptr || !aligned_to(C, out_elem_bytes(dt.c))) return GEMM_ERR_INVALID_VALUE;
     const bool reads_ab = (K > 0 && alpha != 0.0f);
     if (reads_ab && (A == nullptr || B == nullptr)) return GEMM_ERR_INVALID_VALUE;
+    // Every element must sit on its own size's boundary (the pack pre-pass
+    // reads the operands element by element).
+    const size_t es = static_cast<size_t>(in_elem_bytes(dt.a));
+    if (reads_ab && (!aligned_to(A, es) || !aligned_to(B, es))) return GEMM_ERR_INVALID_VALUE;
     (void)beta;
     return GEMM_OK;
 }
@@ -137,23 +146,42 @@ gemm_status_t make_plan(char transA, char transB, int64_t M, int64_t N, int64_t 
         pl.c_rs = ldc;
         pl.c_cs = 1;
     }
+    // One 128-byte swizzle row of K per stage: 64 16-bit or 32 32-bit elements.
+    const int32_t esize = in_elem_bytes(dt.a);
+    const int64_t block_k = 128 / esize;
+    pl.esize = esize;
     for (OperandDesc* o : {&pl.a, &pl.b}) {
-        o->pack = !aligned16(o->ptr) || ((o->ld * 2) % 16) != 0;
-        o->packed_ld = o->pack ? round_up(o->cols, 8) : o->ld;
+        o->pack = !aligned16(o->ptr) || ((o->ld * esize) % 16) != 0;
+        o->transpose = false;
+        o->packed_ld = o->pack ? round_up(o->cols, 16 / esize) : o->ld;
+        if (esize == 4 && o->mn_major) {
+            // kind::tf32 takes K-major operands only: a pre-pass rewrites the
+            // stored K x MN matrix as MN x K.  From here on rows/cols/mn_major
+            // describe the rewritten copy the kernel reads.
+            o->transpose = true;
+            o->pack = true;
+            o->mn_major = false;
+            const int64_t k = o->rows;
+            o->rows = o->cols;
+            o->cols = k;
+            o->packed_ld = round_up(k, 16 / esize);
+        }
     }
+    pl.pub.transpose_ab = ((swap ? pl.b.transpose : pl.a.transpose) ? 1 : 0) |
+                          ((swap ? pl.a.transpose : pl.b.transpose) ? 2 : 0);
     pl.pub.a_mn_major = pl.a.mn_major;
     pl.pub.b_mn_major = pl.b.mn_major;
     pl.pub.pack_a = (swap ? pl.b.pack : pl.a.pack) ? 1 : 0;
     pl.pub.pack_b = (swap ? pl.a.pack : pl.b.pack) ? 1 : 0;
-    pl.pack_a_bytes = pl.a.pack ? pl.a.rows * pl.a.packed_ld * 2 : 0;
-    pl.pack_b_bytes = pl.b.pack ? pl.b.rows * pl.b.packed_ld * 2 : 0;
+    pl.pack_a_bytes = pl.a.pack ? pl.a.rows * pl.a.packed_ld * esize : 0;
+    pl.pack_b_bytes = pl.b.pack ? pl.b.rows * pl.b.packed_ld * esize : 0;
     pl.pub.c_vector = (!swap && aligned16(C) && (ldc * (int64_t)out_elem_bytes(dt.c)) % 16 == 0) ? 1 : 0;
 
     // Tile shape.  Enough 256 x 256 tiles to give every SM pair one: CTA-pair
     // tiles (tcgen05 cta_group::2).  Otherwise single-CTA 128-row tiles, 256
     // columns wide when that still fills the GPU, else narrower ones with
     // stream-K over K for more parallelism.
-    pl.k_blocks = static_cast<int32_t>(ceil_div(K, kBlockK));
+    pl.k_blocks = static_cast<int32_t>(ceil_div(K, block_k));
     const int64_t pair_tiles = ceil_div(pl.Mk, 2 * kBlockM) * ceil_div(pl.Nk, 256);
     const bool pairs = !swap && pl.Mk >= 2 * kBlockM && pl.Nk >= 256 && num_sms >= 2 &&
                        pair_tiles >= num_sms / 2;
@@ -180,10 +208,10 @@ gemm_status_t make_plan(char transA, char transB, int64_t M, int64_t N, int64_t 
     pl.tiles_n = static_cast<int32_t>(tiles_n);
     pl.pub.block_m = static_cast<int32_t>(block_m);
     pl.pub.block_n = bn;
-    pl.pub.block_k = kBlockK;
+    pl.pub.block_k = static_cast<int32_t>(block_k);
     pl.pub.num_tiles = static_cast<int32_t>(tiles);
 
-    const uint32_t stage_bytes = kATileBytes + static_cast<uint32_t>(bn / cg) * kBlockK * 2;
+    const uint32_t stage_bytes = kATileBytes + static_cast<uint32_t>(bn / cg) * 128u;
     const int64_t barrier_bytes = 256;
     int64_t stages = (smem_optin - 1024 - barrier_bytes) / stage_bytes;
     if (stages > kMaxStages) stages = kMaxStages;
@@ -245,17 +273,21 @@ struct gemm_ctx {
 
 namespace {
 
-// 2-D tiled map over a stored 16-bit matrix: dims {inner, outer}, row pitch in
-// bytes, a 64 x box_outer box, 128-byte swizzle, zero fill out of range.
+// 2-D tiled map over a stored matrix: dims {inner, outer}, row pitch in bytes,
+// a box of one 128-byte row (64 16-bit or 32 FP32 elements) by box_outer rows,
+// 128-byte swizzle, zero fill out of range.  FP32 is moved as plain FP32: the
+// tensor core itself takes it as TF32.
 bool encode_operand(EncodeTiledFn encode, CUtensorMap* map, int32_t dtype, const void* ptr,
                     int64_t inner, int64_t outer, int64_t ld, uint32_t box_outer) {
+    const int64_t es = in_elem_bytes(dtype);
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(outer)};
-    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2};
-    const cuuint32_t box[2] = {static_cast<cuuint32_t>(kBlockK), box_outer};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld * es)};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(128 / es), box_outer};
     const cuuint32_t estr[2] = {1, 1};
-    CUresult r = encode(map,
-                           dtype == GEMM_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
-                                              : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+    const CUtensorMapDataType ty = dtype == GEMM_F32    ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                   : dtype == GEMM_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                        : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    CUresult r = encode(map, ty,
                            2, const_cast<void*>(ptr), dims, strides, box, estr,
                            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -318,6 +350,8 @@ gemm_status_t enqueue_plan(const Plan& pl, EncodeTiledFn encode, int num_sms, ui
                            int* err_dev, float alpha, float beta, void* C, gemm_dtypes_t dt,
                            cudaStream_t stream, bool clear_counters, uint32_t debug_flags = 0,
                            uint64_t wait_limit_ns = 0, const gemm_epilogue_t* ep = nullptr) {
+    // kind::tf32 reads K-major operands only; the planner transposes the rest.
+    if (pl.esize == 4 && (pl.a.mn_major || pl.b.mn_major)) return GEMM_ERR_NOT_SUPPORTED;
     int* counters = reinterpret_cast<int*>(ws);
     if (clear_counters && pl.sk_len > 0 &&
         cudaMemsetAsync(counters, 0, kWsHeaderBytes, stream) != cudaSuccess) {
@@ -331,18 +365,33 @@ gemm_status_t enqueue_plan(const Plan& pl, EncodeTiledFn encode, int num_sms, ui
     // Pack operands whose rows TMA cannot address (pitch or base not 16-byte aligned).
     const void* a_ptr = pl.a.ptr;
     const void* b_ptr = pl.b.ptr;
+    auto pack = [&](const OperandDesc& o, uint8_t* dst) {
+        if (o.transpose) {
+            // source: o.cols (K) rows of o.rows (MN) elements, pitch o.ld
+            const int64_t tiles = ceil_div(o.rows, 32) * ceil_div(o.cols, 32);
+            const int64_t cap = static_cast<int64_t>(num_sms) * 8;
+            const int grid = static_cast<int>(tiles < cap ? tiles : cap);
+            transpose_rows_kernel<<<grid, 256, 0, stream>>>(
+                static_cast<const uint32_t*>(o.ptr), o.ld, o.cols, o.rows,
+                reinterpret_cast<uint32_t*>(dst), o.packed_ld);
+            return;
+        }
+        const int grid = grid_for(o.rows * o.packed_ld * pl.esize / 16, num_sms);
+        if (pl.esize == 4)
+            pack_rows_kernel<uint32_t><<<grid, 256, 0, stream>>>(
+                static_cast<const uint32_t*>(o.ptr), o.ld, o.rows, o.cols,
+                reinterpret_cast<uint32_t*>(dst), o.packed_ld);
+        else
+            pack_rows_kernel<uint16_t><<<grid, 256, 0, stream>>>(
+                static_cast<const uint16_t*>(o.ptr), o.ld, o.rows, o.cols,
+                reinterpret_cast<uint16_t*>(dst), o.packed_ld);
+    };
     if (pl.a.pack) {
-        const int grid = grid_for(pl.a.rows * pl.a.packed_ld / 8, num_sms);
-        pack_rows_kernel<<<grid, 256, 0, stream>>>(static_cast<const uint16_t*>(pl.a.ptr), pl.a.ld,
-                                                   pl.a.rows, pl.a.cols,
-                                                   reinterpret_cast<uint16_t*>(ws_a), pl.a.packed_ld);
+        pack(pl.a, ws_a);
         a_ptr = ws_a;
     }
     if (pl.b.pack) {
-        const int grid = grid_for(pl.b.rows * pl.b.packed_ld / 8, num_sms);
-        pack_rows_kernel<<<grid, 256, 0, stream>>>(static_cast<const uint16_t*>(pl.b.ptr), pl.b.ld,
-                                                   pl.b.rows, pl.b.cols,
-                                                   reinterpret_cast<uint16_t*>(ws_b), pl.b.packed_ld);
+        pack(pl.b, ws_b);
         b_ptr = ws_b;
     }
     if ((pl.a.pack || pl.b.pack) && cudaGetLastError() != cudaSuccess) return GEMM_ERR_LAUNCH;
@@ -351,10 +400,12 @@ gemm_status_t enqueue_plan(const Plan& pl, EncodeTiledFn encode, int num_sms, ui
     std::memset(&l, 0, sizeof l);
     const int bn = pl.pub.block_n;
     const int cg = pl.cta_group;
+    // MN-major boxes are one 128-byte row of M/N by block_k rows of K.
+    const uint32_t mn_box = 128u / static_cast<uint32_t>(pl.esize);
     bool ok = encode_operand(encode, &l.tmA, dt.a, a_ptr, pl.a.cols, pl.a.rows, pl.a.packed_ld,
-                             pl.a.mn_major ? 64u : static_cast<uint32_t>(kBlockM));
+                             pl.a.mn_major ? mn_box : static_cast<uint32_t>(kBlockM));
     ok = ok && encode_operand(encode, &l.tmB, dt.b, b_ptr, pl.b.cols, pl.b.rows, pl.b.packed_ld,
-                              pl.b.mn_major ? 64u : static_cast<uint32_t>(bn / cg));
+                              pl.b.mn_major ? mn_box : static_cast<uint32_t>(bn / cg));
     if (!ok) return GEMM_ERR_LAUNCH;
 
     TcParams& p = l.p;
@@ -368,8 +419,10 @@ gemm_status_t enqueue_plan(const Plan& pl, EncodeTiledFn encode, int num_sms, ui
     p.stages = pl.pub.stages;
     p.a_mn_major = pl.a.mn_major ? 1 : 0;
     p.b_mn_major = pl.b.mn_major ? 1 : 0;
-    p.idesc = instr_desc_f16(dt.a == GEMM_BF16, pl.a.mn_major, pl.b.mn_major,
-                             static_cast<uint32_t>(kBlockM * cg), static_cast<uint32_t>(bn));
+    // A/B format field: 0 F16, 1 BF16 (kind::f16); 2 TF32 (kind::tf32).
+    const uint32_t ab_format = dt.a == GEMM_F32 ? 2u : (dt.a == GEMM_BF16 ? 1u : 0u);
+    p.idesc = instr_desc(ab_format, pl.a.mn_major, pl.b.mn_major,
+                         static_cast<uint32_t>(kBlockM * cg), static_cast<uint32_t>(bn));
     p.stream_k = pl.sk_len > 0 ? 1 : 0;
     p.sk_len = pl.sk_len;
     p.sk_max_seg = pl.sk_max_seg;
@@ -396,13 +449,20 @@ gemm_status_t enqueue_plan(const Plan& pl, EncodeTiledFn encode, int num_sms, ui
     l.grid = pl.pub.grid;
     l.cta_group = cg;
     l.block_n = bn;
+    l.esize = pl.esize;
     l.smem_bytes = pl.smem_bytes;
     l.stream = stream;
 
     cudaError_t e;
-    if (dt.c == GEMM_F32) e = launch_tc_f32(l);
-    else if (dt.c == GEMM_F16) e = launch_tc_f16(l);
-    else e = launch_tc_bf16(l);
+    if (pl.esize == 4) {
+        if (dt.c == GEMM_F32) e = launch_tc_tf32_f32(l);
+        else if (dt.c == GEMM_F16) e = launch_tc_tf32_f16(l);
+        else e = launch_tc_tf32_bf16(l);
+    } else {
+        if (dt.c == GEMM_F32) e = launch_tc_f32(l);
+        else if (dt.c == GEMM_F16) e = launch_tc_f16(l);
+        else e = launch_tc_bf16(l);
+    }
     if (e != cudaSuccess) {
         cudaGetLastError();
         return GEMM_ERR_LAUNCH;

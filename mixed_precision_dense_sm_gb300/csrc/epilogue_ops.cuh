@@ -1,7 +1,7 @@
 // epilogue_ops.cuh -- element operations of the fused epilogue,
 //     r = act(alpha * acc + beta * C + bias[n]),
-// the CATLASS page's "keep the GEMM mainloop, replace the epilogue" (section
-// 5.2) in its usual linear-layer form: a per-output-column bias and one of
+// the CATLASS page's fusion by a replaced epilogue after an unchanged mainloop
+// (section 5.2), in its usual linear-layer form: a per-output-column bias and one of
 // ReLU, GELU (erf form) or SiLU, evaluated in FP32 before the output cast.
 #pragma once
 #include <cstdint>

@@ -56,13 +56,19 @@
 namespace gemm103 {
 
 constexpr int kBlockM = 128;      // tcgen05 M (cta_group::1)
-constexpr int kBlockK = 64;       // 64 16-bit elements = one 128-byte swizzle row
-constexpr int kUmmaK = 16;        // K per tcgen05.mma kind::f16
+// One pipeline stage holds one 128-byte swizzle row of K per operand row:
+// 64 16-bit elements (kind::f16, K = 16 per MMA) or 32 FP32 elements used as
+// TF32 (kind::tf32, K = 8 per MMA); either way 4 MMAs per stage.
+template <int ES> struct Elem {
+    static constexpr int kBlockK = 128 / ES;        // K elements per stage
+    static constexpr int kUmmaK = 32 / ES;          // K per tcgen05.mma
+    static constexpr int kMNChunk = 128 / ES;       // M/N elements per MN-major box row
+    static constexpr uint32_t kChunkBytes = kMNChunk * kBlockK * ES;   // one MN-major box
+};
 constexpr int kThreads = 320;     // warp 0 producer, warp 1 MMA, warps 2-9 epilogue
 constexpr int kEpiWarps = 8;      // two per TMEM lane quarter, splitting the columns
 constexpr int kFinBatch = 2;      // stream-K finisher: partial slots loaded per batch
-constexpr uint32_t kATileBytes = kBlockM * kBlockK * 2;   // 16 KB
-constexpr uint32_t kChunkBytes = 64 * kBlockK * 2;        // one 64 x 64 MN-major box, 8 KB
+constexpr uint32_t kATileBytes = kBlockM * 128;          // 16 KB: 128 rows of 128 bytes
 
 enum : int { kErrTimeoutProducer = 1, kErrTimeoutMma = 2, kErrTimeoutEpilogue = 3 };
 
@@ -403,15 +409,20 @@ __device__ __forceinline__ bool epilogue_all(bool ok) {
     return r != 0;
 }
 
-template <int CG, int BN, typename OutT>
+template <int CG, int BN, typename OutT, int ES>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ TcParams p) {
     static_assert(BN == 64 || BN == 128 || BN == 256, "BN");
     static_assert(CG == 1 || (CG == 2 && BN >= 128), "CG");
+    static_assert(ES == 2 || ES == 4, "element size");
+    constexpr int kBlockK = Elem<ES>::kBlockK;
+    constexpr int kUmmaK = Elem<ES>::kUmmaK;
+    constexpr int kMNChunk = Elem<ES>::kMNChunk;
+    constexpr uint32_t kChunkBytes = Elem<ES>::kChunkBytes;
     constexpr int BM = kBlockM * CG;                      // rows per (pair) tile
     constexpr uint32_t kBRows = BN / CG;                  // B rows this CTA loads
-    constexpr uint32_t kBTileBytes = kBRows * kBlockK * 2;
+    constexpr uint32_t kBTileBytes = kBRows * 128;
     constexpr uint32_t kStageBytes = kATileBytes + kBTileBytes;
     constexpr uint32_t kTmemCols = 2 * BN;               // double-buffered accumulator
 
@@ -485,13 +496,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 auto a_parts = [&](int32_t m_first) {
                     if (!p.a_mn_major) return (m_first < p.M) ? 1 : 0;
                     int n = 0;
-                    for (int c = 0; c < kBlockM / 64; ++c) n += (m_first + 64 * c < p.M);
+                    for (int c = 0; c < kBlockM / kMNChunk; ++c) n += (m_first + kMNChunk * c < p.M);
                     return n;
                 };
                 auto b_parts = [&](int32_t n_first) {
                     if (!p.b_mn_major) return (n_first < p.N) ? 1 : 0;
                     int n = 0;
-                    for (int c = 0; c < static_cast<int>(kBRows) / 64; ++c) n += (n_first + 64 * c < p.N);
+                    for (int c = 0; c < static_cast<int>(kBRows) / kMNChunk; ++c)
+                        n += (n_first + kMNChunk * c < p.N);
                     return n;
                 };
                 auto tile_bytes = [&](uint32_t r) {
@@ -533,14 +545,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                         mbar_arrive_expect_tx(&full[stage], bytes);
                         if (p.a_mn_major) {
                             for (int c = 0; c < na; ++c)
-                                tma_load_2d(sa + c * kChunkBytes, &tmA, &full[stage], m0 + 64 * c,
+                                tma_load_2d(sa + c * kChunkBytes, &tmA, &full[stage], m0 + kMNChunk * c,
                                             k0, pol_a);
                         } else if (na) {
                             tma_load_2d(sa, &tmA, &full[stage], k0, m0, pol_a);
                         }
                         if (p.b_mn_major) {
                             for (int c = 0; c < nb; ++c)
-                                tma_load_2d(sb + c * kChunkBytes, &tmB, &full[stage], n0 + 64 * c,
+                                tma_load_2d(sb + c * kChunkBytes, &tmB, &full[stage], n0 + kMNChunk * c,
                                             k0, pol_b);
                         } else if (nb) {
                             tma_load_2d(sb, &tmB, &full[stage], k0, n0, pol_b);
@@ -550,14 +562,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (rank == 0) mbar_arrive_expect_tx(&full[stage], bytes);
                         if (p.a_mn_major) {
                             for (int c = 0; c < na; ++c)
-                                tma_load_2d_pair(sa + c * kChunkBytes, &tmA, fb, m0 + 64 * c, k0,
+                                tma_load_2d_pair(sa + c * kChunkBytes, &tmA, fb, m0 + kMNChunk * c, k0,
                                                  pol_a);
                         } else if (na) {
                             tma_load_2d_pair(sa, &tmA, fb, k0, m0, pol_a);
                         }
                         if (p.b_mn_major) {
                             for (int c = 0; c < nb; ++c)
-                                tma_load_2d_pair(sb + c * kChunkBytes, &tmB, fb, n0 + 64 * c, k0,
+                                tma_load_2d_pair(sb + c * kChunkBytes, &tmB, fb, n0 + kMNChunk * c, k0,
                                                  pol_b);
                         } else if (nb) {
                             tma_load_2d_pair(sb, &tmB, fb, k0, n0, pol_b);
@@ -592,8 +604,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool ok = true;
             const uint32_t a_lbo = p.a_mn_major ? kChunkBytes : 16u;
             const uint32_t b_lbo = p.b_mn_major ? kChunkBytes : 16u;
-            const uint32_t a_kstep = p.a_mn_major ? kUmmaK * 128u : kUmmaK * 2u;
-            const uint32_t b_kstep = p.b_mn_major ? kUmmaK * 128u : kUmmaK * 2u;
+            // advance per MMA: K-major 32 bytes within the 128-byte row;
+            // MN-major kUmmaK rows of 128 bytes
+            const uint32_t a_kstep = p.a_mn_major ? kUmmaK * 128u : kUmmaK * ES;
+            const uint32_t b_kstep = p.b_mn_major ? kUmmaK * 128u : kUmmaK * ES;
             const uint32_t smem_base = smem_addr(smem);
             while (ok && it.next(p, sg)) {
                 const uint32_t buf = acc_i & 1u;
@@ -617,8 +631,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const uint64_t ad = smem_desc_sw128(sa + kk * a_kstep, a_lbo, 1024);
                         const uint64_t bd = smem_desc_sw128(sb + kk * b_kstep, b_lbo, 1024);
                         const uint32_t acc = (kb > sg.kb0 || kk > 0) ? 1u : 0u;
-                        if constexpr (CG == 1) tc_mma_f16(d_tmem, ad, bd, p.idesc, acc);
-                        else tc_mma_f16_pair(d_tmem, ad, bd, p.idesc, acc);
+                        if constexpr (ES == 4) {
+                            if constexpr (CG == 1) tc_mma_tf32(d_tmem, ad, bd, p.idesc, acc);
+                            else tc_mma_tf32_pair(d_tmem, ad, bd, p.idesc, acc);
+                        } else {
+                            if constexpr (CG == 1) tc_mma_f16(d_tmem, ad, bd, p.idesc, acc);
+                            else tc_mma_f16_pair(d_tmem, ad, bd, p.idesc, acc);
+                        }
                     }
                     if constexpr (CG == 1) tc_commit(&empty[stage]);
                     else tc_commit_pair_multicast(&empty[stage], 0x3);

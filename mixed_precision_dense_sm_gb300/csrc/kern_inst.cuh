@@ -1,6 +1,7 @@
-// kern_inst.cuh -- instantiates the tcgen05 GEMM for one output type
-// (KERN_OUT_T): single-CTA tiles of width 64/128/256 and CTA-pair tiles of
-// width 256, behind a plain launcher.
+// kern_inst.cuh -- instantiates the tcgen05 GEMM for one input element size
+// (KERN_ES bytes: 2 for FP16/BF16, 4 for FP32 used as TF32) and one output
+// type (KERN_OUT_T): single-CTA tiles of width 64/128/256 and CTA-pair tiles
+// of width 256, behind a plain launcher.
 #pragma once
 #include <mutex>
 
@@ -13,7 +14,7 @@ namespace gemm103 {
 
 template <int CG, int BN>
 static cudaError_t launch_tc_cfg(const TcLaunch& l) {
-    auto kern = gemm_tc_kernel<CG, BN, KERN_OUT_T>;
+    auto kern = gemm_tc_kernel<CG, BN, KERN_OUT_T, KERN_ES>;
     {
         // The dynamic shared-memory limit is raised once per size (a host
         // call worth avoiding on every launch of a microsecond-scale GEMM).
@@ -71,6 +72,7 @@ static cudaError_t launch_tc_cfg(const TcLaunch& l) {
 }
 
 cudaError_t GEMM103_CAT(launch_tc_, KERN_SUFFIX)(const TcLaunch& l) {
+    if (l.esize != KERN_ES) return cudaErrorInvalidValue;
     if (l.cta_group == 2) {
         switch (l.block_n) {
             case 256: return launch_tc_cfg<2, 256>(l);

@@ -1,0 +1,6 @@
+// kern_tf32_f32.cu -- tcgen05 GEMM kernels with FP32 inputs used as TF32
+// (kind::tf32) and f32 output.
+#define KERN_OUT_T float
+#define KERN_SUFFIX tf32_f32
+#define KERN_ES 4
+#include "kern_inst.cuh"

@@ -15,13 +15,18 @@ struct TcLaunch {
     int grid;
     int cta_group;      // 1: single-CTA tiles, 2: CTA-pair tiles
     int block_n;
+    int esize;          // input element bytes: 2 (FP16/BF16) or 4 (FP32 used as TF32)
     size_t smem_bytes;
     cudaStream_t stream;
 };
 
-// Output type codes follow gemm_dtype_t: 0 = F16, 1 = BF16, 2 = F32.
+// One launcher per (input element size, output type); the output type codes
+// follow gemm_dtype_t: 0 = F16, 1 = BF16, 2 = F32.
 cudaError_t launch_tc_f32(const TcLaunch& l);
 cudaError_t launch_tc_f16(const TcLaunch& l);
 cudaError_t launch_tc_bf16(const TcLaunch& l);
+cudaError_t launch_tc_tf32_f32(const TcLaunch& l);
+cudaError_t launch_tc_tf32_f16(const TcLaunch& l);
+cudaError_t launch_tc_tf32_bf16(const TcLaunch& l);
 
 }  // namespace gemm103

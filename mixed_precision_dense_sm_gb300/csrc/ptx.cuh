@@ -147,6 +147,17 @@ __device__ __forceinline__ void tc_mma_f16(uint32_t d_tmem, uint64_t a_desc, uin
         : "memory");
 }
 
+// kind::tf32: FP32 operands in shared memory enter the product as TF32.
+__device__ __forceinline__ void tc_mma_tf32(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                            uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 // Arrive once on `bar` when every tcgen05 operation this thread issued so far
 // has completed.
 __device__ __forceinline__ void tc_commit(uint64_t* bar) {
@@ -198,14 +209,15 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
     return d;
 }
 
-// Instruction descriptor for tcgen05.mma kind::f16 with an FP32 accumulator:
-//   bits 4-5 D format (1 = F32)     bits 7-9 A format (0 = F16, 1 = BF16)
+// Instruction descriptor for tcgen05.mma kind::f16 / kind::tf32 with an FP32
+// accumulator:
+//   bits 4-5 D format (1 = F32)     bits 7-9 A format (0 = F16, 1 = BF16, 2 = TF32)
 //   bits 10-12 B format             bit 15 A major (0 = K, 1 = MN)
 //   bit 16 B major                  bits 17-22 N >> 3
 //   bits 24-28 M >> 4
-__host__ __device__ constexpr uint32_t instr_desc_f16(bool bf16, bool a_mn_major,
-                                                      bool b_mn_major, uint32_t m, uint32_t n) {
-    return (1u << 4) | ((bf16 ? 1u : 0u) << 7) | ((bf16 ? 1u : 0u) << 10) |
+__host__ __device__ constexpr uint32_t instr_desc(uint32_t ab_format, bool a_mn_major,
+                                                  bool b_mn_major, uint32_t m, uint32_t n) {
+    return (1u << 4) | (ab_format << 7) | (ab_format << 10) |
            ((a_mn_major ? 1u : 0u) << 15) | ((b_mn_major ? 1u : 0u) << 16) |
            ((n >> 3) << 17) | ((m >> 4) << 24);
 }
@@ -298,6 +310,16 @@ __device__ __forceinline__ void tc_mma_f16_pair(uint32_t d_tmem, uint64_t a_desc
         "{\n\t.reg .pred p;\n\t"
         "setp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void tc_mma_tf32_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                                 uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
         "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
 }

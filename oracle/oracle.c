@@ -10,9 +10,9 @@
  *
  * What it computes, and the passage each step follows:
  *
- *   - Semantics.  "C[i][j] accumulates A[i][k] * B[k][j]" -- the naive i-j-k
- *     triple loop of the SGEMM tutorial page (section 3.1), and "C = A * B + C"
- *     of the CATLASS page (section 2.1).  alpha/beta scaling and op() are the
+ *   - Semantics.  Each C[i][j] sums A[i][k] * B[k][j] over k -- the naive
+ *     triple loop of the SGEMM tutorial page (section 3.1) -- and the
+ *     formula C = A * B + C of the CATLASS page (section 2.1).  alpha/beta scaling and op() are the
  *     BLAS reading of that formula (the pages never name alpha or beta):
  *       r_ij = alpha * sum_k op(A)_ik op(B)_kj + beta * C_ij.
  *   - Precision.  Inputs are FP16 or BF16 -- or FP32 used as TF32 (the third
@@ -163,10 +163,11 @@ float oracle_round_f32(double x) { return (float)x; }
 /* ------------------------------------------------------------------- GEMM */
 
 /* TF32 inputs: FP32 storage whose value enters the product with its mantissa
- * cut to the 10 bits TF32 keeps -- "TF32 truncates the FP32 data to a 10-bit
- * mantissa inside the tensor core; inputs and outputs stay FP32 in memory"
- * (CATLASS page, section 3.2).  The low 13 mantissa bits are dropped (round
- * toward zero); the sign, the 8-bit exponent and infinities/NaNs are kept. */
+ * cut to the 10 bits TF32 keeps.  The CATLASS page (section 3.2) describes
+ * TF32 as FP32 data that stays FP32 in memory and is cut short to a 10-bit
+ * mantissa only inside the tensor core.  Reading "cut short" as truncation,
+ * the low 13 mantissa bits are dropped (round toward zero); the sign, the
+ * 8-bit exponent and infinities/NaNs are kept. */
 double oracle_decode_tf32(uint32_t u) {
     const uint32_t e = (u >> 23) & 0xFFu;
     if (e == 0xFFu) return oracle_decode_f32(u);          /* inf / NaN unchanged */
@@ -340,10 +341,10 @@ int oracle_max_threads(void) {
 /* --------------------------------------------------- fused epilogue oracle */
 
 /*
- * Fused epilogue ("keep the GEMM mainloop, replace the epilogue": CATLASS
- * page, section 5.2, which names residual add and activations next to the
- * linear layer; the page gives no formula).  Read as the usual linear-layer
- * form
+ * Fused epilogue.  The CATLASS page (section 5.2) fuses work into the GEMM
+ * by swapping in a different epilogue after an unchanged mainloop, and names
+ * residual add and activations next to the linear layer; it gives no
+ * formula.  Read as the usual linear-layer form
  *     r_ij = act(alpha * sum_k op(A)_ik op(B)_kj + beta * C_ij + bias_j)
  * with act one of: none, ReLU (x if x > 0, else 0; NaN stays NaN),
  * GELU in its erf form x * Phi(x) = 0.5 x (1 + erf(x / sqrt 2)), and

@@ -12,6 +12,7 @@ import workloads
 from workloads import DT_BF16, DT_F16, DT_F32
 
 F16F32 = (DT_F16, DT_F16, DT_F32)
+TF32 = (DT_F32, DT_F32, DT_F32)
 
 
 def test_exports_every_declared_symbol():
@@ -55,13 +56,22 @@ def test_check_args():
     for bad in [dict(ta="X"), dict(tb="?"), dict(M=-1), dict(N=-2), dict(K=-3),
                 dict(lda=7), dict(ldb=7), dict(ldc=7), dict(ta="T", lda=7, M=8),
                 dict(tb="T", ldb=7), dict(dt=(DT_F16, DT_BF16, DT_F32)),
-                dict(dt=(DT_F32, DT_F32, DT_F32)), dict(dt=(DT_F16, DT_F16, 5)),
-                dict(A=0), dict(B=0), dict(C=0), dict(M=2 ** 31)]:
+                dict(dt=(DT_F32, DT_F16, DT_F32)), dict(dt=(DT_BF16, DT_F32, DT_F32)),
+                dict(dt=(DT_F16, DT_F16, 5)), dict(dt=(3, 3, DT_F32)),
+                dict(A=0), dict(B=0), dict(C=0), dict(M=2 ** 31),
+                # each pointer aligned to its own element size
+                dict(A=17), dict(B=19), dict(C=18), dict(C=17, dt=(DT_F16, DT_F16, DT_F16)),
+                dict(A=18, dt=TF32), dict(B=22, dt=TF32)]:
         assert call(**bad) == 1, bad
+    # FP32 inputs are computed as TF32
+    assert call(dt=TF32) == 0
+    assert call(dt=(DT_F32, DT_F32, DT_BF16), C=18) == 0
+    assert call(A=18, B=30) == 0                     # 2-byte aligned FP16 operands
     # quick-return forms
     assert call(M=0, C=0, A=0, B=0) == 0
     assert call(K=0, A=0, B=0) == 0
     assert call(alpha=0.0, A=0, B=0) == 0
+    assert call(alpha=0.0, A=17, B=17) == 0          # A and B are not read
     assert call(K=0, lda=1) == 0
 
 
@@ -87,10 +97,13 @@ def test_plans_of_named_workloads():
     assert rag["b_mn_major"] == 1 and rag["a_mn_major"] == 0
     sq = P["square1024_f16_nt_f16out"]
     assert sq["pack_a"] == 0 and sq["pack_b"] == 0 and sq["b_mn_major"] == 0
-    for p in P.values():
+    for n, p in P.items():
         assert 2 <= p["stages"] <= 8
         cg = p["block_m"] // 128
-        stage = 128 * 64 * 2 + (p["block_n"] // cg) * 64 * 2
+        esize = 4 if workloads.WORKLOADS[n].ab_dtype == DT_F32 else 2
+        assert p["block_k"] * esize == 128          # one 128-byte swizzle row of K per stage
+        assert p["k_blocks"] == -(-workloads.WORKLOADS[n].K // p["block_k"])
+        stage = 128 * 128 + (p["block_n"] // cg) * 128
         assert p["stages"] * stage + 1024 + 256 <= 232448
 
 
@@ -124,8 +137,58 @@ def test_pack_rule_follows_16_byte_alignment():
                            lda=104, ldb=100 + 3)
     p = plan(w)
     assert p["pack_a"] == 0 and p["pack_b"] == 1
-    p = plan(w, ptr=258)          # misaligned base: everything packs, C scalar path
+    p = plan(w, ptr=260)          # misaligned base: everything packs, C scalar path
     assert p["pack_a"] == 1 and p["pack_b"] == 1 and p["c_vector"] == 0
+
+
+def test_tf32_plans():
+    """FP32 inputs (TF32): 32 elements of K per stage, the same tile shapes
+    and rules as 16-bit inputs, packing when rows are not 16-byte aligned
+    (a pitch that is not a multiple of 4 elements)."""
+    w = workloads.WORKLOADS["tf32_linear_8192x4096x4096_f32out"]
+    p = plan(w)
+    assert p["path_name"] == "tiled_2sm" and p["block_k"] == 32 and p["k_blocks"] == 128
+    assert p["pack_a"] == 0 and p["pack_b"] == 0
+    w = workloads.Workload("t", 100, 100, 100, "N", "N", DT_F32, DT_F32, 1.0, 0.0, "U", "U",
+                           lda=104, ldb=102)
+    p = plan(w)
+    assert p["pack_a"] == 0 and p["pack_b"] == 1 and p["k_blocks"] == 4
+    p = plan(w, ptr=260)          # 4-byte but not 16-byte aligned base: everything packs
+    assert p["pack_a"] == 1 and p["pack_b"] == 1 and p["c_vector"] == 0
+    w = workloads.Workload("t", 64, 16384, 8192, "N", "T", DT_F32, DT_F32, 1.0, 0.0, "U", "U")
+    p = plan(w)
+    assert p["path_name"] == "skinny" and p["sk_len"] > 0 and p["k_blocks"] == 256
+    # the same rules as the 16-bit path, for every tile width
+    for M, N, K in [(1000, 1023, 777), (4096, 4096, 4096), (257, 129, 4096), (64, 1000, 513)]:
+        a = plan(workloads.Workload("t", M, N, K, "N", "N", DT_F32, DT_F32, 1.0, 0.0, "U", "U",
+                                    lda=K + 4, ldb=N + 4))
+        b = plan(workloads.Workload("h", M, N, K, "N", "N", DT_F16, DT_F32, 1.0, 0.0, "U", "U",
+                                    lda=K + 8, ldb=N + 8))
+        for key in ("path_name", "block_m", "block_n", "swap_ab", "tiles_m", "tiles_n"):
+            assert a[key] == b[key], (M, N, K, key)
+        assert a["k_blocks"] == -(-K // 32)
+
+
+def test_tf32_operands_stored_mn_major_are_transposed_first():
+    """kind::tf32 reads K-major operands only: an FP32 operand stored with
+    M or N contiguous (A with 'T', B with 'N') is rewritten K-contiguous by a
+    pre-pass into the workspace; 16-bit operands never are."""
+    M, N, K = 300, 400, 500
+    for ta, tb, want in [("N", "T", 0), ("N", "N", 2), ("T", "T", 1), ("T", "N", 3)]:
+        p = plan(workloads.Workload("t", M, N, K, ta, tb, DT_F32, DT_F32, 1.0, 0.0, "U", "U"))
+        assert p["transpose_ab"] == want, (ta, tb, p)
+        assert p["a_mn_major"] == 0 and p["b_mn_major"] == 0
+        assert p["pack_a"] == (want & 1) and p["pack_b"] == (want >> 1)
+        need = (M * 500 if want & 1 else 0) * 4 + (N * 500 if want & 2 else 0) * 4
+        assert p["workspace_bytes"] >= need
+        h = plan(workloads.Workload("h", M, N, K, ta, tb, DT_BF16, DT_F32, 1.0, 0.0, "U", "U"))
+        assert h["transpose_ab"] == 0
+        assert h["a_mn_major"] == (ta == "T") and h["b_mn_major"] == (tb == "N")
+    # the swapped skinny path reports the user's operands
+    p = plan(workloads.Workload("s", 32, 4096, 512, "N", "N", DT_F32, DT_F32, 1.0, 0.0, "U", "U"))
+    assert p["swap_ab"] == 1 and p["transpose_ab"] == 2 and p["pack_b"] == 1 and p["pack_a"] == 0
+    p = plan(workloads.Workload("s", 32, 4096, 512, "T", "T", DT_F32, DT_F32, 1.0, 0.0, "U", "U"))
+    assert p["swap_ab"] == 1 and p["transpose_ab"] == 1 and p["pack_a"] == 1 and p["pack_b"] == 0
 
 
 def simulate_stream_k(p):

@@ -167,8 +167,9 @@ def test_invalid_arguments_enqueue_nothing(g):
     s = torch.cuda.current_stream().cuda_stream
     bad = [
         dict(ta="X"), dict(M=-1), dict(lda=7), dict(ldb=7), dict(ldc=7),
-        dict(dts=(DT_F16, DT_BF16, DT_F32)), dict(dts=(DT_F32, DT_F32, DT_F32)),
+        dict(dts=(DT_F16, DT_BF16, DT_F32)), dict(dts=(DT_F32, DT_F16, DT_F32)),
         dict(dts=(DT_F16, DT_F16, 9)), dict(a=0), dict(c=0),
+        dict(a=A.data_ptr() + 1), dict(c=C.data_ptr() + 2),
     ]
     for b in bad:
         kw = dict(ta="N", M=8, lda=8, ldb=8, ldc=8, dts=(DT_F16, DT_F16, DT_F32),

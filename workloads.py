@@ -70,7 +70,7 @@ class Workload:
 
     def algorithmic_bytes(self) -> int:
         """A and B read once, C written once, C also read when beta != 0."""
-        e_ab = 2
+        e_ab = 4 if self.ab_dtype == DT_F32 else 2
         e_c = 4 if self.c_dtype == DT_F32 else 2
         b = (self.M * self.K + self.K * self.N) * e_ab + self.M * self.N * e_c
         if self.beta != 0:
@@ -92,6 +92,8 @@ WORKLOADS = {
                  DT_BF16, 1.0, 0.0, "N1", "N002"),
         Workload("linear_8192x4096x14336_bf16", 8192, 4096, 14336, "N", "T", DT_BF16,
                  DT_BF16, 1.0, 0.0, "N1", "N002"),
+        Workload("tf32_linear_8192x4096x4096_f32out", 8192, 4096, 4096, "N", "T", DT_F32,
+                 DT_F32, 1.0, 0.0, "N1", "N002"),
         Workload("skinny_64x16384x8192_f16", 64, 16384, 8192, "N", "T", DT_F16, DT_F16,
                  1.0, 0.0, "N1", "N002"),
     ]
@@ -119,7 +121,7 @@ def _stored(values: torch.Tensor, ld: int, dtype: torch.dtype) -> torch.Tensor:
 
 @dataclasses.dataclass
 class Inputs:
-    A: torch.Tensor   # stored (rows x lda), CPU, FP16/BF16
+    A: torch.Tensor   # stored (rows x lda), CPU, FP16/BF16 (or FP32 used as TF32)
     B: torch.Tensor   # stored (rows x ldb)
     C: Optional[torch.Tensor]   # stored (M x ldc) in the output dtype, or None
     lda: int
