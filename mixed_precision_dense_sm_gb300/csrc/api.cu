@@ -27,11 +27,11 @@ namespace {
 
 constexpr int kMaxStages = 8;
 constexpr int kGroupM = 8;
-// Workspace header: two stream-K counters (int32: arrived, written) per output
-// tile.  Stream-K is only planned with fewer tiles than SMs, so 512 tiles'
-// worth always suffices.
+// Workspace header: one stream-K counter (int32: contributors that have
+// stored their sums) per output tile.  Stream-K is only planned with fewer
+// tiles than SMs, so 1024 tiles' worth always suffices.
 constexpr int64_t kWsHeaderBytes = 4096;
-constexpr int64_t kMaxCounterTiles = kWsHeaderBytes / 8;
+constexpr int64_t kMaxCounterTiles = kWsHeaderBytes / 4;
 
 struct OperandDesc {
     // stored matrix: rows x cols with pitch ld (elements); K-major means the

@@ -90,7 +90,7 @@ struct TcParams {
     int64_t c_rs, c_cs;         // D'(i, j) -> C[i * c_rs + j * c_cs]
     int32_t c_vector;           // c_cs == 1 and rows 16-byte aligned
     float* partials;            // stream-K slots: [G * sk_max_seg][BM][BN] FP32
-    int* tile_counters;         // stream-K: per tile {arrived, written} (self-resetting)
+    int* tile_counters;         // stream-K: per split tile, contributors written (self-resetting)
     int* err;                   // device-visible error word (0 = ok)
     int32_t a_stream_once;      // 1: A is read once (evict-first in L2), 0: reused
     int32_t b_stream_once;
@@ -473,6 +473,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     if constexpr (CG == 2) cluster_sync_all();            // peer barriers initialised
     tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_slot;
+    // Everything above (barrier set-up, TMEM allocation, descriptor prefetch)
+    // may overlap the previous kernel on the stream; nothing below touches
+    // global memory before that kernel has completed.
+    grid_dependency_wait();
 
     if (warp == 0) {
         // ------------------------------------------------------ TMA producer
@@ -582,6 +586,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             }
+            // Every load of this CTA is issued: the next kernel on the stream
+            // may begin its own set-up on SMs as they free up.
+            grid_dependents_launch();
             // Wind-down: wait (bounded) until every TMA load issued into this
             // CTA pair has landed.  The even CTA's "full" barriers count the
             // bytes of both CTAs, so only the even CTA waits; the odd CTA is
@@ -667,56 +674,111 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t acc_i = 0;
         SegmentIter it(p, unit, units);
         Segment sg;
+        __shared__ int wait_ok;
         while (it.next(p, sg)) {
             const uint32_t buf = acc_i & 1u;
-            bool ok = wait_or_abort(&acc_full[buf], (acc_i >> 1) & 1u, &abort_flag, p.wait_limit_ns);
+            int32_t tm, tn;
+            tile_coords(p, sg.tile, tm, tn);
+            const int32_t row = tm * BM + row_in_tile;              // D' row
+            const int32_t col0 = tn * BN;                           // D' first column
+            const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
+            const uint32_t t_row = t_lane + buf * BN;               // this tile's sums
+            const uint32_t t_spare = t_lane + (buf ^ 1u) * BN;     // the other buffer
+
+            // Stream-K tile split across CTAs g_first..g_last.  g_first, which
+            // holds the tile's first k-blocks, finishes it.  For g_first this
+            // segment is the last of its range (a range is at most one tile
+            // long), so it ends last, the MMA warp will not write the other
+            // TMEM buffer again, and the epilogue warps are idle until its sums
+            // arrive.  They use that time: wait (bounded) until every other
+            // contributor has stored its sums and counted itself on the tile's
+            // counter, add those sums in increasing CTA order and park the
+            // total in the spare TMEM buffer.  When the finisher's own sums
+            // land, total + own goes through the epilogue -- the same order on
+            // every run.  The others store their sums to their slot.
+            const int32_t KB = p.k_blocks, L = p.sk_len;
+            int32_t g_first = 0, g_last = -1;
+            bool finisher = false;
+            bool ok = true;
+            if (sg.slot >= 0) {
+                g_first = static_cast<int32_t>((static_cast<int64_t>(sg.tile) * KB) / L);
+                g_last = static_cast<int32_t>((static_cast<int64_t>(sg.tile + 1) * KB - 1) / L);
+                finisher = (unit == g_first);
+            }
+            if (finisher) {
+                int* written = p.tile_counters + sg.tile;
+                if (warp == 2 && lane == 0) {
+                    const bool w = wait_counter(written, g_last - g_first, &abort_flag, p.wait_limit_ns);
+                    if (w) *written = 0;                    // self-resetting for the next call
+                    else record_error(p, kErrTimeoutEpilogue, &abort_flag);
+                    wait_ok = w ? 1 : 0;
+                }
+                epilogue_bar_sync();
+                ok = (wait_ok != 0);
+                __threadfence();
+                if (ok) {
+                    #pragma unroll 1
+                    for (int ch = half; ch < BN / 32; ch += 2) {
+                        float acc[32];
+                        #pragma unroll
+                        for (int j = 0; j < 32; ++j) acc[j] = 0.0f;
+                        // 16 columns at a time, up to kFinBatch slots' loads in
+                        // flight together
+                        #pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            for (int32_t g0 = g_first + 1; g0 <= g_last; g0 += kFinBatch) {
+                                float x[kFinBatch][16];
+                                #pragma unroll
+                                for (int u = 0; u < kFinBatch; ++u) {
+                                    const int32_t g = g0 + u;
+                                    if (g > g_last) continue;
+                                    const int32_t first_tile =
+                                        static_cast<int32_t>((static_cast<int64_t>(g) * L) / KB);
+                                    const float* src = p.partials +
+                                                       (static_cast<int64_t>(g) * p.sk_max_seg +
+                                                        (sg.tile - first_tile)) * BM * BN;
+                                    if (p.c_cs == 1) {
+                                        const float4* s4 = reinterpret_cast<const float4*>(
+                                            src + row_in_tile * BN + ch * 32 + h * 16);
+                                        #pragma unroll
+                                        for (int q = 0; q < 4; ++q) {
+                                            const float4 t = __ldcg(s4 + q);
+                                            x[u][4 * q] = t.x;
+                                            x[u][4 * q + 1] = t.y;
+                                            x[u][4 * q + 2] = t.z;
+                                            x[u][4 * q + 3] = t.w;
+                                        }
+                                    } else {
+                                        #pragma unroll
+                                        for (int j = 0; j < 16; ++j)
+                                            x[u][j] = __ldcg(src + (ch * 32 + h * 16 + j) * BM + row_in_tile);
+                                    }
+                                }
+                                #pragma unroll
+                                for (int u = 0; u < kFinBatch; ++u) {
+                                    if (g0 + u > g_last) break;
+                                    #pragma unroll
+                                    for (int j = 0; j < 16; ++j) acc[h * 16 + j] += x[u][j];
+                                }
+                            }
+                        }
+                        uint32_t r[32];
+                        #pragma unroll
+                        for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(acc[j]);
+                        __syncwarp();                  // tcgen05.st is warp-collective
+                        tmem_st_32x32b_x32(t_spare + ch * 32, r);
+                    }
+                    tmem_st_wait();
+                }
+            }
+            ok = ok && wait_or_abort(&acc_full[buf], (acc_i >> 1) & 1u, &abort_flag, p.wait_limit_ns);
             if (p.stream_k) ok = epilogue_all(ok);        // stream-K uses named barriers below
             if (!ok) {
                 record_error(p, kErrTimeoutEpilogue, &abort_flag);
                 break;
             }
             tc_fence_after_sync();
-            int32_t tm, tn;
-            tile_coords(p, sg.tile, tm, tn);
-            const int32_t row = tm * BM + row_in_tile;              // D' row
-            const int32_t col0 = tn * BN;                           // D' first column
-            const uint32_t t_row = tmem_base + buf * BN + (static_cast<uint32_t>(quarter * 32) << 16);
 
-            // Stream-K tile split across CTAs g_first..g_last.  Each
-            // contributor counts itself on the tile's "arrive" counter as soon
-            // as its sums are in TMEM.  The last to arrive is the finisher: it
-            // keeps its own sums in registers, waits (bounded) until the others
-            // have stored theirs and counted them on the "written" counter,
-            // then adds all contributions in increasing CTA order -- the same
-            // order whichever CTA finishes -- applies the epilogue and resets
-            // both counters.  The others store their sums to their slot.
-            const int32_t KB = p.k_blocks, L = p.sk_len;
-            int32_t g_first = 0, g_last = -1;
-            bool finisher = false;
-            __shared__ int role_flag;
-            if (sg.slot >= 0) {
-                g_first = static_cast<int32_t>((static_cast<int64_t>(sg.tile) * KB) / L);
-                g_last = static_cast<int32_t>((static_cast<int64_t>(sg.tile + 1) * KB - 1) / L);
-                int* arrive = p.tile_counters + 2 * sg.tile;
-                if (warp == 2 && lane == 0) {
-                    const int old = atomicAdd(arrive, 1);
-                    const int last = (old == g_last - g_first) ? 1 : 0;
-                    if (last) *arrive = 0;
-                    role_flag = last;
-                }
-                epilogue_bar_sync();
-                finisher = (role_flag != 0);
-                if (finisher) {
-                    epilogue_bar_sync();                   // everyone has read role_flag
-                    if (warp == 2 && lane == 0) {
-                        const bool ok_w = wait_counter(arrive + 1, g_last - g_first, &abort_flag, p.wait_limit_ns);
-                        if (ok_w) arrive[1] = 0;
-                        else record_error(p, kErrTimeoutEpilogue, &abort_flag);
-                    }
-                    epilogue_bar_sync();
-                    __threadfence();
-                }
-            }
             float* my_slot = (sg.slot >= 0 && !finisher)
                                  ? p.partials + static_cast<int64_t>(sg.slot) * BM * BN
                                  : nullptr;
@@ -729,71 +791,28 @@ __global__ void __launch_bounds__(kThreads, 1)
                 float v[32];
                 #pragma unroll
                 for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+                if (finisher) {
+                    uint32_t o[32];
+                    __syncwarp();
+                    tmem_ld_32x32b_x32(t_spare + ch * 32, o);
+                    tmem_ld_wait();
+                    #pragma unroll
+                    for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(o[j]) + v[j];
+                }
                 const int32_t c0 = col0 + ch * 32;
-                if (sg.slot < 0) {
+                if (my_slot == nullptr) {
                     store_chunk<OutT>(p, row, c0, v);
-                } else if (my_slot != nullptr) {
+                } else if (p.c_cs == 1) {
                     // raw FP32 sums, laid out along C's contiguous direction:
                     // [row][col] when C rows are contiguous (c_cs == 1),
                     // [col][row] otherwise, so every warp store is coalesced
-                    if (p.c_cs == 1) {
-                        float4* dst = reinterpret_cast<float4*>(my_slot + row_in_tile * BN + ch * 32);
-                        #pragma unroll
-                        for (int q = 0; q < 8; ++q)
-                            dst[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-                    } else {
-                        #pragma unroll
-                        for (int j = 0; j < 32; ++j) my_slot[(ch * 32 + j) * BM + row_in_tile] = v[j];
-                    }
+                    float4* dst = reinterpret_cast<float4*>(my_slot + row_in_tile * BN + ch * 32);
+                    #pragma unroll
+                    for (int q = 0; q < 8; ++q)
+                        dst[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
                 } else {
-                    // finisher: acc = sum of contributions g_first..g_last in
-                    // that order, its own (g == unit) from registers.  Loads of
-                    // up to kFinBatch slots are issued together, 16 columns at a
-                    // time, so their memory latencies overlap.
-                    float acc[32];
                     #pragma unroll
-                    for (int j = 0; j < 32; ++j) acc[j] = 0.0f;
-                    #pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        for (int32_t g0 = g_first; g0 <= g_last; g0 += kFinBatch) {
-                            float x[kFinBatch][16];
-                            #pragma unroll
-                            for (int u = 0; u < kFinBatch; ++u) {
-                                const int32_t g = g0 + u;
-                                if (g > g_last || g == unit) continue;
-                                const int32_t first_tile =
-                                    static_cast<int32_t>((static_cast<int64_t>(g) * L) / KB);
-                                const float* src = p.partials +
-                                                   (static_cast<int64_t>(g) * p.sk_max_seg +
-                                                    (sg.tile - first_tile)) * BM * BN;
-                                if (p.c_cs == 1) {
-                                    const float4* s4 = reinterpret_cast<const float4*>(
-                                        src + row_in_tile * BN + ch * 32 + h * 16);
-                                    #pragma unroll
-                                    for (int q = 0; q < 4; ++q) {
-                                        const float4 t = __ldcg(s4 + q);
-                                        x[u][4 * q] = t.x;
-                                        x[u][4 * q + 1] = t.y;
-                                        x[u][4 * q + 2] = t.z;
-                                        x[u][4 * q + 3] = t.w;
-                                    }
-                                } else {
-                                    #pragma unroll
-                                    for (int j = 0; j < 16; ++j)
-                                        x[u][j] = __ldcg(src + (ch * 32 + h * 16 + j) * BM + row_in_tile);
-                                }
-                            }
-                            #pragma unroll
-                            for (int u = 0; u < kFinBatch; ++u) {
-                                const int32_t g = g0 + u;
-                                if (g > g_last) break;
-                                #pragma unroll
-                                for (int j = 0; j < 16; ++j)
-                                    acc[h * 16 + j] += (g == unit) ? v[h * 16 + j] : x[u][j];
-                            }
-                        }
-                    }
-                    store_chunk<OutT>(p, row, c0, acc);
+                    for (int j = 0; j < 32; ++j) my_slot[(ch * 32 + j) * BM + row_in_tile] = v[j];
                 }
             }
             tc_fence_before_sync();
@@ -807,9 +826,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!finisher) {
                     __threadfence();                       // this thread's slot stores
                     epilogue_bar_sync();
-                    if (warp == 2 && lane == 0) atomicAdd(p.tile_counters + 2 * sg.tile + 1, 1);
+                    if (warp == 2 && lane == 0) atomicAdd(p.tile_counters + sg.tile, 1);
                 }
-                epilogue_bar_sync();                       // role_flag is reused by the next tile
+                epilogue_bar_sync();                       // wait_ok is reused by the next tile
             }
         }
     }

@@ -28,21 +28,27 @@ static cudaError_t launch_tc_cfg(const TcLaunch& l) {
             raised_to = l.smem_bytes;
         }
     }
+    // Programmatic stream serialisation: the kernel's set-up may overlap the
+    // tail of the previous kernel on the stream (the kernel waits for it with
+    // griddepcontrol.wait before touching global memory).
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = l.smem_bytes;
+    cfg.stream = l.stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     if constexpr (CG == 1) {
-        kern<<<l.grid, kThreads, l.smem_bytes, l.stream>>>(l.tmA, l.tmB, l.p);
-        return cudaGetLastError();
+        cfg.gridDim = dim3(l.grid, 1, 1);
+        return cudaLaunchKernelEx(&cfg, kern, l.tmA, l.tmB, l.p);
     } else {
-        cudaLaunchConfig_t cfg = {};
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = 2;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.blockDim = dim3(kThreads, 1, 1);
-        cfg.dynamicSmemBytes = l.smem_bytes;
-        cfg.stream = l.stream;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
+        attr[1].id = cudaLaunchAttributeClusterDimension;
+        attr[1].val.clusterDim.x = 2;
+        attr[1].val.clusterDim.y = 1;
+        attr[1].val.clusterDim.z = 1;
+        cfg.numAttrs = 2;
         int grid = l.grid;
         if (!l.p.stream_k) {
             // A data-parallel schedule adapts to the grid: launch no more

@@ -194,16 +194,21 @@ def test_tf32_operands_stored_mn_major_are_transposed_first():
 def simulate_stream_k(p):
     """Replays the device-side segment iteration for every CTA and checks the
     schedule: each (tile, k-block) is covered exactly once, partial slots are
-    unique and in range, and the fixup's slot lookup finds the same slots."""
+    unique and in range, the finisher's slot lookup finds the same slots, and
+    the finisher of every split tile (the CTA holding its first k-blocks) meets
+    it in the last segment of its range -- so its other TMEM buffer is free
+    for the pre-summed partials and it is the contributor that ends last."""
     T, KB, L, G, S = p["num_tiles"], p["k_blocks"], p["sk_len"], p["grid"], p["sk_max_seg"]
     total = T * KB
     covered = [0] * total
     slots = {}
+    last_tile = {}
     for g in range(G):
         pos, end = min(g * L, total), min(g * L + L, total)
         assert pos < end, "a CTA without work"
         while pos < end:
             tile = pos // KB
+            last_tile[g] = tile
             kb0 = pos - tile * KB
             take = min(KB - kb0, end - pos)
             for k in range(kb0, kb0 + take):
@@ -223,6 +228,8 @@ def simulate_stream_k(p):
         for g in range(g_first, g_last + 1):
             slot = g * S + tile - (g * L) // KB
             assert slots.get(slot) == (tile, g)
+        assert last_tile[g_first] == tile
+    assert T <= 1024                  # one int32 counter per tile in the 4 KB header
     assert len(slots) * 128 * p["block_n"] * 4 <= p["workspace_bytes"]
 
 
