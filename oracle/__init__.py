@@ -1,4 +1,5 @@
-"""CPU oracle for C = alpha*op(A)*op(B) + beta*C (FP16/BF16 in, FP64 reference).
+"""CPU oracle for C = alpha*op(A)*op(B) + beta*C (FP16/BF16 in, FP64 reference)
+and for the row softmax.
 
 TEST INFRASTRUCTURE ONLY.  Only the test-suite, ``__graft_entry__.smoke()`` and
 the ``cpu_baseline`` / ``--impl reference`` legs of ``bench.py`` may import this
@@ -100,6 +101,8 @@ class Oracle:
         lib.oracle_gemm_ex.argtypes = common + ep + [dp, dp, ctypes.c_int]
         lib.oracle_gemm_sampled_ex.restype = ctypes.c_int
         lib.oracle_gemm_sampled_ex.argtypes = common + ep + [i64, vp, vp, dp, dp, ctypes.c_int]
+        lib.oracle_softmax.restype = ctypes.c_int
+        lib.oracle_softmax.argtypes = [i64, i64, vp, i64, ctypes.c_int, vp, i64, dp, ctypes.c_int]
         self.lib = lib
         self.path = path
 
@@ -217,6 +220,30 @@ def _oracle_ex_methods():
 
 
 _oracle_ex_methods()
+
+
+def _oracle_softmax_methods():
+    def softmax(self, X, rows, cols, ldx, x_dtype, row_ids=None, nthreads: int = 0):
+        """Row softmax of the stored rows x ldx matrix X (uint16 codes for
+        F16/BF16, float32 or uint32 for F32).  Returns float64 (n, cols) for the
+        selected rows (all rows when row_ids is None)."""
+        X = _prep(X, c=True)
+        if row_ids is None:
+            ids, n = None, rows
+        else:
+            ids = np.ascontiguousarray(row_ids, dtype=np.int64)
+            n = ids.size
+        R = np.empty((n, cols), dtype=np.float64)
+        st = self.lib.oracle_softmax(rows, cols, _ptr(X), ldx, x_dtype, _ptr(ids),
+                                     0 if ids is None else n, R.ctypes.data, nthreads)
+        if st != 0:
+            raise ValueError(f"oracle_softmax failed ({st})")
+        return R
+
+    Oracle.softmax = softmax
+
+
+_oracle_softmax_methods()
 
 
 def get() -> Oracle:

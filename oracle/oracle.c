@@ -412,3 +412,69 @@ int oracle_gemm_sampled_ex(char transA, char transB, int64_t M, int64_t N, int64
     }
     return OR_OK;
 }
+
+/* ---------------------------------------------------------- softmax oracle */
+
+/*
+ * Row softmax, the SGEMM tutorial page's memory-bound kernel (section 2):
+ * for each row x_0..x_{n-1} of X,
+ *     m   = max_j x_j
+ *     e_j = exp(x_j - m)
+ *     s   = sum_j e_j
+ *     y_j = e_j / s
+ * Section 2.1 gives the three steps (maximum, sum of exponentials of the
+ * shifted values, division); section 2.2 derives the online rescaling
+ * (m' = max(m, m_new), s' = s exp(m - m') + sum exp(x - m')) that reaches the
+ * same y in one scan.  The oracle is the plain three-step definition: every
+ * input decoded exactly to binary64 (FP32 exactly -- no TF32 cut here), the
+ * maximum, exp from libm and the sum in binary64, in increasing j.
+ *
+ * Special values follow the formula as written (the pages only discuss the
+ * fully masked row, section 2.5, which gives 0/0):
+ *   - a row that contains NaN: m is NaN, so every y_j is NaN;
+ *   - a row that contains +inf: inf - inf is NaN, so every y_j is NaN;
+ *   - a row whose entries are all -inf (fully masked): -inf - (-inf) is NaN,
+ *     so every y_j is NaN;
+ *   - otherwise an entry of -inf gives e_j = 0 and y_j = 0.
+ *
+ * X is rows x cols with row pitch ldx (elements) in x_dtype (F16, BF16 or
+ * F32).  row_ids (length nsel) selects the rows to evaluate; NULL means all
+ * rows (nsel is then ignored).  R receives one row of cols binary64 values per
+ * evaluated row, densely.
+ */
+int oracle_softmax(int64_t rows, int64_t cols, const void* X, int64_t ldx, int x_dtype,
+                   const int64_t* row_ids, int64_t nsel, double* R, int nthreads) {
+    if (rows < 0 || cols < 0 || ldx < (cols > 1 ? cols : 1)) return OR_BAD_ARG;
+    if (x_dtype != OR_F16 && x_dtype != OR_BF16 && x_dtype != OR_F32) return OR_BAD_ARG;
+    const int64_t n_out = row_ids ? nsel : rows;
+    if (n_out < 0) return OR_BAD_ARG;
+    if (cols == 0 || n_out == 0) return OR_OK;
+    if (X == NULL || R == NULL) return OR_BAD_ARG;
+    if (row_ids)
+        for (int64_t t = 0; t < nsel; ++t)
+            if (row_ids[t] < 0 || row_ids[t] >= rows) return OR_BAD_ARG;
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#pragma omp parallel for schedule(dynamic, 4)
+#endif
+    for (int64_t t = 0; t < n_out; ++t) {
+        const int64_t i = row_ids ? row_ids[t] : t;
+        double* y = R + t * cols;
+        int has_nan = 0;
+        double m = -INFINITY;
+        for (int64_t j = 0; j < cols; ++j) {
+            const double x = decode_c(x_dtype, X, i * ldx + j);
+            y[j] = x;
+            if (isnan(x)) has_nan = 1;
+            else if (x > m) m = x;
+        }
+        if (has_nan) m = NAN;
+        double s = 0.0;
+        for (int64_t j = 0; j < cols; ++j) {
+            y[j] = exp(y[j] - m);
+            s = s + y[j];
+        }
+        for (int64_t j = 0; j < cols; ++j) y[j] = y[j] / s;
+    }
+    return OR_OK;
+}

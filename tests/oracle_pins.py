@@ -527,6 +527,106 @@ def pin_gemm_tf32_bruteforce(o):
     assert (R == Ai.astype(np.float64) @ Bi.astype(np.float64)).all()   # 10-bit integers are exact
 
 
+# ----------------------------------------------------------------- softmax
+
+def _softmax_rows(o, X, dt, ldx=None, row_ids=None):
+    """X: float64 values that are exact in dt -> the oracle's softmax of them."""
+    rows, cols = X.shape
+    ldx = ldx or max(cols, 1)
+    if dt == F32:
+        buf = np.full((rows, ldx), np.nan, dtype=np.float32)
+        buf[:, :cols] = X.astype(np.float32)
+        assert (buf[:, :cols].astype(np.float64) == X)[np.isfinite(X)].all()
+    else:
+        buf = np.full((rows, ldx), 0x7E00 if dt == F16 else 0x7FC0, dtype=np.uint16)
+        buf[:, :cols] = _to_codes(X, dt) if X.size else buf[:, :cols]
+    return o.softmax(buf, rows, cols, ldx, dt, row_ids=row_ids)
+
+
+def pin_softmax_closed_forms(o):
+    """Constant rows give exactly 1/n; two-point rows the logistic closed form;
+    a row far above exp's range (1000, 999, 998) gives the shifted result,
+    which only the maximum subtraction reaches (SGEMM page, section 2.2:
+    the shift keeps exp from overflowing); a single entry gives 1."""
+    for dt in (F16, BF16, F32):
+        for n in (1, 2, 3, 7, 64, 1000):
+            for c in (0.0, -3.0, 40.0):
+                R = _softmax_rows(o, np.full((1, n), c), dt)
+                assert (R == 1.0 / n).all(), (dt, n, c)
+    for t in (0.5, -1.25, 3.0, 11.0, -20.0):
+        R = _softmax_rows(o, np.array([[0.0, t]]), F32)
+        want = [1.0 / (1.0 + math.exp(t)), 1.0 / (1.0 + math.exp(-t))]
+        assert np.allclose(R[0], want, rtol=4e-16, atol=0), (t, R, want)
+    R = _softmax_rows(o, np.array([[1000.0, 999.0, 998.0]]), F32)
+    e = np.array([1.0, math.exp(-1.0), math.exp(-2.0)])
+    assert np.allclose(R[0], e / e.sum(), rtol=4e-16, atol=0)
+    R = _softmax_rows(o, np.array([[60000.0, 0.0]]), F16)
+    assert R[0, 0] == 1.0 and R[0, 1] == 0.0
+
+
+def pin_softmax_library_and_invariants(o):
+    """Random rows of every input type against scipy.special.softmax; rows
+    sum to 1; integer rows are bitwise invariant under an integer shift;
+    permuting a row permutes its result; padding (NaN) is never read; the
+    selected-rows entry point matches the full one."""
+    from scipy.special import softmax as sp_softmax
+    rng = _rng(41)
+    for dt in (F16, BF16, F32):
+        X = rng.standard_normal((9, 37)) * 3.0
+        X = X.astype(np.float32).astype(np.float64)
+        if dt != F32:
+            X = exact.codes_to_float64(_to_codes_round(X, dt), dt).reshape(X.shape)
+        R = _softmax_rows(o, X, dt, ldx=45)
+        ref = sp_softmax(X, axis=1)
+        assert np.allclose(R, ref, rtol=1e-14, atol=0), dt
+        assert np.allclose(R.sum(axis=1), 1.0, rtol=0, atol=64 * 2.0 ** -52)
+        perm = rng.permutation(37)
+        Rp = _softmax_rows(o, X[:, perm], dt)
+        assert np.allclose(Rp, R[:, perm], rtol=1e-15, atol=0)
+        ids = np.array([8, 0, 3, 3])
+        Rs = _softmax_rows(o, X, dt, ldx=40, row_ids=ids)
+        assert (Rs == R[ids]).all()
+    Xi = rng.integers(-20, 21, (5, 50)).astype(np.float64)
+    R0 = _softmax_rows(o, Xi, F32)
+    R1 = _softmax_rows(o, Xi + 64.0, F32)
+    assert (R0 == R1).all()
+    # exp(x - m) for integers is e^-k: check the values themselves
+    m = Xi.max(axis=1, keepdims=True)
+    e = np.exp(Xi - m)
+    assert np.allclose(R0, e / e.sum(axis=1, keepdims=True), rtol=1e-15, atol=0)
+
+
+def pin_softmax_special_values(o):
+    """The formula's own values at the edges: NaN or +inf anywhere makes the
+    row NaN; a fully masked row (all -inf) is 0/0 = NaN (SGEMM page, section
+    2.5); a single -inf entry is exactly 0; empty inputs are no-ops; bad
+    arguments are rejected."""
+    inf, nan = math.inf, math.nan
+    X = np.array([[1.0, nan, 2.0], [1.0, inf, 2.0], [-inf, -inf, -inf], [0.0, -inf, 0.0],
+                  [-inf, 5.0, -inf]])
+    for dt in (F16, BF16, F32):
+        R = _softmax_rows(o, X, dt)
+        assert np.isnan(R[0]).all() and np.isnan(R[1]).all() and np.isnan(R[2]).all(), dt
+        assert (R[3] == [0.5, 0.0, 0.5]).all() and (R[4] == [0.0, 1.0, 0.0]).all(), dt
+    assert o.softmax(np.zeros((0, 4), np.float32), 0, 4, 4, F32).shape == (0, 4)
+    assert o.softmax(np.zeros((3, 1), np.float32), 3, 0, 1, F32).shape == (3, 0)
+    for bad in [dict(ldx=3), dict(dt=7), dict(ids=[5])]:
+        try:
+            o.softmax(np.zeros((4, 4), np.float32), 4, 4, bad.get("ldx", 4), bad.get("dt", F32),
+                      row_ids=bad.get("ids"))
+        except ValueError:
+            continue
+        raise AssertionError(f"accepted {bad}")
+
+
+def _to_codes_round(values, dtype):
+    """float64 values -> nearest uint16 codes by torch's conversion (test inputs)."""
+    import torch
+    tdt = torch.float16 if dtype == F16 else torch.bfloat16
+    return torch.tensor(np.asarray(values, dtype=np.float64)).to(tdt).view(torch.int16) \
+        .numpy().view(np.uint16).copy()
+
+
 ALL_PINS = [
     pin_decode_exhaustive, pin_page_format_limits, pin_round_ieee_table,
     pin_round_roundtrip_exhaustive, pin_round_midpoints, pin_round_random_exact,
@@ -535,4 +635,5 @@ ALL_PINS = [
     pin_quick_returns, pin_bad_arguments, pin_threads_deterministic,
     pin_activation_values, pin_epilogue_bruteforce, pin_epilogue_exact_and_sampled,
     pin_tf32_truncation, pin_gemm_tf32_bruteforce,
+    pin_softmax_closed_forms, pin_softmax_library_and_invariants, pin_softmax_special_values,
 ]

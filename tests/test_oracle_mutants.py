@@ -65,6 +65,19 @@ MUTANTS = [
      "return oracle_decode_f32((u + 0x1000u) & 0xFFFFE000u);"),
     ("tf32_not_truncated", "if (dt == OR_F32) return oracle_decode_tf32(((const uint32_t*)p)[idx]);",
      "if (dt == OR_F32) return oracle_decode_f32(((const uint32_t*)p)[idx]);"),
+    ("softmax_no_max_shift", "y[j] = exp(y[j] - m);", "y[j] = exp(y[j]);"),
+    ("softmax_not_normalised", "for (int64_t j = 0; j < cols; ++j) y[j] = y[j] / s;",
+     "for (int64_t j = 0; j < cols; ++j) y[j] = y[j] / (s + 1e-3);"),
+    ("softmax_min_not_max", "else if (x > m) m = x;", "else if (x < m || m == -INFINITY) m = x;"),
+    ("softmax_sum_skips_first", "s = s + y[j];", "if (j > 0) s = s + y[j];"),
+    ("softmax_row_pitch_ignored", "const double x = decode_c(x_dtype, X, i * ldx + j);",
+     "const double x = decode_c(x_dtype, X, i * cols + j);"),
+    ("softmax_f32_as_tf32", "const double x = decode_c(x_dtype, X, i * ldx + j);",
+     "const double x = decode_in(x_dtype, X, i * ldx + j);"),
+    ("softmax_selected_rows_ignored", "const int64_t i = row_ids ? row_ids[t] : t;",
+     "const int64_t i = t;"),
+    ("softmax_masked_row_zero", "for (int64_t j = 0; j < cols; ++j) y[j] = y[j] / s;",
+     "for (int64_t j = 0; j < cols; ++j) y[j] = (s > 0.0) ? y[j] / s : 0.0;"),
     ("beta_read_when_zero", "if (be != 0.0) r = r + be * decode_c(c_dtype, C, i * ldc + j);\n            acc[j] = r;",
      "r = r + be * decode_c(c_dtype, C, i * ldc + j);\n            acc[j] = r;"),
 ]
