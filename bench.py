@@ -27,6 +27,11 @@ Also reported:
                   timed region.
 --impl reference times the CPU oracle as the comparison arm (the pages ship
 no runnable implementation); it runs on rank 0 only.
+
+--workload softmax_* times the row softmax instead (SGEMM tutorial page,
+section 2): a step is one softmax_rows call over the whole matrix; the metric
+is GB/s (X read once + Y written once, per unit time) against the measured
+HBM copy bandwidth; e2e copies X up and Y back every step.
 With N > 1 (torchrun, one rank per GPU) every rank runs the same step on its
 own GPU: replicas, no collective on the data path (weak scaling).
 """
@@ -58,11 +63,15 @@ TF32_OVER_BF16 = 1.1 / 2.25
 KERNEL_SOURCES = ["mixed_precision_dense_sm_gb300/csrc/gemm_tc.cuh",
                   "mixed_precision_dense_sm_gb300/csrc/ptx.cuh",
                   "mixed_precision_dense_sm_gb300/csrc/kern_inst.cuh"]
+SOFTMAX_SOURCES = ["mixed_precision_dense_sm_gb300/csrc/softmax_kern.cuh",
+                   "mixed_precision_dense_sm_gb300/csrc/softmax.cu",
+                   "mixed_precision_dense_sm_gb300/csrc/ptx.cuh"]
+SOFTMAX_METRIC = "softmax GB/s (X read once + Y written once, per second) at 1 GB300; % of HBM"
 
 
-def kernel_hash() -> str:
+def kernel_hash(sources=None) -> str:
     h = hashlib.sha256()
-    for f in KERNEL_SOURCES:
+    for f in (sources or KERNEL_SOURCES):
         with open(os.path.join(ROOT, f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -77,7 +86,7 @@ def load_peaks():
     return dict(FALLBACK), "fallback"
 
 
-def committed_traffic(workload: str):
+def committed_traffic(workload: str, sources=None):
     """DRAM bytes per launch from profiles/traffic.json, if taken on these sources."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
@@ -85,7 +94,7 @@ def committed_traffic(workload: str):
     with open(path) as f:
         d = json.load(f)
     e = d.get(workload)
-    if not e or e.get("kernel_hash") != kernel_hash():
+    if not e or e.get("kernel_hash") != kernel_hash(sources):
         return None
     return e.get("dram_bytes_per_launch")
 
@@ -564,6 +573,187 @@ def run_e2e(lib, g, bufs, stream, args, world):
             "h2d_d2h_gbs": round((h2d + d2h) * steps / (ms * 1e-3) / 1e9, 1)}
 
 
+# ------------------------------------------------------------------ softmax
+
+def softmax_inputs(name):
+    w = workloads.SOFTMAX_WORKLOADS[name]
+    return w, workloads.make_softmax_input(w)
+
+
+class SoftmaxOracleSampler:
+    """Times the CPU oracle's softmax on seeded rows of the workload."""
+
+    def __init__(self, w, Xs):
+        import oracle
+        self.o = oracle.get()
+        self.w, self.Xs = w, Xs
+        self.codes = workloads.as_codes(Xs)
+        self.threads = self.o.max_threads()
+        self.rng = __import__("numpy").random.default_rng(0)
+
+    def run(self, nrows):
+        ids = self.rng.integers(0, self.w.rows, nrows)
+        ldx, _ = self.w.lds()
+        t0 = time.perf_counter()
+        self.o.softmax(self.codes, self.w.rows, self.w.cols, ldx, self.w.x_dtype, row_ids=ids)
+        t = time.perf_counter() - t0
+        ex = 4 if self.w.x_dtype == workloads.DT_F32 else 2
+        ey = 4 if self.w.y_dtype == workloads.DT_F32 else 2
+        return nrows * self.w.cols * (ex + ey), t
+
+    def calibrate(self, seconds):
+        n = 1
+        while True:
+            _, t = self.run(n)
+            if t > seconds / 8 or n >= self.w.rows:
+                break
+            n = min(self.w.rows, n * 4)
+        _, t = self.run(n)
+        return max(1, min(self.w.rows * 4, int(n * seconds / max(t, 1e-6))))
+
+
+def run_softmax(args):
+    import mixed_precision_dense_sm_gb300 as lib
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    w, Xs = softmax_inputs(args.workload)
+    ldx, ldy = w.lds()
+    X = Xs.cuda()
+    Y = torch.empty((w.rows, ldy), dtype=workloads.TORCH_DTYPE[w.y_dtype], device="cuda")
+    stream = torch.cuda.current_stream()
+    sh = stream.cuda_stream
+    sms = torch.cuda.get_device_properties(local).multi_processor_count
+    st, plan = lib.softmax_plan_query(w.rows, w.cols, X.data_ptr(), ldx, w.x_dtype, Y.data_ptr(),
+                                      ldy, w.y_dtype, num_sms=sms)
+    assert st == 0
+    nbytes = w.algorithmic_bytes()
+
+    def step(Xd=X, Yd=Y, s=sh):
+        st = lib.softmax_rows(w.rows, w.cols, Xd.data_ptr(), ldx, w.x_dtype, Yd.data_ptr(), ldy,
+                              w.y_dtype, s)
+        if st != 0:
+            raise lib.GemmError(st, "softmax_rows")
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    w0 = time.time()
+    t_start.record(stream)
+    for _ in range(args.steps):
+        step()
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    w1 = time.time()
+    clk = clocks.stop((w0, w1))
+    barrier(world)
+    ms = max_over_ranks(t_start.elapsed_time(t_end), world)
+    ms_step = ms / args.steps
+    value = world * nbytes * args.steps / (ms * 1e-3) / 1e9
+    peaks, peak_src = load_peaks()
+    # one kernel launch per step: the average launch is the timed region / steps
+    achieved = nbytes / (ms_step * 1e-3) / 1e9
+    roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
+            "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
+            "traffic": committed_traffic(w.name, SOFTMAX_SOURCES),
+            "peak_source": f"{peak_src} ({'MEASURED_PEAKS.json' if peak_src == 'measured' else 'recipe fallback'})",
+            "kernel": "softmax_kernel", "launch_ms": round(ms_step, 4),
+            "launch_ms_source": "timed region / launches (events at the region's ends only)",
+            "algorithmic_bytes_per_launch": nbytes, "plan_hbm_bytes": plan["hbm_bytes"]}
+
+    # e2e: X up from pinned host memory, the softmax, Y back, every step
+    hX = Xs.pin_memory()
+    hY = torch.empty(Y.shape, dtype=Y.dtype).pin_memory()
+    e_steps = max(3, min(args.steps, 20))
+    for _ in range(2):
+        X.copy_(hX, non_blocking=True)
+        step()
+        hY.copy_(Y, non_blocking=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e_steps):
+        X.copy_(hX, non_blocking=True)
+        step()
+        hY.copy_(Y, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ems = max_over_ranks(e0.elapsed_time(e1), world)
+    h2d = hX.numel() * hX.element_size()
+    d2h = hY.numel() * hY.element_size()
+    e2e = {"value": round(world * nbytes * e_steps / (ems * 1e-3) / 1e9, 1), "unit": "GB/s",
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e_steps,
+           "ms_per_step": round(ems / e_steps, 4)}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        smp = SoftmaxOracleSampler(w, Xs)
+        n = smp.calibrate(10.0)
+        b, t = smp.run(n)
+        cpu = {"value": round(b / t / 1e9, 4), "unit": "GB/s", "cores": smp.threads,
+               "kind": "oracle",
+               "sample": f"{n} seeded rows of {w.cols} elements (binary64 max, exp, sum, "
+                         f"divide): {b / 1e9:.3f} GB of X + Y in {t:.1f} s"}
+    out = {
+        "metric": SOFTMAX_METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": workloads.DT_NAME[w.x_dtype], "data": "synthetic",
+        "config": {"workload": f"{w.name}: row softmax of {w.rows} x {w.cols} "
+                               f"{workloads.DT_NAME[w.x_dtype]} -> {workloads.DT_NAME[w.y_dtype]}, "
+                               f"logits {w.dist}" + (f", {w.mask} mask" if w.mask else ""),
+                   "plan": plan,
+                   "l2": f"no flush: each step touches {nbytes / 1e9:.2f} GB > 129 MB L2"
+                         if nbytes > 2.6e8 else "each step touches less than 2x the L2",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "roofline": roof, "e2e": e2e, "gpu_launches": args.steps, "clocks": clk,
+    }
+    if cpu is not None:
+        out["cpu_baseline"] = cpu
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def run_softmax_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    w, Xs = softmax_inputs(args.workload)
+    smp = SoftmaxOracleSampler(w, Xs)
+    per_step = max(0.05, min(5.0, 150.0 / max(1, args.steps + args.warmup)))
+    n = smp.calibrate(per_step)
+    times, b = [], 0
+    for k in range(args.warmup + args.steps):
+        b, t = smp.run(n)
+        if k >= args.warmup:
+            times.append(t)
+    t = sum(times)
+    value = b * len(times) / t / 1e9
+    sample = f"{n} seeded rows of {w.cols} elements per step ({b / 1e9:.4f} GB of X + Y)"
+    out = {"metric": SOFTMAX_METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world,
+           "steps": args.steps, "warmup": args.warmup,
+           "ms_per_step": round(1e3 * t / len(times), 2), "higher_is_better": True,
+           "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+           "impl": "reference", "config": {"workload": w.name},
+           "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": smp.threads,
+                            "kind": "oracle", "sample": sample},
+           "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                   "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+
+
 # ------------------------------------------------------------ reference arm
 
 def run_reference(args):
@@ -606,7 +796,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="transformer_layer",
-                    choices=["transformer_layer"] + list(workloads.WORKLOADS))
+                    choices=["transformer_layer"] + list(workloads.WORKLOADS) +
+                    list(workloads.SOFTMAX_WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--epilogue", action="store_true",
                     help="fused epilogues of a transformer MLP block: bias on every GEMM, "
@@ -614,10 +805,13 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         ap.error("--warmup must be >= 3")
+    softmax = args.workload in workloads.SOFTMAX_WORKLOADS
+    if softmax and args.epilogue:
+        ap.error("--epilogue applies to the transformer_layer workload")
     if args.impl == "reference":
-        run_reference(args)
+        (run_softmax_reference if softmax else run_reference)(args)
     else:
-        run_ours(args)
+        (run_softmax if softmax else run_ours)(args)
 
 
 if __name__ == "__main__":

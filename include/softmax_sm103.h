@@ -1,0 +1,92 @@
+/*
+ * softmax_sm103.h -- C ABI of the GB300 (sm_103a) row softmax, the
+ * memory-bound kernel of the SGEMM tutorial page (section 2).
+ *
+ * What is computed (and where it is defined):
+ *   - For every row x_0..x_{n-1} of X:  m = max_j x_j,  e_j = exp(x_j - m),
+ *     s = sum_j e_j,  y_j = e_j / s  (SGEMM tutorial page, section 2.1: the
+ *     maximum, the sum of exponentials of the shifted values, the division).
+ *     The maximum shift keeps exp from overflowing (section 2.2).
+ *   - Each element is read from HBM once and written once wherever the row
+ *     fits on chip -- in one warp's or one CTA's registers, or, for long rows,
+ *     spread over a thread-block cluster of up to 8 CTAs whose partial
+ *     (maximum, sum) pairs are merged through distributed shared memory with
+ *     the online rule m' = max(m1, m2), s' = s1 e^(m1-m') + s2 e^(m2-m')
+ *     (section 2.2).  Longer rows are read twice: a first pass accumulates
+ *     (m, s) with the same rule chunk by chunk, a second pass writes y.
+ *   - Arithmetic is FP32 whatever the storage type (the CATLASS page, section
+ *     3.4, keeps reductions such as softmax in FP32 with 16-bit data paths);
+ *     exp is the fast hardware exponential (__expf, as on the SGEMM page,
+ *     section 2.5); y is rounded once to its type, round to nearest even.
+ *   - Special values follow the formula: a row containing NaN or +inf, and a
+ *     fully masked row (every entry -inf, 0/0 -- section 2.5), give NaN in
+ *     every position; otherwise an entry of -inf gives exactly 0.
+ *
+ * Layout: row-major; element (r, j) of X is at X + r * ldx + j, of Y at
+ * Y + r * ldy + j, in elements.  X and Y are DEVICE pointers owned by the
+ * caller, each aligned to its element size; X is only read, Y only written
+ * (the columns j >= cols of each row are never touched).  Y may be X itself
+ * (same pointer, same leading dimension, same type: in place); any other
+ * overlap of the two is rejected.
+ *
+ * Errors: returns GEMM_OK, GEMM_ERR_INVALID_VALUE (bad sizes, leading
+ * dimension, type, NULL or misaligned pointer, overlap; nothing enqueued),
+ * GEMM_ERR_NOT_SUPPORTED (the current device is not sm_103) or
+ * GEMM_ERR_LAUNCH.  The call is asynchronous on `stream` and allocates
+ * nothing; its kernels contain no waits that depend on other launches.
+ */
+#ifndef SOFTMAX_SM103_H_
+#define SOFTMAX_SM103_H_
+
+#include <stdint.h>
+
+#include "gemm_sm103.h"
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/*
+ * softmax_rows: Y = softmax(X) along each of `rows` rows of `cols` elements.
+ *   x_dtype, y_dtype: GEMM_F16, GEMM_BF16 or GEMM_F32 (independently).
+ *   cols <= 2^30; ldx, ldy: leading dimensions in elements, >= max(1, cols).
+ * rows == 0 or cols == 0 is a no-op (the pointers may then be NULL).
+ */
+gemm_status_t softmax_rows(int64_t rows, int64_t cols, const void* X, int64_t ldx,
+                           int32_t x_dtype, void* Y, int64_t ldy, int32_t y_dtype,
+                           gemm_stream_t stream);
+
+typedef enum {
+    SOFTMAX_MODE_NOOP = 0,      /* rows == 0 or cols == 0 */
+    SOFTMAX_MODE_WARP = 1,      /* one warp per row, row in registers (cols <= 1024) */
+    SOFTMAX_MODE_CTA = 2,       /* one CTA (or a cluster of CTAs) per row, row in registers */
+    SOFTMAX_MODE_STREAM = 3     /* a cluster per row, two passes over the row */
+} softmax_mode_t;
+
+typedef struct {
+    int32_t mode;          /* softmax_mode_t */
+    int32_t threads;       /* threads per CTA */
+    int32_t cluster;       /* CTAs per row (1 = no cluster) */
+    int32_t slice;         /* elements of a row per CTA (multiple of 8) */
+    int32_t vec;           /* 1: 16-byte loads and stores (rows 16-byte aligned) */
+    int32_t grid;          /* CTAs launched (persistent over rows) */
+    int64_t hbm_bytes;     /* bytes this plan moves to and from HBM */
+} softmax_plan_t;
+
+/*
+ * softmax_plan_query: the plan softmax_rows would use on a device with
+ * `num_sms` SMs, assuming `ctas_per_sm` resident CTAs per SM of the chosen
+ * shape -- or, when a row is split over a cluster, that many resident
+ * clusters on the whole GPU (0: the library's estimate).  Pure host logic;
+ * pointers are used only for their alignment and overlap.  Returns what
+ * softmax_rows would return for invalid arguments.
+ */
+gemm_status_t softmax_plan_query(int64_t rows, int64_t cols, const void* X, int64_t ldx,
+                                 int32_t x_dtype, const void* Y, int64_t ldy, int32_t y_dtype,
+                                 int32_t num_sms, int32_t ctas_per_sm, softmax_plan_t* out);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif  /* SOFTMAX_SM103_H_ */

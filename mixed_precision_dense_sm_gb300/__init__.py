@@ -1,4 +1,5 @@
-"""Python binding for libgemm_sm103.so, the GB300 mixed-precision GEMM.
+"""Python binding for libgemm_sm103.so, the GB300 mixed-precision GEMM and
+row softmax.
 
 Argument marshalling only: every step of C = alpha*op(A)*op(B) + beta*C runs in
 the library's CUDA kernels.  PyTorch is used for device memory and streams.
@@ -9,8 +10,10 @@ The entry points mirror include/gemm_sm103.h one to one:
 ``gemm_create``, ``gemm_run``, ``gemm_sync``, ``gemm_destroy``,
 ``gemm_status_string``, ``gemm_check_args``, ``gemm_plan_query``,
 ``gemm_run_ex`` (fused bias/activation epilogue), ``gemm_debug_set`` and
-``gemm_run_noalloc``.
-``Gemm`` wraps a handle and adds ``__call__`` for torch tensors.
+``gemm_run_noalloc``; and include/softmax_sm103.h: ``softmax_rows``,
+``softmax_plan_query``.
+``Gemm`` wraps a handle and adds ``__call__`` for torch tensors; ``softmax``
+does the same for the row softmax.
 """
 from __future__ import annotations
 
@@ -20,6 +23,7 @@ import os
 HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libgemm_sm103.so")
 HEADER = os.path.join(os.path.dirname(HERE), "include", "gemm_sm103.h")
+HEADERS = [HEADER, os.path.join(os.path.dirname(HERE), "include", "softmax_sm103.h")]
 
 GEMM_F16, GEMM_BF16, GEMM_F32 = 0, 1, 2
 STATUS = {0: "GEMM_OK", 1: "GEMM_ERR_INVALID_VALUE", 2: "GEMM_ERR_NOT_SUPPORTED",
@@ -60,6 +64,19 @@ class Plan(ctypes.Structure):
         return d
 
 
+SOFTMAX_MODES = {0: "noop", 1: "warp", 2: "cta", 3: "stream"}
+
+
+class SoftmaxPlan(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in (
+        "mode", "threads", "cluster", "slice", "vec", "grid")] + [("hbm_bytes", ctypes.c_int64)]
+
+    def as_dict(self):
+        d = {n: getattr(self, n) for n, _ in self._fields_}
+        d["mode_name"] = SOFTMAX_MODES.get(self.mode, "?")
+        return d
+
+
 def _load():
     if not os.path.exists(LIB_PATH):
         raise ImportError(
@@ -90,6 +107,12 @@ def _load():
     lib.gemm_plan_query.restype = ctypes.c_int
     lib.gemm_plan_query.argtypes = run_args + [ctypes.c_int32, ctypes.c_int32,
                                                ctypes.POINTER(Plan)]
+    i32 = ctypes.c_int32
+    smx_args = [i64, i64, vp, i64, i32, vp, i64, i32]
+    lib.softmax_rows.restype = ctypes.c_int
+    lib.softmax_rows.argtypes = smx_args + [vp]
+    lib.softmax_plan_query.restype = ctypes.c_int
+    lib.softmax_plan_query.argtypes = smx_args + [i32, i32, ctypes.POINTER(SoftmaxPlan)]
     return lib
 
 
@@ -171,11 +194,52 @@ def gemm_plan_query(transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc
 
 
 def declared_symbols():
-    """Function names declared in include/gemm_sm103.h."""
+    """Function names declared in include/gemm_sm103.h and softmax_sm103.h."""
     import re
-    text = open(HEADER).read()
-    return sorted(set(re.findall(r"^\s*(?:gemm_status_t|const char\*)\s+(gemm_\w+)\s*\(",
-                                 text, flags=re.M)))
+    names = set()
+    for h in HEADERS:
+        text = open(h).read()
+        names |= set(re.findall(r"^\s*(?:gemm_status_t|const char\*)\s+((?:gemm|softmax)_\w+)\s*\(",
+                                text, flags=re.M))
+    return sorted(names)
+
+
+def softmax_rows(rows, cols, X, ldx, x_dtype, Y, ldy, y_dtype, stream=0) -> int:
+    """Raw C-ABI call: Y = softmax(X) along each row.  X, Y are device
+    addresses (ints); dtypes GEMM_F16/GEMM_BF16/GEMM_F32; stream a
+    cudaStream_t value.  Returns the gemm_status_t code."""
+    return lib.softmax_rows(rows, cols, X, ldx, x_dtype, Y, ldy, y_dtype, stream)
+
+
+def softmax_plan_query(rows, cols, X, ldx, x_dtype, Y, ldy, y_dtype, num_sms=152,
+                       ctas_per_sm=0):
+    """(status, plan dict) of the work split softmax_rows would use (host logic)."""
+    plan = SoftmaxPlan()
+    st = lib.softmax_plan_query(rows, cols, X, ldx, x_dtype, Y, ldy, y_dtype, num_sms,
+                                ctas_per_sm, ctypes.byref(plan))
+    return st, (plan.as_dict() if st == 0 else None)
+
+
+def softmax(X, Y=None, rows=None, cols=None, stream=None):
+    """Row softmax of a 2-D torch tensor on the GPU (unit inner stride, row
+    pitch = stride(0)) into Y (a new tensor of X's type and shape if None;
+    Y may be X for in place).  Returns Y."""
+    import torch
+    if X.dim() != 2 or X.stride(1) != 1:
+        raise ValueError("X must be 2-D with unit inner stride")
+    if Y is None:
+        Y = torch.empty_like(X)
+    if Y.dim() != 2 or Y.stride(1) != 1:
+        raise ValueError("Y must be 2-D with unit inner stride")
+    rows = X.shape[0] if rows is None else rows
+    cols = X.shape[1] if cols is None else cols
+    if stream is None:
+        stream = torch.cuda.current_stream().cuda_stream
+    st = softmax_rows(rows, cols, X.data_ptr(), X.stride(0), dtype_code(X.dtype), Y.data_ptr(),
+                      Y.stride(0), dtype_code(Y.dtype), stream)
+    if st != 0:
+        raise GemmError(st, "softmax_rows")
+    return Y
 
 
 _TORCH_CODE = None

@@ -1,0 +1,214 @@
+// softmax.cu -- the C ABI of the row softmax (include/softmax_sm103.h):
+// argument validation, the host planner that picks the work split, and the
+// launch.
+//
+// The split follows the SGEMM tutorial page's two regimes (sections 2.3-2.4):
+// a row that fits on chip is read once and kept there (registers of a warp or
+// of a CTA); a longer row is spread over a thread-block cluster whose CTAs
+// merge their partial (max, sum) pairs through distributed shared memory --
+// the GB300 form of the page's option of splitting a long row over several
+// blocks that reduce across blocks -- and only rows beyond the cluster's
+// capacity are read twice.
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include <cuda_runtime.h>
+
+#include "softmax_sm103.h"
+#include "softmax_launch.h"
+
+namespace {
+
+constexpr int64_t kWarpMaxCols = 32 * smx::kE;          // 1024
+constexpr int64_t kCtaSmallCols = 256 * smx::kE;        // 8192: 256-thread CTAs
+constexpr int64_t kCtaMaxCols = 512 * smx::kE;          // 16384 per CTA
+constexpr int64_t kMaxCols = int64_t(1) << 30;
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+int64_t round_up(int64_t a, int64_t b) { return ceil_div(a, b) * b; }
+int64_t elem_bytes(int32_t dt) { return dt == GEMM_F32 ? 4 : 2; }
+bool dtype_ok(int32_t dt) { return dt == GEMM_F16 || dt == GEMM_BF16 || dt == GEMM_F32; }
+bool aligned_to(const void* p, uintptr_t n) { return (reinterpret_cast<uintptr_t>(p) % n) == 0; }
+
+struct Plan {
+    softmax_plan_t pub;
+    bool resident;
+};
+
+gemm_status_t check(int64_t rows, int64_t cols, const void* X, int64_t ldx, int32_t xdt,
+                    const void* Y, int64_t ldy, int32_t ydt) {
+    // 32-bit offsets within a row, with headroom for a chunk past its end
+    if (rows < 0 || cols < 0 || cols > kMaxCols) return GEMM_ERR_INVALID_VALUE;
+    if (!dtype_ok(xdt) || !dtype_ok(ydt)) return GEMM_ERR_INVALID_VALUE;
+    const int64_t min_ld = cols > 1 ? cols : 1;
+    if (ldx < min_ld || ldy < min_ld) return GEMM_ERR_INVALID_VALUE;
+    if (rows == 0 || cols == 0) return GEMM_OK;
+    if (X == nullptr || Y == nullptr) return GEMM_ERR_INVALID_VALUE;
+    if (!aligned_to(X, elem_bytes(xdt)) || !aligned_to(Y, elem_bytes(ydt)))
+        return GEMM_ERR_INVALID_VALUE;
+    // In place (the same matrix) is allowed; any other overlap is not.
+    const uintptr_t x0 = reinterpret_cast<uintptr_t>(X);
+    const uintptr_t y0 = reinterpret_cast<uintptr_t>(Y);
+    const uintptr_t x1 = x0 + static_cast<uintptr_t>(((rows - 1) * ldx + cols) * elem_bytes(xdt));
+    const uintptr_t y1 = y0 + static_cast<uintptr_t>(((rows - 1) * ldy + cols) * elem_bytes(ydt));
+    const bool overlap = x0 < y1 && y0 < x1;
+    const bool same = x0 == y0 && ldx == ldy && xdt == ydt;
+    if (overlap && !same) return GEMM_ERR_INVALID_VALUE;
+    return GEMM_OK;
+}
+
+// ctas_per_sm <= 0: estimate from the shape (the launch path asks the
+// occupancy calculator instead).
+gemm_status_t make_plan(int64_t rows, int64_t cols, const void* X, int64_t ldx, int32_t xdt,
+                        const void* Y, int64_t ldy, int32_t ydt, int32_t num_sms,
+                        int32_t ctas_per_sm, Plan& pl) {
+    gemm_status_t st = check(rows, cols, X, ldx, xdt, Y, ldy, ydt);
+    if (st != GEMM_OK) return st;
+    if (num_sms < 1) return GEMM_ERR_INVALID_VALUE;
+    std::memset(&pl, 0, sizeof pl);
+    pl.pub.cluster = 1;
+    if (rows == 0 || cols == 0) {
+        pl.pub.mode = SOFTMAX_MODE_NOOP;
+        return GEMM_OK;
+    }
+    const int64_t ex = elem_bytes(xdt), ey = elem_bytes(ydt);
+    pl.pub.vec = (aligned_to(X, 16) && aligned_to(Y, 16) && (ldx * ex) % 16 == 0 &&
+                  (ldy * ey) % 16 == 0) ? 1 : 0;
+    if (cols <= kWarpMaxCols) {
+        pl.pub.mode = SOFTMAX_MODE_WARP;
+        pl.pub.threads = smx::kWarpCtaThreads;
+        pl.pub.slice = static_cast<int32_t>(round_up(cols, 8));
+        pl.resident = true;
+        const int64_t per_sm = ctas_per_sm > 0 ? ctas_per_sm : 4;
+        const int64_t need = ceil_div(rows, smx::kWarpCtaThreads / 32);
+        const int64_t cap = per_sm * num_sms;
+        pl.pub.grid = static_cast<int32_t>(need < cap ? need : cap);
+    } else {
+        int64_t cl = 1;
+        int threads = cols <= kCtaSmallCols ? 256 : 512;
+        if (cols > kCtaMaxCols) {
+            while (cl < smx::kMaxCluster && cl * kCtaMaxCols < cols) cl *= 2;
+        }
+        const int64_t slice = round_up(ceil_div(cols, cl), 8);
+        pl.resident = slice <= static_cast<int64_t>(threads) * smx::kE;
+        pl.pub.mode = pl.resident ? SOFTMAX_MODE_CTA : SOFTMAX_MODE_STREAM;
+        pl.pub.threads = threads;
+        pl.pub.cluster = static_cast<int32_t>(cl);
+        pl.pub.slice = static_cast<int32_t>(slice);
+        int64_t groups;
+        if (cl == 1) {
+            const int64_t per_sm = ctas_per_sm > 0 ? ctas_per_sm : (threads > 256 ? 1 : 2);
+            groups = per_sm * num_sms;
+        } else {
+            // ctas_per_sm stands for resident clusters on the GPU here
+            groups = ctas_per_sm > 0 ? ctas_per_sm : num_sms / cl;
+            if (groups < 1) groups = 1;
+        }
+        pl.pub.grid = static_cast<int32_t>(cl * (rows < groups ? rows : groups));
+    }
+    pl.pub.hbm_bytes = rows * cols * (ex * (pl.resident ? 1 : 2) + ey);
+    return GEMM_OK;
+}
+
+struct DeviceInfo {
+    int sms = 0;
+    bool sm103 = false;
+};
+
+bool device_info(DeviceInfo& out) {
+    static std::mutex mu;
+    static DeviceInfo cache[64];
+    static bool known[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+        cudaGetLastError();
+        return false;
+    }
+    std::lock_guard<std::mutex> g(mu);
+    if (!known[dev]) {
+        int major = 0, minor = 0, sms = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+            cudaGetLastError();
+            return false;
+        }
+        cache[dev].sms = sms;
+        cache[dev].sm103 = (major == 10 && minor == 3);
+        known[dev] = true;
+    }
+    out = cache[dev];
+    return true;
+}
+
+cudaError_t launch(int32_t xdt, const smx::SoftmaxParams& p, int32_t ydt, bool warp_rows,
+                   int threads, int grid, cudaStream_t s) {
+    if (xdt == GEMM_F32) return smx::launch_softmax_f32(p, ydt, warp_rows, threads, grid, s);
+    if (xdt == GEMM_F16) return smx::launch_softmax_f16(p, ydt, warp_rows, threads, grid, s);
+    return smx::launch_softmax_bf16(p, ydt, warp_rows, threads, grid, s);
+}
+
+int resident(int32_t xdt, int32_t ydt, bool warp_rows, int threads, int cluster, int sms) {
+    if (xdt == GEMM_F32) return smx::resident_groups_f32(ydt, warp_rows, threads, cluster, sms);
+    if (xdt == GEMM_F16) return smx::resident_groups_f16(ydt, warp_rows, threads, cluster, sms);
+    return smx::resident_groups_bf16(ydt, warp_rows, threads, cluster, sms);
+}
+
+}  // namespace
+
+extern "C" {
+
+gemm_status_t softmax_plan_query(int64_t rows, int64_t cols, const void* X, int64_t ldx,
+                                 int32_t x_dtype, const void* Y, int64_t ldy, int32_t y_dtype,
+                                 int32_t num_sms, int32_t ctas_per_sm, softmax_plan_t* out) {
+    if (out == nullptr) return GEMM_ERR_INVALID_VALUE;
+    Plan pl;
+    gemm_status_t st = make_plan(rows, cols, X, ldx, x_dtype, Y, ldy, y_dtype, num_sms,
+                                 ctas_per_sm, pl);
+    if (st == GEMM_OK) *out = pl.pub;
+    return st;
+}
+
+gemm_status_t softmax_rows(int64_t rows, int64_t cols, const void* X, int64_t ldx,
+                           int32_t x_dtype, void* Y, int64_t ldy, int32_t y_dtype,
+                           gemm_stream_t stream) {
+    gemm_status_t st = check(rows, cols, X, ldx, x_dtype, Y, ldy, y_dtype);
+    if (st != GEMM_OK) return st;
+    if (rows == 0 || cols == 0) return GEMM_OK;
+    DeviceInfo dev;
+    if (!device_info(dev)) return GEMM_ERR_LAUNCH;
+    if (!dev.sm103) return GEMM_ERR_NOT_SUPPORTED;
+    // the shape first (threads, cluster), then the resident groups for it
+    Plan pl;
+    st = make_plan(rows, cols, X, ldx, x_dtype, Y, ldy, y_dtype, dev.sms, 1, pl);
+    if (st != GEMM_OK) return st;
+    const bool warp_rows = pl.pub.mode == SOFTMAX_MODE_WARP;
+    const int groups = resident(x_dtype, y_dtype, warp_rows, pl.pub.threads, pl.pub.cluster,
+                                dev.sms);
+    const int per_sm_or_clusters = pl.pub.cluster > 1 ? groups : groups / dev.sms;
+    st = make_plan(rows, cols, X, ldx, x_dtype, Y, ldy, y_dtype, dev.sms,
+                   per_sm_or_clusters > 0 ? per_sm_or_clusters : 1, pl);
+    if (st != GEMM_OK) return st;
+
+    smx::SoftmaxParams p;
+    p.X = X;
+    p.Y = Y;
+    p.ldx = ldx;
+    p.ldy = ldy;
+    p.rows = rows;
+    p.cols = static_cast<int32_t>(cols);
+    p.slice = pl.pub.slice;
+    p.cluster = pl.pub.cluster;
+    p.vec = pl.pub.vec;
+    p.resident = pl.resident ? 1 : 0;
+    cudaError_t e = launch(x_dtype, p, y_dtype, warp_rows, pl.pub.threads, pl.pub.grid,
+                           reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_LAUNCH;
+    }
+    return GEMM_OK;
+}
+
+}  // extern "C"

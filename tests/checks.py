@@ -98,3 +98,52 @@ def compare_epilogue(gpu_vals, gpu_codes, R, S, Cin_vals, bias_vals, alpha, beta
     stats["n"] = int(ok.size)
     stats["fail"] = int((~ok).sum())
     return stats, ~ok
+
+
+def softmax_bound(X, R, levels=16):
+    """Per-element bound on |y_gpu - r| for the FP32 softmax with __expf.
+
+    With t = x - max(x) per row: the kernel's exp(t) is within
+    (2 + 1.16|t|) ulp of exp for __expf (CUDA's documented bound) plus the
+    rounding of t itself (|t| 2^-24): eps_exp(t) <= (2 + 1.7|t|) 2^-23.  The
+    row sum s inherits the exps' errors weighted by their share,
+    W = sum_j e_j eps_exp(t_j) / s, once per merge level of the reduction tree
+    (every partial's rescale exp(m_p - m) has |m_p - m| <= |t_j| for all its
+    elements), plus at most `levels` FP32 additions and rescalings of
+    2^-24 each and 32 more for a thread's own running sum.  The output adds
+    one reciprocal and one product.  Values below FLT_MIN may flush to 0.
+    X: float64 inputs (n, cols); R: the oracle's float64 result."""
+    X = np.asarray(X, dtype=np.float64)
+    R = np.asarray(R, dtype=np.float64)
+    with np.errstate(invalid="ignore", over="ignore"):
+        m = np.max(np.where(np.isnan(X), -np.inf, X), axis=1, keepdims=True)
+        t = X - m
+        e = np.exp(t)
+        e = np.where(np.isfinite(e), e, 0.0)
+        a = np.abs(np.where(np.isfinite(t), t, 0.0))
+        eps_exp = np.where(e > 0, (2.0 + 1.7 * a) * 2.0 ** -23, 0.0)
+        s = e.sum(axis=1, keepdims=True)
+        W = np.where(s > 0, (e * eps_exp).sum(axis=1, keepdims=True) / np.where(s > 0, s, 1.0), 0.0)
+    eps_s = (levels + 1) * W + (2 * levels + 32) * 2.0 ** -24
+    return np.abs(R) * (eps_exp + eps_s + 3 * 2.0 ** -24) + 2.0 ** -126
+
+
+def compare_softmax(gpu_vals, gpu_codes, R, X, y_dtype, oracle_codes=None):
+    """FP32 output: within softmax_bound.  FP16/BF16 output: within one ulp
+    of the correctly rounded oracle value, or within softmax_bound plus one
+    output ulp.  NaN exactly where the oracle has NaN."""
+    bound = softmax_bound(X, R)
+    nan_r, nan_g = np.isnan(R), np.isnan(gpu_vals)
+    err = np.abs(gpu_vals - R)
+    with np.errstate(invalid="ignore"):
+        if y_dtype == F32:
+            ok = err <= bound
+        else:
+            dist = np.abs(_ordered(gpu_codes) - _ordered(oracle_codes))
+            ok = (dist <= 1) | (err <= ulp_of(np.where(nan_r, 0.0, R), y_dtype) + bound)
+    ok = np.where(nan_r | nan_g, nan_r & nan_g, ok)
+    with np.errstate(invalid="ignore", divide="ignore"):
+        rel = np.where(nan_r | (R == 0), 0.0, err / np.abs(R))
+    stats = {"n": int(ok.size), "fail": int((~ok).sum()),
+             "max_rel_err": float(np.max(rel)) if rel.size else 0.0}
+    return stats, ~ok

@@ -1,0 +1,82 @@
+"""Host logic of the row softmax, no GPU: argument checks and the work split
+(include/softmax_sm103.h)."""
+import pytest
+
+import mixed_precision_dense_sm_gb300 as lib
+from workloads import DT_BF16, DT_F16, DT_F32
+
+OK, INVALID = 0, 1
+
+
+def plan(rows, cols, x=256, ldx=None, xdt=DT_F32, y=1 << 44, ldy=None, ydt=DT_F32, sms=152,
+         per_sm=0):
+    ldx = ldx or max(cols, 1)
+    ldy = ldy or max(cols, 1)
+    return lib.softmax_plan_query(rows, cols, x, ldx, xdt, y, ldy, ydt, sms, per_sm)
+
+
+def test_exports():
+    for name in ("softmax_rows", "softmax_plan_query"):
+        assert name in lib.declared_symbols()
+        assert hasattr(lib.lib, name)
+
+
+def test_argument_checks():
+    assert plan(10, 10)[0] == OK
+    bad = [dict(rows=-1), dict(cols=-1), dict(cols=(1 << 30) + 1), dict(ldx=9), dict(ldy=9),
+           dict(xdt=5), dict(ydt=-1), dict(x=0), dict(y=0), dict(x=258), dict(y=2, ydt=DT_F32),
+           dict(x=257, xdt=DT_BF16)]
+    for b in bad:
+        kw = dict(rows=10, cols=10)
+        kw.update(b)
+        assert plan(**kw)[0] == INVALID, b
+    # empty problems need no pointers
+    assert plan(0, 10, x=0, y=0)[0] == OK and plan(0, 10, x=0, y=0)[1]["mode_name"] == "noop"
+    assert plan(10, 0, x=0, y=0)[1]["mode_name"] == "noop"
+    # the raw entry point rejects the same arguments before touching a GPU
+    assert lib.softmax_rows(10, 10, 0, 10, DT_F32, 256, 10, DT_F32, 0) == INVALID
+    assert lib.softmax_rows(0, 10, 0, 10, DT_F32, 0, 10, DT_F32, 0) == OK
+
+
+def test_overlap_rules():
+    # in place: same pointer, same ld, same type
+    assert plan(100, 64, x=4096, y=4096)[0] == OK
+    # same pointer but another type or pitch, or a partial overlap: rejected
+    assert plan(100, 64, x=4096, y=4096, ydt=DT_F16)[0] == INVALID
+    assert plan(100, 64, x=4096, y=4096, ldy=72)[0] == INVALID
+    assert plan(100, 64, x=4096, y=4096 + 256)[0] == INVALID
+    # adjacent, not overlapping
+    assert plan(100, 64, x=4096, y=4096 + 100 * 64 * 4)[0] == OK
+    assert plan(100, 64, x=4096 + 100 * 64 * 4, y=4096)[0] == OK
+
+
+@pytest.mark.parametrize("cols,mode,threads,cluster", [
+    (1, "warp", 256, 1), (1024, "warp", 256, 1), (1025, "cta", 256, 1), (8192, "cta", 256, 1),
+    (8193, "cta", 512, 1), (16384, "cta", 512, 1), (16385, "cta", 512, 2), (32768, "cta", 512, 2),
+    (32769, "cta", 512, 4), (131072, "cta", 512, 8), (131073, "stream", 512, 8),
+    (1 << 20, "stream", 512, 8)])
+def test_work_split(cols, mode, threads, cluster):
+    st, p = plan(64, cols)
+    assert st == OK
+    assert (p["mode_name"], p["threads"], p["cluster"]) == (mode, threads, cluster)
+    assert p["slice"] % 8 == 0 and p["slice"] * p["cluster"] >= cols
+    assert (p["slice"] - 8) * p["cluster"] < cols          # no CTA of the cluster is idle
+    if mode != "warp":
+        assert p["slice"] <= p["threads"] * 32 or mode == "stream"
+        assert p["grid"] % p["cluster"] == 0
+    reads = 2 if mode == "stream" else 1
+    assert p["hbm_bytes"] == 64 * cols * (4 * reads + 4)
+
+
+def test_vector_rule_and_grid():
+    assert plan(8, 4096)[1]["vec"] == 1
+    assert plan(8, 4096, ldx=4097)[1]["vec"] == 0               # FP32 rows 4 B apart
+    assert plan(8, 4096, xdt=DT_BF16, ldx=4100)[1]["vec"] == 0  # 16-bit rows need ld % 8
+    assert plan(8, 4096, xdt=DT_BF16, ldx=4104)[1]["vec"] == 1
+    assert plan(8, 4096, x=260)[1]["vec"] == 0                  # base not 16-byte aligned
+    # persistent grids: never more groups than rows, nor than resident groups
+    assert plan(3, 100)[1]["grid"] == 1                          # 8 rows per CTA
+    assert plan(100000, 100, per_sm=2)[1]["grid"] == 2 * 152
+    assert plan(5, 4096, per_sm=2)[1]["grid"] == 5
+    assert plan(100000, 4096, per_sm=2)[1]["grid"] == 304
+    assert plan(100000, 65536, per_sm=10)[1]["grid"] == 4 * 10  # 10 clusters of 4

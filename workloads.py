@@ -150,3 +150,58 @@ def as_codes(t: torch.Tensor):
     if t.dtype == torch.float32:
         return t.contiguous().numpy().view("uint32")
     raise TypeError(t.dtype)
+
+
+# ------------------------------------------------------------------ softmax
+
+@dataclasses.dataclass(frozen=True)
+class SoftmaxWorkload:
+    """Row softmax of a rows x cols matrix of logits (SGEMM tutorial page,
+    section 2).  dist: "N1" = N(0, 1) logits, "N4" = 4 N(0, 1) (peakier rows).
+    mask: None, or "causal" -- row r keeps columns j <= r mod cols and sets
+    the rest to -inf (the masked-attention pattern; row 0 of every block of
+    cols rows keeps one entry)."""
+    name: str
+    rows: int
+    cols: int
+    x_dtype: int
+    y_dtype: int
+    dist: str = "N1"
+    mask: Optional[str] = None
+    ldx: Optional[int] = None
+    ldy: Optional[int] = None
+    seed: int = 0
+
+    def lds(self):
+        return (self.ldx or max(1, self.cols), self.ldy or max(1, self.cols))
+
+    def algorithmic_bytes(self) -> int:
+        """X read once, Y written once."""
+        ex = 4 if self.x_dtype == DT_F32 else 2
+        ey = 4 if self.y_dtype == DT_F32 else 2
+        return self.rows * self.cols * (ex + ey)
+
+
+SOFTMAX_WORKLOADS = {w.name: w for w in [
+    SoftmaxWorkload("softmax_16384x4096_f32", 16384, 4096, DT_F32, DT_F32),
+    SoftmaxWorkload("softmax_65536x1024_bf16", 65536, 1024, DT_BF16, DT_BF16),
+    SoftmaxWorkload("softmax_8192x8192_bf16_causal", 8192, 8192, DT_BF16, DT_BF16, "N4", "causal"),
+    SoftmaxWorkload("softmax_2048x65536_f32", 2048, 65536, DT_F32, DT_F32),
+    SoftmaxWorkload("softmax_128x1048576_f32", 128, 1048576, DT_F32, DT_F32),
+]}
+
+
+def make_softmax_input(w: SoftmaxWorkload) -> torch.Tensor:
+    """The stored rows x ldx CPU tensor of w.x_dtype (padding NaN), drawn in
+    FP32 from one seeded generator, then masked, then cast (RNE)."""
+    gen = torch.Generator(device="cpu")
+    gen.manual_seed(w.seed)
+    ldx, _ = w.lds()
+    scale = {"N1": 1.0, "N4": 4.0}[w.dist]
+    x = torch.randn((w.rows, w.cols), generator=gen, dtype=torch.float32) * scale
+    if w.mask == "causal" and w.cols > 0:
+        keep = torch.arange(w.cols).view(1, -1) <= (torch.arange(w.rows) % w.cols).view(-1, 1)
+        x = torch.where(keep, x, torch.full_like(x, float("-inf")))
+    elif w.mask is not None:
+        raise ValueError(f"unknown mask {w.mask!r}")
+    return _stored(x, ldx, TORCH_DTYPE[w.x_dtype])
