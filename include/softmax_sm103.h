@@ -29,11 +29,21 @@
  * (same pointer, same leading dimension, same type: in place); any other
  * overlap of the two is rejected.
  *
+ * Rows of 256 bytes to 64 KB that start on 16-byte boundaries are staged in
+ * shared memory by bulk copies (TMA): one CTA of 16 warps per SM, split into
+ * groups of 1-16 warps, each group a pipeline that keeps the copies of its
+ * next few rows in flight while it works on one (~130-190 KB per SM in all),
+ * so HBM is streamed without registers holding the loads.  Other rows are
+ * held in registers (warp, CTA or cluster splits).
+ *
  * Errors: returns GEMM_OK, GEMM_ERR_INVALID_VALUE (bad sizes, leading
  * dimension, type, NULL or misaligned pointer, overlap; nothing enqueued),
  * GEMM_ERR_NOT_SUPPORTED (the current device is not sm_103) or
  * GEMM_ERR_LAUNCH.  The call is asynchronous on `stream` and allocates
- * nothing; its kernels contain no waits that depend on other launches.
+ * nothing.  The staged kernels wait on their own bulk copies; every such wait
+ * is bounded (2 s), and one that runs out sets a per-device error word that
+ * softmax_sync reports as GEMM_ERR_DEVICE_TIMEOUT (the rows of that pipeline
+ * are then not written).  No kernel waits on another launch.
  */
 #ifndef SOFTMAX_SM103_H_
 #define SOFTMAX_SM103_H_
@@ -70,6 +80,14 @@ typedef struct {
     int32_t slice;         /* elements of a row per CTA (multiple of 8) */
     int32_t vec;           /* 1: 16-byte loads and stores (rows 16-byte aligned) */
     int32_t grid;          /* CTAs launched (persistent over rows) */
+    int32_t depth;         /* > 0: rows staged in shared memory by bulk copies (TMA),
+                              this many row slots per pipeline; 0: rows held in registers */
+    int32_t group_warps;   /* staged: warps per pipeline (the CTA runs 16 / group_warps
+                              independent pipelines); 0 otherwise */
+    int32_t unit_rows;     /* staged: rows per slot -- 1: the group's warps share a row;
+                              more: each warp takes its own rows of the slot, and rows that
+                              are adjacent in X arrive in one copy of the whole slot */
+    int32_t reserved;
     int64_t hbm_bytes;     /* bytes this plan moves to and from HBM */
 } softmax_plan_t;
 
@@ -84,6 +102,25 @@ typedef struct {
 gemm_status_t softmax_plan_query(int64_t rows, int64_t cols, const void* X, int64_t ldx,
                                  int32_t x_dtype, const void* Y, int64_t ldy, int32_t y_dtype,
                                  int32_t num_sms, int32_t ctas_per_sm, softmax_plan_t* out);
+
+/*
+ * softmax_sync: wait for `stream`, then report (and clear) a device-side
+ * timeout recorded by any softmax kernel on the current device since the last
+ * softmax_sync: GEMM_ERR_DEVICE_TIMEOUT, else GEMM_OK (GEMM_ERR_LAUNCH if the
+ * CUDA runtime reports an error).
+ */
+gemm_status_t softmax_sync(gemm_stream_t stream);
+
+/*
+ * softmax_debug_set: test hook of the failure path, process-wide.
+ * SOFTMAX_DEBUG_SKIP_FIRST_LOAD makes the first pipeline of the first CTA of
+ * each staged launch arm its first row slot without issuing the copy, so that
+ * wait runs out; wait_limit_ns replaces the 2 s bound (0 restores it).
+ * flags = 0 restores normal operation.  Returns GEMM_ERR_INVALID_VALUE for
+ * unknown flags.
+ */
+#define SOFTMAX_DEBUG_SKIP_FIRST_LOAD 1u
+gemm_status_t softmax_debug_set(uint32_t flags, uint64_t wait_limit_ns);
 
 #ifdef __cplusplus
 }

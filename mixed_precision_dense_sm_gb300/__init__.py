@@ -11,7 +11,7 @@ The entry points mirror include/gemm_sm103.h one to one:
 ``gemm_status_string``, ``gemm_check_args``, ``gemm_plan_query``,
 ``gemm_run_ex`` (fused bias/activation epilogue), ``gemm_debug_set`` and
 ``gemm_run_noalloc``; and include/softmax_sm103.h: ``softmax_rows``,
-``softmax_plan_query``.
+``softmax_plan_query``, ``softmax_sync``, ``softmax_debug_set``.
 ``Gemm`` wraps a handle and adds ``__call__`` for torch tensors; ``softmax``
 does the same for the row softmax.
 """
@@ -69,7 +69,9 @@ SOFTMAX_MODES = {0: "noop", 1: "warp", 2: "cta", 3: "stream"}
 
 class SoftmaxPlan(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
-        "mode", "threads", "cluster", "slice", "vec", "grid")] + [("hbm_bytes", ctypes.c_int64)]
+        "mode", "threads", "cluster", "slice", "vec", "grid", "depth", "group_warps", "unit_rows",
+        "reserved")] + \
+        [("hbm_bytes", ctypes.c_int64)]
 
     def as_dict(self):
         d = {n: getattr(self, n) for n, _ in self._fields_}
@@ -113,6 +115,10 @@ def _load():
     lib.softmax_rows.argtypes = smx_args + [vp]
     lib.softmax_plan_query.restype = ctypes.c_int
     lib.softmax_plan_query.argtypes = smx_args + [i32, i32, ctypes.POINTER(SoftmaxPlan)]
+    lib.softmax_sync.restype = ctypes.c_int
+    lib.softmax_sync.argtypes = [vp]
+    lib.softmax_debug_set.restype = ctypes.c_int
+    lib.softmax_debug_set.argtypes = [ctypes.c_uint32, ctypes.c_uint64]
     return lib
 
 
@@ -209,6 +215,20 @@ def softmax_rows(rows, cols, X, ldx, x_dtype, Y, ldy, y_dtype, stream=0) -> int:
     addresses (ints); dtypes GEMM_F16/GEMM_BF16/GEMM_F32; stream a
     cudaStream_t value.  Returns the gemm_status_t code."""
     return lib.softmax_rows(rows, cols, X, ldx, x_dtype, Y, ldy, y_dtype, stream)
+
+
+SOFTMAX_DEBUG_SKIP_FIRST_LOAD = 1
+
+
+def softmax_sync(stream=0) -> int:
+    """Wait for the stream; GEMM_ERR_DEVICE_TIMEOUT (5) if a softmax kernel
+    recorded a bounded wait that ran out (then cleared)."""
+    return lib.softmax_sync(stream)
+
+
+def softmax_debug_set(flags: int, wait_limit_ns: int = 0) -> int:
+    """Test hook of the softmax failure path (see include/softmax_sm103.h)."""
+    return lib.softmax_debug_set(flags, wait_limit_ns)
 
 
 def softmax_plan_query(rows, cols, X, ldx, x_dtype, Y, ldy, y_dtype, num_sms=152,

@@ -24,6 +24,13 @@ constexpr int64_t kWarpMaxCols = 32 * smx::kE;          // 1024
 constexpr int64_t kCtaSmallCols = 256 * smx::kE;        // 8192: 256-thread CTAs
 constexpr int64_t kCtaMaxCols = 512 * smx::kE;          // 16384 per CTA
 constexpr int64_t kMaxCols = int64_t(1) << 30;
+// Rows staged in shared memory by bulk copies: 256 B to 64 KB, one row per
+// group of warps at a time (the group holds its row in registers, at most
+// kTmaMaxVec 16-byte vectors per thread), slots within this budget.
+constexpr int64_t kStagedMinBytes = 256;
+constexpr int64_t kStagedMaxBytes = 64 * 1024;
+constexpr int64_t kStagedSmemBudget = 200 * 1024;
+constexpr uint64_t kDefaultWaitNs = 2000000000ull;
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 int64_t round_up(int64_t a, int64_t b) { return ceil_div(a, b) * b; }
@@ -34,6 +41,10 @@ bool aligned_to(const void* p, uintptr_t n) { return (reinterpret_cast<uintptr_t
 struct Plan {
     softmax_plan_t pub;
     bool resident;
+    size_t smem;          // staged path: dynamic shared memory per CTA
+    int32_t bulk_elems;   // staged path: elements per row moved by the bulk copy
+    int32_t row_stride;   // staged path: bytes between rows inside a slot
+    int32_t contiguous;   // staged path: a slot's rows are adjacent in X (one copy)
 };
 
 gemm_status_t check(int64_t rows, int64_t cols, const void* X, int64_t ldx, int32_t xdt,
@@ -75,7 +86,44 @@ gemm_status_t make_plan(int64_t rows, int64_t cols, const void* X, int64_t ldx, 
     const int64_t ex = elem_bytes(xdt), ey = elem_bytes(ydt);
     pl.pub.vec = (aligned_to(X, 16) && aligned_to(Y, 16) && (ldx * ex) % 16 == 0 &&
                   (ldy * ey) % 16 == 0) ? 1 : 0;
-    if (cols <= kWarpMaxCols) {
+    const int64_t row_bytes = cols * ex;
+    if (pl.pub.vec && row_bytes >= kStagedMinBytes && row_bytes <= kStagedMaxBytes) {
+        // staged in shared memory: one CTA of 16 warps per SM, split into
+        // groups just large enough to hold a row in registers; each group a
+        // pipeline of `depth` row slots
+        const int64_t nvec = row_bytes / 16;
+        int64_t gw = 1, unit_rows = 1, row_stride = 0;
+        bool contiguous = false;
+        if (nvec <= 32 * smx::kTmaMaxVec) {
+            // a warp holds a row: groups of 8 warps share slots of several
+            // rows, moved by one copy of ~16 KB when the rows are adjacent
+            gw = 8;
+            contiguous = ldx * ex == row_bytes;
+            row_stride = contiguous ? row_bytes : round_up(row_bytes, 16);
+            int64_t k = 16384 / (gw * row_stride);
+            k = k < 1 ? 1 : (k > 4 ? 4 : k);
+            unit_rows = gw * k;
+        } else {
+            while (gw * 32 * smx::kTmaMaxVec < nvec) gw *= 2;
+        }
+        const int64_t groups = (smx::kTmaThreads / 32) / gw;
+        const int64_t slot = round_up(unit_rows == 1 ? row_bytes : unit_rows * row_stride, 128);
+        int64_t depth = kStagedSmemBudget / (groups * slot);
+        if (depth > smx::kTmaMaxDepth) depth = smx::kTmaMaxDepth;
+        pl.pub.mode = unit_rows > 1 ? SOFTMAX_MODE_WARP : SOFTMAX_MODE_CTA;
+        pl.pub.threads = smx::kTmaThreads;
+        pl.pub.slice = static_cast<int32_t>(round_up(cols, 8));
+        pl.pub.depth = static_cast<int32_t>(depth);
+        pl.pub.group_warps = static_cast<int32_t>(gw);
+        pl.pub.unit_rows = static_cast<int32_t>(unit_rows);
+        pl.row_stride = static_cast<int32_t>(row_stride);
+        pl.contiguous = contiguous ? 1 : 0;
+        pl.resident = true;
+        pl.smem = static_cast<size_t>(round_up(groups * depth * 8, 128) + groups * depth * slot);
+        pl.bulk_elems = static_cast<int32_t>((row_bytes / 16) * 16 / ex);
+        const int64_t need = ceil_div(ceil_div(rows, unit_rows), groups);
+        pl.pub.grid = static_cast<int32_t>(need < num_sms ? need : num_sms);
+    } else if (cols <= kWarpMaxCols) {
         pl.pub.mode = SOFTMAX_MODE_WARP;
         pl.pub.threads = smx::kWarpCtaThreads;
         pl.pub.slice = static_cast<int32_t>(round_up(cols, 8));
@@ -149,10 +197,43 @@ cudaError_t launch(int32_t xdt, const smx::SoftmaxParams& p, int32_t ydt, bool w
     return smx::launch_softmax_bf16(p, ydt, warp_rows, threads, grid, s);
 }
 
+cudaError_t launch_tma(int32_t xdt, const smx::TmaSoftmaxParams& p, int32_t ydt, int grid,
+                       size_t smem, cudaStream_t s) {
+    if (xdt == GEMM_F32) return smx::launch_softmax_tma_f32(p, ydt, grid, smem, s);
+    if (xdt == GEMM_F16) return smx::launch_softmax_tma_f16(p, ydt, grid, smem, s);
+    return smx::launch_softmax_tma_bf16(p, ydt, grid, smem, s);
+}
+
 int resident(int32_t xdt, int32_t ydt, bool warp_rows, int threads, int cluster, int sms) {
     if (xdt == GEMM_F32) return smx::resident_groups_f32(ydt, warp_rows, threads, cluster, sms);
     if (xdt == GEMM_F16) return smx::resident_groups_f16(ydt, warp_rows, threads, cluster, sms);
     return smx::resident_groups_bf16(ydt, warp_rows, threads, cluster, sms);
+}
+
+// ------------------------------------------------------------------ errors
+
+// The device error word the staged kernels set when a bounded wait runs out
+// (one per device; its address is looked up with that device current).
+__device__ int g_softmax_error;
+
+std::mutex g_dbg_mu;
+uint32_t g_debug_flags = 0;
+uint64_t g_wait_limit_ns = 0;
+
+int* error_word(int dev) {
+    static std::mutex mu;
+    static int* addr[64] = {};
+    std::lock_guard<std::mutex> g(mu);
+    if (dev < 0 || dev >= 64) return nullptr;
+    if (addr[dev] == nullptr) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_softmax_error) != cudaSuccess) {
+            cudaGetLastError();
+            return nullptr;
+        }
+        addr[dev] = static_cast<int*>(p);
+    }
+    return addr[dev];
 }
 
 }  // namespace
@@ -184,12 +265,53 @@ gemm_status_t softmax_rows(int64_t rows, int64_t cols, const void* X, int64_t ld
     st = make_plan(rows, cols, X, ldx, x_dtype, Y, ldy, y_dtype, dev.sms, 1, pl);
     if (st != GEMM_OK) return st;
     const bool warp_rows = pl.pub.mode == SOFTMAX_MODE_WARP;
-    const int groups = resident(x_dtype, y_dtype, warp_rows, pl.pub.threads, pl.pub.cluster,
-                                dev.sms);
-    const int per_sm_or_clusters = pl.pub.cluster > 1 ? groups : groups / dev.sms;
-    st = make_plan(rows, cols, X, ldx, x_dtype, Y, ldy, y_dtype, dev.sms,
-                   per_sm_or_clusters > 0 ? per_sm_or_clusters : 1, pl);
-    if (st != GEMM_OK) return st;
+    if (pl.pub.depth == 0) {
+        const int groups = resident(x_dtype, y_dtype, warp_rows, pl.pub.threads, pl.pub.cluster,
+                                    dev.sms);
+        const int per_sm_or_clusters = pl.pub.cluster > 1 ? groups : groups / dev.sms;
+        st = make_plan(rows, cols, X, ldx, x_dtype, Y, ldy, y_dtype, dev.sms,
+                       per_sm_or_clusters > 0 ? per_sm_or_clusters : 1, pl);
+        if (st != GEMM_OK) return st;
+    }
+
+    if (pl.pub.depth > 0) {
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess) {
+            cudaGetLastError();
+            return GEMM_ERR_LAUNCH;
+        }
+        int* err = error_word(dev);
+        if (err == nullptr) return GEMM_ERR_LAUNCH;
+        smx::TmaSoftmaxParams q;
+        q.X = X;
+        q.Y = Y;
+        q.ldx = ldx;
+        q.ldy = ldy;
+        q.rows = rows;
+        q.cols = static_cast<int32_t>(cols);
+        q.bulk_elems = pl.bulk_elems;
+        q.slot_bytes = static_cast<int32_t>(
+            round_up(pl.pub.unit_rows == 1 ? cols * elem_bytes(x_dtype)
+                                           : int64_t(pl.pub.unit_rows) * pl.row_stride, 128));
+        q.depth = pl.pub.depth;
+        q.group_warps = pl.pub.group_warps;
+        q.unit_rows = pl.pub.unit_rows;
+        q.row_stride = pl.row_stride;
+        q.contiguous = pl.contiguous;
+        q.err = err;
+        {
+            std::lock_guard<std::mutex> g(g_dbg_mu);
+            q.wait_limit_ns = g_wait_limit_ns ? g_wait_limit_ns : kDefaultWaitNs;
+            q.debug_flags = g_debug_flags;
+        }
+        cudaError_t e = launch_tma(x_dtype, q, y_dtype, pl.pub.grid, pl.smem,
+                                   reinterpret_cast<cudaStream_t>(stream));
+        if (e != cudaSuccess) {
+            cudaGetLastError();
+            return GEMM_ERR_LAUNCH;
+        }
+        return GEMM_OK;
+    }
 
     smx::SoftmaxParams p;
     p.X = X;
@@ -208,6 +330,44 @@ gemm_status_t softmax_rows(int64_t rows, int64_t cols, const void* X, int64_t ld
         cudaGetLastError();
         return GEMM_ERR_LAUNCH;
     }
+    return GEMM_OK;
+}
+
+}  // extern "C"
+
+extern "C" {
+
+gemm_status_t softmax_sync(gemm_stream_t stream) {
+    if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_LAUNCH;
+    }
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_LAUNCH;
+    }
+    int* err = error_word(dev);
+    if (err == nullptr) return GEMM_ERR_LAUNCH;
+    int v = 0;
+    if (cudaMemcpy(&v, err, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_LAUNCH;
+    }
+    if (v != 0) {
+        const int zero = 0;
+        cudaMemcpy(err, &zero, sizeof zero, cudaMemcpyHostToDevice);
+        cudaGetLastError();
+        return GEMM_ERR_DEVICE_TIMEOUT;
+    }
+    return GEMM_OK;
+}
+
+gemm_status_t softmax_debug_set(uint32_t flags, uint64_t wait_limit_ns) {
+    if (flags & ~SOFTMAX_DEBUG_SKIP_FIRST_LOAD) return GEMM_ERR_INVALID_VALUE;
+    std::lock_guard<std::mutex> g(g_dbg_mu);
+    g_debug_flags = flags;
+    g_wait_limit_ns = wait_limit_ns;
     return GEMM_OK;
 }
 

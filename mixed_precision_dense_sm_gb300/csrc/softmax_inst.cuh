@@ -19,6 +19,16 @@ cudaError_t SMX_CAT(launch_softmax_, SMX_SUFFIX)(const SoftmaxParams& p, int y_d
     }
 }
 
+cudaError_t SMX_CAT(launch_softmax_tma_, SMX_SUFFIX)(const TmaSoftmaxParams& p, int y_dtype,
+                                                     int grid, size_t smem, cudaStream_t stream) {
+    switch (y_dtype) {
+        case 0: return launch_softmax_tma<SMX_IN_T, __half>(p, grid, smem, stream);
+        case 1: return launch_softmax_tma<SMX_IN_T, __nv_bfloat16>(p, grid, smem, stream);
+        case 2: return launch_softmax_tma<SMX_IN_T, float>(p, grid, smem, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
 int SMX_CAT(resident_groups_, SMX_SUFFIX)(int y_dtype, bool warp_rows, int threads, int cluster,
                                           int num_sms) {
     switch (y_dtype) {

@@ -6,6 +6,7 @@
 #include <cuda_runtime.h>
 
 #include "softmax_kern.cuh"
+#include "softmax_tma.cuh"
 
 namespace smx {
 
@@ -13,7 +14,9 @@ namespace smx {
     cudaError_t launch_softmax_##suffix(const SoftmaxParams& p, int y_dtype, bool warp_rows,  \
                                         int threads, int grid, cudaStream_t stream);         \
     int resident_groups_##suffix(int y_dtype, bool warp_rows, int threads, int cluster,      \
-                                 int num_sms);
+                                 int num_sms);                                               \
+    cudaError_t launch_softmax_tma_##suffix(const TmaSoftmaxParams& p, int y_dtype, int grid, \
+                                            size_t smem, cudaStream_t stream);
 SMX_DECLARE(f32)
 SMX_DECLARE(f16)
 SMX_DECLARE(bf16)

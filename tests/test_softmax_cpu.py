@@ -16,7 +16,7 @@ def plan(rows, cols, x=256, ldx=None, xdt=DT_F32, y=1 << 44, ldy=None, ydt=DT_F3
 
 
 def test_exports():
-    for name in ("softmax_rows", "softmax_plan_query"):
+    for name in ("softmax_rows", "softmax_plan_query", "softmax_sync", "softmax_debug_set"):
         assert name in lib.declared_symbols()
         assert hasattr(lib.lib, name)
 
@@ -56,7 +56,8 @@ def test_overlap_rules():
     (32769, "cta", 512, 4), (131072, "cta", 512, 8), (131073, "stream", 512, 8),
     (1 << 20, "stream", 512, 8)])
 def test_work_split(cols, mode, threads, cluster):
-    st, p = plan(64, cols)
+    """Rows not 16-byte aligned (base 4 bytes off): held in registers."""
+    st, p = plan(64, cols, x=260)
     assert st == OK
     assert (p["mode_name"], p["threads"], p["cluster"]) == (mode, threads, cluster)
     assert p["slice"] % 8 == 0 and p["slice"] * p["cluster"] >= cols
@@ -66,6 +67,43 @@ def test_work_split(cols, mode, threads, cluster):
         assert p["grid"] % p["cluster"] == 0
     reads = 2 if mode == "stream" else 1
     assert p["hbm_bytes"] == 64 * cols * (4 * reads + 4)
+    assert p["depth"] == 0 and p["vec"] == 0
+
+
+@pytest.mark.parametrize("cols,dt,ld,gw,unit,depth", [
+    (64, DT_F32, 64, 8, 32, 8), (1024, DT_F32, 1024, 8, 8, 3), (1000, DT_F32, 1004, 8, 8, 3),
+    (128, DT_BF16, 128, 8, 32, 8), (2048, DT_F32, 2048, 2, 1, 3), (4096, DT_BF16, 4096, 2, 1, 3),
+    (2052, DT_F32, 2052, 4, 1, 6), (4096, DT_F32, 4096, 4, 1, 3), (8192, DT_F32, 8192, 8, 1, 3),
+    (16384, DT_F32, 16384, 16, 1, 3), (32768, DT_F16, 32768, 16, 1, 3),
+    (16388, DT_F32, 16388, 0, 0, 0), (60, DT_F32, 60, 0, 0, 0), (120, DT_BF16, 120, 0, 0, 0)])
+def test_staged_split(cols, dt, ld, gw, unit, depth):
+    """16-byte-aligned rows of 256 B to 64 KB are staged in shared memory by
+    bulk copies: one CTA of 16 warps per SM.  Rows a warp can hold (<= 4 KB)
+    go to groups of 8 warps whose slots carry several rows (~16 KB, one copy
+    when the rows are adjacent), a warp per row; longer rows are shared by a
+    group just large enough to hold them in registers (<= 8 16-byte vectors
+    per thread).  Each group is a pipeline with as many slots as 200 KB allow
+    (at most 8).  Shorter or longer rows keep the register kernels (depth 0)."""
+    st, p = plan(100000, cols, ldx=ld, ldy=ld, xdt=dt, ydt=dt)
+    assert st == OK
+    assert (p["group_warps"], p["unit_rows"], p["depth"]) == (gw, unit, depth), p
+    es = 4 if dt == DT_F32 else 2
+    if depth:
+        assert p["vec"] == 1 and p["cluster"] == 1 and p["grid"] == 152 and p["threads"] == 512
+        assert p["mode_name"] == ("warp" if unit > 1 else "cta")
+        groups = 16 // gw
+        stride = ld * es if unit > 1 else cols * es
+        slot = -(-unit * stride // 128) * 128
+        assert groups * depth * slot <= 200 * 1024 and depth >= 3
+        if unit == 1:
+            assert gw * 32 * 8 * 16 >= cols * es and (gw == 1 or (gw // 2) * 32 * 8 * 16 < cols * es)
+        else:
+            assert cols * es <= 32 * 8 * 16 and unit % gw == 0
+        assert p["hbm_bytes"] == 100000 * cols * 2 * es
+        rows = 5 * unit
+        assert plan(rows, cols, ldx=ld, ldy=ld, xdt=dt, ydt=dt)[1]["grid"] == -(-5 // groups)
+    few = plan(3, cols, xdt=dt, ydt=dt)[1]
+    assert few["grid"] <= 3 * few["cluster"]
 
 
 def test_vector_rule_and_grid():
@@ -75,8 +113,9 @@ def test_vector_rule_and_grid():
     assert plan(8, 4096, xdt=DT_BF16, ldx=4104)[1]["vec"] == 1
     assert plan(8, 4096, x=260)[1]["vec"] == 0                  # base not 16-byte aligned
     # persistent grids: never more groups than rows, nor than resident groups
-    assert plan(3, 100)[1]["grid"] == 1                          # 8 rows per CTA
-    assert plan(100000, 100, per_sm=2)[1]["grid"] == 2 * 152
-    assert plan(5, 4096, per_sm=2)[1]["grid"] == 5
-    assert plan(100000, 4096, per_sm=2)[1]["grid"] == 304
+    assert plan(3, 100, x=260)[1]["grid"] == 1                    # 8 rows per CTA
+    assert plan(100000, 100, x=260, per_sm=2)[1]["grid"] == 2 * 152
+    assert plan(5, 4096, x=260, per_sm=2)[1]["grid"] == 5
+    assert plan(100000, 4096, x=260, per_sm=2)[1]["grid"] == 304
+    assert plan(100000, 100)[1]["grid"] == 152                    # staged: one CTA per SM
     assert plan(100000, 65536, per_sm=10)[1]["grid"] == 4 * 10  # 10 clusters of 4

@@ -227,3 +227,32 @@ def test_empty_and_errors(lib):
     assert lib.softmax_rows(4, 4, Y.data_ptr() + 2, 4, DT_F32, Y.data_ptr(), 4, DT_F32, s) == 1
     torch.cuda.synchronize()
     assert torch.all(Y == 7.0)
+
+
+@pytest.mark.parametrize("cols", [1024, 8192])
+def test_timeout_reported_without_fault(lib, orc, cols):
+    """The failure path of the staged kernels, without a GPU fault: the test
+    hook arms the first row slot of the first pipeline without issuing its
+    copy, so that bounded wait runs out (limit 0.2 s).  softmax_sync reports
+    GEMM_ERR_DEVICE_TIMEOUT once; the next call on the same device is
+    correct.  1024 FP32 columns run one pipeline per warp, 8192 one per CTA."""
+    g = torch.Generator().manual_seed(5)
+    Xs = stored(torch.randn((64, cols), generator=g), cols, DT_F32)
+    st, p = lib.softmax_plan_query(64, cols, 256, cols, DT_F32, 1 << 44, cols, DT_F32)
+    assert st == 0 and p["depth"] > 0
+    s = torch.cuda.current_stream().cuda_stream
+    assert lib.softmax_sync(s) == 0
+    X = Xs.cuda()
+    Y = torch.empty_like(X)
+    assert lib.softmax_debug_set(lib.SOFTMAX_DEBUG_SKIP_FIRST_LOAD, 200_000_000) == 0
+    try:
+        assert lib.softmax_rows(64, cols, X.data_ptr(), cols, DT_F32, Y.data_ptr(), cols,
+                                DT_F32, s) == 0
+        assert lib.softmax_sync(s) == 5
+    finally:
+        assert lib.softmax_debug_set(0, 0) == 0
+    assert lib.softmax_sync(s) == 0                       # reported once
+    assert lib.softmax_debug_set(7, 0) == 1               # unknown flags
+    Y = run(lib, Xs, cols, DT_F32)
+    assert lib.softmax_sync(s) == 0
+    check(orc, Xs, cols, DT_F32, DT_F32, Y, canary=False)
