@@ -29,8 +29,9 @@
  * (same pointer, same leading dimension, same type: in place); any other
  * overlap of the two is rejected.
  *
- * Rows of 256 bytes to 64 KB that start on 16-byte boundaries are staged in
- * shared memory by bulk copies (TMA): one CTA of 16 warps per SM, split into
+ * Rows of 256 bytes to 64 KB (and at most 16384 elements) that start on
+ * 16-byte boundaries are staged in shared memory by bulk copies (TMA): one
+ * CTA of 16 warps per SM, split into
  * groups of 1-16 warps, each group a pipeline that keeps the copies of its
  * next few rows in flight while it works on one (~130-190 KB per SM in all),
  * so HBM is streamed without registers holding the loads.  Other rows are
@@ -87,7 +88,7 @@ typedef struct {
     int32_t unit_rows;     /* staged: rows per slot -- 1: the group's warps share a row;
                               more: each warp takes its own rows of the slot, and rows that
                               are adjacent in X arrive in one copy of the whole slot */
-    int32_t reserved;
+    int32_t kv;            /* staged: 16-byte vectors of a row per thread (1, 2, 4, 8) */
     int64_t hbm_bytes;     /* bytes this plan moves to and from HBM */
 } softmax_plan_t;
 

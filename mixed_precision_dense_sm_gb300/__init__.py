@@ -70,7 +70,7 @@ SOFTMAX_MODES = {0: "noop", 1: "warp", 2: "cta", 3: "stream"}
 class SoftmaxPlan(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "mode", "threads", "cluster", "slice", "vec", "grid", "depth", "group_warps", "unit_rows",
-        "reserved")] + \
+        "kv")] + \
         [("hbm_bytes", ctypes.c_int64)]
 
     def as_dict(self):

@@ -24,9 +24,10 @@ constexpr int64_t kWarpMaxCols = 32 * smx::kE;          // 1024
 constexpr int64_t kCtaSmallCols = 256 * smx::kE;        // 8192: 256-thread CTAs
 constexpr int64_t kCtaMaxCols = 512 * smx::kE;          // 16384 per CTA
 constexpr int64_t kMaxCols = int64_t(1) << 30;
-// Rows staged in shared memory by bulk copies: 256 B to 64 KB, one row per
-// group of warps at a time (the group holds its row in registers, at most
-// kTmaMaxVec 16-byte vectors per thread), slots within this budget.
+// Rows staged in shared memory by bulk copies: 256 B to 64 KB and at most
+// 16 warps x 32 x kTmaMaxElems elements, one row per group of warps at a time
+// (the group holds its row in registers, at most kTmaMaxElems elements per
+// thread), slots within this budget.
 constexpr int64_t kStagedMinBytes = 256;
 constexpr int64_t kStagedMaxBytes = 64 * 1024;
 constexpr int64_t kStagedSmemBudget = 200 * 1024;
@@ -87,14 +88,17 @@ gemm_status_t make_plan(int64_t rows, int64_t cols, const void* X, int64_t ldx, 
     pl.pub.vec = (aligned_to(X, 16) && aligned_to(Y, 16) && (ldx * ex) % 16 == 0 &&
                   (ldy * ey) % 16 == 0) ? 1 : 0;
     const int64_t row_bytes = cols * ex;
-    if (pl.pub.vec && row_bytes >= kStagedMinBytes && row_bytes <= kStagedMaxBytes) {
+    const int64_t kvmax = smx::kTmaMaxElems / (16 / ex);     // vectors per thread
+    const int64_t max_vec = (smx::kTmaThreads / 32) * 32 * kvmax;
+    if (pl.pub.vec && row_bytes >= kStagedMinBytes && row_bytes <= kStagedMaxBytes &&
+        row_bytes / 16 <= max_vec) {
         // staged in shared memory: one CTA of 16 warps per SM, split into
         // groups just large enough to hold a row in registers; each group a
         // pipeline of `depth` row slots
         const int64_t nvec = row_bytes / 16;
         int64_t gw = 1, unit_rows = 1, row_stride = 0;
         bool contiguous = false;
-        if (nvec <= 32 * smx::kTmaMaxVec) {
+        if (nvec <= 32 * kvmax) {
             // a warp holds a row: groups of 8 warps share slots of several
             // rows, moved by one copy of ~16 KB when the rows are adjacent
             gw = 8;
@@ -104,8 +108,12 @@ gemm_status_t make_plan(int64_t rows, int64_t cols, const void* X, int64_t ldx, 
             k = k < 1 ? 1 : (k > 4 ? 4 : k);
             unit_rows = gw * k;
         } else {
-            while (gw * 32 * smx::kTmaMaxVec < nvec) gw *= 2;
+            while (gw * 32 * kvmax < nvec) gw *= 2;
         }
+        // vectors per thread: the least power of two that covers the row
+        const int64_t threads_per_row = unit_rows > 1 ? 32 : gw * 32;
+        int64_t kv = 1;
+        while (kv * threads_per_row < nvec) kv *= 2;
         const int64_t groups = (smx::kTmaThreads / 32) / gw;
         const int64_t slot = round_up(unit_rows == 1 ? row_bytes : unit_rows * row_stride, 128);
         int64_t depth = kStagedSmemBudget / (groups * slot);
@@ -116,6 +124,7 @@ gemm_status_t make_plan(int64_t rows, int64_t cols, const void* X, int64_t ldx, 
         pl.pub.depth = static_cast<int32_t>(depth);
         pl.pub.group_warps = static_cast<int32_t>(gw);
         pl.pub.unit_rows = static_cast<int32_t>(unit_rows);
+        pl.pub.kv = static_cast<int32_t>(kv);
         pl.row_stride = static_cast<int32_t>(row_stride);
         pl.contiguous = contiguous ? 1 : 0;
         pl.resident = true;
@@ -298,6 +307,7 @@ gemm_status_t softmax_rows(int64_t rows, int64_t cols, const void* X, int64_t ld
         q.unit_rows = pl.pub.unit_rows;
         q.row_stride = pl.row_stride;
         q.contiguous = pl.contiguous;
+        q.kv = pl.pub.kv;
         q.err = err;
         {
             std::lock_guard<std::mutex> g(g_dbg_mu);

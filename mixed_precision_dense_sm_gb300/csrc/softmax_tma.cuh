@@ -3,15 +3,16 @@
 // aligned.
 //
 // One CTA of 16 warps per SM, split into groups of `group_warps` warps (1 to
-// 16, sized so that a row fits in the group's registers at <= 8 16-byte
-// vectors per thread).  Every group is an independent pipeline over its own
+// 16, sized so that a row fits in the group's registers at <= 32 elements
+// per thread).  Every group is an independent pipeline over its own
 // rows with `depth` row slots: its first thread keeps the bulk copies of the
 // next depth - 1 rows in flight while the group works on one, so an SM has
 // ~130-190 KB of loads outstanding without registers holding them, and up to
 // 16 rows are worked on at once.  A row is moved from its slot into registers
-// once; the maximum (NaN-propagating), the sum of exp(x - m) and the output
-// exp(x - m) / s then run on the registers -- the three steps of the SGEMM
-// tutorial page, section 2.1, with HBM and shared memory each read once.  The
+// once, as FP32; the maximum (NaN-propagating), e = exp(x - m) with its sum,
+// and the output e / s then run on the registers -- the three steps of the
+// SGEMM tutorial page, section 2.1, with HBM and shared memory each read once
+// and one exponential per element.  The
 // last (cols * size) % 16 bytes of a row, which a bulk copy cannot move, are
 // read from global memory directly.
 //
@@ -27,7 +28,7 @@ namespace smx {
 
 constexpr int kTmaThreads = 512;         // 16 warps
 constexpr int kTmaMaxDepth = 8;
-constexpr int kTmaMaxVec = 8;            // 16-byte vectors of a row per thread
+constexpr int kTmaMaxElems = 32;         // row elements per thread (held as FP32)
 constexpr uint32_t kSmxDebugSkipFirstLoad = 1u;
 
 struct TmaSoftmaxParams {
@@ -44,6 +45,7 @@ struct TmaSoftmaxParams {
                             // group_warps (each warp of the group takes its own rows)
     int32_t row_stride;     // bytes from one row to the next inside a slot
     int32_t contiguous;     // 1: a slot's rows are adjacent in X, one copy moves them all
+    int32_t kv;             // 16-byte vectors per thread: 1, 2, 4 (or 8 for FP32 input)
     int* err;               // device error word (1: a wait ran out)
     uint64_t wait_limit_ns;
     uint32_t debug_flags;
@@ -135,34 +137,41 @@ __device__ __forceinline__ void issue_unit(const TmaSoftmaxParams& p, uint8_t* s
     }
 }
 
-// One row from its slot: into registers (vector k of thread t is vector
-// t + k * T), maximum, sum of exp(x - m), output.  The T threads are one
-// warp (gw = 1) or the group's gw warps, which combine their partial results
+// One row from its slot: KV 16-byte vectors per thread (vector k of thread t
+// is vector t + k * T) into registers as FP32 -- each element converted once
+// -- then the maximum, e = exp(x - m) kept in place of x, s = sum e, and the
+// output e / s.  One exponential per element.  The T threads are one warp
+// (gw = 1) or the group's gw warps, which combine their partial results
 // through red_m / red_s and the group barrier.
-template <typename InT, typename OutT>
+template <typename InT, typename OutT, int KV>
 __device__ __forceinline__ void process_row(const uint8_t* srow, const InT* __restrict__ grow,
                                             OutT* __restrict__ yrow, int32_t nvec,
                                             int32_t bulk_elems, int32_t cols, int t, int T,
                                             int gw, int group, int warp, int lane,
                                             float* red_m, float* red_s) {
     constexpr int V = VecOf<InT>::V;
-    uint4 u[kTmaMaxVec];
+    float x[KV][V];
     #pragma unroll
-    for (int k = 0; k < kTmaMaxVec; ++k) {
+    for (int k = 0; k < KV; ++k) {
         const int32_t v = t + k * T;
-        if (v < nvec) u[k] = *reinterpret_cast<const uint4*>(srow + static_cast<size_t>(v) * 16);
+        if (v < nvec) {
+            const uint4 u = *reinterpret_cast<const uint4*>(srow + static_cast<size_t>(v) * 16);
+            const InT* q = reinterpret_cast<const InT*>(&u);
+            #pragma unroll
+            for (int e = 0; e < V; ++e) x[k][e] = to_f(q[e]);
+        } else {
+            #pragma unroll
+            for (int e = 0; e < V; ++e) x[k][e] = -INFINITY;
+        }
     }
     const int32_t te = bulk_elems + t;                  // at most one tail element each
-    const float xt = te < cols ? to_f(grow[te]) : -INFINITY;
+    float xt = te < cols ? to_f(grow[te]) : -INFINITY;
 
     float m = xt;
     #pragma unroll
-    for (int k = 0; k < kTmaMaxVec; ++k) {
-        if (t + k * T < nvec) {
-            const InT* q = reinterpret_cast<const InT*>(&u[k]);
-            #pragma unroll
-            for (int e = 0; e < V; ++e) m = fmax_nan(m, to_f(q[e]));
-        }
+    for (int k = 0; k < KV; ++k) {
+        #pragma unroll
+        for (int e = 0; e < V; ++e) m = fmax_nan(m, x[k][e]);
     }
     m = warp_max(m);
     if (gw > 1) {
@@ -171,15 +180,19 @@ __device__ __forceinline__ void process_row(const uint8_t* srow, const InT* __re
         m = red_m[group * gw];
         for (int w = 1; w < gw; ++w) m = fmax_nan(m, red_m[group * gw + w]);
     }
-    float s = te < cols ? __expf(xt - m) : 0.0f;
+    // padding entries are -inf: exp gives 0 unless m is -inf or +inf or NaN,
+    // in which case the row is NaN anyway
+    float s = 0.0f;
     #pragma unroll
-    for (int k = 0; k < kTmaMaxVec; ++k) {
-        if (t + k * T < nvec) {
-            const InT* q = reinterpret_cast<const InT*>(&u[k]);
-            #pragma unroll
-            for (int e = 0; e < V; ++e) s += __expf(to_f(q[e]) - m);
+    for (int k = 0; k < KV; ++k) {
+        #pragma unroll
+        for (int e = 0; e < V; ++e) {
+            x[k][e] = __expf(x[k][e] - m);
+            s += x[k][e];
         }
     }
+    xt = __expf(xt - m);
+    if (te < cols) s += xt;
     s = warp_sum(s);
     if (gw > 1) {
         if (lane == 0) red_s[warp] = s;
@@ -189,20 +202,19 @@ __device__ __forceinline__ void process_row(const uint8_t* srow, const InT* __re
     }
     const float inv_s = 1.0f / s;
     #pragma unroll
-    for (int k = 0; k < kTmaMaxVec; ++k) {
+    for (int k = 0; k < KV; ++k) {
         const int32_t v = t + k * T;
         if (v < nvec) {
-            const InT* q = reinterpret_cast<const InT*>(&u[k]);
             float o[V];
             #pragma unroll
-            for (int e = 0; e < V; ++e) o[e] = __expf(to_f(q[e]) - m) * inv_s;
+            for (int e = 0; e < V; ++e) o[e] = x[k][e] * inv_s;
             store_vec16<InT, OutT>(yrow + static_cast<int64_t>(v) * V, o);
         }
     }
-    if (te < cols) yrow[te] = from_f<OutT>(__expf(xt - m) * inv_s);
+    if (te < cols) yrow[te] = from_f<OutT>(xt * inv_s);
 }
 
-template <typename InT, typename OutT>
+template <typename InT, typename OutT, int KV>
 __global__ void __launch_bounds__(kTmaThreads, 1)
     softmax_tma_kernel(const __grid_constant__ TmaSoftmaxParams p) {
     constexpr int V = VecOf<InT>::V;
@@ -262,14 +274,14 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
         const uint8_t* sunit = ps + (i % D) * p.slot_bytes;
         if (p.unit_rows == 1) {
             // the group shares the row
-            process_row<InT, OutT>(sunit, X + first * p.ldx, Y + first * p.ldy, nvec,
+            process_row<InT, OutT, KV>(sunit, X + first * p.ldx, Y + first * p.ldy, nvec,
                                    p.bulk_elems, p.cols, gt, GT, GW, group, warp, lane, red_m, red_s);
         } else {
             // each warp of the group takes its own rows of the unit
             const int64_t left = p.rows - first;
             const int nr = static_cast<int>(left < p.unit_rows ? left : p.unit_rows);
             for (int j = wg; j < nr; j += GW)
-                process_row<InT, OutT>(sunit + static_cast<size_t>(j) * p.row_stride,
+                process_row<InT, OutT, KV>(sunit + static_cast<size_t>(j) * p.row_stride,
                                        X + (first + j) * p.ldx, Y + (first + j) * p.ldy, nvec,
                                        p.bulk_elems, p.cols, lane, 32, 1, group, warp, lane,
                                        red_m, red_s);
@@ -288,10 +300,10 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
     }
 }
 
-template <typename InT, typename OutT>
-cudaError_t launch_softmax_tma(const TmaSoftmaxParams& p, int grid, size_t smem,
-                               cudaStream_t stream) {
-    auto kern = softmax_tma_kernel<InT, OutT>;
+template <typename InT, typename OutT, int KV>
+cudaError_t launch_softmax_tma_kv(const TmaSoftmaxParams& p, int grid, size_t smem,
+                                  cudaStream_t stream) {
+    auto kern = softmax_tma_kernel<InT, OutT, KV>;
     {
         static std::mutex mu;
         static size_t raised = 0;
@@ -314,6 +326,21 @@ cudaError_t launch_softmax_tma(const TmaSoftmaxParams& p, int grid, size_t smem,
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, kern, p);
+}
+
+template <typename InT, typename OutT>
+cudaError_t launch_softmax_tma(const TmaSoftmaxParams& p, int grid, size_t smem,
+                               cudaStream_t stream) {
+    constexpr int kMaxKV = kTmaMaxElems / VecOf<InT>::V;
+    switch (p.kv) {
+        case 1: return launch_softmax_tma_kv<InT, OutT, 1>(p, grid, smem, stream);
+        case 2: return launch_softmax_tma_kv<InT, OutT, 2>(p, grid, smem, stream);
+        case 4: return launch_softmax_tma_kv<InT, OutT, 4>(p, grid, smem, stream);
+        case 8:
+            if constexpr (kMaxKV >= 8) return launch_softmax_tma_kv<InT, OutT, 8>(p, grid, smem, stream);
+            return cudaErrorInvalidValue;
+        default: return cudaErrorInvalidValue;
+    }
 }
 
 }  // namespace smx
