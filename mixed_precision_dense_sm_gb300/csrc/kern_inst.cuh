@@ -60,8 +60,12 @@ static cudaError_t launch_tc_cfg(const TcLaunch& l) {
             {
                 std::lock_guard<std::mutex> g(mu);
                 if (cached_smem != l.smem_bytes) {
-                    cfg.gridDim = dim3(grid, 1, 1);
-                    if (cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg) != cudaSuccess) {
+                    // the query takes the cluster shape alone
+                    cudaLaunchConfig_t q = cfg;
+                    q.gridDim = dim3(grid, 1, 1);
+                    q.attrs = &attr[1];
+                    q.numAttrs = 1;
+                    if (cudaOccupancyMaxActiveClusters(&clusters, kern, &q) != cudaSuccess) {
                         cudaGetLastError();
                         clusters = 0;
                     }

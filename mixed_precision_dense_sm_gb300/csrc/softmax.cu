@@ -90,15 +90,36 @@ gemm_status_t make_plan(int64_t rows, int64_t cols, const void* X, int64_t ldx, 
     const int64_t row_bytes = cols * ex;
     const int64_t kvmax = smx::kTmaMaxElems / (16 / ex);     // vectors per thread
     const int64_t max_vec = (smx::kTmaThreads / 32) * 32 * kvmax;
-    if (pl.pub.vec && row_bytes >= kStagedMinBytes && row_bytes <= kStagedMaxBytes &&
-        row_bytes / 16 <= max_vec) {
+    // a row (or, split over a cluster, a slice of it) fits one CTA's slots
+    // and registers
+    auto fits = [&](int64_t elems) {
+        const int64_t b = elems * ex;
+        return b >= kStagedMinBytes && b <= kStagedMaxBytes && b / 16 <= max_vec;
+    };
+    int64_t staged_cl = 0;
+    if (pl.pub.vec) {
+        if (fits(cols)) {
+            staged_cl = 1;
+        } else if (cols * ex > kStagedMaxBytes || cols * ex / 16 > max_vec) {
+            for (int64_t c = 2; c <= smx::kMaxCluster; c *= 2)
+                if (fits(round_up(ceil_div(cols, c), 8))) {
+                    staged_cl = c;
+                    break;
+                }
+        }
+    }
+    if (staged_cl > 0) {
         // staged in shared memory: one CTA of 16 warps per SM, split into
         // groups just large enough to hold a row in registers; each group a
-        // pipeline of `depth` row slots
-        const int64_t nvec = row_bytes / 16;
+        // pipeline of `depth` row slots.  A row too long for one CTA is split
+        // over a cluster, each CTA one group with a slice.
+        const int64_t slice = staged_cl > 1 ? round_up(ceil_div(cols, staged_cl), 8) : cols;
+        const int64_t nvec = slice * ex / 16;
         int64_t gw = 1, unit_rows = 1, row_stride = 0;
         bool contiguous = false;
-        if (nvec <= 32 * kvmax) {
+        if (staged_cl > 1) {
+            gw = smx::kTmaThreads / 32;
+        } else if (nvec <= 32 * kvmax) {
             // a warp holds a row: groups of 8 warps share slots of several
             // rows, moved by one copy of ~16 KB when the rows are adjacent
             gw = 8;
@@ -115,12 +136,13 @@ gemm_status_t make_plan(int64_t rows, int64_t cols, const void* X, int64_t ldx, 
         int64_t kv = 1;
         while (kv * threads_per_row < nvec) kv *= 2;
         const int64_t groups = (smx::kTmaThreads / 32) / gw;
-        const int64_t slot = round_up(unit_rows == 1 ? row_bytes : unit_rows * row_stride, 128);
+        const int64_t slot = round_up(unit_rows == 1 ? slice * ex : unit_rows * row_stride, 128);
         int64_t depth = kStagedSmemBudget / (groups * slot);
         if (depth > smx::kTmaMaxDepth) depth = smx::kTmaMaxDepth;
         pl.pub.mode = unit_rows > 1 ? SOFTMAX_MODE_WARP : SOFTMAX_MODE_CTA;
         pl.pub.threads = smx::kTmaThreads;
-        pl.pub.slice = static_cast<int32_t>(round_up(cols, 8));
+        pl.pub.cluster = static_cast<int32_t>(staged_cl);
+        pl.pub.slice = static_cast<int32_t>(round_up(slice, 8));
         pl.pub.depth = static_cast<int32_t>(depth);
         pl.pub.group_warps = static_cast<int32_t>(gw);
         pl.pub.unit_rows = static_cast<int32_t>(unit_rows);
@@ -130,8 +152,14 @@ gemm_status_t make_plan(int64_t rows, int64_t cols, const void* X, int64_t ldx, 
         pl.resident = true;
         pl.smem = static_cast<size_t>(round_up(groups * depth * 8, 128) + groups * depth * slot);
         pl.bulk_elems = static_cast<int32_t>((row_bytes / 16) * 16 / ex);
-        const int64_t need = ceil_div(ceil_div(rows, unit_rows), groups);
-        pl.pub.grid = static_cast<int32_t>(need < num_sms ? need : num_sms);
+        if (staged_cl == 1) {
+            const int64_t need = ceil_div(ceil_div(rows, unit_rows), groups);
+            pl.pub.grid = static_cast<int32_t>(need < num_sms ? need : num_sms);
+        } else {
+            int64_t clusters = ctas_per_sm > 0 ? ctas_per_sm : num_sms / staged_cl;
+            if (clusters < 1) clusters = 1;
+            pl.pub.grid = static_cast<int32_t>(staged_cl * (rows < clusters ? rows : clusters));
+        }
     } else if (cols <= kWarpMaxCols) {
         pl.pub.mode = SOFTMAX_MODE_WARP;
         pl.pub.threads = smx::kWarpCtaThreads;
@@ -269,9 +297,11 @@ gemm_status_t softmax_rows(int64_t rows, int64_t cols, const void* X, int64_t ld
     DeviceInfo dev;
     if (!device_info(dev)) return GEMM_ERR_LAUNCH;
     if (!dev.sm103) return GEMM_ERR_NOT_SUPPORTED;
-    // the shape first (threads, cluster), then the resident groups for it
+    // the shape first (threads, cluster), then, for the register kernels, the
+    // resident groups for it (the staged kernels run one CTA per SM; their
+    // launch caps a cluster grid by the clusters that fit)
     Plan pl;
-    st = make_plan(rows, cols, X, ldx, x_dtype, Y, ldy, y_dtype, dev.sms, 1, pl);
+    st = make_plan(rows, cols, X, ldx, x_dtype, Y, ldy, y_dtype, dev.sms, 0, pl);
     if (st != GEMM_OK) return st;
     const bool warp_rows = pl.pub.mode == SOFTMAX_MODE_WARP;
     if (pl.pub.depth == 0) {
@@ -300,7 +330,8 @@ gemm_status_t softmax_rows(int64_t rows, int64_t cols, const void* X, int64_t ld
         q.cols = static_cast<int32_t>(cols);
         q.bulk_elems = pl.bulk_elems;
         q.slot_bytes = static_cast<int32_t>(
-            round_up(pl.pub.unit_rows == 1 ? cols * elem_bytes(x_dtype)
+            round_up(pl.pub.unit_rows == 1 ? int64_t(pl.pub.slice < cols ? pl.pub.slice : cols) *
+                                                 elem_bytes(x_dtype)
                                            : int64_t(pl.pub.unit_rows) * pl.row_stride, 128));
         q.depth = pl.pub.depth;
         q.group_warps = pl.pub.group_warps;
@@ -308,6 +339,8 @@ gemm_status_t softmax_rows(int64_t rows, int64_t cols, const void* X, int64_t ld
         q.row_stride = pl.row_stride;
         q.contiguous = pl.contiguous;
         q.kv = pl.pub.kv;
+        q.cluster = pl.pub.cluster;
+        q.slice = pl.pub.slice;
         q.err = err;
         {
             std::lock_guard<std::mutex> g(g_dbg_mu);

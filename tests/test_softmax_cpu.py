@@ -70,46 +70,62 @@ def test_work_split(cols, mode, threads, cluster):
     assert p["depth"] == 0 and p["vec"] == 0
 
 
-@pytest.mark.parametrize("cols,dt,ld,gw,unit,depth,kv", [
-    (64, DT_F32, 64, 8, 32, 8, 1), (1024, DT_F32, 1024, 8, 8, 3, 8),
-    (1000, DT_F32, 1004, 8, 8, 3, 8), (128, DT_BF16, 128, 8, 32, 8, 1),
-    (1024, DT_BF16, 1024, 8, 8, 6, 4), (2048, DT_F32, 2048, 2, 1, 3, 8),
-    (4096, DT_BF16, 4096, 4, 1, 6, 4), (2052, DT_F32, 2052, 4, 1, 6, 8),
-    (4096, DT_F32, 4096, 4, 1, 3, 8), (8192, DT_F32, 8192, 8, 1, 3, 8),
-    (16384, DT_F32, 16384, 16, 1, 3, 8), (16384, DT_BF16, 16384, 16, 1, 6, 4),
-    (3000, DT_F16, 3000, 4, 1, 8, 4), (32768, DT_F16, 32768, 0, 0, 0, 0),
-    (16388, DT_F32, 16388, 0, 0, 0, 0), (60, DT_F32, 60, 0, 0, 0, 0),
-    (120, DT_BF16, 120, 0, 0, 0, 0)])
-def test_staged_split(cols, dt, ld, gw, unit, depth, kv):
+@pytest.mark.parametrize("cols,dt,ld,cl,gw,unit,depth,kv", [
+    (64, DT_F32, 64, 1, 8, 32, 8, 1), (1024, DT_F32, 1024, 1, 8, 8, 3, 8),
+    (1000, DT_F32, 1004, 1, 8, 8, 3, 8), (128, DT_BF16, 128, 1, 8, 32, 8, 1),
+    (1024, DT_BF16, 1024, 1, 8, 8, 6, 4), (2048, DT_F32, 2048, 1, 2, 1, 3, 8),
+    (4096, DT_BF16, 4096, 1, 4, 1, 6, 4), (2052, DT_F32, 2052, 1, 4, 1, 6, 8),
+    (4096, DT_F32, 4096, 1, 4, 1, 3, 8), (8192, DT_F32, 8192, 1, 8, 1, 3, 8),
+    (16384, DT_F32, 16384, 1, 16, 1, 3, 8), (16384, DT_BF16, 16384, 1, 16, 1, 6, 4),
+    (3000, DT_F16, 3000, 1, 4, 1, 8, 4),
+    # split over a cluster, one group (the CTA) per slice
+    (16388, DT_F32, 16388, 2, 16, 1, 6, 8), (32768, DT_F16, 32768, 2, 16, 1, 6, 4),
+    (65536, DT_F32, 65536, 4, 16, 1, 3, 8), (131072, DT_F32, 131072, 8, 16, 1, 3, 8),
+    (20000, DT_BF16, 20000, 2, 16, 1, 8, 4),
+    # not staged: too short, too long, or rows not 16-byte aligned
+    (131080, DT_F32, 131080, 8, 0, 0, 0, 0), (60, DT_F32, 60, 1, 0, 0, 0, 0),
+    (120, DT_BF16, 120, 1, 0, 0, 0, 0), (16385, DT_F32, 16385, 2, 0, 0, 0, 0)])
+def test_staged_split(cols, dt, ld, cl, gw, unit, depth, kv):
     """16-byte-aligned rows of 256 B to 64 KB (<= 16384 elements) are staged
     in shared memory by bulk copies: one CTA of 16 warps per SM.  Rows a warp
     can hold (<= 1024 elements) go to groups of 8 warps whose slots carry
     several rows (~16 KB, one copy when the rows are adjacent), a warp per
     row; longer rows are shared by a group just large enough to hold them in
-    registers (<= 32 elements per thread).  Each group is a pipeline with as many slots as 200 KB allow
-    (at most 8).  Shorter or longer rows keep the register kernels (depth 0)."""
+    registers (<= 32 elements per thread); rows longer still are split over a
+    cluster of 2 to 8 CTAs, a slice each.  Each group is a pipeline with as
+    many slots as 200 KB allow (at most 8).  Other rows keep the register
+    kernels (depth 0)."""
     st, p = plan(100000, cols, ldx=ld, ldy=ld, xdt=dt, ydt=dt)
     assert st == OK
-    assert (p["group_warps"], p["unit_rows"], p["depth"], p["kv"]) == (gw, unit, depth, kv), p
+    got = (p["cluster"], p["group_warps"], p["unit_rows"], p["depth"], p["kv"])
+    assert got == (cl, gw, unit, depth, kv), p
     es = 4 if dt == DT_F32 else 2
     kvmax = 32 * es // 16                   # 32 elements per thread
     if depth:
-        assert p["vec"] == 1 and p["cluster"] == 1 and p["grid"] == 152 and p["threads"] == 512
+        assert p["vec"] == 1 and p["threads"] == 512
+        assert p["grid"] == (152 if cl == 1 else cl * (152 // cl))
         assert p["mode_name"] == ("warp" if unit > 1 else "cta")
         groups = 16 // gw
-        stride = ld * es if unit > 1 else cols * es
+        slice_ = p["slice"] if cl > 1 else cols
+        assert slice_ % 8 == 0 or cl == 1
+        assert cl == 1 or ((cols + cl - 1) // cl <= slice_ < (cols + cl - 1) // cl + 8)
+        stride = ld * es if unit > 1 else slice_ * es
         slot = -(-unit * stride // 128) * 128
         assert groups * depth * slot <= 200 * 1024 and depth >= 3
-        nvec = cols * es // 16
+        nvec = slice_ * es // 16
         if unit == 1:
-            assert gw * 32 * kvmax >= nvec and (gw == 1 or (gw // 2) * 32 * kvmax < nvec)
+            assert gw * 32 * kvmax >= nvec
+            assert cl > 1 or gw == 1 or (gw // 2) * 32 * kvmax < nvec
             assert kv * gw * 32 >= nvec and (kv == 1 or (kv // 2) * gw * 32 < nvec)
         else:
             assert nvec <= 32 * kvmax and unit % gw == 0
             assert kv * 32 >= nvec and (kv == 1 or (kv // 2) * 32 < nvec)
         assert p["hbm_bytes"] == 100000 * cols * 2 * es
-        rows = 5 * unit
-        assert plan(rows, cols, ldx=ld, ldy=ld, xdt=dt, ydt=dt)[1]["grid"] == -(-5 // groups)
+        if cl == 1:
+            rows = 5 * unit
+            assert plan(rows, cols, ldx=ld, ldy=ld, xdt=dt, ydt=dt)[1]["grid"] == -(-5 // groups)
+        else:
+            assert plan(3, cols, ldx=ld, ldy=ld, xdt=dt, ydt=dt)[1]["grid"] == 3 * cl
     few = plan(3, cols, xdt=dt, ydt=dt)[1]
     assert few["grid"] <= 3 * few["cluster"]
 

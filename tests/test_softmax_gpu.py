@@ -83,7 +83,7 @@ def check(orc, Xs: torch.Tensor, cols: int, x_dt: int, y_dt: int, Y: torch.Tenso
 
 
 COLS = [1, 2, 7, 31, 32, 33, 100, 1000, 1024, 1025, 2049, 4096, 8192, 8193, 12345, 16384,
-        16385, 40000, 131072, 131073, 300001]
+        16385, 16392, 32768, 40000, 65536, 100000, 131072, 131073, 300001]
 
 
 @pytest.mark.parametrize("cols", COLS)
@@ -229,13 +229,14 @@ def test_empty_and_errors(lib):
     assert torch.all(Y == 7.0)
 
 
-@pytest.mark.parametrize("cols", [1024, 8192])
+@pytest.mark.parametrize("cols", [1024, 8192, 65536])
 def test_timeout_reported_without_fault(lib, orc, cols):
     """The failure path of the staged kernels, without a GPU fault: the test
     hook arms the first row slot of the first pipeline without issuing its
     copy, so that bounded wait runs out (limit 0.2 s).  softmax_sync reports
     GEMM_ERR_DEVICE_TIMEOUT once; the next call on the same device is
-    correct.  1024 FP32 columns run one pipeline per warp, 8192 one per CTA."""
+    correct.  1024 FP32 columns run a warp per row, 8192 a group per row,
+    65536 a cluster of 4 CTAs per row (the whole cluster leaves together)."""
     g = torch.Generator().manual_seed(5)
     Xs = stored(torch.randn((64, cols), generator=g), cols, DT_F32)
     st, p = lib.softmax_plan_query(64, cols, 256, cols, DT_F32, 1 << 44, cols, DT_F32)
