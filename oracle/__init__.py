@@ -1,5 +1,5 @@
-"""CPU oracle for C = alpha*op(A)*op(B) + beta*C (FP16/BF16 in, FP64 reference)
-and for the row softmax.
+"""CPU oracle for C = alpha*op(A)*op(B) + beta*C (FP16/BF16 in, FP64 reference),
+the row softmax and the forward 2-D convolution.
 
 TEST INFRASTRUCTURE ONLY.  Only the test-suite, ``__graft_entry__.smoke()`` and
 the ``cpu_baseline`` / ``--impl reference`` legs of ``bench.py`` may import this
@@ -101,6 +101,11 @@ class Oracle:
         lib.oracle_gemm_ex.argtypes = common + ep + [dp, dp, ctypes.c_int]
         lib.oracle_gemm_sampled_ex.restype = ctypes.c_int
         lib.oracle_gemm_sampled_ex.argtypes = common + ep + [i64, vp, vp, dp, dp, ctypes.c_int]
+        lib.oracle_conv2d_dims.restype = ctypes.c_int
+        lib.oracle_conv2d_dims.argtypes = [i64] * 10 + [ctypes.POINTER(i64)] * 2
+        lib.oracle_conv2d.restype = ctypes.c_int
+        lib.oracle_conv2d.argtypes = [i64] * 13 + [ctypes.c_float, vp, vp, ctypes.c_float, vp,
+                                                    ctypes.c_int, ctypes.c_int, dp, dp, ctypes.c_int]
         lib.oracle_softmax.restype = ctypes.c_int
         lib.oracle_softmax.argtypes = [i64, i64, vp, i64, ctypes.c_int, vp, i64, dp, ctypes.c_int]
         self.lib = lib
@@ -244,6 +249,38 @@ def _oracle_softmax_methods():
 
 
 _oracle_softmax_methods()
+
+
+def _oracle_conv_methods():
+    def conv2d_dims(self, H, W, R, S, pad_h, pad_w, stride_h, stride_w, dil_h, dil_w):
+        P, Q = ctypes.c_int64(), ctypes.c_int64()
+        st = self.lib.oracle_conv2d_dims(H, W, R, S, pad_h, pad_w, stride_h, stride_w, dil_h,
+                                         dil_w, ctypes.byref(P), ctypes.byref(Q))
+        if st != 0:
+            raise ValueError(f"oracle_conv2d_dims failed ({st})")
+        return P.value, Q.value
+
+    def conv2d(self, N, H, W, C, K, R, S, pad_h, pad_w, stride_h, stride_w, dil_h, dil_w,
+               alpha, X, Wt, beta, Yin, x_dtype, y_dtype, nthreads: int = 0):
+        """Forward 2-D convolution, NHWC input X, KRSC filter Wt (uint16 codes),
+        NPQK output.  Returns (R, S), float64 arrays of shape (N*P*Q, K)."""
+        P, Q = self.conv2d_dims(H, W, R, S, pad_h, pad_w, stride_h, stride_w, dil_h, dil_w)
+        X, Wt, Yin = _prep(X), _prep(Wt), _prep(Yin, c=True)
+        Rr = np.empty((N * P * Q, K), dtype=np.float64)
+        Sr = np.empty((N * P * Q, K), dtype=np.float64)
+        st = self.lib.oracle_conv2d(N, H, W, C, K, R, S, pad_h, pad_w, stride_h, stride_w,
+                                    dil_h, dil_w, float(alpha), _ptr(X), _ptr(Wt), float(beta),
+                                    _ptr(Yin), x_dtype, y_dtype, Rr.ctypes.data, Sr.ctypes.data,
+                                    nthreads)
+        if st != 0:
+            raise ValueError(f"oracle_conv2d failed ({st})")
+        return Rr, Sr
+
+    Oracle.conv2d_dims = conv2d_dims
+    Oracle.conv2d = conv2d
+
+
+_oracle_conv_methods()
 
 
 def get() -> Oracle:

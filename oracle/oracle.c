@@ -478,3 +478,90 @@ int oracle_softmax(int64_t rows, int64_t cols, const void* X, int64_t ldx, int x
     }
     return OR_OK;
 }
+
+/* ------------------------------------------------------ convolution oracle */
+
+/*
+ * 2-D convolution, forward (CATLASS page, section 5.1: a convolution is a
+ * four-deep loop that becomes a matrix product once the input windows are
+ * unrolled -- im2col -- which an implicit GEMM does without materialising
+ * them).  The page fixes no layout or padding rule; read as the usual deep
+ * learning convolution (a cross-correlation, the filter is not flipped),
+ * channels last:
+ *     X  N x H x W x C      input, element (n, h, w, c) at ((n*H + h)*W + w)*C + c
+ *     Wt K x R x S x C      filter, element (k, r, s, c) at ((k*R + r)*S + s)*C + c
+ *     Y  N x P x Q x K      output, element (n, p, q, k) at ((n*P + p)*Q + q)*K + k
+ *     P = (H + 2 pad_h - dil_h (R - 1) - 1) / stride_h + 1   (floor), Q alike
+ *     y = alpha * sum_{r, s, c} x(n, p*stride_h - pad_h + r*dil_h,
+ *                                   q*stride_w - pad_w + s*dil_w, c) * w(k, r, s, c)
+ *         + beta * y_in
+ * with x = 0 outside 0 <= h < H, 0 <= w < W (zero padding on every side).
+ * As a GEMM: M = N*P*Q rows, N = K columns, and the reduction runs over
+ * (r, s, c).  Inputs FP16/BF16 decoded exactly, products exact in binary64,
+ * summed in the order r, s, c; S receives sum |products| for the tolerance.
+ * R and S are (N*P*Q) x K row-major.  y_in (the output's own type) is read
+ * only when beta != 0.
+ */
+static int64_t conv_out_dim(int64_t in, int64_t pad, int64_t dil, int64_t f, int64_t stride) {
+    const int64_t span = in + 2 * pad - dil * (f - 1) - 1;
+    return span < 0 ? 0 : span / stride + 1;
+}
+
+int oracle_conv2d_dims(int64_t H, int64_t W, int64_t R, int64_t S, int64_t pad_h, int64_t pad_w,
+                       int64_t stride_h, int64_t stride_w, int64_t dil_h, int64_t dil_w,
+                       int64_t* P, int64_t* Q) {
+    if (H < 1 || W < 1 || R < 1 || S < 1 || pad_h < 0 || pad_w < 0 || stride_h < 1 ||
+        stride_w < 1 || dil_h < 1 || dil_w < 1)
+        return OR_BAD_ARG;
+    *P = conv_out_dim(H, pad_h, dil_h, R, stride_h);
+    *Q = conv_out_dim(W, pad_w, dil_w, S, stride_w);
+    return OR_OK;
+}
+
+int oracle_conv2d(int64_t N, int64_t H, int64_t W, int64_t C, int64_t K, int64_t R, int64_t S,
+                  int64_t pad_h, int64_t pad_w, int64_t stride_h, int64_t stride_w,
+                  int64_t dil_h, int64_t dil_w, float alpha, const void* X, const void* Wt,
+                  float beta, const void* Yin, int x_dtype, int y_dtype,
+                  double* Rout, double* Sout, int nthreads) {
+    int64_t P, Q;
+    if (N < 0 || C < 1 || K < 1) return OR_BAD_ARG;
+    if (oracle_conv2d_dims(H, W, R, S, pad_h, pad_w, stride_h, stride_w, dil_h, dil_w, &P, &Q))
+        return OR_BAD_ARG;
+    if (x_dtype != OR_F16 && x_dtype != OR_BF16) return OR_BAD_ARG;
+    if (y_dtype != OR_F16 && y_dtype != OR_BF16 && y_dtype != OR_F32) return OR_BAD_ARG;
+    const int64_t M = N * P * Q;
+    if (M == 0) return OR_OK;
+    if (X == NULL || Wt == NULL || Rout == NULL || Sout == NULL) return OR_BAD_ARG;
+    if (beta != 0.0f && Yin == NULL) return OR_BAD_ARG;
+    const double al = (double)alpha, be = (double)beta;
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#pragma omp parallel for schedule(dynamic, 8)
+#endif
+    for (int64_t m = 0; m < M; ++m) {
+        const int64_t n = m / (P * Q), p = (m / Q) % P, q = m % Q;
+        for (int64_t k = 0; k < K; ++k) {
+            double acc = 0.0, sabs = 0.0;
+            for (int64_t r = 0; r < R; ++r) {
+                const int64_t h = p * stride_h - pad_h + r * dil_h;
+                if (h < 0 || h >= H) continue;
+                for (int64_t s = 0; s < S; ++s) {
+                    const int64_t w = q * stride_w - pad_w + s * dil_w;
+                    if (w < 0 || w >= W) continue;
+                    for (int64_t c = 0; c < C; ++c) {
+                        const double a = decode_in(x_dtype, X, ((n * H + h) * W + w) * C + c);
+                        const double b = decode_in(x_dtype, Wt, ((k * R + r) * S + s) * C + c);
+                        const double prod = a * b;
+                        acc = acc + prod;
+                        sabs = sabs + fabs(prod);
+                    }
+                }
+            }
+            double y = al * acc;
+            if (be != 0.0) y = y + be * decode_c(y_dtype, Yin, m * K + k);
+            Rout[m * K + k] = y;
+            Sout[m * K + k] = sabs;
+        }
+    }
+    return OR_OK;
+}

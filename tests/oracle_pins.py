@@ -619,6 +619,129 @@ def pin_softmax_special_values(o):
         raise AssertionError(f"accepted {bad}")
 
 
+# --------------------------------------------------------------- convolution
+
+def _conv_case(rng, N, H, W, C, K, R, S, dt, integer=False):
+    if integer:
+        x = rng.integers(-3, 4, (N, H, W, C)).astype(np.float64)
+        w = rng.integers(-3, 4, (K, R, S, C)).astype(np.float64)
+        return _to_codes(x, dt), _to_codes(w, dt), x, w
+    xc = _random_codes(rng, (N, H, W, C), dt)
+    wc = _random_codes(rng, (K, R, S, C), dt)
+    return xc, wc, exact.codes_to_float64(xc, dt).reshape(N, H, W, C), \
+        exact.codes_to_float64(wc, dt).reshape(K, R, S, C)
+
+
+CONV_SHAPES = [
+    # N, H, W, C, K, R, S, pad_h, pad_w, stride_h, stride_w, dil_h, dil_w
+    (2, 5, 6, 3, 4, 3, 3, 1, 1, 1, 1, 1, 1),
+    (1, 7, 9, 2, 3, 3, 2, 0, 1, 2, 3, 2, 1),
+    (3, 4, 4, 5, 2, 1, 1, 0, 0, 1, 1, 1, 1),
+    (1, 8, 5, 4, 5, 5, 3, 2, 0, 1, 2, 1, 2),
+    (2, 3, 3, 1, 1, 3, 3, 2, 2, 1, 1, 1, 1),
+    (1, 8, 9, 2, 3, 3, 3, 1, 1, 2, 2, 1, 1),     # a stride that does not divide the span
+]
+
+
+def pin_conv_vs_torch(o):
+    """Against torch.nn.functional.conv2d in float64 (a cross-correlation with
+    zero padding, stride and dilation) on exactly decoded random inputs, both
+    input types, alpha and beta."""
+    import torch
+    rng = _rng(51)
+    for i, (N, H, W, C, K, R, S, ph, pw, sh, sw, dh, dw) in enumerate(CONV_SHAPES):
+        dt = (F16, BF16)[i % 2]
+        xc, wc, x, w = _conv_case(rng, N, H, W, C, K, R, S, dt)
+        P, Q = o.conv2d_dims(H, W, R, S, ph, pw, sh, sw, dh, dw)
+        yin = rng.standard_normal((N * P * Q, K)).astype(np.float32)
+        alpha, beta = (1.0, 0.0) if i % 2 else (0.5, -2.0)
+        Rr, Sr = o.conv2d(N, H, W, C, K, R, S, ph, pw, sh, sw, dh, dw, alpha, xc, wc, beta,
+                          yin if beta else None, dt, F32)
+        ref = torch.nn.functional.conv2d(torch.from_numpy(x).permute(0, 3, 1, 2),
+                                         torch.from_numpy(w).permute(0, 3, 1, 2),
+                                         stride=(sh, sw), padding=(ph, pw), dilation=(dh, dw))
+        ref = ref.permute(0, 2, 3, 1).reshape(N * P * Q, K).numpy()
+        assert ref.shape == Rr.shape
+        want = alpha * ref + beta * yin.astype(np.float64)
+        assert np.all(np.abs(Rr - want) <= 1e-13 * (np.abs(alpha) * Sr + np.abs(beta * yin)) + 1e-300), i
+
+
+def pin_conv_exact_bruteforce(o):
+    """Tiny shapes against a direct evaluation of the definition in exact
+    rationals (the products of 16-bit inputs are exact in binary64)."""
+    rng = _rng(52)
+    for i, (N, H, W, C, K, R, S, ph, pw, sh, sw, dh, dw) in enumerate(CONV_SHAPES[:4]):
+        dt = (BF16, F16)[i % 2]
+        xc, wc, x, w = _conv_case(rng, N, H, W, C, K, R, S, dt)
+        P, Q = o.conv2d_dims(H, W, R, S, ph, pw, sh, sw, dh, dw)
+        Rr, Sr = o.conv2d(N, H, W, C, K, R, S, ph, pw, sh, sw, dh, dw, 1.0, xc, wc, 0.0, None, dt, F32)
+        for n in range(N):
+            for p_ in range(P):
+                for q in range(Q):
+                    for k in range(K):
+                        acc = Fraction(0)
+                        for r in range(R):
+                            h = p_ * sh - ph + r * dh
+                            if not 0 <= h < H:
+                                continue
+                            for s_ in range(S):
+                                ww = q * sw - pw + s_ * dw
+                                if not 0 <= ww < W:
+                                    continue
+                                for c in range(C):
+                                    acc += Fraction(float(x[n, h, ww, c])) * Fraction(float(w[k, r, s_, c]))
+                        m = (n * P + p_) * Q + q
+                        assert abs(Fraction(float(Rr[m, k])) - acc) <= Fraction(2) ** -50 * Fraction(float(Sr[m, k]))
+
+
+def pin_conv_closed_forms(o):
+    """A 1 x 1 convolution is the matrix product X (NHW x C) W^T; a delta
+    filter copies the input shifted by its tap; all-ones inputs count the
+    taps that fall inside the image.  Integer inputs: exact."""
+    rng = _rng(53)
+    # 1 x 1, stride 1, no padding: a matrix product
+    xc, wc, x, w = _conv_case(rng, 2, 5, 7, 6, 4, 1, 1, BF16, integer=True)
+    Rr, _ = o.conv2d(2, 5, 7, 6, 4, 1, 1, 0, 0, 1, 1, 1, 1, 1.0, xc, wc, 0.0, None, BF16, F32)
+    assert (Rr == x.reshape(-1, 6) @ w.reshape(4, 6).T).all()
+    # delta filter at tap (r0, s0), K = C: output = input at the tapped position
+    N, H, W, C, R, S, ph, pw, sh, sw, dh, dw = 2, 6, 7, 3, 3, 3, 1, 2, 2, 1, 1, 2
+    x = rng.integers(-50, 50, (N, H, W, C)).astype(np.float64)
+    for r0, s0 in [(0, 0), (2, 1), (1, 2)]:
+        w = np.zeros((C, R, S, C))
+        for c in range(C):
+            w[c, r0, s0, c] = 1.0
+        P, Q = o.conv2d_dims(H, W, R, S, ph, pw, sh, sw, dh, dw)
+        Rr, _ = o.conv2d(N, H, W, C, C, R, S, ph, pw, sh, sw, dh, dw, 1.0, _to_codes(x, F16),
+                         _to_codes(w, F16), 0.0, None, F16, F32)
+        for n in range(N):
+            for p_ in range(P):
+                for q in range(Q):
+                    h, ww = p_ * sh - ph + r0 * dh, q * sw - pw + s0 * dw
+                    want = x[n, h, ww] if (0 <= h < H and 0 <= ww < W) else np.zeros(C)
+                    assert (Rr[(n * P + p_) * Q + q] == want).all()
+    # all ones: C times the number of taps inside the image
+    N, H, W, C, K, R, S, ph, pw, sh, sw, dh, dw = 1, 5, 4, 3, 2, 3, 3, 2, 1, 2, 1, 1, 2
+    ones = _to_codes(np.ones(N * H * W * C), F16)
+    wones = _to_codes(np.ones(K * R * S * C), F16)
+    P, Q = o.conv2d_dims(H, W, R, S, ph, pw, sh, sw, dh, dw)
+    Rr, _ = o.conv2d(N, H, W, C, K, R, S, ph, pw, sh, sw, dh, dw, 1.0, ones, wones, 0.0, None, F16, F32)
+    for p_ in range(P):
+        for q in range(Q):
+            taps = sum(1 for r in range(R) for s_ in range(S)
+                       if 0 <= p_ * sh - ph + r * dh < H and 0 <= q * sw - pw + s_ * dw < W)
+            assert (Rr[p_ * Q + q] == C * taps).all()
+    # argument checks and empty outputs
+    assert o.conv2d_dims(3, 3, 5, 1, 0, 0, 1, 1, 1, 1) == (0, 3)
+    for bad in [dict(C=0), dict(st=0), dict(dil=0), dict(pad=-1), dict(dt=F32)]:
+        try:
+            o.conv2d(1, 4, 4, bad.get("C", 2), 2, 3, 3, bad.get("pad", 1), 1, bad.get("st", 1), 1,
+                     bad.get("dil", 1), 1, 1.0, np.zeros(64, np.uint16), np.zeros(64, np.uint16),
+                     0.0, None, bad.get("dt", F16), F32)
+        except ValueError:
+            continue
+        raise AssertionError(f"accepted {bad}")
+
+
 def _to_codes_round(values, dtype):
     """float64 values -> nearest uint16 codes by torch's conversion (test inputs)."""
     import torch
@@ -636,4 +759,5 @@ ALL_PINS = [
     pin_activation_values, pin_epilogue_bruteforce, pin_epilogue_exact_and_sampled,
     pin_tf32_truncation, pin_gemm_tf32_bruteforce,
     pin_softmax_closed_forms, pin_softmax_library_and_invariants, pin_softmax_special_values,
+    pin_conv_vs_torch, pin_conv_exact_bruteforce, pin_conv_closed_forms,
 ]

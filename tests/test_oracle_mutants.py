@@ -78,6 +78,19 @@ MUTANTS = [
      "const int64_t i = t;"),
     ("softmax_masked_row_zero", "for (int64_t j = 0; j < cols; ++j) y[j] = y[j] / s;",
      "for (int64_t j = 0; j < cols; ++j) y[j] = (s > 0.0) ? y[j] / s : 0.0;"),
+    ("conv_filter_flipped", "decode_in(x_dtype, Wt, ((k * R + r) * S + s) * C + c);",
+     "decode_in(x_dtype, Wt, ((k * R + (R - 1 - r)) * S + s) * C + c);"),
+    ("conv_pad_sign", "const int64_t h = p * stride_h - pad_h + r * dil_h;",
+     "const int64_t h = p * stride_h + pad_h + r * dil_h;"),
+    ("conv_stride_ignored", "const int64_t w = q * stride_w - pad_w + s * dil_w;",
+     "const int64_t w = q - pad_w + s * dil_w;"),
+    ("conv_dilation_ignored", "const int64_t h = p * stride_h - pad_h + r * dil_h;",
+     "const int64_t h = p * stride_h - pad_h + r;"),
+    ("conv_channels_reversed", "decode_in(x_dtype, X, ((n * H + h) * W + w) * C + c);",
+     "decode_in(x_dtype, X, ((n * H + h) * W + w) * C + (C - 1 - c));"),
+    ("conv_out_size", "return span < 0 ? 0 : span / stride + 1;", "return span < 0 ? 0 : (span + stride - 1) / stride + 1;"),
+    ("conv_beta_dropped", "if (be != 0.0) y = y + be * decode_c(y_dtype, Yin, m * K + k);", "(void)Yin;"),
+    ("conv_no_padding_check", "if (w < 0 || w >= W) continue;", "if (w < 0) continue;"),
     ("beta_read_when_zero", "if (be != 0.0) r = r + be * decode_c(c_dtype, C, i * ldc + j);\n            acc[j] = r;",
      "r = r + be * decode_c(c_dtype, C, i * ldc + j);\n            acc[j] = r;"),
 ]
