@@ -106,6 +106,10 @@ class Oracle:
         lib.oracle_conv2d.restype = ctypes.c_int
         lib.oracle_conv2d.argtypes = [i64] * 13 + [ctypes.c_float, vp, vp, ctypes.c_float, vp,
                                                     ctypes.c_int, ctypes.c_int, dp, dp, ctypes.c_int]
+        lib.oracle_conv2d_sampled.restype = ctypes.c_int
+        lib.oracle_conv2d_sampled.argtypes = [i64] * 13 + [ctypes.c_float, vp, vp, ctypes.c_float,
+                                                            vp, ctypes.c_int, ctypes.c_int, i64, vp,
+                                                            dp, dp, ctypes.c_int]
         lib.oracle_softmax.restype = ctypes.c_int
         lib.oracle_softmax.argtypes = [i64, i64, vp, i64, ctypes.c_int, vp, i64, dp, ctypes.c_int]
         self.lib = lib
@@ -276,8 +280,26 @@ def _oracle_conv_methods():
             raise ValueError(f"oracle_conv2d failed ({st})")
         return Rr, Sr
 
+    def conv2d_sampled(self, N, H, W, C, K, R, S, pad_h, pad_w, stride_h, stride_w, dil_h, dil_w,
+                       alpha, X, Wt, beta, Yin, x_dtype, y_dtype, rows, nthreads: int = 0):
+        """The convolution at the output pixels `rows` (indices into N*P*Q):
+        (R, S) of shape (len(rows), K)."""
+        X, Wt, Yin = _prep(X), _prep(Wt), _prep(Yin, c=True)
+        rows = np.ascontiguousarray(rows, dtype=np.int64)
+        Rr = np.empty((rows.size, K), dtype=np.float64)
+        Sr = np.empty((rows.size, K), dtype=np.float64)
+        st = self.lib.oracle_conv2d_sampled(N, H, W, C, K, R, S, pad_h, pad_w, stride_h, stride_w,
+                                            dil_h, dil_w, float(alpha), _ptr(X), _ptr(Wt),
+                                            float(beta), _ptr(Yin), x_dtype, y_dtype, rows.size,
+                                            rows.ctypes.data, Rr.ctypes.data, Sr.ctypes.data,
+                                            nthreads)
+        if st != 0:
+            raise ValueError(f"oracle_conv2d_sampled failed ({st})")
+        return Rr, Sr
+
     Oracle.conv2d_dims = conv2d_dims
     Oracle.conv2d = conv2d
+    Oracle.conv2d_sampled = conv2d_sampled
 
 
 _oracle_conv_methods()

@@ -518,6 +518,66 @@ int oracle_conv2d_dims(int64_t H, int64_t W, int64_t R, int64_t S, int64_t pad_h
     return OR_OK;
 }
 
+/* The definition at selected output pixels: rows[t] (0 <= rows[t] < N*P*Q)
+ * gives row t of R and S (all K channels); nrows of them. */
+static void conv2d_row(int64_t m, int64_t H, int64_t W, int64_t C, int64_t K, int64_t R,
+                       int64_t S, int64_t P, int64_t Q, int64_t pad_h, int64_t pad_w,
+                       int64_t stride_h, int64_t stride_w, int64_t dil_h, int64_t dil_w,
+                       double al, const void* X, const void* Wt, double be, const void* Yin,
+                       int x_dtype, int y_dtype, double* Rrow, double* Srow) {
+    const int64_t n = m / (P * Q), p = (m / Q) % P, q = m % Q;
+    for (int64_t k = 0; k < K; ++k) {
+        double acc = 0.0, sabs = 0.0;
+        for (int64_t r = 0; r < R; ++r) {
+            const int64_t h = p * stride_h - pad_h + r * dil_h;
+            if (h < 0 || h >= H) continue;
+            for (int64_t s = 0; s < S; ++s) {
+                const int64_t w = q * stride_w - pad_w + s * dil_w;
+                if (w < 0 || w >= W) continue;
+                for (int64_t c = 0; c < C; ++c) {
+                    const double a = decode_in(x_dtype, X, ((n * H + h) * W + w) * C + c);
+                    const double b = decode_in(x_dtype, Wt, ((k * R + r) * S + s) * C + c);
+                    const double prod = a * b;
+                    acc = acc + prod;
+                    sabs = sabs + fabs(prod);
+                }
+            }
+        }
+        double y = al * acc;
+        if (be != 0.0) y = y + be * decode_c(y_dtype, Yin, m * K + k);
+        Rrow[k] = y;
+        Srow[k] = sabs;
+    }
+}
+
+int oracle_conv2d_sampled(int64_t N, int64_t H, int64_t W, int64_t C, int64_t K, int64_t R,
+                          int64_t S, int64_t pad_h, int64_t pad_w, int64_t stride_h,
+                          int64_t stride_w, int64_t dil_h, int64_t dil_w, float alpha,
+                          const void* X, const void* Wt, float beta, const void* Yin,
+                          int x_dtype, int y_dtype, int64_t nrows, const int64_t* rows,
+                          double* Rout, double* Sout, int nthreads) {
+    int64_t P, Q;
+    if (N < 0 || C < 1 || K < 1 || nrows < 0) return OR_BAD_ARG;
+    if (oracle_conv2d_dims(H, W, R, S, pad_h, pad_w, stride_h, stride_w, dil_h, dil_w, &P, &Q))
+        return OR_BAD_ARG;
+    if (x_dtype != OR_F16 && x_dtype != OR_BF16) return OR_BAD_ARG;
+    if (y_dtype != OR_F16 && y_dtype != OR_BF16 && y_dtype != OR_F32) return OR_BAD_ARG;
+    if (nrows == 0) return OR_OK;
+    if (X == NULL || Wt == NULL || rows == NULL || Rout == NULL || Sout == NULL) return OR_BAD_ARG;
+    if (beta != 0.0f && Yin == NULL) return OR_BAD_ARG;
+    for (int64_t t = 0; t < nrows; ++t)
+        if (rows[t] < 0 || rows[t] >= N * P * Q) return OR_BAD_ARG;
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#pragma omp parallel for schedule(dynamic, 8)
+#endif
+    for (int64_t t = 0; t < nrows; ++t)
+        conv2d_row(rows[t], H, W, C, K, R, S, P, Q, pad_h, pad_w, stride_h, stride_w, dil_h, dil_w,
+                   (double)alpha, X, Wt, (double)beta, Yin, x_dtype, y_dtype, Rout + t * K,
+                   Sout + t * K);
+    return OR_OK;
+}
+
 int oracle_conv2d(int64_t N, int64_t H, int64_t W, int64_t C, int64_t K, int64_t R, int64_t S,
                   int64_t pad_h, int64_t pad_w, int64_t stride_h, int64_t stride_w,
                   int64_t dil_h, int64_t dil_w, float alpha, const void* X, const void* Wt,
@@ -533,35 +593,13 @@ int oracle_conv2d(int64_t N, int64_t H, int64_t W, int64_t C, int64_t K, int64_t
     if (M == 0) return OR_OK;
     if (X == NULL || Wt == NULL || Rout == NULL || Sout == NULL) return OR_BAD_ARG;
     if (beta != 0.0f && Yin == NULL) return OR_BAD_ARG;
-    const double al = (double)alpha, be = (double)beta;
 #ifdef _OPENMP
     if (nthreads > 0) omp_set_num_threads(nthreads);
 #pragma omp parallel for schedule(dynamic, 8)
 #endif
-    for (int64_t m = 0; m < M; ++m) {
-        const int64_t n = m / (P * Q), p = (m / Q) % P, q = m % Q;
-        for (int64_t k = 0; k < K; ++k) {
-            double acc = 0.0, sabs = 0.0;
-            for (int64_t r = 0; r < R; ++r) {
-                const int64_t h = p * stride_h - pad_h + r * dil_h;
-                if (h < 0 || h >= H) continue;
-                for (int64_t s = 0; s < S; ++s) {
-                    const int64_t w = q * stride_w - pad_w + s * dil_w;
-                    if (w < 0 || w >= W) continue;
-                    for (int64_t c = 0; c < C; ++c) {
-                        const double a = decode_in(x_dtype, X, ((n * H + h) * W + w) * C + c);
-                        const double b = decode_in(x_dtype, Wt, ((k * R + r) * S + s) * C + c);
-                        const double prod = a * b;
-                        acc = acc + prod;
-                        sabs = sabs + fabs(prod);
-                    }
-                }
-            }
-            double y = al * acc;
-            if (be != 0.0) y = y + be * decode_c(y_dtype, Yin, m * K + k);
-            Rout[m * K + k] = y;
-            Sout[m * K + k] = sabs;
-        }
-    }
+    for (int64_t m = 0; m < M; ++m)
+        conv2d_row(m, H, W, C, K, R, S, P, Q, pad_h, pad_w, stride_h, stride_w, dil_h, dil_w,
+                   (double)alpha, X, Wt, (double)beta, Yin, x_dtype, y_dtype, Rout + m * K,
+                   Sout + m * K);
     return OR_OK;
 }

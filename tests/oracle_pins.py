@@ -730,6 +730,16 @@ def pin_conv_closed_forms(o):
             taps = sum(1 for r in range(R) for s_ in range(S)
                        if 0 <= p_ * sh - ph + r * dh < H and 0 <= q * sw - pw + s_ * dw < W)
             assert (Rr[p_ * Q + q] == C * taps).all()
+    # the sampled entry point agrees with the full one, row by row
+    N, H, W, C, K, R, S, ph, pw, sh, sw, dh, dw = CONV_SHAPES[1]
+    xc, wc, _, _ = _conv_case(rng, N, H, W, C, K, R, S, F16)
+    P, Q = o.conv2d_dims(H, W, R, S, ph, pw, sh, sw, dh, dw)
+    yin = rng.standard_normal((N * P * Q, K)).astype(np.float32)
+    Rf, Sf = o.conv2d(N, H, W, C, K, R, S, ph, pw, sh, sw, dh, dw, 0.5, xc, wc, 2.0, yin, F16, F32)
+    ids = np.array([N * P * Q - 1, 0, 3, 3])
+    Rs, Ss = o.conv2d_sampled(N, H, W, C, K, R, S, ph, pw, sh, sw, dh, dw, 0.5, xc, wc, 2.0, yin,
+                              F16, F32, ids)
+    assert (Rs == Rf[ids]).all() and (Ss == Sf[ids]).all()
     # argument checks and empty outputs
     assert o.conv2d_dims(3, 3, 5, 1, 0, 0, 1, 1, 1, 1) == (0, 3)
     for bad in [dict(C=0), dict(st=0), dict(dil=0), dict(pad=-1), dict(dt=F32)]:
