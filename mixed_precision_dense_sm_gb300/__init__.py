@@ -11,7 +11,9 @@ The entry points mirror include/gemm_sm103.h one to one:
 ``gemm_status_string``, ``gemm_check_args``, ``gemm_plan_query``,
 ``gemm_run_ex`` (fused bias/activation epilogue), ``gemm_debug_set`` and
 ``gemm_run_noalloc``; and include/softmax_sm103.h: ``softmax_rows``,
-``softmax_plan_query``, ``softmax_sync``, ``softmax_debug_set``.
+``softmax_plan_query``, ``softmax_sync``, ``softmax_debug_set``; and
+include/conv_sm103.h: ``conv2d_fprop``, ``conv2d_plan_query``,
+``conv2d_output_dims``.
 ``Gemm`` wraps a handle and adds ``__call__`` for torch tensors; ``softmax``
 does the same for the row softmax.
 """
@@ -23,7 +25,8 @@ import os
 HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libgemm_sm103.so")
 HEADER = os.path.join(os.path.dirname(HERE), "include", "gemm_sm103.h")
-HEADERS = [HEADER, os.path.join(os.path.dirname(HERE), "include", "softmax_sm103.h")]
+HEADERS = [HEADER, os.path.join(os.path.dirname(HERE), "include", "softmax_sm103.h"),
+           os.path.join(os.path.dirname(HERE), "include", "conv_sm103.h")]
 
 GEMM_F16, GEMM_BF16, GEMM_F32 = 0, 1, 2
 STATUS = {0: "GEMM_OK", 1: "GEMM_ERR_INVALID_VALUE", 2: "GEMM_ERR_NOT_SUPPORTED",
@@ -115,6 +118,15 @@ def _load():
     lib.softmax_rows.argtypes = smx_args + [vp]
     lib.softmax_plan_query.restype = ctypes.c_int
     lib.softmax_plan_query.argtypes = smx_args + [i32, i32, ctypes.POINTER(SoftmaxPlan)]
+    conv_geo = [i64] * 13
+    lib.conv2d_output_dims.restype = ctypes.c_int
+    lib.conv2d_output_dims.argtypes = [i64] * 10 + [ctypes.POINTER(i64)] * 2
+    lib.conv2d_fprop.restype = ctypes.c_int
+    lib.conv2d_fprop.argtypes = [vp] + conv_geo + [ctypes.c_float, vp, vp, ctypes.c_float, vp,
+                                                   Dtypes, ctypes.POINTER(Epilogue), vp]
+    lib.conv2d_plan_query.restype = ctypes.c_int
+    lib.conv2d_plan_query.argtypes = conv_geo + [ctypes.c_float, vp, vp, ctypes.c_float, vp,
+                                                 Dtypes, i32, i32, ctypes.POINTER(Plan)]
     lib.softmax_sync.restype = ctypes.c_int
     lib.softmax_sync.argtypes = [vp]
     lib.softmax_debug_set.restype = ctypes.c_int
@@ -205,7 +217,7 @@ def declared_symbols():
     names = set()
     for h in HEADERS:
         text = open(h).read()
-        names |= set(re.findall(r"^\s*(?:gemm_status_t|const char\*)\s+((?:gemm|softmax)_\w+)\s*\(",
+        names |= set(re.findall(r"^\s*(?:gemm_status_t|const char\*)\s+((?:gemm|softmax|conv2d)_\w+)\s*\(",
                                 text, flags=re.M))
     return sorted(names)
 
@@ -218,6 +230,37 @@ def softmax_rows(rows, cols, X, ldx, x_dtype, Y, ldy, y_dtype, stream=0) -> int:
 
 
 SOFTMAX_DEBUG_SKIP_FIRST_LOAD = 1
+
+
+def conv2d_output_dims(H, W, R, S, pad=(0, 0), stride=(1, 1), dilation=(1, 1)):
+    """(P, Q) of a forward convolution (raises on bad geometry)."""
+    P, Q = ctypes.c_int64(), ctypes.c_int64()
+    st = lib.conv2d_output_dims(H, W, R, S, pad[0], pad[1], stride[0], stride[1], dilation[0],
+                                dilation[1], ctypes.byref(P), ctypes.byref(Q))
+    if st != 0:
+        raise GemmError(st, "conv2d_output_dims")
+    return P.value, Q.value
+
+
+def conv2d_fprop(h, N, H, W, C, K, R, S, pad, stride, dilation, alpha, X, Wt, beta, Y, dtypes,
+                 bias=0, bias_dtype=GEMM_F32, act=ACT_NONE, stream=0) -> int:
+    """Raw C-ABI call (include/conv_sm103.h): X (NHWC), Wt (KRSC), Y (NPQK)
+    device addresses; pad/stride/dilation (h, w) pairs; dtypes (x, w, y).
+    Returns the gemm_status_t code."""
+    ep = Epilogue(bias or None, bias_dtype, act)
+    return lib.conv2d_fprop(h, N, H, W, C, K, R, S, pad[0], pad[1], stride[0], stride[1],
+                            dilation[0], dilation[1], float(alpha), X, Wt, float(beta), Y,
+                            Dtypes(*dtypes), ctypes.byref(ep), stream)
+
+
+def conv2d_plan_query(N, H, W, C, K, R, S, pad, stride, dilation, alpha, X, Wt, beta, Y, dtypes,
+                      num_sms=152, smem_optin=232448):
+    """(status, GEMM plan dict) conv2d_fprop would use (host logic only)."""
+    plan = Plan()
+    st = lib.conv2d_plan_query(N, H, W, C, K, R, S, pad[0], pad[1], stride[0], stride[1],
+                               dilation[0], dilation[1], float(alpha), X, Wt, float(beta), Y,
+                               Dtypes(*dtypes), num_sms, smem_optin, ctypes.byref(plan))
+    return st, (plan.as_dict() if st == 0 else None)
 
 
 def softmax_sync(stream=0) -> int:

@@ -18,6 +18,7 @@
 #include <cuda_runtime.h>
 
 #include "gemm_sm103.h"
+#include "conv_sm103.h"
 #include "aux_kernels.cuh"
 #include "launch.h"
 
@@ -98,7 +99,7 @@ gemm_status_t check_args(char transA, char transB, int64_t M, int64_t N, int64_t
 gemm_status_t make_plan(char transA, char transB, int64_t M, int64_t N, int64_t K, float alpha,
                         const void* A, int64_t lda, const void* B, int64_t ldb, float beta,
                         const void* C, int64_t ldc, gemm_dtypes_t dt, int32_t num_sms,
-                        int32_t smem_optin, Plan& pl) {
+                        int32_t smem_optin, Plan& pl, bool allow_swap = true) {
     gemm_status_t st = check_args(transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, dt);
     if (st != GEMM_OK) return st;
     if (num_sms < 1 || smem_optin < 64 * 1024) return GEMM_ERR_INVALID_VALUE;
@@ -129,7 +130,7 @@ gemm_status_t make_plan(char transA, char transB, int64_t M, int64_t N, int64_t 
 
     // Skinny M: compute C^T = op(B)^T op(A)^T so the large N fills the
     // 128-row MMA side and the small M becomes the MMA's N.
-    const bool swap = (M <= 64 && N >= 128);
+    const bool swap = allow_swap && (M <= 64 && N >= 128);
     pl.pub.swap_ab = swap ? 1 : 0;
     if (swap) {
         pl.a = opB;
@@ -255,6 +256,21 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+typedef CUresult (*EncodeIm2colFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const int*, const int*,
+                                   cuuint32_t, cuuint32_t, const cuuint32_t*,
+                                   CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// A forward 2-D convolution seen as a GEMM (M = N*P*Q output pixels, N = K
+// output channels, the reduction over filter taps x channels).
+struct ConvDesc {
+    int64_t N, H, W, C, K, R, S, P, Q;
+    int64_t pad_h, pad_w, stride_h, stride_w, dil_h, dil_w;
+    const void* X;
+    const void* Wt;
+    EncodeIm2colFn encode_im2col;
+};
 
 }  // namespace
 
@@ -269,6 +285,7 @@ struct gemm_ctx {
     void* ws;             // device workspace
     size_t ws_bytes;
     EncodeTiledFn encode;
+    EncodeIm2colFn encode_im2col;
 };
 
 namespace {
@@ -291,6 +308,54 @@ bool encode_operand(EncodeTiledFn encode, CUtensorMap* map, int32_t dtype, const
                            2, const_cast<void*>(ptr), dims, strides, box, estr,
                            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+// The input X (N, H, W, C) as an im2col map: windows traversed W, H, N with
+// the convolution's stride, 64 channels x 128 windows per load, 128-byte
+// swizzle, zeros outside the image.  The box corners make the traversal
+// visit exactly the windows of the output (P x Q per image).
+bool encode_conv_input(const ConvDesc& cd, CUtensorMap* map, int32_t dtype) {
+    const int64_t es = 2;
+    const cuuint64_t dims[4] = {static_cast<cuuint64_t>(cd.C), static_cast<cuuint64_t>(cd.W),
+                                static_cast<cuuint64_t>(cd.H), static_cast<cuuint64_t>(cd.N)};
+    const cuuint64_t strides[3] = {static_cast<cuuint64_t>(cd.C * es),
+                                   static_cast<cuuint64_t>(cd.W * cd.C * es),
+                                   static_cast<cuuint64_t>(cd.H * cd.W * cd.C * es)};
+    const int lower[2] = {static_cast<int>(-cd.pad_w), static_cast<int>(-cd.pad_h)};
+    const int upper[2] = {static_cast<int>(cd.pad_w - (cd.S - 1) * cd.dil_w),
+                          static_cast<int>(cd.pad_h - (cd.R - 1) * cd.dil_h)};
+    const cuuint32_t estr[4] = {1, static_cast<cuuint32_t>(cd.stride_w),
+                                static_cast<cuuint32_t>(cd.stride_h), 1};
+    CUresult r = cd.encode_im2col(map,
+                                  dtype == GEMM_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                     : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                                  4, const_cast<void*>(cd.X), dims, strides, lower, upper,
+                                  64u /* channels per 128-byte row */, kBlockM, estr,
+                                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+// The filter (K, R, S, C) as a 3-D map (C, R*S, K): a box is 64 channels of
+// one tap for box_rows output channels; channels past C read zeros.
+bool encode_conv_filter(EncodeTiledFn encode, const ConvDesc& cd, CUtensorMap* map,
+                        int32_t dtype, uint32_t box_rows) {
+    const int64_t es = 2;
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(cd.C),
+                                static_cast<cuuint64_t>(cd.R * cd.S),
+                                static_cast<cuuint64_t>(cd.K)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(cd.C * es),
+                                   static_cast<cuuint64_t>(cd.R * cd.S * cd.C * es)};
+    const cuuint32_t box[3] = {64, 1, box_rows};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = encode(map,
+                        dtype == GEMM_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                           : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                        3, const_cast<void*>(cd.Wt), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
 
@@ -349,7 +414,8 @@ int grid_for(int64_t elems_per_thread_unit, int num_sms) {
 gemm_status_t enqueue_plan(const Plan& pl, EncodeTiledFn encode, int num_sms, uint8_t* ws,
                            int* err_dev, float alpha, float beta, void* C, gemm_dtypes_t dt,
                            cudaStream_t stream, bool clear_counters, uint32_t debug_flags = 0,
-                           uint64_t wait_limit_ns = 0, const gemm_epilogue_t* ep = nullptr) {
+                           uint64_t wait_limit_ns = 0, const gemm_epilogue_t* ep = nullptr,
+                           const ConvDesc* conv = nullptr) {
     // kind::tf32 reads K-major operands only; the planner transposes the rest.
     if (pl.esize == 4 && (pl.a.mn_major || pl.b.mn_major)) return GEMM_ERR_NOT_SUPPORTED;
     int* counters = reinterpret_cast<int*>(ws);
@@ -402,10 +468,17 @@ gemm_status_t enqueue_plan(const Plan& pl, EncodeTiledFn encode, int num_sms, ui
     const int cg = pl.cta_group;
     // MN-major boxes are one 128-byte row of M/N by block_k rows of K.
     const uint32_t mn_box = 128u / static_cast<uint32_t>(pl.esize);
-    bool ok = encode_operand(encode, &l.tmA, dt.a, a_ptr, pl.a.cols, pl.a.rows, pl.a.packed_ld,
-                             pl.a.mn_major ? mn_box : static_cast<uint32_t>(kBlockM));
-    ok = ok && encode_operand(encode, &l.tmB, dt.b, b_ptr, pl.b.cols, pl.b.rows, pl.b.packed_ld,
-                              pl.b.mn_major ? mn_box : static_cast<uint32_t>(bn / cg));
+    bool ok;
+    if (conv != nullptr) {
+        ok = encode_conv_input(*conv, &l.tmA, dt.a) &&
+             encode_conv_filter(encode, *conv, &l.tmB, dt.b, static_cast<uint32_t>(bn / cg));
+    } else {
+        ok = encode_operand(encode, &l.tmA, dt.a, a_ptr, pl.a.cols, pl.a.rows, pl.a.packed_ld,
+                            pl.a.mn_major ? mn_box : static_cast<uint32_t>(kBlockM));
+        ok = ok && encode_operand(encode, &l.tmB, dt.b, b_ptr, pl.b.cols, pl.b.rows,
+                                  pl.b.packed_ld,
+                                  pl.b.mn_major ? mn_box : static_cast<uint32_t>(bn / cg));
+    }
     if (!ok) return GEMM_ERR_LAUNCH;
 
     TcParams& p = l.p;
@@ -446,6 +519,19 @@ gemm_status_t enqueue_plan(const Plan& pl, EncodeTiledFn encode, int num_sms, ui
     p.bias_dtype = (ep && ep->bias) ? ep->bias_dtype : GEMM_F32;
     p.bias_on_rows = pl.pub.swap_ab ? 1 : 0;      // swapped: C columns are D' rows
     p.act = ep ? ep->activation : GEMM_ACT_NONE;
+    if (conv != nullptr) {
+        p.conv = 1;
+        p.conv_cblocks = static_cast<int32_t>(ceil_div(conv->C, 64));
+        p.conv_S = static_cast<int32_t>(conv->S);
+        p.conv_P = static_cast<int32_t>(conv->P);
+        p.conv_Q = static_cast<int32_t>(conv->Q);
+        p.conv_stride_h = static_cast<int32_t>(conv->stride_h);
+        p.conv_stride_w = static_cast<int32_t>(conv->stride_w);
+        p.conv_pad_h = static_cast<int32_t>(conv->pad_h);
+        p.conv_pad_w = static_cast<int32_t>(conv->pad_w);
+        p.conv_dil_h = static_cast<int32_t>(conv->dil_h);
+        p.conv_dil_w = static_cast<int32_t>(conv->dil_w);
+    }
     l.grid = pl.pub.grid;
     l.cta_group = cg;
     l.block_n = bn;
@@ -487,6 +573,50 @@ gemm_status_t enqueue_scale(int64_t M, int64_t N, void* C, int64_t ldc, float be
         scale_c_kernel<__nv_bfloat16><<<grid, 256, 0, stream>>>(
             static_cast<__nv_bfloat16*>(C), M, N, ldc, beta, bias, bdt, act);
     return cudaGetLastError() == cudaSuccess ? GEMM_OK : GEMM_ERR_LAUNCH;
+}
+
+int64_t conv_dim(int64_t in, int64_t pad, int64_t dil, int64_t f, int64_t stride) {
+    const int64_t span = in + 2 * pad - dil * (f - 1) - 1;
+    return span < 0 ? 0 : span / stride + 1;
+}
+
+// Checks a convolution and fills its descriptor; then the GEMM plan of
+// M = N*P*Q by K with R*S*ceil(C/64) k-blocks (both operands K-major, never
+// swapped: the im2col load fills the MMA's 128-row side).
+gemm_status_t conv_plan(int64_t N, int64_t H, int64_t W, int64_t C, int64_t K, int64_t R,
+                        int64_t S, int64_t pad_h, int64_t pad_w, int64_t stride_h,
+                        int64_t stride_w, int64_t dil_h, int64_t dil_w, float alpha,
+                        const void* X, const void* Wt, float beta, const void* Y,
+                        gemm_dtypes_t dt, int32_t num_sms, int32_t smem_optin, ConvDesc& cd,
+                        Plan& pl) {
+    if (N < 0 || H < 1 || W < 1 || C < 1 || K < 1 || R < 1 || S < 1) return GEMM_ERR_INVALID_VALUE;
+    if (pad_h < 0 || pad_w < 0 || stride_h < 1 || stride_w < 1 || dil_h < 1 || dil_w < 1)
+        return GEMM_ERR_INVALID_VALUE;
+    if (dt.a != dt.b || (dt.a != GEMM_F16 && dt.a != GEMM_BF16)) return GEMM_ERR_INVALID_VALUE;
+    if (dt.c != GEMM_F32 && dt.c != GEMM_F16 && dt.c != GEMM_BF16) return GEMM_ERR_INVALID_VALUE;
+    if (N > INT32_MAX || H > INT32_MAX || W > INT32_MAX || C > INT32_MAX || K > INT32_MAX ||
+        R > 65535 || S > 65535 || dil_h > 65535 || dil_w > 65535)
+        return GEMM_ERR_INVALID_VALUE;
+    const int64_t P = conv_dim(H, pad_h, dil_h, R, stride_h);
+    const int64_t Q = conv_dim(W, pad_w, dil_w, S, stride_w);
+    const int64_t M = N * P * Q;
+    if (M > INT32_MAX) return GEMM_ERR_INVALID_VALUE;
+    // limits of the im2col load: 16-byte pixel rows, traversal strides up to
+    // 8, window corners in [-128, 127], 16-bit tap offsets
+    const int64_t up_w = pad_w - (S - 1) * dil_w, up_h = pad_h - (R - 1) * dil_h;
+    if (C % 8 != 0 || stride_h > 8 || stride_w > 8 || pad_h > 128 || pad_w > 128 ||
+        up_w < -128 || up_w > 127 || up_h < -128 || up_h > 127 ||
+        (R - 1) * dil_h > 65535 || (S - 1) * dil_w > 65535)
+        return GEMM_ERR_NOT_SUPPORTED;
+    cd = ConvDesc{N, H, W, C, K, R, S, P, Q, pad_h, pad_w, stride_h, stride_w, dil_h, dil_w,
+                  X, Wt, nullptr};
+    if (M > 0 && alpha != 0.0f && (!aligned16(X) || !aligned16(Wt))) {
+        if (X == nullptr || Wt == nullptr) return GEMM_ERR_INVALID_VALUE;
+        return GEMM_ERR_NOT_SUPPORTED;
+    }
+    const int64_t kfake = R * S * ceil_div(C, 64) * 64;
+    return make_plan('N', 'T', M, K, kfake, alpha, X, kfake, Wt, kfake, beta, Y, K, dt, num_sms,
+                     smem_optin, pl, false);
 }
 
 bool epilogue_ok(const gemm_epilogue_t* ep) {
@@ -566,6 +696,15 @@ gemm_status_t gemm_create(gemm_handle_t* out) {
     h->num_sms = sms;
     h->smem_optin = smem;
     h->encode = reinterpret_cast<EncodeTiledFn>(fn);
+    void* fn2 = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeIm2col", &fn2, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || fn2 == nullptr) {
+        cudaGetLastError();
+        delete h;
+        return GEMM_ERR_LAUNCH;
+    }
+    h->encode_im2col = reinterpret_cast<EncodeIm2colFn>(fn2);
     if (cudaHostAlloc(reinterpret_cast<void**>(&h->err_host), 64, cudaHostAllocMapped) !=
             cudaSuccess ||
         cudaHostGetDevicePointer(reinterpret_cast<void**>(&h->err_dev), h->err_host, 0) !=
@@ -739,3 +878,59 @@ extern "C" gemm_status_t gemm_run_noalloc(char transA, char transB, int64_t M, i
     return enqueue_plan(pl, d.encode, d.num_sms, static_cast<uint8_t*>(d.scratch), nullptr, alpha,
                         beta, C, dt, stream, true);
 }
+
+extern "C" {
+
+gemm_status_t conv2d_output_dims(int64_t H, int64_t W, int64_t R, int64_t S, int64_t pad_h,
+                                 int64_t pad_w, int64_t stride_h, int64_t stride_w, int64_t dil_h,
+                                 int64_t dil_w, int64_t* P, int64_t* Q) {
+    if (P == nullptr || Q == nullptr || H < 1 || W < 1 || R < 1 || S < 1 || pad_h < 0 ||
+        pad_w < 0 || stride_h < 1 || stride_w < 1 || dil_h < 1 || dil_w < 1)
+        return GEMM_ERR_INVALID_VALUE;
+    *P = conv_dim(H, pad_h, dil_h, R, stride_h);
+    *Q = conv_dim(W, pad_w, dil_w, S, stride_w);
+    return GEMM_OK;
+}
+
+gemm_status_t conv2d_plan_query(int64_t N, int64_t H, int64_t W, int64_t C, int64_t K, int64_t R,
+                                int64_t S, int64_t pad_h, int64_t pad_w, int64_t stride_h,
+                                int64_t stride_w, int64_t dil_h, int64_t dil_w, float alpha,
+                                const void* X, const void* Wt, float beta, const void* Y,
+                                gemm_dtypes_t dt, int32_t num_sms, int32_t smem_optin,
+                                gemm_plan_t* out) {
+    if (out == nullptr) return GEMM_ERR_INVALID_VALUE;
+    if (num_sms < 1 || smem_optin < 64 * 1024) return GEMM_ERR_INVALID_VALUE;
+    ConvDesc cd;
+    Plan pl;
+    gemm_status_t st = conv_plan(N, H, W, C, K, R, S, pad_h, pad_w, stride_h, stride_w, dil_h,
+                                 dil_w, alpha, X, Wt, beta, Y, dt, num_sms, smem_optin, cd, pl);
+    if (st == GEMM_OK) *out = pl.pub;
+    return st;
+}
+
+gemm_status_t conv2d_fprop(gemm_handle_t h, int64_t N, int64_t H, int64_t W, int64_t C,
+                           int64_t K, int64_t R, int64_t S, int64_t pad_h, int64_t pad_w,
+                           int64_t stride_h, int64_t stride_w, int64_t dil_h, int64_t dil_w,
+                           float alpha, const void* X, const void* Wt, float beta, void* Y,
+                           gemm_dtypes_t dt, const gemm_epilogue_t* ep, gemm_stream_t stream_) {
+    if (h == nullptr) return GEMM_ERR_INVALID_VALUE;
+    gemm_status_t st = take_device_error(h);
+    if (st != GEMM_OK) return st;
+    if (!epilogue_ok(ep)) return GEMM_ERR_INVALID_VALUE;
+    ConvDesc cd;
+    Plan pl;
+    st = conv_plan(N, H, W, C, K, R, S, pad_h, pad_w, stride_h, stride_w, dil_h, dil_w, alpha, X,
+                   Wt, beta, Y, dt, h->num_sms, h->smem_optin, cd, pl);
+    if (st != GEMM_OK) return st;
+    cd.encode_im2col = h->encode_im2col;
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    if (pl.pub.path == GEMM_PATH_NOOP) return GEMM_OK;
+    if (pl.pub.path == GEMM_PATH_SCALE)
+        return enqueue_scale(cd.N * cd.P * cd.Q, K, Y, K, beta, dt, h->num_sms, stream, ep);
+    st = ensure_workspace(h, static_cast<size_t>(pl.pub.workspace_bytes));
+    if (st != GEMM_OK) return st;
+    return enqueue_plan(pl, h->encode, h->num_sms, static_cast<uint8_t*>(h->ws), h->err_dev, alpha,
+                        beta, Y, dt, stream, false, h->debug_flags, h->wait_limit_ns, ep, &cd);
+}
+
+}  // extern "C"

@@ -101,6 +101,15 @@ struct TcParams {
     int32_t bias_dtype;         // 0 F16, 1 BF16, 2 F32
     int32_t bias_on_rows;       // 1: bias indexed by D' row (swapped problem), 0: by column
     int32_t act;                // 0 none, 1 ReLU, 2 GELU (erf), 3 SiLU
+    // implicit-GEMM convolution (conv != 0): A is an im2col map over the
+    // NHWC input, B a 3-D map (C, R*S, K) over the KRSC filter; k-block kb is
+    // filter tap kb / conv_cblocks with channels from (kb % conv_cblocks) * 64
+    // (16-bit inputs), D row m the output pixel (n, p, q) of m = (n*P + p)*Q + q
+    int32_t conv;
+    int32_t conv_cblocks;       // ceil(C / 64)
+    int32_t conv_S;             // filter width
+    int32_t conv_P, conv_Q;     // output height and width
+    int32_t conv_stride_h, conv_stride_w, conv_pad_h, conv_pad_w, conv_dil_h, conv_dil_w;
 };
 
 // Test hook: CTA 0's producer arms its first pipeline slot but issues no load
@@ -526,6 +535,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // transaction count may go transiently negative).
                 const uint32_t bytes = (CG == 1) ? tile_bytes(0)
                                                  : (rank == 0 ? tile_bytes(0) + tile_bytes(1) : 0u);
+                // convolution: the first window of this CTA's rows (output
+                // pixel m0) as the input coordinates of its top-left pixel
+                int32_t cn = 0, ch = 0, cw = 0;
+                if (p.conv) {
+                    const int32_t pq = p.conv_P * p.conv_Q;
+                    cn = m0 / pq;
+                    const int32_t rem = m0 - cn * pq;
+                    const int32_t pp = rem / p.conv_Q;
+                    ch = pp * p.conv_stride_h - p.conv_pad_h;
+                    cw = (rem - pp * p.conv_Q) * p.conv_stride_w - p.conv_pad_w;
+                }
                 for (int32_t kb = sg.kb0; kb < sg.kb1; ++kb) {
                     if (!wait_or_abort(&empty[stage], phase ^ 1u, &abort_flag, p.wait_limit_ns)) {
                         record_error(p, kErrTimeoutProducer, &abort_flag);
@@ -545,7 +565,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                         continue;
                     }
-                    if constexpr (CG == 1) {
+                    if (p.conv) {
+                        // filter tap (r, s), channels c0 .. c0 + 63
+                        const int32_t tap = kb / p.conv_cblocks;
+                        const int32_t c0 = (kb - tap * p.conv_cblocks) * kBlockK;
+                        const int32_t r = tap / p.conv_S;
+                        const uint16_t ow = static_cast<uint16_t>((tap - r * p.conv_S) * p.conv_dil_w);
+                        const uint16_t oh = static_cast<uint16_t>(r * p.conv_dil_h);
+                        if constexpr (CG == 1) {
+                            mbar_arrive_expect_tx(&full[stage], bytes);
+                            if (na) tma_load_im2col_4d(sa, &tmA, &full[stage], c0, cw, ch, cn, ow, oh, pol_a);
+                            if (nb) tma_load_3d(sb, &tmB, &full[stage], c0, tap, n0, pol_b);
+                        } else {
+                            const uint32_t fb = map_to_rank(smem_addr(&full[stage]), 0);
+                            if (rank == 0) mbar_arrive_expect_tx(&full[stage], bytes);
+                            if (na) tma_load_im2col_4d_pair(sa, &tmA, fb, c0, cw, ch, cn, ow, oh, pol_a);
+                            if (nb) tma_load_3d_pair(sb, &tmB, fb, c0, tap, n0, pol_b);
+                        }
+                    } else if constexpr (CG == 1) {
                         mbar_arrive_expect_tx(&full[stage], bytes);
                         if (p.a_mn_major) {
                             for (int c = 0; c < na; ++c)

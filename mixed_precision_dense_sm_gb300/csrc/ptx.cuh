@@ -95,6 +95,36 @@ __device__ __forceinline__ void tma_load_2d(void* smem_dst, const CUtensorMap* m
         : "memory");
 }
 
+// 3-D tiled load of one box at coordinates (c0 innermost, c1, c2).
+__device__ __forceinline__ void tma_load_3d(void* smem_dst, const CUtensorMap* map, uint64_t* bar,
+                                            int32_t c0, int32_t c1, int32_t c2,
+                                            uint64_t cache_policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_addr(smem_dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_addr(bar)),
+        "l"(cache_policy)
+        : "memory");
+}
+
+// im2col load from a 4-D (C, W, H, N) map: `pixelsPerColumn` consecutive
+// convolution windows starting at the window whose top-left input pixel is
+// (w, h) of image n, each contributing channels c .. c + channelsPerPixel - 1
+// of the input pixel at offset (ow, oh) inside the window; positions outside
+// the image read zeros.
+__device__ __forceinline__ void tma_load_im2col_4d(void* smem_dst, const CUtensorMap* map,
+                                                   uint64_t* bar, int32_t c, int32_t w, int32_t h,
+                                                   int32_t n, uint16_t ow, uint16_t oh,
+                                                   uint64_t cache_policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.im2col.mbarrier::complete_tx::bytes"
+        ".L2::cache_hint [%0], [%1, {%2, %3, %4, %5}], [%6], {%7, %8}, %9;" ::"r"(
+            smem_addr(smem_dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c), "r"(w), "r"(h), "r"(n), "r"(smem_addr(bar)),
+        "h"(ow), "h"(oh), "l"(cache_policy)
+        : "memory");
+}
+
 // 1-D bulk copy of `bytes` (a multiple of 16) from global to shared memory;
 // both addresses 16-byte aligned; completion is signalled on `bar` as
 // transaction bytes.
@@ -325,6 +355,32 @@ __device__ __forceinline__ void tma_load_2d_pair(void* smem_dst, const CUtensorM
         ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_addr(smem_dst)),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar_cluster),
         "l"(cache_policy)
+        : "memory");
+}
+
+// CTA-pair forms of the 3-D and im2col loads (completion on the even CTA's
+// barrier, `bar_cluster` a shared::cluster address).
+__device__ __forceinline__ void tma_load_3d_pair(void* smem_dst, const CUtensorMap* map,
+                                                 uint32_t bar_cluster, int32_t c0, int32_t c1,
+                                                 int32_t c2, uint64_t cache_policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+        ".L2::cache_hint [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_addr(smem_dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar_cluster),
+        "l"(cache_policy)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_load_im2col_4d_pair(void* smem_dst, const CUtensorMap* map,
+                                                        uint32_t bar_cluster, int32_t c, int32_t w,
+                                                        int32_t h, int32_t n, uint16_t ow,
+                                                        uint16_t oh, uint64_t cache_policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.cta_group::2.shared::cluster.global.im2col.mbarrier::"
+        "complete_tx::bytes.L2::cache_hint [%0], [%1, {%2, %3, %4, %5}], [%6], {%7, %8}, %9;" ::"r"(
+            smem_addr(smem_dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c), "r"(w), "r"(h), "r"(n), "r"(bar_cluster),
+        "h"(ow), "h"(oh), "l"(cache_policy)
         : "memory");
 }
 
