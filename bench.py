@@ -28,6 +28,10 @@ Also reported:
 --impl reference times the CPU oracle as the comparison arm (the pages ship
 no runnable implementation); it runs on rank 0 only.
 
+--workload conv* times the implicit-GEMM convolution (CATLASS page, section
+5.1): a step is one conv2d_fprop call; the metric is TFLOP/s
+(2 N P Q K R S C / t) against the dense BF16 peak.
+
 --workload softmax_* times the row softmax instead (SGEMM tutorial page,
 section 2): a step is one softmax_rows call over the whole matrix; the metric
 is GB/s (X read once + Y written once, per unit time) against the measured
@@ -67,6 +71,7 @@ SOFTMAX_SOURCES = ["mixed_precision_dense_sm_gb300/csrc/softmax_kern.cuh",
                    "mixed_precision_dense_sm_gb300/csrc/softmax.cu",
                    "mixed_precision_dense_sm_gb300/csrc/ptx.cuh"]
 SOFTMAX_METRIC = "softmax GB/s (X read once + Y written once, per second) at 1 GB300; % of HBM"
+CONV_METRIC = "conv2d TFLOP/s (2 N P Q K R S C / t) at 1 GB300; % of dense tensor peak"
 
 
 def kernel_hash(sources=None) -> str:
@@ -754,6 +759,192 @@ def run_softmax_reference(args):
     print(json.dumps(out), flush=True)
 
 
+# -------------------------------------------------------------- convolution
+
+class ConvOracleSampler:
+    """Times the CPU oracle's convolution at seeded output pixels."""
+
+    def __init__(self, w, x, wt):
+        import numpy as np
+        import oracle
+        self.o = oracle.get()
+        self.w = w
+        self.xc, self.wc = workloads.as_codes(x), workloads.as_codes(wt)
+        self.threads = self.o.max_threads()
+        self.rng = np.random.default_rng(0)
+        M, _, _ = w.gemm_mnk()
+        self.M = M
+
+    def run(self, n):
+        w = self.w
+        rows = self.rng.integers(0, self.M, n)
+        t0 = time.perf_counter()
+        self.o.conv2d_sampled(w.N, w.H, w.W, w.C, w.K, w.R, w.S, w.pad[0], w.pad[1], w.stride[0],
+                              w.stride[1], w.dil[0], w.dil[1], 1.0, self.xc, self.wc, 0.0, None,
+                              w.x_dtype, w.y_dtype, rows)
+        t = time.perf_counter() - t0
+        _, N, K = w.gemm_mnk()
+        return 2.0 * n * N * K, t
+
+    def calibrate(self, seconds):
+        n = 8
+        while True:
+            _, t = self.run(n)
+            if t > seconds / 8 or n >= self.M:
+                break
+            n = min(self.M, n * 4)
+        _, t = self.run(n)
+        return max(1, int(n * seconds / max(t, 1e-6)))
+
+
+def run_conv(args):
+    import mixed_precision_dense_sm_gb300 as lib
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    w = workloads.CONV_WORKLOADS[args.workload]
+    x, wt = workloads.make_conv_inputs(w)
+    M, Ng, Kg = w.gemm_mnk()
+    X, Wd = x.cuda(), wt.cuda()
+    Y = torch.empty((M, w.K), dtype=workloads.TORCH_DTYPE[w.y_dtype], device="cuda")
+    g = lib.Gemm()
+    stream = torch.cuda.current_stream()
+    sh = stream.cuda_stream
+    dts = (w.x_dtype, w.x_dtype, w.y_dtype)
+    sms = torch.cuda.get_device_properties(local).multi_processor_count
+    st, plan = lib.conv2d_plan_query(w.N, w.H, w.W, w.C, w.K, w.R, w.S, w.pad, w.stride, w.dil,
+                                     1.0, X.data_ptr(), Wd.data_ptr(), 0.0, Y.data_ptr(), dts,
+                                     num_sms=sms)
+    assert st == 0
+
+    def step(Xd=X, Wdd=Wd, Yd=Y, s=sh):
+        st = lib.conv2d_fprop(g.h, w.N, w.H, w.W, w.C, w.K, w.R, w.S, w.pad, w.stride, w.dil, 1.0,
+                              Xd.data_ptr(), Wdd.data_ptr(), 0.0, Yd.data_ptr(), dts, stream=s)
+        if st != 0:
+            raise lib.GemmError(st, "conv2d_fprop")
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    for _ in range(args.warmup):
+        step()
+    g.sync()
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    w0 = time.time()
+    t_start.record(stream)
+    for _ in range(args.steps):
+        step()
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    w1 = time.time()
+    clk = clocks.stop((w0, w1))
+    barrier(world)
+    g.sync()
+    ms = max_over_ranks(t_start.elapsed_time(t_end), world)
+    ms_step = ms / args.steps
+    value = world * w.flops() * args.steps / (ms * 1e-3) / 1e12
+    peaks, peak_src = load_peaks()
+    long_region = ms > 500.0
+    peak = peaks["bf16_tflops_sustained"] if long_region else peaks["bf16_tflops"]
+    achieved = w.flops() / (ms_step * 1e-3) / 1e12
+    roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
+            "frac": round(achieved / peak, 4),
+            "peak_kind": "sustained (timed region %.0f ms at the power cap)" % ms if long_region
+            else "burst",
+            "traffic": committed_traffic(w.name),
+            "peak_source": f"{peak_src} ({'MEASURED_PEAKS.json' if peak_src == 'measured' else 'recipe fallback'})",
+            "kernel": "gemm_tc_kernel (im2col A operand)", "launch_ms": round(ms_step, 4),
+            "launch_ms_source": "timed region / launches (events at the region's ends only)"}
+    # e2e: X and Wt up from pinned host memory, the convolution, Y back
+    hX, hW = x.pin_memory(), wt.pin_memory()
+    hY = torch.empty(Y.shape, dtype=Y.dtype).pin_memory()
+    e_steps = max(3, min(args.steps, 20))
+    for _ in range(2):
+        X.copy_(hX, non_blocking=True)
+        Wd.copy_(hW, non_blocking=True)
+        step()
+        hY.copy_(Y, non_blocking=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e_steps):
+        X.copy_(hX, non_blocking=True)
+        Wd.copy_(hW, non_blocking=True)
+        step()
+        hY.copy_(Y, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ems = max_over_ranks(e0.elapsed_time(e1), world)
+    e2e = {"value": round(world * w.flops() * e_steps / (ems * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+           "h2d_bytes_per_step": hX.numel() * hX.element_size() + hW.numel() * hW.element_size(),
+           "d2h_bytes_per_step": hY.numel() * hY.element_size(), "steps": e_steps,
+           "ms_per_step": round(ems / e_steps, 4)}
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        smp = ConvOracleSampler(w, x, wt)
+        n = smp.calibrate(10.0)
+        f, t = smp.run(n)
+        cpu = {"value": round(f / t / 1e12, 6), "unit": "TFLOP/s", "cores": smp.threads,
+               "kind": "oracle",
+               "sample": f"{n} seeded output pixels, all {w.K} channels, each a full "
+                         f"{Kg}-term sum: {f / 1e9:.2f} GFLOP in {t:.1f} s"}
+    P, Q = w.out_hw()
+    out = {
+        "metric": CONV_METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": workloads.DT_NAME[w.x_dtype], "data": "synthetic",
+        "config": {"workload": f"{w.name}: N={w.N} H={w.H} W={w.W} C={w.C} K={w.K} R={w.R} "
+                               f"S={w.S} pad={w.pad} stride={w.stride} dilation={w.dil} -> "
+                               f"P={P} Q={Q}; GEMM {M} x {Ng} x {Kg}",
+                   "plan": plan, "parallelism": "replicas" if world > 1 else "single GPU",
+                   "l2": "no flush between steps"},
+        "roofline": roof, "e2e": e2e, "gpu_launches": args.steps, "clocks": clk,
+    }
+    if cpu is not None:
+        out["cpu_baseline"] = cpu
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    g.close()
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def run_conv_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    w = workloads.CONV_WORKLOADS[args.workload]
+    x, wt = workloads.make_conv_inputs(w)
+    smp = ConvOracleSampler(w, x, wt)
+    per_step = max(0.05, min(5.0, 150.0 / max(1, args.steps + args.warmup)))
+    n = smp.calibrate(per_step)
+    times, f = [], 0.0
+    for k in range(args.warmup + args.steps):
+        f, t = smp.run(n)
+        if k >= args.warmup:
+            times.append(t)
+    t = sum(times)
+    value = f * len(times) / t / 1e12
+    out = {"metric": CONV_METRIC, "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": world,
+           "steps": args.steps, "warmup": args.warmup,
+           "ms_per_step": round(1e3 * t / len(times), 2), "higher_is_better": True,
+           "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+           "impl": "reference", "config": {"workload": w.name},
+           "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": smp.threads,
+                            "kind": "oracle",
+                            "sample": f"{n} seeded output pixels per step ({f / 1e9:.3f} GFLOP)"},
+           "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                   "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+
+
 # ------------------------------------------------------------ reference arm
 
 def run_reference(args):
@@ -797,7 +988,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="transformer_layer",
                     choices=["transformer_layer"] + list(workloads.WORKLOADS) +
-                    list(workloads.SOFTMAX_WORKLOADS))
+                    list(workloads.SOFTMAX_WORKLOADS) + list(workloads.CONV_WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--epilogue", action="store_true",
                     help="fused epilogues of a transformer MLP block: bias on every GEMM, "
@@ -806,12 +997,13 @@ def main():
     if args.warmup < 3 and args.impl == "ours":
         ap.error("--warmup must be >= 3")
     softmax = args.workload in workloads.SOFTMAX_WORKLOADS
-    if softmax and args.epilogue:
+    conv = args.workload in workloads.CONV_WORKLOADS
+    if (softmax or conv) and args.epilogue:
         ap.error("--epilogue applies to the transformer_layer workload")
     if args.impl == "reference":
-        (run_softmax_reference if softmax else run_reference)(args)
+        (run_softmax_reference if softmax else run_conv_reference if conv else run_reference)(args)
     else:
-        (run_softmax if softmax else run_ours)(args)
+        (run_softmax if softmax else run_conv if conv else run_ours)(args)
 
 
 if __name__ == "__main__":

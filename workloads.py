@@ -205,3 +205,61 @@ def make_softmax_input(w: SoftmaxWorkload) -> torch.Tensor:
     elif w.mask is not None:
         raise ValueError(f"unknown mask {w.mask!r}")
     return _stored(x, ldx, TORCH_DTYPE[w.x_dtype])
+
+
+# -------------------------------------------------------------- convolution
+
+@dataclasses.dataclass(frozen=True)
+class ConvWorkload:
+    """Forward 2-D convolution (CATLASS page, section 5.1), NHWC input,
+    KRSC filter, NPQK output; activations N(0, 1), weights N(0, 0.02)."""
+    name: str
+    N: int
+    H: int
+    W: int
+    C: int
+    K: int
+    R: int
+    S: int
+    pad: tuple
+    stride: tuple
+    dil: tuple
+    x_dtype: int
+    y_dtype: int
+    seed: int = 0
+
+    def out_hw(self):
+        P = (self.H + 2 * self.pad[0] - self.dil[0] * (self.R - 1) - 1) // self.stride[0] + 1
+        Q = (self.W + 2 * self.pad[1] - self.dil[1] * (self.S - 1) - 1) // self.stride[1] + 1
+        return P, Q
+
+    def gemm_mnk(self):
+        P, Q = self.out_hw()
+        return self.N * P * Q, self.K, self.R * self.S * self.C
+
+    def flops(self) -> float:
+        M, N, K = self.gemm_mnk()
+        return 2.0 * M * N * K
+
+
+CONV_WORKLOADS = {w.name: w for w in [
+    ConvWorkload("conv3x3_n32_56x56_c64_k64_bf16", 32, 56, 56, 64, 64, 3, 3, (1, 1), (1, 1),
+                 (1, 1), DT_BF16, DT_BF16),
+    ConvWorkload("conv3x3_n32_28x28_c128_k128_bf16", 32, 28, 28, 128, 128, 3, 3, (1, 1), (1, 1),
+                 (1, 1), DT_BF16, DT_BF16),
+    ConvWorkload("conv3x3_n16_64x64_c256_k256_bf16", 16, 64, 64, 256, 256, 3, 3, (1, 1), (1, 1),
+                 (1, 1), DT_BF16, DT_BF16),
+    ConvWorkload("conv3x3_n32_14x14_c512_k512_bf16", 32, 14, 14, 512, 512, 3, 3, (1, 1), (1, 1),
+                 (1, 1), DT_BF16, DT_BF16),
+]}
+
+
+def make_conv_inputs(w: ConvWorkload):
+    """(X NHWC, Wt KRSC) CPU tensors of w.x_dtype, drawn X then Wt in FP32 from
+    one seeded generator, then rounded."""
+    gen = torch.Generator(device="cpu")
+    gen.manual_seed(w.seed)
+    x = torch.randn((w.N, w.H, w.W, w.C), generator=gen, dtype=torch.float32)
+    wt = torch.randn((w.K, w.R, w.S, w.C), generator=gen, dtype=torch.float32) * 0.02
+    t = TORCH_DTYPE[w.x_dtype]
+    return x.to(t), wt.to(t)
