@@ -29,10 +29,14 @@ namespace {
 constexpr int kMaxStages = 8;
 constexpr int kGroupM = 8;
 // Workspace header: one stream-K counter (int32: contributors that have
-// stored their sums) per output tile.  Stream-K is only planned with fewer
-// tiles than SMs, so 1024 tiles' worth always suffices.
+// stored their sums) per output tile; the planner uses stream-K only for
+// schedules of at most 1024 tiles.
 constexpr int64_t kWsHeaderBytes = 4096;
 constexpr int64_t kMaxCounterTiles = kWsHeaderBytes / 4;
+// Stream-K thresholds: tiles at least this many k-blocks long, and data-parallel
+// schedules whose last wave leaves more than 1 - kMinWaveFill of the GPU idle.
+constexpr int32_t kLongK = 32;
+constexpr double kMinWaveFill = 0.8;
 
 struct OperandDesc {
     // stored matrix: rows x cols with pitch ld (elements); K-major means the
@@ -182,10 +186,25 @@ gemm_status_t make_plan(char transA, char transB, int64_t M, int64_t N, int64_t 
     // tiles (tcgen05 cta_group::2).  Otherwise single-CTA 128-row tiles, 256
     // columns wide when that still fills the GPU, else narrower ones with
     // stream-K over K for more parallelism.
+    //
+    // Wave quantisation: when the last wave of a data-parallel schedule would
+    // leave more than kMinWaveFill of the SMs idle and each tile is long in K,
+    // single-CTA stream-K over the widest tiles balances the work instead
+    // (the fix-up of a split tile costs one FP32 tile through L2, small beside
+    // a K loop of kLongK or more k-blocks).
     pl.k_blocks = static_cast<int32_t>(ceil_div(K, block_k));
+    const bool long_k = !swap && pl.k_blocks >= kLongK;
+    auto wave_fill = [](int64_t tiles, int64_t units) {
+        return static_cast<double>(tiles) / static_cast<double>(ceil_div(tiles, units) * units);
+    };
     const int64_t pair_tiles = ceil_div(pl.Mk, 2 * kBlockM) * ceil_div(pl.Nk, 256);
-    const bool pairs = !swap && pl.Mk >= 2 * kBlockM && pl.Nk >= 256 && num_sms >= 2 &&
-                       pair_tiles >= num_sms / 2;
+    bool pairs = !swap && pl.Mk >= 2 * kBlockM && pl.Nk >= 256 && num_sms >= 2 &&
+                 pair_tiles >= num_sms / 2;
+    bool balance_sk = false;
+    if (pairs && long_k && wave_fill(pair_tiles, num_sms / 2) < kMinWaveFill) {
+        pairs = false;
+        balance_sk = true;
+    }
     const int cg = pairs ? 2 : 1;
     const int64_t block_m = static_cast<int64_t>(kBlockM) * cg;
     const int64_t tiles_m = ceil_div(pl.Mk, block_m);
@@ -201,6 +220,14 @@ gemm_status_t make_plan(char transA, char transB, int64_t M, int64_t N, int64_t 
         bn = 128;                           // too few tiles either way: stream-K below
     } else {
         bn = 64;
+    }
+    if (!pairs && long_k) {
+        const int64_t t = tiles_m * ceil_div(pl.Nk, bn);
+        if (t >= half_wave && wave_fill(t, num_sms) < kMinWaveFill) balance_sk = true;
+        if (balance_sk) {
+            bn = pl.Nk > 128 ? 256 : (pl.Nk > 64 ? 128 : 64);
+            if (tiles_m * ceil_div(pl.Nk, bn) > kMaxCounterTiles) balance_sk = false;
+        }
     }
     const int64_t tiles_n = ceil_div(pl.Nk, bn);
     const int64_t tiles = tiles_m * tiles_n;
@@ -221,12 +248,12 @@ gemm_status_t make_plan(char transA, char transB, int64_t M, int64_t N, int64_t 
     pl.smem_bytes = static_cast<size_t>(stages * stage_bytes + 1024 + barrier_bytes);
 
     const int64_t work = tiles * pl.k_blocks;
-    // Stream-K spreads the K loop of too few tiles over all SMs.  It pays for
-    // itself only when the tiles are long in K; the swapped skinny path
-    // (a weight-streaming GEMM) always uses it.
-    const bool stream_k = !pairs && (tiles < num_sms) && (tiles <= kMaxCounterTiles) &&
-                          (work < INT32_MAX) &&
-                          (swap ? pl.k_blocks >= 4 : (tiles < half_wave && pl.k_blocks >= 32));
+    // Stream-K spreads the K loop of too few tiles (or of a badly filled last
+    // wave, above) over all SMs.  It pays for itself only when the tiles are
+    // long in K; the swapped skinny path (a weight-streaming GEMM) always uses it.
+    const bool stream_k = !pairs && (tiles <= kMaxCounterTiles) && (work < INT32_MAX) &&
+                          (balance_sk || ((tiles < num_sms) &&
+                           (swap ? pl.k_blocks >= 4 : (tiles < half_wave && long_k))));
     if (stream_k) {
         int64_t G = num_sms < work ? num_sms : work;
         const int64_t L = ceil_div(work, G);

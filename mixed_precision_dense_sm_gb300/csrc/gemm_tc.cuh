@@ -103,8 +103,8 @@ struct TcParams {
     int32_t act;                // 0 none, 1 ReLU, 2 GELU (erf), 3 SiLU
     // implicit-GEMM convolution (conv != 0): A is an im2col map over the
     // NHWC input, B a 3-D map (C, R*S, K) over the KRSC filter; k-block kb is
-    // filter tap kb / conv_cblocks with channels from (kb % conv_cblocks) * 64
-    // (16-bit inputs), D row m the output pixel (n, p, q) of m = (n*P + p)*Q + q
+    // filter tap kb % (R*S) with channels from (kb / (R*S)) * 64 (16-bit
+    // inputs), D row m the output pixel (n, p, q) of m = (n*P + p)*Q + q
     int32_t conv;
     int32_t conv_cblocks;       // ceil(C / 64)
     int32_t conv_S;             // filter width
@@ -566,9 +566,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                         continue;
                     }
                     if (p.conv) {
-                        // filter tap (r, s), channels c0 .. c0 + 63
-                        const int32_t tap = kb / p.conv_cblocks;
-                        const int32_t c0 = (kb - tap * p.conv_cblocks) * kBlockK;
+                        // channels c0 .. c0 + 63 of filter tap (r, s): the taps
+                        // of one channel block run back to back, so the shifted
+                        // windows they read are in L2 together
+                        const int32_t taps = p.k_blocks / p.conv_cblocks;
+                        const int32_t cb = kb / taps;
+                        const int32_t tap = kb - cb * taps;
+                        const int32_t c0 = cb * kBlockK;
                         const int32_t r = tap / p.conv_S;
                         const uint16_t ow = static_cast<uint16_t>((tap - r * p.conv_S) * p.conv_dil_w);
                         const uint16_t oh = static_cast<uint16_t>(r * p.conv_dil_h);

@@ -235,7 +235,8 @@ def simulate_stream_k(p):
 
 @pytest.mark.parametrize("shape", [(256, 256, 256), (1024, 1024, 1024), (1000, 1023, 777),
                                    (64, 16384, 8192), (5, 300, 700), (129, 300, 777),
-                                   (257, 129, 4096), (33, 128, 2048), (1, 1, 100000)])
+                                   (257, 129, 4096), (33, 128, 2048), (1, 1, 100000),
+                                   (6272, 512, 4608), (25088, 256, 4096), (9000, 700, 3000)])
 @pytest.mark.parametrize("sms", [148, 152, 7])
 def test_stream_k_schedule_covers_every_block_once(shape, sms):
     M, N, K = shape
@@ -243,17 +244,25 @@ def test_stream_k_schedule_covers_every_block_once(shape, sms):
     p = plan(w, num_sms=sms)
     if p["sk_len"] == 0:
         return                      # data-parallel plan: nothing to replay
-    assert p["grid"] <= sms and p["num_tiles"] < sms
+    assert p["grid"] <= sms
     simulate_stream_k(p)
 
 
-def test_stream_k_only_for_skinny_or_tile_starved_long_k():
+def test_stream_k_only_for_skinny_tile_starved_or_badly_filled_long_k():
     def P(M, N, K, sms=152):
         w = workloads.Workload("s", M, N, K, "N", "T", DT_BF16, DT_BF16, 1.0, 0.0, "U", "U")
         return plan(w, num_sms=sms)
     assert P(64, 16384, 8192)["sk_len"] > 0          # swapped weight-streaming GEMM
     assert P(257, 129, 4096)["sk_len"] > 0           # 6 tiles, 64 k-blocks each
     assert P(1, 1, 100000)["sk_len"] > 0
+    # data-parallel waves filled below 80 % with 32+ k-blocks per tile: stream-K
+    # over the widest single-CTA tiles, possibly more tiles than SMs
+    p = P(6272, 512, 4608)                           # 196 tiles of 128 x 128: 1.29 waves
+    assert p["sk_len"] > 0 and p["block_n"] == 256 and p["path_name"] == "tiled_1sm"
+    p = P(25088, 256, 4096)                          # 98 CTA-pair tiles on 76 pairs
+    assert p["sk_len"] > 0 and p["num_tiles"] > 152 and p["grid"] <= 152
+    assert P(25088, 128, 1152)["sk_len"] == 0        # same fill, 18 k-blocks: not worth it
+    assert P(65536, 256, 2304)["path_name"] == "tiled_2sm"   # 256 pair tiles: 84 % fill
     for shape in [(1024, 1024, 1024), (1000, 1023, 777), (256, 256, 256), (300, 520, 1000)]:
         assert P(*shape)["sk_len"] == 0, shape
     assert P(1024, 1024, 1024)["block_n"] == 64      # 128 tiles of 128 x 64
