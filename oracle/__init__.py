@@ -1,4 +1,5 @@
 """CPU oracle for C = alpha*op(A)*op(B) + beta*C (FP16/BF16 in, FP64 reference),
+its fused epilogues (bias and activation; LayerNorm after the linear layer),
 the row softmax and the forward 2-D convolution.
 
 TEST INFRASTRUCTURE ONLY.  Only the test-suite, ``__graft_entry__.smoke()`` and
@@ -112,6 +113,10 @@ class Oracle:
                                                             dp, dp, ctypes.c_int]
         lib.oracle_softmax.restype = ctypes.c_int
         lib.oracle_softmax.argtypes = [i64, i64, vp, i64, ctypes.c_int, vp, i64, dp, ctypes.c_int]
+        lib.oracle_gemm_layernorm.restype = ctypes.c_int
+        lib.oracle_gemm_layernorm.argtypes = common + ep[:2] + [vp, vp, ctypes.c_int,
+                                                                ctypes.c_double, i64, vp, dp, dp,
+                                                                dp, ctypes.c_int]
         self.lib = lib
         self.path = path
 
@@ -312,3 +317,33 @@ def get() -> Oracle:
         if _default is None:
             _default = Oracle(build())
         return _default
+
+
+def _oracle_layernorm_methods():
+    def gemm_layernorm(self, transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc,
+                       ab_dtype, c_dtype, bias=None, bias_dtype=F32, gamma=None, shift=None,
+                       ln_dtype=F32, eps=1e-5, row_ids=None, nthreads: int = 0):
+        """LayerNorm after the linear layer (oracle.c, oracle_gemm_layernorm):
+        returns (Y, H, S), one row of N per selected row -- y before its final
+        rounding, the decoded h, and the |product| sums of h's dot products."""
+        A, B, C = _prep(A), _prep(B), _prep(C, c=True)
+        bias, gamma, shift = _prep(bias, c=True), _prep(gamma, c=True), _prep(shift, c=True)
+        if row_ids is not None:
+            row_ids = np.ascontiguousarray(row_ids, dtype=np.int64)
+        nr = M if row_ids is None else row_ids.size
+        Y = np.empty((nr, N), dtype=np.float64)
+        H = np.empty((nr, N), dtype=np.float64)
+        S = np.empty((nr, N), dtype=np.float64)
+        st = self.lib.oracle_gemm_layernorm(
+            transA.encode(), transB.encode(), M, N, K, float(alpha), _ptr(A), lda, _ptr(B), ldb,
+            float(beta), _ptr(C), ldc, ab_dtype, c_dtype, _ptr(bias), bias_dtype, _ptr(gamma),
+            _ptr(shift), ln_dtype, float(eps), nr, _ptr(row_ids), Y.ctypes.data, H.ctypes.data,
+            S.ctypes.data, nthreads)
+        if st != 0:
+            raise ValueError(f"oracle_gemm_layernorm failed ({st})")
+        return Y, H, S
+
+    Oracle.gemm_layernorm = gemm_layernorm
+
+
+_oracle_layernorm_methods()

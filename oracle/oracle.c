@@ -603,3 +603,93 @@ int oracle_conv2d(int64_t N, int64_t H, int64_t W, int64_t C, int64_t K, int64_t
                    Sout + m * K);
     return OR_OK;
 }
+
+/* ------------------------------------------ LayerNorm-after-linear oracle */
+
+/* A binary64 value rounded to the output type (round to nearest even) and
+ * read back: the value the stored element holds. */
+static double round_to_type(int dt, double x) {
+    if (dt == OR_F32) return (double)oracle_round_f32(x);
+    if (dt == OR_F16) return oracle_decode_f16(oracle_round_f16(x));
+    return oracle_decode_bf16(oracle_round_bf16(x));
+}
+
+/*
+ * A linear layer with a residual add followed by LayerNorm -- the fused layer
+ * the CATLASS page sets out from (its introduction; section 4.1 adds that a
+ * normalisation is usually fused into the operator before it) -- with the
+ * page's mixed precision rule for normalisations (section 3.4): the data path
+ * stays in the storage type, the reduction is done in a wider type.  Read as
+ *     h_ij  = round_C(alpha * sum_k op(A)_ik op(B)_kj + beta * C_ij + bias_j)
+ *     mu_i  = (1/N) sum_j h_ij
+ *     var_i = (1/N) sum_j (h_ij - mu_i)^2          (the biased variance)
+ *     y_ij  = (h_ij - mu_i) / sqrt(var_i + eps) * gamma_j + shift_j
+ * round_C is the output type's round to nearest even: h is the linear
+ * layer's output as the storage type holds it.  The residual is C (scaled by
+ * beta, usually 1).  bias, gamma and shift have N elements each in ln_dtype
+ * for gamma/shift and bias_dtype for bias; NULL bias or shift reads as 0,
+ * NULL gamma as 1.  mu, var and y are evaluated in binary64 from the decoded
+ * h, in increasing j; y is returned before its final rounding.
+ *
+ * row_ids (nsel entries) selects the rows; NULL means every row (nsel is then
+ * ignored).  Y and H receive one row of N values per selected row: y, and
+ * the decoded h.  S receives, per element, the sum of |products| of h's dot
+ * product (the GEMM oracle's tolerance scale).
+ */
+int oracle_gemm_layernorm(char transA, char transB, int64_t M, int64_t N, int64_t K,
+                          float alpha, const void* A, int64_t lda,
+                          const void* B, int64_t ldb,
+                          float beta, const void* C, int64_t ldc,
+                          int ab_dtype, int c_dtype,
+                          const void* bias, int bias_dtype,
+                          const void* gamma, const void* shift, int ln_dtype, double eps,
+                          int64_t nsel, const int64_t* row_ids,
+                          double* Y, double* H, double* S, int nthreads) {
+    int st = check_epilogue(bias, bias_dtype, OR_ACT_NONE);
+    if (st != OR_OK) return st;
+    if ((gamma != NULL || shift != NULL) && ln_dtype != OR_F16 && ln_dtype != OR_BF16 &&
+        ln_dtype != OR_F32)
+        return OR_BAD_ARG;
+    if (!(eps >= 0.0) || N < 1) return OR_BAD_ARG;
+    const int64_t nr = row_ids != NULL ? nsel : M;
+    if (nr < 0) return OR_BAD_ARG;
+    int64_t* rr = (int64_t*)malloc(sizeof(int64_t) * (size_t)(nr * N + 1));
+    int64_t* cc = (int64_t*)malloc(sizeof(int64_t) * (size_t)(nr * N + 1));
+    if (rr == NULL || cc == NULL) {
+        free(rr);
+        free(cc);
+        return OR_NO_MEM;
+    }
+    for (int64_t s = 0; s < nr; ++s)
+        for (int64_t j = 0; j < N; ++j) {
+            rr[s * N + j] = row_ids != NULL ? row_ids[s] : s;
+            cc[s * N + j] = j;
+        }
+    /* alpha * sum + beta * C for every element of the selected rows */
+    st = oracle_gemm_sampled(transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc,
+                             ab_dtype, c_dtype, nr * N, rr, cc, H, S, nthreads);
+    free(rr);
+    free(cc);
+    if (st != OR_OK) return st;
+    for (int64_t s = 0; s < nr; ++s) {
+        double* h = H + s * N;
+        for (int64_t j = 0; j < N; ++j) {
+            double x = h[j];
+            if (bias != NULL) x = x + decode_c(bias_dtype, bias, j);
+            h[j] = round_to_type(c_dtype, x);
+        }
+        double sum = 0.0;
+        for (int64_t j = 0; j < N; ++j) sum = sum + h[j];
+        const double mu = sum / (double)N;
+        double sq = 0.0;
+        for (int64_t j = 0; j < N; ++j) sq = sq + (h[j] - mu) * (h[j] - mu);
+        const double var = sq / (double)N;
+        const double inv = 1.0 / sqrt(var + eps);
+        for (int64_t j = 0; j < N; ++j) {
+            const double g = gamma != NULL ? decode_c(ln_dtype, gamma, j) : 1.0;
+            const double t = shift != NULL ? decode_c(ln_dtype, shift, j) : 0.0;
+            Y[s * N + j] = (h[j] - mu) * inv * g + t;
+        }
+    }
+    return OR_OK;
+}

@@ -752,6 +752,102 @@ def pin_conv_closed_forms(o):
         raise AssertionError(f"accepted {bad}")
 
 
+# ------------------------------------------------- LayerNorm after linear
+
+def _ln_call(o, M, N, K, A, B, C, c_dtype, beta=0.0, bias=None, bias_dtype=F32, gamma=None,
+             shift=None, ln_dtype=F32, eps=1e-5, row_ids=None, dt=F16, alpha=1.0):
+    return o.gemm_layernorm("N", "N", M, N, K, alpha, A, K, B, N, beta, C, N, dt, c_dtype,
+                            bias, bias_dtype, gamma, shift, ln_dtype, eps, row_ids)
+
+
+def pin_layernorm_closed_forms(o):
+    """Rows of two values have a closed form: h = (a, b) gives
+    y = +-(a - b)/2 / sqrt(((a - b)/2)^2 + eps), then gamma and shift per
+    column; a constant row gives y = shift; with eps = 0 every row of y has
+    mean 0 and mean square 1 (the biased variance)."""
+    A = _to_codes([1.0, 2.0, -1.0], F16).reshape(3, 1)
+    B = _to_codes([3.0, 1.0], F16).reshape(1, 2)
+    gamma = np.array([2.0, 3.0], dtype=np.float32)
+    shift = np.array([0.5, -1.0], dtype=np.float32)
+    eps = 0.25
+    Y, H, _ = _ln_call(o, 3, 2, 1, A, B, None, F32, gamma=gamma, shift=shift, eps=eps)
+    assert (H == np.array([[3.0, 1.0], [6.0, 2.0], [-3.0, -1.0]])).all()
+    for i, (a, b) in enumerate(H):
+        d = (a - b) / 2.0
+        u = d / np.sqrt(d * d + eps)
+        want = np.array([u * 2.0 + 0.5, -u * 3.0 - 1.0])
+        assert np.allclose(Y[i], want, rtol=1e-15, atol=1e-15), (i, Y[i], want)
+    # constant rows: zero deviation, y = shift
+    A1 = _to_codes([1.0, -2.0], F16).reshape(2, 1)
+    B1 = _to_codes([1.5] * 5, F16).reshape(1, 5)
+    sh = np.array([0.25, -1.0, 3.0, 0.0, 7.5], dtype=np.float32)
+    Y, _, _ = _ln_call(o, 2, 5, 1, A1, B1, None, F32, gamma=np.full(5, 4.0, np.float32),
+                       shift=sh, eps=1e-3)
+    assert (Y == sh[None, :].astype(np.float64)).all()
+    # eps = 0: standardised rows
+    rng = _rng(61)
+    M, N, K = 7, 33, 19
+    A = _random_codes(rng, (M, K), BF16)
+    B = _random_codes(rng, (K, N), BF16)
+    Y, _, _ = _ln_call(o, M, N, K, A, B, None, F32, eps=0.0, dt=BF16)
+    assert np.abs(Y.mean(axis=1)).max() < 1e-13
+    assert np.abs((Y * Y).mean(axis=1) - 1.0).max() < 1e-13
+
+
+def pin_layernorm_vs_library(o):
+    """h is the fused-epilogue oracle's result rounded to C's type; y is
+    torch's layer_norm (binary64) of h with gamma and shift; selected rows
+    equal the full evaluation's; NULL gamma / shift are ones / zeros."""
+    import torch
+    rng = _rng(62)
+    for (M, N, K, cdt, ldt, dt) in [(5, 40, 24, BF16, F32, BF16), (4, 17, 9, F16, BF16, F16),
+                                    (3, 64, 50, F32, F16, BF16)]:
+        A = _random_codes(rng, (M, K), dt)
+        B = _random_codes(rng, (K, N), dt)
+        if cdt == F32:
+            C = rng.standard_normal((M, N)).astype(np.float32)
+        else:
+            C = _random_codes(rng, (M, N), cdt)
+        bias = _random_codes(rng, (N,), BF16, 0.5)
+        if ldt == F32:
+            gamma = (1.0 + 0.1 * rng.standard_normal(N)).astype(np.float32)
+            shift = (0.1 * rng.standard_normal(N)).astype(np.float32)
+            g64, t64 = gamma.astype(np.float64), shift.astype(np.float64)
+        else:
+            gamma = _random_codes(rng, (N,), ldt, 0.5)
+            shift = _random_codes(rng, (N,), ldt, 0.1)
+            g64, t64 = exact.codes_to_float64(gamma, ldt), exact.codes_to_float64(shift, ldt)
+        eps = 1e-5
+        Y, H, S = _ln_call(o, M, N, K, A, B, C, cdt, beta=1.0, bias=bias, bias_dtype=BF16,
+                           gamma=gamma, shift=shift, ln_dtype=ldt, eps=eps, dt=dt)
+        R, S2 = o.gemm_ex("N", "N", M, N, K, 1.0, A, K, B, N, 1.0, C, N, dt, cdt, bias, BF16, 0)
+        codes = o.round_output(R, cdt)
+        Hw = (codes.view(np.float32).astype(np.float64) if cdt == F32
+              else exact.codes_to_float64(codes, cdt))
+        assert (H == Hw).all() and (S == S2).all()
+        yt = torch.nn.functional.layer_norm(torch.from_numpy(H), (N,), torch.from_numpy(g64),
+                                            torch.from_numpy(t64), eps).numpy()
+        assert np.abs(Y - yt).max() <= 1e-12 * max(1.0, np.abs(yt).max())
+        rows = np.array([M - 1, 0, M // 2, M - 1])
+        Ys, Hs, Ss = _ln_call(o, M, N, K, A, B, C, cdt, beta=1.0, bias=bias, bias_dtype=BF16,
+                              gamma=gamma, shift=shift, ln_dtype=ldt, eps=eps, row_ids=rows, dt=dt)
+        assert (Ys == Y[rows]).all() and (Hs == H[rows]).all() and (Ss == S[rows]).all()
+        Y1, _, _ = _ln_call(o, M, N, K, A, B, C, cdt, beta=1.0, bias=bias, bias_dtype=BF16,
+                            gamma=np.ones(N, np.float32), shift=np.zeros(N, np.float32),
+                            ln_dtype=F32, eps=eps, dt=dt)
+        Y0, _, _ = _ln_call(o, M, N, K, A, B, C, cdt, beta=1.0, bias=bias, bias_dtype=BF16,
+                            eps=eps, dt=dt)
+        assert (Y1 == Y0).all()
+    for bad in (dict(eps=-1.0), dict(gamma=np.ones(3, np.float32), ln_dtype=7)):
+        try:
+            _ln_call(o, 1, 3, 1, _to_codes([1.0], F16).reshape(1, 1),
+                     _to_codes([1.0, 2.0, 3.0], F16).reshape(1, 3), None, F32, **bad)
+        except ValueError:
+            pass
+        else:
+            raise AssertionError(f"bad argument accepted: {bad}")
+
+
 def _to_codes_round(values, dtype):
     """float64 values -> nearest uint16 codes by torch's conversion (test inputs)."""
     import torch
@@ -770,4 +866,5 @@ ALL_PINS = [
     pin_tf32_truncation, pin_gemm_tf32_bruteforce,
     pin_softmax_closed_forms, pin_softmax_library_and_invariants, pin_softmax_special_values,
     pin_conv_vs_torch, pin_conv_exact_bruteforce, pin_conv_closed_forms,
+    pin_layernorm_closed_forms, pin_layernorm_vs_library,
 ]

@@ -93,6 +93,21 @@ MUTANTS = [
     ("conv_no_padding_check", "if (w < 0 || w >= W) continue;", "if (w < 0) continue;"),
     ("beta_read_when_zero", "if (be != 0.0) r = r + be * decode_c(c_dtype, C, i * ldc + j);\n            acc[j] = r;",
      "r = r + be * decode_c(c_dtype, C, i * ldc + j);\n            acc[j] = r;"),
+    ("ln_unbiased_variance", "const double var = sq / (double)N;",
+     "const double var = sq / (double)(N - 1);"),
+    ("ln_eps_outside_sqrt", "const double inv = 1.0 / sqrt(var + eps);",
+     "const double inv = 1.0 / (sqrt(var) + eps);"),
+    ("ln_h_not_rounded", "h[j] = round_to_type(c_dtype, x);", "h[j] = x;"),
+    ("ln_bias_dropped", "if (bias != NULL) x = x + decode_c(bias_dtype, bias, j);\n            h[j]",
+     "(void)bias;\n            h[j]"),
+    ("ln_gamma_shift_swapped", "Y[s * N + j] = (h[j] - mu) * inv * g + t;",
+     "Y[s * N + j] = (h[j] - mu) * inv * t + g;"),
+    ("ln_variance_about_zero", "sq = sq + (h[j] - mu) * (h[j] - mu);", "sq = sq + h[j] * h[j];"),
+    ("ln_row_ids_ignored", "rr[s * N + j] = row_ids != NULL ? row_ids[s] : s;", "rr[s * N + j] = s;"),
+    ("ln_gamma_first_only", "const double g = gamma != NULL ? decode_c(ln_dtype, gamma, j) : 1.0;",
+     "const double g = gamma != NULL ? decode_c(ln_dtype, gamma, 0) : 1.0;"),
+    ("ln_mean_over_n_minus_1", "const double mu = sum / (double)N;",
+     "const double mu = sum / (double)(N > 1 ? N - 1 : 1);"),
 ]
 
 
