@@ -44,10 +44,12 @@ MUTANTS = [
     ("abs_sum_signed", "sabs[j] = sabs[j] + fabs(p);", "sabs[j] = sabs[j] + p;"),
     ("sampled_transB", "decode_in(ab_dtype, B, b_off(transB, k, j, ldb));\n                acc = acc + p;",
      "decode_in(ab_dtype, B, b_off('N', k, j, ldb));\n                acc = acc + p;"),
-    ("epilogue_bias_dropped", "if (bias != NULL) x = x + decode_c(bias_dtype, bias, j);",
-     "if (bias != NULL) x = x + 0.0 * decode_c(bias_dtype, bias, j);"),
-    ("epilogue_bias_by_row", "if (bias != NULL) x = x + decode_c(bias_dtype, bias, j);",
-     "if (bias != NULL) x = x + decode_c(bias_dtype, bias, i);"),
+    ("epilogue_bias_dropped",
+     "if (bias != NULL) x = x + decode_c(bias_dtype, bias, j);\n            R[i * N + j]",
+     "if (bias != NULL) x = x + 0.0 * decode_c(bias_dtype, bias, j);\n            R[i * N + j]"),
+    ("epilogue_bias_by_row",
+     "if (bias != NULL) x = x + decode_c(bias_dtype, bias, j);\n            R[i * N + j]",
+     "if (bias != NULL) x = x + decode_c(bias_dtype, bias, i);\n            R[i * N + j]"),
     ("sampled_bias_by_row", "if (bias != NULL) x = x + decode_c(bias_dtype, bias, cols[s]);",
      "if (bias != NULL) x = x + decode_c(bias_dtype, bias, rows[s]);"),
     ("gelu_missing_half", "return 0.5 * x * (1.0 + erf(x / sqrt(2.0)));",
