@@ -146,6 +146,52 @@ gemm_status_t gemm_run_ex(gemm_handle_t h, char transA, char transB,
                           gemm_stream_t stream);
 
 /*
+ * LayerNorm after the linear layer -- the layer the CATLASS page starts from
+ * (its introduction: a linear layer fused with a residual add and LayerNorm;
+ * section 4.1: a normalisation is usually fused into the operator before it;
+ * section 3.4: the normalisation keeps its reduction in FP32 while its data
+ * path stays 16-bit):
+ *     h_ij = round_C(alpha * (op(A) op(B))_ij + beta * C_ij + bias_j)
+ *     C_ij <- round_C((h_ij - mean_i) / sqrt(var_i + eps) * gamma_j + shift_j)
+ * where round_C rounds to C's type (h is the linear layer's output as C's type
+ * holds it), mean_i and var_i are the mean and the biased variance of row i of
+ * h over its N columns, and everything after the accumulation is FP32.  The
+ * residual is C itself (beta = 1 adds it; beta = 0 does not read C), and C
+ * receives y in place.  bias (bias_dtype) and gamma, shift (ln_dtype: F16,
+ * BF16 or F32) are device vectors of N elements; NULL bias or shift reads as
+ * 0, NULL gamma as 1.
+ *
+ * Rows of N <= 256 are normalised inside the GEMM's epilogue (the row is whole
+ * in one tile): h never leaves the chip.  Wider rows: the epilogue stores h and
+ * each row's per-tile (sum, M2) into the handle's workspace, then one row pass
+ * combines them (mean = sum of sums / N; M2 = sum of the tiles' M2 plus
+ * n_t (tile mean - mean)^2 per tile) and rewrites the row once.  K == 0 or
+ * alpha == 0: h = round_C(beta * C + bias), then the row pass computes the
+ * statistics itself.
+ *
+ * Inputs A and B: F16 or BF16 (FP32/TF32 inputs return NOT_SUPPORTED); the
+ * problem is never swapped or split along K.  Returns INVALID_VALUE for
+ * ln == NULL, eps not positive and finite, or an unknown bias / ln type;
+ * otherwise as gemm_run.
+ */
+typedef struct {
+    const void* bias;     /* device, N elements, or NULL */
+    int32_t bias_dtype;   /* GEMM_F16, GEMM_BF16 or GEMM_F32 */
+    const void* gamma;    /* device, N elements, or NULL (1) */
+    const void* shift;    /* device, N elements, or NULL (0) */
+    int32_t ln_dtype;     /* type of gamma and shift */
+    float eps;            /* > 0 */
+} gemm_layernorm_t;
+
+gemm_status_t gemm_run_layernorm(gemm_handle_t h, char transA, char transB,
+                                 int64_t M, int64_t N, int64_t K,
+                                 float alpha, const void* A, int64_t lda,
+                                 const void* B, int64_t ldb,
+                                 float beta, void* C, int64_t ldc,
+                                 gemm_dtypes_t dt, const gemm_layernorm_t* ln,
+                                 gemm_stream_t stream);
+
+/*
  * gemm_sync: wait for `stream`, then report (and clear) a device-side timeout
  * recorded by any kernel of this handle.  Returns LAUNCH if the stream itself
  * reports an error.
@@ -234,6 +280,17 @@ gemm_status_t gemm_plan_query(char transA, char transB, int64_t M, int64_t N, in
                               float beta, const void* C, int64_t ldc,
                               gemm_dtypes_t dt, int32_t num_sms, int32_t smem_optin,
                               gemm_plan_t* out);
+
+/* The plan gemm_run_layernorm would use (host logic only, as gemm_plan_query);
+ * *fused (if not NULL) is 1 when rows are normalised inside the epilogue. */
+gemm_status_t gemm_layernorm_plan_query(char transA, char transB,
+                                        int64_t M, int64_t N, int64_t K,
+                                        float alpha, const void* A, int64_t lda,
+                                        const void* B, int64_t ldb,
+                                        float beta, const void* C, int64_t ldc,
+                                        gemm_dtypes_t dt, const gemm_layernorm_t* ln,
+                                        int32_t num_sms, int32_t smem_optin,
+                                        gemm_plan_t* out, int32_t* fused);
 
 /* Size of the static device scratch used by gemm_run_noalloc (32 MiB). */
 #define GEMM_NOALLOC_SCRATCH_BYTES (32u << 20)

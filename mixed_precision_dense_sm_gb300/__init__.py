@@ -9,8 +9,9 @@ no fallback implementation.
 The entry points mirror include/gemm_sm103.h one to one:
 ``gemm_create``, ``gemm_run``, ``gemm_sync``, ``gemm_destroy``,
 ``gemm_status_string``, ``gemm_check_args``, ``gemm_plan_query``,
-``gemm_run_ex`` (fused bias/activation epilogue), ``gemm_debug_set`` and
-``gemm_run_noalloc``; and include/softmax_sm103.h: ``softmax_rows``,
+``gemm_run_ex`` (fused bias/activation epilogue), ``gemm_run_layernorm``
+and ``gemm_layernorm_plan_query`` (LayerNorm after the linear layer),
+``gemm_debug_set`` and ``gemm_run_noalloc``; and include/softmax_sm103.h: ``softmax_rows``,
 ``softmax_plan_query``, ``softmax_sync``, ``softmax_debug_set``; and
 include/conv_sm103.h: ``conv2d_fprop``, ``conv2d_plan_query``,
 ``conv2d_output_dims``.
@@ -47,6 +48,12 @@ class Dtypes(ctypes.Structure):
 class Epilogue(ctypes.Structure):
     _fields_ = [("bias", ctypes.c_void_p), ("bias_dtype", ctypes.c_int32),
                 ("activation", ctypes.c_int32)]
+
+
+class LayerNorm(ctypes.Structure):
+    _fields_ = [("bias", ctypes.c_void_p), ("bias_dtype", ctypes.c_int32),
+                ("gamma", ctypes.c_void_p), ("shift", ctypes.c_void_p),
+                ("ln_dtype", ctypes.c_int32), ("eps", ctypes.c_float)]
 
 
 ACT_NONE, ACT_RELU, ACT_GELU, ACT_SILU = 0, 1, 2, 3
@@ -97,6 +104,12 @@ def _load():
     lib.gemm_run.argtypes = [vp] + run_args + [vp]
     lib.gemm_run_ex.restype = ctypes.c_int
     lib.gemm_run_ex.argtypes = [vp] + run_args + [ctypes.POINTER(Epilogue), vp]
+    lib.gemm_run_layernorm.restype = ctypes.c_int
+    lib.gemm_run_layernorm.argtypes = [vp] + run_args + [ctypes.POINTER(LayerNorm), vp]
+    lib.gemm_layernorm_plan_query.restype = ctypes.c_int
+    lib.gemm_layernorm_plan_query.argtypes = run_args + [
+        ctypes.POINTER(LayerNorm), ctypes.c_int32, ctypes.c_int32, ctypes.POINTER(Plan),
+        ctypes.POINTER(ctypes.c_int32)]
     lib.gemm_run_noalloc.restype = ctypes.c_int
     lib.gemm_run_noalloc.argtypes = run_args + [vp]
     lib.gemm_debug_set.restype = ctypes.c_int
@@ -185,6 +198,37 @@ def gemm_run_ex(h, transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc,
     ep = Epilogue(bias or None, bias_dtype, act)
     return lib.gemm_run_ex(h, _tr(transA), _tr(transB), M, N, K, float(alpha), A, lda, B, ldb,
                            float(beta), C, ldc, Dtypes(*dtypes), ctypes.byref(ep), stream)
+
+
+def gemm_run_layernorm(h, transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, dtypes,
+                       bias=0, bias_dtype=GEMM_F32, gamma=0, shift=0, ln_dtype=GEMM_F32,
+                       eps=1e-5, stream=0) -> int:
+    """Raw C-ABI call of LayerNorm after the linear layer: C <- LayerNorm(
+    round_C(alpha*AB + beta*C + bias)) * gamma + shift along each row of C.
+    bias, gamma, shift are device addresses (0 for none)."""
+    ln = LayerNorm(bias or None, bias_dtype, gamma or None, shift or None, ln_dtype, eps)
+    return lib.gemm_run_layernorm(h, _tr(transA), _tr(transB), M, N, K, float(alpha), A, lda, B,
+                                  ldb, float(beta), C, ldc, Dtypes(*dtypes), ctypes.byref(ln),
+                                  stream)
+
+
+def gemm_layernorm_plan_query(transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc,
+                              dtypes, bias=0, bias_dtype=GEMM_F32, gamma=0, shift=0,
+                              ln_dtype=GEMM_F32, eps=1e-5, num_sms=152, smem_optin=232448):
+    """(status, plan dict with "ln_fused") gemm_run_layernorm would use
+    (host logic only)."""
+    ln = LayerNorm(bias or None, bias_dtype, gamma or None, shift or None, ln_dtype, eps)
+    plan = Plan()
+    fused = ctypes.c_int32(-1)
+    st = lib.gemm_layernorm_plan_query(_tr(transA), _tr(transB), M, N, K, float(alpha), A, lda, B,
+                                       ldb, float(beta), C, ldc, Dtypes(*dtypes), ctypes.byref(ln),
+                                       num_sms, smem_optin, ctypes.byref(plan),
+                                       ctypes.byref(fused))
+    if st != 0:
+        return st, None
+    d = plan.as_dict()
+    d["ln_fused"] = fused.value
+    return st, d
 
 
 def gemm_run_noalloc(transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc,
@@ -365,6 +409,38 @@ class Gemm:
                              ACTIVATIONS[act] if not isinstance(act, int) else act, stream)
         if st != 0:
             raise GemmError(st, "gemm_run")
+        return C
+
+    def layernorm(self, A, B, C, transA="N", transB="N", alpha=1.0, beta=1.0, bias=None,
+                  gamma=None, shift=None, eps=1e-5, M=None, N=None, K=None, stream=None):
+        """LayerNorm after the linear layer, in place on C (the residual when
+        beta != 0): C <- (h - mean) / sqrt(var + eps) * gamma + shift per row,
+        h = round_C(alpha*op(A)op(B) + beta*C + bias).  gamma and shift share
+        one dtype."""
+        import torch
+        if stream is None:
+            stream = torch.cuda.current_stream().cuda_stream
+        for t in (A, B, C):
+            if t is not None and (t.dim() != 2 or t.stride(1) != 1):
+                raise ValueError("operands must be 2-D with unit inner stride")
+        if gamma is not None and shift is not None and gamma.dtype != shift.dtype:
+            raise ValueError("gamma and shift must share a dtype")
+        M = C.shape[0] if M is None else M
+        N = C.shape[1] if N is None else N
+        if K is None:
+            K = A.shape[1] if transA in "Nn" else A.shape[0]
+        ln_t = gamma if gamma is not None else shift
+        dts = (dtype_code(A.dtype), dtype_code(B.dtype), dtype_code(C.dtype))
+        st = gemm_run_layernorm(
+            self.h, transA, transB, M, N, K, alpha, A.data_ptr(), A.stride(0), B.data_ptr(),
+            B.stride(0), beta, C.data_ptr(), C.stride(0), dts,
+            bias.data_ptr() if bias is not None else 0,
+            dtype_code(bias.dtype) if bias is not None else GEMM_F32,
+            gamma.data_ptr() if gamma is not None else 0,
+            shift.data_ptr() if shift is not None else 0,
+            dtype_code(ln_t.dtype) if ln_t is not None else GEMM_F32, eps, stream)
+        if st != 0:
+            raise GemmError(st, "gemm_run_layernorm")
         return C
 
     def sync(self, stream=None):

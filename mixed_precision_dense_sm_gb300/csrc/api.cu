@@ -9,6 +9,7 @@
 // tiles than SMs spread their K loop across SMs (stream-K) so the whole GPU
 // streams the operands; very small M swaps the operands so the 128-row MMA
 // dimension is filled by the large side (the skinny, memory-bound path).
+#include <cmath>
 #include <cstdint>
 #include <cstdlib>
 #include <cstring>
@@ -61,6 +62,11 @@ struct Plan {
     int32_t sk_len, sk_max_seg;
     int64_t pack_a_bytes, pack_b_bytes, partial_bytes;
     size_t smem_bytes;
+    // LayerNorm after the linear layer: whole rows in one tile (normalised in
+    // the epilogue), else per-tile row statistics for a row pass
+    bool ln;
+    bool ln_fused;
+    int64_t ln_stats_bytes;
 };
 
 bool is_n(char t) { return t == 'N' || t == 'n'; }
@@ -103,13 +109,14 @@ gemm_status_t check_args(char transA, char transB, int64_t M, int64_t N, int64_t
 gemm_status_t make_plan(char transA, char transB, int64_t M, int64_t N, int64_t K, float alpha,
                         const void* A, int64_t lda, const void* B, int64_t ldb, float beta,
                         const void* C, int64_t ldc, gemm_dtypes_t dt, int32_t num_sms,
-                        int32_t smem_optin, Plan& pl, bool allow_swap = true) {
+                        int32_t smem_optin, Plan& pl, bool allow_swap = true, bool ln = false) {
     gemm_status_t st = check_args(transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, dt);
     if (st != GEMM_OK) return st;
     if (num_sms < 1 || smem_optin < 64 * 1024) return GEMM_ERR_INVALID_VALUE;
     std::memset(&pl, 0, sizeof pl);
     pl.pub.split_k = 1;
     pl.K = K;
+    pl.ln = ln;
     if (M == 0 || N == 0) {
         pl.pub.path = GEMM_PATH_NOOP;
         return GEMM_OK;
@@ -134,7 +141,7 @@ gemm_status_t make_plan(char transA, char transB, int64_t M, int64_t N, int64_t 
 
     // Skinny M: compute C^T = op(B)^T op(A)^T so the large N fills the
     // 128-row MMA side and the small M becomes the MMA's N.
-    const bool swap = allow_swap && (M <= 64 && N >= 128);
+    const bool swap = allow_swap && !ln && (M <= 64 && N >= 128);
     pl.pub.swap_ab = swap ? 1 : 0;
     if (swap) {
         pl.a = opB;
@@ -193,13 +200,15 @@ gemm_status_t make_plan(char transA, char transB, int64_t M, int64_t N, int64_t 
     // (the fix-up of a split tile costs one FP32 tile through L2, small beside
     // a K loop of kLongK or more k-blocks).
     pl.k_blocks = static_cast<int32_t>(ceil_div(K, block_k));
-    const bool long_k = !swap && pl.k_blocks >= kLongK;
+    // (LayerNorm needs each tile's rows complete in one CTA: no stream-K)
+    const bool long_k = !swap && !ln && pl.k_blocks >= kLongK;
     auto wave_fill = [](int64_t tiles, int64_t units) {
         return static_cast<double>(tiles) / static_cast<double>(ceil_div(tiles, units) * units);
     };
     const int64_t pair_tiles = ceil_div(pl.Mk, 2 * kBlockM) * ceil_div(pl.Nk, 256);
     bool pairs = !swap && pl.Mk >= 2 * kBlockM && pl.Nk >= 256 && num_sms >= 2 &&
                  pair_tiles >= num_sms / 2;
+    if (ln && pl.Nk <= 128) pairs = false;
     bool balance_sk = false;
     if (pairs && long_k && wave_fill(pair_tiles, num_sms / 2) < kMinWaveFill) {
         pairs = false;
@@ -221,6 +230,13 @@ gemm_status_t make_plan(char transA, char transB, int64_t M, int64_t N, int64_t 
     } else {
         bn = 64;
     }
+    if (ln) {
+        // LayerNorm kernels come in widths 128 and 256: a row of up to 256
+        // columns is whole in one tile
+        if (pl.Nk <= 256) bn = (pl.Nk <= 128 && !pairs) ? 128 : 256;
+        else if (bn < 128) bn = 128;
+        pl.ln_fused = (pl.Nk <= bn);
+    }
     if (!pairs && long_k) {
         const int64_t t = tiles_m * ceil_div(pl.Nk, bn);
         if (t >= half_wave && wave_fill(t, num_sms) < kMinWaveFill) balance_sk = true;
@@ -241,7 +257,9 @@ gemm_status_t make_plan(char transA, char transB, int64_t M, int64_t N, int64_t 
 
     const uint32_t stage_bytes = kATileBytes + static_cast<uint32_t>(bn / cg) * 128u;
     const int64_t barrier_bytes = 256;
-    int64_t stages = (smem_optin - 1024 - barrier_bytes) / stage_bytes;
+    // static shared memory of the kernel: flags, and the LayerNorm exchange
+    const int64_t static_bytes = 64 + (ln ? 4 * kBlockM * 4 : 4);
+    int64_t stages = (smem_optin - 1024 - barrier_bytes - static_bytes) / stage_bytes;
     if (stages > kMaxStages) stages = kMaxStages;
     if (stages < 2) return GEMM_ERR_NOT_SUPPORTED;
     pl.pub.stages = static_cast<int32_t>(stages);
@@ -251,7 +269,7 @@ gemm_status_t make_plan(char transA, char transB, int64_t M, int64_t N, int64_t 
     // Stream-K spreads the K loop of too few tiles (or of a badly filled last
     // wave, above) over all SMs.  It pays for itself only when the tiles are
     // long in K; the swapped skinny path (a weight-streaming GEMM) always uses it.
-    const bool stream_k = !pairs && (tiles <= kMaxCounterTiles) && (work < INT32_MAX) &&
+    const bool stream_k = !pairs && !ln && (tiles <= kMaxCounterTiles) && (work < INT32_MAX) &&
                           (balance_sk || ((tiles < num_sms) &&
                            (swap ? pl.k_blocks >= 4 : (tiles < half_wave && long_k))));
     if (stream_k) {
@@ -273,8 +291,9 @@ gemm_status_t make_plan(char transA, char transB, int64_t M, int64_t N, int64_t 
     pl.pub.k_blocks = pl.k_blocks;
     pl.pub.tiles_m = pl.tiles_m;
     pl.pub.tiles_n = pl.tiles_n;
+    if (ln && !pl.ln_fused) pl.ln_stats_bytes = pl.Mk * tiles_n * 8;
     const int64_t body = round_up(pl.pack_a_bytes, 256) + round_up(pl.pack_b_bytes, 256) +
-                         round_up(pl.partial_bytes, 256);
+                         round_up(pl.partial_bytes, 256) + round_up(pl.ln_stats_bytes, 256);
     pl.pub.workspace_bytes = body > 0 ? kWsHeaderBytes + body : 0;
     return GEMM_OK;
 }
@@ -434,6 +453,42 @@ int grid_for(int64_t elems_per_thread_unit, int num_sms) {
 }
 
 
+// The LayerNorm row pass over C (M x N, row pitch ldc): from per-tile
+// statistics, or (stats == nullptr) computing them.
+template <typename OutT>
+void launch_ln_rows(int64_t M, int64_t N, OutT* C, int64_t ldc, const float2* stats,
+                    int32_t tiles_n, int32_t block_n, const gemm_layernorm_t* ln, int32_t ldt,
+                    int num_sms, cudaStream_t stream) {
+    if (stats != nullptr) {
+        const int64_t want = static_cast<int64_t>(num_sms) * 8;   // resident CTAs
+        const int grid = static_cast<int>(M < want ? M : want);
+        ln_rows_stats_kernel<OutT><<<grid, kLnRowThreads, 0, stream>>>(C, ldc, M, N, stats, tiles_n,
+                                                             block_n, ln->gamma, ln->shift, ldt,
+                                                             ln->eps);
+    } else {
+        const int64_t want = static_cast<int64_t>(num_sms) * 8;
+        const int grid = static_cast<int>(M < want ? M : want);
+        ln_rows_kernel<OutT><<<grid, 256, 0, stream>>>(C, ldc, M, N, ln->gamma, ln->shift, ldt,
+                                                       ln->eps);
+    }
+}
+
+gemm_status_t enqueue_ln_rows(int64_t M, int64_t N, void* C, int64_t ldc, gemm_dtypes_t dt,
+                              const float2* stats, int32_t tiles_n, int32_t block_n,
+                              const gemm_layernorm_t* ln, int num_sms, cudaStream_t stream) {
+    const int32_t ldt = (ln->gamma || ln->shift) ? ln->ln_dtype : GEMM_F32;
+    if (dt.c == GEMM_F32)
+        launch_ln_rows(M, N, static_cast<float*>(C), ldc, stats, tiles_n, block_n, ln, ldt,
+                       num_sms, stream);
+    else if (dt.c == GEMM_F16)
+        launch_ln_rows(M, N, static_cast<__half*>(C), ldc, stats, tiles_n, block_n, ln, ldt,
+                       num_sms, stream);
+    else
+        launch_ln_rows(M, N, static_cast<__nv_bfloat16*>(C), ldc, stats, tiles_n, block_n, ln,
+                       ldt, num_sms, stream);
+    return cudaGetLastError() == cudaSuccess ? GEMM_OK : GEMM_ERR_LAUNCH;
+}
+
 // Everything gemm_run enqueues after planning: the optional pack pre-passes,
 // the TMA descriptors and the GEMM kernel.  `ws` is the workspace laid out as
 // [tile counters (4 KB)][packed A][packed B][partial slots]; with
@@ -442,7 +497,7 @@ gemm_status_t enqueue_plan(const Plan& pl, EncodeTiledFn encode, int num_sms, ui
                            int* err_dev, float alpha, float beta, void* C, gemm_dtypes_t dt,
                            cudaStream_t stream, bool clear_counters, uint32_t debug_flags = 0,
                            uint64_t wait_limit_ns = 0, const gemm_epilogue_t* ep = nullptr,
-                           const ConvDesc* conv = nullptr) {
+                           const ConvDesc* conv = nullptr, const gemm_layernorm_t* ln = nullptr) {
     // kind::tf32 reads K-major operands only; the planner transposes the rest.
     if (pl.esize == 4 && (pl.a.mn_major || pl.b.mn_major)) return GEMM_ERR_NOT_SUPPORTED;
     int* counters = reinterpret_cast<int*>(ws);
@@ -454,6 +509,8 @@ gemm_status_t enqueue_plan(const Plan& pl, EncodeTiledFn encode, int num_sms, ui
     uint8_t* ws_a = ws + kWsHeaderBytes;
     uint8_t* ws_b = ws_a + round_up(pl.pack_a_bytes, 256);
     float* ws_part = reinterpret_cast<float*>(ws_b + round_up(pl.pack_b_bytes, 256));
+    float2* ws_stats = reinterpret_cast<float2*>(reinterpret_cast<uint8_t*>(ws_part) +
+                                                 round_up(pl.partial_bytes, 256));
 
     // Pack operands whose rows TMA cannot address (pitch or base not 16-byte aligned).
     const void* a_ptr = pl.a.ptr;
@@ -546,6 +603,18 @@ gemm_status_t enqueue_plan(const Plan& pl, EncodeTiledFn encode, int num_sms, ui
     p.bias_dtype = (ep && ep->bias) ? ep->bias_dtype : GEMM_F32;
     p.bias_on_rows = pl.pub.swap_ab ? 1 : 0;      // swapped: C columns are D' rows
     p.act = ep ? ep->activation : GEMM_ACT_NONE;
+    if (pl.ln) {
+        l.epi = kEpiLayerNorm;
+        p.bias = ln->bias;
+        p.bias_dtype = ln->bias ? ln->bias_dtype : GEMM_F32;
+        p.act = GEMM_ACT_NONE;
+        p.ln_gamma = ln->gamma;
+        p.ln_shift = ln->shift;
+        p.ln_dtype = (ln->gamma || ln->shift) ? ln->ln_dtype : GEMM_F32;
+        p.ln_eps = ln->eps;
+        p.ln_fused = pl.ln_fused ? 1 : 0;
+        p.ln_stats = pl.ln_fused ? nullptr : ws_stats;
+    }
     if (conv != nullptr) {
         p.conv = 1;
         p.conv_cblocks = static_cast<int32_t>(ceil_div(conv->C, 64));
@@ -580,6 +649,9 @@ gemm_status_t enqueue_plan(const Plan& pl, EncodeTiledFn encode, int num_sms, ui
         cudaGetLastError();
         return GEMM_ERR_LAUNCH;
     }
+    if (pl.ln && !pl.ln_fused)
+        return enqueue_ln_rows(pl.Mk, pl.Nk, C, pl.c_rs, dt, ws_stats, pl.tiles_n, bn, ln, num_sms,
+                               stream);
     return GEMM_OK;
 }
 
@@ -644,6 +716,16 @@ gemm_status_t conv_plan(int64_t N, int64_t H, int64_t W, int64_t C, int64_t K, i
     const int64_t kfake = R * S * ceil_div(C, 64) * 64;
     return make_plan('N', 'T', M, K, kfake, alpha, X, kfake, Wt, kfake, beta, Y, K, dt, num_sms,
                      smem_optin, pl, false);
+}
+
+bool dtype16or32(int32_t t) { return t == GEMM_F16 || t == GEMM_BF16 || t == GEMM_F32; }
+
+bool layernorm_ok(const gemm_layernorm_t* ln) {
+    if (ln == nullptr) return false;
+    if (ln->bias != nullptr && !dtype16or32(ln->bias_dtype)) return false;
+    if ((ln->gamma != nullptr || ln->shift != nullptr) && !dtype16or32(ln->ln_dtype)) return false;
+    if (!(ln->eps > 0.0f) || !std::isfinite(ln->eps)) return false;
+    return true;
 }
 
 bool epilogue_ok(const gemm_epilogue_t* ep) {
@@ -804,6 +886,52 @@ gemm_status_t gemm_run(gemm_handle_t h, char transA, char transB, int64_t M, int
                        float beta, void* C, int64_t ldc, gemm_dtypes_t dt, gemm_stream_t stream) {
     return gemm_run_ex(h, transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, dt,
                        nullptr, stream);
+}
+
+gemm_status_t gemm_layernorm_plan_query(char transA, char transB, int64_t M, int64_t N, int64_t K,
+                                        float alpha, const void* A, int64_t lda, const void* B,
+                                        int64_t ldb, float beta, const void* C, int64_t ldc,
+                                        gemm_dtypes_t dt, const gemm_layernorm_t* ln,
+                                        int32_t num_sms, int32_t smem_optin, gemm_plan_t* out,
+                                        int32_t* fused) {
+    if (out == nullptr || !layernorm_ok(ln)) return GEMM_ERR_INVALID_VALUE;
+    Plan pl;
+    gemm_status_t st = make_plan(transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, dt,
+                                 num_sms, smem_optin, pl, false, true);
+    if (st != GEMM_OK) return st;
+    if (dt.a == GEMM_F32) return GEMM_ERR_NOT_SUPPORTED;
+    *out = pl.pub;
+    if (fused) *fused = pl.ln_fused ? 1 : 0;
+    return GEMM_OK;
+}
+
+gemm_status_t gemm_run_layernorm(gemm_handle_t h, char transA, char transB, int64_t M, int64_t N,
+                                 int64_t K, float alpha, const void* A, int64_t lda, const void* B,
+                                 int64_t ldb, float beta, void* C, int64_t ldc, gemm_dtypes_t dt,
+                                 const gemm_layernorm_t* ln, gemm_stream_t stream_) {
+    if (h == nullptr || !layernorm_ok(ln)) return GEMM_ERR_INVALID_VALUE;
+    gemm_status_t st = take_device_error(h);
+    if (st != GEMM_OK) return st;
+    Plan pl;
+    st = make_plan(transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, dt, h->num_sms,
+                   h->smem_optin, pl, false, true);
+    if (st != GEMM_OK) return st;
+    if (dt.a == GEMM_F32) return GEMM_ERR_NOT_SUPPORTED;
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    if (pl.pub.path == GEMM_PATH_NOOP) return GEMM_OK;
+    if (pl.pub.path == GEMM_PATH_SCALE) {
+        // h = beta * C + bias (rounded to C's type), then whole-row LayerNorm
+        gemm_epilogue_t ep{ln->bias, ln->bias_dtype, GEMM_ACT_NONE};
+        st = enqueue_scale(M, N, C, ldc, beta, dt, h->num_sms, stream, &ep);
+        if (st != GEMM_OK) return st;
+        return enqueue_ln_rows(M, N, C, ldc, dt, nullptr, 1, static_cast<int32_t>(N), ln,
+                               h->num_sms, stream);
+    }
+    st = ensure_workspace(h, static_cast<size_t>(pl.pub.workspace_bytes));
+    if (st != GEMM_OK) return st;
+    return enqueue_plan(pl, h->encode, h->num_sms, static_cast<uint8_t*>(h->ws), h->err_dev, alpha,
+                        beta, C, dt, stream, false, h->debug_flags, h->wait_limit_ns, nullptr,
+                        nullptr, ln);
 }
 
 }  // extern "C"

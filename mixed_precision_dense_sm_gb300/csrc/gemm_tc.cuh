@@ -110,6 +110,18 @@ struct TcParams {
     int32_t conv_S;             // filter width
     int32_t conv_P, conv_Q;     // output height and width
     int32_t conv_stride_h, conv_stride_w, conv_pad_h, conv_pad_w, conv_dil_h, conv_dil_w;
+    // LayerNorm after the linear layer (kernels instantiated with EPI ==
+    // kEpiLayerNorm): h = round_C(alpha * acc + beta * C + bias) per element;
+    // ln_fused (the whole row in one tile): each row is normalised in the
+    // epilogue, y = (h - mean) / sqrt(var + eps) * gamma + shift, and only y is
+    // stored; otherwise h is stored and (sum, M2) of the tile's columns of
+    // each row go to ln_stats[row * tiles_n + tile column] for a row pass
+    const void* ln_gamma;       // N elements or nullptr (1)
+    const void* ln_shift;       // N elements or nullptr (0)
+    int32_t ln_dtype;           // 0 F16, 1 BF16, 2 F32
+    int32_t ln_fused;
+    float ln_eps;
+    float2* ln_stats;
 };
 
 // Test hook: CTA 0's producer arms its first pipeline slot but issues no load
@@ -257,6 +269,50 @@ __device__ __forceinline__ float load_bias(const TcParams& p, int64_t idx) {
     return load_bias_elem(p.bias, p.bias_dtype, idx);
 }
 
+// Elements c0..c0+31 of a per-column vector (bias, gamma, shift) of type
+// 0 = F16, 1 = BF16, 2 = F32; zeros past column N.
+__device__ __forceinline__ void load_col_vec32(const void* vec, int32_t dtype, int32_t c0,
+                                               int32_t N, float (&b)[32]) {
+    const int esize = dtype == 2 ? 4 : 2;
+    const uintptr_t addr = reinterpret_cast<uintptr_t>(vec) + static_cast<uintptr_t>(c0) * esize;
+    if (c0 + 32 <= N && (addr & 15u) == 0) {
+        // 16-byte loads (every thread of the warp reads the same columns: one
+        // L1 line serves the warp)
+        const uint4* src = reinterpret_cast<const uint4*>(addr);
+        if (dtype == 2) {
+            #pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                const uint4 t = __ldg(src + q);
+                b[4 * q] = __uint_as_float(t.x);
+                b[4 * q + 1] = __uint_as_float(t.y);
+                b[4 * q + 2] = __uint_as_float(t.z);
+                b[4 * q + 3] = __uint_as_float(t.w);
+            }
+        } else {
+            #pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const uint4 t = __ldg(src + q);
+                const uint32_t w[4] = {t.x, t.y, t.z, t.w};
+                #pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const uint16_t lo = static_cast<uint16_t>(w[e] & 0xFFFFu);
+                    const uint16_t hi = static_cast<uint16_t>(w[e] >> 16);
+                    if (dtype == 1) {
+                        b[8 * q + 2 * e] = __bfloat162float(__ushort_as_bfloat16(lo));
+                        b[8 * q + 2 * e + 1] = __bfloat162float(__ushort_as_bfloat16(hi));
+                    } else {
+                        b[8 * q + 2 * e] = __half2float(__ushort_as_half(lo));
+                        b[8 * q + 2 * e + 1] = __half2float(__ushort_as_half(hi));
+                    }
+                }
+            }
+        }
+    } else {
+        #pragma unroll
+        for (int j = 0; j < 32; ++j) b[j] = (c0 + j < N) ? load_bias_elem(vec, dtype, c0 + j) : 0.0f;
+    }
+}
+
 // Adds the bias and applies the activation to one row's 32 values at D'
 // columns c0..c0+31 (in place); the beta * C term is already in v.
 __device__ __forceinline__ void bias_act(const TcParams& p, int32_t row, int32_t c0,
@@ -268,44 +324,7 @@ __device__ __forceinline__ void bias_act(const TcParams& p, int32_t row, int32_t
             for (int j = 0; j < 32; ++j) v[j] += b;
         } else {
             float b[32];
-            const int esize = p.bias_dtype == 2 ? 4 : 2;
-            const uintptr_t addr = reinterpret_cast<uintptr_t>(p.bias) + static_cast<uintptr_t>(c0) * esize;
-            if (c0 + 32 <= p.N && (addr & 15u) == 0) {
-                // 16-byte loads (every thread of the warp reads the same
-                // columns: one L1 line serves the warp)
-                const uint4* src = reinterpret_cast<const uint4*>(addr);
-                if (p.bias_dtype == 2) {
-                    #pragma unroll
-                    for (int q = 0; q < 8; ++q) {
-                        const uint4 t = __ldg(src + q);
-                        b[4 * q] = __uint_as_float(t.x);
-                        b[4 * q + 1] = __uint_as_float(t.y);
-                        b[4 * q + 2] = __uint_as_float(t.z);
-                        b[4 * q + 3] = __uint_as_float(t.w);
-                    }
-                } else {
-                    #pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        const uint4 t = __ldg(src + q);
-                        const uint32_t w[4] = {t.x, t.y, t.z, t.w};
-                        #pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const uint16_t lo = static_cast<uint16_t>(w[e] & 0xFFFFu);
-                            const uint16_t hi = static_cast<uint16_t>(w[e] >> 16);
-                            if (p.bias_dtype == 1) {
-                                b[8 * q + 2 * e] = __bfloat162float(__ushort_as_bfloat16(lo));
-                                b[8 * q + 2 * e + 1] = __bfloat162float(__ushort_as_bfloat16(hi));
-                            } else {
-                                b[8 * q + 2 * e] = __half2float(__ushort_as_half(lo));
-                                b[8 * q + 2 * e + 1] = __half2float(__ushort_as_half(hi));
-                            }
-                        }
-                    }
-                }
-            } else {
-                #pragma unroll
-                for (int j = 0; j < 32; ++j) b[j] = (c0 + j < p.N) ? load_bias(p, c0 + j) : 0.0f;
-            }
+            load_col_vec32(p.bias, p.bias_dtype, c0, p.N, b);
             #pragma unroll
             for (int j = 0; j < 32; ++j) v[j] += b[j];
         }
@@ -418,11 +437,204 @@ __device__ __forceinline__ bool epilogue_all(bool ok) {
     return r != 0;
 }
 
-template <int CG, int BN, typename OutT, int ES>
+// ----------------------------------------- LayerNorm after the linear layer
+
+constexpr int kEpiPlain = 0;
+constexpr int kEpiLayerNorm = 1;
+
+// A value as the output type holds it (rounded to nearest even, read back).
+template <typename OutT>
+__device__ __forceinline__ float round_to_out(float v) {
+    const OutT t = cvt_out<OutT>(v);
+    return load_out<OutT>(&t);
+}
+
+// Stores 32 values of one C row at D' columns c0..c0+31 (the columns < N),
+// cast to the output type; vector stores when the chunk is whole and aligned.
+template <typename OutT>
+__device__ __forceinline__ void store_out32(const TcParams& p, int32_t row, int32_t c0,
+                                            const float (&v)[32]) {
+    OutT* base = reinterpret_cast<OutT*>(p.C) + static_cast<int64_t>(row) * p.c_rs;
+    if (p.c_vector && c0 + 32 <= p.N) {
+        constexpr int kPer16 = 16 / sizeof(OutT);
+        #pragma unroll
+        for (int q = 0; q < 32 / kPer16; ++q) {
+            uint4 pack;
+            OutT* pk = reinterpret_cast<OutT*>(&pack);
+            #pragma unroll
+            for (int e = 0; e < kPer16; ++e) pk[e] = cvt_out<OutT>(v[q * kPer16 + e]);
+            *reinterpret_cast<uint4*>(base + c0 + q * kPer16) = pack;
+        }
+    } else {
+        #pragma unroll
+        for (int j = 0; j < 32; ++j)
+            if (c0 + j < p.N) base[static_cast<int64_t>(c0 + j) * p.c_cs] = cvt_out<OutT>(v[j]);
+    }
+}
+
+// Warp-collective: v[0..31] = TMEM row `taddr`, 32 consecutive columns.
+__device__ __forceinline__ void tmem_row32(uint32_t taddr, float (&v)[32]) {
+    uint32_t r[32];
+    __syncwarp();
+    tmem_ld_32x32b_x32(taddr, r);
+    tmem_ld_wait();
+    #pragma unroll
+    for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+}
+
+// h for one row's 32 columns c0..c0+31 of the accumulator at TMEM address
+// `taddr`: round_C(alpha * acc + beta * C + bias), 0 past column N.  The
+// residual C and the bias are read only for rows inside the matrix (`rv`).
+// Warp-collective (tcgen05.ld).
+template <typename OutT>
+__device__ __forceinline__ void ln_chunk_h(const TcParams& p, uint32_t taddr, int32_t row, bool rv,
+                                           int32_t c0, float (&v)[32]) {
+    tmem_row32(taddr, v);
+    #pragma unroll
+    for (int j = 0; j < 32; ++j) v[j] *= p.alpha;
+    if (rv && c0 < p.N) {
+        const OutT* base = reinterpret_cast<const OutT*>(p.C) + static_cast<int64_t>(row) * p.c_rs;
+        if (p.beta != 0.0f) {
+            if (p.c_vector && c0 + 32 <= p.N) {
+                constexpr int kPer16 = 16 / sizeof(OutT);
+                uint4 old[32 / kPer16];
+                #pragma unroll
+                for (int q = 0; q < 32 / kPer16; ++q)
+                    old[q] = *reinterpret_cast<const uint4*>(base + c0 + q * kPer16);
+                #pragma unroll
+                for (int q = 0; q < 32 / kPer16; ++q) {
+                    const OutT* o = reinterpret_cast<const OutT*>(&old[q]);
+                    #pragma unroll
+                    for (int e = 0; e < kPer16; ++e)
+                        v[q * kPer16 + e] = fmaf(p.beta, load_out<OutT>(o + e), v[q * kPer16 + e]);
+                }
+            } else {
+                #pragma unroll
+                for (int j = 0; j < 32; ++j)
+                    if (c0 + j < p.N)
+                        v[j] = fmaf(p.beta, load_out<OutT>(base + static_cast<int64_t>(c0 + j) * p.c_cs),
+                                    v[j]);
+            }
+        }
+        if (p.bias != nullptr) {
+            float b[32];
+            load_col_vec32(p.bias, p.bias_dtype, c0, p.N, b);
+            #pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] += b[j];
+        }
+    }
+    #pragma unroll
+    for (int j = 0; j < 32; ++j) v[j] = (c0 + j < p.N) ? round_to_out<OutT>(v[j]) : 0.0f;
+}
+
+// Asks L2 for the residual C of one row's chunks of a tile (the chunks this
+// thread will read, columns < N), so the first epilogue pass finds it there.
+// Issued before the tile's accumulator is ready: the loads overlap the MMA.
+template <typename OutT, int BN>
+__device__ __forceinline__ void ln_prefetch_residual(const TcParams& p, int32_t row, int half,
+                                                     int32_t col0) {
+    if (p.beta == 0.0f || row >= p.M) return;
+    const uint8_t* base = reinterpret_cast<const uint8_t*>(p.C) +
+                          static_cast<int64_t>(row) * p.c_rs * static_cast<int64_t>(sizeof(OutT));
+    #pragma unroll
+    for (int ch = half; ch < BN / 32; ch += 2) {
+        const int32_t c0 = col0 + ch * 32;
+        if (c0 >= p.N) break;
+        const int32_t n = (p.N - c0) < 32 ? (p.N - c0) : 32;
+        const int32_t bytes = n * static_cast<int32_t>(sizeof(OutT));
+        const uint8_t* q = base + static_cast<int64_t>(c0) * static_cast<int64_t>(sizeof(OutT));
+        for (int32_t b = 0; b < bytes; b += 32) prefetch_l2(q + b);
+        prefetch_l2(q + bytes - 1);
+    }
+}
+
+// The LayerNorm epilogue of one tile.  Each row's columns are split between
+// two warps (alternate 32-column chunks); their partial sums meet in shared
+// memory (red[0..2*kBlockM) for the mean, red[2*kBlockM..4*kBlockM) for M2).
+// Pass 1 forms h = round_C(alpha * acc + beta * C + bias) (0 past column N),
+// sums it and writes it back over the accumulator in TMEM: the later passes
+// read TMEM only, and C (the residual) is read once, by the thread that
+// overwrites it.  Pass 2 sums the squared deviations from the tile mean
+// (two-pass, no cancellation) and, when a row spans several tiles, stores h.
+// Pass 3 -- the row whole in this tile -- stores
+// y = (h - mean) / sqrt(M2 / N + eps) * gamma + shift; otherwise the tile's
+// (sum, M2) of each row go to ln_stats for the row pass.
+template <typename OutT, int BN>
+__device__ __forceinline__ void ln_tile(const TcParams& p, uint32_t t_row, int32_t row,
+                                        int row_in_cta, int half, int32_t col0, int32_t tn,
+                                        float* red) {
+    const bool rv = row < p.M;
+    const int32_t nvalid = (p.N - col0) < BN ? (p.N - col0) : BN;
+    float s = 0.0f;
+    #pragma unroll 1
+    for (int ch = half; ch < BN / 32; ch += 2) {
+        float v[32];
+        ln_chunk_h<OutT>(p, t_row + ch * 32, row, rv, col0 + ch * 32, v);
+        #pragma unroll
+        for (int j = 0; j < 32; ++j) s += v[j];
+        uint32_t r[32];
+        #pragma unroll
+        for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(v[j]);
+        __syncwarp();                              // tcgen05.st is warp-collective
+        tmem_st_32x32b_x32(t_row + ch * 32, r);
+    }
+    tmem_st_wait();                                // h is in TMEM before it is read back
+    red[half * kBlockM + row_in_cta] = s;
+    epilogue_bar_sync();
+    const float mean = (red[row_in_cta] + red[kBlockM + row_in_cta]) / static_cast<float>(nvalid);
+    float q = 0.0f;
+    #pragma unroll 1
+    for (int ch = half; ch < BN / 32; ch += 2) {
+        float v[32];
+        const int32_t c0 = col0 + ch * 32;
+        tmem_row32(t_row + ch * 32, v);
+        #pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            const float d = (c0 + j < p.N) ? v[j] - mean : 0.0f;
+            q = fmaf(d, d, q);
+        }
+        if (!p.ln_fused && rv && c0 < p.N) store_out32<OutT>(p, row, c0, v);
+    }
+    red[(2 + half) * kBlockM + row_in_cta] = q;
+    epilogue_bar_sync();
+    const float m2 = red[2 * kBlockM + row_in_cta] + red[3 * kBlockM + row_in_cta];
+    if (p.ln_fused) {
+        const float rstd = 1.0f / sqrtf(m2 / static_cast<float>(nvalid) + p.ln_eps);
+        #pragma unroll 1
+        for (int ch = half; ch < BN / 32; ch += 2) {
+            const int32_t c0 = col0 + ch * 32;
+            float v[32];
+            tmem_row32(t_row + ch * 32, v);
+            if (rv && c0 < p.N) {
+                #pragma unroll
+                for (int j = 0; j < 32; ++j) v[j] = (v[j] - mean) * rstd;
+                if (p.ln_gamma != nullptr) {
+                    float g[32];
+                    load_col_vec32(p.ln_gamma, p.ln_dtype, c0, p.N, g);
+                    #pragma unroll
+                    for (int j = 0; j < 32; ++j) v[j] *= g[j];
+                }
+                if (p.ln_shift != nullptr) {
+                    float t[32];
+                    load_col_vec32(p.ln_shift, p.ln_dtype, c0, p.N, t);
+                    #pragma unroll
+                    for (int j = 0; j < 32; ++j) v[j] += t[j];
+                }
+                store_out32<OutT>(p, row, c0, v);
+            }
+        }
+    } else if (half == 0 && rv) {
+        const float sum = red[row_in_cta] + red[kBlockM + row_in_cta];
+        p.ln_stats[static_cast<int64_t>(row) * p.tiles_n + tn] = make_float2(sum, m2);
+    }
+}
+
+template <int CG, int BN, typename OutT, int ES, int EPI = kEpiPlain>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ TcParams p) {
     static_assert(BN == 64 || BN == 128 || BN == 256, "BN");
+    static_assert(EPI == kEpiPlain || EPI == kEpiLayerNorm, "epilogue");
     static_assert(CG == 1 || (CG == 2 && BN >= 128), "CG");
     static_assert(ES == 2 || ES == 4, "element size");
     constexpr int kBlockK = Elem<ES>::kBlockK;
@@ -716,6 +928,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         SegmentIter it(p, unit, units);
         Segment sg;
         __shared__ int wait_ok;
+        // LayerNorm: the two warps of each row exchange partial sums here
+        __shared__ float ln_red[EPI == kEpiLayerNorm ? 4 * kBlockM : 1];
         while (it.next(p, sg)) {
             const uint32_t buf = acc_i & 1u;
             int32_t tm, tn;
@@ -812,48 +1026,54 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tmem_st_wait();
                 }
             }
+            if constexpr (EPI == kEpiLayerNorm) ln_prefetch_residual<OutT, BN>(p, row, half, col0);
             ok = ok && wait_or_abort(&acc_full[buf], (acc_i >> 1) & 1u, &abort_flag, p.wait_limit_ns);
-            if (p.stream_k) ok = epilogue_all(ok);        // stream-K uses named barriers below
+            // stream-K and LayerNorm use named barriers below
+            if (p.stream_k || EPI == kEpiLayerNorm) ok = epilogue_all(ok);
             if (!ok) {
                 record_error(p, kErrTimeoutEpilogue, &abort_flag);
                 break;
             }
             tc_fence_after_sync();
-
-            float* my_slot = (sg.slot >= 0 && !finisher)
-                                 ? p.partials + static_cast<int64_t>(sg.slot) * BM * BN
-                                 : nullptr;
-            #pragma unroll 1
-            for (int ch = half; ch < BN / 32; ch += 2) {
-                uint32_t r[32];
-                __syncwarp();                      // tcgen05.ld is warp-collective
-                tmem_ld_32x32b_x32(t_row + ch * 32, r);
-                tmem_ld_wait();
-                float v[32];
-                #pragma unroll
-                for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
-                if (finisher) {
-                    uint32_t o[32];
-                    __syncwarp();
-                    tmem_ld_32x32b_x32(t_spare + ch * 32, o);
+            if constexpr (EPI == kEpiLayerNorm) {
+                // data-parallel only (the planner gives LayerNorm no stream-K)
+                ln_tile<OutT, BN>(p, t_row, row, row_in_cta, half, col0, tn, ln_red);
+            } else {
+                float* my_slot = (sg.slot >= 0 && !finisher)
+                                     ? p.partials + static_cast<int64_t>(sg.slot) * BM * BN
+                                     : nullptr;
+                #pragma unroll 1
+                for (int ch = half; ch < BN / 32; ch += 2) {
+                    uint32_t r[32];
+                    __syncwarp();                      // tcgen05.ld is warp-collective
+                    tmem_ld_32x32b_x32(t_row + ch * 32, r);
                     tmem_ld_wait();
+                    float v[32];
                     #pragma unroll
-                    for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(o[j]) + v[j];
-                }
-                const int32_t c0 = col0 + ch * 32;
-                if (my_slot == nullptr) {
-                    store_chunk<OutT>(p, row, c0, v);
-                } else if (p.c_cs == 1) {
-                    // raw FP32 sums, laid out along C's contiguous direction:
-                    // [row][col] when C rows are contiguous (c_cs == 1),
-                    // [col][row] otherwise, so every warp store is coalesced
-                    float4* dst = reinterpret_cast<float4*>(my_slot + row_in_tile * BN + ch * 32);
-                    #pragma unroll
-                    for (int q = 0; q < 8; ++q)
-                        dst[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-                } else {
-                    #pragma unroll
-                    for (int j = 0; j < 32; ++j) my_slot[(ch * 32 + j) * BM + row_in_tile] = v[j];
+                    for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+                    if (finisher) {
+                        uint32_t o[32];
+                        __syncwarp();
+                        tmem_ld_32x32b_x32(t_spare + ch * 32, o);
+                        tmem_ld_wait();
+                        #pragma unroll
+                        for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(o[j]) + v[j];
+                    }
+                    const int32_t c0 = col0 + ch * 32;
+                    if (my_slot == nullptr) {
+                        store_chunk<OutT>(p, row, c0, v);
+                    } else if (p.c_cs == 1) {
+                        // raw FP32 sums, laid out along C's contiguous direction:
+                        // [row][col] when C rows are contiguous (c_cs == 1),
+                        // [col][row] otherwise, so every warp store is coalesced
+                        float4* dst = reinterpret_cast<float4*>(my_slot + row_in_tile * BN + ch * 32);
+                        #pragma unroll
+                        for (int q = 0; q < 8; ++q)
+                            dst[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+                    } else {
+                        #pragma unroll
+                        for (int j = 0; j < 32; ++j) my_slot[(ch * 32 + j) * BM + row_in_tile] = v[j];
+                    }
                 }
             }
             tc_fence_before_sync();

@@ -1,7 +1,8 @@
 // kern_inst.cuh -- instantiates the tcgen05 GEMM for one input element size
 // (KERN_ES bytes: 2 for FP16/BF16, 4 for FP32 used as TF32) and one output
 // type (KERN_OUT_T): single-CTA tiles of width 64/128/256 and CTA-pair tiles
-// of width 256, behind a plain launcher.
+// of width 256, behind a plain launcher -- and, for 16-bit inputs, the
+// LayerNorm-epilogue variants (single-CTA 128/256, CTA-pair 256).
 #pragma once
 #include <mutex>
 
@@ -12,9 +13,9 @@
 
 namespace gemm103 {
 
-template <int CG, int BN>
+template <int CG, int BN, int EPI = kEpiPlain>
 static cudaError_t launch_tc_cfg(const TcLaunch& l) {
-    auto kern = gemm_tc_kernel<CG, BN, KERN_OUT_T, KERN_ES>;
+    auto kern = gemm_tc_kernel<CG, BN, KERN_OUT_T, KERN_ES, EPI>;
     {
         // The dynamic shared-memory limit is raised once per size (a host
         // call worth avoiding on every launch of a microsecond-scale GEMM).
@@ -83,6 +84,20 @@ static cudaError_t launch_tc_cfg(const TcLaunch& l) {
 
 cudaError_t GEMM103_CAT(launch_tc_, KERN_SUFFIX)(const TcLaunch& l) {
     if (l.esize != KERN_ES) return cudaErrorInvalidValue;
+    if (l.epi == kEpiLayerNorm) {
+        if constexpr (KERN_ES == 2) {
+            if (l.cta_group == 2)
+                return l.block_n == 256 ? launch_tc_cfg<2, 256, kEpiLayerNorm>(l)
+                                        : cudaErrorInvalidValue;
+            switch (l.block_n) {
+                case 128: return launch_tc_cfg<1, 128, kEpiLayerNorm>(l);
+                case 256: return launch_tc_cfg<1, 256, kEpiLayerNorm>(l);
+                default: return cudaErrorInvalidValue;
+            }
+        }
+        return cudaErrorInvalidValue;
+    }
+    if (l.epi != kEpiPlain) return cudaErrorInvalidValue;
     if (l.cta_group == 2) {
         switch (l.block_n) {
             case 256: return launch_tc_cfg<2, 256>(l);

@@ -16,6 +16,7 @@ struct TcLaunch {
     int cta_group;      // 1: single-CTA tiles, 2: CTA-pair tiles
     int block_n;
     int esize;          // input element bytes: 2 (FP16/BF16) or 4 (FP32 used as TF32)
+    int epi;            // kEpiPlain or kEpiLayerNorm (16-bit inputs only)
     size_t smem_bytes;
     cudaStream_t stream;
 };

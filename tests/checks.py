@@ -147,3 +147,80 @@ def compare_softmax(gpu_vals, gpu_codes, R, X, y_dtype, oracle_codes=None):
     stats = {"n": int(ok.size), "fail": int((~ok).sum()),
              "max_rel_err": float(np.max(rel)) if rel.size else 0.0}
     return stats, ~ok
+
+
+U32 = 2.0 ** -24          # unit roundoff of binary32
+
+
+def layernorm_bound(H, S, Cin_vals, bias_vals, gamma_vals, shift_vals, alpha, beta, c_dtype,
+                    eps, exact_h=False):
+    """Per-element bound on |y_gpu - y| for LayerNorm after the linear layer,
+    before the output's own rounding.  H, S: the oracle's h (as C's type holds
+    it) and |product| sums, one row of N per selected row.
+
+    1. h on the GPU is round_C(v) with |v - h_exact| <= a = the GEMM's FP32
+       rule 1e-5 * (|alpha| S + |beta c| + |bias|) + 1e-6, so
+       |h_gpu - H| <= e = a + ulp_C(|H| + a)  (0 for exact_h: integer inputs
+       whose FP32 sums are exact).
+    2. Through the row statistics: mean moves by at most mean(e); the biased
+       variance by dv = (2/N) sum |h - mu| e + (1/N) sum e^2; sigma by at most
+       dv / (sigma + sigma_lo), sigma_lo = sqrt(max(var - dv, 0) + eps).
+       y - shift = gamma (h - mu) / sigma moves by
+       |gamma| ((e + mean(e)) / sigma_lo + |h - mu| dv / (sigma sigma_lo (sigma + sigma_lo))).
+    3. The FP32 evaluation on the GPU (with the GEMM rule for an FP32 sum of
+       n terms: 1e-5 of the sum of magnitudes): mean off by
+       dm = 1e-5 mean|h| + 1e-6, M2 relatively by 1e-5 + (dm/sigma)^2, then
+       1/sqrt and three products, 3 roundings each:
+       |gamma| (dm / sigma + |z| (0.5e-5 + (dm/sigma)^2 + 4u)) + 3u (|gamma z| + |shift|).
+    """
+    H = np.asarray(H, dtype=np.float64)
+    n = H.shape[1]
+    a = REL * (abs(alpha) * S) + ABS
+    if beta != 0 and Cin_vals is not None:
+        a = a + REL * np.abs(beta * Cin_vals)
+    if bias_vals is not None:
+        a = a + REL * np.abs(bias_vals)
+    if exact_h:
+        e = np.zeros_like(H)
+    elif c_dtype == F32:
+        e = a + U32 * 2 * (np.abs(H) + a)
+    else:
+        e = a + ulp_of(np.abs(H) + a, c_dtype)
+    mu = H.mean(axis=1, keepdims=True)
+    dev = np.abs(H - mu)
+    var = (dev * dev).mean(axis=1, keepdims=True)
+    sigma = np.sqrt(var + eps)
+    ebar = e.mean(axis=1, keepdims=True)
+    dv = 2.0 * (dev * e).mean(axis=1, keepdims=True) + (e * e).mean(axis=1, keepdims=True)
+    sigma_lo = np.sqrt(np.maximum(var - dv, 0.0) + eps)
+    g = np.ones_like(H) if gamma_vals is None else np.abs(np.asarray(gamma_vals))[None, :n]
+    t = np.zeros_like(H) if shift_vals is None else np.abs(np.asarray(shift_vals))[None, :n]
+    prop = g * ((e + ebar) / sigma_lo + dev * dv / (sigma * sigma_lo * (sigma + sigma_lo)))
+    dm = REL * np.abs(H).mean(axis=1, keepdims=True) + ABS
+    z = dev / sigma
+    rm = (dm / sigma) ** 2
+    arith = g * (dm / sigma + z * (0.5 * REL + rm + 4 * U32)) + 3 * U32 * (g * z + t)
+    return prop + arith
+
+
+def compare_layernorm(gpu_vals, gpu_codes, Y, bound, y_dtype, oracle_codes=None):
+    """FP32 output: |y_gpu - y| <= bound.  FP16/BF16 output: within one ulp
+    of the correctly rounded oracle value, or |y_gpu - y| <= bound plus one
+    output ulp at |y| + bound."""
+    err = np.abs(gpu_vals - Y)
+    if y_dtype == F32:
+        ok = err <= bound + U32 * np.abs(Y)
+        stats = {}
+    else:
+        dist = np.abs(_ordered(gpu_codes) - _ordered(oracle_codes))
+        strict = dist <= 1
+        ok = strict | (err <= bound + ulp_of(np.abs(Y) + bound, y_dtype))
+        stats = {"strict_1ulp_frac": float(strict.mean()) if strict.size else 1.0,
+                 "max_ulp": int(dist.max()) if dist.size else 0}
+    ok &= np.isfinite(gpu_vals)
+    stats["n"] = int(ok.size)
+    stats["fail"] = int((~ok).sum())
+    with np.errstate(divide="ignore", invalid="ignore"):
+        r = np.where(bound > 0, err / bound, 0.0)
+    stats["max_err_over_bound"] = float(np.max(r)) if r.size else 0.0
+    return stats, ~ok

@@ -278,3 +278,62 @@ def test_create_fails_cleanly_without_gpu():
     assert lib.gemm_destroy(None) == 0
     assert lib.gemm_sync(None, None) == 1
     assert lib.gemm_run(None, "N", "N", 1, 1, 1, 1.0, 16, 1, 16, 1, 0.0, 16, 1, F16F32) == 1
+
+
+# ------------------------------------------------ LayerNorm after the linear layer
+
+def _ln_plan(M, N, K, dts=(DT_BF16, DT_BF16, DT_BF16), num_sms=152, **kw):
+    args = dict(bias=0x100, bias_dtype=DT_BF16, gamma=0x100, shift=0x100, ln_dtype=DT_F32,
+                eps=1e-5)
+    args.update(kw)
+    return lib.gemm_layernorm_plan_query("N", "T", M, N, K, 1.0, 0x100, K, 0x100, K, 1.0, 0x100,
+                                         N, dts, num_sms=num_sms, **args)
+
+
+def test_layernorm_plan_whole_rows_fused():
+    """Rows of up to 256 columns are normalised inside the epilogue: one tile
+    column, no stream-K, never the swapped skinny path."""
+    for M, N, K, path, bn in [(300, 100, 200, "tiled_1sm", 128), (517, 256, 333, "tiled_1sm", 256),
+                              (40, 200, 8192, "tiled_1sm", 256),
+                              (20000, 256, 192, "tiled_2sm", 256),
+                              (20000, 128, 192, "tiled_1sm", 128)]:
+        st, p = _ln_plan(M, N, K)
+        assert st == 0, (M, N, K)
+        assert p["ln_fused"] == 1 and p["tiles_n"] == 1, p
+        assert (p["path_name"], p["block_n"]) == (path, bn), (M, N, K, p)
+        assert p["sk_len"] == 0 and p["swap_ab"] == 0, p
+
+
+def test_layernorm_plan_row_pass():
+    """Wider rows: per-tile (mean, M2) in the workspace, 8 bytes per row and
+    tile column; tiles of 128 or 256 columns; no stream-K even for long K."""
+    for M, N, K in [(333, 1000, 500), (40, 3000, 700), (8192, 4096, 4096), (64, 16384, 8192),
+                    (8192, 1024, 320)]:
+        st, p = _ln_plan(M, N, K)
+        assert st == 0
+        assert p["ln_fused"] == 0 and p["tiles_n"] >= 2, p
+        assert p["block_n"] in (128, 256) and p["sk_len"] == 0 and p["swap_ab"] == 0, p
+        assert p["workspace_bytes"] >= M * p["tiles_n"] * 8, p
+        st, q = lib.gemm_plan_query("N", "T", M, N, K, 1.0, 0x100, K, 0x100, K, 1.0, 0x100, N,
+                                    (DT_BF16, DT_BF16, DT_BF16))
+        assert st == 0
+
+
+def test_layernorm_plan_rejects():
+    assert _ln_plan(64, 64, 64, eps=0.0)[0] == 1
+    assert _ln_plan(64, 64, 64, eps=-1e-5)[0] == 1
+    assert _ln_plan(64, 64, 64, eps=float("nan"))[0] == 1
+    assert _ln_plan(64, 64, 64, eps=float("inf"))[0] == 1
+    assert _ln_plan(64, 64, 64, ln_dtype=5)[0] == 1
+    assert _ln_plan(64, 64, 64, bias_dtype=-1)[0] == 1
+    # without gamma and shift their dtype is not read
+    assert _ln_plan(64, 64, 64, gamma=0, shift=0, ln_dtype=5)[0] == 0
+    assert _ln_plan(64, 64, 64, dts=TF32)[0] == 2
+    plan = lib.Plan()
+    assert lib.lib.gemm_layernorm_plan_query(b"N", b"T", 64, 64, 64, 1.0, 0x100, 64, 0x100, 64,
+                                             0.0, 0x100, 64, lib.Dtypes(0, 0, 0), None, 152,
+                                             232448, ctypes.byref(plan), None) == 1
+    # the GEMM's own checks still apply
+    assert _ln_plan(-1, 64, 64)[0] == 1
+    st, p = _ln_plan(0, 64, 64)
+    assert st == 0 and p["path_name"] == "noop"

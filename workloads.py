@@ -33,6 +33,7 @@ import torch
 DT_F16, DT_BF16, DT_F32 = 0, 1, 2
 TORCH_DTYPE = {DT_F16: torch.float16, DT_BF16: torch.bfloat16, DT_F32: torch.float32}
 DT_NAME = {DT_F16: "f16", DT_BF16: "bf16", DT_F32: "f32"}
+DT_OF = {v: k for k, v in TORCH_DTYPE.items()}
 
 
 @dataclasses.dataclass(frozen=True)
