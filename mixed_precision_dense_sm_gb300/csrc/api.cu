@@ -57,6 +57,7 @@ struct Plan {
     int64_t K;
     int64_t c_rs, c_cs;
     int32_t k_blocks, tiles_m, tiles_n;
+    int32_t kc;         // K chunks (128-byte rows of K) per pipeline stage
     int32_t cta_group;
     int32_t esize;      // input element bytes: 2 (FP16/BF16) or 4 (FP32 as TF32)
     int32_t sk_len, sk_max_seg;
@@ -109,7 +110,8 @@ gemm_status_t check_args(char transA, char transB, int64_t M, int64_t N, int64_t
 gemm_status_t make_plan(char transA, char transB, int64_t M, int64_t N, int64_t K, float alpha,
                         const void* A, int64_t lda, const void* B, int64_t ldb, float beta,
                         const void* C, int64_t ldc, gemm_dtypes_t dt, int32_t num_sms,
-                        int32_t smem_optin, Plan& pl, bool allow_swap = true, bool ln = false) {
+                        int32_t smem_optin, Plan& pl, bool allow_swap = true, bool ln = false,
+                        int32_t max_kc = kMaxKc) {
     gemm_status_t st = check_args(transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, dt);
     if (st != GEMM_OK) return st;
     if (num_sms < 1 || smem_optin < 64 * 1024) return GEMM_ERR_INVALID_VALUE;
@@ -158,9 +160,10 @@ gemm_status_t make_plan(char transA, char transB, int64_t M, int64_t N, int64_t 
         pl.c_rs = ldc;
         pl.c_cs = 1;
     }
-    // One 128-byte swizzle row of K per stage: 64 16-bit or 32 32-bit elements.
+    // A K chunk is one 128-byte swizzle row of K: 64 16-bit or 32 32-bit
+    // elements.  A stage holds kc chunks (below).
     const int32_t esize = in_elem_bytes(dt.a);
-    const int64_t block_k = 128 / esize;
+    const int64_t chunk_k = 128 / esize;
     pl.esize = esize;
     for (OperandDesc* o : {&pl.a, &pl.b}) {
         o->pack = !aligned16(o->ptr) || ((o->ld * esize) % 16) != 0;
@@ -189,6 +192,14 @@ gemm_status_t make_plan(char transA, char transB, int64_t M, int64_t N, int64_t 
     pl.pack_b_bytes = pl.b.pack ? pl.b.rows * pl.b.packed_ld * esize : 0;
     pl.pub.c_vector = (!swap && aligned16(C) && (ldc * (int64_t)out_elem_bytes(dt.c)) % 16 == 0) ? 1 : 0;
 
+    // Two K chunks per stage halve the TMA operations per MMA (the TMA unit
+    // completes about one box per 160 ns per SM, nearly independent of the
+    // box's size).  A K-major operand is then read through a 3-D view
+    // (chunk, rows, chunk index) whose chunks must not run past K: one chunk
+    // per stage unless K is a whole number of chunks.  The choice is final
+    // once the tile width is known (below: at least 3 stages must fit).
+    const bool kc2_ok = max_kc >= 2 && !((!pl.a.mn_major || !pl.b.mn_major) && K % chunk_k != 0);
+    const int64_t k_chunks = ceil_div(K, chunk_k);
     // Tile shape.  Enough 256 x 256 tiles to give every SM pair one: CTA-pair
     // tiles (tcgen05 cta_group::2).  Otherwise single-CTA 128-row tiles, 256
     // columns wide when that still fills the GPU, else narrower ones with
@@ -199,9 +210,8 @@ gemm_status_t make_plan(char transA, char transB, int64_t M, int64_t N, int64_t 
     // single-CTA stream-K over the widest tiles balances the work instead
     // (the fix-up of a split tile costs one FP32 tile through L2, small beside
     // a K loop of kLongK or more k-blocks).
-    pl.k_blocks = static_cast<int32_t>(ceil_div(K, block_k));
     // (LayerNorm needs each tile's rows complete in one CTA: no stream-K)
-    const bool long_k = !swap && !ln && pl.k_blocks >= kLongK;
+    const bool long_k = !swap && !ln && k_chunks >= kLongK;
     auto wave_fill = [](int64_t tiles, int64_t units) {
         return static_cast<double>(tiles) / static_cast<double>(ceil_div(tiles, units) * units);
     };
@@ -252,14 +262,19 @@ gemm_status_t make_plan(char transA, char transB, int64_t M, int64_t N, int64_t 
     pl.tiles_n = static_cast<int32_t>(tiles_n);
     pl.pub.block_m = static_cast<int32_t>(block_m);
     pl.pub.block_n = bn;
-    pl.pub.block_k = static_cast<int32_t>(block_k);
     pl.pub.num_tiles = static_cast<int32_t>(tiles);
 
-    const uint32_t stage_bytes = kATileBytes + static_cast<uint32_t>(bn / cg) * 128u;
+    const uint32_t chunk_bytes = kATileBytes + static_cast<uint32_t>(bn / cg) * 128u;
     const int64_t barrier_bytes = 256;
     // static shared memory of the kernel: flags, and the LayerNorm exchange
     const int64_t static_bytes = 64 + (ln ? 4 * kBlockM * 4 : 4);
-    int64_t stages = (smem_optin - 1024 - barrier_bytes - static_bytes) / stage_bytes;
+    const int64_t avail = smem_optin - 1024 - barrier_bytes - static_bytes;
+    pl.kc = (kc2_ok && avail / (2 * static_cast<int64_t>(chunk_bytes)) >= 3) ? 2 : 1;
+    const int64_t block_k = chunk_k * pl.kc;
+    pl.k_blocks = static_cast<int32_t>(ceil_div(K, block_k));
+    pl.pub.block_k = static_cast<int32_t>(block_k);
+    const uint32_t stage_bytes = static_cast<uint32_t>(pl.kc) * chunk_bytes;
+    int64_t stages = avail / stage_bytes;
     if (stages > kMaxStages) stages = kMaxStages;
     if (stages < 2) return GEMM_ERR_NOT_SUPPORTED;
     pl.pub.stages = static_cast<int32_t>(stages);
@@ -271,7 +286,7 @@ gemm_status_t make_plan(char transA, char transB, int64_t M, int64_t N, int64_t 
     // long in K; the swapped skinny path (a weight-streaming GEMM) always uses it.
     const bool stream_k = !pairs && !ln && (tiles <= kMaxCounterTiles) && (work < INT32_MAX) &&
                           (balance_sk || ((tiles < num_sms) &&
-                           (swap ? pl.k_blocks >= 4 : (tiles < half_wave && long_k))));
+                           (swap ? k_chunks >= 4 : (tiles < half_wave && long_k))));
     if (stream_k) {
         int64_t G = num_sms < work ? num_sms : work;
         const int64_t L = ceil_div(work, G);
@@ -336,24 +351,45 @@ struct gemm_ctx {
 
 namespace {
 
-// 2-D tiled map over a stored matrix: dims {inner, outer}, row pitch in bytes,
-// a box of one 128-byte row (64 16-bit or 32 FP32 elements) by box_outer rows,
-// 128-byte swizzle, zero fill out of range.  FP32 is moved as plain FP32: the
-// tensor core itself takes it as TF32.
+// Tiled map over a stored matrix (row pitch ld elements), 128-byte swizzle,
+// zero fill out of range.  FP32 is moved as plain FP32: the tensor core itself
+// takes it as TF32.
+//  * chunks == 1: 2-D, dims {inner, outer}, a box of one 128-byte row (64
+//    16-bit or 32 FP32 elements) by box_outer rows.
+//  * chunks > 1 (K-major operands, inner a whole number of 128-byte chunks):
+//    3-D, dims {chunk, outer, inner / chunk} with the chunk index striding 128
+//    bytes along the row, a box of `chunks` chunks of box_outer rows -- in
+//    shared memory one swizzled box_outer x 128-byte tile per chunk, back to
+//    back.
 bool encode_operand(EncodeTiledFn encode, CUtensorMap* map, int32_t dtype, const void* ptr,
-                    int64_t inner, int64_t outer, int64_t ld, uint32_t box_outer) {
+                    int64_t inner, int64_t outer, int64_t ld, uint32_t box_outer,
+                    int32_t chunks = 1) {
     const int64_t es = in_elem_bytes(dtype);
-    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(outer)};
-    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld * es)};
-    const cuuint32_t box[2] = {static_cast<cuuint32_t>(128 / es), box_outer};
-    const cuuint32_t estr[2] = {1, 1};
+    const int64_t chunk = 128 / es;
     const CUtensorMapDataType ty = dtype == GEMM_F32    ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
                                    : dtype == GEMM_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
                                                         : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-    CUresult r = encode(map, ty,
-                           2, const_cast<void*>(ptr), dims, strides, box, estr,
-                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    CUresult r;
+    if (chunks == 1) {
+        const cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(outer)};
+        const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld * es)};
+        const cuuint32_t box[2] = {static_cast<cuuint32_t>(chunk), box_outer};
+        const cuuint32_t estr[2] = {1, 1};
+        r = encode(map, ty, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    } else {
+        if (inner % chunk != 0) return false;
+        const cuuint64_t dims[3] = {static_cast<cuuint64_t>(chunk), static_cast<cuuint64_t>(outer),
+                                    static_cast<cuuint64_t>(inner / chunk)};
+        const cuuint64_t strides[2] = {static_cast<cuuint64_t>(ld * es), 128u};
+        const cuuint32_t box[3] = {static_cast<cuuint32_t>(chunk), box_outer,
+                                   static_cast<cuuint32_t>(chunks)};
+        const cuuint32_t estr[3] = {1, 1, 1};
+        r = encode(map, ty, 3, const_cast<void*>(ptr), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    }
     return r == CUDA_SUCCESS;
 }
 
@@ -550,18 +586,21 @@ gemm_status_t enqueue_plan(const Plan& pl, EncodeTiledFn encode, int num_sms, ui
     std::memset(&l, 0, sizeof l);
     const int bn = pl.pub.block_n;
     const int cg = pl.cta_group;
-    // MN-major boxes are one 128-byte row of M/N by block_k rows of K.
-    const uint32_t mn_box = 128u / static_cast<uint32_t>(pl.esize);
+    // MN-major boxes are one 128-byte row of M/N by block_k rows of K;
+    // K-major ones kc chunks of 128 bytes of K by the tile's rows.
+    const uint32_t mn_box = static_cast<uint32_t>(pl.pub.block_k);
     bool ok;
     if (conv != nullptr) {
         ok = encode_conv_input(*conv, &l.tmA, dt.a) &&
              encode_conv_filter(encode, *conv, &l.tmB, dt.b, static_cast<uint32_t>(bn / cg));
     } else {
         ok = encode_operand(encode, &l.tmA, dt.a, a_ptr, pl.a.cols, pl.a.rows, pl.a.packed_ld,
-                            pl.a.mn_major ? mn_box : static_cast<uint32_t>(kBlockM));
+                            pl.a.mn_major ? mn_box : static_cast<uint32_t>(kBlockM),
+                            pl.a.mn_major ? 1 : pl.kc);
         ok = ok && encode_operand(encode, &l.tmB, dt.b, b_ptr, pl.b.cols, pl.b.rows,
                                   pl.b.packed_ld,
-                                  pl.b.mn_major ? mn_box : static_cast<uint32_t>(bn / cg));
+                                  pl.b.mn_major ? mn_box : static_cast<uint32_t>(bn / cg),
+                                  pl.b.mn_major ? 1 : pl.kc);
     }
     if (!ok) return GEMM_ERR_LAUNCH;
 
@@ -632,6 +671,7 @@ gemm_status_t enqueue_plan(const Plan& pl, EncodeTiledFn encode, int num_sms, ui
     l.cta_group = cg;
     l.block_n = bn;
     l.esize = pl.esize;
+    l.kc = pl.kc;
     l.smem_bytes = pl.smem_bytes;
     l.stream = stream;
 
@@ -714,8 +754,9 @@ gemm_status_t conv_plan(int64_t N, int64_t H, int64_t W, int64_t C, int64_t K, i
         return GEMM_ERR_NOT_SUPPORTED;
     }
     const int64_t kfake = R * S * ceil_div(C, 64) * 64;
+    // one chunk per stage: the im2col box holds 64 channels of one filter tap
     return make_plan('N', 'T', M, K, kfake, alpha, X, kfake, Wt, kfake, beta, Y, K, dt, num_sms,
-                     smem_optin, pl, false);
+                     smem_optin, pl, false, false, 1);
 }
 
 bool dtype16or32(int32_t t) { return t == GEMM_F16 || t == GEMM_BF16 || t == GEMM_F32; }

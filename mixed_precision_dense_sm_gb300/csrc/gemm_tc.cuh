@@ -56,15 +56,20 @@
 namespace gemm103 {
 
 constexpr int kBlockM = 128;      // tcgen05 M (cta_group::1)
-// One pipeline stage holds one 128-byte swizzle row of K per operand row:
-// 64 16-bit elements (kind::f16, K = 16 per MMA) or 32 FP32 elements used as
-// TF32 (kind::tf32, K = 8 per MMA); either way 4 MMAs per stage.
+// A K chunk is one 128-byte swizzle row of K per operand row: 64 16-bit
+// elements (kind::f16, K = 16 per MMA) or 32 FP32 elements used as TF32
+// (kind::tf32, K = 8 per MMA); either way 4 MMAs per chunk.  A pipeline stage
+// holds KC chunks (1 or 2, a template parameter of the kernel).  The TMA unit completes about one box per
+// 160 ns per SM whatever its size (8-32 KB), so two chunks per box halve the
+// TMA operations per MMA: K-major operands are then read through a 3-D map
+// (chunk of K, rows, chunk index) whose box spans both chunks, and MN-major
+// boxes span kc * 64 rows of K.
 template <int ES> struct Elem {
-    static constexpr int kBlockK = 128 / ES;        // K elements per stage
+    static constexpr int kChunkK = 128 / ES;        // K elements per chunk
     static constexpr int kUmmaK = 32 / ES;          // K per tcgen05.mma
     static constexpr int kMNChunk = 128 / ES;       // M/N elements per MN-major box row
-    static constexpr uint32_t kChunkBytes = kMNChunk * kBlockK * ES;   // one MN-major box
 };
+constexpr int kMaxKc = 2;
 constexpr int kThreads = 320;     // warp 0 producer, warp 1 MMA, warps 2-9 epilogue
 constexpr int kEpiWarps = 8;      // two per TMEM lane quarter, splitting the columns
 constexpr int kFinBatch = 2;      // stream-K finisher: partial slots loaded per batch
@@ -74,7 +79,7 @@ enum : int { kErrTimeoutProducer = 1, kErrTimeoutMma = 2, kErrTimeoutEpilogue = 
 
 struct TcParams {
     int32_t M, N;               // logical rows (M') / columns (N') of D
-    int32_t k_blocks;           // ceil(K / 64)
+    int32_t k_blocks;           // ceil(K / (KC * chunk)): pipeline stages of K per tile
     int32_t tiles_m, tiles_n, num_tiles;
     int32_t group_m;            // raster: tiles walk down group_m tile-rows at a time
     int32_t stages;
@@ -629,22 +634,29 @@ __device__ __forceinline__ void ln_tile(const TcParams& p, uint32_t t_row, int32
     }
 }
 
-template <int CG, int BN, typename OutT, int ES, int EPI = kEpiPlain>
+template <int CG, int BN, typename OutT, int ES, int EPI = kEpiPlain, int KC = 1>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ TcParams p) {
     static_assert(BN == 64 || BN == 128 || BN == 256, "BN");
     static_assert(EPI == kEpiPlain || EPI == kEpiLayerNorm, "epilogue");
+    static_assert(KC == 1 || KC == 2, "K chunks per stage");
     static_assert(CG == 1 || (CG == 2 && BN >= 128), "CG");
     static_assert(ES == 2 || ES == 4, "element size");
-    constexpr int kBlockK = Elem<ES>::kBlockK;
+    constexpr int kChunkK = Elem<ES>::kChunkK;
     constexpr int kUmmaK = Elem<ES>::kUmmaK;
     constexpr int kMNChunk = Elem<ES>::kMNChunk;
-    constexpr uint32_t kChunkBytes = Elem<ES>::kChunkBytes;
     constexpr int BM = kBlockM * CG;                      // rows per (pair) tile
     constexpr uint32_t kBRows = BN / CG;                  // B rows this CTA loads
-    constexpr uint32_t kBTileBytes = kBRows * 128;
-    constexpr uint32_t kStageBytes = kATileBytes + kBTileBytes;
+    // per stage: kc chunks of A (kBlockM rows) and of B (kBRows rows), each
+    // chunk a 128-byte-wide swizzled tile; an MN-major box is 128 bytes of
+    // M/N by kc * kChunkK rows of K
+    constexpr int kc = KC;
+    constexpr int32_t kBlockK = kc * kChunkK;             // K elements per stage
+    constexpr uint32_t kATile = static_cast<uint32_t>(kc) * kATileBytes;
+    constexpr uint32_t kBTile = static_cast<uint32_t>(kc) * kBRows * 128u;
+    constexpr uint32_t kStageBytes = kATile + kBTile;
+    constexpr uint32_t kChunkBytes = static_cast<uint32_t>(kBlockK) * 128u;   // one MN-major box
     constexpr uint32_t kTmemCols = 2 * BN;               // double-buffered accumulator
 
     extern __shared__ uint8_t smem_raw[];
@@ -735,9 +747,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int32_t mf = tm * BM + static_cast<int32_t>(r) * kBlockM;
                     const int32_t nf = tn * BN + static_cast<int32_t>(r * kBRows);
                     return static_cast<uint32_t>(a_parts(mf)) *
-                               (p.a_mn_major ? kChunkBytes : kATileBytes) +
+                               (p.a_mn_major ? kChunkBytes : kATile) +
                            static_cast<uint32_t>(b_parts(nf)) *
-                               (p.b_mn_major ? kChunkBytes : kBTileBytes);
+                               (p.b_mn_major ? kChunkBytes : kBTile);
                 };
                 const int32_t m0 = tm * BM + static_cast<int32_t>(rank) * kBlockM;
                 const int32_t n0 = tn * BN + static_cast<int32_t>(rank * kBRows);
@@ -765,7 +777,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     }
                     uint8_t* sa = smem + stage * kStageBytes;
-                    uint8_t* sb = sa + kATileBytes;
+                    uint8_t* sb = sa + kATile;
                     const int32_t k0 = kb * kBlockK;
                     if ((p.debug_flags & kDebugSkipFirstLoad) && armed == 0 && blockIdx.x == 0) {
                         // test hook: arm the slot, load nothing into it
@@ -784,7 +796,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const int32_t taps = p.k_blocks / p.conv_cblocks;
                         const int32_t cb = kb / taps;
                         const int32_t tap = kb - cb * taps;
-                        const int32_t c0 = cb * kBlockK;
+                        const int32_t c0 = cb * kChunkK;
                         const int32_t r = tap / p.conv_S;
                         const uint16_t ow = static_cast<uint16_t>((tap - r * p.conv_S) * p.conv_dil_w);
                         const uint16_t oh = static_cast<uint16_t>(r * p.conv_dil_h);
@@ -805,14 +817,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 tma_load_2d(sa + c * kChunkBytes, &tmA, &full[stage], m0 + kMNChunk * c,
                                             k0, pol_a);
                         } else if (na) {
-                            tma_load_2d(sa, &tmA, &full[stage], k0, m0, pol_a);
+                            if constexpr (kc == 1) tma_load_2d(sa, &tmA, &full[stage], k0, m0, pol_a);
+                            else tma_load_3d(sa, &tmA, &full[stage], 0, m0, kb * kc, pol_a);
                         }
                         if (p.b_mn_major) {
                             for (int c = 0; c < nb; ++c)
                                 tma_load_2d(sb + c * kChunkBytes, &tmB, &full[stage], n0 + kMNChunk * c,
                                             k0, pol_b);
                         } else if (nb) {
-                            tma_load_2d(sb, &tmB, &full[stage], k0, n0, pol_b);
+                            if constexpr (kc == 1) tma_load_2d(sb, &tmB, &full[stage], k0, n0, pol_b);
+                            else tma_load_3d(sb, &tmB, &full[stage], 0, n0, kb * kc, pol_b);
                         }
                     } else {
                         const uint32_t fb = map_to_rank(smem_addr(&full[stage]), 0);
@@ -822,14 +836,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 tma_load_2d_pair(sa + c * kChunkBytes, &tmA, fb, m0 + kMNChunk * c, k0,
                                                  pol_a);
                         } else if (na) {
-                            tma_load_2d_pair(sa, &tmA, fb, k0, m0, pol_a);
+                            if constexpr (kc == 1) tma_load_2d_pair(sa, &tmA, fb, k0, m0, pol_a);
+                            else tma_load_3d_pair(sa, &tmA, fb, 0, m0, kb * kc, pol_a);
                         }
                         if (p.b_mn_major) {
                             for (int c = 0; c < nb; ++c)
                                 tma_load_2d_pair(sb + c * kChunkBytes, &tmB, fb, n0 + kMNChunk * c, k0,
                                                  pol_b);
                         } else if (nb) {
-                            tma_load_2d_pair(sb, &tmB, fb, k0, n0, pol_b);
+                            if constexpr (kc == 1) tma_load_2d_pair(sb, &tmB, fb, k0, n0, pol_b);
+                            else tma_load_3d_pair(sb, &tmB, fb, 0, n0, kb * kc, pol_b);
                         }
                     }
                     ++armed;
@@ -864,10 +880,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool ok = true;
             const uint32_t a_lbo = p.a_mn_major ? kChunkBytes : 16u;
             const uint32_t b_lbo = p.b_mn_major ? kChunkBytes : 16u;
-            // advance per MMA: K-major 32 bytes within the 128-byte row;
-            // MN-major kUmmaK rows of 128 bytes
+            // advance per MMA: K-major 32 bytes within the 128-byte row, and
+            // the next chunk's tile after four; MN-major kUmmaK rows of 128 bytes
             const uint32_t a_kstep = p.a_mn_major ? kUmmaK * 128u : kUmmaK * ES;
             const uint32_t b_kstep = p.b_mn_major ? kUmmaK * 128u : kUmmaK * ES;
+            const uint32_t a_cstep = p.a_mn_major ? 4u * a_kstep : kATileBytes;
+            const uint32_t b_cstep = p.b_mn_major ? 4u * b_kstep : kBRows * 128u;
+
             const uint32_t smem_base = smem_addr(smem);
             while (ok && it.next(p, sg)) {
                 const uint32_t buf = acc_i & 1u;
@@ -885,11 +904,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     tc_fence_after_sync();
                     const uint32_t sa = smem_base + stage * kStageBytes;
-                    const uint32_t sb = sa + kATileBytes;
+                    const uint32_t sb = sa + kATile;
                     #pragma unroll
-                    for (int kk = 0; kk < kBlockK / kUmmaK; ++kk) {
-                        const uint64_t ad = smem_desc_sw128(sa + kk * a_kstep, a_lbo, 1024);
-                        const uint64_t bd = smem_desc_sw128(sb + kk * b_kstep, b_lbo, 1024);
+                    for (int kk = 0; kk < kc * 4; ++kk) {
+                        const uint32_t ka = (kk >> 2) * a_cstep + (kk & 3) * a_kstep;
+                        const uint32_t kb2 = (kk >> 2) * b_cstep + (kk & 3) * b_kstep;
+                        const uint64_t ad = smem_desc_sw128(sa + ka, a_lbo, 1024);
+                        const uint64_t bd = smem_desc_sw128(sb + kb2, b_lbo, 1024);
                         const uint32_t acc = (kb > sg.kb0 || kk > 0) ? 1u : 0u;
                         if constexpr (ES == 4) {
                             if constexpr (CG == 1) tc_mma_tf32(d_tmem, ad, bd, p.idesc, acc);

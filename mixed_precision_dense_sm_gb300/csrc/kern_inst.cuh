@@ -2,7 +2,9 @@
 // (KERN_ES bytes: 2 for FP16/BF16, 4 for FP32 used as TF32) and one output
 // type (KERN_OUT_T): single-CTA tiles of width 64/128/256 and CTA-pair tiles
 // of width 256, behind a plain launcher -- and, for 16-bit inputs, the
-// LayerNorm-epilogue variants (single-CTA 128/256, CTA-pair 256).
+// LayerNorm-epilogue variants (single-CTA 128/256, CTA-pair 256).  Each with
+// one K chunk per stage, and those whose three stages of two chunks fit in
+// shared memory (all but the single-CTA 256-wide tile) also with two.
 #pragma once
 #include <mutex>
 
@@ -13,9 +15,9 @@
 
 namespace gemm103 {
 
-template <int CG, int BN, int EPI = kEpiPlain>
+template <int CG, int BN, int EPI = kEpiPlain, int KC = 1>
 static cudaError_t launch_tc_cfg(const TcLaunch& l) {
-    auto kern = gemm_tc_kernel<CG, BN, KERN_OUT_T, KERN_ES, EPI>;
+    auto kern = gemm_tc_kernel<CG, BN, KERN_OUT_T, KERN_ES, EPI, KC>;
     {
         // The dynamic shared-memory limit is raised once per size (a host
         // call worth avoiding on every launch of a microsecond-scale GEMM).
@@ -82,16 +84,18 @@ static cudaError_t launch_tc_cfg(const TcLaunch& l) {
     }
 }
 
-cudaError_t GEMM103_CAT(launch_tc_, KERN_SUFFIX)(const TcLaunch& l) {
-    if (l.esize != KERN_ES) return cudaErrorInvalidValue;
+template <int KC>
+static cudaError_t launch_tc_kc(const TcLaunch& l) {
     if (l.epi == kEpiLayerNorm) {
         if constexpr (KERN_ES == 2) {
             if (l.cta_group == 2)
-                return l.block_n == 256 ? launch_tc_cfg<2, 256, kEpiLayerNorm>(l)
+                return l.block_n == 256 ? launch_tc_cfg<2, 256, kEpiLayerNorm, KC>(l)
                                         : cudaErrorInvalidValue;
             switch (l.block_n) {
-                case 128: return launch_tc_cfg<1, 128, kEpiLayerNorm>(l);
-                case 256: return launch_tc_cfg<1, 256, kEpiLayerNorm>(l);
+                case 128: return launch_tc_cfg<1, 128, kEpiLayerNorm, KC>(l);
+                case 256:
+                    if constexpr (KC == 1) return launch_tc_cfg<1, 256, kEpiLayerNorm, 1>(l);
+                    return cudaErrorInvalidValue;
                 default: return cudaErrorInvalidValue;
             }
         }
@@ -100,16 +104,25 @@ cudaError_t GEMM103_CAT(launch_tc_, KERN_SUFFIX)(const TcLaunch& l) {
     if (l.epi != kEpiPlain) return cudaErrorInvalidValue;
     if (l.cta_group == 2) {
         switch (l.block_n) {
-            case 256: return launch_tc_cfg<2, 256>(l);
+            case 256: return launch_tc_cfg<2, 256, kEpiPlain, KC>(l);
             default: return cudaErrorInvalidValue;
         }
     }
     switch (l.block_n) {
-        case 64: return launch_tc_cfg<1, 64>(l);
-        case 128: return launch_tc_cfg<1, 128>(l);
-        case 256: return launch_tc_cfg<1, 256>(l);
+        case 64: return launch_tc_cfg<1, 64, kEpiPlain, KC>(l);
+        case 128: return launch_tc_cfg<1, 128, kEpiPlain, KC>(l);
+        case 256:
+            if constexpr (KC == 1) return launch_tc_cfg<1, 256, kEpiPlain, 1>(l);
+            return cudaErrorInvalidValue;
         default: return cudaErrorInvalidValue;
     }
+}
+
+cudaError_t GEMM103_CAT(launch_tc_, KERN_SUFFIX)(const TcLaunch& l) {
+    if (l.esize != KERN_ES) return cudaErrorInvalidValue;
+    if (l.kc == 1) return launch_tc_kc<1>(l);
+    if (l.kc == 2) return launch_tc_kc<2>(l);
+    return cudaErrorInvalidValue;
 }
 
 }  // namespace gemm103

@@ -101,10 +101,37 @@ def test_plans_of_named_workloads():
         assert 2 <= p["stages"] <= 8
         cg = p["block_m"] // 128
         esize = 4 if workloads.WORKLOADS[n].ab_dtype == DT_F32 else 2
-        assert p["block_k"] * esize == 128          # one 128-byte swizzle row of K per stage
+        # one or two 128-byte swizzle rows (chunks) of K per stage
+        kc = p["block_k"] * esize // 128
+        assert p["block_k"] * esize in (128, 256)
         assert p["k_blocks"] == -(-workloads.WORKLOADS[n].K // p["block_k"])
-        stage = 128 * 128 + (p["block_n"] // cg) * 128
+        stage = kc * (128 * 128 + (p["block_n"] // cg) * 128)
         assert p["stages"] * stage + 1024 + 256 <= 232448
+        if kc == 2:
+            assert p["stages"] >= 3
+
+
+def test_two_k_chunks_per_stage():
+    """Two 128-byte rows of K per stage (half the TMA boxes per MMA) whenever
+    a K-major operand's K is a whole number of chunks and 3 stages fit;
+    otherwise one (a 3-D view would read past the row's end)."""
+    def p(ta, tb, M, N, K, dt=(DT_BF16, DT_BF16, DT_BF16)):
+        lda = K if ta == "N" else M
+        ldb = K if tb == "T" else N
+        st, q = lib.gemm_plan_query(ta, tb, M, N, K, 1.0, 256, lda, 256, ldb, 0.0, 256, N, dt)
+        assert st == 0
+        return q
+    assert p("N", "T", 8192, 4096, 4096)["block_k"] == 128           # CTA pairs: 3 x 64 KB
+    assert p("N", "T", 1024, 1024, 1024)["block_k"] == 128
+    assert p("N", "T", 1024, 1024, 1000)["block_k"] == 64            # K not a whole chunk
+    assert p("T", "N", 1024, 1024, 1000)["block_k"] == 128           # both MN-major: zero fill
+    assert p("N", "N", 1024, 1024, 1000)["block_k"] == 64            # A K-major
+    q = p("N", "T", 512, 3072, 4096)                                 # 1-SM 256 wide: 2 x 96 KB
+    assert (q["path_name"], q["block_n"], q["block_k"]) == ("tiled_1sm", 256, 64), q
+    assert p("N", "T", 100, 100, 128, (DT_F32, DT_F32, DT_F32))["block_k"] == 64   # TF32: 2 x 32
+    st, c = lib.conv2d_plan_query(32, 56, 56, 64, 64, 3, 3, (1, 1), (1, 1), (1, 1), 1.0, 256, 256,
+                                  0.0, 256, (DT_BF16, DT_BF16, DT_BF16))
+    assert st == 0 and c["block_k"] == 64                            # im2col: one tap per box
 
 
 def test_quick_paths_and_swap_rule():
@@ -142,12 +169,13 @@ def test_pack_rule_follows_16_byte_alignment():
 
 
 def test_tf32_plans():
-    """FP32 inputs (TF32): 32 elements of K per stage, the same tile shapes
-    and rules as 16-bit inputs, packing when rows are not 16-byte aligned
-    (a pitch that is not a multiple of 4 elements)."""
+    """FP32 inputs (TF32): chunks of 32 elements of K (two per stage when K
+    is a whole number of chunks), the same tile shapes and rules as 16-bit
+    inputs, packing when rows are not 16-byte aligned (a pitch that is not a
+    multiple of 4 elements)."""
     w = workloads.WORKLOADS["tf32_linear_8192x4096x4096_f32out"]
     p = plan(w)
-    assert p["path_name"] == "tiled_2sm" and p["block_k"] == 32 and p["k_blocks"] == 128
+    assert p["path_name"] == "tiled_2sm" and p["block_k"] == 64 and p["k_blocks"] == 64
     assert p["pack_a"] == 0 and p["pack_b"] == 0
     w = workloads.Workload("t", 100, 100, 100, "N", "N", DT_F32, DT_F32, 1.0, 0.0, "U", "U",
                            lda=104, ldb=102)
@@ -157,7 +185,7 @@ def test_tf32_plans():
     assert p["pack_a"] == 1 and p["pack_b"] == 1 and p["c_vector"] == 0
     w = workloads.Workload("t", 64, 16384, 8192, "N", "T", DT_F32, DT_F32, 1.0, 0.0, "U", "U")
     p = plan(w)
-    assert p["path_name"] == "skinny" and p["sk_len"] > 0 and p["k_blocks"] == 256
+    assert p["path_name"] == "skinny" and p["sk_len"] > 0 and p["k_blocks"] == 128
     # the same rules as the 16-bit path, for every tile width
     for M, N, K in [(1000, 1023, 777), (4096, 4096, 4096), (257, 129, 4096), (64, 1000, 513)]:
         a = plan(workloads.Workload("t", M, N, K, "N", "N", DT_F32, DT_F32, 1.0, 0.0, "U", "U",
@@ -166,7 +194,7 @@ def test_tf32_plans():
                                     lda=K + 8, ldb=N + 8))
         for key in ("path_name", "block_m", "block_n", "swap_ab", "tiles_m", "tiles_n"):
             assert a[key] == b[key], (M, N, K, key)
-        assert a["k_blocks"] == -(-K // 32)
+        assert a["k_blocks"] == -(-K // a["block_k"]) and a["block_k"] in (32, 64)
 
 
 def test_tf32_operands_stored_mn_major_are_transposed_first():
