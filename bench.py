@@ -303,8 +303,9 @@ def run_ours(args):
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     ws = workload_list(args.workload)
-    if args.epilogue and args.workload != "transformer_layer":
-        raise SystemExit("--epilogue applies to the transformer_layer workload")
+    if (args.epilogue or args.layernorm) and args.workload != "transformer_layer":
+        raise SystemExit("--epilogue / --layernorm apply to the transformer_layer workload")
+    fused = args.epilogue or args.layernorm
     g = lib.Gemm()
     stream = torch.cuda.current_stream()
     sh = stream.cuda_stream
@@ -312,7 +313,7 @@ def run_ours(args):
     bufs = []
     epis = []
     for j, w in enumerate(ws):
-        if args.epilogue:
+        if fused:
             # transformer MLP block: bias on every GEMM, GELU after the
             # up-projection, the residual added (beta = 1) after the down one
             w = dataclasses.replace(w, beta=1.0, c_dist="N1") if j == 2 else w
@@ -323,11 +324,18 @@ def run_ours(args):
         C = (inp.C.cuda() if inp.C is not None
              else torch.zeros((w.M, inp.ldc), dtype=cdt, device="cuda"))
         bufs.append((w, inp, A, B, C))
-        if args.epilogue:
+        if fused:
             gen = torch.Generator().manual_seed(100 + j)
             bias = (0.02 * torch.randn(w.N, generator=gen)).to(cdt).cuda()
             act = lib.ACT_GELU if j == 1 else lib.ACT_NONE
-            epis.append((bias, lib.dtype_code(bias.dtype), act))
+            if args.layernorm and j == 2:
+                # post-LN block: LayerNorm(x + W2 h + b2) over the 4096 columns,
+                # gamma = 1 + 0.1 N(0,1), shift = 0.1 N(0,1) in BF16
+                gamma = (1.0 + 0.1 * torch.randn(w.N, generator=gen)).to(cdt).cuda()
+                shift = (0.1 * torch.randn(w.N, generator=gen)).to(cdt).cuda()
+                epis.append(("ln", bias, gamma, shift))
+            else:
+                epis.append(("ex", bias, act))
         else:
             epis.append(None)
     del inp
@@ -340,26 +348,53 @@ def run_ours(args):
                                     num_sms=torch.cuda.get_device_properties(local).multi_processor_count)
         plans.append(p)
     # one gemm_tc_kernel launch per call, plus a pack pre-pass per operand
-    # that needs one (the stream-K finish runs inside the GEMM kernel)
-    launches_per_step = sum(1 + p["pack_a"] + p["pack_b"] for p in plans)
-    gemm_only = all(p["pack_a"] == 0 and p["pack_b"] == 0 for p in plans)
+    # that needs one (the stream-K finish runs inside the GEMM kernel), plus
+    # the LayerNorm row pass where rows span several tiles
+    ln_rows = [0] * len(bufs)
+    for i, (w, inp, A, B, C) in enumerate(bufs):
+        if epis[i] is not None and epis[i][0] == "ln":
+            bias, gamma, shift = epis[i][1:]
+            st, q = lib.gemm_layernorm_plan_query(
+                w.transA, w.transB, w.M, w.N, w.K, w.alpha, A.data_ptr(), inp.lda, B.data_ptr(),
+                inp.ldb, w.beta, C.data_ptr(), inp.ldc, (w.ab_dtype, w.ab_dtype, w.c_dtype),
+                bias=bias.data_ptr(), bias_dtype=lib.dtype_code(bias.dtype),
+                gamma=gamma.data_ptr(), shift=shift.data_ptr(),
+                ln_dtype=lib.dtype_code(gamma.dtype),
+                num_sms=torch.cuda.get_device_properties(local).multi_processor_count)
+            plans[i] = q
+            ln_rows[i] = 0 if q["ln_fused"] else 1
+    launches_per_step = sum(1 + p["pack_a"] + p["pack_b"] + r for p, r in zip(plans, ln_rows))
+    gemm_only = all(p["pack_a"] == 0 and p["pack_b"] == 0 for p in plans) and not any(ln_rows)
+
+    def launch(i, A, B, C, s):
+        """The step's call i through the C ABI on stream s (the plain GEMM, the
+        fused bias/activation epilogue, or LayerNorm after the linear layer)."""
+        w, inp = bufs[i][0], bufs[i][1]
+        dts = (w.ab_dtype, w.ab_dtype, w.c_dtype)
+        e = epis[i]
+        if e is None:
+            st = lib.gemm_run(g.h, w.transA, w.transB, w.M, w.N, w.K, w.alpha, A.data_ptr(),
+                              inp.lda, B.data_ptr(), inp.ldb, w.beta, C.data_ptr(), inp.ldc, dts, s)
+        elif e[0] == "ex":
+            bias, act = e[1], e[2]
+            st = lib.gemm_run_ex(g.h, w.transA, w.transB, w.M, w.N, w.K, w.alpha, A.data_ptr(),
+                                 inp.lda, B.data_ptr(), inp.ldb, w.beta, C.data_ptr(), inp.ldc,
+                                 dts, bias.data_ptr(), lib.dtype_code(bias.dtype), act, s)
+        else:
+            bias, gamma, shift = e[1:]
+            st = lib.gemm_run_layernorm(
+                g.h, w.transA, w.transB, w.M, w.N, w.K, w.alpha, A.data_ptr(), inp.lda,
+                B.data_ptr(), inp.ldb, w.beta, C.data_ptr(), inp.ldc, dts, bias.data_ptr(),
+                lib.dtype_code(bias.dtype), gamma.data_ptr(), shift.data_ptr(),
+                lib.dtype_code(gamma.dtype), 1e-5, s)
+        if st != 0:
+            raise lib.GemmError(st, "gemm_run")
 
     def step(events=None):
         for i, (w, inp, A, B, C) in enumerate(bufs):
             if events is not None:
                 events[i][0].record(stream)
-            if epis[i] is None:
-                st = lib.gemm_run(g.h, w.transA, w.transB, w.M, w.N, w.K, w.alpha, A.data_ptr(),
-                                  inp.lda, B.data_ptr(), inp.ldb, w.beta, C.data_ptr(), inp.ldc,
-                                  (w.ab_dtype, w.ab_dtype, w.c_dtype), sh)
-            else:
-                bias, bdt, act = epis[i]
-                st = lib.gemm_run_ex(g.h, w.transA, w.transB, w.M, w.N, w.K, w.alpha,
-                                     A.data_ptr(), inp.lda, B.data_ptr(), inp.ldb, w.beta,
-                                     C.data_ptr(), inp.ldc, (w.ab_dtype, w.ab_dtype, w.c_dtype),
-                                     bias.data_ptr(), bdt, act, sh)
-            if st != 0:
-                raise lib.GemmError(st, "gemm_run")
+            launch(i, A, B, C, sh)
             if events is not None:
                 events[i][1].record(stream)
 
@@ -424,6 +459,9 @@ def run_ours(args):
                                       for k in range(args.steps)) for i in range(len(bufs))]
         shape_ms = launch_ms
         launch_src = "events around each GEMM launch inside the timed region"
+        if any(ln_rows):
+            launch_src = ("events around each call inside the timed region; the LayerNorm "
+                          "call's time includes its row pass")
     achieved = sum(w.flops() for w in ws) / (sum(launch_ms) * 1e-3) / 1e12
     peaks, peak_src = load_peaks()
     bound = "tensor"
@@ -454,7 +492,8 @@ def run_ours(args):
     traffic = [committed_traffic(n) for n in ws_names]
     roof["traffic"] = (sum(traffic) / len(traffic)) if all(t is not None for t in traffic) else None
     roof["peak_source"] = f"{peak_src} ({'MEASURED_PEAKS.json' if peak_src == 'measured' else 'recipe fallback'})"
-    roof["kernel"] = "gemm_tc_kernel"
+    roof["kernel"] = "gemm_tc_kernel" + (" (+ ln_rows_stats_kernel in the LayerNorm call)"
+                                         if any(ln_rows) else "")
     roof["launch_ms"] = [round(x, 4) for x in launch_ms]
     roof["launch_ms_source"] = launch_src
     roof["per_launch_tflops"] = [round(w.flops() / (t * 1e-3) / 1e12, 1)
@@ -462,7 +501,7 @@ def run_ours(args):
     roof["per_shape_events_ms"] = [round(x, 4) for x in shape_ms]
 
     # e2e: host buffers through the C ABI; copies inside the timed region
-    e2e = run_e2e(lib, g, bufs, stream, args, world)
+    e2e = run_e2e(lib, g, bufs, stream, args, world, launch)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -474,7 +513,9 @@ def run_ours(args):
         cpu = {"value": round(f / t / 1e12, 6), "unit": "TFLOP/s", "cores": smp.threads,
                "kind": "oracle",
                "sample": f"{n} seeded output elements of each GEMM of the step, each a full "
-                         f"K-long dot product: {f / 1e9:.2f} GFLOP in {t:.1f} s",
+                         f"K-long dot product: {f / 1e9:.2f} GFLOP in {t:.1f} s" + (
+                             " (the fused epilogue's per-element work is not in the sample)"
+                             if fused else ""),
                "full_matrix_entry_point": {
                    "value": round(fr / tr / 1e12, 6), "unit": "TFLOP/s",
                    "sample": f"first {rows} rows of each GEMM (decode once, then the triple "
@@ -488,6 +529,9 @@ def run_ours(args):
                                       else "bf16"),
         "data": "synthetic",
         "config": {"workload": describe(args.workload, ws) + (
+                       "; fused epilogues: bias, bias + GELU, bias + residual (beta = 1) + "
+                       "LayerNorm over the 4096 columns (BF16 gamma, shift; eps 1e-5)"
+                       if args.layernorm else
                        "; fused epilogues: bias, bias + GELU, bias + residual (beta = 1)"
                        if args.epilogue else ""), "shapes": ws_names,
                    "l2": "no flush: each step touches "
@@ -507,7 +551,7 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
-def run_e2e(lib, g, bufs, stream, args, world):
+def run_e2e(lib, g, bufs, stream, args, world, launch):
     """Same step with inputs in pinned host memory: H2D copies, the GEMMs,
     D2H of every output, all inside the timed region.  Three streams pipeline
     the step: the inputs of GEMM i+1 go up and the output of GEMM i-1 comes
@@ -545,11 +589,7 @@ def run_e2e(lib, g, bufs, stream, args, world):
             ev_in[i].record(s_up)
             s_mm.wait_event(ev_in[i])
             s_mm.wait_event(ev_out[i])
-            st = lib.gemm_run(g.h, w.transA, w.transB, w.M, w.N, w.K, w.alpha, A.data_ptr(),
-                              inp.lda, B.data_ptr(), inp.ldb, w.beta, C.data_ptr(), inp.ldc,
-                              (w.ab_dtype, w.ab_dtype, w.c_dtype), s_mm.cuda_stream)
-            if st != 0:
-                raise lib.GemmError(st, "gemm_run")
+            launch(i, A, B, C, s_mm.cuda_stream)
             ev_mm[i].record(s_mm)
             s_down.wait_event(ev_mm[i])
             with torch.cuda.stream(s_down):
@@ -993,13 +1033,16 @@ def main():
     ap.add_argument("--epilogue", action="store_true",
                     help="fused epilogues of a transformer MLP block: bias on every GEMM, "
                          "GELU after the up-projection, residual add after the down-projection")
+    ap.add_argument("--layernorm", action="store_true",
+                    help="as --epilogue, with LayerNorm after the down-projection's residual "
+                         "add (a post-LN transformer block)")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         ap.error("--warmup must be >= 3")
     softmax = args.workload in workloads.SOFTMAX_WORKLOADS
     conv = args.workload in workloads.CONV_WORKLOADS
-    if (softmax or conv) and args.epilogue:
-        ap.error("--epilogue applies to the transformer_layer workload")
+    if (softmax or conv) and (args.epilogue or args.layernorm):
+        ap.error("--epilogue / --layernorm apply to the transformer_layer workload")
     if args.impl == "reference":
         (run_softmax_reference if softmax else run_conv_reference if conv else run_reference)(args)
     else:
