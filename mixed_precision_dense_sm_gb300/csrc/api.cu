@@ -591,8 +591,13 @@ gemm_status_t enqueue_plan(const Plan& pl, EncodeTiledFn encode, int num_sms, ui
     const uint32_t mn_box = static_cast<uint32_t>(pl.pub.block_k);
     bool ok;
     if (conv != nullptr) {
-        ok = encode_conv_input(*conv, &l.tmA, dt.a) &&
-             encode_conv_filter(encode, *conv, &l.tmB, dt.b, static_cast<uint32_t>(bn / cg));
+        ok = encode_conv_input(*conv, &l.tmA, dt.a);
+        if (pl.kc == 1)
+            ok = ok && encode_conv_filter(encode, *conv, &l.tmB, dt.b, static_cast<uint32_t>(bn / cg));
+        else
+            ok = ok && encode_operand(encode, &l.tmB, dt.b, conv->Wt, conv->R * conv->S * conv->C,
+                                      conv->K, conv->R * conv->S * conv->C,
+                                      static_cast<uint32_t>(bn / cg), pl.kc);
     } else {
         ok = encode_operand(encode, &l.tmA, dt.a, a_ptr, pl.a.cols, pl.a.rows, pl.a.packed_ld,
                             pl.a.mn_major ? mn_box : static_cast<uint32_t>(kBlockM),
@@ -657,6 +662,7 @@ gemm_status_t enqueue_plan(const Plan& pl, EncodeTiledFn encode, int num_sms, ui
     if (conv != nullptr) {
         p.conv = 1;
         p.conv_cblocks = static_cast<int32_t>(ceil_div(conv->C, 64));
+        p.conv_taps = static_cast<int32_t>(conv->R * conv->S);
         p.conv_S = static_cast<int32_t>(conv->S);
         p.conv_P = static_cast<int32_t>(conv->P);
         p.conv_Q = static_cast<int32_t>(conv->Q);
@@ -754,9 +760,12 @@ gemm_status_t conv_plan(int64_t N, int64_t H, int64_t W, int64_t C, int64_t K, i
         return GEMM_ERR_NOT_SUPPORTED;
     }
     const int64_t kfake = R * S * ceil_div(C, 64) * 64;
-    // one chunk per stage: the im2col box holds 64 channels of one filter tap
+    // Two chunks per stage take two im2col boxes (64 channels of one tap
+    // each) and one filter box, when C is a whole number of 64-channel blocks
+    // (the KRSC filter is then a K-major K x (R*S*C) matrix whose chunks never
+    // straddle taps); otherwise one chunk.
     return make_plan('N', 'T', M, K, kfake, alpha, X, kfake, Wt, kfake, beta, Y, K, dt, num_sms,
-                     smem_optin, pl, false, false, 1);
+                     smem_optin, pl, false, false, C % 64 == 0 ? kMaxKc : 1);
 }
 
 bool dtype16or32(int32_t t) { return t == GEMM_F16 || t == GEMM_BF16 || t == GEMM_F32; }

@@ -107,11 +107,15 @@ struct TcParams {
     int32_t bias_on_rows;       // 1: bias indexed by D' row (swapped problem), 0: by column
     int32_t act;                // 0 none, 1 ReLU, 2 GELU (erf), 3 SiLU
     // implicit-GEMM convolution (conv != 0): A is an im2col map over the
-    // NHWC input, B a 3-D map (C, R*S, K) over the KRSC filter; k-block kb is
-    // filter tap kb % (R*S) with channels from (kb / (R*S)) * 64 (16-bit
-    // inputs), D row m the output pixel (n, p, q) of m = (n*P + p)*Q + q
+    // NHWC input; chunk j of K (64 channels, 16-bit inputs) is filter tap
+    // j / cblocks with channels from (j % cblocks) * 64, chunks past the last
+    // tap read channels past C (zeros); D row m is the output pixel (n, p, q)
+    // of m = (n*P + p)*Q + q.  B is the KRSC filter: with one chunk per stage
+    // a 3-D map (C, R*S, K) loaded by (channel, tap); with two (C a multiple
+    // of 64) the filter as a K-major K x (R*S*C) matrix in chunks
     int32_t conv;
     int32_t conv_cblocks;       // ceil(C / 64)
+    int32_t conv_taps;          // R * S
     int32_t conv_S;             // filter width
     int32_t conv_P, conv_Q;     // output height and width
     int32_t conv_stride_h, conv_stride_w, conv_pad_h, conv_pad_w, conv_dil_h, conv_dil_w;
@@ -790,25 +794,41 @@ __global__ void __launch_bounds__(kThreads, 1)
                         continue;
                     }
                     if (p.conv) {
-                        // channels c0 .. c0 + 63 of filter tap (r, s): the taps
-                        // of one channel block run back to back, so the shifted
-                        // windows they read are in L2 together
-                        const int32_t taps = p.k_blocks / p.conv_cblocks;
-                        const int32_t cb = kb / taps;
-                        const int32_t tap = kb - cb * taps;
-                        const int32_t c0 = cb * kChunkK;
-                        const int32_t r = tap / p.conv_S;
-                        const uint16_t ow = static_cast<uint16_t>((tap - r * p.conv_S) * p.conv_dil_w);
-                        const uint16_t oh = static_cast<uint16_t>(r * p.conv_dil_h);
-                        if constexpr (CG == 1) {
-                            mbar_arrive_expect_tx(&full[stage], bytes);
-                            if (na) tma_load_im2col_4d(sa, &tmA, &full[stage], c0, cw, ch, cn, ow, oh, pol_a);
-                            if (nb) tma_load_3d(sb, &tmB, &full[stage], c0, tap, n0, pol_b);
-                        } else {
-                            const uint32_t fb = map_to_rank(smem_addr(&full[stage]), 0);
-                            if (rank == 0) mbar_arrive_expect_tx(&full[stage], bytes);
-                            if (na) tma_load_im2col_4d_pair(sa, &tmA, fb, c0, cw, ch, cn, ow, oh, pol_a);
-                            if (nb) tma_load_3d_pair(sb, &tmB, fb, c0, tap, n0, pol_b);
+                        // chunk j = kb * kc + q: channels c0 .. c0 + 63 of filter
+                        // tap (r, s), the channel blocks of one tap back to back
+                        uint32_t fb = 0;                       // the even CTA's barrier (pairs)
+                        if constexpr (CG == 2) fb = map_to_rank(smem_addr(&full[stage]), 0);
+                        if (CG == 1 || rank == 0) mbar_arrive_expect_tx(&full[stage], bytes);
+                        int32_t c0 = 0, tap = 0;
+                        #pragma unroll
+                        for (int q = 0; q < kc; ++q) {
+                            const int32_t j = kb * kc + q;
+                            tap = j / p.conv_cblocks;
+                            c0 = (j - tap * p.conv_cblocks) * kChunkK;
+                            if (tap >= p.conv_taps) {          // past the last tap: zeros
+                                tap = 0;
+                                c0 = p.conv_cblocks * kChunkK;
+                            }
+                            const int32_t r = tap / p.conv_S;
+                            const uint16_t ow = static_cast<uint16_t>((tap - r * p.conv_S) * p.conv_dil_w);
+                            const uint16_t oh = static_cast<uint16_t>(r * p.conv_dil_h);
+                            if (na) {
+                                if constexpr (CG == 1)
+                                    tma_load_im2col_4d(sa + q * kATileBytes, &tmA, &full[stage], c0, cw,
+                                                       ch, cn, ow, oh, pol_a);
+                                else
+                                    tma_load_im2col_4d_pair(sa + q * kATileBytes, &tmA, fb, c0, cw, ch,
+                                                            cn, ow, oh, pol_a);
+                            }
+                        }
+                        if (nb) {
+                            if constexpr (kc == 1) {
+                                if constexpr (CG == 1) tma_load_3d(sb, &tmB, &full[stage], c0, tap, n0, pol_b);
+                                else tma_load_3d_pair(sb, &tmB, fb, c0, tap, n0, pol_b);
+                            } else {
+                                if constexpr (CG == 1) tma_load_3d(sb, &tmB, &full[stage], 0, n0, kb * kc, pol_b);
+                                else tma_load_3d_pair(sb, &tmB, fb, 0, n0, kb * kc, pol_b);
+                            }
                         }
                     } else if constexpr (CG == 1) {
                         mbar_arrive_expect_tx(&full[stage], bytes);

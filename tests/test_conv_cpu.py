@@ -32,14 +32,18 @@ def test_output_dims_match_the_oracle(orc, geo):
 
 
 def test_plan_is_the_gemm_of_the_convolution():
+    # k_blocks counts pipeline stages: 9 taps x ceil(C / 64) chunks of 64
+    # channels, two chunks per stage when C is a multiple of 64
     st, p = plan(N=32, H=56, W=56, C=64, K=64)
-    assert st == OK and p["k_blocks"] == 9 and p["tiles_m"] * 128 >= 32 * 56 * 56
+    assert st == OK and p["k_blocks"] == 5 and p["block_k"] == 128
+    assert p["tiles_m"] * 128 >= 32 * 56 * 56
     assert p["swap_ab"] == 0 and p["pack_a"] == 0 and p["pack_b"] == 0
     assert p["a_mn_major"] == 0 and p["b_mn_major"] == 0
     st, p = plan(N=16, H=64, W=64, C=256, K=256)
-    assert st == OK and p["path_name"] == "tiled_2sm" and p["k_blocks"] == 9 * 4
+    assert st == OK and p["path_name"] == "tiled_2sm" and p["k_blocks"] == 9 * 4 // 2
     st, p = plan(N=2, H=12, W=10, C=72, K=40, R=5, S=5, pad=(2, 2))
     assert st == OK and p["k_blocks"] == 25 * 2                 # 72 channels: 2 blocks of 64
+    assert p["block_k"] == 64                                   # one chunk per stage
     # few output pixels never swap (the im2col load fills the 128-row side);
     # a long reduction then runs stream-K
     st, p = plan(N=1, H=8, W=8, C=512, K=256)
