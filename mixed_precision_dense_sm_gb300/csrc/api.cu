@@ -111,7 +111,7 @@ gemm_status_t make_plan(char transA, char transB, int64_t M, int64_t N, int64_t 
                         const void* A, int64_t lda, const void* B, int64_t ldb, float beta,
                         const void* C, int64_t ldc, gemm_dtypes_t dt, int32_t num_sms,
                         int32_t smem_optin, Plan& pl, bool allow_swap = true, bool ln = false,
-                        int32_t max_kc = kMaxKc) {
+                        int32_t max_kc = kMaxKc, int32_t min_kc2_stages = 3) {
     gemm_status_t st = check_args(transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, dt);
     if (st != GEMM_OK) return st;
     if (num_sms < 1 || smem_optin < 64 * 1024) return GEMM_ERR_INVALID_VALUE;
@@ -269,7 +269,7 @@ gemm_status_t make_plan(char transA, char transB, int64_t M, int64_t N, int64_t 
     // static shared memory of the kernel: flags, and the LayerNorm exchange
     const int64_t static_bytes = 64 + (ln ? 4 * kBlockM * 4 : 4);
     const int64_t avail = smem_optin - 1024 - barrier_bytes - static_bytes;
-    pl.kc = (kc2_ok && avail / (2 * static_cast<int64_t>(chunk_bytes)) >= 3) ? 2 : 1;
+    pl.kc = (kc2_ok && avail / (2 * static_cast<int64_t>(chunk_bytes)) >= min_kc2_stages) ? 2 : 1;
     const int64_t block_k = chunk_k * pl.kc;
     pl.k_blocks = static_cast<int32_t>(ceil_div(K, block_k));
     pl.pub.block_k = static_cast<int32_t>(block_k);
@@ -763,9 +763,12 @@ gemm_status_t conv_plan(int64_t N, int64_t H, int64_t W, int64_t C, int64_t K, i
     // Two chunks per stage take two im2col boxes (64 channels of one tap
     // each) and one filter box, when C is a whole number of 64-channel blocks
     // (the KRSC filter is then a K-major K x (R*S*C) matrix whose chunks never
-    // straddle taps); otherwise one chunk.
+    // straddle taps); otherwise one chunk.  Two such stages suffice here (the
+    // single-CTA 256-wide tile): the im2col boxes re-read X from L2 (R*S
+    // times) and the filter stays in L2, so one stage in flight covers the
+    // load latency, where a GEMM streaming an operand from DRAM needs three.
     return make_plan('N', 'T', M, K, kfake, alpha, X, kfake, Wt, kfake, beta, Y, K, dt, num_sms,
-                     smem_optin, pl, false, false, C % 64 == 0 ? kMaxKc : 1);
+                     smem_optin, pl, false, false, C % 64 == 0 ? kMaxKc : 1, 2);
 }
 
 bool dtype16or32(int32_t t) { return t == GEMM_F16 || t == GEMM_BF16 || t == GEMM_F32; }

@@ -4,7 +4,8 @@
 // of width 256, behind a plain launcher -- and, for 16-bit inputs, the
 // LayerNorm-epilogue variants (single-CTA 128/256, CTA-pair 256).  Each with
 // one K chunk per stage, and those whose three stages of two chunks fit in
-// shared memory (all but the single-CTA 256-wide tile) also with two.
+// shared memory also with two; the plain single-CTA 256-wide tile also with
+// two (two stages, used by convolutions).
 #pragma once
 #include <mutex>
 
@@ -111,9 +112,7 @@ static cudaError_t launch_tc_kc(const TcLaunch& l) {
     switch (l.block_n) {
         case 64: return launch_tc_cfg<1, 64, kEpiPlain, KC>(l);
         case 128: return launch_tc_cfg<1, 128, kEpiPlain, KC>(l);
-        case 256:
-            if constexpr (KC == 1) return launch_tc_cfg<1, 256, kEpiPlain, 1>(l);
-            return cudaErrorInvalidValue;
+        case 256: return launch_tc_cfg<1, 256, kEpiPlain, KC>(l);   // KC = 2: convolutions
         default: return cudaErrorInvalidValue;
     }
 }

@@ -137,6 +137,12 @@ def test_two_k_chunks_per_stage():
     st, c = lib.conv2d_plan_query(8, 20, 20, 96, 64, 3, 3, (1, 1), (1, 1), (1, 1), 1.0, 256, 256,
                                   0.0, 256, (DT_BF16, DT_BF16, DT_BF16))
     assert st == 0 and c["block_k"] == 64 and c["k_blocks"] == 18, c
+    # a convolution on single-CTA 256-wide tiles keeps two chunks in two
+    # stages (operands re-read from L2); a GEMM of that tile keeps one chunk
+    st, c = lib.conv2d_plan_query(32, 14, 14, 512, 512, 3, 3, (1, 1), (1, 1), (1, 1), 1.0, 256, 256,
+                                  0.0, 256, (DT_BF16, DT_BF16, DT_BF16))
+    assert st == 0 and (c["path_name"], c["block_n"], c["block_k"], c["stages"]) == \
+        ("tiled_1sm", 256, 128, 2), c
 
 
 def test_quick_paths_and_swap_rule():

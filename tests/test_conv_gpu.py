@@ -145,6 +145,21 @@ def test_cta_pairs_and_stream_k(g, orc):
     run_and_check(g, orc, long_k, dt=DT_BF16, ydt=DT_BF16, integer=False, seed=3)
 
 
+def test_single_cta_wide_tiles_two_chunks(g, orc):
+    """The 32 x 14 x 14, C = K = 512 layer: single-CTA 256-wide tiles with two
+    K chunks per stage in two stages, stream-K over 36 stages; sampled pixels
+    (every 37th and the last) against the oracle, both input types."""
+    import mixed_precision_dense_sm_gb300 as lib
+    geo = (32, 14, 14, 512, 512, 3, 3, (1, 1), (1, 1), (1, 1))
+    st, p = lib.conv2d_plan_query(*geo, 1.0, 256, 256, 0.0, 1 << 44, (DT_BF16, DT_BF16, DT_BF16),
+                                  num_sms=torch.cuda.get_device_properties(0).multi_processor_count)
+    assert st == 0 and (p["path_name"], p["block_n"], p["block_k"], p["stages"]) == \
+        ("tiled_1sm", 256, 128, 2), p
+    sample = lambda M: np.unique(np.concatenate([np.arange(0, M, 37), [M - 1, 1, 2]]))
+    run_and_check(g, orc, geo, dt=DT_BF16, ydt=DT_BF16, integer=True, sample=sample)
+    run_and_check(g, orc, geo, dt=DT_F16, ydt=DT_F32, integer=False, beta=1.0, sample=sample)
+
+
 def test_errors_enqueue_nothing(g):
     import mixed_precision_dense_sm_gb300 as lib
     Y = torch.full((64, 16), 5.0, device="cuda")
