@@ -64,10 +64,16 @@ LAYER = ["linear_8192x4096x4096_bf16", "linear_8192x14336x4096_bf16",
          "linear_8192x4096x14336_bf16"]
 FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 TF32_OVER_BF16 = 1.1 / 2.25
+# every file the timed kernels compile from: a committed traffic figure is
+# reported only while these hash to the build it was captured on
 KERNEL_SOURCES = ["mixed_precision_dense_sm_gb300/csrc/gemm_tc.cuh",
                   "mixed_precision_dense_sm_gb300/csrc/ptx.cuh",
+                  "mixed_precision_dense_sm_gb300/csrc/epilogue_ops.cuh",
                   "mixed_precision_dense_sm_gb300/csrc/kern_inst.cuh"]
 SOFTMAX_SOURCES = ["mixed_precision_dense_sm_gb300/csrc/softmax_kern.cuh",
+                   "mixed_precision_dense_sm_gb300/csrc/softmax_tma.cuh",
+                   "mixed_precision_dense_sm_gb300/csrc/softmax_inst.cuh",
+                   "mixed_precision_dense_sm_gb300/csrc/softmax_launch.h",
                    "mixed_precision_dense_sm_gb300/csrc/softmax.cu",
                    "mixed_precision_dense_sm_gb300/csrc/ptx.cuh"]
 SOFTMAX_METRIC = "softmax GB/s (X read once + Y written once, per second) at 1 GB300; % of HBM"
