@@ -96,7 +96,10 @@ __device__ __forceinline__ void warp_merge(float& m, float& s) {
 // scalar path interleaves single elements across the threads (element e of
 // thread t is element e * T + t).  Both cover the chunk once and keep each
 // warp's accesses contiguous.  Offsets are 32-bit: a row has < 2^31 elements.
-template <typename InT>
+// KEEP: the chunk will be read again soon (the first of two passes over a
+// slice), so its lines stay in L2 (ld.global.cg); otherwise this is the last
+// read and they go first (ld.global.cs).
+template <typename InT, bool KEEP = false>
 __device__ __forceinline__ void load_chunk(const InT* __restrict__ x, int32_t base, int32_t end,
                                            bool vec, int t, int T, float (&v)[kE]) {
     constexpr int V = VecOf<InT>::V;
@@ -105,7 +108,8 @@ __device__ __forceinline__ void load_chunk(const InT* __restrict__ x, int32_t ba
         for (int k = 0; k < kE / V; ++k) {
             const int32_t e0 = base + (k * T + t) * V;
             if (e0 + V <= end) {
-                const uint4 u = __ldcs(reinterpret_cast<const uint4*>(x + e0));
+                const uint4 u = KEEP ? __ldcg(reinterpret_cast<const uint4*>(x + e0))
+                                     : __ldcs(reinterpret_cast<const uint4*>(x + e0));
                 const InT* q = reinterpret_cast<const InT*>(&u);
                 #pragma unroll
                 for (int i = 0; i < V; ++i) v[k * V + i] = to_f(q[i]);
@@ -236,7 +240,11 @@ __global__ void __launch_bounds__(512)
             float m = -INFINITY, s = 0.0f;
             for (int32_t c = s0; c < s1; c += chunk) {
                 const int32_t ce = s1 - c > chunk ? c + chunk : s1;
-                load_chunk<InT>(x, c, ce, vec, threadIdx.x, T, v);
+                // a slice of several chunks is read again by the second pass
+                // while it is still in L2 (the slices of all resident CTAs,
+                // 152 x 512 KB for the longest rows, fit in it)
+                if (p.resident) load_chunk<InT, false>(x, c, ce, vec, threadIdx.x, T, v);
+                else load_chunk<InT, true>(x, c, ce, vec, threadIdx.x, T, v);
                 float mc, sc;
                 chunk_stats(v, mc, sc);
                 merge(m, s, mc, sc);                 // the online rule, chunk by chunk
