@@ -4,11 +4,16 @@
 //
 // The split follows the SGEMM tutorial page's two regimes (sections 2.3-2.4):
 // a row that fits on chip is read once and kept there (registers of a warp or
-// of a CTA); a longer row is spread over a thread-block cluster whose CTAs
-// merge their partial (max, sum) pairs through distributed shared memory --
-// the GB300 form of the page's option of splitting a long row over several
-// blocks that reduce across blocks -- and only rows beyond the cluster's
-// capacity are read twice.
+// of a CTA, staged through shared memory); a longer row is read twice by one
+// CTA -- a first pass folds it into a running (max, sum) by the online rule,
+// a second writes y -- with the first pass's lines kept in L2, so that DRAM
+// still sees the row once.  Only when the slices of all resident CTAs would
+// not fit half the L2 is a row spread over a thread-block cluster whose CTAs
+// merge their (max, sum) pairs through distributed shared memory (the page's
+// option of splitting a long row over blocks that reduce across blocks).
+// Measured on GB300: per-row cluster synchronisation cost more than the
+// L2-resident second read (2048 x 65536 FP32: 298 us over a cluster of 4,
+// 217 us in one CTA with two passes).
 #include <cstdint>
 #include <cstring>
 #include <mutex>
@@ -31,6 +36,11 @@ constexpr int64_t kMaxCols = int64_t(1) << 30;
 constexpr int64_t kStagedMinBytes = 256;
 constexpr int64_t kStagedMaxBytes = 64 * 1024;
 constexpr int64_t kStagedSmemBudget = 200 * 1024;
+// Two-pass rows: the first pass's lines must still be in L2 when the second
+// pass reads them, so the slices of all resident CTAs stay within half the
+// 129 MB L2 of a GB300 (a cluster splits the row when one CTA per row would
+// not).
+constexpr int64_t kTwoPassL2Budget = int64_t(64) << 20;
 constexpr uint64_t kDefaultWaitNs = 2000000000ull;
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
@@ -90,36 +100,19 @@ gemm_status_t make_plan(int64_t rows, int64_t cols, const void* X, int64_t ldx, 
     const int64_t row_bytes = cols * ex;
     const int64_t kvmax = smx::kTmaMaxElems / (16 / ex);     // vectors per thread
     const int64_t max_vec = (smx::kTmaThreads / 32) * 32 * kvmax;
-    // a row (or, split over a cluster, a slice of it) fits one CTA's slots
-    // and registers
-    auto fits = [&](int64_t elems) {
-        const int64_t b = elems * ex;
-        return b >= kStagedMinBytes && b <= kStagedMaxBytes && b / 16 <= max_vec;
-    };
-    int64_t staged_cl = 0;
-    if (pl.pub.vec) {
-        if (fits(cols)) {
-            staged_cl = 1;
-        } else if (cols * ex > kStagedMaxBytes || cols * ex / 16 > max_vec) {
-            for (int64_t c = 2; c <= smx::kMaxCluster; c *= 2)
-                if (fits(round_up(ceil_div(cols, c), 8))) {
-                    staged_cl = c;
-                    break;
-                }
-        }
-    }
-    if (staged_cl > 0) {
+    // a row fits one CTA's slots and registers
+    const int64_t b = cols * ex;
+    const bool staged = pl.pub.vec && b >= kStagedMinBytes && b <= kStagedMaxBytes &&
+                        b / 16 <= max_vec;
+    if (staged) {
         // staged in shared memory: one CTA of 16 warps per SM, split into
         // groups just large enough to hold a row in registers; each group a
-        // pipeline of `depth` row slots.  A row too long for one CTA is split
-        // over a cluster, each CTA one group with a slice.
-        const int64_t slice = staged_cl > 1 ? round_up(ceil_div(cols, staged_cl), 8) : cols;
+        // pipeline of `depth` row slots
+        const int64_t slice = cols;
         const int64_t nvec = slice * ex / 16;
         int64_t gw = 1, unit_rows = 1, row_stride = 0;
         bool contiguous = false;
-        if (staged_cl > 1) {
-            gw = smx::kTmaThreads / 32;
-        } else if (nvec <= 32 * kvmax) {
+        if (nvec <= 32 * kvmax) {
             // a warp holds a row: groups of 8 warps share slots of several
             // rows, moved by one copy of ~16 KB when the rows are adjacent
             gw = 8;
@@ -141,7 +134,7 @@ gemm_status_t make_plan(int64_t rows, int64_t cols, const void* X, int64_t ldx, 
         if (depth > smx::kTmaMaxDepth) depth = smx::kTmaMaxDepth;
         pl.pub.mode = unit_rows > 1 ? SOFTMAX_MODE_WARP : SOFTMAX_MODE_CTA;
         pl.pub.threads = smx::kTmaThreads;
-        pl.pub.cluster = static_cast<int32_t>(staged_cl);
+        pl.pub.cluster = 1;
         pl.pub.slice = static_cast<int32_t>(round_up(slice, 8));
         pl.pub.depth = static_cast<int32_t>(depth);
         pl.pub.group_warps = static_cast<int32_t>(gw);
@@ -152,14 +145,8 @@ gemm_status_t make_plan(int64_t rows, int64_t cols, const void* X, int64_t ldx, 
         pl.resident = true;
         pl.smem = static_cast<size_t>(round_up(groups * depth * 8, 128) + groups * depth * slot);
         pl.bulk_elems = static_cast<int32_t>((row_bytes / 16) * 16 / ex);
-        if (staged_cl == 1) {
-            const int64_t need = ceil_div(ceil_div(rows, unit_rows), groups);
-            pl.pub.grid = static_cast<int32_t>(need < num_sms ? need : num_sms);
-        } else {
-            int64_t clusters = ctas_per_sm > 0 ? ctas_per_sm : num_sms / staged_cl;
-            if (clusters < 1) clusters = 1;
-            pl.pub.grid = static_cast<int32_t>(staged_cl * (rows < clusters ? rows : clusters));
-        }
+        const int64_t need = ceil_div(ceil_div(rows, unit_rows), groups);
+        pl.pub.grid = static_cast<int32_t>(need < num_sms ? need : num_sms);
     } else if (cols <= kWarpMaxCols) {
         pl.pub.mode = SOFTMAX_MODE_WARP;
         pl.pub.threads = smx::kWarpCtaThreads;
@@ -173,7 +160,11 @@ gemm_status_t make_plan(int64_t rows, int64_t cols, const void* X, int64_t ldx, 
         int64_t cl = 1;
         int threads = cols <= kCtaSmallCols ? 256 : 512;
         if (cols > kCtaMaxCols) {
-            while (cl < smx::kMaxCluster && cl * kCtaMaxCols < cols) cl *= 2;
+            // two passes: the smallest cluster whose resident slices fit the
+            // L2 budget (one CTA per row unless the rows are very long)
+            while (cl < smx::kMaxCluster &&
+                   static_cast<int64_t>(num_sms) * ceil_div(cols, cl) * ex > kTwoPassL2Budget)
+                cl *= 2;
         }
         const int64_t slice = round_up(ceil_div(cols, cl), 8);
         pl.resident = slice <= static_cast<int64_t>(threads) * smx::kE;
@@ -330,8 +321,7 @@ gemm_status_t softmax_rows(int64_t rows, int64_t cols, const void* X, int64_t ld
         q.cols = static_cast<int32_t>(cols);
         q.bulk_elems = pl.bulk_elems;
         q.slot_bytes = static_cast<int32_t>(
-            round_up(pl.pub.unit_rows == 1 ? int64_t(pl.pub.slice < cols ? pl.pub.slice : cols) *
-                                                 elem_bytes(x_dtype)
+            round_up(pl.pub.unit_rows == 1 ? cols * elem_bytes(x_dtype)
                                            : int64_t(pl.pub.unit_rows) * pl.row_stride, 128));
         q.depth = pl.pub.depth;
         q.group_warps = pl.pub.group_warps;
@@ -339,8 +329,6 @@ gemm_status_t softmax_rows(int64_t rows, int64_t cols, const void* X, int64_t ld
         q.row_stride = pl.row_stride;
         q.contiguous = pl.contiguous;
         q.kv = pl.pub.kv;
-        q.cluster = pl.pub.cluster;
-        q.slice = pl.pub.slice;
         q.err = err;
         {
             std::lock_guard<std::mutex> g(g_dbg_mu);

@@ -46,8 +46,6 @@ struct TmaSoftmaxParams {
     int32_t row_stride;     // bytes from one row to the next inside a slot
     int32_t contiguous;     // 1: a slot's rows are adjacent in X, one copy moves them all
     int32_t kv;             // 16-byte vectors per thread: 1, 2, 4 (or 8 for FP32 input)
-    int32_t cluster;        // CTAs per row (1: none); > 1 only with one group per CTA
-    int32_t slice;          // elements of a row per CTA of a cluster (multiple of 8)
     int* err;               // device error word (1: a wait ran out)
     uint64_t wait_limit_ns;
     uint32_t debug_flags;
@@ -120,13 +118,11 @@ __device__ __forceinline__ void store_vec16(OutT* dst, const float (&o)[VecOf<In
 
 // Arm `bar` for the rows of unit u and issue their copies: one copy when the
 // rows are adjacent in X, else one per row (unless the test hook says not to).
-// X0 is X shifted to this CTA's slice of the row; bulk_elems its elements
-// moved by the copy.
+// bulk_elems: the elements of a row moved by the copy.
 template <typename InT>
-__device__ __forceinline__ void issue_unit(const TmaSoftmaxParams& p, const InT* X0,
+__device__ __forceinline__ void issue_unit(const TmaSoftmaxParams& p, const InT* X,
                                            int32_t bulk_elems, uint8_t* slot, int64_t u,
                                            uint64_t* bar, uint64_t policy, bool skip) {
-    const InT* X = X0;
     const int64_t first = u * p.unit_rows;
     const int64_t left = p.rows - first;
     const uint32_t nr = static_cast<uint32_t>(left < p.unit_rows ? left : p.unit_rows);
@@ -148,37 +144,12 @@ __device__ __forceinline__ void issue_unit(const TmaSoftmaxParams& p, const InT*
 // output e / s.  One exponential per element.  The T threads are one warp
 // (gw = 1) or the group's gw warps, which combine their partial results
 // through red_m / red_s and the group barrier.
-// Cluster exchange: every CTA publishes its value (and `ok`), then reads all
-// of them, in rank order, through distributed shared memory.
-struct ClusterSlots {
-    float* m;      // [2] by row parity
-    float* s;      // [2]
-    int* ok;       // [2]
-};
-
-__device__ __forceinline__ float ld_cluster_f32(const void* local, uint32_t rank) {
-    float v;
-    asm volatile("ld.shared::cluster.f32 %0, [%1];"
-                 : "=f"(v) : "r"(gemm103::map_to_rank(gemm103::smem_addr(local), rank)) : "memory");
-    return v;
-}
-
-__device__ __forceinline__ int ld_cluster_s32(const void* local, uint32_t rank) {
-    int v;
-    asm volatile("ld.shared::cluster.s32 %0, [%1];"
-                 : "=r"(v) : "r"(gemm103::map_to_rank(gemm103::smem_addr(local), rank)) : "memory");
-    return v;
-}
-
-// Returns false when some CTA of the cluster reported !ok (then nothing is
-// written); every CTA of the cluster returns the same.
-template <typename InT, typename OutT, int KV, bool CLUSTER>
-__device__ __forceinline__ bool process_row(const uint8_t* srow, const InT* __restrict__ grow,
+template <typename InT, typename OutT, int KV>
+__device__ __forceinline__ void process_row(const uint8_t* srow, const InT* __restrict__ grow,
                                             OutT* __restrict__ yrow, int32_t nvec,
                                             int32_t bulk_elems, int32_t cols, int t, int T,
                                             int gw, int group, int warp, int lane,
-                                            float* red_m, float* red_s, int cl,
-                                            const ClusterSlots& cs, int par, bool ok) {
+                                            float* red_m, float* red_s) {
     constexpr int V = VecOf<InT>::V;
     // FP32 input: the raw vectors stay in registers and the output pass
     // evaluates exp(x - m) again next to its stores (the row is bound by HBM,
@@ -216,21 +187,6 @@ __device__ __forceinline__ bool process_row(const uint8_t* srow, const InT* __re
         m = red_m[group * gw];
         for (int w = 1; w < gw; ++w) m = fmax_nan(m, red_m[group * gw + w]);
     }
-    if constexpr (CLUSTER) {
-        if (threadIdx.x == 0) {
-            cs.m[par] = m;
-            cs.ok[par] = ok ? 1 : 0;
-        }
-        __syncwarp();                        // the cluster barrier is warp-aligned
-        gemm103::cluster_sync_all();
-        bool all = true;
-        m = -INFINITY;
-        for (int q = 0; q < cl; ++q) {
-            m = fmax_nan(m, ld_cluster_f32(&cs.m[par], q));
-            all = all && ld_cluster_s32(&cs.ok[par], q) != 0;
-        }
-        if (!all) return false;
-    }
     // padding entries are -inf: exp gives 0 unless m is -inf or +inf or NaN,
     // in which case the row is NaN anyway
     float s = 0.0f;
@@ -252,13 +208,6 @@ __device__ __forceinline__ bool process_row(const uint8_t* srow, const InT* __re
         s = red_s[group * gw];
         for (int w = 1; w < gw; ++w) s += red_s[group * gw + w];
     }
-    if constexpr (CLUSTER) {
-        if (threadIdx.x == 0) cs.s[par] = s;
-        __syncwarp();
-        gemm103::cluster_sync_all();
-        s = 0.0f;
-        for (int q = 0; q < cl; ++q) s += ld_cluster_f32(&cs.s[par], q);
-    }
     const float inv_s = 1.0f / s;
     #pragma unroll
     for (int k = 0; k < KV; ++k) {
@@ -272,10 +221,9 @@ __device__ __forceinline__ bool process_row(const uint8_t* srow, const InT* __re
         }
     }
     if (te < cols) yrow[te] = from_f<OutT>(xt * inv_s);
-    return true;
 }
 
-template <typename InT, typename OutT, int KV, bool CLUSTER>
+template <typename InT, typename OutT, int KV>
 __global__ void __launch_bounds__(kTmaThreads, 1)
     softmax_tma_kernel(const __grid_constant__ TmaSoftmaxParams p) {
     constexpr int V = VecOf<InT>::V;
@@ -291,18 +239,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
     const int group = warp / GW;
     const int gt = threadIdx.x - group * GT;     // thread index within the group
     const int D = p.depth;
-    const int CL = CLUSTER ? p.cluster : 1;
-    // this CTA's slice of a row: [s0, s0 + slen) (the whole row without a cluster)
-    const uint32_t rank = CLUSTER ? gemm103::cluster_ctarank() : 0u;
-    const int32_t s0 = static_cast<int32_t>(rank) * p.slice;
-    const int32_t slen = CLUSTER ? (p.cols - s0 < p.slice ? p.cols - s0 : p.slice) : p.cols;
-    const int32_t cta_bulk = CLUSTER
-        ? static_cast<int32_t>((static_cast<int64_t>(slen) * sizeof(InT) / 16) * 16 / sizeof(InT))
-        : p.bulk_elems;
-    const int32_t nvec = cta_bulk / V;
-    __shared__ float cl_m[2], cl_s[2];
-    __shared__ int cl_ok[2];
-    const ClusterSlots cslots{cl_m, cl_s, cl_ok};
+    const int32_t nvec = p.bulk_elems / V;
     // layout: [barriers: one per slot, 128 B aligned][slots]
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem_raw);
     uint8_t* slots = smem_raw + ((NG * D * 8 + 127) / 128) * 128;
@@ -317,20 +254,18 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
 
     // this group's units (slots' worth of rows): u0, u0 + stride, ...; n in all
     const int64_t units = (p.rows + p.unit_rows - 1) / p.unit_rows;
-    const int64_t u0 = static_cast<int64_t>(blockIdx.x / CL) * NG + group;
-    const int64_t stride = static_cast<int64_t>(gridDim.x / CL) * NG;
+    const int64_t u0 = static_cast<int64_t>(blockIdx.x) * NG + group;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * NG;
     const int64_t n = u0 < units ? (units - 1 - u0) / stride + 1 : 0;
     uint64_t* pb = bars + group * D;
     uint8_t* ps = slots + static_cast<size_t>(group) * D * p.slot_bytes;
     const bool issuer = (gt == 0);
     const bool skip_first = (p.debug_flags & kSmxDebugSkipFirstLoad) && blockIdx.x == 0 && group == 0;
     const int wg = warp - group * GW;                 // warp index within the group
-    const InT* X0 = X + s0;
-    OutT* Y0 = Y + s0;
 
     if (issuer) {
         for (int64_t i = 0; i < n && i < D - 1; ++i)
-            issue_unit<InT>(p, X0, cta_bulk, ps + (i % D) * p.slot_bytes, u0 + i * stride,
+            issue_unit<InT>(p, X, p.bulk_elems, ps + (i % D) * p.slot_bytes, u0 + i * stride,
                             &pb[i % D], policy, skip_first && i == 0);
     }
     int64_t i = 0;
@@ -339,57 +274,48 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
         // with unit i + D - 1
         const int64_t nxt = i + D - 1;
         if (issuer && nxt < n)
-            issue_unit<InT>(p, X0, cta_bulk, ps + (nxt % D) * p.slot_bytes, u0 + nxt * stride,
+            issue_unit<InT>(p, X, p.bulk_elems, ps + (nxt % D) * p.slot_bytes, u0 + nxt * stride,
                             &pb[nxt % D], policy, false);
         bool ok = gemm103::mbar_wait(&pb[i % D], static_cast<uint32_t>((i / D) & 1),
                                      p.wait_limit_ns);
         ok = group_all(GW, group, ok);
-        // a CTA of a cluster goes on to the cluster exchange either way, so
-        // that the whole cluster leaves the loop at the same row
         if (!ok) {
             if (issuer) atomicExch(p.err, 1);
-            if (!CLUSTER) break;
+            break;
         }
         const int64_t first = (u0 + i * stride) * p.unit_rows;
         const uint8_t* sunit = ps + (i % D) * p.slot_bytes;
         if (p.unit_rows == 1) {
-            // the group (or the cluster) shares the row
-            if (!process_row<InT, OutT, KV, CLUSTER>(sunit, X0 + first * p.ldx, Y0 + first * p.ldy, nvec,
-                                            cta_bulk, slen, gt, GT, GW, group, warp, lane, red_m,
-                                            red_s, CL, cslots, static_cast<int>(i & 1), ok))
-                break;
+            // the group shares the row
+            process_row<InT, OutT, KV>(sunit, X + first * p.ldx, Y + first * p.ldy, nvec,
+                                       p.bulk_elems, p.cols, gt, GT, GW, group, warp, lane, red_m,
+                                       red_s);
         } else {
             // each warp of the group takes its own rows of the unit
             const int64_t left = p.rows - first;
             const int nr = static_cast<int>(left < p.unit_rows ? left : p.unit_rows);
             for (int j = wg; j < nr; j += GW)
-                process_row<InT, OutT, KV, false>(sunit + static_cast<size_t>(j) * p.row_stride,
+                process_row<InT, OutT, KV>(sunit + static_cast<size_t>(j) * p.row_stride,
                                            X + (first + j) * p.ldx, Y + (first + j) * p.ldy,
                                            nvec, p.bulk_elems, p.cols, lane, 32, 1, group, warp,
-                                           lane, red_m, red_s, 1, cslots, 0, true);
+                                           lane, red_m, red_s);
         }
         // every thread is past this unit's slot and reduction words
         group_sync(GW, group);
     }
     if (i < n && issuer) {
-        // a wait ran out (here or, in a cluster, in a peer CTA): let the
-        // copies already issued into this group's slots (units i .. i + D - 1)
+        // a wait ran out: let the copies already issued into this group's slots (units i .. i + D - 1)
         // land before shared memory is released
         const int64_t last = i + D < n ? i + D : n;
         for (int64_t j = i; j < last; ++j)
             gemm103::mbar_wait(&pb[j % D], static_cast<uint32_t>((j / D) & 1), p.wait_limit_ns);
     }
-    // no CTA of a cluster leaves while a peer may still read its shared memory
-    if constexpr (CLUSTER) {
-        __syncwarp();
-        gemm103::cluster_sync_all();
-    }
 }
 
-template <typename InT, typename OutT, int KV, bool CLUSTER>
+template <typename InT, typename OutT, int KV>
 cudaError_t launch_softmax_tma_kv(const TmaSoftmaxParams& p, int grid, size_t smem,
                                   cudaStream_t stream) {
-    auto kern = softmax_tma_kernel<InT, OutT, KV, CLUSTER>;
+    auto kern = softmax_tma_kernel<InT, OutT, KV>;
     {
         static std::mutex mu;
         static size_t raised = 0;
@@ -402,7 +328,7 @@ cudaError_t launch_softmax_tma_kv(const TmaSoftmaxParams& p, int grid, size_t sm
         }
     }
     cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[2];
+    cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.gridDim = dim3(grid, 1, 1);
@@ -411,37 +337,6 @@ cudaError_t launch_softmax_tma_kv(const TmaSoftmaxParams& p, int grid, size_t sm
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if constexpr (CLUSTER) {
-        attr[1].id = cudaLaunchAttributeClusterDimension;
-        attr[1].val.clusterDim.x = p.cluster;
-        attr[1].val.clusterDim.y = 1;
-        attr[1].val.clusterDim.z = 1;
-        cfg.numAttrs = 2;
-        if (p.rows > 0) {
-            // no more clusters than can be resident at once (persistent)
-            static std::mutex mu;
-            static int cached[kMaxCluster + 1] = {};
-            int clusters;
-            {
-                std::lock_guard<std::mutex> g(mu);
-                if (cached[p.cluster] == 0) {
-                    // the query takes the cluster shape alone
-                    cudaLaunchConfig_t q = cfg;
-                    q.attrs = &attr[1];
-                    q.numAttrs = 1;
-                    int c = 0;
-                    if (cudaOccupancyMaxActiveClusters(&c, kern, &q) != cudaSuccess) {
-                        cudaGetLastError();
-                        c = 0;
-                    }
-                    cached[p.cluster] = c > 0 ? c : -1;     // -1: unknown, keep the plan's grid
-                }
-                clusters = cached[p.cluster];
-            }
-            if (clusters > 0 && grid > clusters * p.cluster)
-                cfg.gridDim = dim3(clusters * p.cluster, 1, 1);
-        }
-    }
     return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
@@ -449,26 +344,13 @@ template <typename InT, typename OutT>
 cudaError_t launch_softmax_tma(const TmaSoftmaxParams& p, int grid, size_t smem,
                                cudaStream_t stream) {
     constexpr int kMaxKV = kTmaMaxElems / VecOf<InT>::V;
-    if (p.cluster > 1) {
-        // a cluster slice fills the CTA: more than 2048 elements, so >= 4
-        // 16-bit or >= 2 FP32 vectors per thread
-        switch (p.kv) {
-            case 2: return launch_softmax_tma_kv<InT, OutT, 2, true>(p, grid, smem, stream);
-            case 4: return launch_softmax_tma_kv<InT, OutT, 4, true>(p, grid, smem, stream);
-            case 8:
-                if constexpr (kMaxKV >= 8)
-                    return launch_softmax_tma_kv<InT, OutT, 8, true>(p, grid, smem, stream);
-                return cudaErrorInvalidValue;
-            default: return cudaErrorInvalidValue;
-        }
-    }
     switch (p.kv) {
-        case 1: return launch_softmax_tma_kv<InT, OutT, 1, false>(p, grid, smem, stream);
-        case 2: return launch_softmax_tma_kv<InT, OutT, 2, false>(p, grid, smem, stream);
-        case 4: return launch_softmax_tma_kv<InT, OutT, 4, false>(p, grid, smem, stream);
+        case 1: return launch_softmax_tma_kv<InT, OutT, 1>(p, grid, smem, stream);
+        case 2: return launch_softmax_tma_kv<InT, OutT, 2>(p, grid, smem, stream);
+        case 4: return launch_softmax_tma_kv<InT, OutT, 4>(p, grid, smem, stream);
         case 8:
             if constexpr (kMaxKV >= 8)
-                return launch_softmax_tma_kv<InT, OutT, 8, false>(p, grid, smem, stream);
+                return launch_softmax_tma_kv<InT, OutT, 8>(p, grid, smem, stream);
             return cudaErrorInvalidValue;
         default: return cudaErrorInvalidValue;
     }

@@ -52,11 +52,13 @@ def test_overlap_rules():
 
 @pytest.mark.parametrize("cols,mode,threads,cluster", [
     (1, "warp", 256, 1), (1024, "warp", 256, 1), (1025, "cta", 256, 1), (8192, "cta", 256, 1),
-    (8193, "cta", 512, 1), (16384, "cta", 512, 1), (16385, "cta", 512, 2), (32768, "cta", 512, 2),
-    (32769, "cta", 512, 4), (131072, "cta", 512, 8), (131073, "stream", 512, 8),
-    (1 << 20, "stream", 512, 8)])
+    (8193, "cta", 512, 1), (16384, "cta", 512, 1), (16385, "stream", 512, 1),
+    (32768, "stream", 512, 1), (32769, "stream", 512, 1), (131072, "stream", 512, 2),
+    (131073, "stream", 512, 2), (1 << 20, "stream", 512, 8)])
 def test_work_split(cols, mode, threads, cluster):
-    """Rows not 16-byte aligned (base 4 bytes off): held in registers."""
+    """Rows not 16-byte aligned (base 4 bytes off): held in registers up to
+    16384 elements; longer rows in two passes by one CTA, or by a cluster
+    when the slices of 152 resident CTAs would exceed 64 MB (half the L2)."""
     st, p = plan(64, cols, x=260)
     assert st == OK
     assert (p["mode_name"], p["threads"], p["cluster"]) == (mode, threads, cluster)
@@ -78,21 +80,21 @@ def test_work_split(cols, mode, threads, cluster):
     (4096, DT_F32, 4096, 1, 4, 1, 3, 8), (8192, DT_F32, 8192, 1, 8, 1, 3, 8),
     (16384, DT_F32, 16384, 1, 16, 1, 3, 8), (16384, DT_BF16, 16384, 1, 16, 1, 6, 4),
     (3000, DT_F16, 3000, 1, 4, 1, 8, 4),
-    # split over a cluster, one group (the CTA) per slice
-    (16388, DT_F32, 16388, 2, 16, 1, 6, 8), (32768, DT_F16, 32768, 2, 16, 1, 6, 4),
-    (65536, DT_F32, 65536, 4, 16, 1, 3, 8), (131072, DT_F32, 131072, 8, 16, 1, 3, 8),
-    (20000, DT_BF16, 20000, 2, 16, 1, 8, 4),
-    # not staged: too short, too long, or rows not 16-byte aligned
-    (131080, DT_F32, 131080, 8, 0, 0, 0, 0), (60, DT_F32, 60, 1, 0, 0, 0, 0),
-    (120, DT_BF16, 120, 1, 0, 0, 0, 0), (16385, DT_F32, 16385, 2, 0, 0, 0, 0)])
+    # not staged: too long for one CTA (two passes; a cluster of 2 for rows
+    # whose 152 resident slices exceed 64 MB), too short, or rows not 16-byte
+    # aligned
+    (16388, DT_F32, 16388, 1, 0, 0, 0, 0), (32768, DT_F16, 32768, 1, 0, 0, 0, 0),
+    (65536, DT_F32, 65536, 1, 0, 0, 0, 0), (131072, DT_F32, 131072, 2, 0, 0, 0, 0),
+    (20000, DT_BF16, 20000, 1, 0, 0, 0, 0), (131080, DT_F32, 131080, 2, 0, 0, 0, 0),
+    (60, DT_F32, 60, 1, 0, 0, 0, 0), (120, DT_BF16, 120, 1, 0, 0, 0, 0),
+    (16385, DT_F32, 16385, 1, 0, 0, 0, 0)])
 def test_staged_split(cols, dt, ld, cl, gw, unit, depth, kv):
     """16-byte-aligned rows of 256 B to 64 KB (<= 16384 elements) are staged
     in shared memory by bulk copies: one CTA of 16 warps per SM.  Rows a warp
     can hold (<= 1024 elements) go to groups of 8 warps whose slots carry
     several rows (~16 KB, one copy when the rows are adjacent), a warp per
     row; longer rows are shared by a group just large enough to hold them in
-    registers (<= 32 elements per thread); rows longer still are split over a
-    cluster of 2 to 8 CTAs, a slice each.  Each group is a pipeline with as
+    registers (<= 32 elements per thread).  Each group is a pipeline with as
     many slots as 200 KB allow (at most 8).  Other rows keep the register
     kernels (depth 0)."""
     st, p = plan(100000, cols, ldx=ld, ldy=ld, xdt=dt, ydt=dt)
@@ -142,4 +144,5 @@ def test_vector_rule_and_grid():
     assert plan(5, 4096, x=260, per_sm=2)[1]["grid"] == 5
     assert plan(100000, 4096, x=260, per_sm=2)[1]["grid"] == 304
     assert plan(100000, 100)[1]["grid"] == 152                    # staged: one CTA per SM
-    assert plan(100000, 65536, per_sm=10)[1]["grid"] == 4 * 10  # 10 clusters of 4
+    assert plan(100000, 65536, per_sm=10)[1]["grid"] == 10 * 152  # two passes, a CTA per row
+    assert plan(100000, 1 << 20, per_sm=10)[1]["grid"] == 8 * 10  # 10 clusters of 8
