@@ -7,13 +7,15 @@
  *     s = sum_j e_j,  y_j = e_j / s  (SGEMM tutorial page, section 2.1: the
  *     maximum, the sum of exponentials of the shifted values, the division).
  *     The maximum shift keeps exp from overflowing (section 2.2).
- *   - Each element is read from HBM once and written once wherever the row
- *     fits on chip -- in one warp's or one CTA's registers, or, for long rows,
- *     spread over a thread-block cluster of up to 8 CTAs whose partial
- *     (maximum, sum) pairs are merged through distributed shared memory with
- *     the online rule m' = max(m1, m2), s' = s1 e^(m1-m') + s2 e^(m2-m')
- *     (section 2.2).  Longer rows are read twice: a first pass accumulates
- *     (m, s) with the same rule chunk by chunk, a second pass writes y.
+ *   - Each element is read from HBM once and written once.  A row that fits
+ *     on chip (one warp's or one CTA's registers, up to 16384 elements) is
+ *     read once; a longer row is read twice by one CTA -- a first pass
+ *     accumulates (m, s) chunk by chunk with the online rule m' = max(m1, m2),
+ *     s' = s1 e^(m1-m') + s2 e^(m2-m') (section 2.2), a second pass writes
+ *     y -- and the first pass leaves the row in L2 for the second.  Rows so
+ *     long that the slices of all resident CTAs would exceed half the L2 are
+ *     spread over a thread-block cluster of up to 8 CTAs whose (m, s) pairs
+ *     merge by the same rule through distributed shared memory.
  *   - Arithmetic is FP32 whatever the storage type (the CATLASS page, section
  *     3.4, keeps reductions such as softmax in FP32 with 16-bit data paths);
  *     exp is the fast hardware exponential (__expf, as on the SGEMM page,
@@ -35,7 +37,7 @@
  * groups of 1-16 warps, each group a pipeline that keeps the copies of its
  * next few rows in flight while it works on one (~130-190 KB per SM in all),
  * so HBM is streamed without registers holding the loads.  Other rows are
- * held in registers (warp, CTA or cluster splits).
+ * held in registers (warp or CTA splits) or take the two passes above.
  *
  * Errors: returns GEMM_OK, GEMM_ERR_INVALID_VALUE (bad sizes, leading
  * dimension, type, NULL or misaligned pointer, overlap; nothing enqueued),
@@ -70,8 +72,8 @@ gemm_status_t softmax_rows(int64_t rows, int64_t cols, const void* X, int64_t ld
 typedef enum {
     SOFTMAX_MODE_NOOP = 0,      /* rows == 0 or cols == 0 */
     SOFTMAX_MODE_WARP = 1,      /* one warp per row, row in registers (cols <= 1024) */
-    SOFTMAX_MODE_CTA = 2,       /* one CTA (or a cluster of CTAs) per row, row in registers */
-    SOFTMAX_MODE_STREAM = 3     /* a cluster per row, two passes over the row */
+    SOFTMAX_MODE_CTA = 2,       /* one CTA per row, row in registers or staged */
+    SOFTMAX_MODE_STREAM = 3     /* one CTA (or a cluster of CTAs) per row, two passes */
 } softmax_mode_t;
 
 typedef struct {
@@ -89,14 +91,17 @@ typedef struct {
                               more: each warp takes its own rows of the slot, and rows that
                               are adjacent in X arrive in one copy of the whole slot */
     int32_t kv;            /* staged: 16-byte vectors of a row per thread (1, 2, 4, 8) */
-    int64_t hbm_bytes;     /* bytes this plan moves to and from HBM */
+    int64_t hbm_bytes;     /* bytes this plan reads and writes (two-pass rows count X
+                              twice; the second read is meant to hit L2) */
 } softmax_plan_t;
 
 /*
  * softmax_plan_query: the plan softmax_rows would use on a device with
  * `num_sms` SMs, assuming `ctas_per_sm` resident CTAs per SM of the chosen
  * shape -- or, when a row is split over a cluster, that many resident
- * clusters on the whole GPU (0: the library's estimate).  Pure host logic;
+ * clusters on the whole GPU (0: the library's estimate).  Two-pass rows
+ * take the smallest cluster (1, 2, 4 or 8) whose resident slices,
+ * num_sms x slice x input size, stay within 64 MB.  Pure host logic;
  * pointers are used only for their alignment and overlap.  Returns what
  * softmax_rows would return for invalid arguments.
  */
