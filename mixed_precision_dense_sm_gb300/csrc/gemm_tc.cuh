@@ -536,27 +536,6 @@ __device__ __forceinline__ void ln_chunk_h(const TcParams& p, uint32_t taddr, in
     for (int j = 0; j < 32; ++j) v[j] = (c0 + j < p.N) ? round_to_out<OutT>(v[j]) : 0.0f;
 }
 
-// Asks L2 for the residual C of one row's chunks of a tile (the chunks this
-// thread will read, columns < N), so the first epilogue pass finds it there.
-// Issued before the tile's accumulator is ready: the loads overlap the MMA.
-template <typename OutT, int BN>
-__device__ __forceinline__ void ln_prefetch_residual(const TcParams& p, int32_t row, int half,
-                                                     int32_t col0) {
-    if (p.beta == 0.0f || row >= p.M) return;
-    const uint8_t* base = reinterpret_cast<const uint8_t*>(p.C) +
-                          static_cast<int64_t>(row) * p.c_rs * static_cast<int64_t>(sizeof(OutT));
-    #pragma unroll
-    for (int ch = half; ch < BN / 32; ch += 2) {
-        const int32_t c0 = col0 + ch * 32;
-        if (c0 >= p.N) break;
-        const int32_t n = (p.N - c0) < 32 ? (p.N - c0) : 32;
-        const int32_t bytes = n * static_cast<int32_t>(sizeof(OutT));
-        const uint8_t* q = base + static_cast<int64_t>(c0) * static_cast<int64_t>(sizeof(OutT));
-        for (int32_t b = 0; b < bytes; b += 32) prefetch_l2(q + b);
-        prefetch_l2(q + bytes - 1);
-    }
-}
-
 // The LayerNorm epilogue of one tile.  Each row's columns are split between
 // two warps (alternate 32-column chunks); their partial sums meet in shared
 // memory (red[0..2*kBlockM) for the mean, red[2*kBlockM..4*kBlockM) for M2).
@@ -1067,7 +1046,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tmem_st_wait();
                 }
             }
-            if constexpr (EPI == kEpiLayerNorm) ln_prefetch_residual<OutT, BN>(p, row, half, col0);
             ok = ok && wait_or_abort(&acc_full[buf], (acc_i >> 1) & 1u, &abort_flag, p.wait_limit_ns);
             // stream-K and LayerNorm use named barriers below
             if (p.stream_k || EPI == kEpiLayerNorm) ok = epilogue_all(ok);

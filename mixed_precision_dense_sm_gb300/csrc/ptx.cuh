@@ -260,11 +260,6 @@ __device__ __forceinline__ void tmem_st_wait() {
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
-// Hint: bring the cache line holding `p` into L2 (no register result, never
-// faults on the hint itself; callers pass addresses inside their buffers).
-__device__ __forceinline__ void prefetch_l2(const void* p) {
-    asm volatile("prefetch.global.L2 [%0];" ::"l"(static_cast<uint64_t>(__cvta_generic_to_global(p))));
-}
 
 // Shared-memory matrix descriptor for a tile stored with the 128-byte swizzle
 // (the layout TMA writes with CU_TENSOR_MAP_SWIZZLE_128B):
