@@ -38,6 +38,10 @@ constexpr int64_t kMaxCounterTiles = kWsHeaderBytes / 4;
 // schedules whose last wave leaves more than 1 - kMinWaveFill of the GPU idle.
 constexpr int32_t kLongK = 32;
 constexpr double kMinWaveFill = 0.8;
+// Stream-K fix-up: one FP32 partial tile read back by the finisher costs about
+// as long as this many k-blocks of 256 bytes per row (128 BF16 / FP16 or 64
+// TF32 elements) of the tile's MMA (measured on GB300).
+constexpr double kSkFixupKBlocks = 8.0;
 
 struct OperandDesc {
     // stored matrix: rows x cols with pitch ld (elements); K-major means the
@@ -203,7 +207,7 @@ gemm_status_t make_plan(char transA, char transB, int64_t M, int64_t N, int64_t 
     // Tile shape.  Enough 256 x 256 tiles to give every SM pair one: CTA-pair
     // tiles (tcgen05 cta_group::2).  Otherwise single-CTA 128-row tiles, 256
     // columns wide when that still fills the GPU, else narrower ones with
-    // stream-K over K for more parallelism.
+    // stream-K over K for more parallelism (on CTA pairs for 256-wide tiles).
     //
     // Wave quantisation: when the last wave of a data-parallel schedule would
     // leave more than kMinWaveFill of the SMs idle and each tile is long in K,
@@ -224,9 +228,9 @@ gemm_status_t make_plan(char transA, char transB, int64_t M, int64_t N, int64_t 
         pairs = false;
         balance_sk = true;
     }
-    const int cg = pairs ? 2 : 1;
-    const int64_t block_m = static_cast<int64_t>(kBlockM) * cg;
-    const int64_t tiles_m = ceil_div(pl.Mk, block_m);
+    int cg = pairs ? 2 : 1;
+    int64_t block_m = static_cast<int64_t>(kBlockM) * cg;
+    int64_t tiles_m = ceil_div(pl.Mk, block_m);
     // Single-CTA tiles: the widest of 256 / 128 / 64 columns that still gives
     // every SM a tile (256) or at least half a wave (128, 64).
     int bn;
@@ -253,6 +257,20 @@ gemm_status_t make_plan(char transA, char transB, int64_t M, int64_t N, int64_t 
         if (balance_sk) {
             bn = pl.Nk > 128 ? 256 : (pl.Nk > 64 ? 128 : 64);
             if (tiles_m * ceil_div(pl.Nk, bn) > kMaxCounterTiles) balance_sk = false;
+        }
+    }
+    // Stream-K over single-CTA 256-wide tiles (below) runs on CTA pairs
+    // instead when M allows: per MMA a pair tile loads two thirds of the
+    // operand bytes of a single-CTA 128 x 256 tile, and that is the limit
+    // once the operands come from L2 (each re-read by several tiles).
+    bool pair_sk = false;
+    if (!pairs && !ln && !swap && bn == 256 && pl.Mk >= 2 * kBlockM && num_sms >= 2) {
+        const int64_t t1 = tiles_m * ceil_div(pl.Nk, bn);
+        if (t1 <= kMaxCounterTiles && (balance_sk || (t1 < half_wave && long_k))) {
+            pair_sk = pairs = true;
+            cg = 2;
+            block_m = 2 * kBlockM;
+            tiles_m = ceil_div(pl.Mk, block_m);
         }
     }
     const int64_t tiles_n = ceil_div(pl.Nk, bn);
@@ -284,18 +302,33 @@ gemm_status_t make_plan(char transA, char transB, int64_t M, int64_t N, int64_t 
     // Stream-K spreads the K loop of too few tiles (or of a badly filled last
     // wave, above) over all SMs.  It pays for itself only when the tiles are
     // long in K; the swapped skinny path (a weight-streaming GEMM) always uses it.
-    const bool stream_k = !pairs && !ln && (tiles <= kMaxCounterTiles) && (work < INT32_MAX) &&
-                          (balance_sk || ((tiles < num_sms) &&
-                           (swap ? k_chunks >= 4 : (tiles < half_wave && long_k))));
+    const bool stream_k = work < INT32_MAX &&
+                          (pair_sk || (!pairs && !ln && (tiles <= kMaxCounterTiles) &&
+                                       (balance_sk || ((tiles < num_sms) &&
+                                        (swap ? k_chunks >= 4 : (tiles < half_wave && long_k))))));
     if (stream_k) {
-        int64_t G = num_sms < work ? num_sms : work;
-        const int64_t L = ceil_div(work, G);
+        const int64_t units = num_sms / cg;            // CTAs or CTA pairs
+        int64_t G = units < work ? units : work;
+        int64_t L = ceil_div(work, G);
+        if (!swap) {
+            // A tile split s ways saves (1 - 1/s) of its K loop and costs its
+            // finisher s - 1 partial tiles read back through L2, each about
+            // `fixup` k-blocks of MMA time: beyond sqrt(k_blocks / fixup) ways a
+            // split costs more than it saves, and the ranges stay at least
+            // k_blocks / that long.
+            const double fixup = kSkFixupKBlocks * 256.0 / static_cast<double>(block_k * esize);
+            int64_t s_max = static_cast<int64_t>(
+                std::floor(std::sqrt(static_cast<double>(pl.k_blocks) / fixup)));
+            if (s_max < 1) s_max = 1;
+            const int64_t l_min = ceil_div(pl.k_blocks, s_max);
+            if (L < l_min) L = l_min;
+        }
         G = ceil_div(work, L);
         pl.sk_len = static_cast<int32_t>(L);
         pl.sk_max_seg = static_cast<int32_t>((L + pl.k_blocks - 2) / pl.k_blocks + 1);
-        pl.pub.grid = static_cast<int32_t>(G);
+        pl.pub.grid = static_cast<int32_t>(G * cg);
         pl.pub.split_k = static_cast<int32_t>(ceil_div(pl.k_blocks, L));
-        pl.partial_bytes = G * pl.sk_max_seg * (int64_t)kBlockM * bn * 4;
+        pl.partial_bytes = G * pl.sk_max_seg * block_m * bn * 4;
     } else {
         const int64_t units = num_sms / cg;
         pl.pub.grid = static_cast<int32_t>(cg * (tiles < units ? tiles : units));

@@ -94,8 +94,9 @@ struct TcParams {
     void* C;
     int64_t c_rs, c_cs;         // D'(i, j) -> C[i * c_rs + j * c_cs]
     int32_t c_vector;           // c_cs == 1 and rows 16-byte aligned
-    float* partials;            // stream-K slots: [G * sk_max_seg][BM][BN] FP32
-    int* tile_counters;         // stream-K: per split tile, contributors written (self-resetting)
+    float* partials;            // stream-K slots: [G * sk_max_seg][BN / 4][BM] float4 (FP32)
+    int* tile_counters;         // stream-K: per split tile and CTA of the pair, contributors
+                                // written (self-resetting)
     int* err;                   // device-visible error word (0 = ok)
     int32_t a_stream_once;      // 1: A is read once (evict-first in L2), 0: reused
     int32_t b_stream_once;
@@ -981,7 +982,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 finisher = (unit == g_first);
             }
             if (finisher) {
-                int* written = p.tile_counters + sg.tile;
+                // one counter per tile and CTA of the pair: CTA r of a pair
+                // finishes rows r * 128.. of the tile from the sums that CTA
+                // r of each contributing pair stored
+                int* written = p.tile_counters + sg.tile * CG + static_cast<int32_t>(rank);
                 if (warp == 2 && lane == 0) {
                     const bool w = wait_counter(written, g_last - g_first, &abort_flag, p.wait_limit_ns);
                     if (w) *written = 0;                    // self-resetting for the next call
@@ -998,7 +1002,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         #pragma unroll
                         for (int j = 0; j < 32; ++j) acc[j] = 0.0f;
                         // 16 columns at a time, up to kFinBatch slots' loads in
-                        // flight together
+                        // flight together; each warp load is 512 contiguous bytes
                         #pragma unroll
                         for (int h = 0; h < 2; ++h) {
                             for (int32_t g0 = g_first + 1; g0 <= g_last; g0 += kFinBatch) {
@@ -1009,24 +1013,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                                     if (g > g_last) continue;
                                     const int32_t first_tile =
                                         static_cast<int32_t>((static_cast<int64_t>(g) * L) / KB);
-                                    const float* src = p.partials +
-                                                       (static_cast<int64_t>(g) * p.sk_max_seg +
-                                                        (sg.tile - first_tile)) * BM * BN;
-                                    if (p.c_cs == 1) {
-                                        const float4* s4 = reinterpret_cast<const float4*>(
-                                            src + row_in_tile * BN + ch * 32 + h * 16);
-                                        #pragma unroll
-                                        for (int q = 0; q < 4; ++q) {
-                                            const float4 t = __ldcg(s4 + q);
-                                            x[u][4 * q] = t.x;
-                                            x[u][4 * q + 1] = t.y;
-                                            x[u][4 * q + 2] = t.z;
-                                            x[u][4 * q + 3] = t.w;
-                                        }
-                                    } else {
-                                        #pragma unroll
-                                        for (int j = 0; j < 16; ++j)
-                                            x[u][j] = __ldcg(src + (ch * 32 + h * 16 + j) * BM + row_in_tile);
+                                    const float4* s4 =
+                                        reinterpret_cast<const float4*>(
+                                            p.partials + (static_cast<int64_t>(g) * p.sk_max_seg +
+                                                          (sg.tile - first_tile)) * BM * BN) +
+                                        (ch * 8 + h * 4) * BM + row_in_tile;
+                                    #pragma unroll
+                                    for (int q = 0; q < 4; ++q) {
+                                        const float4 t = __ldcg(s4 + q * BM);
+                                        x[u][4 * q] = t.x;
+                                        x[u][4 * q + 1] = t.y;
+                                        x[u][4 * q + 2] = t.z;
+                                        x[u][4 * q + 3] = t.w;
                                     }
                                 }
                                 #pragma unroll
@@ -1081,17 +1079,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int32_t c0 = col0 + ch * 32;
                     if (my_slot == nullptr) {
                         store_chunk<OutT>(p, row, c0, v);
-                    } else if (p.c_cs == 1) {
-                        // raw FP32 sums, laid out along C's contiguous direction:
-                        // [row][col] when C rows are contiguous (c_cs == 1),
-                        // [col][row] otherwise, so every warp store is coalesced
-                        float4* dst = reinterpret_cast<float4*>(my_slot + row_in_tile * BN + ch * 32);
+                    } else {
+                        // raw FP32 sums as float4s of four columns, laid out
+                        // [column / 4][row]: the 32 rows of a warp store (and of
+                        // the finisher's load) are 512 contiguous bytes
+                        float4* dst = reinterpret_cast<float4*>(my_slot) + (ch * 8) * BM + row_in_tile;
                         #pragma unroll
                         for (int q = 0; q < 8; ++q)
-                            dst[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-                    } else {
-                        #pragma unroll
-                        for (int j = 0; j < 32; ++j) my_slot[(ch * 32 + j) * BM + row_in_tile] = v[j];
+                            dst[q * BM] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
                     }
                 }
             }
@@ -1106,7 +1101,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!finisher) {
                     __threadfence();                       // this thread's slot stores
                     epilogue_bar_sync();
-                    if (warp == 2 && lane == 0) atomicAdd(p.tile_counters + sg.tile, 1);
+                    if (warp == 2 && lane == 0)
+                        atomicAdd(p.tile_counters + sg.tile * CG + static_cast<int32_t>(rank), 1);
                 }
                 epilogue_bar_sync();                       // wait_ok is reused by the next tile
             }

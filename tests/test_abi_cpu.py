@@ -1,6 +1,7 @@
 """The C ABI library on the CPU: it loads, exports every symbol the header
 declares, validates arguments and plans paths (host logic only, no GPU)."""
 import ctypes
+import math
 import itertools
 import subprocess
 
@@ -126,8 +127,10 @@ def test_two_k_chunks_per_stage():
     assert p("N", "T", 1024, 1024, 1000)["block_k"] == 64            # K not a whole chunk
     assert p("T", "N", 1024, 1024, 1000)["block_k"] == 128           # both MN-major: zero fill
     assert p("N", "N", 1024, 1024, 1000)["block_k"] == 64            # A K-major
-    q = p("N", "T", 512, 3072, 4096)                                 # 1-SM 256 wide: 2 x 96 KB
+    q = p("N", "T", 200, 3072, 4096)                                 # 1-SM 256 wide: 2 x 96 KB
     assert (q["path_name"], q["block_n"], q["block_k"]) == ("tiled_1sm", 256, 64), q
+    q = p("N", "T", 512, 3072, 4096)                                 # CTA pairs, stream-K
+    assert (q["path_name"], q["block_n"], q["block_k"]) == ("tiled_2sm", 256, 128), q
     assert p("N", "T", 100, 100, 128, (DT_F32, DT_F32, DT_F32))["block_k"] == 64   # TF32: 2 x 32
     # convolutions: two chunks (two im2col boxes, one filter box) when C is a
     # whole number of 64-channel blocks; 9 taps x 1 block = 9 chunks, 5 stages
@@ -139,10 +142,15 @@ def test_two_k_chunks_per_stage():
     assert st == 0 and c["block_k"] == 64 and c["k_blocks"] == 18, c
     # a convolution on single-CTA 256-wide tiles keeps two chunks in two
     # stages (operands re-read from L2); a GEMM of that tile keeps one chunk
-    st, c = lib.conv2d_plan_query(32, 14, 14, 512, 512, 3, 3, (1, 1), (1, 1), (1, 1), 1.0, 256, 256,
+    st, c = lib.conv2d_plan_query(1, 14, 14, 64, 19456, 3, 3, (1, 1), (1, 1), (1, 1), 1.0, 256, 256,
                                   0.0, 256, (DT_BF16, DT_BF16, DT_BF16))
     assert st == 0 and (c["path_name"], c["block_n"], c["block_k"], c["stages"]) == \
         ("tiled_1sm", 256, 128, 2), c
+    # the 14 x 14 layer, C = K = 512: too few pair tiles, long K -> stream-K on CTA pairs
+    st, c = lib.conv2d_plan_query(32, 14, 14, 512, 512, 3, 3, (1, 1), (1, 1), (1, 1), 1.0, 256, 256,
+                                  0.0, 256, (DT_BF16, DT_BF16, DT_BF16))
+    assert st == 0 and (c["path_name"], c["block_n"], c["block_k"], c["stages"]) == \
+        ("tiled_2sm", 256, 128, 3) and c["sk_len"] > 0, c
 
 
 def test_quick_paths_and_swap_rule():
@@ -237,7 +245,9 @@ def simulate_stream_k(p):
     the finisher of every split tile (the CTA holding its first k-blocks) meets
     it in the last segment of its range -- so its other TMEM buffer is free
     for the pre-summed partials and it is the contributor that ends last."""
-    T, KB, L, G, S = p["num_tiles"], p["k_blocks"], p["sk_len"], p["grid"], p["sk_max_seg"]
+    cg = 2 if p["path_name"] == "tiled_2sm" else 1          # CTAs per unit (a pair shares a range)
+    assert p["grid"] % cg == 0
+    T, KB, L, G, S = p["num_tiles"], p["k_blocks"], p["sk_len"], p["grid"] // cg, p["sk_max_seg"]
     total = T * KB
     covered = [0] * total
     slots = {}
@@ -268,8 +278,8 @@ def simulate_stream_k(p):
             slot = g * S + tile - (g * L) // KB
             assert slots.get(slot) == (tile, g)
         assert last_tile[g_first] == tile
-    assert T <= 1024                  # one int32 counter per tile in the 4 KB header
-    assert len(slots) * 128 * p["block_n"] * 4 <= p["workspace_bytes"]
+    assert T * cg <= 1024             # one int32 counter per tile and CTA in the 4 KB header
+    assert len(slots) * p["block_m"] * p["block_n"] * 4 <= p["workspace_bytes"]
 
 
 @pytest.mark.parametrize("shape", [(256, 256, 256), (1024, 1024, 1024), (1000, 1023, 777),
@@ -296,16 +306,43 @@ def test_stream_k_only_for_skinny_tile_starved_or_badly_filled_long_k():
     assert P(1, 1, 100000)["sk_len"] > 0
     # data-parallel waves filled below 80 % with 32+ k-blocks per tile: stream-K
     # over the widest single-CTA tiles, possibly more tiles than SMs
+    # over the widest tiles, on CTA pairs when M has 256 rows
     p = P(6272, 512, 4608)                           # 196 tiles of 128 x 128: 1.29 waves
-    assert p["sk_len"] > 0 and p["block_n"] == 256 and p["path_name"] == "tiled_1sm"
+    assert p["sk_len"] > 0 and p["block_n"] == 256 and p["path_name"] == "tiled_2sm"
     p = P(25088, 256, 4096)                          # 98 CTA-pair tiles on 76 pairs
-    assert p["sk_len"] > 0 and p["num_tiles"] > 152 and p["grid"] <= 152
+    assert p["sk_len"] > 0 and p["num_tiles"] == 98 and p["grid"] <= 152
+    assert p["path_name"] == "tiled_2sm"
+    p = P(200, 3072, 4096)                           # 24 tiles, fewer than 256 rows: single CTAs
+    assert p["sk_len"] > 0 and p["block_n"] == 256 and p["path_name"] == "tiled_1sm"
     assert P(25088, 128, 1152)["sk_len"] == 0        # same fill, 18 k-blocks: not worth it
     assert P(65536, 256, 2304)["path_name"] == "tiled_2sm"   # 256 pair tiles: 84 % fill
     for shape in [(1024, 1024, 1024), (1000, 1023, 777), (256, 256, 256), (300, 520, 1000)]:
         assert P(*shape)["sk_len"] == 0, shape
     assert P(1024, 1024, 1024)["block_n"] == 64      # 128 tiles of 128 x 64
     assert P(256, 256, 256)["num_tiles"] >= 4
+
+
+@pytest.mark.parametrize("shape", [(256, 256, 2048), (2048, 256, 4096), (300, 2048, 4096),
+                                   (512, 3072, 4096), (6272, 512, 4608), (1536, 2048, 14336),
+                                   (200, 3072, 4096), (257, 129, 4096), (33, 128, 2048)])
+def test_stream_k_split_is_capped(shape):
+    """A tile split s ways saves (1 - 1/s) of its K loop and costs its finisher
+    s - 1 partial tiles read back, each worth about 8 k-blocks of 256-byte rows:
+    ranges are at least k_blocks / floor(sqrt(k_blocks / 8)) long (the skinny
+    weight-streaming path excepted), so no tile has more contributors than
+    that bound plus one."""
+    M, N, K = shape
+    w = workloads.Workload("s", M, N, K, "N", "T", DT_BF16, DT_BF16, 1.0, 0.0, "U", "U")
+    p = plan(w)
+    KB, L = p["k_blocks"], p["sk_len"]
+    fixup = 8.0 * 256 / (p["block_k"] * 2)
+    s_max = max(1, int(math.floor(math.sqrt(KB / fixup))))
+    if L and p["path_name"] != "skinny":
+        assert L >= -(-KB // s_max), p
+        for tile in range(p["num_tiles"]):
+            assert ((tile + 1) * KB - 1) // L - (tile * KB) // L + 1 <= s_max + 1
+    if shape == (256, 256, 2048):                    # 16 k-blocks: never split
+        assert L in (0, KB), p
 
 
 def test_create_fails_cleanly_without_gpu():

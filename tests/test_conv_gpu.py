@@ -145,19 +145,34 @@ def test_cta_pairs_and_stream_k(g, orc):
     run_and_check(g, orc, long_k, dt=DT_BF16, ydt=DT_BF16, integer=False, seed=3)
 
 
-def test_single_cta_wide_tiles_two_chunks(g, orc):
-    """The 32 x 14 x 14, C = K = 512 layer: single-CTA 256-wide tiles with two
-    K chunks per stage in two stages, stream-K over 36 stages; sampled pixels
-    (every 37th and the last) against the oracle, both input types."""
+def test_pair_stream_k_full_layer(g, orc):
+    """The 32 x 14 x 14, C = K = 512 layer: 50 CTA-pair tiles, fewer than the
+    SM pairs, with two K chunks per stage in three stages and stream-K over
+    36 stages per tile; sampled pixels (every 37th and the last) against the
+    oracle, both input types."""
     import mixed_precision_dense_sm_gb300 as lib
     geo = (32, 14, 14, 512, 512, 3, 3, (1, 1), (1, 1), (1, 1))
     st, p = lib.conv2d_plan_query(*geo, 1.0, 256, 256, 0.0, 1 << 44, (DT_BF16, DT_BF16, DT_BF16),
                                   num_sms=torch.cuda.get_device_properties(0).multi_processor_count)
     assert st == 0 and (p["path_name"], p["block_n"], p["block_k"], p["stages"]) == \
-        ("tiled_1sm", 256, 128, 2), p
+        ("tiled_2sm", 256, 128, 3) and p["sk_len"] > 0, p
     sample = lambda M: np.unique(np.concatenate([np.arange(0, M, 37), [M - 1, 1, 2]]))
     run_and_check(g, orc, geo, dt=DT_BF16, ydt=DT_BF16, integer=True, sample=sample)
     run_and_check(g, orc, geo, dt=DT_F16, ydt=DT_F32, integer=False, beta=1.0, sample=sample)
+
+
+def test_single_cta_wide_tiles_two_chunks(g, orc):
+    """196 output pixels by 19456 filters, C = 64: 152 single-CTA 256-wide
+    tiles with two K chunks per stage in two stages (the operands are re-read
+    from L2); sampled pixels against the oracle."""
+    import mixed_precision_dense_sm_gb300 as lib
+    geo = (1, 14, 14, 64, 19456, 3, 3, (1, 1), (1, 1), (1, 1))
+    st, p = lib.conv2d_plan_query(*geo, 1.0, 256, 256, 0.0, 1 << 44, (DT_BF16, DT_BF16, DT_BF16),
+                                  num_sms=torch.cuda.get_device_properties(0).multi_processor_count)
+    assert st == 0 and (p["path_name"], p["block_n"], p["block_k"], p["stages"]) == \
+        ("tiled_1sm", 256, 128, 2), p
+    sample = lambda M: np.unique(np.concatenate([np.arange(0, M, 13), [M - 1, 1, 2]]))
+    run_and_check(g, orc, geo, dt=DT_BF16, ydt=DT_BF16, integer=True, sample=sample)
 
 
 def test_errors_enqueue_nothing(g):

@@ -81,6 +81,14 @@ def test_fused_epilogue_paths(g, orc, M, N, K, ta, tb, path):
               seed=M + n, path=path if n == 0 else None)
 
 
+def test_fused_epilogue_pair_stream_k(g, orc):
+    """Stream-K on CTA pairs: 20 pair tiles of 256 x 256, each split in two,
+    so the finishing pair adds its partner's partial sums before the fused
+    bias, residual and GELU."""
+    _case(g, orc, 512, 2432, 4096, "N", "T", DT_BF16, DT_BF16, 2, DT_F32, 1.0, seed=11,
+          path=("tiled_2sm", True))
+
+
 def test_fused_epilogue_quick_return(g, orc):
     """K == 0: C = act(beta * C + bias)."""
     for act, beta in itertools.product(ACTS, (0.0, 1.5)):

@@ -221,16 +221,19 @@ def test_cta_pair_tiles_integer_exact(g, orc, M, N, K):
         gc.check_full(orc, w, inp, C, exact=True)
 
 
-BALANCE_SHAPES = [(2560, 1000, 2048), (20480, 256, 2048)]
+BALANCE_SHAPES = [(2560, 1000, 4096, "tiled_2sm", 256), (20480, 256, 2048, "tiled_2sm", 256),
+                  (200, 3072, 4096, "tiled_1sm", 256), (2048, 256, 4096, "tiled_1sm", 128)]
 
 
-@pytest.mark.parametrize("M,N,K", BALANCE_SHAPES, ids=[f"{m}x{n}x{k}" for m, n, k in BALANCE_SHAPES])
-def test_wave_balancing_stream_k_integer_exact(g, orc, M, N, K):
-    """Shapes whose data-parallel last wave would leave most SMs idle: the
-    planner runs single-CTA stream-K over 128 x 256 tiles instead -- 2560 x
-    1000 with fewer tiles than SMs, 20480 x 256 with more (each CTA's range
-    then spans whole tiles as well as split ones).  Bit-exact with integer
-    inputs."""
+@pytest.mark.parametrize("M,N,K,path,bn", BALANCE_SHAPES,
+                         ids=[f"{m}x{n}x{k}" for m, n, k, _, _ in BALANCE_SHAPES])
+def test_wave_balancing_stream_k_integer_exact(g, orc, M, N, K, path, bn):
+    """Shapes whose data-parallel schedule would leave most SMs idle run
+    stream-K: over 256 x 256 CTA-pair tiles when M has 256 rows -- 2560 x 1000
+    with fewer tiles than pairs (tiles split up to three ways, each CTA of the
+    finishing pair summing its own half), 20480 x 256 with more (each pair's
+    range then spans whole tiles as well as split ones) -- else over
+    single-CTA tiles.  Bit-exact with integer inputs."""
     import mixed_precision_dense_sm_gb300 as lib
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     for ta, tb in (("N", "T"), ("T", "N")):
@@ -239,7 +242,8 @@ def test_wave_balancing_stream_k_integer_exact(g, orc, M, N, K):
         lda, ldb, ldc = w.lds()
         st, plan = lib.gemm_plan_query(ta, tb, M, N, K, 1.0, 256, lda, 256, ldb, w.beta, 256, ldc,
                                        (w.ab_dtype, w.ab_dtype, w.c_dtype), num_sms=sms)
-        assert st == 0 and plan["sk_len"] > 0 and plan["block_n"] == 256, plan
+        assert st == 0 and plan["sk_len"] > 0, plan
+        assert (plan["path_name"], plan["block_n"]) == (path, bn), plan
         inp = gc.integer_inputs(w)
         C = gc.run_gpu(g, w, inp)
         gc.check_full(orc, w, inp, C, exact=True)
