@@ -266,7 +266,9 @@ gemm_status_t make_plan(char transA, char transB, int64_t M, int64_t N, int64_t 
     bool pair_sk = false;
     if (!pairs && !ln && !swap && bn == 256 && pl.Mk >= 2 * kBlockM && num_sms >= 2) {
         const int64_t t1 = tiles_m * ceil_div(pl.Nk, bn);
-        if (t1 <= kMaxCounterTiles && (balance_sk || (t1 < half_wave && long_k))) {
+        // one counter per tile and CTA of the pair
+        const bool fits = pair_tiles * 2 <= kMaxCounterTiles;
+        if (fits && t1 <= kMaxCounterTiles && (balance_sk || (t1 < half_wave && long_k))) {
             pair_sk = pairs = true;
             cg = 2;
             block_m = 2 * kBlockM;
