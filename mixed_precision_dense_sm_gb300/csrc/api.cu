@@ -38,6 +38,9 @@ constexpr int64_t kMaxCounterTiles = kWsHeaderBytes / 4;
 // schedules whose last wave leaves more than 1 - kMinWaveFill of the GPU idle.
 constexpr int32_t kLongK = 32;
 constexpr double kMinWaveFill = 0.8;
+// An operand read once and at least this large (about three quarters of the
+// GB300 L2) is loaded evict-first so that it does not push reused data out.
+constexpr int64_t kStreamOnceBytes = 96ll << 20;
 // Stream-K fix-up: one FP32 partial tile read back by the finisher costs about
 // as long as this many k-blocks of 256 bytes per row (128 BF16 / FP16 or 64
 // TF32 elements) of the tile's MMA (measured on GB300).
@@ -673,9 +676,15 @@ gemm_status_t enqueue_plan(const Plan& pl, EncodeTiledFn encode, int num_sms, ui
     p.err = err_dev;
     // In the swapped skinny path each tile of A' (the large operand) is read
     // by exactly one CTA while B' (the few rows of the original A) is re-read
-    // by every CTA.
-    p.a_stream_once = pl.pub.swap_ab ? 1 : 0;
-    p.b_stream_once = 0;
+    // by every CTA.  Likewise a GEMM with one tile column reads each row
+    // panel of A once, and one with one tile row each column panel of B (a
+    // convolution re-reads its input once per filter tap: never).  A smaller
+    // operand read once stays evict-last: it fits in L2 beside the rest, and a
+    // caller that runs the GEMM again on it finds it there.
+    const bool a_big = pl.a.rows * pl.a.cols * pl.esize >= kStreamOnceBytes;
+    const bool b_big = pl.b.rows * pl.b.cols * pl.esize >= kStreamOnceBytes;
+    p.a_stream_once = (pl.pub.swap_ab || (conv == nullptr && pl.tiles_n == 1 && a_big)) ? 1 : 0;
+    p.b_stream_once = (!pl.pub.swap_ab && conv == nullptr && pl.tiles_m == 1 && b_big) ? 1 : 0;
     p.wait_limit_ns = wait_limit_ns ? wait_limit_ns : kWaitTimeoutNs;
     p.debug_flags = debug_flags;
     p.bias = ep ? ep->bias : nullptr;
