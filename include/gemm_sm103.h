@@ -264,6 +264,9 @@ typedef struct {
                               operand is stored M/N-contiguous and a pre-pass rewrites it
                               K-contiguous into the workspace (kind::tf32 reads K-major
                               operands only) */
+    int32_t c_tma;         /* 1: the epilogue stages C in shared memory and stores it by TMA
+                              (C rows 16-byte aligned, beta == 0, FP32 C or two or more
+                              data-parallel tiles per CTA); 0: per-thread row stores */
     int64_t workspace_bytes;
 } gemm_plan_t;
 

@@ -65,7 +65,7 @@ class Plan(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "path", "block_m", "block_n", "block_k", "stages", "split_k", "grid", "num_tiles",
         "pack_a", "pack_b", "a_mn_major", "b_mn_major", "swap_ab", "c_vector", "sk_len",
-        "sk_max_seg", "k_blocks", "tiles_m", "tiles_n", "transpose_ab")] + \
+        "sk_max_seg", "k_blocks", "tiles_m", "tiles_n", "transpose_ab", "c_tma")] + \
         [("workspace_bytes", ctypes.c_int64)]
 
     def as_dict(self):

@@ -75,6 +75,9 @@ struct Plan {
     bool ln;
     bool ln_fused;
     int64_t ln_stats_bytes;
+    // the plain epilogue stores C through shared memory by TMA (C rows
+    // 16-byte aligned, not swapped): kCStageBytes of staging after the stages
+    bool c_tma;
 };
 
 bool is_n(char t) { return t == 'N' || t == 'n'; }
@@ -291,7 +294,15 @@ gemm_status_t make_plan(char transA, char transB, int64_t M, int64_t N, int64_t 
     const int64_t barrier_bytes = 256;
     // static shared memory of the kernel: flags, and the LayerNorm exchange
     const int64_t static_bytes = 64 + (ln ? 4 * kBlockM * 4 : 4);
-    const int64_t avail = smem_optin - 1024 - barrier_bytes - static_bytes;
+    // C may be stored by TMA from a 32 KB staging area (decided below, with
+    // the schedule): 128-row boxes of 128 bytes, full lines and one store per
+    // box, where per-thread row stores each write 16 bytes of 32 different
+    // lines.  The K chunks per stage are chosen with the staging set aside;
+    // without it the stages are counted again (shared memory the kernel does
+    // not use is left to the L1 cache).
+    const bool c_stage_ok = pl.pub.c_vector && !ln;
+    const int64_t avail_all = smem_optin - 1024 - barrier_bytes - static_bytes;
+    const int64_t avail = avail_all - (c_stage_ok ? kCStageBytes : 0);
     pl.kc = (kc2_ok && avail / (2 * static_cast<int64_t>(chunk_bytes)) >= min_kc2_stages) ? 2 : 1;
     const int64_t block_k = chunk_k * pl.kc;
     pl.k_blocks = static_cast<int32_t>(ceil_div(K, block_k));
@@ -337,6 +348,22 @@ gemm_status_t make_plan(char transA, char transB, int64_t M, int64_t N, int64_t 
     } else {
         const int64_t units = num_sms / cg;
         pl.pub.grid = static_cast<int32_t>(cg * (tiles < units ? tiles : units));
+    }
+    // TMA stores of C pay off where a tile's stores overlap later tiles'
+    // mainloops (data-parallel, two or more tiles per CTA or pair) and for
+    // FP32 C (a chunk is 32 rows of 128 bytes); with a residual (beta != 0)
+    // the reads of C come first and the staging steps' barriers serialise
+    // them, and a lone or last tile pays the steps' latency: row stores there.
+    pl.c_tma = c_stage_ok && beta == 0.0f &&
+               (dt.c == GEMM_F32 || (!stream_k && tiles >= 2 * (num_sms / cg)));
+    pl.pub.c_tma = pl.c_tma ? 1 : 0;
+    if (pl.c_tma) {
+        pl.smem_bytes += kCStageBytes;
+    } else if (c_stage_ok) {
+        int64_t s_all = avail_all / stage_bytes;
+        if (s_all > kMaxStages) s_all = kMaxStages;
+        pl.pub.stages = static_cast<int32_t>(s_all);
+        pl.smem_bytes = static_cast<size_t>(s_all * stage_bytes + 1024 + barrier_bytes);
     }
     pl.pub.path = swap ? GEMM_PATH_SKINNY : (pairs ? GEMM_PATH_TILED_2SM : GEMM_PATH_TILED_1SM);
     pl.pub.sk_len = pl.sk_len;
@@ -429,6 +456,24 @@ bool encode_operand(EncodeTiledFn encode, CUtensorMap* map, int32_t dtype, const
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     }
     return r == CUDA_SUCCESS;
+}
+
+// C (rows x cols, row pitch ld elements) for the epilogue's TMA stores:
+// boxes of 128 bytes of a row (64 16-bit or 32 FP32 elements) by 128 rows,
+// 128-byte swizzle; the parts of a box outside C are not written.
+bool encode_c_store(EncodeTiledFn encode, CUtensorMap* map, int32_t dtype, const void* ptr,
+                    int64_t cols, int64_t rows, int64_t ld) {
+    const int64_t es = out_elem_bytes(dtype);
+    const CUtensorMapDataType ty = dtype == GEMM_F32    ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                   : dtype == GEMM_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                        : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld * es)};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(128 / es), static_cast<cuuint32_t>(kBlockM)};
+    const cuuint32_t estr[2] = {1, 1};
+    return encode(map, ty, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 // The input X (N, H, W, C) as an im2col map: windows traversed W, H, N with
@@ -646,6 +691,7 @@ gemm_status_t enqueue_plan(const Plan& pl, EncodeTiledFn encode, int num_sms, ui
                                   pl.b.mn_major ? 1 : pl.kc);
     }
     if (!ok) return GEMM_ERR_LAUNCH;
+    const bool c_tma = pl.c_tma && encode_c_store(encode, &l.tmC, dt.c, C, pl.Nk, pl.Mk, pl.c_rs);
 
     TcParams& p = l.p;
     p.M = static_cast<int32_t>(pl.Mk);
@@ -671,6 +717,7 @@ gemm_status_t enqueue_plan(const Plan& pl, EncodeTiledFn encode, int num_sms, ui
     p.c_rs = pl.c_rs;
     p.c_cs = pl.c_cs;
     p.c_vector = pl.pub.c_vector;
+    p.c_tma = c_tma ? 1 : 0;
     p.partials = pl.partial_bytes > 0 ? ws_part : nullptr;
     p.tile_counters = pl.partial_bytes > 0 ? counters : nullptr;
     p.err = err_dev;

@@ -73,6 +73,10 @@ constexpr int kMaxKc = 2;
 constexpr int kThreads = 320;     // warp 0 producer, warp 1 MMA, warps 2-9 epilogue
 constexpr int kEpiWarps = 8;      // two per TMEM lane quarter, splitting the columns
 constexpr int kFinBatch = 2;      // stream-K finisher: partial slots loaded per batch
+// Staging for C stores by TMA: 32 KB after the pipeline stages, two boxes of
+// 128 rows x 128 bytes (128-byte swizzle), each 1024-byte aligned.
+constexpr uint32_t kCStageBytes = 32768;
+constexpr uint32_t kCBoxBytes = 16384;
 constexpr uint32_t kATileBytes = kBlockM * 128;          // 16 KB: 128 rows of 128 bytes
 
 enum : int { kErrTimeoutProducer = 1, kErrTimeoutMma = 2, kErrTimeoutEpilogue = 3 };
@@ -94,6 +98,7 @@ struct TcParams {
     void* C;
     int64_t c_rs, c_cs;         // D'(i, j) -> C[i * c_rs + j * c_cs]
     int32_t c_vector;           // c_cs == 1 and rows 16-byte aligned
+    int32_t c_tma;              // C stored through shared memory by TMA (tmC, plain epilogue)
     float* partials;            // stream-K slots: [G * sk_max_seg][BN / 4][BM] float4 (FP32)
     int* tile_counters;         // stream-K: per split tile and CTA of the pair, contributors
                                 // written (self-resetting)
@@ -345,65 +350,81 @@ __device__ __forceinline__ void bias_act(const TcParams& p, int32_t row, int32_t
     }
 }
 
-// Store 32 consecutive values v[0..31] of one C row at `dst` (16-byte aligned,
-// all in range): r = act(v + beta * C + bias).
+// act(alpha * v + beta * C + bias) in place for one row of 32 columns at D'
+// column c0, without the store (C is read only for columns < N; rows >= M,
+// which are never stored, are left as they are).
 template <typename OutT>
-__device__ __forceinline__ void store_row32_vec(const TcParams& p, OutT* dst, int32_t row,
-                                                int32_t c0, float (&v)[32]) {
-    constexpr int kPer16 = 16 / sizeof(OutT);      // elements per 16-byte vector
-    constexpr int kVecs = 32 / kPer16;
-    // Read every old value before the first store: a load that follows a
-    // store to the same array cannot be hoisted, and each would cost a full
-    // memory round trip.
-    if (p.beta != 0.0f) {
-        uint4 old[kVecs];
-        #pragma unroll
-        for (int q = 0; q < kVecs; ++q) old[q] = *reinterpret_cast<const uint4*>(dst + q * kPer16);
-        #pragma unroll
-        for (int q = 0; q < kVecs; ++q) {
-            const OutT* o = reinterpret_cast<const OutT*>(&old[q]);
-            #pragma unroll
-            for (int e = 0; e < kPer16; ++e)
-                v[q * kPer16 + e] = fmaf(p.beta, load_out<OutT>(o + e), v[q * kPer16 + e]);
-        }
-    }
-    bias_act(p, row, c0, v);
-    #pragma unroll
-    for (int q = 0; q < kVecs; ++q) {
-        uint4 pack;
-        OutT* pk = reinterpret_cast<OutT*>(&pack);
-        #pragma unroll
-        for (int e = 0; e < kPer16; ++e) pk[e] = cvt_out<OutT>(v[q * kPer16 + e]);
-        *reinterpret_cast<uint4*>(dst + q * kPer16) = pack;
-    }
-}
-
-// r = act(alpha * v + beta * C + bias) for one row of 32 columns starting at
-// D' column c0, cast and stored (vector stores when C rows are 16-byte aligned
-// and the chunk is whole, element stores otherwise).
-template <typename OutT>
-__device__ __forceinline__ void store_chunk(const TcParams& p, int32_t row, int32_t c0,
-                                            float (&v)[32]) {
-    OutT* C = reinterpret_cast<OutT*>(p.C);
+__device__ __forceinline__ void epilogue_values(const TcParams& p, int32_t row, int32_t c0,
+                                                float (&v)[32]) {
     if (p.alpha != 1.0f) {
         #pragma unroll
         for (int j = 0; j < 32; ++j) v[j] *= p.alpha;
     }
-    if (row >= p.M) return;
-    if (p.c_vector && c0 + 32 <= p.N) {
-        store_row32_vec<OutT>(p, C + static_cast<int64_t>(row) * p.c_rs + c0, row, c0, v);
-    } else {
-        OutT* base = C + static_cast<int64_t>(row) * p.c_rs;
-        if (p.beta != 0.0f) {
-            float old[32];
+    if (row >= p.M) return;                 // never stored
+    if (p.beta != 0.0f) {
+        const OutT* src = reinterpret_cast<const OutT*>(p.C) + static_cast<int64_t>(row) * p.c_rs;
+        if (p.c_vector && c0 + 32 <= p.N) {
+            constexpr int kPer16 = 16 / sizeof(OutT);
+            uint4 raw[32 / kPer16];
+            #pragma unroll
+            for (int q = 0; q < 32 / kPer16; ++q)
+                raw[q] = *reinterpret_cast<const uint4*>(src + c0 + q * kPer16);
+            #pragma unroll
+            for (int q = 0; q < 32 / kPer16; ++q) {
+                const OutT* o = reinterpret_cast<const OutT*>(&raw[q]);
+                #pragma unroll
+                for (int e = 0; e < kPer16; ++e)
+                    v[q * kPer16 + e] = fmaf(p.beta, load_out<OutT>(o + e), v[q * kPer16 + e]);
+            }
+        } else {
             #pragma unroll
             for (int j = 0; j < 32; ++j)
-                old[j] = (c0 + j < p.N) ? load_out<OutT>(base + static_cast<int64_t>(c0 + j) * p.c_cs)
-                                        : 0.0f;
-            #pragma unroll
-            for (int j = 0; j < 32; ++j) v[j] = fmaf(p.beta, old[j], v[j]);
+                if (c0 + j < p.N)
+                    v[j] = fmaf(p.beta, load_out<OutT>(src + static_cast<int64_t>(c0 + j) * p.c_cs),
+                                v[j]);
         }
-        bias_act(p, row, c0, v);
+    }
+    bias_act(p, row, c0, v);
+}
+
+// Writes v[0..31], cast to the output type, to row r of a staging box whose
+// rows are 128 bytes with the 128-byte swizzle (16-byte unit u of row r sits
+// at unit u ^ (r % 8)), from 16-byte unit u0 of the row on.  Eight
+// consecutive rows write eight different bank groups.
+template <typename OutT>
+__device__ __forceinline__ void stage_row32(uint8_t* box, int r, int u0, const float (&v)[32]) {
+    constexpr int kPer16 = 16 / sizeof(OutT);
+    uint8_t* base = box + r * 128;
+    #pragma unroll
+    for (int q = 0; q < 32 / kPer16; ++q) {
+        uint4 pack;
+        OutT* pk = reinterpret_cast<OutT*>(&pack);
+        #pragma unroll
+        for (int e = 0; e < kPer16; ++e) pk[e] = cvt_out<OutT>(v[q * kPer16 + e]);
+        *reinterpret_cast<uint4*>(base + (((u0 + q) ^ (r & 7)) << 4)) = pack;
+    }
+}
+
+// Stores v[0..31] (final values), cast to the output type, to C row `row`
+// at D' columns c0..c0+31: 16-byte vector stores when the chunk is whole and
+// C's rows are aligned, element stores (columns < N) otherwise; rows >= M
+// are not stored.
+template <typename OutT>
+__device__ __forceinline__ void store_row32(const TcParams& p, int32_t row, int32_t c0,
+                                            const float (&v)[32]) {
+    if (row >= p.M) return;
+    OutT* base = reinterpret_cast<OutT*>(p.C) + static_cast<int64_t>(row) * p.c_rs;
+    if (p.c_vector && c0 + 32 <= p.N) {
+        constexpr int kPer16 = 16 / sizeof(OutT);
+        #pragma unroll
+        for (int q = 0; q < 32 / kPer16; ++q) {
+            uint4 pack;
+            OutT* pk = reinterpret_cast<OutT*>(&pack);
+            #pragma unroll
+            for (int e = 0; e < kPer16; ++e) pk[e] = cvt_out<OutT>(v[q * kPer16 + e]);
+            *reinterpret_cast<uint4*>(base + c0 + q * kPer16) = pack;
+        }
+    } else {
         #pragma unroll
         for (int j = 0; j < 32; ++j)
             if (c0 + j < p.N) base[static_cast<int64_t>(c0 + j) * p.c_cs] = cvt_out<OutT>(v[j]);
@@ -621,7 +642,7 @@ __device__ __forceinline__ void ln_tile(const TcParams& p, uint32_t t_row, int32
 template <int CG, int BN, typename OutT, int ES, int EPI = kEpiPlain, int KC = 1>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const __grid_constant__ TcParams p) {
+                   const __grid_constant__ CUtensorMap tmC, const __grid_constant__ TcParams p) {
     static_assert(BN == 64 || BN == 128 || BN == 256, "BN");
     static_assert(EPI == kEpiPlain || EPI == kEpiLayerNorm, "epilogue");
     static_assert(KC == 1 || KC == 2, "K chunks per stage");
@@ -640,6 +661,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr uint32_t kATile = static_cast<uint32_t>(kc) * kATileBytes;
     constexpr uint32_t kBTile = static_cast<uint32_t>(kc) * kBRows * 128u;
     constexpr uint32_t kStageBytes = kATile + kBTile;
+    static_assert(kStageBytes % 1024 == 0, "stages keep the C staging boxes 1024-byte aligned");
     constexpr uint32_t kChunkBytes = static_cast<uint32_t>(kBlockK) * 128u;   // one MN-major box
     constexpr uint32_t kTmemCols = 2 * BN;               // double-buffered accumulator
 
@@ -647,7 +669,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     const int S = p.stages;
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + S * kStageBytes);
+    // [stages][C staging, when C is stored by TMA][barriers]
+    uint8_t* cstage = smem + S * kStageBytes;
+    uint64_t* full = reinterpret_cast<uint64_t*>(cstage + (p.c_tma ? kCStageBytes : 0u));
     uint64_t* empty = full + S;
     uint64_t* acc_full = empty + S;
     uint64_t* acc_empty = acc_full + 2;
@@ -675,6 +699,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_barrier_init();
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
+        if (p.c_tma) tma_prefetch_desc(&tmC);
     }
     if (warp == 1) {
         if constexpr (CG == 1) {
@@ -946,6 +971,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int row_in_cta = quarter * 32 + lane;
         const int row_in_tile = static_cast<int>(rank) * kBlockM + row_in_cta;
         uint32_t acc_i = 0;
+        uint32_t cstep = 0;                     // TMA-store steps so far (the same in every warp)
         SegmentIter it(p, unit, units);
         Segment sg;
         __shared__ int wait_ok;
@@ -1045,8 +1071,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             ok = ok && wait_or_abort(&acc_full[buf], (acc_i >> 1) & 1u, &abort_flag, p.wait_limit_ns);
-            // stream-K and LayerNorm use named barriers below
-            if (p.stream_k || EPI == kEpiLayerNorm) ok = epilogue_all(ok);
+            // stream-K, LayerNorm and the TMA store of C use named barriers below
+            if (p.stream_k || EPI == kEpiLayerNorm || p.c_tma) ok = epilogue_all(ok);
             if (!ok) {
                 record_error(p, kErrTimeoutEpilogue, &abort_flag);
                 break;
@@ -1077,8 +1103,46 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(o[j]) + v[j];
                     }
                     const int32_t c0 = col0 + ch * 32;
-                    if (my_slot == nullptr) {
-                        store_chunk<OutT>(p, row, c0, v);
+                    if (my_slot == nullptr) epilogue_values<OutT>(p, row, c0, v);
+                    if (my_slot == nullptr && p.c_tma) {
+                        // C through shared memory: step ch / 2 of the tile is
+                        // 64 columns (one 32-column chunk per half); the eight
+                        // warps fill the staging box(es) and one thread stores
+                        // them by TMA
+                        uint8_t* box;
+                        int u0;
+                        if constexpr (sizeof(OutT) == 4) {
+                            box = cstage + half * kCBoxBytes;      // 32 columns per box
+                            u0 = 0;
+                        } else {
+                            box = cstage + (cstep & 1u) * kCBoxBytes;   // 64 columns, two buffers
+                            u0 = 4 * half;
+                        }
+                        if (warp == 2 && lane == 0) {
+                            // the box's previous store has finished reading it
+                            if constexpr (sizeof(OutT) == 4) bulk_wait_group_read<0>();
+                            else bulk_wait_group_read<1>();
+                        }
+                        epilogue_bar_sync();
+                        stage_row32<OutT>(box, row_in_cta, u0, v);
+                        fence_proxy_async_shared();
+                        epilogue_bar_sync();
+                        if (warp == 2 && lane == 0) {
+                            const int32_t y = tm * BM + static_cast<int32_t>(rank) * kBlockM;
+                            const int32_t x = col0 + (ch >> 1) * 64;
+                            if (y < p.M) {
+                                if constexpr (sizeof(OutT) == 4) {
+                                    if (x < p.N) tma_store_2d(&tmC, cstage, x, y);
+                                    if (x + 32 < p.N) tma_store_2d(&tmC, cstage + kCBoxBytes, x + 32, y);
+                                } else {
+                                    if (x < p.N) tma_store_2d(&tmC, box, x, y);
+                                }
+                            }
+                            bulk_commit_group();
+                        }
+                        ++cstep;
+                    } else if (my_slot == nullptr) {
+                        store_row32<OutT>(p, row, c0, v);
                     } else {
                         // raw FP32 sums as float4s of four columns, laid out
                         // [column / 4][row]: the 32 rows of a warp store (and of
@@ -1107,6 +1171,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 epilogue_bar_sync();                       // wait_ok is reused by the next tile
             }
         }
+        // the C stores have written global memory and released the staging
+        // boxes before the CTA moves on to exit
+        if (p.c_tma && warp == 2 && lane == 0) bulk_wait_group_all();
     }
 
     tc_fence_before_sync();

@@ -46,7 +46,7 @@ static cudaError_t launch_tc_cfg(const TcLaunch& l) {
     cfg.numAttrs = 1;
     if constexpr (CG == 1) {
         cfg.gridDim = dim3(l.grid, 1, 1);
-        return cudaLaunchKernelEx(&cfg, kern, l.tmA, l.tmB, l.p);
+        return cudaLaunchKernelEx(&cfg, kern, l.tmA, l.tmB, l.tmC, l.p);
     } else {
         attr[1].id = cudaLaunchAttributeClusterDimension;
         attr[1].val.clusterDim.x = 2;
@@ -81,7 +81,7 @@ static cudaError_t launch_tc_cfg(const TcLaunch& l) {
             if (clusters > 0 && grid > 2 * clusters) grid = 2 * clusters;
         }
         cfg.gridDim = dim3(grid, 1, 1);
-        return cudaLaunchKernelEx(&cfg, kern, l.tmA, l.tmB, l.p);
+        return cudaLaunchKernelEx(&cfg, kern, l.tmA, l.tmB, l.tmC, l.p);
     }
 }
 

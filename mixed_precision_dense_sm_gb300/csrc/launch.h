@@ -11,6 +11,7 @@ namespace gemm103 {
 
 struct TcLaunch {
     CUtensorMap tmA, tmB;
+    CUtensorMap tmC;    // C for the epilogue's TMA stores (p.c_tma), else unused
     TcParams p;
     int grid;
     int cta_group;      // 1: single-CTA tiles, 2: CTA-pair tiles

@@ -19,12 +19,24 @@ def _args(w, inp, A, B, C):
             inp.ldb, w.beta, C.data_ptr(), inp.ldc, (w.ab_dtype, w.ab_dtype, w.c_dtype))
 
 
+# 50 pair tiles of 256 x 256, fewer than the SM pairs: stream-K over CTA pairs
+PAIR_SK = workloads.Workload("pair_sk_6272x512x4608", 6272, 512, 4608, "N", "T", workloads.DT_BF16,
+                             workloads.DT_F32, 1.0, 0.0, "U", "U")
+
+
 @pytest.mark.parametrize("name", ["square1024_f16_nt_f16out",       # single-CTA tiles
                                   "skinny_64x16384x8192_f16",       # stream-K, split tiles
-                                  "linear_8192x4096x4096_bf16"])    # CTA pairs
+                                  "linear_8192x4096x4096_bf16",     # CTA pairs
+                                  "pair_sk"])                       # stream-K on CTA pairs
 def test_timeout_is_reported_and_handle_recovers(orc, name):
     import mixed_precision_dense_sm_gb300 as lib
-    w = workloads.WORKLOADS[name]
+    w = PAIR_SK if name == "pair_sk" else workloads.WORKLOADS[name]
+    if name == "pair_sk":
+        lda, ldb, ldc = w.lds()
+        st, plan = lib.gemm_plan_query("N", "T", w.M, w.N, w.K, 1.0, 256, lda, 256, ldb, 0.0, 256,
+                                       ldc, (w.ab_dtype, w.ab_dtype, w.c_dtype),
+                                       num_sms=torch.cuda.get_device_properties(0).multi_processor_count)
+        assert st == 0 and plan["path_name"] == "tiled_2sm" and plan["sk_len"] > 0, plan
     inp = workloads.make_inputs(w)
     A, B = inp.A.cuda(), inp.B.cuda()
     C = torch.zeros((w.M, inp.ldc), dtype=workloads.TORCH_DTYPE[w.c_dtype], device="cuda")
