@@ -51,17 +51,26 @@ def _close(orc, w, inp, got, ref):
 
 
 CASES = ["skinny_64x16384x8192_f16", "ragged1000x1023x777_bf16_beta1",
-         "square1024_f16_nt_f16out"]
+         "square1024_f16_nt_f16out",
+         # FP32 C: the epilogue stages C in shared memory and stores it by TMA
+         workloads.Workload("noalloc_tma_store_1000x1000x256", 1000, 1000, 256, "N", "T", DT_BF16,
+                            DT_F32, 1.0, 0.0, "N1", "N1")]
 
 
 def test_noalloc_matches_gemm_run_twice(orc):
     """Two calls in a row per workload (scratch reused, stream-K partial sums
-    and packed operands), each checked against gemm_run."""
+    and packed operands, C stored by TMA), each checked against gemm_run."""
     import mixed_precision_dense_sm_gb300 as lib
     g = lib.Gemm()
     try:
         for name in CASES:
-            w = workloads.WORKLOADS[name]
+            w = workloads.WORKLOADS[name] if isinstance(name, str) else name
+            if not isinstance(name, str):
+                lda, ldb, ldc = w.lds()
+                st, plan = lib.gemm_plan_query(w.transA, w.transB, w.M, w.N, w.K, 1.0, 256, lda,
+                                               256, ldb, 0.0, 256, ldc,
+                                               (w.ab_dtype, w.ab_dtype, w.c_dtype))
+                assert st == 0 and plan["c_tma"] == 1, plan
             inp = workloads.make_inputs(w)
             ref = _run("run", w, inp, lib, g.h)
             for _ in range(2):
