@@ -265,8 +265,9 @@ typedef struct {
                               K-contiguous into the workspace (kind::tf32 reads K-major
                               operands only) */
     int32_t c_tma;         /* 1: the epilogue stages C in shared memory and stores it by TMA
-                              (C rows 16-byte aligned, beta == 0, FP32 C or two or more
-                              data-parallel tiles per CTA); 0: per-thread row stores */
+                              (C rows 16-byte aligned, beta == 0, and FP32 C with K >= 2048
+                              or two or more data-parallel tiles per CTA); 0: per-thread
+                              row stores */
     int64_t workspace_bytes;
 } gemm_plan_t;
 

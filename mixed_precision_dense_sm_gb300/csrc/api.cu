@@ -351,11 +351,12 @@ gemm_status_t make_plan(char transA, char transB, int64_t M, int64_t N, int64_t 
     }
     // TMA stores of C pay off where a tile's stores overlap later tiles'
     // mainloops (data-parallel, two or more tiles per CTA or pair) and for
-    // FP32 C (a chunk is 32 rows of 128 bytes); with a residual (beta != 0)
-    // the reads of C come first and the staging steps' barriers serialise
-    // them, and a lone or last tile pays the steps' latency: row stores there.
+    // FP32 C (a chunk is 32 rows of 128 bytes) once K is long enough (2048)
+    // that the steps' latency after a lone or last tile is small beside its
+    // mainloop; with a residual (beta != 0) the reads of C come first and the
+    // steps' barriers serialise them: row stores there.
     pl.c_tma = c_stage_ok && beta == 0.0f &&
-               (dt.c == GEMM_F32 || (!stream_k && tiles >= 2 * (num_sms / cg)));
+               ((dt.c == GEMM_F32 && K >= 2048) || (!stream_k && tiles >= 2 * (num_sms / cg)));
     pl.pub.c_tma = pl.c_tma ? 1 : 0;
     if (pl.c_tma) {
         pl.smem_bytes += kCStageBytes;

@@ -347,9 +347,9 @@ def test_stream_k_split_is_capped(shape):
 
 def test_tma_store_of_c_where_it_pays():
     """C goes through shared memory and TMA stores when its rows are 16-byte
-    aligned, beta == 0 and either C is FP32 or each CTA (pair) gets two or more
-    data-parallel tiles; never for the swapped skinny path or LayerNorm, and
-    the staging never costs a pipeline stage."""
+    aligned, beta == 0 and either C is FP32 with K >= 2048 or each CTA (pair)
+    gets two or more data-parallel tiles; never for the swapped skinny path or
+    LayerNorm, and the staging never costs a pipeline stage."""
     def q(M, N, K, c=DT_BF16, beta=0.0, ldc=None, ab=DT_BF16):
         st, p = lib.gemm_plan_query("N", "T", M, N, K, 1.0, 256, K, 256, K, beta, 256,
                                     ldc or N, (ab, ab, c), num_sms=152)
@@ -360,7 +360,8 @@ def test_tma_store_of_c_where_it_pays():
     assert q(8192, 4096, 4096, beta=1.0)["c_tma"] == 0        # residual: row stores
     assert q(8192, 4096, 4096, c=DT_F32)["c_tma"] == 1
     assert q(1024, 1024, 1024, c=DT_F16)["c_tma"] == 0        # 128 tiles: one wave
-    assert q(1024, 1024, 1024, c=DT_F32)["c_tma"] == 1
+    assert q(1024, 1024, 1024, c=DT_F32)["c_tma"] == 0        # FP32, short K
+    assert q(1024, 1024, 2048, c=DT_F32)["c_tma"] == 1        # FP32, K >= 2048
     assert q(6272, 512, 4608)["c_tma"] == 0                   # stream-K, 16-bit C
     assert q(512, 3072, 4096, c=DT_F32)["c_tma"] == 1         # stream-K, FP32 C
     assert q(64, 16384, 8192, c=DT_F16, ab=DT_F16)["c_tma"] == 0   # swapped

@@ -223,11 +223,11 @@ def test_cta_pair_tiles_integer_exact(g, orc, M, N, K):
 
 TMA_STORE_CASES = [
     # (M, N, K, transA, transB, input, output, path): ragged M and N, each output type
-    (777, 1000, 300, "N", "N", DT_F16, DT_F32, "tiled_1sm"),     # 64-wide tiles, FP32 C
+    (777, 1000, 2048, "N", "N", DT_F16, DT_F32, "tiled_2sm"),    # CTA pairs (stream-K, no split), FP32 C
     (5000, 1800, 96, "T", "N", DT_BF16, DT_BF16, "tiled_2sm"),   # pairs; the last pair's odd
                                                                   # CTA (rows 5120+) stores nothing
     (200, 40008, 64, "N", "T", DT_F16, DT_F16, "tiled_1sm"),     # 256-wide tiles, 2+ per SM
-    (1000, 1000, 256, "N", "T", DT_F32, DT_F32, "tiled_1sm"),    # TF32 inputs
+    (1000, 1000, 2048, "N", "T", DT_F32, DT_F32, "tiled_1sm"),   # TF32 inputs
 ]
 
 

@@ -53,8 +53,8 @@ def _close(orc, w, inp, got, ref):
 CASES = ["skinny_64x16384x8192_f16", "ragged1000x1023x777_bf16_beta1",
          "square1024_f16_nt_f16out",
          # FP32 C: the epilogue stages C in shared memory and stores it by TMA
-         workloads.Workload("noalloc_tma_store_1000x1000x256", 1000, 1000, 256, "N", "T", DT_BF16,
-                            DT_F32, 1.0, 0.0, "N1", "N1")]
+         workloads.Workload("noalloc_tma_store_1000x1000x2048", 1000, 1000, 2048, "N", "T",
+                            DT_BF16, DT_F32, 1.0, 0.0, "N1", "N1")]
 
 
 def test_noalloc_matches_gemm_run_twice(orc):
