@@ -222,23 +222,25 @@ def test_cta_pair_tiles_integer_exact(g, orc, M, N, K):
 
 
 TMA_STORE_CASES = [
-    # (M, N, K, transA, transB, input, output, path): ragged M and N, each output type
-    (777, 1000, 2048, "N", "N", DT_F16, DT_F32, "tiled_2sm"),    # CTA pairs (stream-K, no split), FP32 C
-    (5000, 1800, 96, "T", "N", DT_BF16, DT_BF16, "tiled_2sm"),   # pairs; the last pair's odd
-                                                                  # CTA (rows 5120+) stores nothing
-    (200, 40008, 64, "N", "T", DT_F16, DT_F16, "tiled_1sm"),     # 256-wide tiles, 2+ per SM
-    (1000, 1000, 2048, "N", "T", DT_F32, DT_F32, "tiled_1sm"),   # TF32 inputs
+    # (M, N, K, transA, transB, input, output, path, ldc): ragged M and N, each output type
+    (777, 1000, 2048, "N", "N", DT_F16, DT_F32, "tiled_2sm", None),   # CTA pairs (stream-K,
+                                                                       # no split), FP32 C
+    (5000, 1800, 96, "T", "N", DT_BF16, DT_BF16, "tiled_2sm", 1808),  # pairs; the last pair's odd
+                                                                       # CTA (rows 5120+) stores
+                                                                       # nothing; C pitch > N
+    (200, 40008, 64, "N", "T", DT_F16, DT_F16, "tiled_1sm", None),    # 256-wide tiles, 2+ per SM
+    (1000, 1000, 2048, "N", "T", DT_F32, DT_F32, "tiled_1sm", None),  # TF32 inputs
 ]
 
 
-@pytest.mark.parametrize("M,N,K,ta,tb,ab,c,path", TMA_STORE_CASES,
+@pytest.mark.parametrize("M,N,K,ta,tb,ab,c,path,ldc", TMA_STORE_CASES,
                          ids=[f"{m}x{n}x{k}" for m, n, k, *_ in TMA_STORE_CASES])
-def test_tma_store_epilogue_integer_exact(g, orc, M, N, K, ta, tb, ab, c, path):
+def test_tma_store_epilogue_integer_exact(g, orc, M, N, K, ta, tb, ab, c, path, ldc):
     """C staged in shared memory (128-byte swizzle) and written by TMA stores of
     128-row boxes, the boxes clipped at M and N: bit-exact with integer inputs,
-    and the canary columns past N untouched."""
+    and the canary columns between N and the C pitch untouched."""
     import mixed_precision_dense_sm_gb300 as lib
-    w = W(M, N, K, ta, tb, ab, c)
+    w = W(M, N, K, ta, tb, ab, c, ldc=ldc)
     lda, ldb, ldc = w.lds()
     st, plan = lib.gemm_plan_query(ta, tb, M, N, K, 1.0, 256, lda, 256, ldb, 0.0, 256, ldc,
                                    (ab, ab, c),
