@@ -358,7 +358,10 @@ double oracle_activation(int act, double x) {
     switch (act) {
         case OR_ACT_NONE: return x;
         case OR_ACT_RELU: return isnan(x) ? x : (x > 0.0 ? x : 0.0);
-        case OR_ACT_GELU: return 0.5 * x * (1.0 + erf(x / sqrt(2.0)));
+        /* x Phi(x) with Phi(x) = erfc(-x / sqrt 2) / 2, the same value as
+           (1 + erf(x / sqrt 2)) / 2 but without its cancellation where Phi(x)
+           is tiny (x well below zero): full relative precision on both tails */
+        case OR_ACT_GELU: return 0.5 * x * erfc(-x / sqrt(2.0));
         case OR_ACT_SILU: return x / (1.0 + exp(-x));
     }
     return NAN;

@@ -397,6 +397,13 @@ def pin_activation_values(o):
         assert o.activation(ACT_NONE, x) == x
     assert math.isnan(o.activation(ACT_RELU, float("nan")))
     assert o.activation(ACT_GELU, 0.0) == 0.0 and o.activation(ACT_SILU, 0.0) == 0.0
+    # GELU's negative tail to full relative precision: x Phi(x) is tiny there
+    # (about 1e-13 at x = -7.5, 1e-300 near x = -37), and a 16-bit output
+    # rounds it relative to its own size, so the oracle must not lose it to
+    # cancellation.  scipy's ndtr is accurate in the tail (via erfc).
+    for x in np.concatenate([-np.linspace(1.0, 37.0, 400), [-5.0, -10.0, -20.0]]):
+        want = x * ndtr(x)
+        assert abs(o.activation(ACT_GELU, x) - want) <= 1e-12 * abs(want), x
 
 
 def pin_epilogue_bruteforce(o):

@@ -52,10 +52,12 @@ MUTANTS = [
      "if (bias != NULL) x = x + decode_c(bias_dtype, bias, i);\n            R[i * N + j]"),
     ("sampled_bias_by_row", "if (bias != NULL) x = x + decode_c(bias_dtype, bias, cols[s]);",
      "if (bias != NULL) x = x + decode_c(bias_dtype, bias, rows[s]);"),
-    ("gelu_missing_half", "return 0.5 * x * (1.0 + erf(x / sqrt(2.0)));",
-     "return x * (1.0 + erf(x / sqrt(2.0)));"),
-    ("gelu_wrong_scale", "return 0.5 * x * (1.0 + erf(x / sqrt(2.0)));",
-     "return 0.5 * x * (1.0 + erf(x / 2.0));"),
+    ("gelu_missing_half", "return 0.5 * x * erfc(-x / sqrt(2.0));",
+     "return x * erfc(-x / sqrt(2.0));"),
+    ("gelu_wrong_scale", "return 0.5 * x * erfc(-x / sqrt(2.0));",
+     "return 0.5 * x * erfc(-x / 2.0);"),
+    ("gelu_cancelling_form", "return 0.5 * x * erfc(-x / sqrt(2.0));",
+     "return 0.5 * x * (1.0 + erf(x / sqrt(2.0)));"),
     ("silu_sign", "return x / (1.0 + exp(-x));", "return x / (1.0 + exp(x));"),
     ("relu_leaky", "return isnan(x) ? x : (x > 0.0 ? x : 0.0);",
      "return isnan(x) ? x : (x > 0.0 ? x : 0.01 * x);"),
