@@ -24,7 +24,16 @@ Also reported:
   cpu_baseline -- the CPU oracle (plain FP64 triple loop, all host cores) timed
                   on a bounded sample of the same workload (rank 0, N = 1);
   clocks       -- nvidia-smi SM clocks and throttle reasons sampled during the
-                  timed region.
+                  timed region;
+  sustained    -- (default workload) the same step back to back for about two
+                  seconds, at the power cap, against the measured sustained
+                  BF16 peak, with its own clocks;
+  skinny       -- (default workload) the skinny decode GEMM 64 x 16384 x 8192
+                  (FP16, weights N x K) back to back: GB/s against the
+                  measured HBM copy bandwidth, with its own clocks;
+  context      -- (default workload) cuBLAS via torch.matmul on this GPU:
+                  BF16, FP16 and TF32 8192^3 rates and the step's three shapes
+                  (denominator checks, not part of the measurement).
 --impl reference times the CPU oracle as the comparison arm (the pages ship
 no runnable implementation); it runs on rank 0 only.
 
@@ -63,7 +72,6 @@ METRIC = "GEMM TFLOP/s (2MNK/t) at 1 GB300; % of dense tensor peak or HBM roofli
 LAYER = ["linear_8192x4096x4096_bf16", "linear_8192x14336x4096_bf16",
          "linear_8192x4096x14336_bf16"]
 FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-TF32_OVER_BF16 = 1.1 / 2.25
 # every file the timed kernels compile from: a committed traffic figure is
 # reported only while these hash to the build it was captured on
 KERNEL_SOURCES = ["mixed_precision_dense_sm_gb300/csrc/gemm_tc.cuh",
@@ -475,10 +483,15 @@ def run_ours(args):
     # at the power cap: the sustained peak is the matching denominator.
     long_region = ms_total > 500.0
     peak = peaks["bf16_tflops_sustained"] if long_region else peaks["bf16_tflops"]
-    # FP32 inputs run kind::tf32, whose dense rate is the BF16 rate times the
-    # nominal ratio 1.1 / 2.25 PFLOP/s.
+    # FP32 inputs run kind::tf32.  Its dense rate is measured here, on this
+    # GPU: cuBLAS's FP32 8192^3 GEMM with TF32 allowed (burst, best of 10),
+    # as a ratio to cuBLAS's BF16 rate timed the same way; the measured BF16
+    # peaks scaled by that ratio are the TF32 burst / sustained peaks.
     tf32 = all(w.ab_dtype == workloads.DT_F32 for w in ws)
-    dscale = TF32_OVER_BF16 if tf32 else 1.0
+    dscale, tf32_ctx = 1.0, None
+    if tf32:
+        tf32_ctx = cublas_dense_rates(("bf16", "tf32"))
+        dscale = tf32_ctx["tf32_8192cubed_tflops"] / tf32_ctx["bf16_8192cubed_tflops"]
     peak = peak * dscale
     ws_names = [w.name for w in ws]
     if all(w.M <= 64 for w in ws):       # skinny: HBM-bound
@@ -494,7 +507,9 @@ def run_ours(args):
                 "frac_of_burst": round(achieved / (peaks["bf16_tflops"] * dscale), 4),
                 "frac_of_sustained": round(achieved / (peaks["bf16_tflops_sustained"] * dscale), 4)}
         if tf32:
-            roof["peak_kind"] += "; TF32 = measured BF16 x 1.1/2.25 (nominal dense ratio)"
+            roof["peak_kind"] += ("; TF32 = measured BF16 x %.4f, the cuBLAS TF32 / BF16 8192^3 "
+                                  "rate ratio measured in this run" % dscale)
+            roof["tf32_context"] = tf32_ctx
     traffic = [committed_traffic(n) for n in ws_names]
     roof["traffic"] = (sum(traffic) / len(traffic)) if all(t is not None for t in traffic) else None
     roof["peak_source"] = f"{peak_src} ({'MEASURED_PEAKS.json' if peak_src == 'measured' else 'recipe fallback'})"
@@ -508,6 +523,16 @@ def run_ours(args):
 
     # e2e: host buffers through the C ABI; copies inside the timed region
     e2e = run_e2e(lib, g, bufs, stream, args, world, launch)
+
+    # Default line only: the same step at the power cap, the skinny decode
+    # GEMM against the HBM roofline, and cuBLAS denominators as context.
+    extra = {}
+    if args.workload == "transformer_layer" and not fused and not args.no_extra:
+        peaks_m, _ = load_peaks()
+        extra["sustained"] = run_sustained(step, stream, ms_step, flops_step, peaks_m, local,
+                                           world, launches_per_step)
+        extra["skinny"] = run_skinny_leg(lib, g, local, world, peaks_m)
+        extra["context"] = run_context(bufs, local, peaks_m)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -547,6 +572,7 @@ def run_ours(args):
         "roofline": roof, "e2e": e2e, "gpu_launches": launches_per_step * args.steps,
         "clocks": clk,
     }
+    out.update(extra)
     if cpu is not None:
         out["cpu_baseline"] = cpu
     g.close()
@@ -555,6 +581,136 @@ def run_ours(args):
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+
+
+def timed_region(fn, n, stream, local, world):
+    """n back-to-back calls of fn() between two events on `stream`, with a
+    barrier + synchronize on both sides and nvidia-smi clocks sampled
+    meanwhile.  Returns (ms over the region, max over ranks; clocks)."""
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    w0 = time.time()
+    e0.record(stream)
+    for _ in range(n):
+        fn()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    w1 = time.time()
+    clk = clocks.stop((w0, w1))
+    barrier(world)
+    return max_over_ranks(e0.elapsed_time(e1), world), clk
+
+
+def run_sustained(step, stream, ms_step, flops_step, peaks, local, world, launches_per_step):
+    """The layer step back to back for about two seconds: long enough to run
+    at the power cap, so the measured sustained cuBLAS figure is the matching
+    denominator."""
+    n = max(50, int(2000.0 / max(ms_step, 1e-3)))
+    ms, clk = timed_region(step, n, stream, local, world)
+    value = world * flops_step * n / (ms * 1e-3) / 1e12
+    peak = peaks["bf16_tflops_sustained"]
+    return {"value": round(value, 2), "unit": "TFLOP/s", "steps": n, "region_ms": round(ms, 1),
+            "ms_per_step": round(ms / n, 4), "peak": peak,
+            "peak_kind": "sustained (bf16_tflops_sustained, cuBLAS back to back at the power cap)",
+            "frac": round(value / world / peak, 4), "gpu_launches": launches_per_step * n,
+            "clocks": clk}
+
+
+def run_skinny_leg(lib, g, local, world, peaks, calls=200, warmup=20):
+    """The skinny decode GEMM (64 x 16384 x 8192 FP16, weights stored N x K)
+    through gemm_run, back to back: bytes moved (A + B read once, C written
+    once) per second against the measured HBM copy bandwidth.  The 268 MB of
+    weights exceed the 129 MB L2, so each call streams them from HBM."""
+    w = workloads.WORKLOADS["skinny_64x16384x8192_f16"]
+    inp = workloads.make_inputs(w)
+    A, B = inp.A.cuda(), inp.B.cuda()
+    C = torch.zeros((w.M, inp.ldc), dtype=workloads.TORCH_DTYPE[w.c_dtype], device="cuda")
+    stream = torch.cuda.current_stream()
+    sh = stream.cuda_stream
+    dts = (w.ab_dtype, w.ab_dtype, w.c_dtype)
+
+    def call():
+        st = lib.gemm_run(g.h, w.transA, w.transB, w.M, w.N, w.K, w.alpha, A.data_ptr(), inp.lda,
+                          B.data_ptr(), inp.ldb, w.beta, C.data_ptr(), inp.ldc, dts, sh)
+        if st != 0:
+            raise lib.GemmError(st, "gemm_run")
+
+    for _ in range(warmup):
+        call()
+    g.sync()
+    ms, clk = timed_region(call, calls, stream, local, world)
+    g.sync()
+    us = ms * 1e3 / calls
+    gbs = w.algorithmic_bytes() / (us * 1e-6) / 1e9
+    st, plan = lib.gemm_plan_query(w.transA, w.transB, w.M, w.N, w.K, w.alpha, A.data_ptr(),
+                                   inp.lda, B.data_ptr(), inp.ldb, w.beta, C.data_ptr(), inp.ldc,
+                                   dts, num_sms=torch.cuda.get_device_properties(local)
+                                   .multi_processor_count)
+    return {"workload": f"{w.name}: {w.M}x{w.N}x{w.K} {w.transA}{w.transB}, X N(0,1), "
+                        "W N(0,0.02) stored N x K, FP16 in, FP32 accumulate, FP16 out",
+            "bound": "hbm", "achieved": round(gbs * world, 1), "unit": "GB/s",
+            "peak": peaks["hbm_gbs"], "frac": round(gbs / peaks["hbm_gbs"], 4),
+            "us_per_call": round(us, 2), "tflops": round(world * w.flops() / (us * 1e-6) / 1e12, 1),
+            "calls": calls, "path": plan["path_name"] if st == 0 else None,
+            "bytes_per_call": w.algorithmic_bytes(), "gpu_launches": calls, "clocks": clk}
+
+
+def best_ms(fn, reps=10):
+    """Best of `reps` calls of fn() timed one by one with CUDA events."""
+    fn()
+    torch.cuda.synchronize()
+    best = float("inf")
+    for _ in range(reps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        fn()
+        e1.record()
+        torch.cuda.synchronize()
+        best = min(best, e0.elapsed_time(e1))
+    return best
+
+
+def cublas_dense_rates(kinds=("bf16", "f16", "tf32"), n=8192, reps=10):
+    """cuBLAS (torch.matmul) n^3 GEMM rates on this GPU, burst (best of
+    `reps`): BF16, FP16, and FP32 with TF32 allowed."""
+    gen = torch.Generator(device="cuda").manual_seed(0)
+    dts = {"bf16": torch.bfloat16, "f16": torch.float16, "tf32": torch.float32}
+    out = {"source": "torch.matmul (cuBLAS), best of %d, burst" % reps}
+    tf32_prev = torch.backends.cuda.matmul.allow_tf32
+    try:
+        for name in kinds:
+            a = torch.randn((n, n), device="cuda", generator=gen).to(dts[name])
+            b = torch.randn((n, n), device="cuda", generator=gen).to(dts[name])
+            torch.backends.cuda.matmul.allow_tf32 = (name == "tf32")
+            ms = best_ms(lambda: torch.matmul(a, b), reps)
+            out[f"{name}_8192cubed_tflops"] = round(2.0 * n ** 3 / (ms * 1e-3) / 1e12, 1)
+            del a, b
+    finally:
+        torch.backends.cuda.matmul.allow_tf32 = tf32_prev
+    return out
+
+
+def run_context(bufs, local, peaks, reps=10):
+    """cuBLAS (torch.matmul) timings on this GPU, for context only: the dense
+    8192^3 rates of BF16, FP16 and FP32 with TF32 allowed (best of `reps`
+    calls, burst), and the step's three layer shapes in BF16."""
+    out = cublas_dense_rates(reps=reps)
+    b16 = out["bf16_8192cubed_tflops"]
+    out["f16_over_bf16"] = round(out["f16_8192cubed_tflops"] / b16, 4)
+    out["tf32_over_bf16"] = round(out["tf32_8192cubed_tflops"] / b16, 4)
+    out["bf16_tflops_measured_peak"] = peaks.get("bf16_tflops")
+    shapes = {}
+    for (w, inp, A, B, C) in bufs:
+        x, wt = A[:, :w.K], B[:, :w.K]
+        ms = best_ms(lambda: torch.matmul(x, wt.t()), reps)
+        shapes[w.name] = {"cublas_us": round(ms * 1e3, 1),
+                          "cublas_tflops": round(w.flops() / (ms * 1e-3) / 1e12, 1)}
+    out["layer_shapes"] = shapes
+    return out
 
 
 def run_e2e(lib, g, bufs, stream, args, world, launch):
@@ -1036,6 +1192,8 @@ def main():
                     choices=["transformer_layer"] + list(workloads.WORKLOADS) +
                     list(workloads.SOFTMAX_WORKLOADS) + list(workloads.CONV_WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="skip the sustained, skinny and cuBLAS-context legs of the default line")
     ap.add_argument("--epilogue", action="store_true",
                     help="fused epilogues of a transformer MLP block: bias on every GEMM, "
                          "GELU after the up-projection, residual add after the down-projection")

@@ -117,11 +117,20 @@ gemm_status_t gemm_run(gemm_handle_t h, char transA, char transB,
  * evaluated in FP32 before the single cast to C's type.  bias has N elements
  * (one per output column n), is read only, and may be NULL.  A residual add
  * is beta = 1 with the residual in C.
+ *
+ * Accuracy of the activations (x the FP32 pre-activation value):
+ *   GELU -- relative error <= (x^2 / 2 + 2) 2^-21 + 3e-7 wherever the result
+ *           is an FP32 normal, the negative tail included (no cancellation:
+ *           it is evaluated through erfc); below about x = -13 the result
+ *           leaves FP32's normal range and may be flushed to zero.  A 16-bit
+ *           output is within one ulp of the correctly rounded value.
+ *   SiLU -- relative error <= |x| 2^-23 + 2^-20 (the fast exponential).
+ *   ReLU -- exact.
  */
 typedef enum {
     GEMM_ACT_NONE = 0,
     GEMM_ACT_RELU = 1,   /* x > 0 ? x : 0 (NaN stays NaN) */
-    GEMM_ACT_GELU = 2,   /* x * Phi(x) = 0.5 x (1 + erf(x / sqrt 2)) */
+    GEMM_ACT_GELU = 2,   /* x * Phi(x) = 0.5 x erfc(-x / sqrt 2) */
     GEMM_ACT_SILU = 3    /* x / (1 + exp(-x)) */
 } gemm_activation_t;
 
@@ -306,25 +315,34 @@ gemm_status_t gemm_layernorm_plan_query(char transA, char transB,
  * that must not re-enter the CUDA allocator, code that has handed all device
  * memory to another owner, or code that must not trigger the implicit device
  * synchronisation a first cudaMalloc brings.  It takes no handle, calls no
- * cudaMalloc, cudaFree or other allocating routine, and computes exactly what
- * gemm_run computes, with the same arguments, conventions and argument errors.
+ * cudaMalloc, cudaFree or other allocating routine, and computes what
+ * gemm_run computes, with the same arguments, conventions and argument errors
+ * (bit for bit whenever gemm_run's plan fits the scratch, below).
  *
  * Scratch: packed operand copies and split-K partial sums go to one file-scope
  * device array of GEMM_NOALLOC_SCRATCH_BYTES, which every GPU that loads this
- * library holds until the process exits.  A problem that needs more scratch
- * than that (see gemm_plan_t.workspace_bytes) is rejected with
- * GEMM_ERR_INVALID_VALUE and nothing is enqueued.  All calls on a device share
- * the array and it keeps the last call's contents; the part that must start at
- * zero (split-K tile counters) is cleared on the stream by each call that uses
- * it.  Calls that overlap on the GPU -- on different streams, or from
- * different host threads without ordering -- race on it, so order them on one
- * stream.
+ * library holds until the process exits.  When gemm_run's plan would need
+ * more scratch than that for its split-K partial sums, the same problem is
+ * planned with fewer split-K units (and, if that is not enough, without
+ * split-K); the result then obeys the same accuracy bound as gemm_run's but
+ * may differ from it in the last bits (another summation split).  A problem
+ * whose packed operand copies alone exceed the array is rejected with
+ * GEMM_ERR_INVALID_VALUE and nothing is enqueued.  All calls on a device
+ * share the array and it keeps the last call's contents; the part that must
+ * start at zero (split-K tile counters) is cleared on the stream by each call
+ * that uses it.  Calls that overlap on the GPU -- on different streams, or
+ * from different host threads without ordering -- race on it, so order them
+ * on one stream.
  *
  * Set-up: the first call on each device (with that device current) resolves
  * the array's device address and loads the kernels; make that first call
- * before any stream capture.  Device-side timeouts still wind the kernel down
- * cleanly but are not reported, since there is no handle error word.
- * Returns NOT_SUPPORTED off sm_103 and LAUNCH if a CUDA call fails.
+ * before any stream capture.  A set-up that fails (LAUNCH or NOT_SUPPORTED
+ * returned) is tried again by the next call on that device.  `stream` must
+ * belong to the current device (GEMM_ERR_INVALID_VALUE otherwise: the
+ * array's address is the current device's).  Device-side timeouts still wind
+ * the kernel down cleanly but are not reported, since there is no handle
+ * error word.  Returns NOT_SUPPORTED off sm_103 and LAUNCH if a CUDA call
+ * fails.
  */
 gemm_status_t gemm_run_noalloc(char transA, char transB,
                                int64_t M, int64_t N, int64_t K,

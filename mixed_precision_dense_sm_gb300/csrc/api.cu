@@ -121,7 +121,8 @@ gemm_status_t make_plan(char transA, char transB, int64_t M, int64_t N, int64_t 
                         const void* A, int64_t lda, const void* B, int64_t ldb, float beta,
                         const void* C, int64_t ldc, gemm_dtypes_t dt, int32_t num_sms,
                         int32_t smem_optin, Plan& pl, bool allow_swap = true, bool ln = false,
-                        int32_t max_kc = kMaxKc, int32_t min_kc2_stages = 3) {
+                        int32_t max_kc = kMaxKc, int32_t min_kc2_stages = 3,
+                        bool allow_sk = true, int32_t max_sk_units = 0) {
     gemm_status_t st = check_args(transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, dt);
     if (st != GEMM_OK) return st;
     if (num_sms < 1 || smem_optin < 64 * 1024) return GEMM_ERR_INVALID_VALUE;
@@ -221,7 +222,8 @@ gemm_status_t make_plan(char transA, char transB, int64_t M, int64_t N, int64_t 
     // (the fix-up of a split tile costs one FP32 tile through L2, small beside
     // a K loop of kLongK or more k-blocks).
     // (LayerNorm needs each tile's rows complete in one CTA: no stream-K)
-    const bool long_k = !swap && !ln && k_chunks >= kLongK;
+    // (allow_sk = false: data-parallel only, for callers with bounded scratch)
+    const bool long_k = allow_sk && !swap && !ln && k_chunks >= kLongK;
     auto wave_fill = [](int64_t tiles, int64_t units) {
         return static_cast<double>(tiles) / static_cast<double>(ceil_div(tiles, units) * units);
     };
@@ -318,12 +320,13 @@ gemm_status_t make_plan(char transA, char transB, int64_t M, int64_t N, int64_t 
     // Stream-K spreads the K loop of too few tiles (or of a badly filled last
     // wave, above) over all SMs.  It pays for itself only when the tiles are
     // long in K; the swapped skinny path (a weight-streaming GEMM) always uses it.
-    const bool stream_k = work < INT32_MAX &&
+    const bool stream_k = allow_sk && work < INT32_MAX &&
                           (pair_sk || (!pairs && !ln && (tiles <= kMaxCounterTiles) &&
                                        (balance_sk || ((tiles < num_sms) &&
                                         (swap ? k_chunks >= 4 : (tiles < half_wave && long_k))))));
     if (stream_k) {
-        const int64_t units = num_sms / cg;            // CTAs or CTA pairs
+        int64_t units = num_sms / cg;                  // CTAs or CTA pairs
+        if (max_sk_units > 0 && units > max_sk_units) units = max_sk_units;
         int64_t G = units < work ? units : work;
         int64_t L = ceil_div(work, G);
         if (!swap) {
@@ -1086,7 +1089,6 @@ gemm_status_t gemm_run_layernorm(gemm_handle_t h, char transA, char transB, int6
 // memory.  Its scratch (packed operand copies and stream-K partial sums) lives
 // in the file-scope array below instead of a handle's cudaMalloc'd workspace.
 // ---------------------------------------------------------------------------
-#include <functional>
 #include <mutex>
 
 namespace {
@@ -1100,46 +1102,82 @@ constexpr int kNoAllocMaxDevices = 64;
 static __device__ __align__(256) unsigned char g_noalloc_scratch[GEMM_NOALLOC_SCRATCH_BYTES];
 
 struct NoAllocDevice {
-    std::once_flag once;
-    gemm_status_t status;      // outcome of the set-up
+    std::mutex mu;
+    bool ready;                // set-up succeeded (a failed one is retried by the next call)
     void* scratch;             // device address of g_noalloc_scratch on this device
     int num_sms, smem_optin;
     EncodeTiledFn encode;
 };
 NoAllocDevice g_noalloc_dev[kNoAllocMaxDevices];
 
-// Runs once per device, with that device current.
-void noalloc_setup(NoAllocDevice& d, int dev) {
-    d.status = GEMM_ERR_LAUNCH;
-    int major = 0, minor = 0;
+// Per-device set-up, with that device current; called under d.mu until it
+// succeeds once.
+gemm_status_t noalloc_setup(NoAllocDevice& d, int dev) {
+    int major = 0, minor = 0, sms = 0, smem = 0;
     if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
             cudaSuccess) {
         cudaGetLastError();
-        return;
+        return GEMM_ERR_LAUNCH;
     }
-    if (major != 10 || minor != 3) {
-        d.status = GEMM_ERR_NOT_SUPPORTED;
-        return;
-    }
+    if (major != 10 || minor != 3) return GEMM_ERR_NOT_SUPPORTED;
     void* fn = nullptr;
     cudaDriverEntryPointQueryResult q;
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
                                          &q) != cudaSuccess ||
         q != cudaDriverEntryPointSuccess || fn == nullptr) {
         cudaGetLastError();
-        return;
+        return GEMM_ERR_LAUNCH;
     }
-    d.encode = reinterpret_cast<EncodeTiledFn>(fn);
     void* ptr = nullptr;
     if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || ptr == nullptr) {
         cudaGetLastError();
-        return;
+        return GEMM_ERR_LAUNCH;
     }
+    d.num_sms = sms;
+    d.smem_optin = smem;
+    d.encode = reinterpret_cast<EncodeTiledFn>(fn);
     d.scratch = ptr;
-    d.status = GEMM_OK;
+    d.ready = true;
+    return GEMM_OK;
+}
+
+// gemm_run's plan, made to fit the static scratch: when its stream-K partial
+// sums do not fit, the same problem is planned again with fewer stream-K
+// units (CTAs or CTA pairs) -- every split tile's partial slots shrink with
+// them -- and, failing that, data-parallel without stream-K.  Only when the
+// packed operand copies alone exceed the scratch is the problem refused.
+gemm_status_t noalloc_plan(char transA, char transB, int64_t M, int64_t N, int64_t K, float alpha,
+                           const void* A, int64_t lda, const void* B, int64_t ldb, float beta,
+                           const void* C, int64_t ldc, gemm_dtypes_t dt, const NoAllocDevice& d,
+                           Plan& pl) {
+    const int64_t limit = static_cast<int64_t>(GEMM_NOALLOC_SCRATCH_BYTES);
+    gemm_status_t st = make_plan(transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, dt,
+                                 d.num_sms, d.smem_optin, pl);
+    if (st != GEMM_OK || pl.pub.workspace_bytes <= limit) return st;
+    int64_t units = pl.pub.grid / pl.cta_group;
+    while (pl.partial_bytes > 0 && units > 1) {
+        // the slots scale with the units (sk_max_seg grows by at most one
+        // as the ranges lengthen): shrink in proportion, then step down
+        const int64_t fixed = pl.pub.workspace_bytes - round_up(pl.partial_bytes, 256);
+        const int64_t per_unit = pl.partial_bytes / units;
+        int64_t fit = per_unit > 0 ? (limit - fixed) / per_unit : units - 1;
+        if (fit >= units) fit = units - 1;
+        if (fit < 1) break;
+        units = fit;
+        st = make_plan(transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, dt,
+                       d.num_sms, d.smem_optin, pl, true, false, kMaxKc, 3, true,
+                       static_cast<int32_t>(units));
+        if (st != GEMM_OK || pl.pub.workspace_bytes <= limit) return st;
+        units = pl.pub.grid / pl.cta_group;
+    }
+    st = make_plan(transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, dt, d.num_sms,
+                   d.smem_optin, pl, true, false, kMaxKc, 3, false);
+    if (st != GEMM_OK) return st;
+    // needs more scratch than the static array holds (packed operand copies)
+    return pl.pub.workspace_bytes <= limit ? GEMM_OK : GEMM_ERR_INVALID_VALUE;
 }
 
 }  // namespace
@@ -1155,16 +1193,30 @@ extern "C" gemm_status_t gemm_run_noalloc(char transA, char transB, int64_t M, i
     }
     if (dev < 0 || dev >= kNoAllocMaxDevices) return GEMM_ERR_NOT_SUPPORTED;
     NoAllocDevice& d = g_noalloc_dev[dev];
-    std::call_once(d.once, noalloc_setup, std::ref(d), dev);
-    if (d.status != GEMM_OK) return d.status;
+    {
+        std::lock_guard<std::mutex> lock(d.mu);
+        if (!d.ready) {
+            const gemm_status_t s0 = noalloc_setup(d, dev);
+            if (s0 != GEMM_OK) return s0;
+        }
+    }
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    // The scratch address belongs to the current device: a stream of another
+    // device would have the kernels use it there.  (The legacy and per-thread
+    // default streams always belong to the current device.)
+    if (stream != nullptr && stream != cudaStreamLegacy && stream != cudaStreamPerThread) {
+        int sdev = -1;
+        if (cudaStreamGetDevice(stream, &sdev) != cudaSuccess) {
+            cudaGetLastError();
+            return GEMM_ERR_INVALID_VALUE;
+        }
+        if (sdev != dev) return GEMM_ERR_INVALID_VALUE;
+    }
 
     Plan pl;
-    gemm_status_t st = make_plan(transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, dt,
-                                 d.num_sms, d.smem_optin, pl);
+    gemm_status_t st = noalloc_plan(transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc,
+                                    dt, d, pl);
     if (st != GEMM_OK) return st;
-    if (pl.pub.workspace_bytes > static_cast<int64_t>(GEMM_NOALLOC_SCRATCH_BYTES))
-        return GEMM_ERR_INVALID_VALUE;      // needs more scratch than the static array holds
-    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
 
     if (pl.pub.path == GEMM_PATH_NOOP) return GEMM_OK;
     if (pl.pub.path == GEMM_PATH_SCALE)

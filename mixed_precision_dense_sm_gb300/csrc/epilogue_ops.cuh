@@ -12,32 +12,45 @@ namespace gemm103 {
 
 enum : int { kActNone = 0, kActRelu = 1, kActGelu = 2, kActSilu = 3 };
 
-// erf(x) by the rational approximation of Abramowitz and Stegun, Handbook of
-// Mathematical Functions, formula 7.1.26 (after Hastings):
-//     erf(x) = 1 - (a1 t + a2 t^2 + a3 t^3 + a4 t^4 + a5 t^5) exp(-x^2),
-//     t = 1 / (1 + p x),  x >= 0,  |error| <= 1.5e-7,
-// extended to x < 0 by oddness; t uses the approximate reciprocal (a couple of
-// ulps, scaled by the polynomial and exp(-x^2) <= 1 in erf).  About a dozen
-// instructions against the
-// several dozen of a fully accurate erf: the GELU epilogue runs once per output
-// element and must hide under the MMA of the next tile.  The error is far
-// inside the GEMM's own tolerance (1e-5 of the operand scale).
-__device__ __forceinline__ float erf_as7126(float x) {
-    const float ax = fabsf(x);
-    const float t = __fdividef(1.0f, fmaf(0.3275911f, ax, 1.0f));   // approximate reciprocal
-    float poly = fmaf(1.061405429f, t, -1.453152027f);
-    poly = fmaf(poly, t, 1.421413741f);
-    poly = fmaf(poly, t, -0.284496736f);
-    poly = fmaf(poly, t, 0.254829592f);
-    poly *= t;
-    const float y = fmaf(-poly, __expf(-ax * ax), 1.0f);
-    return copysignf(y, x);
+// erfc(u), u >= 0, with a small *relative* error everywhere: the Chebyshev
+// fit of Press, Teukolsky, Vetterling and Flannery, Numerical Recipes in C
+// (2nd ed.), section 6.2, routine erfcc:
+//     erfc(u) = t exp(-u^2 + P(t)),  t = 1 / (1 + u / 2),
+// P a degree-9 polynomial, fractional error < 1.2e-7 for every u >= 0.
+// Here t uses the approximate reciprocal (2 ulp) and exp the fast
+// exponential, whose error grows like |argument| 2^-23; in all
+// |relative error| <= (u^2 + 2) 2^-22 + 3e-7.
+__device__ __forceinline__ float erfc_nr(float u) {
+    const float t = __fdividef(1.0f, fmaf(0.5f, u, 1.0f));
+    float p = fmaf(t, 0.17087277f, -0.82215223f);
+    p = fmaf(t, p, 1.48851587f);
+    p = fmaf(t, p, -1.13520398f);
+    p = fmaf(t, p, 0.27886807f);
+    p = fmaf(t, p, -0.18628806f);
+    p = fmaf(t, p, 0.09678418f);
+    p = fmaf(t, p, 0.37409196f);
+    p = fmaf(t, p, 1.00002368f);
+    p = fmaf(t, p, -1.26551223f);
+    return t * __expf(fmaf(-u, u, p));
+}
+
+// GELU(x) = x Phi(x), Phi(x) = erfc(-x / sqrt 2) / 2: for x >= 0
+// x (1 - erfc(x / sqrt 2) / 2), for x < 0 x erfc(|x| / sqrt 2) / 2 -- no
+// cancellation on either side, so the relative error stays near that of
+// erfc_nr even where Phi(x) is tiny (a 16-bit output of a very negative x is
+// then still correctly rounded or one ulp off).  About twenty instructions:
+// the epilogue runs once per output element and hides under the next tile's
+// MMA.  NaN stays NaN; GELU(+inf) = inf, GELU(-inf) = NaN (-inf * 0), as
+// x Phi(x) evaluates in IEEE arithmetic.
+__device__ __forceinline__ float gelu(float x) {
+    const float e = erfc_nr(fabsf(x) * 0.70710678118654752f);
+    return x >= 0.0f ? x * fmaf(-0.5f, e, 1.0f) : 0.5f * x * e;
 }
 
 __device__ __forceinline__ float activate(int act, float x) {
     switch (act) {
         case kActRelu: return x > 0.0f ? x : (x != x ? x : 0.0f);     // NaN stays NaN
-        case kActGelu: return 0.5f * x * (1.0f + erf_as7126(x * 0.70710678118654752f));
+        case kActGelu: return gelu(x);
         case kActSilu: return __fdividef(x, 1.0f + __expf(-x));
         default: return x;
     }

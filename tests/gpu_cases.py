@@ -73,11 +73,15 @@ def cin_values(w, inp):
     return inp.C[:, :w.N].to(torch.float64).numpy()
 
 
-def check_full(orc, w, inp, Cdev, exact=False):
-    """Compare every output element with the oracle; returns the stats dict."""
+def check_full(orc, w, inp, Cdev, exact=False, keep=None):
+    """Compare every output element with the oracle; returns the stats dict.
+    With a dict `keep`, the oracle's output codes (16-bit C) are left in
+    keep["codes"]."""
     R, S = oracle_full(orc, w, inp)
     vals, codes = checks.gpu_values(Cdev, w.M, w.N)
     ocodes = None if w.c_dtype == DT_F32 else orc.round_output(R, w.c_dtype)
+    if keep is not None:
+        keep["codes"] = ocodes
     if exact:
         if w.c_dtype == DT_F32:
             want = orc.round_output(R, DT_F32).astype(np.float64)
@@ -139,3 +143,30 @@ def check_canary(w, Cdev):
         pad = Cdev[:, w.N:].float().cpu()
         want = torch.tensor(CANARY, dtype=Cdev.dtype).float()
         assert torch.all(pad == want), f"{w.name}: C padding columns were written"
+
+
+def cublas_strict_frac(w, inp, want):
+    """Context for the accuracy record: the strict one-ulp rate of cuBLAS
+    (torch.matmul, FP32 accumulation, reduced-precision reductions off) on
+    the same inputs against the oracle's codes `want`, for alpha = 1,
+    beta = 0 problems (else None)."""
+    if w.alpha != 1.0 or w.beta != 0.0:
+        return None
+    A, B = inp.A[:, :w.a_shape()[1]].cuda(), inp.B[:, :w.b_shape()[1]].cuda()
+    opA = A if w.transA in "Nn" else A.t()
+    opB = B if w.transB in "Nn" else B.t()
+    m = torch.backends.cuda.matmul
+    keep = (m.allow_fp16_reduced_precision_reduction, m.allow_bf16_reduced_precision_reduction)
+    try:
+        m.allow_fp16_reduced_precision_reduction = False
+        m.allow_bf16_reduced_precision_reduction = False
+        C = torch.matmul(opA, opB).to(TORCH_DTYPE[w.c_dtype])
+    finally:
+        m.allow_fp16_reduced_precision_reduction, m.allow_bf16_reduced_precision_reduction = keep
+    torch.cuda.synchronize()
+    got = C.cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+    def ordered(c):
+        c = c.astype(np.int64)
+        return np.where(c & 0x8000, -(c & 0x7FFF), c)
+    return float((np.abs(ordered(got) - ordered(want)) <= 1).mean())

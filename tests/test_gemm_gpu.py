@@ -85,26 +85,58 @@ def test_medium_integer_exact(g, orc, M, N, K):
         gc.check_full(orc, w, inp, C, exact=True)
 
 
-@pytest.mark.parametrize("name", ["square256_f16_f32out", "square1024_f16_nt_f16out",
-                                  "ragged1000x1023x777_bf16_beta1", "skinny_64x16384x8192_f16"])
+# The strict one-ulp rate that FP32 accumulation in the tensor core permits
+# for 16-bit outputs.  Rounding the FP32 sum once more can leave the correctly
+# rounded value by one ulp, and by more only where the accumulation error
+# exceeds an output ulp, i.e. for outputs far below their S = sum |a b|.  The
+# tensor core does not add in round-to-nearest FP32: its multi-term adder
+# aligns every term of an MMA step to the largest one and truncates the bits
+# below (M. Fasi, N. J. Higham, M. Mikaitis, S. Pranesh, "Numerical behavior
+# of NVIDIA tensor cores", PeerJ Computer Science, 2021), so the error grows
+# faster with K than a round-to-nearest sum.  A simulation of that model on
+# each workload's value distributions (0 to 3 extra bits) predicts
+# 0.9995-0.9998 for the 1024^3 FP16 case, 0.9965-0.999 for the skinny FP16
+# case (K = 8192, values N(0,1) x N(0,0.02)) and 0.9998-1.0 for the BF16
+# layer GEMMs; the floors sit below those ranges.  The measured rates, and
+# cuBLAS's on the same inputs for context, are printed.
+STRICT_FLOOR = {"square1024_f16_nt_f16out": 0.999, "skinny_64x16384x8192_f16": 0.995,
+                "linear_8192x4096x4096_bf16": 0.999, "linear_8192x14336x4096_bf16": 0.999,
+                "linear_8192x4096x14336_bf16": 0.999}
+
+FULL = ["square256_f16_f32out", "square1024_f16_nt_f16out", "ragged1000x1023x777_bf16_beta1",
+        "skinny_64x16384x8192_f16", "linear_8192x4096x4096_bf16", "linear_8192x14336x4096_bf16",
+        "linear_8192x4096x14336_bf16"]
+
+
+@pytest.mark.parametrize("name", FULL)
 def test_workload_full(g, orc, name):
-    """The named workloads at full size, every output element checked."""
+    """The named workloads at full size -- including the three transformer-layer
+    GEMMs in the launch configuration bench.py times -- every output element
+    checked against the oracle; 16-bit outputs also keep the strict one-ulp
+    rate above its floor."""
     w = workloads.WORKLOADS[name]
     inp = workloads.make_inputs(w)
     C = gc.run_gpu(g, w, inp)
-    stats = gc.check_full(orc, w, inp, C)
+    keep = {}
+    stats = gc.check_full(orc, w, inp, C, keep=keep)
+    if w.c_dtype != DT_F32:
+        stats["cublas_strict_1ulp_frac"] = gc.cublas_strict_frac(w, inp, keep["codes"])
     print(name, stats)
+    if w.c_dtype != DT_F32:
+        assert stats["strict_1ulp_frac"] >= STRICT_FLOOR[name], stats
 
 
-@pytest.mark.parametrize("name", ["linear_8192x4096x4096_bf16", "linear_8192x14336x4096_bf16",
-                                  "linear_8192x4096x14336_bf16"])
-def test_workload_sampled(g, orc, name):
-    """The transformer-layer shapes at full size, sampled outputs."""
+@pytest.mark.parametrize("name", ["linear_8192x4096x14336_bf16", "linear_8192x14336x4096_bf16"])
+def test_workload_integer_exact(g, orc, name):
+    """A transformer-layer GEMM at full size with integer inputs in [-8, 8]:
+    every FP32 partial sum is an integer below 2^24 (at most K * 64), so the
+    BF16 output must equal the oracle's correctly rounded value bit for bit
+    on every element (wave boundaries, raster and the TMA-store epilogue
+    included)."""
     w = workloads.WORKLOADS[name]
-    inp = workloads.make_inputs(w)
+    inp = gc.integer_inputs(w)
     C = gc.run_gpu(g, w, inp)
-    stats = gc.check_sampled(orc, w, inp, C)
-    print(name, stats)
+    gc.check_full(orc, w, inp, C, exact=True)
 
 
 def test_padded_leading_dimensions(g, orc):
