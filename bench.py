@@ -72,9 +72,11 @@ METRIC = "GEMM TFLOP/s (2MNK/t) at 1 GB300; % of dense tensor peak or HBM roofli
 LAYER = ["linear_8192x4096x4096_bf16", "linear_8192x14336x4096_bf16",
          "linear_8192x4096x14336_bf16"]
 FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-# every file the timed kernels compile from: a committed traffic figure is
-# reported only while these hash to the build it was captured on
+# every file the timed kernels compile from, and the host planner whose
+# raster and L2 policies set their DRAM traffic: a committed traffic figure
+# is reported only while these hash to the build it was captured on
 KERNEL_SOURCES = ["mixed_precision_dense_sm_gb300/csrc/gemm_tc.cuh",
+                  "mixed_precision_dense_sm_gb300/csrc/api.cu",
                   "mixed_precision_dense_sm_gb300/csrc/ptx.cuh",
                   "mixed_precision_dense_sm_gb300/csrc/epilogue_ops.cuh",
                   "mixed_precision_dense_sm_gb300/csrc/kern_inst.cuh"]

@@ -29,6 +29,13 @@ namespace {
 
 constexpr int kMaxStages = 8;
 constexpr int kGroupM = 8;
+// Raster (raster_columns): the B strips that one group of tile-columns keeps
+// in L2 fit in this many bytes (half of GB300's L2: each die's half caches
+// what that die's SMs read), and a group has at most kRasterMaxColumns.
+constexpr int64_t kRasterResidentBytes = 64ll << 20;
+constexpr int64_t kRasterMaxColumns = 16;
+// Data-parallel tiles alternate their K direction from wave to wave.
+constexpr bool kSerpentineK = true;
 // Workspace header: one stream-K counter (int32: contributors that have
 // stored their sums) per output tile; the planner uses stream-K only for
 // schedules of at most 1024 tiles.
@@ -382,6 +389,25 @@ gemm_status_t make_plan(char transA, char transB, int64_t M, int64_t N, int64_t 
     return GEMM_OK;
 }
 
+// Raster of a data-parallel GEMM schedule: groups of g tile-columns, each
+// visited row by row, so the tiles of one wave (consecutive tiles) cover a
+// few tile-rows across the group's g columns.  The group's g column strips of
+// B (g x block_n rows, each K long) are reused by every tile of the group and
+// stay in L2, while each row strip of A serves the g tiles of its row in one
+// wave and comes back once per group.  g = 16 columns, fewer where their
+// strips would pass kRasterResidentBytes.  (The pages' advice to reuse tiles
+// through fast memory, applied to L2: CATLASS page, section 2.2; SGEMM page,
+// section 1.2.)  Chosen by measurement on GB300 over groups of 4-16
+// tile-rows or tile-columns, either L2 policy for the streamed operand and
+// either K direction: see the tuning log.
+int32_t raster_columns(int64_t tiles_n, int64_t b_strip_bytes) {
+    int64_t g = b_strip_bytes > 0 ? kRasterResidentBytes / b_strip_bytes : kRasterMaxColumns;
+    if (g > kRasterMaxColumns) g = kRasterMaxColumns;
+    if (g > tiles_n) g = tiles_n;
+    if (g < 1) g = 1;
+    return static_cast<int32_t>(g);
+}
+
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
@@ -704,7 +730,8 @@ gemm_status_t enqueue_plan(const Plan& pl, EncodeTiledFn encode, int num_sms, ui
     p.tiles_m = pl.tiles_m;
     p.tiles_n = pl.tiles_n;
     p.num_tiles = pl.pub.num_tiles;
-    p.group_m = kGroupM;
+    p.group = kGroupM;
+    p.raster_n = 0;
     p.stages = pl.pub.stages;
     p.a_mn_major = pl.a.mn_major ? 1 : 0;
     p.b_mn_major = pl.b.mn_major ? 1 : 0;
@@ -734,8 +761,19 @@ gemm_status_t enqueue_plan(const Plan& pl, EncodeTiledFn encode, int num_sms, ui
     // caller that runs the GEMM again on it finds it there.
     const bool a_big = pl.a.rows * pl.a.cols * pl.esize >= kStreamOnceBytes;
     const bool b_big = pl.b.rows * pl.b.cols * pl.esize >= kStreamOnceBytes;
-    p.a_stream_once = (pl.pub.swap_ab || (conv == nullptr && pl.tiles_n == 1 && a_big)) ? 1 : 0;
-    p.b_stream_once = (!pl.pub.swap_ab && conv == nullptr && pl.tiles_m == 1 && b_big) ? 1 : 0;
+    const bool a_once = pl.pub.swap_ab || (conv == nullptr && pl.tiles_n == 1 && a_big);
+    const bool b_once = !pl.pub.swap_ab && conv == nullptr && pl.tiles_m == 1 && b_big;
+    p.a_policy = a_once ? kL2EvictFirst : kL2EvictLast;
+    p.b_policy = b_once ? kL2EvictFirst : kL2EvictLast;
+    // Data-parallel GEMMs: groups of tile-columns (raster_columns); every
+    // wave reverses the K direction of the last.
+    p.serpentine = 0;
+    if (conv == nullptr && p.stream_k == 0 && !pl.pub.swap_ab) {
+        const int64_t kpad = static_cast<int64_t>(pl.k_blocks) * pl.pub.block_k * pl.esize;
+        p.raster_n = 1;
+        p.group = raster_columns(pl.tiles_n, static_cast<int64_t>(bn) * kpad);
+        p.serpentine = kSerpentineK ? 1 : 0;
+    }
     p.wait_limit_ns = wait_limit_ns ? wait_limit_ns : kWaitTimeoutNs;
     p.debug_flags = debug_flags;
     p.bias = ep ? ep->bias : nullptr;

@@ -85,7 +85,9 @@ struct TcParams {
     int32_t M, N;               // logical rows (M') / columns (N') of D
     int32_t k_blocks;           // ceil(K / (KC * chunk)): pipeline stages of K per tile
     int32_t tiles_m, tiles_n, num_tiles;
-    int32_t group_m;            // raster: tiles walk down group_m tile-rows at a time
+    int32_t group;              // raster: tiles go in groups of `group` tile-rows (raster_n = 0)
+    int32_t raster_n;           // or of `group` tile-columns (raster_n = 1)
+    int32_t serpentine;         // data-parallel: odd tiles of a CTA walk K backwards
     int32_t stages;
     int32_t a_mn_major, b_mn_major;
     uint32_t idesc;
@@ -103,8 +105,8 @@ struct TcParams {
     int* tile_counters;         // stream-K: per split tile and CTA of the pair, contributors
                                 // written (self-resetting)
     int* err;                   // device-visible error word (0 = ok)
-    int32_t a_stream_once;      // 1: A is read once (evict-first in L2), 0: reused
-    int32_t b_stream_once;
+    int32_t a_policy;           // L2 policy of A's loads: kL2EvictLast / kL2EvictFirst / kL2EvictNormal
+    int32_t b_policy;
     uint64_t wait_limit_ns;     // bound on every in-kernel wait
     uint32_t debug_flags;       // test hook (kDebugSkipFirstLoad), 0 in normal use
     // fused epilogue: r = act(alpha * acc + beta * C + bias)
@@ -138,6 +140,13 @@ struct TcParams {
     float ln_eps;
     float2* ln_stats;
 };
+
+enum : int { kL2EvictLast = 0, kL2EvictFirst = 1, kL2EvictNormal = 2 };
+
+__device__ __forceinline__ uint64_t l2_policy(int32_t which) {
+    return which == kL2EvictFirst ? l2_policy_evict_first()
+           : which == kL2EvictNormal ? l2_policy_evict_normal() : l2_policy_evict_last();
+}
 
 // Test hook: CTA 0's producer arms its first pipeline slot but issues no load
 // into it, so the MMA's bounded wait on that slot runs out.
@@ -194,16 +203,24 @@ struct SegmentIter {
     }
 };
 
+// Tile `tile` of the raster: groups of p.group tile-rows, each visited column
+// by column (every column, the group's rows together), or -- raster_n --
+// groups of p.group tile-columns visited row by row.  Consecutive tiles, which
+// run in the same wave, share the group's strips of one operand.
 __device__ __forceinline__ void tile_coords(const TcParams& p, int32_t tile, int32_t& tm,
                                             int32_t& tn) {
-    const int32_t per_group = p.group_m * p.tiles_n;
+    const int32_t along = p.raster_n ? p.tiles_n : p.tiles_m;    // the grouped dimension
+    const int32_t across = p.raster_n ? p.tiles_m : p.tiles_n;
+    const int32_t per_group = p.group * across;
     const int32_t group = tile / per_group;
-    const int32_t first_m = group * p.group_m;
-    int32_t gsz = p.tiles_m - first_m;
-    if (gsz > p.group_m) gsz = p.group_m;
+    const int32_t first = group * p.group;
+    int32_t gsz = along - first;
+    if (gsz > p.group) gsz = p.group;
     const int32_t local = tile - group * per_group;
-    tm = first_m + local % gsz;
-    tn = local / gsz;
+    const int32_t g_idx = first + local % gsz;
+    const int32_t a_idx = local / gsz;
+    tm = p.raster_n ? a_idx : g_idx;
+    tn = p.raster_n ? g_idx : a_idx;
 }
 
 __device__ __forceinline__ void record_error(const TcParams& p, int code, volatile int* abort_flag) {
@@ -726,16 +743,24 @@ __global__ void __launch_bounds__(kThreads, 1)
             // Operands that every tile re-reads stay in L2 (evict-last); an
             // operand streamed once (the weights of a skinny GEMM) is marked
             // evict-first so it does not push the reused one out.
-            const uint64_t pol_a = p.a_stream_once ? l2_policy_evict_first() : l2_policy_evict_last();
-            const uint64_t pol_b = p.b_stream_once ? l2_policy_evict_first() : l2_policy_evict_last();
+            const uint64_t pol_a = l2_policy(p.a_policy);
+            const uint64_t pol_b = l2_policy(p.b_policy);
             uint32_t stage = 0, phase = 0;
             uint32_t armed = 0;                   // number of slot armings so far
+            uint32_t seg_i = 0;                   // segments (tiles) so far
             SegmentIter it(p, unit, units);
             Segment sg;
             bool ok = true;
             while (ok && it.next(p, sg)) {
                 int32_t tm, tn;
                 tile_coords(p, sg.tile, tm, tn);
+                // Serpentine K: a CTA's odd tiles walk K backwards.  The CTAs
+                // run their j-th tiles together (one wave), so a wave starts
+                // where the previous one ended: on the k-blocks it left most
+                // recently in L2, which the next wave's tiles that share its
+                // strips then find there.  (The MMA warp only counts k-blocks.)
+                const bool rev = p.serpentine && (seg_i & 1u);
+                ++seg_i;
                 // Parts of a CTA's A / B tiles that lie wholly outside the
                 // matrix only feed outputs that are never stored: not loaded.
                 // tile_bytes(r) is what CTA r of the pair loads per k-block.
@@ -779,7 +804,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ch = pp * p.conv_stride_h - p.conv_pad_h;
                     cw = (rem - pp * p.conv_Q) * p.conv_stride_w - p.conv_pad_w;
                 }
-                for (int32_t kb = sg.kb0; kb < sg.kb1; ++kb) {
+                for (int32_t kbi = sg.kb0; kbi < sg.kb1; ++kbi) {
+                    const int32_t kb = rev ? sg.kb0 + sg.kb1 - 1 - kbi : kbi;
                     if (!wait_or_abort(&empty[stage], phase ^ 1u, &abort_flag, p.wait_limit_ns)) {
                         record_error(p, kErrTimeoutProducer, &abort_flag);
                         ok = false;

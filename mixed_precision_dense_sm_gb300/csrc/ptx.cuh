@@ -184,6 +184,12 @@ __device__ __forceinline__ uint64_t l2_policy_evict_first() {
     return p;
 }
 
+__device__ __forceinline__ uint64_t l2_policy_evict_normal() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
 // ------------------------------------------------------------------- tcgen05
 
 // Allocate `ncols` (power of two, 32..512) TMEM columns; the base address is
