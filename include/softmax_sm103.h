@@ -86,7 +86,7 @@ typedef struct {
     int32_t depth;         /* > 0: rows staged in shared memory by bulk copies (TMA),
                               this many row slots per pipeline; 0: rows held in registers */
     int32_t group_warps;   /* staged: warps per pipeline (the CTA runs 16 / group_warps
-                              independent pipelines); 0 otherwise */
+                              independent pipelines, fed by one producer warp); 0 otherwise */
     int32_t unit_rows;     /* staged: rows per slot -- 1: the group's warps share a row;
                               more: each warp takes its own rows of the slot, and rows that
                               are adjacent in X arrive in one copy of the whole slot */

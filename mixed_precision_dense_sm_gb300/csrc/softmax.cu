@@ -36,6 +36,7 @@ constexpr int64_t kMaxCols = int64_t(1) << 30;
 constexpr int64_t kStagedMinBytes = 256;
 constexpr int64_t kStagedMaxBytes = 64 * 1024;
 constexpr int64_t kStagedSmemBudget = 200 * 1024;
+constexpr int64_t kStagedMinDepth = 6;
 // Two-pass rows: the first pass's lines must still be in L2 when the second
 // pass reads them, so the slices of all resident CTAs stay within half the
 // 129 MB L2 of a GB300 (a cluster splits the row when one CTA per row would
@@ -56,6 +57,7 @@ struct Plan {
     int32_t bulk_elems;   // staged path: elements per row moved by the bulk copy
     int32_t row_stride;   // staged path: bytes between rows inside a slot
     int32_t contiguous;   // staged path: a slot's rows are adjacent in X (one copy)
+    bool whole;           // staged path: rows fill the threads' vectors exactly, no tail
 };
 
 gemm_status_t check(int64_t rows, int64_t cols, const void* X, int64_t ldx, int32_t xdt,
@@ -99,7 +101,7 @@ gemm_status_t make_plan(int64_t rows, int64_t cols, const void* X, int64_t ldx, 
                   (ldy * ey) % 16 == 0) ? 1 : 0;
     const int64_t row_bytes = cols * ex;
     const int64_t kvmax = smx::kTmaMaxElems / (16 / ex);     // vectors per thread
-    const int64_t max_vec = (smx::kTmaThreads / 32) * 32 * kvmax;
+    const int64_t max_vec = smx::kTmaComputeWarps * 32 * kvmax;
     // a row fits one CTA's slots and registers
     const int64_t b = cols * ex;
     const bool staged = pl.pub.vec && b >= kStagedMinBytes && b <= kStagedMaxBytes &&
@@ -122,13 +124,21 @@ gemm_status_t make_plan(int64_t rows, int64_t cols, const void* X, int64_t ldx, 
             k = k < 1 ? 1 : (k > 4 ? 4 : k);
             unit_rows = gw * k;
         } else {
+            // the fewest warps that hold the row, doubled while a group
+            // would get fewer than six slots: slots in flight beat
+            // independent groups (16384 x 4096 FP32: 4 groups of 4 warps
+            // with 3 slots 90.7 us, 2 groups of 8 with 6 slots 84.3 us)
             while (gw * 32 * kvmax < nvec) gw *= 2;
+            while (gw < smx::kTmaComputeWarps &&
+                   kStagedSmemBudget / ((smx::kTmaComputeWarps / gw) * round_up(slice * ex, 128)) <
+                       kStagedMinDepth)
+                gw *= 2;
         }
         // vectors per thread: the least power of two that covers the row
         const int64_t threads_per_row = unit_rows > 1 ? 32 : gw * 32;
         int64_t kv = 1;
         while (kv * threads_per_row < nvec) kv *= 2;
-        const int64_t groups = (smx::kTmaThreads / 32) / gw;
+        const int64_t groups = smx::kTmaComputeWarps / gw;
         const int64_t slot = round_up(unit_rows == 1 ? slice * ex : unit_rows * row_stride, 128);
         int64_t depth = kStagedSmemBudget / (groups * slot);
         if (depth > smx::kTmaMaxDepth) depth = smx::kTmaMaxDepth;
@@ -143,8 +153,12 @@ gemm_status_t make_plan(int64_t rows, int64_t cols, const void* X, int64_t ldx, 
         pl.row_stride = static_cast<int32_t>(row_stride);
         pl.contiguous = contiguous ? 1 : 0;
         pl.resident = true;
-        pl.smem = static_cast<size_t>(round_up(groups * depth * 8, 128) + groups * depth * slot);
+        // a "full" and an "empty" barrier per slot, then the slots
+        pl.smem = static_cast<size_t>(round_up(2 * groups * depth * 8, 128) + groups * depth * slot);
         pl.bulk_elems = static_cast<int32_t>((row_bytes / 16) * 16 / ex);
+        // no 16-byte tail and every thread's kv vectors inside the row: the
+        // kernel's variant without bounds checks
+        pl.whole = pl.bulk_elems == cols && kv * threads_per_row * (16 / ex) == slice;
         const int64_t need = ceil_div(ceil_div(rows, unit_rows), groups);
         pl.pub.grid = static_cast<int32_t>(need < num_sms ? need : num_sms);
     } else if (cols <= kWarpMaxCols) {
@@ -329,6 +343,7 @@ gemm_status_t softmax_rows(int64_t rows, int64_t cols, const void* X, int64_t ld
         q.row_stride = pl.row_stride;
         q.contiguous = pl.contiguous;
         q.kv = pl.pub.kv;
+        q.whole = pl.whole ? 1 : 0;
         q.err = err;
         {
             std::lock_guard<std::mutex> g(g_dbg_mu);

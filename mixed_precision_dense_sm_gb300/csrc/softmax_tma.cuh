@@ -2,32 +2,45 @@
 // bulk copies (TMA), for rows of 256 bytes to 64 KB whose starts are 16-byte
 // aligned.
 //
-// One CTA of 16 warps per SM, split into groups of `group_warps` warps (1 to
-// 16, sized so that a row fits in the group's registers at <= 32 elements
-// per thread).  Every group is an independent pipeline over its own
-// rows with `depth` row slots: its first thread keeps the bulk copies of the
-// next depth - 1 rows in flight while the group works on one, so an SM has
-// ~130-190 KB of loads outstanding without registers holding them, and up to
-// 16 rows are worked on at once.  A row is moved from its slot into registers
-// once, as FP32; the maximum (NaN-propagating), e = exp(x - m) with its sum,
-// and the output e / s then run on the registers -- the three steps of the
-// SGEMM tutorial page, section 2.1, with HBM and shared memory each read once
-// and one exponential per element.  The
-// last (cols * size) % 16 bytes of a row, which a bulk copy cannot move, are
-// read from global memory directly.
+// One CTA per SM: 16 compute warps in groups of `group_warps` warps (1 to 16,
+// sized so that a row fits in the group's registers at <= 32 elements per
+// thread) and one producer warp.  Each group owns a ring of `depth` row slots,
+// each slot with a "full" mbarrier (the bulk copy's bytes) and an "empty" one
+// (one arrival per warp of the group once it has read the slot).  The
+// producer's first thread keeps every group's ring filled: it polls the empty
+// barriers of all groups in turn and refills a slot as soon as its group has
+// read it, so a group waits on a barrier only when its own data is late, and
+// no barrier ties the warps of a group together between units.  An SM keeps
+// ~130-190 KB of loads in flight without registers holding them.
 //
-// Every wait is bounded; a wait that runs out sets the error word, waits
-// (bounded) for the group's other copies to land and leaves.
+// A row is moved from its slot into registers once, as FP32; the slot is
+// released right then; the maximum (NaN-propagating), e = exp(x - m) with its
+// sum, and the output e / s then run on the registers -- the three steps of
+// the SGEMM tutorial page, section 2.1, with HBM and shared memory each read
+// once.  A row shared by several warps merges its warps' (max, sum) pairs
+// through shared memory at one group barrier.  When a row is whole in the
+// vectors the threads hold (no 16-byte tail, every vector slot used) the
+// kernel runs a variant without per-vector bounds checks.  The last
+// (cols * size) % 16 bytes of a row, which a bulk copy cannot move, are read
+// from global memory directly.
+//
+// Every wait is bounded; a wait that runs out sets the error word.  Compute
+// warps that give up leave their loop; the producer stops refilling a group
+// whose slots stay unread past the limit and, before the CTA exits, waits
+// (bounded) for every copy it issued to land.
 #pragma once
 #include <cstdint>
 #include <mutex>
+#include <type_traits>
 
 #include "softmax_kern.cuh"
 
 namespace smx {
 
-constexpr int kTmaThreads = 512;         // 16 warps
+constexpr int kTmaComputeWarps = 16;
+constexpr int kTmaThreads = (kTmaComputeWarps + 1) * 32;    // + the producer warp
 constexpr int kTmaMaxDepth = 8;
+constexpr int kTmaMaxGroups = kTmaComputeWarps;
 constexpr int kTmaMaxElems = 32;         // row elements per thread (held as FP32)
 constexpr uint32_t kSmxDebugSkipFirstLoad = 1u;
 
@@ -46,6 +59,7 @@ struct TmaSoftmaxParams {
     int32_t row_stride;     // bytes from one row to the next inside a slot
     int32_t contiguous;     // 1: a slot's rows are adjacent in X, one copy moves them all
     int32_t kv;             // 16-byte vectors per thread: 1, 2, 4 (or 8 for FP32 input)
+    int32_t whole;          // 1: bulk_elems == cols and every thread holds kv vectors
     int* err;               // device error word (1: a wait ran out)
     uint64_t wait_limit_ns;
     uint32_t debug_flags;
@@ -73,7 +87,8 @@ __device__ __forceinline__ void group_sync(int gw, int group) {
     }
 }
 
-// true on every thread of the group iff `pred` is true on all of them
+// true on every thread of the group iff `pred` is true on all of them (a
+// group barrier as well)
 __device__ __forceinline__ bool group_all(int gw, int group, bool pred) {
     if (gw == 1) return __all_sync(0xffffffffu, pred) != 0;
     uint32_t r;
@@ -88,45 +103,73 @@ __device__ __forceinline__ bool group_all(int gw, int group, bool pred) {
     return r != 0;
 }
 
+// Eight 16-bit values of a 16-byte vector as FP32 (a BF16 is the top half of
+// its FP32; FP16 converts by pairs), or four FP32 values as they are.
+template <typename InT>
+__device__ __forceinline__ void unpack16(const uint4 u, float* x);
+template <>
+__device__ __forceinline__ void unpack16<float>(const uint4 u, float* x) {
+    x[0] = __uint_as_float(u.x);
+    x[1] = __uint_as_float(u.y);
+    x[2] = __uint_as_float(u.z);
+    x[3] = __uint_as_float(u.w);
+}
+template <>
+__device__ __forceinline__ void unpack16<__nv_bfloat16>(const uint4 u, float* x) {
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+    #pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        x[2 * i] = __uint_as_float(w[i] << 16);
+        x[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+    }
+}
+template <>
+__device__ __forceinline__ void unpack16<__half>(const uint4 u, float* x) {
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+    #pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
+        x[2 * i] = f.x;
+        x[2 * i + 1] = f.y;
+    }
+}
+
+// V (one input vector's worth of) FP32 outputs, cast and stored with
+// streaming 16-byte (or 8-byte) stores.
 template <typename InT, typename OutT>
 __device__ __forceinline__ void store_vec16(OutT* dst, const float (&o)[VecOf<InT>::V]) {
     constexpr int V = VecOf<InT>::V;
-    constexpr int VO = VecOf<OutT>::V;
-    if constexpr (V == VO) {
-        uint4 w;
-        OutT* r = reinterpret_cast<OutT*>(&w);
+    if constexpr (sizeof(OutT) == 2) {
+        uint32_t w[V / 2];
         #pragma unroll
-        for (int i = 0; i < V; ++i) r[i] = from_f<OutT>(o[i]);
-        __stcs(reinterpret_cast<uint4*>(dst), w);
-    } else if constexpr (V > VO) {               // 8 16-bit inputs -> 8 FP32 outputs
-        #pragma unroll
-        for (int h = 0; h < V / VO; ++h) {
-            uint4 w;
-            OutT* r = reinterpret_cast<OutT*>(&w);
-            #pragma unroll
-            for (int i = 0; i < VO; ++i) r[i] = from_f<OutT>(o[h * VO + i]);
-            __stcs(reinterpret_cast<uint4*>(dst + h * VO), w);
+        for (int i = 0; i < V / 2; ++i) {
+            if constexpr (std::is_same<OutT, __nv_bfloat16>::value) {
+                const __nv_bfloat162 h = __floats2bfloat162_rn(o[2 * i], o[2 * i + 1]);
+                w[i] = *reinterpret_cast<const uint32_t*>(&h);
+            } else {
+                const __half2 h = __floats2half2_rn(o[2 * i], o[2 * i + 1]);
+                w[i] = *reinterpret_cast<const uint32_t*>(&h);
+            }
         }
-    } else {                                     // 4 FP32 inputs -> 4 16-bit outputs
-        uint2 w;
-        OutT* r = reinterpret_cast<OutT*>(&w);
+        if constexpr (V == 8) __stcs(reinterpret_cast<uint4*>(dst), make_uint4(w[0], w[1], w[2], w[3]));
+        else __stcs(reinterpret_cast<uint2*>(dst), make_uint2(w[0], w[1]));
+    } else {
         #pragma unroll
-        for (int i = 0; i < V; ++i) r[i] = from_f<OutT>(o[i]);
-        __stcs(reinterpret_cast<uint2*>(dst), w);
+        for (int h = 0; h < V / 4; ++h)
+            __stcs(reinterpret_cast<float4*>(dst + 4 * h),
+                   make_float4(o[4 * h], o[4 * h + 1], o[4 * h + 2], o[4 * h + 3]));
     }
 }
 
 // Arm `bar` for the rows of unit u and issue their copies: one copy when the
 // rows are adjacent in X, else one per row (unless the test hook says not to).
-// bulk_elems: the elements of a row moved by the copy.
 template <typename InT>
-__device__ __forceinline__ void issue_unit(const TmaSoftmaxParams& p, const InT* X,
-                                           int32_t bulk_elems, uint8_t* slot, int64_t u,
-                                           uint64_t* bar, uint64_t policy, bool skip) {
+__device__ __forceinline__ void issue_unit(const TmaSoftmaxParams& p, const InT* X, uint8_t* slot,
+                                           int64_t u, uint64_t* bar, uint64_t policy, bool skip) {
     const int64_t first = u * p.unit_rows;
     const int64_t left = p.rows - first;
     const uint32_t nr = static_cast<uint32_t>(left < p.unit_rows ? left : p.unit_rows);
-    const uint32_t bytes = static_cast<uint32_t>(bulk_elems) * sizeof(InT);
+    const uint32_t bytes = static_cast<uint32_t>(p.bulk_elems) * sizeof(InT);
     gemm103::mbar_arrive_expect_tx(bar, nr * bytes);
     if (skip) return;
     if (p.contiguous) {
@@ -138,42 +181,53 @@ __device__ __forceinline__ void issue_unit(const TmaSoftmaxParams& p, const InT*
     }
 }
 
-// One row from its slot: KV 16-byte vectors per thread (vector k of thread t
-// is vector t + k * T) into registers as FP32 -- each element converted once
-// -- then the maximum, e = exp(x - m) kept in place of x, s = sum e, and the
-// output e / s.  One exponential per element.  The T threads are one warp
-// (gw = 1) or the group's gw warps, which combine their partial results
-// through red_m / red_s and the group barrier.
-template <typename InT, typename OutT, int KV>
-__device__ __forceinline__ void process_row(const uint8_t* srow, const InT* __restrict__ grow,
-                                            OutT* __restrict__ yrow, int32_t nvec,
-                                            int32_t bulk_elems, int32_t cols, int t, int T,
-                                            int gw, int group, int warp, int lane,
-                                            float* red_m, float* red_s) {
+// The row's values held by this thread: KV 16-byte vectors (vector k of
+// thread t is vector t + k * T of the row) converted to FP32 once, plus at
+// most one tail element past the bulk-copied part.  WHOLE: every vector slot
+// is inside the row and there is no tail.
+template <typename InT, int KV, bool WHOLE>
+__device__ __forceinline__ void load_row(const uint8_t* srow, const InT* __restrict__ grow,
+                                         int32_t nvec, int32_t bulk_elems, int32_t cols, int t,
+                                         int T, float (&x)[KV][VecOf<InT>::V], float& xt) {
     constexpr int V = VecOf<InT>::V;
-    // FP32 input: the raw vectors stay in registers and the output pass
-    // evaluates exp(x - m) again next to its stores (the row is bound by HBM,
-    // and this order keeps the stores spread over the pass); 16-bit input:
-    // each element is converted once and exp(x - m) is kept (the row is
-    // bound by the per-element arithmetic).
-    constexpr bool kKeepExp = sizeof(InT) == 2;
-    float x[KV][V];
     #pragma unroll
     for (int k = 0; k < KV; ++k) {
         const int32_t v = t + k * T;
-        if (v < nvec) {
-            const uint4 u = *reinterpret_cast<const uint4*>(srow + static_cast<size_t>(v) * 16);
-            const InT* q = reinterpret_cast<const InT*>(&u);
-            #pragma unroll
-            for (int e = 0; e < V; ++e) x[k][e] = to_f(q[e]);
+        if (WHOLE || v < nvec) {
+            unpack16<InT>(*reinterpret_cast<const uint4*>(srow + static_cast<size_t>(v) * 16), x[k]);
         } else {
             #pragma unroll
             for (int e = 0; e < V; ++e) x[k][e] = -INFINITY;
         }
     }
-    const int32_t te = bulk_elems + t;                  // at most one tail element each
-    float xt = te < cols ? to_f(grow[te]) : -INFINITY;
+    xt = -INFINITY;
+    if (!WHOLE) {
+        const int32_t te = bulk_elems + t;
+        if (te < cols) xt = to_f(grow[te]);
+    }
+}
 
+// The rest of one row from registers: maximum, exponentials and their sum,
+// output.  One exponential per element: e = exp(x - m) replaces x.  The T
+// threads are one warp (gw = 1, shuffles only) or the group's gw warps.  A
+// group meets once per row: each warp exponentiates against its own maximum
+// m_w and publishes (m_w, s_w) in red_m / red_s (buffer `buf`, alternating
+// between consecutive rows, so a warp that runs ahead never overwrites pairs
+// another warp has yet to read); after the group barrier every warp merges
+// the pairs by the online rule (SGEMM tutorial page, section 2.2):
+//     M = max m_w,  S = sum_w s_w exp(m_w - M)   (a warp whose elements are
+//     all -inf contributes 0),
+// and scales its e by exp(m_w - M) / S.  NaN in any m_w makes the row NaN,
+// as do +inf (inf - inf) and a fully masked row (S = 0).  `ok` (the slot's
+// data arrived) is combined over the group at that barrier and the row is
+// abandoned unless it holds everywhere.  Returns that.
+template <typename InT, typename OutT, int KV, bool WHOLE>
+__device__ __forceinline__ bool finish_row(float (&x)[KV][VecOf<InT>::V], float xt, bool ok,
+                                           OutT* __restrict__ yrow, int32_t nvec,
+                                           int32_t bulk_elems, int32_t cols, int t, int T, int gw,
+                                           int group, int warp, int lane, float* red_m,
+                                           float* red_s) {
+    constexpr int V = VecOf<InT>::V;
     float m = xt;
     #pragma unroll
     for (int k = 0; k < KV; ++k) {
@@ -181,141 +235,226 @@ __device__ __forceinline__ void process_row(const uint8_t* srow, const InT* __re
         for (int e = 0; e < V; ++e) m = fmax_nan(m, x[k][e]);
     }
     m = warp_max(m);
-    if (gw > 1) {
-        if (lane == 0) red_m[warp] = m;
-        group_sync(gw, group);
-        m = red_m[group * gw];
-        for (int w = 1; w < gw; ++w) m = fmax_nan(m, red_m[group * gw + w]);
-    }
-    // padding entries are -inf: exp gives 0 unless m is -inf or +inf or NaN,
-    // in which case the row is NaN anyway
+    // this warp's elements are all -inf: its e are 0 (not exp(-inf - -inf))
+    const float mz = (m == -INFINITY) ? 0.0f : m;
     float s = 0.0f;
     #pragma unroll
     for (int k = 0; k < KV; ++k) {
         #pragma unroll
         for (int e = 0; e < V; ++e) {
-            const float ex = __expf(x[k][e] - m);
-            if constexpr (kKeepExp) x[k][e] = ex;
-            s += ex;
+            x[k][e] = __expf(x[k][e] - mz);
+            s += x[k][e];
         }
     }
-    xt = __expf(xt - m);
-    if (te < cols) s += xt;
-    s = warp_sum(s);
-    if (gw > 1) {
-        if (lane == 0) red_s[warp] = s;
-        group_sync(gw, group);
-        s = red_s[group * gw];
-        for (int w = 1; w < gw; ++w) s += red_s[group * gw + w];
+    if (!WHOLE) {
+        xt = __expf(xt - mz);
+        if (bulk_elems + t < cols) s += xt;
     }
-    const float inv_s = 1.0f / s;
+    s = warp_sum(s);
+    float scale;
+    if (gw > 1) {
+        if (lane == 0) {
+            red_m[warp] = m;
+            red_s[warp] = s;
+        }
+        ok = group_all(gw, group, ok);
+        if (!ok) return false;
+        // lanes 0 .. gw-1 merge the gw pairs by a butterfly over log2(gw)
+        // levels, (m1, s1) + (m2, s2) = (M, s1 e^(m1 - M) + s2 e^(m2 - M)),
+        // a side with m = -inf contributing 0; lane 0's result is everyone's
+        // (every lane of the butterfly ends with the same bits)
+        const int li = lane & (gw - 1);
+        float Mi = red_m[group * gw + li];
+        float Si = red_s[group * gw + li];
+        for (int off = gw >> 1; off > 0; off >>= 1) {
+            const float mo = __shfl_xor_sync(0xffffffffu, Mi, off);
+            const float so = __shfl_xor_sync(0xffffffffu, Si, off);
+            const float mm = fmax_nan(Mi, mo);
+            const float mmz = (mm == -INFINITY) ? 0.0f : mm;
+            Si = (Mi == -INFINITY ? 0.0f : Si * __expf(Mi - mmz)) +
+                 (mo == -INFINITY ? 0.0f : so * __expf(mo - mmz));
+            Mi = mm;
+        }
+        const float Mz = (Mi == -INFINITY) ? 0.0f : Mi;
+        scale = (m == -INFINITY ? 0.0f : __expf(m - Mz)) / Si;
+    } else {
+        ok = __all_sync(0xffffffffu, ok) != 0;
+        if (!ok) return false;
+        scale = 1.0f / s;
+    }
     #pragma unroll
     for (int k = 0; k < KV; ++k) {
         const int32_t v = t + k * T;
-        if (v < nvec) {
+        if (WHOLE || v < nvec) {
             float o[V];
             #pragma unroll
-            for (int e = 0; e < V; ++e)
-                o[e] = (kKeepExp ? x[k][e] : __expf(x[k][e] - m)) * inv_s;
+            for (int e = 0; e < V; ++e) o[e] = x[k][e] * scale;
             store_vec16<InT, OutT>(yrow + static_cast<int64_t>(v) * V, o);
         }
     }
-    if (te < cols) yrow[te] = from_f<OutT>(xt * inv_s);
+    if (!WHOLE) {
+        const int32_t te = bulk_elems + t;
+        if (te < cols) yrow[te] = from_f<OutT>(xt * scale);
+    }
+    return true;
 }
 
-template <typename InT, typename OutT, int KV>
+template <typename InT, typename OutT, int KV, bool WHOLE>
 __global__ void __launch_bounds__(kTmaThreads, 1)
     softmax_tma_kernel(const __grid_constant__ TmaSoftmaxParams p) {
     constexpr int V = VecOf<InT>::V;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
-    __shared__ float red_m[16], red_s[16];      // per warp, reduced within its group
+    // per warp (m_w, s_w) of a shared row, two buffers alternating by row
+    __shared__ float red_m[2][kTmaComputeWarps], red_s[2][kTmaComputeWarps];
     const InT* __restrict__ X = static_cast<const InT*>(p.X);
     OutT* __restrict__ Y = static_cast<OutT*>(p.Y);
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
     const int GW = p.group_warps;
     const int GT = GW * 32;
-    const int NG = (blockDim.x >> 5) / GW;
-    const int group = warp / GW;
-    const int gt = threadIdx.x - group * GT;     // thread index within the group
+    const int NG = kTmaComputeWarps / GW;
     const int D = p.depth;
     const int32_t nvec = p.bulk_elems / V;
-    // layout: [barriers: one per slot, 128 B aligned][slots]
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem_raw);
-    uint8_t* slots = smem_raw + ((NG * D * 8 + 127) / 128) * 128;
+    // layout: [full barriers NG * D][empty barriers NG * D] (128-byte aligned) [slots]
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem_raw);
+    uint64_t* empty = full + NG * D;
+    uint8_t* slots = smem_raw + ((2 * NG * D * 8 + 127) / 128) * 128;
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < NG * D; ++i) gemm103::mbar_init(&bars[i], 1);
+        for (int i = 0; i < NG * D; ++i) {
+            gemm103::mbar_init(&full[i], 1);
+            gemm103::mbar_init(&empty[i], GW);
+        }
         gemm103::fence_barrier_init();
     }
     __syncthreads();
     gemm103::grid_dependency_wait();      // inputs of the previous kernel are visible
-    const uint64_t policy = gemm103::l2_policy_evict_first();
 
-    // this group's units (slots' worth of rows): u0, u0 + stride, ...; n in all
+    // group g's units (slots' worth of rows): g0, g0 + stride, ... with
+    // g0 = blockIdx.x * NG + g; n(g) of them
     const int64_t units = (p.rows + p.unit_rows - 1) / p.unit_rows;
-    const int64_t u0 = static_cast<int64_t>(blockIdx.x) * NG + group;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * NG;
-    const int64_t n = u0 < units ? (units - 1 - u0) / stride + 1 : 0;
-    uint64_t* pb = bars + group * D;
-    uint8_t* ps = slots + static_cast<size_t>(group) * D * p.slot_bytes;
-    const bool issuer = (gt == 0);
-    const bool skip_first = (p.debug_flags & kSmxDebugSkipFirstLoad) && blockIdx.x == 0 && group == 0;
-    const int wg = warp - group * GW;                 // warp index within the group
+    auto units_of = [&](int g) -> int64_t {
+        const int64_t u0 = static_cast<int64_t>(blockIdx.x) * NG + g;
+        return u0 < units ? (units - 1 - u0) / stride + 1 : 0;
+    };
 
-    if (issuer) {
-        for (int64_t i = 0; i < n && i < D - 1; ++i)
-            issue_unit<InT>(p, X, p.bulk_elems, ps + (i % D) * p.slot_bytes, u0 + i * stride,
-                            &pb[i % D], policy, skip_first && i == 0);
-    }
-    int64_t i = 0;
-    for (; i < n; ++i) {
-        // the slot of unit i - 1 is free (the group is past it): refill it
-        // with unit i + D - 1
-        const int64_t nxt = i + D - 1;
-        if (issuer && nxt < n)
-            issue_unit<InT>(p, X, p.bulk_elems, ps + (nxt % D) * p.slot_bytes, u0 + nxt * stride,
-                            &pb[nxt % D], policy, false);
-        bool ok = gemm103::mbar_wait(&pb[i % D], static_cast<uint32_t>((i / D) & 1),
-                                     p.wait_limit_ns);
-        ok = group_all(GW, group, ok);
-        if (!ok) {
-            if (issuer) atomicExch(p.err, 1);
-            break;
+    if (warp == kTmaComputeWarps) {
+        // ------------------------------------------------------- producer
+        if (lane != 0) return;
+        const uint64_t policy = gemm103::l2_policy_evict_first();
+        const bool skip_first = (p.debug_flags & kSmxDebugSkipFirstLoad) && blockIdx.x == 0;
+        int64_t issued[kTmaMaxGroups];
+        for (int g = 0; g < NG; ++g) issued[g] = 0;
+        uint32_t dead = 0;                // groups no longer refilled (their slots timed out)
+        // every slot starts free: the first D units of each group at once
+        for (int g = 0; g < NG; ++g) {
+            const int64_t n = units_of(g);
+            const int64_t u0 = static_cast<int64_t>(blockIdx.x) * NG + g;
+            for (int64_t i = 0; i < n && i < D; ++i)
+                issue_unit<InT>(p, X, slots + (static_cast<size_t>(g) * D + i) * p.slot_bytes,
+                                u0 + i * stride, &full[g * D + i], policy,
+                                skip_first && g == 0 && i == 0);
+            issued[g] = n < D ? n : D;
         }
+        uint64_t t0 = gemm103::global_timer_ns();
+        for (;;) {
+            bool pending = false, progress = false;
+            for (int g = 0; g < NG; ++g) {
+                const int64_t i = issued[g];
+                if (i >= units_of(g) || ((dead >> g) & 1u)) continue;
+                pending = true;
+                const int d = static_cast<int>(i % D);
+                // unit i - D, the slot's previous contents, has been read
+                const uint32_t par = static_cast<uint32_t>((i / D - 1) & 1);
+                if (!gemm103::mbar_test_wait(gemm103::smem_addr(&empty[g * D + d]), par)) continue;
+                const int64_t u0 = static_cast<int64_t>(blockIdx.x) * NG + g;
+                issue_unit<InT>(p, X, slots + (static_cast<size_t>(g) * D + d) * p.slot_bytes,
+                                u0 + i * stride, &full[g * D + d], policy, false);
+                issued[g] = i + 1;
+                progress = true;
+            }
+            if (!pending) break;
+            const uint64_t now = gemm103::global_timer_ns();
+            if (progress) {
+                t0 = now;
+            } else if (now - t0 > p.wait_limit_ns) {
+                // no slot freed within the limit: the consumers gave up
+                atomicExch(p.err, 1);
+                for (int g = 0; g < NG; ++g) dead |= 1u << g;
+            }
+        }
+        // every copy issued lands before the CTA (and its shared memory) goes
+        for (int g = 0; g < NG; ++g) {
+            const int64_t n = issued[g];
+            for (int64_t i = n > D ? n - D : 0; i < n; ++i)
+                gemm103::mbar_wait(&full[g * D + static_cast<int>(i % D)],
+                                   static_cast<uint32_t>((i / D) & 1), p.wait_limit_ns);
+        }
+        return;
+    }
+
+    // ------------------------------------------------------------ compute
+    const int group = warp / GW;
+    const int gt = threadIdx.x - group * GT;     // thread index within the group
+    const int wg = warp - group * GW;            // warp index within the group
+    const int64_t n = units_of(group);
+    const int64_t u0 = static_cast<int64_t>(blockIdx.x) * NG + group;
+    uint64_t* pf = full + group * D;
+    uint64_t* pe = empty + group * D;
+    const uint8_t* ps = slots + static_cast<size_t>(group) * D * p.slot_bytes;
+    for (int64_t i = 0; i < n; ++i) {
+        const int d = static_cast<int>(i % D);
+        bool ok = gemm103::mbar_wait(&pf[d], static_cast<uint32_t>((i / D) & 1), p.wait_limit_ns);
         const int64_t first = (u0 + i * stride) * p.unit_rows;
-        const uint8_t* sunit = ps + (i % D) * p.slot_bytes;
+        const uint8_t* sunit = ps + static_cast<size_t>(d) * p.slot_bytes;
+        float x[KV][V];
+        float xt;
         if (p.unit_rows == 1) {
-            // the group shares the row
-            process_row<InT, OutT, KV>(sunit, X + first * p.ldx, Y + first * p.ldy, nvec,
-                                       p.bulk_elems, p.cols, gt, GT, GW, group, warp, lane, red_m,
-                                       red_s);
+            // the group shares the row: read it, release the slot, finish it
+            load_row<InT, KV, WHOLE>(sunit, X + first * p.ldx, nvec, p.bulk_elems, p.cols, gt, GT,
+                                     x, xt);
+            __syncwarp();
+            if (lane == 0) gemm103::mbar_arrive(&pe[d]);
+            ok = finish_row<InT, OutT, KV, WHOLE>(x, xt, ok, Y + first * p.ldy, nvec, p.bulk_elems,
+                                                  p.cols, gt, GT, GW, group, warp, lane,
+                                                  red_m[i & 1], red_s[i & 1]);
         } else {
             // each warp of the group takes its own rows of the unit
-            const int64_t left = p.rows - first;
-            const int nr = static_cast<int>(left < p.unit_rows ? left : p.unit_rows);
-            for (int j = wg; j < nr; j += GW)
-                process_row<InT, OutT, KV>(sunit + static_cast<size_t>(j) * p.row_stride,
-                                           X + (first + j) * p.ldx, Y + (first + j) * p.ldy,
-                                           nvec, p.bulk_elems, p.cols, lane, 32, 1, group, warp,
-                                           lane, red_m, red_s);
+            ok = __all_sync(0xffffffffu, ok) != 0;
+            if (ok) {
+                const int64_t left = p.rows - first;
+                const int nr = static_cast<int>(left < p.unit_rows ? left : p.unit_rows);
+                for (int j = wg; j < nr; j += GW) {
+                    load_row<InT, KV, WHOLE>(sunit + static_cast<size_t>(j) * p.row_stride,
+                                             X + (first + j) * p.ldx, nvec, p.bulk_elems, p.cols,
+                                             lane, 32, x, xt);
+                    if (j + GW >= nr) {
+                        // this warp's last read of the slot
+                        __syncwarp();
+                        if (lane == 0) gemm103::mbar_arrive(&pe[d]);
+                    }
+                    finish_row<InT, OutT, KV, WHOLE>(x, xt, true, Y + (first + j) * p.ldy, nvec,
+                                                     p.bulk_elems, p.cols, lane, 32, 1, group, warp,
+                                                     lane, red_m[0], red_s[0]);
+                }
+                if (wg >= nr) {
+                    __syncwarp();
+                    if (lane == 0) gemm103::mbar_arrive(&pe[d]);
+                }
+            }
         }
-        // every thread is past this unit's slot and reduction words
-        group_sync(GW, group);
-    }
-    if (i < n && issuer) {
-        // a wait ran out: let the copies already issued into this group's slots (units i .. i + D - 1)
-        // land before shared memory is released
-        const int64_t last = i + D < n ? i + D : n;
-        for (int64_t j = i; j < last; ++j)
-            gemm103::mbar_wait(&pb[j % D], static_cast<uint32_t>((j / D) & 1), p.wait_limit_ns);
+        if (!ok) {
+            if (gt == 0) atomicExch(p.err, 1);
+            break;
+        }
     }
 }
 
-template <typename InT, typename OutT, int KV>
+template <typename InT, typename OutT, int KV, bool WHOLE>
 cudaError_t launch_softmax_tma_kv(const TmaSoftmaxParams& p, int grid, size_t smem,
                                   cudaStream_t stream) {
-    auto kern = softmax_tma_kernel<InT, OutT, KV>;
+    auto kern = softmax_tma_kernel<InT, OutT, KV, WHOLE>;
     {
         static std::mutex mu;
         static size_t raised = 0;
@@ -340,17 +479,24 @@ cudaError_t launch_softmax_tma_kv(const TmaSoftmaxParams& p, int grid, size_t sm
     return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
+template <typename InT, typename OutT, int KV>
+cudaError_t launch_softmax_tma_w(const TmaSoftmaxParams& p, int grid, size_t smem,
+                                 cudaStream_t stream) {
+    return p.whole ? launch_softmax_tma_kv<InT, OutT, KV, true>(p, grid, smem, stream)
+                   : launch_softmax_tma_kv<InT, OutT, KV, false>(p, grid, smem, stream);
+}
+
 template <typename InT, typename OutT>
 cudaError_t launch_softmax_tma(const TmaSoftmaxParams& p, int grid, size_t smem,
                                cudaStream_t stream) {
     constexpr int kMaxKV = kTmaMaxElems / VecOf<InT>::V;
     switch (p.kv) {
-        case 1: return launch_softmax_tma_kv<InT, OutT, 1>(p, grid, smem, stream);
-        case 2: return launch_softmax_tma_kv<InT, OutT, 2>(p, grid, smem, stream);
-        case 4: return launch_softmax_tma_kv<InT, OutT, 4>(p, grid, smem, stream);
+        case 1: return launch_softmax_tma_w<InT, OutT, 1>(p, grid, smem, stream);
+        case 2: return launch_softmax_tma_w<InT, OutT, 2>(p, grid, smem, stream);
+        case 4: return launch_softmax_tma_w<InT, OutT, 4>(p, grid, smem, stream);
         case 8:
             if constexpr (kMaxKV >= 8)
-                return launch_softmax_tma_kv<InT, OutT, 8>(p, grid, smem, stream);
+                return launch_softmax_tma_w<InT, OutT, 8>(p, grid, smem, stream);
             return cudaErrorInvalidValue;
         default: return cudaErrorInvalidValue;
     }

@@ -75,11 +75,12 @@ def test_work_split(cols, mode, threads, cluster):
 @pytest.mark.parametrize("cols,dt,ld,cl,gw,unit,depth,kv", [
     (64, DT_F32, 64, 1, 8, 32, 8, 1), (1024, DT_F32, 1024, 1, 8, 8, 3, 8),
     (1000, DT_F32, 1004, 1, 8, 8, 3, 8), (128, DT_BF16, 128, 1, 8, 32, 8, 1),
-    (1024, DT_BF16, 1024, 1, 8, 8, 6, 4), (2048, DT_F32, 2048, 1, 2, 1, 3, 8),
+    (1024, DT_BF16, 1024, 1, 8, 8, 6, 4), (2048, DT_F32, 2048, 1, 4, 1, 6, 4),
     (4096, DT_BF16, 4096, 1, 4, 1, 6, 4), (2052, DT_F32, 2052, 1, 4, 1, 6, 8),
-    (4096, DT_F32, 4096, 1, 4, 1, 3, 8), (8192, DT_F32, 8192, 1, 8, 1, 3, 8),
+    (4096, DT_F32, 4096, 1, 8, 1, 6, 4), (8192, DT_F32, 8192, 1, 16, 1, 6, 4),
     (16384, DT_F32, 16384, 1, 16, 1, 3, 8), (16384, DT_BF16, 16384, 1, 16, 1, 6, 4),
-    (3000, DT_F16, 3000, 1, 4, 1, 8, 4),
+    (3000, DT_F16, 3000, 1, 4, 1, 8, 4), (8192, DT_BF16, 8192, 1, 8, 1, 6, 4),
+    (2048, DT_BF16, 2048, 1, 2, 1, 6, 4),
     # not staged: too long for one CTA (two passes; a cluster of 2 for rows
     # whose 152 resident slices exceed 64 MB), too short, or rows not 16-byte
     # aligned
@@ -90,13 +91,14 @@ def test_work_split(cols, mode, threads, cluster):
     (16385, DT_F32, 16385, 1, 0, 0, 0, 0)])
 def test_staged_split(cols, dt, ld, cl, gw, unit, depth, kv):
     """16-byte-aligned rows of 256 B to 64 KB (<= 16384 elements) are staged
-    in shared memory by bulk copies: one CTA of 16 warps per SM.  Rows a warp
-    can hold (<= 1024 elements) go to groups of 8 warps whose slots carry
-    several rows (~16 KB, one copy when the rows are adjacent), a warp per
-    row; longer rows are shared by a group just large enough to hold them in
-    registers (<= 32 elements per thread).  Each group is a pipeline with as
-    many slots as 200 KB allow (at most 8).  Other rows keep the register
-    kernels (depth 0)."""
+    in shared memory by bulk copies: one CTA of 16 compute warps and a
+    producer warp per SM.  Rows a warp can hold (<= 1024 elements) go to
+    groups of 8 warps whose slots carry several rows (~16 KB, one copy when
+    the rows are adjacent), a warp per row; longer rows are shared by the
+    smallest group that holds them in registers (<= 32 elements per thread),
+    doubled while a group would get fewer than six slots.  Each group is a
+    pipeline with as many slots as 200 KB allow (at most 8).  Other rows keep
+    the register kernels (depth 0)."""
     st, p = plan(100000, cols, ldx=ld, ldy=ld, xdt=dt, ydt=dt)
     assert st == OK
     got = (p["cluster"], p["group_warps"], p["unit_rows"], p["depth"], p["kv"])
@@ -104,7 +106,7 @@ def test_staged_split(cols, dt, ld, cl, gw, unit, depth, kv):
     es = 4 if dt == DT_F32 else 2
     kvmax = 32 * es // 16                   # 32 elements per thread
     if depth:
-        assert p["vec"] == 1 and p["threads"] == 512
+        assert p["vec"] == 1 and p["threads"] == 544          # 16 compute warps + the producer
         assert p["grid"] == (152 if cl == 1 else cl * (152 // cl))
         assert p["mode_name"] == ("warp" if unit > 1 else "cta")
         groups = 16 // gw
@@ -117,7 +119,10 @@ def test_staged_split(cols, dt, ld, cl, gw, unit, depth, kv):
         nvec = slice_ * es // 16
         if unit == 1:
             assert gw * 32 * kvmax >= nvec
-            assert cl > 1 or gw == 1 or (gw // 2) * 32 * kvmax < nvec
+            # the fewest warps that hold the row, unless half as many would
+            # leave a group fewer than six slots
+            assert cl > 1 or gw == 1 or (gw // 2) * 32 * kvmax < nvec or \
+                (16 // (gw // 2)) * 6 * slot > 200 * 1024
             assert kv * gw * 32 >= nvec and (kv == 1 or (kv // 2) * gw * 32 < nvec)
         else:
             assert nvec <= 32 * kvmax and unit % gw == 0

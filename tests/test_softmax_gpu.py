@@ -111,6 +111,30 @@ def test_every_type_pair(lib, orc, cols):
         check(orc, Xs, cols, xdt, ydt, Y)
 
 
+@pytest.mark.parametrize("cols,gw,unit", [(1024, 8, 8), (1001, 8, 8), (2048, 2, 1), (4096, 4, 1),
+                                          (6001, 8, 1), (8192, 8, 1), (16000, 16, 1),
+                                          (16384, 16, 1)])
+def test_staged_16bit_splits(lib, orc, cols, gw, unit):
+    """16-bit rows in the staged kernel: a warp per row up to 1024 elements,
+    else groups of 2-16 warps that merge their warps' (max, sum) pairs;
+    whole rows, rows whose vectors do not fill every thread and rows with a
+    tail past the last 16-byte vector; FP16 and BF16 inputs with 16-bit and
+    FP32 outputs; fully and half masked rows; more rows than slots."""
+    rows = 300 if cols <= 8192 else 80
+    ld = cols + (-cols) % 8
+    st, p = lib.softmax_plan_query(rows, cols, 256, ld, DT_BF16, 1 << 44, ld, DT_BF16)
+    assert st == 0 and p["depth"] > 0 and (p["group_warps"], p["unit_rows"]) == (gw, unit), p
+    g = torch.Generator().manual_seed(cols + 3)
+    x = torch.randn((rows, cols), generator=g) * 3.0
+    x[1, :] = float("-inf")
+    x[2, cols // 2:] = float("-inf")
+    x[3, :cols // 3] = float("-inf")
+    for xdt, ydt in [(DT_BF16, DT_BF16), (DT_F16, DT_F32), (DT_BF16, DT_F16)]:
+        Xs = stored(x, ld, xdt)
+        Y = run(lib, Xs, cols, ydt, ldy=ld)
+        check(orc, Xs, cols, xdt, ydt, Y, canary=False)
+
+
 @pytest.mark.parametrize("cols", [77, 1000, 3001, 9000, 20001, 140001])
 def test_unaligned_rows(lib, orc, cols):
     """Row pitches that are not a multiple of 16 bytes and base addresses one
@@ -230,14 +254,14 @@ def test_empty_and_errors(lib):
     assert torch.all(Y == 7.0)
 
 
-@pytest.mark.parametrize("cols", [1024, 8192, 16384])
+@pytest.mark.parametrize("cols", [1024, 4096, 16384])
 def test_timeout_reported_without_fault(lib, orc, cols):
     """The failure path of the staged kernels, without a GPU fault: the test
     hook arms the first row slot of the first pipeline without issuing its
     copy, so that bounded wait runs out (limit 0.2 s).  softmax_sync reports
     GEMM_ERR_DEVICE_TIMEOUT once; the next call on the same device is
-    correct.  1024 FP32 columns run a warp per row, 8192 a group of 8 warps
-    per row, 16384 a group of 16 warps (the whole CTA) per row."""
+    correct.  1024 FP32 columns run a warp per row, 4096 a group of 8 warps
+    per row, 16384 a group of 16 warps (every compute warp) per row."""
     g = torch.Generator().manual_seed(5)
     Xs = stored(torch.randn((64, cols), generator=g), cols, DT_F32)
     st, p = lib.softmax_plan_query(64, cols, 256, cols, DT_F32, 1 << 44, cols, DT_F32)
