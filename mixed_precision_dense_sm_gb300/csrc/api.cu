@@ -48,6 +48,9 @@ constexpr double kMinWaveFill = 0.8;
 // An operand read once and at least this large (about three quarters of the
 // GB300 L2) is loaded evict-first so that it does not push reused data out.
 constexpr int64_t kStreamOnceBytes = 96ll << 20;
+// Convolutions with at most 128 output channels run 256-row single-CTA tiles
+// (make_plan's mh2): the im2col box of 256 output pixels feeds two MMAs.
+constexpr bool kConvTwoHalves = true;
 // Stream-K fix-up: one FP32 partial tile read back by the finisher costs about
 // as long as this many k-blocks of 256 bytes per row (128 BF16 / FP16 or 64
 // TF32 elements) of the tile's MMA (measured on GB300).
@@ -73,6 +76,7 @@ struct Plan {
     int32_t k_blocks, tiles_m, tiles_n;
     int32_t kc;         // K chunks (128-byte rows of K) per pipeline stage
     int32_t cta_group;
+    int32_t mh;         // M halves per single-CTA tile: 1 (128 rows) or 2 (256 rows)
     int32_t esize;      // input element bytes: 2 (FP16/BF16) or 4 (FP32 as TF32)
     int32_t sk_len, sk_max_seg;
     int64_t pack_a_bytes, pack_b_bytes, partial_bytes;
@@ -129,7 +133,7 @@ gemm_status_t make_plan(char transA, char transB, int64_t M, int64_t N, int64_t 
                         const void* C, int64_t ldc, gemm_dtypes_t dt, int32_t num_sms,
                         int32_t smem_optin, Plan& pl, bool allow_swap = true, bool ln = false,
                         int32_t max_kc = kMaxKc, int32_t min_kc2_stages = 3,
-                        bool allow_sk = true, int32_t max_sk_units = 0) {
+                        bool allow_sk = true, int32_t max_sk_units = 0, bool mh2 = false) {
     gemm_status_t st = check_args(transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, dt);
     if (st != GEMM_OK) return st;
     if (num_sms < 1 || smem_optin < 64 * 1024) return GEMM_ERR_INVALID_VALUE;
@@ -230,12 +234,16 @@ gemm_status_t make_plan(char transA, char transB, int64_t M, int64_t N, int64_t 
     // a K loop of kLongK or more k-blocks).
     // (LayerNorm needs each tile's rows complete in one CTA: no stream-K)
     // (allow_sk = false: data-parallel only, for callers with bounded scratch)
-    const bool long_k = allow_sk && !swap && !ln && k_chunks >= kLongK;
+    // 256-row single-CTA tiles (two M = 128 halves sharing each B tile) for
+    // N <= 128 when asked (convolutions): twice the MMA per A box of a
+    // 128-row tile; data-parallel, plain epilogue, 16-bit inputs.
+    const bool use_mh2 = mh2 && !swap && !ln && esize == 2 && pl.Nk <= 128 && pl.Mk > kBlockM;
+    const bool long_k = allow_sk && !use_mh2 && !swap && !ln && k_chunks >= kLongK;
     auto wave_fill = [](int64_t tiles, int64_t units) {
         return static_cast<double>(tiles) / static_cast<double>(ceil_div(tiles, units) * units);
     };
     const int64_t pair_tiles = ceil_div(pl.Mk, 2 * kBlockM) * ceil_div(pl.Nk, 256);
-    bool pairs = !swap && pl.Mk >= 2 * kBlockM && pl.Nk >= 256 && num_sms >= 2 &&
+    bool pairs = !use_mh2 && !swap && pl.Mk >= 2 * kBlockM && pl.Nk >= 256 && num_sms >= 2 &&
                  pair_tiles >= num_sms / 2;
     if (ln && pl.Nk <= 128) pairs = false;
     bool balance_sk = false;
@@ -244,7 +252,8 @@ gemm_status_t make_plan(char transA, char transB, int64_t M, int64_t N, int64_t 
         balance_sk = true;
     }
     int cg = pairs ? 2 : 1;
-    int64_t block_m = static_cast<int64_t>(kBlockM) * cg;
+    pl.mh = use_mh2 ? 2 : 1;
+    int64_t block_m = static_cast<int64_t>(kBlockM) * cg * pl.mh;
     int64_t tiles_m = ceil_div(pl.Mk, block_m);
     // Single-CTA tiles: the widest of 256 / 128 / 64 columns that still gives
     // every SM a tile (256) or at least half a wave (128, 64).
@@ -259,6 +268,7 @@ gemm_status_t make_plan(char transA, char transB, int64_t M, int64_t N, int64_t 
     } else {
         bn = 64;
     }
+    if (use_mh2) bn = pl.Nk <= 64 ? 64 : 128;
     if (ln) {
         // LayerNorm kernels come in widths 128 and 256: a row of up to 256
         // columns is whole in one tile
@@ -279,7 +289,7 @@ gemm_status_t make_plan(char transA, char transB, int64_t M, int64_t N, int64_t 
     // operand bytes of a single-CTA 128 x 256 tile, and that is the limit
     // once the operands come from L2 (each re-read by several tiles).
     bool pair_sk = false;
-    if (!pairs && !ln && !swap && bn == 256 && pl.Mk >= 2 * kBlockM && num_sms >= 2) {
+    if (!use_mh2 && !pairs && !ln && !swap && bn == 256 && pl.Mk >= 2 * kBlockM && num_sms >= 2) {
         const int64_t t1 = tiles_m * ceil_div(pl.Nk, bn);
         // one counter per tile and CTA of the pair
         const bool fits = pair_tiles * 2 <= kMaxCounterTiles;
@@ -299,7 +309,8 @@ gemm_status_t make_plan(char transA, char transB, int64_t M, int64_t N, int64_t 
     pl.pub.block_n = bn;
     pl.pub.num_tiles = static_cast<int32_t>(tiles);
 
-    const uint32_t chunk_bytes = kATileBytes + static_cast<uint32_t>(bn / cg) * 128u;
+    const uint32_t chunk_bytes = kATileBytes * static_cast<uint32_t>(pl.mh) +
+                                 static_cast<uint32_t>(bn / cg) * 128u;
     const int64_t barrier_bytes = 256;
     // static shared memory of the kernel: flags, and the LayerNorm exchange
     const int64_t static_bytes = 64 + (ln ? 4 * kBlockM * 4 : 4);
@@ -309,7 +320,7 @@ gemm_status_t make_plan(char transA, char transB, int64_t M, int64_t N, int64_t 
     // lines.  The K chunks per stage are chosen with the staging set aside;
     // without it the stages are counted again (shared memory the kernel does
     // not use is left to the L1 cache).
-    const bool c_stage_ok = pl.pub.c_vector && !ln;
+    const bool c_stage_ok = pl.pub.c_vector && !ln && !use_mh2;
     const int64_t avail_all = smem_optin - 1024 - barrier_bytes - static_bytes;
     const int64_t avail = avail_all - (c_stage_ok ? kCStageBytes : 0);
     pl.kc = (kc2_ok && avail / (2 * static_cast<int64_t>(chunk_bytes)) >= min_kc2_stages) ? 2 : 1;
@@ -327,7 +338,7 @@ gemm_status_t make_plan(char transA, char transB, int64_t M, int64_t N, int64_t 
     // Stream-K spreads the K loop of too few tiles (or of a badly filled last
     // wave, above) over all SMs.  It pays for itself only when the tiles are
     // long in K; the swapped skinny path (a weight-streaming GEMM) always uses it.
-    const bool stream_k = allow_sk && work < INT32_MAX &&
+    const bool stream_k = allow_sk && !use_mh2 && work < INT32_MAX &&
                           (pair_sk || (!pairs && !ln && (tiles <= kMaxCounterTiles) &&
                                        (balance_sk || ((tiles < num_sms) &&
                                         (swap ? k_chunks >= 4 : (tiles < half_wave && long_k))))));
@@ -509,8 +520,9 @@ bool encode_c_store(EncodeTiledFn encode, CUtensorMap* map, int32_t dtype, const
 // The input X (N, H, W, C) as an im2col map: windows traversed W, H, N with
 // the convolution's stride, 64 channels x 128 windows per load, 128-byte
 // swizzle, zeros outside the image.  The box corners make the traversal
-// visit exactly the windows of the output (P x Q per image).
-bool encode_conv_input(const ConvDesc& cd, CUtensorMap* map, int32_t dtype) {
+// visit exactly the windows of the output (P x Q per image); `pixels` windows
+// (the tile's rows) per load.
+bool encode_conv_input(const ConvDesc& cd, CUtensorMap* map, int32_t dtype, uint32_t pixels) {
     const int64_t es = 2;
     const cuuint64_t dims[4] = {static_cast<cuuint64_t>(cd.C), static_cast<cuuint64_t>(cd.W),
                                 static_cast<cuuint64_t>(cd.H), static_cast<cuuint64_t>(cd.N)};
@@ -526,7 +538,7 @@ bool encode_conv_input(const ConvDesc& cd, CUtensorMap* map, int32_t dtype) {
                                   dtype == GEMM_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
                                                      : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
                                   4, const_cast<void*>(cd.X), dims, strides, lower, upper,
-                                  64u /* channels per 128-byte row */, kBlockM, estr,
+                                  64u /* channels per 128-byte row */, pixels, estr,
                                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -704,7 +716,7 @@ gemm_status_t enqueue_plan(const Plan& pl, EncodeTiledFn encode, int num_sms, ui
     const uint32_t mn_box = static_cast<uint32_t>(pl.pub.block_k);
     bool ok;
     if (conv != nullptr) {
-        ok = encode_conv_input(*conv, &l.tmA, dt.a);
+        ok = encode_conv_input(*conv, &l.tmA, dt.a, static_cast<uint32_t>(kBlockM * pl.mh));
         if (pl.kc == 1)
             ok = ok && encode_conv_filter(encode, *conv, &l.tmB, dt.b, static_cast<uint32_t>(bn / cg));
         else
@@ -713,7 +725,7 @@ gemm_status_t enqueue_plan(const Plan& pl, EncodeTiledFn encode, int num_sms, ui
                                       static_cast<uint32_t>(bn / cg), pl.kc);
     } else {
         ok = encode_operand(encode, &l.tmA, dt.a, a_ptr, pl.a.cols, pl.a.rows, pl.a.packed_ld,
-                            pl.a.mn_major ? mn_box : static_cast<uint32_t>(kBlockM),
+                            pl.a.mn_major ? mn_box : static_cast<uint32_t>(kBlockM * pl.mh),
                             pl.a.mn_major ? 1 : pl.kc);
         ok = ok && encode_operand(encode, &l.tmB, dt.b, b_ptr, pl.b.cols, pl.b.rows,
                                   pl.b.packed_ld,
@@ -811,6 +823,7 @@ gemm_status_t enqueue_plan(const Plan& pl, EncodeTiledFn encode, int num_sms, ui
     l.block_n = bn;
     l.esize = pl.esize;
     l.kc = pl.kc;
+    l.mh = pl.mh;
     l.smem_bytes = pl.smem_bytes;
     l.stream = stream;
 
@@ -901,7 +914,8 @@ gemm_status_t conv_plan(int64_t N, int64_t H, int64_t W, int64_t C, int64_t K, i
     // times) and the filter stays in L2, so one stage in flight covers the
     // load latency, where a GEMM streaming an operand from DRAM needs three.
     return make_plan('N', 'T', M, K, kfake, alpha, X, kfake, Wt, kfake, beta, Y, K, dt, num_sms,
-                     smem_optin, pl, false, false, C % 64 == 0 ? kMaxKc : 1, 2);
+                     smem_optin, pl, false, false, C % 64 == 0 ? kMaxKc : 1, 2, true, 0,
+                     kConvTwoHalves);
 }
 
 bool dtype16or32(int32_t t) { return t == GEMM_F16 || t == GEMM_BF16 || t == GEMM_F32; }

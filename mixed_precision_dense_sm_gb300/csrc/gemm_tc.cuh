@@ -656,7 +656,13 @@ __device__ __forceinline__ void ln_tile(const TcParams& p, uint32_t t_row, int32
     }
 }
 
-template <int CG, int BN, typename OutT, int ES, int EPI = kEpiPlain, int KC = 1>
+// MH = 2 (single CTA, plain epilogue, BN <= 128, data-parallel schedules):
+//   a 256 x BN tile in one CTA, as two M = 128 halves.  One A box of 256 rows
+//   per K chunk feeds both halves' MMAs, which share the chunk's B tile and
+//   accumulate into two TMEM accumulators (columns [0, BN) and [BN, 2 BN) of
+//   each buffer): twice the MMA per TMA box of a 128-row tile.  Epilogue warps
+//   2-5 drain the first half, 6-9 the second.
+template <int CG, int BN, typename OutT, int ES, int EPI = kEpiPlain, int KC = 1, int MH = 1>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmC, const __grid_constant__ TcParams p) {
@@ -665,22 +671,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     static_assert(KC == 1 || KC == 2, "K chunks per stage");
     static_assert(CG == 1 || (CG == 2 && BN >= 128), "CG");
     static_assert(ES == 2 || ES == 4, "element size");
+    static_assert(MH == 1 || (MH == 2 && CG == 1 && EPI == kEpiPlain && BN <= 128), "MH");
     constexpr int kChunkK = Elem<ES>::kChunkK;
     constexpr int kUmmaK = Elem<ES>::kUmmaK;
     constexpr int kMNChunk = Elem<ES>::kMNChunk;
-    constexpr int BM = kBlockM * CG;                      // rows per (pair) tile
+    constexpr int BM = kBlockM * CG * MH;                 // rows per (pair) tile
+    constexpr int kARows = kBlockM * MH;                  // A rows this CTA loads
     constexpr uint32_t kBRows = BN / CG;                  // B rows this CTA loads
     // per stage: kc chunks of A (kBlockM rows) and of B (kBRows rows), each
     // chunk a 128-byte-wide swizzled tile; an MN-major box is 128 bytes of
     // M/N by kc * kChunkK rows of K
     constexpr int kc = KC;
     constexpr int32_t kBlockK = kc * kChunkK;             // K elements per stage
-    constexpr uint32_t kATile = static_cast<uint32_t>(kc) * kATileBytes;
+    constexpr uint32_t kATile = static_cast<uint32_t>(kc) * kARows * 128u;
     constexpr uint32_t kBTile = static_cast<uint32_t>(kc) * kBRows * 128u;
     constexpr uint32_t kStageBytes = kATile + kBTile;
     static_assert(kStageBytes % 1024 == 0, "stages keep the C staging boxes 1024-byte aligned");
     constexpr uint32_t kChunkBytes = static_cast<uint32_t>(kBlockK) * 128u;   // one MN-major box
-    constexpr uint32_t kTmemCols = 2 * BN;               // double-buffered accumulator
+    constexpr uint32_t kTmemCols = 2 * MH * BN;          // double-buffered accumulator(s)
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -767,7 +775,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 auto a_parts = [&](int32_t m_first) {
                     if (!p.a_mn_major) return (m_first < p.M) ? 1 : 0;
                     int n = 0;
-                    for (int c = 0; c < kBlockM / kMNChunk; ++c) n += (m_first + kMNChunk * c < p.M);
+                    for (int c = 0; c < kARows / kMNChunk; ++c) n += (m_first + kMNChunk * c < p.M);
                     return n;
                 };
                 auto b_parts = [&](int32_t n_first) {
@@ -778,14 +786,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     return n;
                 };
                 auto tile_bytes = [&](uint32_t r) {
-                    const int32_t mf = tm * BM + static_cast<int32_t>(r) * kBlockM;
+                    const int32_t mf = tm * BM + static_cast<int32_t>(r) * kARows;
                     const int32_t nf = tn * BN + static_cast<int32_t>(r * kBRows);
                     return static_cast<uint32_t>(a_parts(mf)) *
                                (p.a_mn_major ? kChunkBytes : kATile) +
                            static_cast<uint32_t>(b_parts(nf)) *
                                (p.b_mn_major ? kChunkBytes : kBTile);
                 };
-                const int32_t m0 = tm * BM + static_cast<int32_t>(rank) * kBlockM;
+                const int32_t m0 = tm * BM + static_cast<int32_t>(rank) * kARows;
                 const int32_t n0 = tn * BN + static_cast<int32_t>(rank * kBRows);
                 const int na = a_parts(m0), nb = b_parts(n0);
                 // The even CTA's "full" barrier counts the bytes of both CTAs;
@@ -845,10 +853,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                             const uint16_t oh = static_cast<uint16_t>(r * p.conv_dil_h);
                             if (na) {
                                 if constexpr (CG == 1)
-                                    tma_load_im2col_4d(sa + q * kATileBytes, &tmA, &full[stage], c0, cw,
+                                    tma_load_im2col_4d(sa + q * kARows * 128, &tmA, &full[stage], c0, cw,
                                                        ch, cn, ow, oh, pol_a);
                                 else
-                                    tma_load_im2col_4d_pair(sa + q * kATileBytes, &tmA, fb, c0, cw, ch,
+                                    tma_load_im2col_4d_pair(sa + q * kARows * 128, &tmA, fb, c0, cw, ch,
                                                             cn, ow, oh, pol_a);
                             }
                         }
@@ -935,7 +943,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             // the next chunk's tile after four; MN-major kUmmaK rows of 128 bytes
             const uint32_t a_kstep = p.a_mn_major ? kUmmaK * 128u : kUmmaK * ES;
             const uint32_t b_kstep = p.b_mn_major ? kUmmaK * 128u : kUmmaK * ES;
-            const uint32_t a_cstep = p.a_mn_major ? 4u * a_kstep : kATileBytes;
+            const uint32_t a_cstep = p.a_mn_major ? 4u * a_kstep : kARows * 128u;
+            // MH = 2: the second half's A rows, 128 rows on (K-major) or two
+            // 64-row MN-major boxes on
+            const uint32_t a_hstep = p.a_mn_major ? 2u * kChunkBytes : kATileBytes;
             const uint32_t b_cstep = p.b_mn_major ? 4u * b_kstep : kBRows * 128u;
 
             const uint32_t smem_base = smem_addr(smem);
@@ -946,7 +957,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 tc_fence_after_sync();
-                const uint32_t d_tmem = tmem_base + buf * BN;
+                const uint32_t d_tmem = tmem_base + buf * (MH * BN);
                 for (int32_t kb = sg.kb0; kb < sg.kb1; ++kb) {
                     if (!wait_or_abort(&full[stage], phase, &abort_flag, p.wait_limit_ns)) {
                         record_error(p, kErrTimeoutMma, &abort_flag);
@@ -970,6 +981,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                             if constexpr (CG == 1) tc_mma_f16(d_tmem, ad, bd, p.idesc, acc);
                             else tc_mma_f16_pair(d_tmem, ad, bd, p.idesc, acc);
                         }
+                        if constexpr (MH == 2) {
+                            // the second half: its A rows, the same B, its accumulator
+                            const uint64_t ad2 = smem_desc_sw128(sa + a_hstep + ka, a_lbo, 1024);
+                            if constexpr (ES == 4) tc_mma_tf32(d_tmem + BN, ad2, bd, p.idesc, acc);
+                            else tc_mma_f16(d_tmem + BN, ad2, bd, p.idesc, acc);
+                        }
                     }
                     if constexpr (CG == 1) tc_commit(&empty[stage]);
                     else tc_commit_pair_multicast(&empty[stage], 0x3);
@@ -991,11 +1008,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
         // --------------------------------------------------------- epilogue
         // Warp w may read TMEM lanes 32*(w%4)..+31: two epilogue warps share each
-        // lane quarter and take alternate 32-column chunks of the tile.
+        // lane quarter and take alternate 32-column chunks of the tile (MH = 2:
+        // the two warps of a lane quarter take the two halves' accumulators,
+        // every chunk of each).
         const int quarter = warp & 3;                   // TMEM lanes 32*quarter..+31
-        const int half = (warp - 2) >> 2;               // 0: even chunks, 1: odd chunks
+        const int half = (warp - 2) >> 2;               // 0: even chunks, 1: odd chunks (MH = 2: M half)
         const int row_in_cta = quarter * 32 + lane;
-        const int row_in_tile = static_cast<int>(rank) * kBlockM + row_in_cta;
+        const int row_in_tile = (MH == 2 ? half : static_cast<int>(rank)) * kBlockM + row_in_cta;
+        const int ch_first = MH == 2 ? 0 : half;        // this warp's first chunk and step
+        const int ch_step = MH == 2 ? 1 : 2;
         uint32_t acc_i = 0;
         uint32_t cstep = 0;                     // TMA-store steps so far (the same in every warp)
         SegmentIter it(p, unit, units);
@@ -1010,8 +1031,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int32_t row = tm * BM + row_in_tile;              // D' row
             const int32_t col0 = tn * BN;                           // D' first column
             const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
-            const uint32_t t_row = t_lane + buf * BN;               // this tile's sums
-            const uint32_t t_spare = t_lane + (buf ^ 1u) * BN;     // the other buffer
+            const uint32_t t_row = t_lane + buf * (MH * BN) + (MH == 2 ? half * BN : 0);  // this tile's sums
+            const uint32_t t_spare = t_lane + (buf ^ 1u) * BN;     // the other buffer (MH = 1)
 
             // Stream-K tile split across CTAs g_first..g_last.  g_first, which
             // holds the tile's first k-blocks, finishes it.  For g_first this
@@ -1028,12 +1049,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             int32_t g_first = 0, g_last = -1;
             bool finisher = false;
             bool ok = true;
-            if (sg.slot >= 0) {
+            if (MH == 1 && sg.slot >= 0) {                        // (MH = 2: never split)
                 g_first = static_cast<int32_t>((static_cast<int64_t>(sg.tile) * KB) / L);
                 g_last = static_cast<int32_t>((static_cast<int64_t>(sg.tile + 1) * KB - 1) / L);
                 finisher = (unit == g_first);
             }
-            if (finisher) {
+            if (MH == 1 && finisher) {
                 // one counter per tile and CTA of the pair: CTA r of a pair
                 // finishes rows r * 128.. of the tile from the sums that CTA
                 // r of each contributing pair stored
@@ -1108,11 +1129,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // data-parallel only (the planner gives LayerNorm no stream-K)
                 ln_tile<OutT, BN>(p, t_row, row, row_in_cta, half, col0, tn, ln_red);
             } else {
-                float* my_slot = (sg.slot >= 0 && !finisher)
+                float* my_slot = (MH == 1 && sg.slot >= 0 && !finisher)
                                      ? p.partials + static_cast<int64_t>(sg.slot) * BM * BN
                                      : nullptr;
                 #pragma unroll 1
-                for (int ch = half; ch < BN / 32; ch += 2) {
+                for (int ch = ch_first; ch < BN / 32; ch += ch_step) {
                     uint32_t r[32];
                     __syncwarp();                      // tcgen05.ld is warp-collective
                     tmem_ld_32x32b_x32(t_row + ch * 32, r);
@@ -1120,7 +1141,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     float v[32];
                     #pragma unroll
                     for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
-                    if (finisher) {
+                    if (MH == 1 && finisher) {
                         uint32_t o[32];
                         __syncwarp();
                         tmem_ld_32x32b_x32(t_spare + ch * 32, o);
@@ -1130,7 +1151,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     const int32_t c0 = col0 + ch * 32;
                     if (my_slot == nullptr) epilogue_values<OutT>(p, row, c0, v);
-                    if (my_slot == nullptr && p.c_tma) {
+                    if (MH == 1 && my_slot == nullptr && p.c_tma) {
                         // C through shared memory: step ch / 2 of the tile is
                         // 64 columns (one 32-column chunk per half); the eight
                         // warps fill the staging box(es) and one thread stores

@@ -2,7 +2,8 @@
 // (KERN_ES bytes: 2 for FP16/BF16, 4 for FP32 used as TF32) and one output
 // type (KERN_OUT_T): single-CTA tiles of width 64/128/256 and CTA-pair tiles
 // of width 256, behind a plain launcher -- and, for 16-bit inputs, the
-// LayerNorm-epilogue variants (single-CTA 128/256, CTA-pair 256).  Each with
+// LayerNorm-epilogue variants (single-CTA 128/256, CTA-pair 256) and the
+// 256-row single-CTA tiles of width 64/128 (MH = 2, used by convolutions).  Each with
 // one K chunk per stage, and those whose three stages of two chunks fit in
 // shared memory also with two; the plain single-CTA 256-wide tile also with
 // two (two stages, used by convolutions).
@@ -16,9 +17,9 @@
 
 namespace gemm103 {
 
-template <int CG, int BN, int EPI = kEpiPlain, int KC = 1>
+template <int CG, int BN, int EPI = kEpiPlain, int KC = 1, int MH = 1>
 static cudaError_t launch_tc_cfg(const TcLaunch& l) {
-    auto kern = gemm_tc_kernel<CG, BN, KERN_OUT_T, KERN_ES, EPI, KC>;
+    auto kern = gemm_tc_kernel<CG, BN, KERN_OUT_T, KERN_ES, EPI, KC, MH>;
     {
         // The dynamic shared-memory limit is raised once per size (a host
         // call worth avoiding on every launch of a microsecond-scale GEMM).
@@ -103,6 +104,18 @@ static cudaError_t launch_tc_kc(const TcLaunch& l) {
         return cudaErrorInvalidValue;
     }
     if (l.epi != kEpiPlain) return cudaErrorInvalidValue;
+    if (l.mh == 2) {
+        // 256-row single-CTA tiles (16-bit inputs: convolutions)
+        if constexpr (KERN_ES == 2) {
+            if (l.cta_group != 1) return cudaErrorInvalidValue;
+            switch (l.block_n) {
+                case 64: return launch_tc_cfg<1, 64, kEpiPlain, KC, 2>(l);
+                case 128: return launch_tc_cfg<1, 128, kEpiPlain, KC, 2>(l);
+                default: return cudaErrorInvalidValue;
+            }
+        }
+        return cudaErrorInvalidValue;
+    }
     if (l.cta_group == 2) {
         switch (l.block_n) {
             case 256: return launch_tc_cfg<2, 256, kEpiPlain, KC>(l);

@@ -19,6 +19,7 @@ struct TcLaunch {
     int esize;          // input element bytes: 2 (FP16/BF16) or 4 (FP32 used as TF32)
     int epi;            // kEpiPlain or kEpiLayerNorm (16-bit inputs only)
     int kc;             // K chunks per stage: 1, or 2 (tiles whose 3 stages fit)
+    int mh;             // M halves per single-CTA tile: 1 (128 rows) or 2 (256 rows, BN <= 128)
     size_t smem_bytes;
     cudaStream_t stream;
 };
