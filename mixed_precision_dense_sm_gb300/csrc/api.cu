@@ -164,8 +164,21 @@ gemm_status_t make_plan(char transA, char transB, int64_t M, int64_t N, int64_t 
     opB.ld = ldb;
 
     // Skinny M: compute C^T = op(B)^T op(A)^T so the large N fills the
-    // 128-row MMA side and the small M becomes the MMA's N.
-    const bool swap = allow_swap && !ln && (M <= 64 && N >= 128);
+    // 128-row MMA side and the small M becomes the MMA's N.  Always for
+    // M <= 64; for M <= 128 (one tile row either way) only when the unswapped
+    // one-row plan would leave its single wave of 128-wide tiles under 80 %
+    // full and balance it by stream-K over 256-wide tiles, which the swapped
+    // stream-K beats (measured on GB300, FP16, weights N x K: M = 80-128 x
+    // 14336 x 4096 32 -> 27 us swapped, while 16384 x 8192 (one wave 84 %
+    // full) and 4096 x 4096 (too few tiles for a wave) ran 10-25 % faster
+    // unswapped).
+    const int64_t one_row_tiles = ceil_div(N, 128);
+    const double one_row_fill =
+        static_cast<double>(one_row_tiles) /
+        static_cast<double>(ceil_div(one_row_tiles, num_sms) * num_sms);
+    const bool mid_swap = M > 64 && M <= 128 && K >= kLongK * 64 &&
+                          one_row_tiles >= (num_sms + 1) / 2 && one_row_fill < kMinWaveFill;
+    const bool swap = allow_swap && !ln && N >= 128 && (M <= 64 || mid_swap);
     pl.pub.swap_ab = swap ? 1 : 0;
     if (swap) {
         pl.a = opB;

@@ -166,6 +166,24 @@ def test_quick_paths_and_swap_rule():
     assert plan(w)["swap_ab"] == 0
 
 
+@pytest.mark.parametrize("N,K,swapped", [(16384, 8192, False), (4096, 4096, False),
+                                         (14336, 4096, True), (14336, 1024, False),
+                                         (8192, 8192, False)])
+def test_decode_batches_up_to_128_rows(N, K, swapped):
+    """64 < M <= 128 (one tile row): swapped only when the unswapped plan's
+    single wave of 128-wide tiles would be under 80 % full and long in K
+    (then balanced by stream-K over 256-wide tiles, which the swapped stream-K
+    beats); M <= 64 always swaps, M > 128 never."""
+    for M in (80, 96, 112, 128):
+        w = workloads.Workload("d", M, N, K, "N", "T", DT_F16, DT_F16, 1.0, 0.0, "N1", "N002")
+        p = plan(w)
+        assert p["swap_ab"] == (1 if swapped else 0), (M, p)
+        assert p["path_name"] == ("skinny" if swapped else "tiled_1sm")
+    for M, want in ((64, 1), (129, 0)):
+        w = workloads.Workload("d", M, N, K, "N", "T", DT_F16, DT_F16, 1.0, 0.0, "N1", "N002")
+        assert plan(w)["swap_ab"] == want
+
+
 def test_pair_tiles_only_when_they_fill_the_gpu():
     def path(M, N, K, sms=152):
         w = workloads.Workload("p", M, N, K, "N", "T", DT_BF16, DT_BF16, 1.0, 0.0, "U", "U")

@@ -1,4 +1,5 @@
 """GPU parity: the CUDA path (through the C ABI) against the CPU oracle."""
+import dataclasses
 import itertools
 
 import numpy as np
@@ -124,6 +125,29 @@ def test_workload_full(g, orc, name):
     print(name, stats)
     if w.c_dtype != DT_F32:
         assert stats["strict_1ulp_frac"] >= STRICT_FLOOR[name], stats
+
+
+@pytest.mark.parametrize("M", [96, 128])
+@pytest.mark.parametrize("N,K", [(14336, 4096), (16384, 8192)], ids=["swapped", "tiled"])
+def test_decode_batch_up_to_128_rows(g, orc, M, N, K):
+    """Decode batches of 96 and 128 tokens (FP16, weights N x K, FP16 out) on
+    both plans the planner picks between for 64 < M <= 128: swapped stream-K
+    (14336 x 4096) and unswapped one-row tiles (16384 x 8192); every output
+    element against the oracle, and integer inputs bit-exact."""
+    import mixed_precision_dense_sm_gb300 as lib
+    w = W(M, N, K, "N", "T", DT_F16, DT_F16, name=f"decode_{M}x{N}x{K}")
+    w = dataclasses.replace(w, b_dist="N002")
+    st, p = lib.gemm_plan_query("N", "T", M, N, K, 1.0, 256, K, 256, K, 0.0, 256, N,
+                                (DT_F16, DT_F16, DT_F16),
+                                num_sms=torch.cuda.get_device_properties(0).multi_processor_count)
+    assert st == 0 and p["swap_ab"] == (1 if N == 14336 else 0), p
+    inp = workloads.make_inputs(w)
+    C = gc.run_gpu(g, w, inp)
+    stats = gc.check_full(orc, w, inp, C)
+    assert stats["strict_1ulp_frac"] >= 0.995, stats
+    inp = gc.integer_inputs(w, -4, 4)
+    C = gc.run_gpu(g, w, inp)
+    gc.check_full(orc, w, inp, C, exact=True)
 
 
 @pytest.mark.parametrize("name", ["linear_8192x4096x14336_bf16", "linear_8192x14336x4096_bf16"])
