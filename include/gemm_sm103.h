@@ -278,6 +278,10 @@ typedef struct {
                               or two or more data-parallel tiles per CTA); 0: per-thread
                               row stores */
     int64_t workspace_bytes;
+    int32_t conv_rows;     /* convolutions: > 0 when each tile is this many whole output rows
+                              of one image, loaded per filter tap as one tiled box of the
+                              input (stride 1, 256-row single-CTA tiles); 0: im2col tiles
+                              (and every GEMM) */
 } gemm_plan_t;
 
 /*

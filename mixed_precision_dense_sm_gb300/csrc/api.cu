@@ -51,6 +51,8 @@ constexpr int64_t kStreamOnceBytes = 96ll << 20;
 // Convolutions with at most 128 output channels run 256-row single-CTA tiles
 // (make_plan's mh2): the im2col box of 256 output pixels feeds two MMAs.
 constexpr bool kConvTwoHalves = true;
+// ... and, at stride 1, tiles of whole output rows loaded by tiled boxes.
+constexpr bool kConvWholeRows = true;
 // Stream-K fix-up: one FP32 partial tile read back by the finisher costs about
 // as long as this many k-blocks of 256 bytes per row (128 BF16 / FP16 or 64
 // TF32 elements) of the tile's MMA (measured on GB300).
@@ -89,6 +91,9 @@ struct Plan {
     // the plain epilogue stores C through shared memory by TMA (C rows
     // 16-byte aligned, not swapped): kCStageBytes of staging after the stages
     bool c_tma;
+    // convolution on whole-row tiles (conv_plan): output rows per tile and
+    // tiles per image; 0 for im2col tiles
+    int32_t conv_rows, conv_tpi;
 };
 
 bool is_n(char t) { return t == 'N' || t == 'n'; }
@@ -558,6 +563,30 @@ bool encode_conv_input(const ConvDesc& cd, CUtensorMap* map, int32_t dtype, uint
     return r == CUDA_SUCCESS;
 }
 
+// The input X (N, H, W, C) as a tiled 4-D map (C, W, H, N) for whole-row
+// convolution tiles: a box is 64 channels x Q pixels x `rows` image rows of
+// one image (stride 1), in shared memory rows x Q pixel rows of 128 bytes in
+// the 128-byte swizzle -- the K-major A tile the MMA reads; positions outside
+// the image (the padding, or a window past the last row) read zeros.
+bool encode_conv_rows(EncodeTiledFn encode, const ConvDesc& cd, CUtensorMap* map, int32_t dtype,
+                      uint32_t rows) {
+    const int64_t es = 2;
+    const cuuint64_t dims[4] = {static_cast<cuuint64_t>(cd.C), static_cast<cuuint64_t>(cd.W),
+                                static_cast<cuuint64_t>(cd.H), static_cast<cuuint64_t>(cd.N)};
+    const cuuint64_t strides[3] = {static_cast<cuuint64_t>(cd.C * es),
+                                   static_cast<cuuint64_t>(cd.W * cd.C * es),
+                                   static_cast<cuuint64_t>(cd.H * cd.W * cd.C * es)};
+    const cuuint32_t box[4] = {64u, static_cast<cuuint32_t>(cd.Q), rows, 1u};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    return encode(map,
+                  dtype == GEMM_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                     : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                  4, const_cast<void*>(cd.X), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+           CUDA_SUCCESS;
+}
+
 // The filter (K, R, S, C) as a 3-D map (C, R*S, K): a box is 64 channels of
 // one tap for box_rows output channels; channels past C read zeros.
 bool encode_conv_filter(EncodeTiledFn encode, const ConvDesc& cd, CUtensorMap* map,
@@ -728,7 +757,15 @@ gemm_status_t enqueue_plan(const Plan& pl, EncodeTiledFn encode, int num_sms, ui
     // K-major ones kc chunks of 128 bytes of K by the tile's rows.
     const uint32_t mn_box = static_cast<uint32_t>(pl.pub.block_k);
     bool ok;
-    if (conv != nullptr) {
+    if (conv != nullptr && pl.conv_rows > 0) {
+        ok = encode_conv_rows(encode, *conv, &l.tmA, dt.a, static_cast<uint32_t>(pl.conv_rows));
+        if (pl.kc == 1)
+            ok = ok && encode_conv_filter(encode, *conv, &l.tmB, dt.b, static_cast<uint32_t>(bn / cg));
+        else
+            ok = ok && encode_operand(encode, &l.tmB, dt.b, conv->Wt, conv->R * conv->S * conv->C,
+                                      conv->K, conv->R * conv->S * conv->C,
+                                      static_cast<uint32_t>(bn / cg), pl.kc);
+    } else if (conv != nullptr) {
         ok = encode_conv_input(*conv, &l.tmA, dt.a, static_cast<uint32_t>(kBlockM * pl.mh));
         if (pl.kc == 1)
             ok = ok && encode_conv_filter(encode, *conv, &l.tmB, dt.b, static_cast<uint32_t>(bn / cg));
@@ -830,6 +867,12 @@ gemm_status_t enqueue_plan(const Plan& pl, EncodeTiledFn encode, int num_sms, ui
         p.conv_pad_w = static_cast<int32_t>(conv->pad_w);
         p.conv_dil_h = static_cast<int32_t>(conv->dil_h);
         p.conv_dil_w = static_cast<int32_t>(conv->dil_w);
+        if (pl.conv_rows > 0) {
+            p.conv_tiled = 1;
+            p.conv_rows = pl.conv_rows;
+            p.conv_tpi = pl.conv_tpi;
+            p.conv_a_bytes = static_cast<uint32_t>(conv->Q * pl.conv_rows * 128);
+        }
     }
     l.grid = pl.pub.grid;
     l.cta_group = cg;
@@ -926,9 +969,33 @@ gemm_status_t conv_plan(int64_t N, int64_t H, int64_t W, int64_t C, int64_t K, i
     // single-CTA 256-wide tile): the im2col boxes re-read X from L2 (R*S
     // times) and the filter stays in L2, so one stage in flight covers the
     // load latency, where a GEMM streaming an operand from DRAM needs three.
-    return make_plan('N', 'T', M, K, kfake, alpha, X, kfake, Wt, kfake, beta, Y, K, dt, num_sms,
-                     smem_optin, pl, false, false, C % 64 == 0 ? kMaxKc : 1, 2, true, 0,
-                     kConvTwoHalves);
+    gemm_status_t st = make_plan('N', 'T', M, K, kfake, alpha, X, kfake, Wt, kfake, beta, Y, K,
+                                 dt, num_sms, smem_optin, pl, false, false,
+                                 C % 64 == 0 ? kMaxKc : 1, 2, true, 0, kConvTwoHalves);
+    if (st != GEMM_OK || pl.pub.path != GEMM_PATH_TILED_1SM || pl.mh != 2) return st;
+    // Stride 1 on 256-row tiles: a tile is T whole output rows of one image
+    // (T Q <= 256), and each filter tap's A operand one tiled box of the
+    // input -- 64 channels x Q x T pixels at the tap's shifted window, zero
+    // outside the image -- fetched as T contiguous runs of Q pixels, where an
+    // im2col box fetches every pixel on its own.  The images' rows are split
+    // evenly: tiles per image = ceil(P / floor(256 / Q)), T = ceil(P / that).
+    if (kConvWholeRows && stride_h == 1 && stride_w == 1 && Q <= 256 && P > 0) {
+        const int64_t tmax = (kBlockM * 2) / Q;
+        const int64_t tpi = ceil_div(P, tmax);
+        const int64_t T = ceil_div(P, tpi);
+        const int64_t tiles_m = N * tpi;
+        if (tiles_m <= INT32_MAX / pl.tiles_n) {
+            pl.conv_rows = static_cast<int32_t>(T);
+            pl.conv_tpi = static_cast<int32_t>(tpi);
+            pl.pub.conv_rows = pl.conv_rows;
+            pl.tiles_m = static_cast<int32_t>(tiles_m);
+            pl.pub.tiles_m = pl.tiles_m;
+            pl.pub.num_tiles = static_cast<int32_t>(tiles_m * pl.tiles_n);
+            const int64_t units = num_sms;
+            pl.pub.grid = static_cast<int32_t>(pl.pub.num_tiles < units ? pl.pub.num_tiles : units);
+        }
+    }
+    return GEMM_OK;
 }
 
 bool dtype16or32(int32_t t) { return t == GEMM_F16 || t == GEMM_BF16 || t == GEMM_F32; }

@@ -127,6 +127,16 @@ struct TcParams {
     int32_t conv_S;             // filter width
     int32_t conv_P, conv_Q;     // output height and width
     int32_t conv_stride_h, conv_stride_w, conv_pad_h, conv_pad_w, conv_dil_h, conv_dil_w;
+    // conv_tiled (stride 1, single-CTA tiles): a tile is conv_rows whole
+    // output rows of one image (tile row tm: image tm / conv_tpi, first row
+    // (tm % conv_tpi) * conv_rows), and A is loaded per filter tap by a tiled
+    // 4-D map over X (C, W, H, N) -- a box of 64 channels x Q x conv_rows
+    // pixels at the tap's shifted window, zeros outside the image -- instead
+    // of the im2col map; conv_a_bytes = one such box
+    int32_t conv_tiled;
+    int32_t conv_rows;
+    int32_t conv_tpi;
+    uint32_t conv_a_bytes;
     // LayerNorm after the linear layer (kernels instantiated with EPI ==
     // kEpiLayerNorm): h = round_C(alpha * acc + beta * C + bias) per element;
     // ln_fused (the whole row in one tile): each row is normalised in the
@@ -788,6 +798,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 auto tile_bytes = [&](uint32_t r) {
                     const int32_t mf = tm * BM + static_cast<int32_t>(r) * kARows;
                     const int32_t nf = tn * BN + static_cast<int32_t>(r * kBRows);
+                    if (p.conv_tiled)
+                        return static_cast<uint32_t>(kc) * p.conv_a_bytes +
+                               static_cast<uint32_t>(b_parts(nf)) * kBTile;
                     return static_cast<uint32_t>(a_parts(mf)) *
                                (p.a_mn_major ? kChunkBytes : kATile) +
                            static_cast<uint32_t>(b_parts(nf)) *
@@ -804,7 +817,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // convolution: the first window of this CTA's rows (output
                 // pixel m0) as the input coordinates of its top-left pixel
                 int32_t cn = 0, ch = 0, cw = 0;
-                if (p.conv) {
+                if (p.conv_tiled) {
+                    // the tile's image and first output row
+                    cn = tm / p.conv_tpi;
+                    ch = (tm - cn * p.conv_tpi) * p.conv_rows - p.conv_pad_h;
+                    cw = -p.conv_pad_w;
+                } else if (p.conv) {
                     const int32_t pq = p.conv_P * p.conv_Q;
                     cn = m0 / pq;
                     const int32_t rem = m0 - cn * pq;
@@ -851,7 +869,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                             const int32_t r = tap / p.conv_S;
                             const uint16_t ow = static_cast<uint16_t>((tap - r * p.conv_S) * p.conv_dil_w);
                             const uint16_t oh = static_cast<uint16_t>(r * p.conv_dil_h);
-                            if (na) {
+                            if (p.conv_tiled) {
+                                // the tap's window of the tile's output rows:
+                                // input (cw + ow + q', ch + oh + p') for output (p', q')
+                                if constexpr (CG == 1)
+                                    tma_load_4d(sa + q * kARows * 128, &tmA, &full[stage], c0,
+                                                cw + ow, ch + oh, cn, pol_a);
+                            } else if (na) {
                                 if constexpr (CG == 1)
                                     tma_load_im2col_4d(sa + q * kARows * 128, &tmA, &full[stage], c0, cw,
                                                        ch, cn, ow, oh, pol_a);
@@ -1028,7 +1052,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t buf = acc_i & 1u;
             int32_t tm, tn;
             tile_coords(p, sg.tile, tm, tn);
-            const int32_t row = tm * BM + row_in_tile;              // D' row
+            int32_t row = tm * BM + row_in_tile;                    // D' row
+            if (p.conv_tiled) {
+                // output pixel row_in_tile of the tile's conv_rows image rows
+                // (rows past the image's last output row are not stored)
+                const int32_t n = tm / p.conv_tpi;
+                const int32_t p0 = (tm - n * p.conv_tpi) * p.conv_rows;
+                const int32_t nrow = p.conv_P - p0 < p.conv_rows ? p.conv_P - p0 : p.conv_rows;
+                row = row_in_tile < nrow * p.conv_Q ? (n * p.conv_P + p0) * p.conv_Q + row_in_tile
+                                                    : p.M;
+            }
             const int32_t col0 = tn * BN;                           // D' first column
             const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
             const uint32_t t_row = t_lane + buf * (MH * BN) + (MH == 2 ? half * BN : 0);  // this tile's sums

@@ -120,6 +120,19 @@ __device__ __forceinline__ void tma_load_3d(void* smem_dst, const CUtensorMap* m
         : "memory");
 }
 
+// 4-D tiled load of one box at coordinates (c0 innermost, c1, c2, c3);
+// elements outside the tensor (negative coordinates included) read zero.
+__device__ __forceinline__ void tma_load_4d(void* smem_dst, const CUtensorMap* map, uint64_t* bar,
+                                            int32_t c0, int32_t c1, int32_t c2, int32_t c3,
+                                            uint64_t cache_policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3, %4, %5}], [%6], %7;" ::"r"(smem_addr(smem_dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3),
+        "r"(smem_addr(bar)), "l"(cache_policy)
+        : "memory");
+}
+
 // im2col load from a 4-D (C, W, H, N) map: `pixelsPerColumn` consecutive
 // convolution windows starting at the window whose top-left input pixel is
 // (w, h) of image n, each contributing channels c .. c + channelsPerPixel - 1

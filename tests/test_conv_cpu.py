@@ -36,7 +36,8 @@ def test_plan_is_the_gemm_of_the_convolution():
     # channels, two chunks per stage when C is a multiple of 64
     st, p = plan(N=32, H=56, W=56, C=64, K=64)
     assert st == OK and p["k_blocks"] == 5 and p["block_k"] == 128
-    assert p["tiles_m"] * 128 >= 32 * 56 * 56
+    # whole-row tiles: 32 images x 14 tiles of 4 output rows (4 x 56 <= 256)
+    assert p["conv_rows"] == 4 and p["tiles_m"] == 32 * 14 and p["block_m"] == 256
     assert p["swap_ab"] == 0 and p["pack_a"] == 0 and p["pack_b"] == 0
     assert p["a_mn_major"] == 0 and p["b_mn_major"] == 0
     st, p = plan(N=16, H=64, W=64, C=256, K=256)
@@ -51,6 +52,27 @@ def test_plan_is_the_gemm_of_the_convolution():
     # empty output and alpha = 0 read nothing
     assert plan(N=0)[1]["path_name"] == "noop"
     assert plan(alpha=0.0, X=0, Wt=0, beta=1.0)[1]["path_name"] == "scale"
+
+
+@pytest.mark.parametrize("H,W,stride,R,K,rows", [
+    (56, 56, 1, 3, 64, 4), (28, 28, 1, 3, 128, 7), (14, 14, 1, 3, 64, 14), (9, 300, 1, 3, 64, 0),
+    (56, 56, 2, 3, 64, 0), (64, 64, 1, 3, 256, 0), (17, 17, 1, 1, 96, 9), (40, 50, 1, 5, 64, 5)])
+def test_whole_row_tiles(H, W, stride, R, K, rows):
+    """Stride-1 convolutions on 256-row single-CTA tiles (at most 128 output
+    channels) tile each image by whole output rows, T Q <= 256, the rows split
+    evenly: tiles per image = ceil(P / floor(256 / Q)), T = ceil(P / that).
+    Strided layers, rows wider than 256 pixels and CTA-pair tiles keep the
+    im2col tiles (conv_rows 0)."""
+    pad = (R // 2, R // 2)
+    st, p = plan(N=3, H=H, W=W, C=64, K=K, R=R, S=R, pad=pad, stride=(stride, stride))
+    assert st == OK and p["conv_rows"] == rows, p
+    if rows:
+        P = (H + 2 * pad[0] - R) // stride + 1
+        Q = (W + 2 * pad[1] - R) // stride + 1
+        tpi = p["tiles_m"] // 3
+        assert p["tiles_m"] == 3 * tpi and tpi == -(-P // (256 // Q))
+        assert rows == -(-P // tpi) and rows * Q <= 256 and (tpi - 1) * rows < P
+        assert p["block_m"] == 256 and p["path_name"] == "tiled_1sm" and p["sk_len"] == 0
 
 
 def test_argument_checks():

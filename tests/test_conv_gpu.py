@@ -110,6 +110,29 @@ def test_geometries_integer_exact(g, orc, geo):
     run_and_check(g, orc, geo, dt=(DT_BF16, DT_F16)[hash(geo) % 2], ydt=DT_F32, seed=sum(geo[:7]))
 
 
+WHOLE_ROWS = [
+    # N, H, W, C, K, R, S, pad, stride, dilation
+    (3, 23, 21, 64, 64, 3, 3, (1, 1), (1, 1), (1, 1)),      # 12 rows per tile, the last 11
+    (2, 30, 40, 24, 40, 3, 3, (2, 2), (1, 1), (2, 2)),      # dilation 2, 24 channels (one chunk)
+    (2, 9, 130, 64, 128, 3, 5, (1, 2), (1, 1), (1, 1)),     # 130-pixel rows: one row per tile
+    (1, 33, 33, 128, 96, 1, 1, (0, 0), (1, 1), (1, 1)),     # 1 x 1: 7 rows per tile, the last 5
+]
+
+
+@pytest.mark.parametrize("geo", WHOLE_ROWS, ids=[f"r{i}" for i in range(len(WHOLE_ROWS))])
+def test_whole_row_tiles(g, orc, geo):
+    """Stride-1 layers with at most 128 output channels run whole-row tiles:
+    each tap's A tile is one tiled box of the input (T output rows x Q
+    pixels, zeros outside the image), masked past the image's last row.
+    Integer inputs bit-exact, then random inputs with a 16-bit output."""
+    import mixed_precision_dense_sm_gb300 as lib
+    st, p = lib.conv2d_plan_query(*geo, 1.0, 256, 256, 0.0, 1 << 44, (DT_BF16, DT_BF16, DT_F32),
+                                  num_sms=torch.cuda.get_device_properties(0).multi_processor_count)
+    assert st == 0 and p["conv_rows"] > 0, p
+    run_and_check(g, orc, geo, dt=DT_BF16, ydt=DT_F32, seed=sum(geo[:7]))
+    run_and_check(g, orc, geo, dt=DT_F16, ydt=DT_BF16, integer=False, beta=0.5, seed=3)
+
+
 @pytest.mark.parametrize("ydt", [DT_F32, DT_F16, DT_BF16])
 def test_random_every_output_type(g, orc, ydt):
     for i, geo in enumerate(GEOS[:8]):
