@@ -38,8 +38,9 @@ __device__ __forceinline__ float erfc_nr(float u) {
 // x (1 - erfc(x / sqrt 2) / 2), for x < 0 x erfc(|x| / sqrt 2) / 2 -- no
 // cancellation on either side, so the relative error stays near that of
 // erfc_nr even where Phi(x) is tiny (a 16-bit output of a very negative x is
-// then still correctly rounded or one ulp off).  About twenty instructions:
-// the epilogue runs once per output element and hides under the next tile's
+// then still correctly rounded or one ulp off).  About twenty instructions,
+// run once per output element; the epilogue evaluates 32 of them at a time
+// (act32 below) so their chains interleave and hide under the next tile's
 // MMA.  NaN stays NaN; GELU(+inf) = inf, GELU(-inf) = NaN (-inf * 0), as
 // x Phi(x) evaluates in IEEE arithmetic.
 __device__ __forceinline__ float gelu(float x) {
@@ -47,12 +48,33 @@ __device__ __forceinline__ float gelu(float x) {
     return x >= 0.0f ? x * fmaf(-0.5f, e, 1.0f) : 0.5f * x * e;
 }
 
+__device__ __forceinline__ float silu(float x) { return __fdividef(x, 1.0f + __expf(-x)); }
+
+__device__ __forceinline__ float relu(float x) {
+    return x > 0.0f ? x : (x != x ? x : 0.0f);     // NaN stays NaN
+}
+
 __device__ __forceinline__ float activate(int act, float x) {
     switch (act) {
-        case kActRelu: return x > 0.0f ? x : (x != x ? x : 0.0f);     // NaN stays NaN
+        case kActRelu: return relu(x);
         case kActGelu: return gelu(x);
-        case kActSilu: return __fdividef(x, 1.0f + __expf(-x));
+        case kActSilu: return silu(x);
         default: return x;
+    }
+}
+
+// The activation on 32 values, the choice made once outside the element loop
+// so that the 32 independent evaluations interleave.
+__device__ __forceinline__ void act32(int act, float (&v)[32]) {
+    if (act == kActGelu) {
+        #pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = gelu(v[j]);
+    } else if (act == kActSilu) {
+        #pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = silu(v[j]);
+    } else if (act == kActRelu) {
+        #pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = relu(v[j]);
     }
 }
 

@@ -371,10 +371,7 @@ __device__ __forceinline__ void bias_act(const TcParams& p, int32_t row, int32_t
             for (int j = 0; j < 32; ++j) v[j] += b[j];
         }
     }
-    if (p.act != 0) {
-        #pragma unroll
-        for (int j = 0; j < 32; ++j) v[j] = activate(p.act, v[j]);
-    }
+    act32(p.act, v);
 }
 
 // act(alpha * v + beta * C + bias) in place for one row of 32 columns at D'
