@@ -279,9 +279,13 @@ typedef struct {
                               row stores */
     int64_t workspace_bytes;
     int32_t conv_rows;     /* convolutions: > 0 when each tile is this many whole output rows
-                              of one image, loaded per filter tap as one tiled box of the
-                              input (stride 1, 256-row single-CTA tiles); 0: im2col tiles
-                              (and every GEMM) */
+                              of one image, loaded as tiled boxes of the input (stride 1,
+                              256-row single-CTA tiles); 0: im2col tiles (and every GEMM) */
+    int32_t conv_pitch;    /* whole-row tiles: the tile's A rows per output row.  Q rounded
+                              up to 8 for halo units (one box of conv_rows + (R - 1) dil_h
+                              input rows per filter column and 64-channel block, the R taps
+                              read at row offsets of the box: k_blocks = S ceil(C / 64));
+                              Q for one box per filter tap; 0 for im2col tiles */
 } gemm_plan_t;
 
 /*

@@ -66,7 +66,8 @@ class Plan(ctypes.Structure):
         "path", "block_m", "block_n", "block_k", "stages", "split_k", "grid", "num_tiles",
         "pack_a", "pack_b", "a_mn_major", "b_mn_major", "swap_ab", "c_vector", "sk_len",
         "sk_max_seg", "k_blocks", "tiles_m", "tiles_n", "transpose_ab", "c_tma")] + \
-        [("workspace_bytes", ctypes.c_int64), ("conv_rows", ctypes.c_int32)]
+        [("workspace_bytes", ctypes.c_int64), ("conv_rows", ctypes.c_int32),
+         ("conv_pitch", ctypes.c_int32)]
 
     def as_dict(self):
         d = {n: getattr(self, n) for n, _ in self._fields_}

@@ -51,8 +51,10 @@ constexpr int64_t kStreamOnceBytes = 96ll << 20;
 // Convolutions with at most 128 output channels run 256-row single-CTA tiles
 // (make_plan's mh2): the im2col box of 256 output pixels feeds two MMAs.
 constexpr bool kConvTwoHalves = true;
-// ... and, at stride 1, tiles of whole output rows loaded by tiled boxes.
+// ... and, at stride 1, tiles of whole output rows loaded by tiled boxes,
+// as halo units (one box per filter column) where they fit.
 constexpr bool kConvWholeRows = true;
+constexpr bool kConvHalo = true;
 // Stream-K fix-up: one FP32 partial tile read back by the finisher costs about
 // as long as this many k-blocks of 256 bytes per row (128 BF16 / FP16 or 64
 // TF32 elements) of the tile's MMA (measured on GB300).
@@ -92,8 +94,12 @@ struct Plan {
     // 16-byte aligned, not swapped): kCStageBytes of staging after the stages
     bool c_tma;
     // convolution on whole-row tiles (conv_plan): output rows per tile and
-    // tiles per image; 0 for im2col tiles
+    // tiles per image; 0 for im2col tiles.  conv_halo: halo units (pitch,
+    // the halo box's bytes, the A region and the whole stage)
     int32_t conv_rows, conv_tpi;
+    bool conv_halo;
+    int32_t conv_pitch;
+    uint32_t halo_box_bytes, halo_a_region, halo_stage_bytes;
 };
 
 bool is_n(char t) { return t == 'N' || t == 'n'; }
@@ -564,19 +570,20 @@ bool encode_conv_input(const ConvDesc& cd, CUtensorMap* map, int32_t dtype, uint
 }
 
 // The input X (N, H, W, C) as a tiled 4-D map (C, W, H, N) for whole-row
-// convolution tiles: a box is 64 channels x Q pixels x `rows` image rows of
-// one image (stride 1), in shared memory rows x Q pixel rows of 128 bytes in
-// the 128-byte swizzle -- the K-major A tile the MMA reads; positions outside
-// the image (the padding, or a window past the last row) read zeros.
+// convolution tiles: a box is 64 channels x `pixels` pixels x `rows` image
+// rows of one image (stride 1), in shared memory rows x pixels rows of 128
+// bytes in the 128-byte swizzle -- the K-major A tile the MMA reads;
+// positions outside the image (the padding, or a window past the last row
+// or column) read zeros.
 bool encode_conv_rows(EncodeTiledFn encode, const ConvDesc& cd, CUtensorMap* map, int32_t dtype,
-                      uint32_t rows) {
+                      uint32_t rows, uint32_t pixels) {
     const int64_t es = 2;
     const cuuint64_t dims[4] = {static_cast<cuuint64_t>(cd.C), static_cast<cuuint64_t>(cd.W),
                                 static_cast<cuuint64_t>(cd.H), static_cast<cuuint64_t>(cd.N)};
     const cuuint64_t strides[3] = {static_cast<cuuint64_t>(cd.C * es),
                                    static_cast<cuuint64_t>(cd.W * cd.C * es),
                                    static_cast<cuuint64_t>(cd.H * cd.W * cd.C * es)};
-    const cuuint32_t box[4] = {64u, static_cast<cuuint32_t>(cd.Q), rows, 1u};
+    const cuuint32_t box[4] = {64u, pixels, rows, 1u};
     const cuuint32_t estr[4] = {1, 1, 1, 1};
     return encode(map,
                   dtype == GEMM_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
@@ -757,8 +764,14 @@ gemm_status_t enqueue_plan(const Plan& pl, EncodeTiledFn encode, int num_sms, ui
     // K-major ones kc chunks of 128 bytes of K by the tile's rows.
     const uint32_t mn_box = static_cast<uint32_t>(pl.pub.block_k);
     bool ok;
-    if (conv != nullptr && pl.conv_rows > 0) {
-        ok = encode_conv_rows(encode, *conv, &l.tmA, dt.a, static_cast<uint32_t>(pl.conv_rows));
+    if (conv != nullptr && pl.conv_halo) {
+        ok = encode_conv_rows(encode, *conv, &l.tmA, dt.a,
+                              static_cast<uint32_t>(pl.conv_rows + (conv->R - 1) * conv->dil_h),
+                              static_cast<uint32_t>(pl.conv_pitch));
+        ok = ok && encode_conv_filter(encode, *conv, &l.tmB, dt.b, static_cast<uint32_t>(bn / cg));
+    } else if (conv != nullptr && pl.conv_rows > 0) {
+        ok = encode_conv_rows(encode, *conv, &l.tmA, dt.a, static_cast<uint32_t>(pl.conv_rows),
+                              static_cast<uint32_t>(conv->Q));
         if (pl.kc == 1)
             ok = ok && encode_conv_filter(encode, *conv, &l.tmB, dt.b, static_cast<uint32_t>(bn / cg));
         else
@@ -868,10 +881,15 @@ gemm_status_t enqueue_plan(const Plan& pl, EncodeTiledFn encode, int num_sms, ui
         p.conv_dil_h = static_cast<int32_t>(conv->dil_h);
         p.conv_dil_w = static_cast<int32_t>(conv->dil_w);
         if (pl.conv_rows > 0) {
-            p.conv_tiled = 1;
+            p.conv_tiled = pl.conv_halo ? 2 : 1;
             p.conv_rows = pl.conv_rows;
             p.conv_tpi = pl.conv_tpi;
-            p.conv_a_bytes = static_cast<uint32_t>(conv->Q * pl.conv_rows * 128);
+            p.conv_pitch = pl.conv_pitch;
+            p.conv_R = static_cast<int32_t>(conv->R);
+            p.conv_a_bytes = pl.conv_halo ? pl.halo_box_bytes
+                                          : static_cast<uint32_t>(conv->Q * pl.conv_rows * 128);
+            p.halo_a_region = pl.halo_a_region;
+            p.halo_stage_bytes = pl.halo_stage_bytes;
         }
     }
     l.grid = pl.pub.grid;
@@ -973,17 +991,40 @@ gemm_status_t conv_plan(int64_t N, int64_t H, int64_t W, int64_t C, int64_t K, i
                                  dt, num_sms, smem_optin, pl, false, false,
                                  C % 64 == 0 ? kMaxKc : 1, 2, true, 0, kConvTwoHalves);
     if (st != GEMM_OK || pl.pub.path != GEMM_PATH_TILED_1SM || pl.mh != 2) return st;
-    // Stride 1 on 256-row tiles: a tile is T whole output rows of one image
-    // (T Q <= 256), and each filter tap's A operand one tiled box of the
-    // input -- 64 channels x Q x T pixels at the tap's shifted window, zero
-    // outside the image -- fetched as T contiguous runs of Q pixels, where an
-    // im2col box fetches every pixel on its own.  The images' rows are split
-    // evenly: tiles per image = ceil(P / floor(256 / Q)), T = ceil(P / that).
+    // Stride 1 on 256-row tiles: a tile is T whole output rows of one image,
+    // and A is loaded by tiled boxes of the input instead of im2col boxes.
+    //  * Halo units (kConvHalo): the tile's rows sit at a pitch of Q rounded
+    //    up to 8 pixels (T pitch <= 256); pipeline step = (filter column s,
+    //    64-channel block): one box of T + (R - 1) dil_h image rows x pitch
+    //    pixels at the column's shifted window, and the column's R filter
+    //    taps; tap r's A starts r dil_h pitch rows into the box (a multiple of
+    //    8 rows: the swizzle atoms line up).  Each input pixel is fetched once
+    //    per filter column, not once per tap.
+    //  * Otherwise one box per tap of T rows x Q pixels (pitch Q).
+    // The images' rows are split evenly: tiles per image = ceil(P / Tmax),
+    // T = ceil(P / that).
     if (kConvWholeRows && stride_h == 1 && stride_w == 1 && Q <= 256 && P > 0) {
-        const int64_t tmax = (kBlockM * 2) / Q;
+        const int64_t pitch = kConvHalo ? round_up(Q, 8) : Q;
+        const int64_t tmax = (kBlockM * 2) / pitch;
         const int64_t tpi = ceil_div(P, tmax);
         const int64_t T = ceil_div(P, tpi);
         const int64_t tiles_m = N * tpi;
+        bool halo = kConvHalo && pitch <= 256 && T + (R - 1) * dil_h <= 256;
+        uint32_t box = 0, a_region = 0, stage = 0;
+        int64_t stages = 0;
+        if (halo) {
+            const int64_t rows = T + (R - 1) * dil_h;
+            box = static_cast<uint32_t>(rows * pitch * 128);
+            // the MMAs of the last tap read 256 rows from (R - 1) dil_h pitch
+            // on: the A region covers them (rows past the box are junk that
+            // feeds only masked output rows)
+            const int64_t span = ((R - 1) * dil_h * pitch + 2 * kBlockM) * 128;
+            a_region = static_cast<uint32_t>(round_up(box > span ? box : span, 1024));
+            stage = a_region + static_cast<uint32_t>(R * pl.pub.block_n * 128);
+            stages = (smem_optin - 1024 - 256 - 64 - 4) / stage;
+            if (stages > kMaxStages) stages = kMaxStages;
+            halo = stages >= 2;
+        }
         if (tiles_m <= INT32_MAX / pl.tiles_n) {
             pl.conv_rows = static_cast<int32_t>(T);
             pl.conv_tpi = static_cast<int32_t>(tpi);
@@ -993,6 +1034,19 @@ gemm_status_t conv_plan(int64_t N, int64_t H, int64_t W, int64_t C, int64_t K, i
             pl.pub.num_tiles = static_cast<int32_t>(tiles_m * pl.tiles_n);
             const int64_t units = num_sms;
             pl.pub.grid = static_cast<int32_t>(pl.pub.num_tiles < units ? pl.pub.num_tiles : units);
+            pl.conv_pitch = static_cast<int32_t>(halo ? pitch : Q);
+            pl.pub.conv_pitch = pl.conv_pitch;
+            if (halo) {
+                pl.conv_halo = true;
+                pl.halo_box_bytes = box;
+                pl.halo_a_region = a_region;
+                pl.halo_stage_bytes = stage;
+                pl.k_blocks = static_cast<int32_t>(S * ceil_div(C, 64));
+                pl.pub.k_blocks = pl.k_blocks;
+                pl.pub.block_k = 64;
+                pl.pub.stages = static_cast<int32_t>(stages);
+                pl.smem_bytes = static_cast<size_t>(stages * stage + 1024 + 256);
+            }
         }
     }
     return GEMM_OK;

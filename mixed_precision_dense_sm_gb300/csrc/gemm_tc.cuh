@@ -137,6 +137,18 @@ struct TcParams {
     int32_t conv_rows;
     int32_t conv_tpi;
     uint32_t conv_a_bytes;
+    // conv_tiled == 2 (halo units): a tile's output pixel (p', q) is A row
+    // p' * conv_pitch + q (conv_pitch = Q rounded up to 8; 1: conv_pitch = Q).
+    // Pipeline step kb is filter column s = kb / conv_cblocks and channel
+    // block kb % conv_cblocks: one tiled box of conv_rows + (R - 1) dil_h
+    // image rows x conv_pitch pixels (the halo, conv_a_bytes) and the R
+    // filter taps of that column (R boxes of BN rows); tap r's A is the box
+    // from row r * dil_h * conv_pitch on.  The stage geometry is set at run
+    // time: halo_a_region bytes of A, then R * BN * 128 of B, stage_bytes in all
+    int32_t conv_pitch;
+    int32_t conv_R;
+    uint32_t halo_a_region;
+    uint32_t halo_stage_bytes;
     // LayerNorm after the linear layer (kernels instantiated with EPI ==
     // kEpiLayerNorm): h = round_C(alpha * acc + beta * C + bias) per element;
     // ln_fused (the whole row in one tile): each row is normalised in the
@@ -701,8 +713,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     const int S = p.stages;
+    const bool halo = (p.conv_tiled == 2);
+    const uint32_t stage_bytes = halo ? p.halo_stage_bytes : kStageBytes;
+    const uint32_t a_region = halo ? p.halo_a_region : kATile;
     // [stages][C staging, when C is stored by TMA][barriers]
-    uint8_t* cstage = smem + S * kStageBytes;
+    uint8_t* cstage = smem + S * stage_bytes;
     uint64_t* full = reinterpret_cast<uint64_t*>(cstage + (p.c_tma ? kCStageBytes : 0u));
     uint64_t* empty = full + S;
     uint64_t* acc_full = empty + S;
@@ -795,6 +810,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 auto tile_bytes = [&](uint32_t r) {
                     const int32_t mf = tm * BM + static_cast<int32_t>(r) * kARows;
                     const int32_t nf = tn * BN + static_cast<int32_t>(r * kBRows);
+                    if (halo)
+                        return p.conv_a_bytes +
+                               static_cast<uint32_t>(b_parts(nf)) * p.conv_R * kBRows * 128u;
                     if (p.conv_tiled)
                         return static_cast<uint32_t>(kc) * p.conv_a_bytes +
                                static_cast<uint32_t>(b_parts(nf)) * kBTile;
@@ -834,8 +852,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ok = false;
                         break;
                     }
-                    uint8_t* sa = smem + stage * kStageBytes;
-                    uint8_t* sb = sa + kATile;
+                    uint8_t* sa = smem + stage * stage_bytes;
+                    uint8_t* sb = sa + a_region;
                     const int32_t k0 = kb * kBlockK;
                     if ((p.debug_flags & kDebugSkipFirstLoad) && armed == 0 && blockIdx.x == 0) {
                         // test hook: arm the slot, load nothing into it
@@ -847,7 +865,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                         continue;
                     }
-                    if (p.conv) {
+                    if (halo) {
+                        // filter column s, channel block cb: the halo box, then
+                        // the column's R taps (3-D filter map, one box per tap)
+                        if constexpr (CG == 1) {
+                            mbar_arrive_expect_tx(&full[stage], bytes);
+                            const int32_t sc = kb / p.conv_cblocks;
+                            const int32_t cb0 = (kb - sc * p.conv_cblocks) * kChunkK;
+                            tma_load_4d(sa, &tmA, &full[stage], cb0, cw + sc * p.conv_dil_w, ch, cn,
+                                        pol_a);
+                            if (nb) {
+                                for (int32_t r = 0; r < p.conv_R; ++r)
+                                    tma_load_3d(sb + r * kBRows * 128u, &tmB, &full[stage], cb0,
+                                                r * p.conv_S + sc, n0, pol_b);
+                            }
+                        }
+                    } else if (p.conv) {
                         // chunk j = kb * kc + q: channels c0 .. c0 + 63 of filter
                         // tap (r, s), the channel blocks of one tap back to back
                         uint32_t fb = 0;                       // the even CTA's barrier (pairs)
@@ -986,8 +1019,28 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     }
                     tc_fence_after_sync();
-                    const uint32_t sa = smem_base + stage * kStageBytes;
-                    const uint32_t sb = sa + kATile;
+                    const uint32_t sa = smem_base + stage * stage_bytes;
+                    const uint32_t sb = sa + a_region;
+                    if (halo) {
+                        // tap r of this filter column: A from halo row
+                        // r * dil_h * pitch on (a multiple of 8 rows, so the
+                        // swizzle atoms line up), its own B tile
+                        const uint32_t a_tap = static_cast<uint32_t>(p.conv_dil_h * p.conv_pitch) * 128u;
+                        for (int32_t r = 0; r < p.conv_R; ++r) {
+                            #pragma unroll
+                            for (int kk = 0; kk < 4; ++kk) {
+                                const uint64_t ad = smem_desc_sw128(sa + r * a_tap + kk * 32u, 16u, 1024);
+                                const uint64_t bd =
+                                    smem_desc_sw128(sb + r * kBRows * 128u + kk * 32u, 16u, 1024);
+                                const uint32_t acc = (kb > sg.kb0 || r > 0 || kk > 0) ? 1u : 0u;
+                                if constexpr (ES == 2 && CG == 1) {
+                                    tc_mma_f16(d_tmem, ad, bd, p.idesc, acc);
+                                    if constexpr (MH == 2)
+                                        tc_mma_f16(d_tmem + BN, ad + (kATileBytes >> 4), bd, p.idesc, acc);
+                                }
+                            }
+                        }
+                    } else {
                     #pragma unroll
                     for (int kk = 0; kk < kc * 4; ++kk) {
                         const uint32_t ka = (kk >> 2) * a_cstep + (kk & 3) * a_kstep;
@@ -1003,11 +1056,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                             else tc_mma_f16_pair(d_tmem, ad, bd, p.idesc, acc);
                         }
                         if constexpr (MH == 2) {
-                            // the second half: its A rows, the same B, its accumulator
-                            const uint64_t ad2 = smem_desc_sw128(sa + a_hstep + ka, a_lbo, 1024);
+                            // the second half: its A rows (the descriptor's start
+                            // address, in 16-byte units, moved on by a_hstep: a
+                            // shared-memory offset stays inside the field's 14
+                            // bits), the same B, its accumulator
+                            const uint64_t ad2 = ad + (a_hstep >> 4);
                             if constexpr (ES == 4) tc_mma_tf32(d_tmem + BN, ad2, bd, p.idesc, acc);
                             else tc_mma_f16(d_tmem + BN, ad2, bd, p.idesc, acc);
                         }
+                    }
                     }
                     if constexpr (CG == 1) tc_commit(&empty[stage]);
                     else tc_commit_pair_multicast(&empty[stage], 0x3);
@@ -1056,8 +1113,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int32_t n = tm / p.conv_tpi;
                 const int32_t p0 = (tm - n * p.conv_tpi) * p.conv_rows;
                 const int32_t nrow = p.conv_P - p0 < p.conv_rows ? p.conv_P - p0 : p.conv_rows;
-                row = row_in_tile < nrow * p.conv_Q ? (n * p.conv_P + p0) * p.conv_Q + row_in_tile
-                                                    : p.M;
+                const int32_t pl = row_in_tile / p.conv_pitch;
+                const int32_t q = row_in_tile - pl * p.conv_pitch;
+                row = (pl < nrow && q < p.conv_Q) ? (n * p.conv_P + p0 + pl) * p.conv_Q + q : p.M;
             }
             const int32_t col0 = tn * BN;                           // D' first column
             const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);

@@ -132,12 +132,13 @@ def test_two_k_chunks_per_stage():
     q = p("N", "T", 512, 3072, 4096)                                 # CTA pairs, stream-K
     assert (q["path_name"], q["block_n"], q["block_k"]) == ("tiled_2sm", 256, 128), q
     assert p("N", "T", 100, 100, 128, (DT_F32, DT_F32, DT_F32))["block_k"] == 64   # TF32: 2 x 32
-    # convolutions: two chunks (two im2col boxes, one filter box) when C is a
-    # whole number of 64-channel blocks; 9 taps x 1 block = 9 chunks, 5 stages
-    st, c = lib.conv2d_plan_query(32, 56, 56, 64, 64, 3, 3, (1, 1), (1, 1), (1, 1), 1.0, 256, 256,
+    # strided convolutions (im2col tiles): two chunks (two im2col boxes, one
+    # filter box) when C is a whole number of 64-channel blocks; 9 taps x 1
+    # block = 9 chunks, 5 stages
+    st, c = lib.conv2d_plan_query(32, 112, 112, 64, 64, 3, 3, (1, 1), (2, 2), (1, 1), 1.0, 256, 256,
                                   0.0, 256, (DT_BF16, DT_BF16, DT_BF16))
     assert st == 0 and c["block_k"] == 128 and c["k_blocks"] == 5, c
-    st, c = lib.conv2d_plan_query(8, 20, 20, 96, 64, 3, 3, (1, 1), (1, 1), (1, 1), 1.0, 256, 256,
+    st, c = lib.conv2d_plan_query(8, 40, 40, 96, 64, 3, 3, (1, 1), (2, 2), (1, 1), 1.0, 256, 256,
                                   0.0, 256, (DT_BF16, DT_BF16, DT_BF16))
     assert st == 0 and c["block_k"] == 64 and c["k_blocks"] == 18, c
     # a convolution on single-CTA 256-wide tiles keeps two chunks in two

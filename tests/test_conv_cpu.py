@@ -32,19 +32,25 @@ def test_output_dims_match_the_oracle(orc, geo):
 
 
 def test_plan_is_the_gemm_of_the_convolution():
-    # k_blocks counts pipeline stages: 9 taps x ceil(C / 64) chunks of 64
-    # channels, two chunks per stage when C is a multiple of 64
-    st, p = plan(N=32, H=56, W=56, C=64, K=64)
-    assert st == OK and p["k_blocks"] == 5 and p["block_k"] == 128
-    # whole-row tiles: 32 images x 14 tiles of 4 output rows (4 x 56 <= 256)
-    assert p["conv_rows"] == 4 and p["tiles_m"] == 32 * 14 and p["block_m"] == 256
+    # im2col tiles (stride 2): k_blocks counts pipeline stages, 9 taps x
+    # ceil(C / 64) chunks of 64 channels, two chunks per stage when C is a
+    # multiple of 64
+    st, p = plan(N=32, H=112, W=112, C=64, K=64, stride=(2, 2))
+    assert st == OK and p["k_blocks"] == 5 and p["block_k"] == 128 and p["conv_rows"] == 0
     assert p["swap_ab"] == 0 and p["pack_a"] == 0 and p["pack_b"] == 0
     assert p["a_mn_major"] == 0 and p["b_mn_major"] == 0
+    # halo units (stride 1): one step per filter column and channel block;
+    # 32 images x 14 tiles of 4 output rows (4 x 56 <= 256)
+    st, p = plan(N=32, H=56, W=56, C=64, K=64)
+    assert st == OK and p["k_blocks"] == 3 and p["block_k"] == 64
+    assert p["conv_rows"] == 4 and p["conv_pitch"] == 56 and p["tiles_m"] == 32 * 14
+    assert p["block_m"] == 256 and p["stages"] >= 2
     st, p = plan(N=16, H=64, W=64, C=256, K=256)
     assert st == OK and p["path_name"] == "tiled_2sm" and p["k_blocks"] == 9 * 4 // 2
     st, p = plan(N=2, H=12, W=10, C=72, K=40, R=5, S=5, pad=(2, 2))
-    assert st == OK and p["k_blocks"] == 25 * 2                 # 72 channels: 2 blocks of 64
-    assert p["block_k"] == 64                                   # one chunk per stage
+    assert st == OK and p["conv_pitch"] == 16 and p["k_blocks"] == 5 * 2   # 72 channels: 2 blocks
+    st, p = plan(N=2, H=12, W=10, C=72, K=40, R=5, S=5, pad=(2, 2), stride=(1, 2))
+    assert st == OK and p["k_blocks"] == 25 * 2 and p["block_k"] == 64     # one chunk per stage
     # few output pixels never swap (the im2col load fills the 128-row side);
     # a long reduction then runs stream-K
     st, p = plan(N=1, H=8, W=8, C=512, K=256)
@@ -54,25 +60,33 @@ def test_plan_is_the_gemm_of_the_convolution():
     assert plan(alpha=0.0, X=0, Wt=0, beta=1.0)[1]["path_name"] == "scale"
 
 
-@pytest.mark.parametrize("H,W,stride,R,K,rows", [
-    (56, 56, 1, 3, 64, 4), (28, 28, 1, 3, 128, 7), (14, 14, 1, 3, 64, 14), (9, 300, 1, 3, 64, 0),
-    (56, 56, 2, 3, 64, 0), (64, 64, 1, 3, 256, 0), (17, 17, 1, 1, 96, 9), (40, 50, 1, 5, 64, 5)])
-def test_whole_row_tiles(H, W, stride, R, K, rows):
+@pytest.mark.parametrize("H,W,stride,R,K,rows,pitch,halo", [
+    (56, 56, 1, 3, 64, 4, 56, True), (28, 28, 1, 3, 128, 7, 32, True),
+    (14, 14, 1, 3, 64, 14, 16, True), (9, 300, 1, 3, 64, 0, 0, False),
+    (56, 56, 2, 3, 64, 0, 0, False), (64, 64, 1, 3, 256, 0, 0, False),
+    (17, 17, 1, 1, 96, 9, 24, True), (40, 50, 1, 5, 64, 4, 56, True),
+    (8, 250, 1, 3, 64, 1, 250, False)])
+def test_whole_row_tiles(H, W, stride, R, K, rows, pitch, halo):
     """Stride-1 convolutions on 256-row single-CTA tiles (at most 128 output
-    channels) tile each image by whole output rows, T Q <= 256, the rows split
-    evenly: tiles per image = ceil(P / floor(256 / Q)), T = ceil(P / that).
-    Strided layers, rows wider than 256 pixels and CTA-pair tiles keep the
-    im2col tiles (conv_rows 0)."""
+    channels) tile each image by whole output rows at a pitch of A rows per
+    output row, T pitch <= 256, the rows split evenly: tiles per image =
+    ceil(P / floor(256 / pitch)), T = ceil(P / that).  Halo units (pitch = Q
+    rounded up to 8) take one step per filter column and channel block; where
+    their stages do not fit two to shared memory (250-pixel rows) each tap
+    loads its own box (pitch = Q, one step per tap).  Strided layers, rows
+    wider than 256 pixels and CTA-pair tiles keep the im2col tiles."""
     pad = (R // 2, R // 2)
     st, p = plan(N=3, H=H, W=W, C=64, K=K, R=R, S=R, pad=pad, stride=(stride, stride))
-    assert st == OK and p["conv_rows"] == rows, p
+    assert st == OK and p["conv_rows"] == rows and p["conv_pitch"] == pitch, p
     if rows:
         P = (H + 2 * pad[0] - R) // stride + 1
         Q = (W + 2 * pad[1] - R) // stride + 1
         tpi = p["tiles_m"] // 3
-        assert p["tiles_m"] == 3 * tpi and tpi == -(-P // (256 // Q))
-        assert rows == -(-P // tpi) and rows * Q <= 256 and (tpi - 1) * rows < P
+        assert p["tiles_m"] == 3 * tpi and tpi == -(-P // (256 // pitch))
+        assert rows == -(-P // tpi) and rows * pitch <= 256 and (tpi - 1) * rows < P
         assert p["block_m"] == 256 and p["path_name"] == "tiled_1sm" and p["sk_len"] == 0
+        assert pitch == (-(-Q // 8) * 8 if halo else Q)
+        assert p["k_blocks"] == (R if halo else -(-R * R // 2)), p
 
 
 def test_argument_checks():

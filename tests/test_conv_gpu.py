@@ -111,24 +111,33 @@ def test_geometries_integer_exact(g, orc, geo):
 
 
 WHOLE_ROWS = [
-    # N, H, W, C, K, R, S, pad, stride, dilation
-    (3, 23, 21, 64, 64, 3, 3, (1, 1), (1, 1), (1, 1)),      # 12 rows per tile, the last 11
-    (2, 30, 40, 24, 40, 3, 3, (2, 2), (1, 1), (2, 2)),      # dilation 2, 24 channels (one chunk)
-    (2, 9, 130, 64, 128, 3, 5, (1, 2), (1, 1), (1, 1)),     # 130-pixel rows: one row per tile
-    (1, 33, 33, 128, 96, 1, 1, (0, 0), (1, 1), (1, 1)),     # 1 x 1: 7 rows per tile, the last 5
+    # N, H, W, C, K, R, S, pad, stride, dilation; halo units?
+    ((3, 23, 21, 64, 64, 3, 3, (1, 1), (1, 1), (1, 1)), True),    # 8 rows per tile, the last 7
+    ((2, 30, 40, 24, 40, 3, 3, (2, 2), (1, 1), (2, 2)), True),    # dilation 2, 24 channels
+    ((2, 9, 130, 64, 128, 3, 5, (1, 2), (1, 1), (1, 1)), False),  # 130-pixel rows: a box per tap
+    ((1, 33, 33, 128, 96, 1, 1, (0, 0), (1, 1), (1, 1)), True),   # 1 x 1: 6 rows, the last 3
+    ((2, 20, 19, 16, 32, 7, 7, (3, 3), (1, 1), (1, 1)), True),    # 7 x 7: 16-row halo boxes
+    ((2, 15, 26, 40, 48, 3, 3, (2, 1), (1, 1), (2, 1)), True),    # dilation (2, 1), pitch 32
+    ((2, 22, 9, 136, 72, 3, 3, (0, 1), (1, 1), (1, 1)), True),    # 3 channel blocks, no row pad
 ]
 
 
-@pytest.mark.parametrize("geo", WHOLE_ROWS, ids=[f"r{i}" for i in range(len(WHOLE_ROWS))])
-def test_whole_row_tiles(g, orc, geo):
+@pytest.mark.parametrize("case", WHOLE_ROWS, ids=[f"r{i}" for i in range(len(WHOLE_ROWS))])
+def test_whole_row_tiles(g, orc, case):
     """Stride-1 layers with at most 128 output channels run whole-row tiles:
-    each tap's A tile is one tiled box of the input (T output rows x Q
-    pixels, zeros outside the image), masked past the image's last row.
-    Integer inputs bit-exact, then random inputs with a 16-bit output."""
+    halo units (one tiled box of the input per filter column and channel
+    block, the column's taps read at row offsets of it, rows at a pitch of Q
+    rounded up to 8) or, where those stages do not fit, one box per tap
+    (T output rows x Q pixels); zeros outside the image, rows past the
+    image's last row and pitch columns past Q masked.  Integer inputs
+    bit-exact, then random inputs with a 16-bit output."""
     import mixed_precision_dense_sm_gb300 as lib
+    geo, halo = case
     st, p = lib.conv2d_plan_query(*geo, 1.0, 256, 256, 0.0, 1 << 44, (DT_BF16, DT_BF16, DT_F32),
                                   num_sms=torch.cuda.get_device_properties(0).multi_processor_count)
     assert st == 0 and p["conv_rows"] > 0, p
+    C, S = geo[3], geo[6]
+    assert (p["k_blocks"] == S * -(-C // 64)) == halo, p
     run_and_check(g, orc, geo, dt=DT_BF16, ydt=DT_F32, seed=sum(geo[:7]))
     run_and_check(g, orc, geo, dt=DT_F16, ydt=DT_BF16, integer=False, beta=0.5, seed=3)
 
