@@ -19,7 +19,10 @@
  *   - Arithmetic is FP32 whatever the storage type (the CATLASS page, section
  *     3.4, keeps reductions such as softmax in FP32 with 16-bit data paths);
  *     exp is the fast hardware exponential (__expf, as on the SGEMM page,
- *     section 2.5); y is rounded once to its type, round to nearest even.
+ *     section 2.5; staged rows of 16-bit inputs take 2^(t log2 e) from the
+ *     hardware base-2 exponential, with results below 2^-126 flushed to
+ *     zero: the same error form); y is rounded once to its type, round to
+ *     nearest even.
  *   - Special values follow the formula: a row containing NaN or +inf, and a
  *     fully masked row (every entry -inf, 0/0 -- section 2.5), give NaN in
  *     every position; otherwise an entry of -inf gives exactly 0.
@@ -31,9 +34,9 @@
  * (same pointer, same leading dimension, same type: in place); any other
  * overlap of the two is rejected.
  *
- * Rows of 256 bytes to 64 KB (and at most 16384 elements) that start on
- * 16-byte boundaries are staged in shared memory by bulk copies (TMA): one
- * CTA of 16 warps per SM, split into
+ * Rows of 256 bytes to 64 KB (at most 16384 FP32 or 32768 16-bit elements)
+ * that start on 16-byte boundaries are staged in shared memory by bulk
+ * copies (TMA): one CTA of 16 warps per SM, split into
  * groups of 1-16 warps, each group a pipeline that keeps the copies of its
  * next few rows in flight while it works on one (~130-190 KB per SM in all),
  * so HBM is streamed without registers holding the loads.  Other rows are

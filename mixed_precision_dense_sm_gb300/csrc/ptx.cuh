@@ -78,14 +78,18 @@ __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Wait until the phase with the given parity has completed.  Bounded: returns
-// false after limit_ns instead of spinning forever.
+// false once limit_ns have passed since the 64th unsuccessful try (the clock
+// is read only every 64 tries, so short waits never read it).
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
     const uint32_t a = smem_addr(bar);
-    if (mbar_try_wait(a, parity)) return true;
-    const uint64_t t0 = global_timer_ns();
+    uint64_t t0 = 0;
     for (uint32_t i = 1;; ++i) {
         if (mbar_try_wait(a, parity)) return true;
-        if ((i & 255u) == 0 && global_timer_ns() - t0 > limit_ns) return false;
+        if ((i & 63u) == 0) {
+            const uint64_t now = global_timer_ns();
+            if (i == 64u) t0 = now;
+            else if (now - t0 > limit_ns) return false;
+        }
     }
 }
 

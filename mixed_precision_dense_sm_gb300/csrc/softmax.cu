@@ -30,8 +30,8 @@ constexpr int64_t kCtaSmallCols = 256 * smx::kE;        // 8192: 256-thread CTAs
 constexpr int64_t kCtaMaxCols = 512 * smx::kE;          // 16384 per CTA
 constexpr int64_t kMaxCols = int64_t(1) << 30;
 // Rows staged in shared memory by bulk copies: 256 B to 64 KB and at most
-// 16 warps x 32 x kTmaMaxElems elements, one row per group of warps at a time
-// (the group holds its row in registers, at most kTmaMaxElems elements per
+// 16 warps x 32 x kTmaMaxVec 16-byte vectors, one row per group of warps at a
+// time (the group holds its row in registers, at most kTmaMaxVec vectors per
 // thread), slots within this budget.
 constexpr int64_t kStagedMinBytes = 256;
 constexpr int64_t kStagedMaxBytes = 64 * 1024;
@@ -100,7 +100,7 @@ gemm_status_t make_plan(int64_t rows, int64_t cols, const void* X, int64_t ldx, 
     pl.pub.vec = (aligned_to(X, 16) && aligned_to(Y, 16) && (ldx * ex) % 16 == 0 &&
                   (ldy * ey) % 16 == 0) ? 1 : 0;
     const int64_t row_bytes = cols * ex;
-    const int64_t kvmax = smx::kTmaMaxElems / (16 / ex);     // vectors per thread
+    const int64_t kvmax = smx::kTmaMaxVec;                   // vectors per thread
     const int64_t max_vec = smx::kTmaComputeWarps * 32 * kvmax;
     // a row fits one CTA's slots and registers
     const int64_t b = cols * ex;

@@ -3,15 +3,16 @@
 // aligned.
 //
 // One CTA per SM: 16 compute warps in groups of `group_warps` warps (1 to 16,
-// sized so that a row fits in the group's registers at <= 32 elements per
-// thread) and one producer warp.  Each group owns a ring of `depth` row slots,
-// each slot with a "full" mbarrier (the bulk copy's bytes) and an "empty" one
-// (one arrival per warp of the group once it has read the slot).  The
-// producer's first thread keeps every group's ring filled: it polls the empty
-// barriers of all groups in turn and refills a slot as soon as its group has
-// read it, so a group waits on a barrier only when its own data is late, and
-// no barrier ties the warps of a group together between units.  An SM keeps
-// ~130-190 KB of loads in flight without registers holding them.
+// sized so that a row fits in the group's registers at <= 8 16-byte vectors
+// per thread: 32 FP32 or 64 16-bit elements) and one producer warp.  Each
+// group owns a ring of `depth` row slots, each slot with a "full" mbarrier
+// (the bulk copy's bytes) and an "empty" one (one arrival per warp of the
+// group once it has read the slot).  The producer's first thread keeps the
+// rings filled: the groups take equal rows at the same pace, so it refills in
+// one fixed order (unit i of every group, then unit i + 1), waiting on each
+// slot's empty barrier in turn, and no barrier ties the warps of a group
+// together between units.  An SM keeps ~130-190 KB of loads in flight
+// without registers holding them.
 //
 // A row is moved from its slot into registers once, as FP32; the slot is
 // released right then; the maximum (NaN-propagating), e = exp(x - m) with its
@@ -25,8 +26,8 @@
 // from global memory directly.
 //
 // Every wait is bounded; a wait that runs out sets the error word.  Compute
-// warps that give up leave their loop; the producer stops refilling a group
-// whose slots stay unread past the limit and, before the CTA exits, waits
+// warps that give up leave their loop; the producer stops refilling once a
+// slot stays unread past the limit and, before the CTA exits, waits
 // (bounded) for every copy it issued to land.
 #pragma once
 #include <cstdint>
@@ -41,7 +42,8 @@ constexpr int kTmaComputeWarps = 16;
 constexpr int kTmaThreads = (kTmaComputeWarps + 1) * 32;    // + the producer warp
 constexpr int kTmaMaxDepth = 8;
 constexpr int kTmaMaxGroups = kTmaComputeWarps;
-constexpr int kTmaMaxElems = 32;         // row elements per thread (held as FP32)
+constexpr int kTmaMaxVec = 8;           // 16-byte row vectors per thread: 32 FP32 or 64 16-bit
+                                         // elements, held as FP32
 constexpr uint32_t kSmxDebugSkipFirstLoad = 1u;
 
 struct TmaSoftmaxParams {
@@ -161,6 +163,23 @@ __device__ __forceinline__ void store_vec16(OutT* dst, const float (&o)[VecOf<In
     }
 }
 
+// e^t per element.  Rows of 16-bit inputs use the identity e^t = 2^(t log2 e):
+// the product rounded once to FP32, then the hardware base-2 exponential
+// (PTX ex2.approx.ftz.f32), so the error is the exponential's own plus
+// |t| 2^-24 relative from the product -- the same form as the bound of
+// __expf, which rows of FP32 inputs keep (measured faster on them).
+// Results below 2^-126 flush to zero.
+template <typename InT>
+__device__ __forceinline__ float exp_elem(float t) {
+    if constexpr (sizeof(InT) == 2) {
+        float r;
+        asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(t * 1.4426950408889634f));
+        return r;
+    } else {
+        return __expf(t);
+    }
+}
+
 // Arm `bar` for the rows of unit u and issue their copies: one copy when the
 // rows are adjacent in X, else one per row (unless the test hook says not to).
 template <typename InT>
@@ -242,12 +261,12 @@ __device__ __forceinline__ bool finish_row(float (&x)[KV][VecOf<InT>::V], float 
     for (int k = 0; k < KV; ++k) {
         #pragma unroll
         for (int e = 0; e < V; ++e) {
-            x[k][e] = __expf(x[k][e] - mz);
+            x[k][e] = exp_elem<InT>(x[k][e] - mz);
             s += x[k][e];
         }
     }
     if (!WHOLE) {
-        xt = __expf(xt - mz);
+        xt = exp_elem<InT>(xt - mz);
         if (bulk_elems + t < cols) s += xt;
     }
     s = warp_sum(s);
@@ -344,9 +363,13 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
         if (lane != 0) return;
         const uint64_t policy = gemm103::l2_policy_evict_first();
         const bool skip_first = (p.debug_flags & kSmxDebugSkipFirstLoad) && blockIdx.x == 0;
-        int64_t issued[kTmaMaxGroups];
-        for (int g = 0; g < NG; ++g) issued[g] = 0;
-        uint32_t dead = 0;                // groups no longer refilled (their slots timed out)
+        // Every group's i-th unit goes to its slot i % D, and the groups
+        // consume at the same pace (equal rows), so the refills run in one
+        // fixed order -- unit i of group 0, 1, ..., NG - 1, then unit i + 1 --
+        // each waiting (bounded, the thread suspended in the barrier's
+        // try_wait) for its slot's "empty" phase.  The loop's state is a few
+        // scalars: no per-group tables to reload on every poll.
+        int64_t issued[kTmaMaxGroups];    // per group; read only at the end
         // every slot starts free: the first D units of each group at once
         for (int g = 0; g < NG; ++g) {
             const int64_t n = units_of(g);
@@ -357,31 +380,29 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
                                 skip_first && g == 0 && i == 0);
             issued[g] = n < D ? n : D;
         }
-        uint64_t t0 = gemm103::global_timer_ns();
-        for (;;) {
-            bool pending = false, progress = false;
+        int d = 0;                        // slot of unit i; unit i - D's "empty" parity
+        uint32_t par = 0;
+        bool alive = true;
+        for (int64_t i = D; alive; ++i) {
+            bool any = false;
             for (int g = 0; g < NG; ++g) {
-                const int64_t i = issued[g];
-                if (i >= units_of(g) || ((dead >> g) & 1u)) continue;
-                pending = true;
-                const int d = static_cast<int>(i % D);
-                // unit i - D, the slot's previous contents, has been read
-                const uint32_t par = static_cast<uint32_t>((i / D - 1) & 1);
-                if (!gemm103::mbar_test_wait(gemm103::smem_addr(&empty[g * D + d]), par)) continue;
-                const int64_t u0 = static_cast<int64_t>(blockIdx.x) * NG + g;
-                issue_unit<InT>(p, X, slots + (static_cast<size_t>(g) * D + d) * p.slot_bytes,
-                                u0 + i * stride, &full[g * D + d], policy, false);
+                const int64_t u = static_cast<int64_t>(blockIdx.x) * NG + g + i * stride;
+                if (u >= units) break;    // nor for the groups after g
+                any = true;
+                if (!gemm103::mbar_wait(&empty[g * D + d], par, p.wait_limit_ns)) {
+                    // the slot was never read: the consumers gave up
+                    atomicExch(p.err, 1);
+                    alive = false;
+                    break;
+                }
+                issue_unit<InT>(p, X, slots + (static_cast<size_t>(g) * D + d) * p.slot_bytes, u,
+                                &full[g * D + d], policy, false);
                 issued[g] = i + 1;
-                progress = true;
             }
-            if (!pending) break;
-            const uint64_t now = gemm103::global_timer_ns();
-            if (progress) {
-                t0 = now;
-            } else if (now - t0 > p.wait_limit_ns) {
-                // no slot freed within the limit: the consumers gave up
-                atomicExch(p.err, 1);
-                for (int g = 0; g < NG; ++g) dead |= 1u << g;
+            if (!any) break;
+            if (++d == D) {
+                d = 0;
+                par ^= 1u;
             }
         }
         // every copy issued lands before the CTA (and its shared memory) goes
@@ -403,9 +424,14 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
     uint64_t* pf = full + group * D;
     uint64_t* pe = empty + group * D;
     const uint8_t* ps = slots + static_cast<size_t>(group) * D * p.slot_bytes;
+    int d = 0;                                   // slot of unit i, and its "full" parity
+    uint32_t par = 0;
     for (int64_t i = 0; i < n; ++i) {
-        const int d = static_cast<int>(i % D);
-        bool ok = gemm103::mbar_wait(&pf[d], static_cast<uint32_t>((i / D) & 1), p.wait_limit_ns);
+        if (i > 0 && ++d == D) {
+            d = 0;
+            par ^= 1u;
+        }
+        bool ok = gemm103::mbar_wait(&pf[d], par, p.wait_limit_ns);
         const int64_t first = (u0 + i * stride) * p.unit_rows;
         const uint8_t* sunit = ps + static_cast<size_t>(d) * p.slot_bytes;
         float x[KV][V];
@@ -489,15 +515,11 @@ cudaError_t launch_softmax_tma_w(const TmaSoftmaxParams& p, int grid, size_t sme
 template <typename InT, typename OutT>
 cudaError_t launch_softmax_tma(const TmaSoftmaxParams& p, int grid, size_t smem,
                                cudaStream_t stream) {
-    constexpr int kMaxKV = kTmaMaxElems / VecOf<InT>::V;
     switch (p.kv) {
         case 1: return launch_softmax_tma_w<InT, OutT, 1>(p, grid, smem, stream);
         case 2: return launch_softmax_tma_w<InT, OutT, 2>(p, grid, smem, stream);
         case 4: return launch_softmax_tma_w<InT, OutT, 4>(p, grid, smem, stream);
-        case 8:
-            if constexpr (kMaxKV >= 8)
-                return launch_softmax_tma_w<InT, OutT, 8>(p, grid, smem, stream);
-            return cudaErrorInvalidValue;
+        case 8: return launch_softmax_tma_w<InT, OutT, 8>(p, grid, smem, stream);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -80,23 +80,25 @@ def test_work_split(cols, mode, threads, cluster):
     (4096, DT_F32, 4096, 1, 8, 1, 6, 4), (8192, DT_F32, 8192, 1, 16, 1, 6, 4),
     (16384, DT_F32, 16384, 1, 16, 1, 3, 8), (16384, DT_BF16, 16384, 1, 16, 1, 6, 4),
     (3000, DT_F16, 3000, 1, 4, 1, 8, 4), (8192, DT_BF16, 8192, 1, 8, 1, 6, 4),
-    (2048, DT_BF16, 2048, 1, 2, 1, 6, 4),
+    (2048, DT_BF16, 2048, 1, 8, 8, 3, 8), (1536, DT_F16, 1536, 1, 8, 8, 4, 8),
+    (32768, DT_F16, 32768, 1, 16, 1, 3, 8), (20000, DT_BF16, 20000, 1, 16, 1, 5, 8),
     # not staged: too long for one CTA (two passes; a cluster of 2 for rows
     # whose 152 resident slices exceed 64 MB), too short, or rows not 16-byte
     # aligned
-    (16388, DT_F32, 16388, 1, 0, 0, 0, 0), (32768, DT_F16, 32768, 1, 0, 0, 0, 0),
+    (16388, DT_F32, 16388, 1, 0, 0, 0, 0), (32776, DT_F16, 32776, 1, 0, 0, 0, 0),
     (65536, DT_F32, 65536, 1, 0, 0, 0, 0), (131072, DT_F32, 131072, 2, 0, 0, 0, 0),
-    (20000, DT_BF16, 20000, 1, 0, 0, 0, 0), (131080, DT_F32, 131080, 2, 0, 0, 0, 0),
+    (131080, DT_F32, 131080, 2, 0, 0, 0, 0),
     (60, DT_F32, 60, 1, 0, 0, 0, 0), (120, DT_BF16, 120, 1, 0, 0, 0, 0),
     (16385, DT_F32, 16385, 1, 0, 0, 0, 0)])
 def test_staged_split(cols, dt, ld, cl, gw, unit, depth, kv):
-    """16-byte-aligned rows of 256 B to 64 KB (<= 16384 elements) are staged
-    in shared memory by bulk copies: one CTA of 16 compute warps and a
-    producer warp per SM.  Rows a warp can hold (<= 1024 elements) go to
-    groups of 8 warps whose slots carry several rows (~16 KB, one copy when
-    the rows are adjacent), a warp per row; longer rows are shared by the
-    smallest group that holds them in registers (<= 32 elements per thread),
-    doubled while a group would get fewer than six slots.  Each group is a
+    """16-byte-aligned rows of 256 B to 64 KB and at most 16 x 32 x 8
+    16-byte vectors (16384 FP32 or 32768 16-bit elements) are staged in
+    shared memory by bulk copies: one CTA of 16 compute warps and a producer
+    warp per SM.  Rows a warp can hold (<= 8 vectors per thread: 256 FP32 or
+    2048 16-bit elements) go to groups of 8 warps whose slots carry several
+    rows (~16 KB, one copy when the rows are adjacent), a warp per row;
+    longer rows are shared by the smallest group that holds them in
+    registers, doubled while a group would get fewer than six slots.  Each group is a
     pipeline with as many slots as 200 KB allow (at most 8).  Other rows keep
     the register kernels (depth 0)."""
     st, p = plan(100000, cols, ldx=ld, ldy=ld, xdt=dt, ydt=dt)
@@ -104,7 +106,7 @@ def test_staged_split(cols, dt, ld, cl, gw, unit, depth, kv):
     got = (p["cluster"], p["group_warps"], p["unit_rows"], p["depth"], p["kv"])
     assert got == (cl, gw, unit, depth, kv), p
     es = 4 if dt == DT_F32 else 2
-    kvmax = 32 * es // 16                   # 32 elements per thread
+    kvmax = 8                               # 16-byte vectors per thread
     if depth:
         assert p["vec"] == 1 and p["threads"] == 544          # 16 compute warps + the producer
         assert p["grid"] == (152 if cl == 1 else cl * (152 // cl))

@@ -111,12 +111,13 @@ def test_every_type_pair(lib, orc, cols):
         check(orc, Xs, cols, xdt, ydt, Y)
 
 
-@pytest.mark.parametrize("cols,gw,unit", [(1024, 8, 8), (1001, 8, 8), (2048, 2, 1), (4096, 4, 1),
-                                          (6001, 8, 1), (8192, 8, 1), (16000, 16, 1),
-                                          (16384, 16, 1)])
+@pytest.mark.parametrize("cols,gw,unit", [(1024, 8, 8), (1001, 8, 8), (2048, 8, 8), (1536, 8, 8),
+                                          (4096, 4, 1), (6001, 8, 1), (8192, 8, 1), (16000, 16, 1),
+                                          (16384, 16, 1), (20000, 16, 1), (32768, 16, 1)])
 def test_staged_16bit_splits(lib, orc, cols, gw, unit):
-    """16-bit rows in the staged kernel: a warp per row up to 1024 elements,
-    else groups of 2-16 warps that merge their warps' (max, sum) pairs;
+    """16-bit rows in the staged kernel: a warp per row up to 2048 elements
+    (64 per lane), else groups of 4-16 warps that merge their warps' (max,
+    sum) pairs;
     whole rows, rows whose vectors do not fill every thread and rows with a
     tail past the last 16-byte vector; FP16 and BF16 inputs with 16-bit and
     FP32 outputs; fully and half masked rows; more rows than slots."""
