@@ -58,6 +58,7 @@ struct Plan {
     int32_t row_stride;   // staged path: bytes between rows inside a slot
     int32_t contiguous;   // staged path: a slot's rows are adjacent in X (one copy)
     bool whole;           // staged path: rows fill the threads' vectors exactly, no tail
+    bool long_rows;       // staged path: rows streamed twice in chunks
 };
 
 gemm_status_t check(int64_t rows, int64_t cols, const void* X, int64_t ldx, int32_t xdt,
@@ -179,6 +180,25 @@ gemm_status_t make_plan(int64_t rows, int64_t cols, const void* X, int64_t ldx, 
             while (cl < smx::kMaxCluster &&
                    static_cast<int64_t>(num_sms) * ceil_div(cols, cl) * ex > kTwoPassL2Budget)
                 cl *= 2;
+        }
+        if (pl.pub.vec && cl == 1 && cols > kCtaMaxCols) {
+            // 16-byte aligned rows too long to stage whole, whose slices on
+            // every SM fit the L2 budget: streamed twice through shared
+            // memory in chunks by bulk copies (softmax_long_kernel)
+            pl.pub.mode = SOFTMAX_MODE_STREAM;
+            pl.pub.threads = smx::kTmaThreads;
+            pl.pub.slice = static_cast<int32_t>(round_up(cols, 8));
+            pl.pub.depth = smx::kLongDepth;
+            pl.pub.group_warps = smx::kTmaComputeWarps;
+            pl.pub.unit_rows = 1;
+            pl.pub.kv = smx::kLongKV;
+            pl.long_rows = true;
+            pl.resident = false;
+            pl.smem = static_cast<size_t>(1024 + smx::kLongDepth * smx::kLongChunkBytes);
+            pl.bulk_elems = static_cast<int32_t>((row_bytes / 16) * 16 / ex);
+            pl.pub.grid = static_cast<int32_t>(rows < num_sms ? rows : num_sms);
+            pl.pub.hbm_bytes = rows * cols * (2 * ex + ey);
+            return GEMM_OK;
         }
         const int64_t slice = round_up(ceil_div(cols, cl), 8);
         pl.resident = slice <= static_cast<int64_t>(threads) * smx::kE;
@@ -344,6 +364,7 @@ gemm_status_t softmax_rows(int64_t rows, int64_t cols, const void* X, int64_t ld
         q.contiguous = pl.contiguous;
         q.kv = pl.pub.kv;
         q.whole = pl.whole ? 1 : 0;
+        q.long_rows = pl.long_rows ? 1 : 0;
         q.err = err;
         {
             std::lock_guard<std::mutex> g(g_dbg_mu);

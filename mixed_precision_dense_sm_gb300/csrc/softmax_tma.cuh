@@ -62,6 +62,7 @@ struct TmaSoftmaxParams {
     int32_t contiguous;     // 1: a slot's rows are adjacent in X, one copy moves them all
     int32_t kv;             // 16-byte vectors per thread: 1, 2, 4 (or 8 for FP32 input)
     int32_t whole;          // 1: bulk_elems == cols and every thread holds kv vectors
+    int32_t long_rows;      // 1: rows streamed twice in chunks (softmax_long_kernel)
     int* err;               // device error word (1: a wait ran out)
     uint64_t wait_limit_ns;
     uint32_t debug_flags;
@@ -477,6 +478,268 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
     }
 }
 
+// ------------------------------------------------------------ long rows
+// Rows longer than the staged kernel holds (more than 64 KB or more vectors
+// than its threads keep), 16-byte aligned, whose slices on all SMs fit the
+// L2 budget: one CTA of 16 compute warps and a producer warp per SM takes
+// rows in turn and streams each twice through a ring of kLongDepth slots of
+// kLongChunkBytes -- the two-pass scheme of the SGEMM tutorial page, section
+// 2.2, with the loads moved by bulk copies instead of registers.  Pass 1
+// folds the row chunk by chunk into per-thread (m, s) by the online rule
+// (m' = max(m, c), s' = s e^(m - m') + sum e^(x - m') over the chunk), and
+// the CTA merges its 512 pairs (warp butterflies, then the 16 warps' pairs
+// in one fixed order, so every thread holds the same (M, S)).  Pass 2 reads
+// the chunks again -- from L2: pass 1's copies are evict-normal, pass 2's
+// evict-first -- and writes y = e^(x - M) / S.
+constexpr int kLongKV = 4;                                          // vectors per thread per chunk
+constexpr int kLongChunkBytes = kTmaComputeWarps * 32 * kLongKV * 16;  // 32 KB
+constexpr int kLongDepth = 6;
+
+// Bounded wait that also gives up once another thread of the CTA has set
+// `abort` (the clock is read every 64 tries).
+__device__ __forceinline__ bool wait_full(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                          uint64_t limit_ns) {
+    const uint32_t a = gemm103::smem_addr(bar);
+    uint64_t t0 = 0;
+    for (uint32_t i = 1;; ++i) {
+        if (gemm103::mbar_try_wait(a, parity)) return true;
+        if ((i & 63u) == 0) {
+            if (*abort) return false;
+            const uint64_t now = gemm103::global_timer_ns();
+            if (i == 64u) t0 = now;
+            else if (now - t0 > limit_ns) return false;
+        }
+    }
+}
+
+template <typename InT, typename OutT>
+__global__ void __launch_bounds__(kTmaThreads, 1)
+    softmax_long_kernel(const __grid_constant__ TmaSoftmaxParams p) {
+    constexpr int V = VecOf<InT>::V;
+    constexpr int T = kTmaComputeWarps * 32;                 // compute threads
+    constexpr int D = kLongDepth;
+    constexpr int32_t kChunkElems = kLongChunkBytes / static_cast<int>(sizeof(InT));
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    __shared__ float red_m[2][kTmaComputeWarps], red_s[2][kTmaComputeWarps];
+    __shared__ int abort_flag;
+    const InT* __restrict__ X = static_cast<const InT*>(p.X);
+    OutT* __restrict__ Y = static_cast<OutT*>(p.Y);
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem_raw);
+    uint64_t* empty = full + D;
+    uint8_t* slots = smem_raw + 1024;
+    const int32_t C = (p.bulk_elems + kChunkElems - 1) / kChunkElems;   // chunks per row
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < D; ++i) {
+            gemm103::mbar_init(&full[i], 1);
+            gemm103::mbar_init(&empty[i], kTmaComputeWarps);
+        }
+        abort_flag = 0;
+        gemm103::fence_barrier_init();
+    }
+    __syncthreads();
+    gemm103::grid_dependency_wait();      // inputs of the previous kernel are visible
+
+    if (warp == kTmaComputeWarps) {
+        // ------------------------------------------------------- producer
+        // unit i of this CTA: row blockIdx.x + (i / 2C) gridDim.x, pass
+        // (i % 2C) / C, chunk (i % 2C) % C; slot i % D
+        if (lane != 0) return;
+        const uint64_t keep = gemm103::l2_policy_evict_normal();
+        const uint64_t last = gemm103::l2_policy_evict_first();
+        const bool skip_first = (p.debug_flags & kSmxDebugSkipFirstLoad) && blockIdx.x == 0;
+        int64_t issued = 0;
+        int d = 0;
+        uint32_t round = 0;               // times slot 0 has been reached
+        for (int64_t row = blockIdx.x; row < p.rows; row += gridDim.x) {
+            bool ok = true;
+            for (int32_t j = 0; j < 2 * C; ++j) {
+                if (round > 0 &&
+                    !wait_full(&empty[d], (round - 1) & 1u, &abort_flag, p.wait_limit_ns)) {
+                    ok = false;
+                    break;
+                }
+                const int32_t c = j < C ? j : j - C;
+                const int32_t e0 = c * kChunkElems;
+                const int32_t n = p.bulk_elems - e0 < kChunkElems ? p.bulk_elems - e0 : kChunkElems;
+                const uint32_t bytes = static_cast<uint32_t>(n) * sizeof(InT);
+                gemm103::mbar_arrive_expect_tx(&full[d], bytes);
+                if (!(skip_first && issued == 0))
+                    gemm103::bulk_load_1d(slots + static_cast<size_t>(d) * kLongChunkBytes,
+                                          X + row * p.ldx + e0, bytes, &full[d], j < C ? keep : last);
+                ++issued;
+                if (++d == D) {
+                    d = 0;
+                    ++round;
+                }
+            }
+            if (!ok) {
+                atomicExch(p.err, 1);
+                abort_flag = 1;
+                break;
+            }
+        }
+        // every copy issued lands before the CTA (and its shared memory) goes
+        for (int64_t i = issued > D ? issued - D : 0; i < issued; ++i)
+            gemm103::mbar_wait(&full[static_cast<int>(i % D)], static_cast<uint32_t>((i / D) & 1),
+                               p.wait_limit_ns);
+        return;
+    }
+
+    // ------------------------------------------------------------ compute
+    const int t = threadIdx.x;
+    const int32_t tail = p.cols - p.bulk_elems;               // < V elements past the copies
+    int d = 0;
+    uint32_t round = 0;
+    bool ok = true;
+    int parity_buf = 0;
+    // wait for slot d's data; a wait that runs out tells every other waiter
+    // of the CTA (and the producer) to give up too
+    auto take = [&](int dd, uint32_t rr) {
+        if (!ok) return;
+        ok = wait_full(&full[dd], rr & 1u, &abort_flag, p.wait_limit_ns);
+        if (!ok) abort_flag = 1;
+    };
+    // the warp has read slot dd: one arrival, and only when every lane got
+    // its data (a slot whose copy never landed is never refilled)
+    auto release = [&](int dd) {
+        const bool wok = __all_sync(0xffffffffu, ok) != 0;
+        if (lane == 0 && wok) gemm103::mbar_arrive(&empty[dd]);
+    };
+    for (int64_t row = blockIdx.x; row < p.rows; row += gridDim.x) {
+        const InT* __restrict__ xrow = X + row * p.ldx;
+        OutT* __restrict__ yrow = Y + row * p.ldy;
+        // pass 1: (m, s) of this thread's elements, chunk by chunk
+        float m = -INFINITY, s = 0.0f;
+        for (int32_t c = 0; c < C; ++c) {
+            take(d, round);
+            const int32_t nv = (p.bulk_elems - c * kChunkElems < kChunkElems
+                                    ? p.bulk_elems - c * kChunkElems : kChunkElems) / V;
+            const uint8_t* slot = slots + static_cast<size_t>(d) * kLongChunkBytes;
+            float x[kLongKV][V];
+            #pragma unroll
+            for (int k = 0; k < kLongKV; ++k) {
+                const int32_t v = t + k * T;
+                if (v < nv) {
+                    unpack16<InT>(*reinterpret_cast<const uint4*>(slot + static_cast<size_t>(v) * 16),
+                                  x[k]);
+                } else {
+                    #pragma unroll
+                    for (int e = 0; e < V; ++e) x[k][e] = -INFINITY;
+                }
+            }
+            release(d);
+            float cm = -INFINITY;
+            #pragma unroll
+            for (int k = 0; k < kLongKV; ++k) {
+                #pragma unroll
+                for (int e = 0; e < V; ++e) cm = fmax_nan(cm, x[k][e]);
+            }
+            const float mm = fmax_nan(m, cm);
+            const float mmz = (mm == -INFINITY) ? 0.0f : mm;
+            float add = 0.0f;
+            #pragma unroll
+            for (int k = 0; k < kLongKV; ++k) {
+                #pragma unroll
+                for (int e = 0; e < V; ++e) add += exp_elem<InT>(x[k][e] - mmz);
+            }
+            s = (m == -INFINITY ? 0.0f : s * __expf(m - mmz)) + add;
+            m = mm;
+            if (++d == D) {
+                d = 0;
+                ++round;
+            }
+        }
+        float xt = -INFINITY;
+        if (t < tail) {
+            xt = to_f(xrow[p.bulk_elems + t]);
+            merge(m, s, xt, 1.0f);
+        }
+        // the CTA's 512 pairs: warp butterflies, then the 16 warps' pairs in
+        // warp order (the same bits in every thread)
+        warp_merge(m, s);
+        if (lane == 0) {
+            red_m[parity_buf][warp] = m;
+            red_s[parity_buf][warp] = s;
+        }
+        ok = group_all(kTmaComputeWarps, 0, ok);
+        if (!ok) break;
+        float M = red_m[parity_buf][0], S = red_s[parity_buf][0];
+        #pragma unroll
+        for (int w = 1; w < kTmaComputeWarps; ++w)
+            merge(M, S, red_m[parity_buf][w], red_s[parity_buf][w]);
+        parity_buf ^= 1;
+        const float Mz = (M == -INFINITY) ? 0.0f : M;
+        const float inv = 1.0f / S;
+        // pass 2: y = e^(x - M) / S, chunk by chunk
+        for (int32_t c = 0; c < C; ++c) {
+            take(d, round);
+            const int32_t e0 = c * kChunkElems;
+            const int32_t nv = (p.bulk_elems - e0 < kChunkElems ? p.bulk_elems - e0 : kChunkElems) / V;
+            const uint8_t* slot = slots + static_cast<size_t>(d) * kLongChunkBytes;
+            float x[kLongKV][V];
+            #pragma unroll
+            for (int k = 0; k < kLongKV; ++k) {
+                const int32_t v = t + k * T;
+                if (v < nv)
+                    unpack16<InT>(*reinterpret_cast<const uint4*>(slot + static_cast<size_t>(v) * 16),
+                                  x[k]);
+            }
+            release(d);
+            if (ok) {
+                #pragma unroll
+                for (int k = 0; k < kLongKV; ++k) {
+                    const int32_t v = t + k * T;
+                    if (v < nv) {
+                        float o[V];
+                        #pragma unroll
+                        for (int e = 0; e < V; ++e) o[e] = exp_elem<InT>(x[k][e] - Mz) * inv;
+                        store_vec16<InT, OutT>(yrow + e0 + static_cast<int64_t>(v) * V, o);
+                    }
+                }
+            }
+            if (++d == D) {
+                d = 0;
+                ++round;
+            }
+        }
+        if (t < tail && ok) yrow[p.bulk_elems + t] = from_f<OutT>(exp_elem<InT>(xt - Mz) * inv);
+    }
+    if (!ok) {
+        abort_flag = 1;
+        atomicExch(p.err, 1);
+    }
+}
+
+template <typename InT, typename OutT>
+cudaError_t launch_softmax_long(const TmaSoftmaxParams& p, int grid, size_t smem,
+                                cudaStream_t stream) {
+    auto kern = softmax_long_kernel<InT, OutT>;
+    {
+        static std::mutex mu;
+        static bool raised = false;
+        std::lock_guard<std::mutex> g(mu);
+        if (!raised) {
+            cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 static_cast<int>(smem));
+            if (e != cudaSuccess) return e;
+            raised = true;
+        }
+    }
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.gridDim = dim3(grid, 1, 1);
+    cfg.blockDim = dim3(kTmaThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, p);
+}
+
 template <typename InT, typename OutT, int KV, bool WHOLE>
 cudaError_t launch_softmax_tma_kv(const TmaSoftmaxParams& p, int grid, size_t smem,
                                   cudaStream_t stream) {
@@ -515,6 +778,7 @@ cudaError_t launch_softmax_tma_w(const TmaSoftmaxParams& p, int grid, size_t sme
 template <typename InT, typename OutT>
 cudaError_t launch_softmax_tma(const TmaSoftmaxParams& p, int grid, size_t smem,
                                cudaStream_t stream) {
+    if (p.long_rows) return launch_softmax_long<InT, OutT>(p, grid, smem, stream);
     switch (p.kv) {
         case 1: return launch_softmax_tma_w<InT, OutT, 1>(p, grid, smem, stream);
         case 2: return launch_softmax_tma_w<InT, OutT, 2>(p, grid, smem, stream);

@@ -82,11 +82,14 @@ def test_work_split(cols, mode, threads, cluster):
     (3000, DT_F16, 3000, 1, 4, 1, 8, 4), (8192, DT_BF16, 8192, 1, 8, 1, 6, 4),
     (2048, DT_BF16, 2048, 1, 8, 8, 3, 8), (1536, DT_F16, 1536, 1, 8, 8, 4, 8),
     (32768, DT_F16, 32768, 1, 16, 1, 3, 8), (20000, DT_BF16, 20000, 1, 16, 1, 5, 8),
-    # not staged: too long for one CTA (two passes; a cluster of 2 for rows
-    # whose 152 resident slices exceed 64 MB), too short, or rows not 16-byte
-    # aligned
-    (16388, DT_F32, 16388, 1, 0, 0, 0, 0), (32776, DT_F16, 32776, 1, 0, 0, 0, 0),
-    (65536, DT_F32, 65536, 1, 0, 0, 0, 0), (131072, DT_F32, 131072, 2, 0, 0, 0, 0),
+    # too long to stage whole: streamed twice in 32 KB chunks (6 slots, the
+    # CTA's 16 warps on one row, 4 vectors per thread per chunk) while the
+    # slices of 152 SMs fit 64 MB of L2
+    (16388, DT_F32, 16388, 1, 16, 1, 6, 4), (32776, DT_F16, 32776, 1, 16, 1, 6, 4),
+    (65536, DT_F32, 65536, 1, 16, 1, 6, 4), (110376, DT_F32, 110376, 1, 16, 1, 6, 4),
+    # not staged: a cluster of 2 for rows whose 152 resident slices exceed
+    # 64 MB (two passes), too short, or rows not 16-byte aligned
+    (131072, DT_F32, 131072, 2, 0, 0, 0, 0), (110384, DT_F32, 110384, 2, 0, 0, 0, 0),
     (131080, DT_F32, 131080, 2, 0, 0, 0, 0),
     (60, DT_F32, 60, 1, 0, 0, 0, 0), (120, DT_BF16, 120, 1, 0, 0, 0, 0),
     (16385, DT_F32, 16385, 1, 0, 0, 0, 0)])
@@ -107,6 +110,13 @@ def test_staged_split(cols, dt, ld, cl, gw, unit, depth, kv):
     assert got == (cl, gw, unit, depth, kv), p
     es = 4 if dt == DT_F32 else 2
     kvmax = 8                               # 16-byte vectors per thread
+    if depth and p["mode_name"] == "stream":
+        # long rows: a 32 KB chunk per slot, X read twice (the second time from L2)
+        assert p["vec"] == 1 and p["threads"] == 544 and p["grid"] == 152
+        assert 152 * cols * es <= 64 << 20 and cols * es > 64 * 1024 or cols > 16 * 32 * 8 * 16 // es
+        assert p["hbm_bytes"] == 100000 * cols * 3 * es
+        assert plan(5, cols, ldx=ld, ldy=ld, xdt=dt, ydt=dt)[1]["grid"] == 5
+        return
     if depth:
         assert p["vec"] == 1 and p["threads"] == 544          # 16 compute warps + the producer
         assert p["grid"] == (152 if cl == 1 else cl * (152 // cl))
@@ -151,5 +161,7 @@ def test_vector_rule_and_grid():
     assert plan(5, 4096, x=260, per_sm=2)[1]["grid"] == 5
     assert plan(100000, 4096, x=260, per_sm=2)[1]["grid"] == 304
     assert plan(100000, 100)[1]["grid"] == 152                    # staged: one CTA per SM
-    assert plan(100000, 65536, per_sm=10)[1]["grid"] == 10 * 152  # two passes, a CTA per row
+    assert plan(100000, 65536, per_sm=10)[1]["grid"] == 152       # long rows: one CTA per SM
+    assert plan(100, 65536)[1]["grid"] == 100
+    assert plan(100000, 65536, x=260, per_sm=10)[1]["grid"] == 10 * 152  # two passes, a CTA per row
     assert plan(100000, 1 << 20, per_sm=10)[1]["grid"] == 8 * 10  # 10 clusters of 8
