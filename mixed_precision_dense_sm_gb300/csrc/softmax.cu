@@ -181,13 +181,15 @@ gemm_status_t make_plan(int64_t rows, int64_t cols, const void* X, int64_t ldx, 
                    static_cast<int64_t>(num_sms) * ceil_div(cols, cl) * ex > kTwoPassL2Budget)
                 cl *= 2;
         }
-        if (pl.pub.vec && cl == 1 && cols > kCtaMaxCols) {
-            // 16-byte aligned rows too long to stage whole, whose slices on
-            // every SM fit the L2 budget: streamed twice through shared
-            // memory in chunks by bulk copies (softmax_long_kernel)
+        if (pl.pub.vec && cols > kCtaMaxCols && cl <= smx::kMaxLongCluster) {
+            // 16-byte aligned rows too long to stage whole: streamed twice
+            // through shared memory in chunks by bulk copies
+            // (softmax_long_kernel), each row split over a cluster of `cl`
+            // CTAs when one CTA per row would overrun the L2 budget
             pl.pub.mode = SOFTMAX_MODE_STREAM;
             pl.pub.threads = smx::kTmaThreads;
-            pl.pub.slice = static_cast<int32_t>(round_up(cols, 8));
+            pl.pub.cluster = static_cast<int32_t>(cl);
+            pl.pub.slice = static_cast<int32_t>(round_up(ceil_div(cols, cl), 8));
             pl.pub.depth = smx::kLongDepth;
             pl.pub.group_warps = smx::kTmaComputeWarps;
             pl.pub.unit_rows = 1;
@@ -196,7 +198,11 @@ gemm_status_t make_plan(int64_t rows, int64_t cols, const void* X, int64_t ldx, 
             pl.resident = false;
             pl.smem = static_cast<size_t>(1024 + smx::kLongDepth * smx::kLongChunkBytes);
             pl.bulk_elems = static_cast<int32_t>((row_bytes / 16) * 16 / ex);
-            pl.pub.grid = static_cast<int32_t>(rows < num_sms ? rows : num_sms);
+            // clusters resident at once: ctas_per_sm stands for them here
+            // (the launch asks the occupancy calculator)
+            int64_t groups = cl == 1 ? num_sms : (ctas_per_sm > 0 ? ctas_per_sm : num_sms / cl);
+            if (groups < 1) groups = 1;
+            pl.pub.grid = static_cast<int32_t>(cl * (rows < groups ? rows : groups));
             pl.pub.hbm_bytes = rows * cols * (2 * ex + ey);
             return GEMM_OK;
         }
@@ -365,6 +371,8 @@ gemm_status_t softmax_rows(int64_t rows, int64_t cols, const void* X, int64_t ld
         q.kv = pl.pub.kv;
         q.whole = pl.whole ? 1 : 0;
         q.long_rows = pl.long_rows ? 1 : 0;
+        q.cluster = pl.pub.cluster;
+        q.slice = pl.pub.slice;
         q.err = err;
         {
             std::lock_guard<std::mutex> g(g_dbg_mu);

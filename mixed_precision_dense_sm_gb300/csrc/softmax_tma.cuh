@@ -63,6 +63,8 @@ struct TmaSoftmaxParams {
     int32_t kv;             // 16-byte vectors per thread: 1, 2, 4 (or 8 for FP32 input)
     int32_t whole;          // 1: bulk_elems == cols and every thread holds kv vectors
     int32_t long_rows;      // 1: rows streamed twice in chunks (softmax_long_kernel)
+    int32_t cluster;        // long rows: CTAs per row (a thread-block cluster when > 1)
+    int32_t slice;          // long rows: elements of a row per CTA (a multiple of 8)
     int* err;               // device error word (1: a wait ran out)
     uint64_t wait_limit_ns;
     uint32_t debug_flags;
@@ -494,6 +496,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
 constexpr int kLongKV = 4;                                          // vectors per thread per chunk
 constexpr int kLongChunkBytes = kTmaComputeWarps * 32 * kLongKV * 16;  // 32 KB
 constexpr int kLongDepth = 6;
+constexpr int kMaxLongCluster = 8;
 
 // Bounded wait that also gives up once another thread of the CTA has set
 // `abort` (the clock is read every 64 tries).
@@ -512,6 +515,47 @@ __device__ __forceinline__ bool wait_full(uint64_t* bar, uint32_t parity, volati
     }
 }
 
+// (m, s) of this CTA's part of a row sent to every CTA of the cluster: the
+// pair into the peer's receive buffer (slot `rank`), then a release-arrive on
+// the peer's exchange barrier, which counts one arrival per CTA.
+__device__ __forceinline__ void send_pair(float m, float s, float* recv_m, float* recv_s,
+                                          uint64_t* xbar, uint32_t rank, int cl) {
+    const uint32_t am = gemm103::smem_addr(recv_m + rank);
+    const uint32_t as = gemm103::smem_addr(recv_s + rank);
+    const uint32_t ab = gemm103::smem_addr(xbar);
+    for (int q = 0; q < cl; ++q) {
+        asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(gemm103::map_to_rank(am, q)), "f"(m)
+                     : "memory");
+        asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(gemm103::map_to_rank(as, q)), "f"(s)
+                     : "memory");
+        asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];"
+                     ::"r"(gemm103::map_to_rank(ab, q)) : "memory");
+    }
+}
+
+// Bounded wait on a barrier that peers of the cluster arrive on.
+__device__ __forceinline__ bool wait_peers(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                           uint64_t limit_ns) {
+    const uint32_t a = gemm103::smem_addr(bar);
+    uint64_t t0 = 0;
+    for (uint32_t i = 1;; ++i) {
+        if (gemm103::mbar_try_wait_cluster(a, parity)) return true;
+        if ((i & 63u) == 0) {
+            if (*abort) return false;
+            const uint64_t now = gemm103::global_timer_ns();
+            if (i == 64u) t0 = now;
+            else if (now - t0 > limit_ns) return false;
+        }
+    }
+}
+
+// A row longer than one CTA's share of L2 is split over a cluster of
+// p.cluster CTAs (slice p.slice elements each); after pass 1 every CTA sends
+// its (m, s) to all the others, and each merges the cluster's pairs in rank
+// order, so all hold the same (M, S).  Every loop of every thread is bounded
+// and no thread leaves early: the rows, chunks and exchanges of a cluster
+// run the same count on all its CTAs whatever fails, and the CTAs meet once
+// more before they exit, so no CTA can go while a peer still writes to it.
 template <typename InT, typename OutT>
 __global__ void __launch_bounds__(kTmaThreads, 1)
     softmax_long_kernel(const __grid_constant__ TmaSoftmaxParams p) {
@@ -521,222 +565,290 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
     constexpr int32_t kChunkElems = kLongChunkBytes / static_cast<int>(sizeof(InT));
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     __shared__ float red_m[2][kTmaComputeWarps], red_s[2][kTmaComputeWarps];
+    __shared__ float recv_m[2][kMaxLongCluster], recv_s[2][kMaxLongCluster];
+    __shared__ __align__(8) uint64_t xbar[2];
     __shared__ int abort_flag;
     const InT* __restrict__ X = static_cast<const InT*>(p.X);
     OutT* __restrict__ Y = static_cast<OutT*>(p.Y);
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
+    const int CL = p.cluster;
+    const uint32_t rank = CL > 1 ? gemm103::cluster_ctarank() : 0u;
+    const int64_t cid = blockIdx.x / CL;                       // this CTA's cluster
+    const int64_t nclusters = gridDim.x / CL;
+    // this CTA's part of every row: elements [e_lo, e_lo + nb) by bulk copies,
+    // and the tail [bulk_elems, cols) in the CTA whose part ends the row
+    const int32_t e_lo = static_cast<int32_t>(rank) * p.slice;
+    const int32_t e_hi = p.cols - e_lo < p.slice ? p.cols : e_lo + p.slice;
+    const bool ends_row = e_hi == p.cols;
+    const int32_t b_hi = ends_row ? p.bulk_elems : e_hi;
+    const int32_t nb = b_hi > e_lo ? b_hi - e_lo : 0;
+    const int32_t C = (nb + kChunkElems - 1) / kChunkElems;   // chunks per pass
     uint64_t* full = reinterpret_cast<uint64_t*>(smem_raw);
     uint64_t* empty = full + D;
     uint8_t* slots = smem_raw + 1024;
-    const int32_t C = (p.bulk_elems + kChunkElems - 1) / kChunkElems;   // chunks per row
     if (threadIdx.x == 0) {
         for (int i = 0; i < D; ++i) {
             gemm103::mbar_init(&full[i], 1);
             gemm103::mbar_init(&empty[i], kTmaComputeWarps);
         }
+        gemm103::mbar_init(&xbar[0], CL);
+        gemm103::mbar_init(&xbar[1], CL);
         abort_flag = 0;
         gemm103::fence_barrier_init();
     }
-    __syncthreads();
+    // every CTA's barriers are initialised before a peer arrives on them
+    if (CL > 1) gemm103::cluster_sync_all();
+    else __syncthreads();
     gemm103::grid_dependency_wait();      // inputs of the previous kernel are visible
 
     if (warp == kTmaComputeWarps) {
         // ------------------------------------------------------- producer
-        // unit i of this CTA: row blockIdx.x + (i / 2C) gridDim.x, pass
-        // (i % 2C) / C, chunk (i % 2C) % C; slot i % D
-        if (lane != 0) return;
-        const uint64_t keep = gemm103::l2_policy_evict_normal();
-        const uint64_t last = gemm103::l2_policy_evict_first();
-        const bool skip_first = (p.debug_flags & kSmxDebugSkipFirstLoad) && blockIdx.x == 0;
-        int64_t issued = 0;
-        int d = 0;
-        uint32_t round = 0;               // times slot 0 has been reached
-        for (int64_t row = blockIdx.x; row < p.rows; row += gridDim.x) {
+        // unit i of this CTA: row cid + (i / 2C) nclusters, pass (i % 2C) / C,
+        // chunk (i % 2C) % C; slot i % D
+        if (lane == 0) {
+            const uint64_t keep = gemm103::l2_policy_evict_normal();
+            const uint64_t last = gemm103::l2_policy_evict_first();
+            const bool skip_first = (p.debug_flags & kSmxDebugSkipFirstLoad) && blockIdx.x == 0;
+            int64_t issued = 0;
+            int d = 0;
+            uint32_t round = 0;               // times slot 0 has been reached
             bool ok = true;
-            for (int32_t j = 0; j < 2 * C; ++j) {
-                if (round > 0 &&
-                    !wait_full(&empty[d], (round - 1) & 1u, &abort_flag, p.wait_limit_ns)) {
-                    ok = false;
-                    break;
-                }
-                const int32_t c = j < C ? j : j - C;
-                const int32_t e0 = c * kChunkElems;
-                const int32_t n = p.bulk_elems - e0 < kChunkElems ? p.bulk_elems - e0 : kChunkElems;
-                const uint32_t bytes = static_cast<uint32_t>(n) * sizeof(InT);
-                gemm103::mbar_arrive_expect_tx(&full[d], bytes);
-                if (!(skip_first && issued == 0))
-                    gemm103::bulk_load_1d(slots + static_cast<size_t>(d) * kLongChunkBytes,
-                                          X + row * p.ldx + e0, bytes, &full[d], j < C ? keep : last);
-                ++issued;
-                if (++d == D) {
-                    d = 0;
-                    ++round;
+            for (int64_t row = cid; ok && row < p.rows; row += nclusters) {
+                for (int32_t j = 0; j < 2 * C; ++j) {
+                    if (round > 0 &&
+                        !wait_full(&empty[d], (round - 1) & 1u, &abort_flag, p.wait_limit_ns)) {
+                        ok = false;
+                        break;
+                    }
+                    const int32_t c = j < C ? j : j - C;
+                    const int32_t e0 = c * kChunkElems;
+                    const int32_t n = nb - e0 < kChunkElems ? nb - e0 : kChunkElems;
+                    const uint32_t bytes = static_cast<uint32_t>(n) * sizeof(InT);
+                    gemm103::mbar_arrive_expect_tx(&full[d], bytes);
+                    if (!(skip_first && issued == 0))
+                        gemm103::bulk_load_1d(slots + static_cast<size_t>(d) * kLongChunkBytes,
+                                              X + row * p.ldx + e_lo + e0, bytes, &full[d],
+                                              j < C ? keep : last);
+                    ++issued;
+                    if (++d == D) {
+                        d = 0;
+                        ++round;
+                    }
                 }
             }
             if (!ok) {
                 atomicExch(p.err, 1);
                 abort_flag = 1;
-                break;
             }
+            // every copy issued lands before the CTA (and its shared memory) goes
+            for (int64_t i = issued > D ? issued - D : 0; i < issued; ++i)
+                gemm103::mbar_wait(&full[static_cast<int>(i % D)],
+                                   static_cast<uint32_t>((i / D) & 1), p.wait_limit_ns);
         }
-        // every copy issued lands before the CTA (and its shared memory) goes
-        for (int64_t i = issued > D ? issued - D : 0; i < issued; ++i)
-            gemm103::mbar_wait(&full[static_cast<int>(i % D)], static_cast<uint32_t>((i / D) & 1),
-                               p.wait_limit_ns);
-        return;
-    }
-
-    // ------------------------------------------------------------ compute
-    const int t = threadIdx.x;
-    const int32_t tail = p.cols - p.bulk_elems;               // < V elements past the copies
-    int d = 0;
-    uint32_t round = 0;
-    bool ok = true;
-    int parity_buf = 0;
-    // wait for slot d's data; a wait that runs out tells every other waiter
-    // of the CTA (and the producer) to give up too
-    auto take = [&](int dd, uint32_t rr) {
-        if (!ok) return;
-        ok = wait_full(&full[dd], rr & 1u, &abort_flag, p.wait_limit_ns);
-        if (!ok) abort_flag = 1;
-    };
-    // the warp has read slot dd: one arrival, and only when every lane got
-    // its data (a slot whose copy never landed is never refilled)
-    auto release = [&](int dd) {
-        const bool wok = __all_sync(0xffffffffu, ok) != 0;
-        if (lane == 0 && wok) gemm103::mbar_arrive(&empty[dd]);
-    };
-    for (int64_t row = blockIdx.x; row < p.rows; row += gridDim.x) {
-        const InT* __restrict__ xrow = X + row * p.ldx;
-        OutT* __restrict__ yrow = Y + row * p.ldy;
-        // pass 1: (m, s) of this thread's elements, chunk by chunk
-        float m = -INFINITY, s = 0.0f;
-        for (int32_t c = 0; c < C; ++c) {
-            take(d, round);
-            const int32_t nv = (p.bulk_elems - c * kChunkElems < kChunkElems
-                                    ? p.bulk_elems - c * kChunkElems : kChunkElems) / V;
-            const uint8_t* slot = slots + static_cast<size_t>(d) * kLongChunkBytes;
-            float x[kLongKV][V];
-            #pragma unroll
-            for (int k = 0; k < kLongKV; ++k) {
-                const int32_t v = t + k * T;
-                if (v < nv) {
-                    unpack16<InT>(*reinterpret_cast<const uint4*>(slot + static_cast<size_t>(v) * 16),
-                                  x[k]);
-                } else {
-                    #pragma unroll
-                    for (int e = 0; e < V; ++e) x[k][e] = -INFINITY;
-                }
-            }
-            release(d);
-            float cm = -INFINITY;
-            #pragma unroll
-            for (int k = 0; k < kLongKV; ++k) {
-                #pragma unroll
-                for (int e = 0; e < V; ++e) cm = fmax_nan(cm, x[k][e]);
-            }
-            const float mm = fmax_nan(m, cm);
-            const float mmz = (mm == -INFINITY) ? 0.0f : mm;
-            float add = 0.0f;
-            #pragma unroll
-            for (int k = 0; k < kLongKV; ++k) {
-                #pragma unroll
-                for (int e = 0; e < V; ++e) add += exp_elem<InT>(x[k][e] - mmz);
-            }
-            s = (m == -INFINITY ? 0.0f : s * __expf(m - mmz)) + add;
-            m = mm;
-            if (++d == D) {
-                d = 0;
-                ++round;
-            }
-        }
-        float xt = -INFINITY;
-        if (t < tail) {
-            xt = to_f(xrow[p.bulk_elems + t]);
-            merge(m, s, xt, 1.0f);
-        }
-        // the CTA's 512 pairs: warp butterflies, then the 16 warps' pairs in
-        // warp order (the same bits in every thread)
-        warp_merge(m, s);
-        if (lane == 0) {
-            red_m[parity_buf][warp] = m;
-            red_s[parity_buf][warp] = s;
-        }
-        ok = group_all(kTmaComputeWarps, 0, ok);
-        if (!ok) break;
-        float M = red_m[parity_buf][0], S = red_s[parity_buf][0];
-        #pragma unroll
-        for (int w = 1; w < kTmaComputeWarps; ++w)
-            merge(M, S, red_m[parity_buf][w], red_s[parity_buf][w]);
-        parity_buf ^= 1;
-        const float Mz = (M == -INFINITY) ? 0.0f : M;
-        const float inv = 1.0f / S;
-        // pass 2: y = e^(x - M) / S, chunk by chunk
-        for (int32_t c = 0; c < C; ++c) {
-            take(d, round);
-            const int32_t e0 = c * kChunkElems;
-            const int32_t nv = (p.bulk_elems - e0 < kChunkElems ? p.bulk_elems - e0 : kChunkElems) / V;
-            const uint8_t* slot = slots + static_cast<size_t>(d) * kLongChunkBytes;
-            float x[kLongKV][V];
-            #pragma unroll
-            for (int k = 0; k < kLongKV; ++k) {
-                const int32_t v = t + k * T;
-                if (v < nv)
-                    unpack16<InT>(*reinterpret_cast<const uint4*>(slot + static_cast<size_t>(v) * 16),
-                                  x[k]);
-            }
-            release(d);
-            if (ok) {
+        __syncwarp();
+    } else {
+        // -------------------------------------------------------- compute
+        const int t = threadIdx.x;
+        const int32_t tail = ends_row ? p.cols - p.bulk_elems : 0;   // < V elements
+        int d = 0;
+        uint32_t round = 0;
+        bool ok = true;
+        uint32_t iter = 0;                // rows done by this CTA
+        // wait for slot dd's data; a wait that runs out tells every other
+        // waiter of the CTA (and the producer) to give up too
+        auto take = [&](int dd, uint32_t rr) {
+            if (!ok) return;
+            ok = wait_full(&full[dd], rr & 1u, &abort_flag, p.wait_limit_ns);
+            if (!ok) abort_flag = 1;
+        };
+        // the warp has read slot dd: one arrival, and only when every lane
+        // got its data (a slot whose copy never landed is never refilled)
+        auto release = [&](int dd) {
+            const bool wok = __all_sync(0xffffffffu, ok) != 0;
+            if (lane == 0 && wok) gemm103::mbar_arrive(&empty[dd]);
+        };
+        for (int64_t row = cid; row < p.rows; row += nclusters, ++iter) {
+            const InT* __restrict__ xrow = X + row * p.ldx + e_lo;
+            OutT* __restrict__ yrow = Y + row * p.ldy + e_lo;
+            const int pb = static_cast<int>(iter & 1u);
+            // pass 1: (m, s) of this thread's elements, chunk by chunk
+            float m = -INFINITY, s = 0.0f;
+            for (int32_t c = 0; c < C; ++c) {
+                take(d, round);
+                const int32_t e0 = c * kChunkElems;
+                const int32_t nv = (nb - e0 < kChunkElems ? nb - e0 : kChunkElems) / V;
+                const uint8_t* slot = slots + static_cast<size_t>(d) * kLongChunkBytes;
+                float x[kLongKV][V];
                 #pragma unroll
                 for (int k = 0; k < kLongKV; ++k) {
                     const int32_t v = t + k * T;
                     if (v < nv) {
-                        float o[V];
+                        unpack16<InT>(
+                            *reinterpret_cast<const uint4*>(slot + static_cast<size_t>(v) * 16), x[k]);
+                    } else {
                         #pragma unroll
-                        for (int e = 0; e < V; ++e) o[e] = exp_elem<InT>(x[k][e] - Mz) * inv;
-                        store_vec16<InT, OutT>(yrow + e0 + static_cast<int64_t>(v) * V, o);
+                        for (int e = 0; e < V; ++e) x[k][e] = -INFINITY;
                     }
                 }
+                release(d);
+                float cm = -INFINITY;
+                #pragma unroll
+                for (int k = 0; k < kLongKV; ++k) {
+                    #pragma unroll
+                    for (int e = 0; e < V; ++e) cm = fmax_nan(cm, x[k][e]);
+                }
+                const float mm = fmax_nan(m, cm);
+                const float mmz = (mm == -INFINITY) ? 0.0f : mm;
+                float add = 0.0f;
+                #pragma unroll
+                for (int k = 0; k < kLongKV; ++k) {
+                    #pragma unroll
+                    for (int e = 0; e < V; ++e) add += exp_elem<InT>(x[k][e] - mmz);
+                }
+                s = (m == -INFINITY ? 0.0f : s * __expf(m - mmz)) + add;
+                m = mm;
+                if (++d == D) {
+                    d = 0;
+                    ++round;
+                }
             }
-            if (++d == D) {
-                d = 0;
-                ++round;
+            float xt = -INFINITY;
+            if (t < tail) {
+                xt = to_f(X[row * p.ldx + p.bulk_elems + t]);
+                merge(m, s, xt, 1.0f);
             }
+            // the CTA's 512 pairs: warp butterflies, then the 16 warps' pairs
+            // in warp order (the same bits in every thread)
+            warp_merge(m, s);
+            if (lane == 0) {
+                red_m[pb][warp] = m;
+                red_s[pb][warp] = s;
+            }
+            ok = group_all(kTmaComputeWarps, 0, ok);
+            if (!ok && CL == 1) break;
+            float M = red_m[pb][0], S = red_s[pb][0];
+            #pragma unroll
+            for (int w = 1; w < kTmaComputeWarps; ++w) merge(M, S, red_m[pb][w], red_s[pb][w]);
+            if (CL > 1) {
+                // the cluster's pairs, merged in rank order in every CTA
+                if (t == 0) send_pair(M, S, recv_m[pb], recv_s[pb], &xbar[pb], rank, CL);
+                if (!wait_peers(&xbar[pb], (iter >> 1) & 1u, &abort_flag, p.wait_limit_ns)) {
+                    ok = false;
+                    abort_flag = 1;
+                }
+                M = recv_m[pb][0];
+                S = recv_s[pb][0];
+                for (int q = 1; q < CL; ++q) merge(M, S, recv_m[pb][q], recv_s[pb][q]);
+            }
+            const float Mz = (M == -INFINITY) ? 0.0f : M;
+            const float inv = 1.0f / S;
+            // pass 2: y = e^(x - M) / S, chunk by chunk
+            for (int32_t c = 0; c < C; ++c) {
+                take(d, round);
+                const int32_t e0 = c * kChunkElems;
+                const int32_t nv = (nb - e0 < kChunkElems ? nb - e0 : kChunkElems) / V;
+                const uint8_t* slot = slots + static_cast<size_t>(d) * kLongChunkBytes;
+                float x[kLongKV][V];
+                #pragma unroll
+                for (int k = 0; k < kLongKV; ++k) {
+                    const int32_t v = t + k * T;
+                    if (v < nv)
+                        unpack16<InT>(
+                            *reinterpret_cast<const uint4*>(slot + static_cast<size_t>(v) * 16), x[k]);
+                }
+                release(d);
+                if (ok) {
+                    #pragma unroll
+                    for (int k = 0; k < kLongKV; ++k) {
+                        const int32_t v = t + k * T;
+                        if (v < nv) {
+                            float o[V];
+                            #pragma unroll
+                            for (int e = 0; e < V; ++e) o[e] = exp_elem<InT>(x[k][e] - Mz) * inv;
+                            store_vec16<InT, OutT>(yrow + e0 + static_cast<int64_t>(v) * V, o);
+                        }
+                    }
+                }
+                if (++d == D) {
+                    d = 0;
+                    ++round;
+                }
+            }
+            if (t < tail && ok)
+                Y[row * p.ldy + p.bulk_elems + t] = from_f<OutT>(exp_elem<InT>(xt - Mz) * inv);
         }
-        if (t < tail && ok) yrow[p.bulk_elems + t] = from_f<OutT>(exp_elem<InT>(xt - Mz) * inv);
+        if (!ok) {
+            abort_flag = 1;
+            atomicExch(p.err, 1);
+        }
     }
-    if (!ok) {
-        abort_flag = 1;
-        atomicExch(p.err, 1);
-    }
+    // no CTA leaves while a peer may still write to its shared memory
+    if (CL > 1) gemm103::cluster_sync_all();
 }
 
 template <typename InT, typename OutT>
 cudaError_t launch_softmax_long(const TmaSoftmaxParams& p, int grid, size_t smem,
                                 cudaStream_t stream) {
     auto kern = softmax_long_kernel<InT, OutT>;
+    const int cl = p.cluster;
+    if (cl < 1 || cl > kMaxLongCluster || grid % cl != 0) return cudaErrorInvalidValue;
+    int clusters_max = 0;                 // clusters of `cl` CTAs resident at once (cl > 1)
     {
         static std::mutex mu;
         static bool raised = false;
+        static int resident[kMaxLongCluster + 1] = {};
         std::lock_guard<std::mutex> g(mu);
         if (!raised) {
             cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                  static_cast<int>(smem));
             if (e != cudaSuccess) return e;
+            if (cl > 1) {
+                e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+                if (e != cudaSuccess) return e;
+            }
             raised = true;
         }
+        if (cl > 1 && resident[cl] == 0) {
+            cudaLaunchConfig_t q = {};
+            cudaLaunchAttribute qa[1];
+            qa[0].id = cudaLaunchAttributeClusterDimension;
+            qa[0].val.clusterDim.x = cl;
+            qa[0].val.clusterDim.y = 1;
+            qa[0].val.clusterDim.z = 1;
+            q.gridDim = dim3(grid, 1, 1);
+            q.blockDim = dim3(kTmaThreads, 1, 1);
+            q.dynamicSmemBytes = smem;
+            q.attrs = qa;
+            q.numAttrs = 1;
+            int n = 0;
+            if (cudaOccupancyMaxActiveClusters(&n, kern, &q) != cudaSuccess || n < 1) {
+                cudaGetLastError();
+                n = 1;
+            }
+            resident[cl] = n;
+        }
+        clusters_max = cl > 1 ? resident[cl] : 0;
     }
+    if (cl > 1 && grid > cl * clusters_max) grid = cl * clusters_max;
     cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
+    int na = 1;
+    if (cl > 1) {
+        attr[1].id = cudaLaunchAttributeClusterDimension;
+        attr[1].val.clusterDim.x = cl;
+        attr[1].val.clusterDim.y = 1;
+        attr[1].val.clusterDim.z = 1;
+        na = 2;
+    }
     cfg.gridDim = dim3(grid, 1, 1);
     cfg.blockDim = dim3(kTmaThreads, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = na;
     return cudaLaunchKernelEx(&cfg, kern, p);
 }
 

@@ -83,14 +83,15 @@ def test_work_split(cols, mode, threads, cluster):
     (2048, DT_BF16, 2048, 1, 8, 8, 3, 8), (1536, DT_F16, 1536, 1, 8, 8, 4, 8),
     (32768, DT_F16, 32768, 1, 16, 1, 3, 8), (20000, DT_BF16, 20000, 1, 16, 1, 5, 8),
     # too long to stage whole: streamed twice in 32 KB chunks (6 slots, the
-    # CTA's 16 warps on one row, 4 vectors per thread per chunk) while the
-    # slices of 152 SMs fit 64 MB of L2
+    # CTA's 16 warps on one row, 4 vectors per thread per chunk), the row
+    # split over a cluster of 2-8 CTAs when the slices of 152 SMs would
+    # exceed 64 MB of L2
     (16388, DT_F32, 16388, 1, 16, 1, 6, 4), (32776, DT_F16, 32776, 1, 16, 1, 6, 4),
     (65536, DT_F32, 65536, 1, 16, 1, 6, 4), (110376, DT_F32, 110376, 1, 16, 1, 6, 4),
-    # not staged: a cluster of 2 for rows whose 152 resident slices exceed
-    # 64 MB (two passes), too short, or rows not 16-byte aligned
-    (131072, DT_F32, 131072, 2, 0, 0, 0, 0), (110384, DT_F32, 110384, 2, 0, 0, 0, 0),
-    (131080, DT_F32, 131080, 2, 0, 0, 0, 0),
+    (131072, DT_F32, 131072, 2, 16, 1, 6, 4), (110384, DT_F32, 110384, 2, 16, 1, 6, 4),
+    (131080, DT_F32, 131080, 2, 16, 1, 6, 4), (1 << 20, DT_F32, 1 << 20, 8, 16, 1, 6, 4),
+    (300001 + 7, DT_BF16, 300008, 2, 16, 1, 6, 4),
+    # not staged: too short, or rows not 16-byte aligned
     (60, DT_F32, 60, 1, 0, 0, 0, 0), (120, DT_BF16, 120, 1, 0, 0, 0, 0),
     (16385, DT_F32, 16385, 1, 0, 0, 0, 0)])
 def test_staged_split(cols, dt, ld, cl, gw, unit, depth, kv):
@@ -111,11 +112,16 @@ def test_staged_split(cols, dt, ld, cl, gw, unit, depth, kv):
     es = 4 if dt == DT_F32 else 2
     kvmax = 8                               # 16-byte vectors per thread
     if depth and p["mode_name"] == "stream":
-        # long rows: a 32 KB chunk per slot, X read twice (the second time from L2)
-        assert p["vec"] == 1 and p["threads"] == 544 and p["grid"] == 152
-        assert 152 * cols * es <= 64 << 20 and cols * es > 64 * 1024 or cols > 16 * 32 * 8 * 16 // es
+        # long rows: a 32 KB chunk per slot, X read twice (the second time
+        # from L2); a cluster's CTAs take equal slices, multiples of 8
+        assert p["vec"] == 1 and p["threads"] == 544 and p["grid"] == cl * (152 // cl)
+        assert cols * es > 64 * 1024
+        sl = p["slice"]
+        assert sl % 8 == 0 and sl * cl >= cols and (sl - 8) * cl < cols
+        assert 152 * sl * es <= 64 << 20 or cl == 8
+        assert cl == 1 or 152 * -(-cols // (cl // 2)) * es > 64 << 20
         assert p["hbm_bytes"] == 100000 * cols * 3 * es
-        assert plan(5, cols, ldx=ld, ldy=ld, xdt=dt, ydt=dt)[1]["grid"] == 5
+        assert plan(5, cols, ldx=ld, ldy=ld, xdt=dt, ydt=dt)[1]["grid"] == 5 * cl
         return
     if depth:
         assert p["vec"] == 1 and p["threads"] == 544          # 16 compute warps + the producer

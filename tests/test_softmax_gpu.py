@@ -89,10 +89,10 @@ COLS = [1, 2, 7, 31, 32, 33, 100, 1000, 1024, 1025, 2049, 4096, 8192, 8193, 1234
 @pytest.mark.parametrize("cols", COLS)
 def test_every_work_split(lib, orc, cols):
     """Ragged and exact row lengths on each side of every split boundary
-    (warp 1024, CTA 8192 / 16384, two passes by one CTA above 16384 -- the
-    rows streamed twice through shared memory in 32 KB chunks -- and by a
-    cluster of 2 above about 110000), 16-byte aligned rows, FP32 in and out,
-    4 N(0,1) logits."""
+    (warp 1024, CTA 8192 / 16384, two passes above 16384 -- the rows
+    streamed twice through shared memory in 32 KB chunks, by one CTA or,
+    above about 110000, by a cluster of 2-4), 16-byte aligned rows, FP32 in
+    and out, 4 N(0,1) logits."""
     rows = 5 if cols > 20000 else 37
     g = torch.Generator().manual_seed(cols)
     x = torch.randn((rows, cols), generator=g) * 4.0
@@ -256,7 +256,7 @@ def test_empty_and_errors(lib):
     assert torch.all(Y == 7.0)
 
 
-@pytest.mark.parametrize("cols", [1024, 4096, 16384, 65536])
+@pytest.mark.parametrize("cols", [1024, 4096, 16384, 65536, 262144])
 def test_timeout_reported_without_fault(lib, orc, cols):
     """The failure path of the staged kernels, without a GPU fault: the test
     hook arms the first row slot of the first pipeline without issuing its
@@ -264,7 +264,9 @@ def test_timeout_reported_without_fault(lib, orc, cols):
     GEMM_ERR_DEVICE_TIMEOUT once; the next call on the same device is
     correct.  1024 FP32 columns run a warp per row, 4096 a group of 8 warps
     per row, 16384 a group of 16 warps (every compute warp) per row, 65536
-    the long-row kernel (the row streamed twice in chunks)."""
+    the long-row kernel (the row streamed twice in chunks), 262144 that
+    kernel with each row split over a cluster of 4 CTAs (the failing CTA
+    keeps exchanging with its peers, so none waits for it unbounded)."""
     g = torch.Generator().manual_seed(5)
     Xs = stored(torch.randn((64, cols), generator=g), cols, DT_F32)
     st, p = lib.softmax_plan_query(64, cols, 256, cols, DT_F32, 1 << 44, cols, DT_F32)
