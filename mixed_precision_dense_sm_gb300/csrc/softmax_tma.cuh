@@ -500,7 +500,7 @@ constexpr int kMaxLongCluster = 8;
 
 // Bounded wait that also gives up once another thread of the CTA has set
 // `abort` (the clock is read every 64 tries).
-__device__ __forceinline__ bool wait_full(uint64_t* bar, uint32_t parity, volatile int* abort,
+__device__ __forceinline__ bool wait_abortable(uint64_t* bar, uint32_t parity, volatile int* abort,
                                           uint64_t limit_ns) {
     const uint32_t a = gemm103::smem_addr(bar);
     uint64_t t0 = 0;
@@ -617,7 +617,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
             for (int64_t row = cid; ok && row < p.rows; row += nclusters) {
                 for (int32_t j = 0; j < 2 * C; ++j) {
                     if (round > 0 &&
-                        !wait_full(&empty[d], (round - 1) & 1u, &abort_flag, p.wait_limit_ns)) {
+                        !wait_abortable(&empty[d], (round - 1) & 1u, &abort_flag, p.wait_limit_ns)) {
                         ok = false;
                         break;
                     }
@@ -659,7 +659,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
         // waiter of the CTA (and the producer) to give up too
         auto take = [&](int dd, uint32_t rr) {
             if (!ok) return;
-            ok = wait_full(&full[dd], rr & 1u, &abort_flag, p.wait_limit_ns);
+            ok = wait_abortable(&full[dd], rr & 1u, &abort_flag, p.wait_limit_ns);
             if (!ok) abort_flag = 1;
         };
         // the warp has read slot dd: one arrival, and only when every lane
