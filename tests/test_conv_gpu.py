@@ -207,6 +207,45 @@ def test_single_cta_wide_tiles_two_chunks(g, orc):
     run_and_check(g, orc, geo, dt=DT_BF16, ydt=DT_BF16, integer=True, sample=sample)
 
 
+@pytest.mark.parametrize("name", list(workloads.CONV_WORKLOADS))
+def test_conv_workloads_sampled(g, orc, name):
+    """The named convolution layers at full size, with the benchmark's seeded
+    inputs and in the launch configuration it times (halo units for the
+    64- and 128-channel layers, CTA pairs and stream-K for the others):
+    sampled output pixels -- the first and last of every image and a spread
+    between -- against the oracle, every output channel."""
+    import mixed_precision_dense_sm_gb300 as lib
+    w = workloads.CONV_WORKLOADS[name]
+    x, wt = workloads.make_conv_inputs(w)
+    P, Q = w.out_hw()
+    M = w.N * P * Q
+    X, Wd = x.cuda(), wt.cuda()
+    Y = torch.full((M, w.K), float("nan"), dtype=TORCH_DTYPE[w.y_dtype], device="cuda")
+    st = lib.conv2d_fprop(g.h, w.N, w.H, w.W, w.C, w.K, w.R, w.S, w.pad, w.stride, w.dil, 1.0,
+                          X.data_ptr(), Wd.data_ptr(), 0.0, Y.data_ptr(),
+                          (w.x_dtype, w.x_dtype, w.y_dtype), 0, DT_F32, 0,
+                          torch.cuda.current_stream().cuda_stream)
+    assert st == 0, lib.gemm_status_string(st)
+    g.sync()
+    per = P * Q
+    rows = np.unique(np.concatenate([np.arange(0, M, max(1, M // 700)), np.arange(0, M, per),
+                                     np.arange(per - 1, M, per), [1, Q, Q + 1]]))
+    xc, wc = workloads.as_codes(x), workloads.as_codes(wt)
+    Rr, Sr = orc.conv2d_sampled(w.N, w.H, w.W, w.C, w.K, w.R, w.S, w.pad[0], w.pad[1], w.stride[0],
+                                w.stride[1], w.dil[0], w.dil[1], 1.0, xc, wc, 0.0, None,
+                                w.x_dtype, w.y_dtype, rows)
+    got = Y.cpu()[torch.as_tensor(rows)]
+    vals = got.double().numpy()
+    codes = None if w.y_dtype == DT_F32 else got.contiguous().view(torch.int16).numpy().view(np.uint16)
+    ocodes = None if w.y_dtype == DT_F32 else orc.round_output(Rr, w.y_dtype)
+    stats, bad = checks.compare(vals, codes, Rr, Sr, None, 1.0, 0.0, w.y_dtype, ocodes)
+    if stats["fail"]:
+        i, j = np.argwhere(bad)[0]
+        raise AssertionError(f"{name}: {stats}; first bad ({rows[i]}, {j}) gpu={vals[i, j]!r} "
+                             f"oracle={Rr[i, j]!r}")
+    print(name, len(rows), "pixels", stats)
+
+
 def test_errors_enqueue_nothing(g):
     import mixed_precision_dense_sm_gb300 as lib
     Y = torch.full((64, 16), 5.0, device="cuda")
