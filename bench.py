@@ -720,8 +720,9 @@ def run_e2e(lib, g, bufs, stream, args, world, launch):
     D2H of every output, all inside the timed region.  Three streams pipeline
     the step: the inputs of GEMM i+1 go up and the output of GEMM i-1 comes
     back while GEMM i runs; events order the reuse of each device buffer
-    across steps (a buffer is refilled only after the GEMM that read it, and a
-    GEMM overwrites C only after the previous step's copy-back of it)."""
+    across steps (A and B are refilled only after the GEMM that read them, C
+    -- when beta != 0 uploads it -- only after its copy-back, and a GEMM
+    overwrites C only after the previous step's copy-back of it)."""
     host = []
     h2d = d2h = 0
     for (w, inp, A, B, C) in bufs:
@@ -744,7 +745,8 @@ def run_e2e(lib, g, bufs, stream, args, world, launch):
     def step():
         for i, ((w, inp, A, B, C), (hA, hB, hC, hCin)) in enumerate(zip(bufs, host)):
             s_up.wait_event(ev_mm[i])           # previous step's GEMM i has read A, B (and C)
-            s_up.wait_event(ev_out[i])          # ... and C_i has been copied back
+            if hCin is not None:
+                s_up.wait_event(ev_out[i])      # C_i is refilled only once it has been copied back
             with torch.cuda.stream(s_up):
                 A.copy_(hA, non_blocking=True)
                 B.copy_(hB, non_blocking=True)
