@@ -713,7 +713,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     const int S = p.stages;
-    const bool halo = (p.conv_tiled == 2);
+    // whole-row convolution tiles (conv_tiled) run on 256-row tiles only
+    const bool whole_rows = MH == 2 && p.conv_tiled != 0;
+    const bool halo = MH == 2 && p.conv_tiled == 2;
     const uint32_t stage_bytes = halo ? p.halo_stage_bytes : kStageBytes;
     const uint32_t a_region = halo ? p.halo_a_region : kATile;
     // [stages][C staging, when C is stored by TMA][barriers]
@@ -813,7 +815,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (halo)
                         return p.conv_a_bytes +
                                static_cast<uint32_t>(b_parts(nf)) * p.conv_R * kBRows * 128u;
-                    if (p.conv_tiled)
+                    if (whole_rows)
                         return static_cast<uint32_t>(kc) * p.conv_a_bytes +
                                static_cast<uint32_t>(b_parts(nf)) * kBTile;
                     return static_cast<uint32_t>(a_parts(mf)) *
@@ -832,7 +834,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // convolution: the first window of this CTA's rows (output
                 // pixel m0) as the input coordinates of its top-left pixel
                 int32_t cn = 0, ch = 0, cw = 0;
-                if (p.conv_tiled) {
+                if (whole_rows) {
                     // the tile's image and first output row
                     cn = tm / p.conv_tpi;
                     ch = (tm - cn * p.conv_tpi) * p.conv_rows - p.conv_pad_h;
@@ -865,10 +867,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                         continue;
                     }
-                    if (halo) {
+                    if (MH == 2 && halo) {
                         // filter column s, channel block cb: the halo box, then
                         // the column's R taps (3-D filter map, one box per tap)
-                        if constexpr (CG == 1) {
+                        if constexpr (CG == 1 && MH == 2) {
                             mbar_arrive_expect_tx(&full[stage], bytes);
                             const int32_t sc = kb / p.conv_cblocks;
                             const int32_t cb0 = (kb - sc * p.conv_cblocks) * kChunkK;
@@ -899,7 +901,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             const int32_t r = tap / p.conv_S;
                             const uint16_t ow = static_cast<uint16_t>((tap - r * p.conv_S) * p.conv_dil_w);
                             const uint16_t oh = static_cast<uint16_t>(r * p.conv_dil_h);
-                            if (p.conv_tiled) {
+                            if (whole_rows) {
                                 // the tap's window of the tile's output rows:
                                 // input (cw + ow + q', ch + oh + p') for output (p', q')
                                 if constexpr (CG == 1)
@@ -1021,23 +1023,29 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tc_fence_after_sync();
                     const uint32_t sa = smem_base + stage * stage_bytes;
                     const uint32_t sb = sa + a_region;
-                    if (halo) {
+                    if (MH == 2 && halo) {
                         // tap r of this filter column: A from halo row
                         // r * dil_h * pitch on (a multiple of 8 rows, so the
-                        // swizzle atoms line up), its own B tile
-                        const uint32_t a_tap = static_cast<uint32_t>(p.conv_dil_h * p.conv_pitch) * 128u;
-                        for (int32_t r = 0; r < p.conv_R; ++r) {
+                        // swizzle atoms line up), its own B tile.  The
+                        // descriptors advance by (byte offset >> 4) added to
+                        // their start-address field (shared-memory offsets
+                        // never overflow its 14 bits): one add per MMA
+                        const uint32_t a_tap = static_cast<uint32_t>(p.conv_dil_h * p.conv_pitch) * 8u;
+                        const uint64_t a_desc = smem_desc_sw128(sa, 16u, 1024);
+                        const uint64_t b_desc = smem_desc_sw128(sb, 16u, 1024);
+                        // A and B share the high word (stride offset, layout)
+                        const uint32_t hi = static_cast<uint32_t>(a_desc >> 32);
+                        uint32_t ar = static_cast<uint32_t>(a_desc);
+                        uint32_t br = static_cast<uint32_t>(b_desc);
+                        uint32_t acc = kb > sg.kb0 ? 1u : 0u;
+                        for (int32_t r = 0; r < p.conv_R; ++r, ar += a_tap, br += kBRows * 8u) {
                             #pragma unroll
                             for (int kk = 0; kk < 4; ++kk) {
-                                const uint64_t ad = smem_desc_sw128(sa + r * a_tap + kk * 32u, 16u, 1024);
-                                const uint64_t bd =
-                                    smem_desc_sw128(sb + r * kBRows * 128u + kk * 32u, 16u, 1024);
-                                const uint32_t acc = (kb > sg.kb0 || r > 0 || kk > 0) ? 1u : 0u;
-                                if constexpr (ES == 2 && CG == 1) {
-                                    tc_mma_f16(d_tmem, ad, bd, p.idesc, acc);
-                                    if constexpr (MH == 2)
-                                        tc_mma_f16(d_tmem + BN, ad + (kATileBytes >> 4), bd, p.idesc, acc);
-                                }
+                                if constexpr (ES == 2 && CG == 1 && MH == 2)
+                                    tc_mma_f16_x2(d_tmem, d_tmem + BN, ar + kk * 2u,
+                                                  ar + kk * 2u + (kATileBytes >> 4), br + kk * 2u, hi,
+                                                  p.idesc, acc);
+                                acc = 1u;
                             }
                         }
                     } else {
@@ -1056,10 +1064,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             else tc_mma_f16_pair(d_tmem, ad, bd, p.idesc, acc);
                         }
                         if constexpr (MH == 2) {
-                            // the second half: its A rows (the descriptor's start
-                            // address, in 16-byte units, moved on by a_hstep: a
-                            // shared-memory offset stays inside the field's 14
-                            // bits), the same B, its accumulator
+                            // the second half: its A rows, the same B, its accumulator
                             const uint64_t ad2 = ad + (a_hstep >> 4);
                             if constexpr (ES == 4) tc_mma_tf32(d_tmem + BN, ad2, bd, p.idesc, acc);
                             else tc_mma_f16(d_tmem + BN, ad2, bd, p.idesc, acc);
@@ -1107,7 +1112,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             int32_t tm, tn;
             tile_coords(p, sg.tile, tm, tn);
             int32_t row = tm * BM + row_in_tile;                    // D' row
-            if (p.conv_tiled) {
+            if (whole_rows) {
                 // output pixel row_in_tile of the tile's conv_rows image rows
                 // (rows past the image's last output row are not stored)
                 const int32_t n = tm / p.conv_tpi;

@@ -260,6 +260,25 @@ __device__ __forceinline__ void tc_mma_f16(uint32_t d_tmem, uint64_t a_desc, uin
         : "memory");
 }
 
+// Two MMAs of one K step into two accumulators (d0, d1), sharing B: A and B
+// descriptors given as their low words over one common high word (the
+// start address and leading offset change, the stride offset and layout do
+// not), so the issuing thread spends no 64-bit arithmetic per MMA.
+__device__ __forceinline__ void tc_mma_f16_x2(uint32_t d0, uint32_t d1, uint32_t a0_lo,
+                                              uint32_t a1_lo, uint32_t b_lo, uint32_t desc_hi,
+                                              uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t.reg .b64 a0, a1, b;\n\t"
+        "setp.ne.b32 p, %7, 0;\n\t"
+        "mov.b64 a0, {%2, %5};\n\t"
+        "mov.b64 a1, {%3, %5};\n\t"
+        "mov.b64 b, {%4, %5};\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], a0, b, %6, p;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%1], a1, b, %6, p;\n\t}" ::"r"(d0),
+        "r"(d1), "r"(a0_lo), "r"(a1_lo), "r"(b_lo), "r"(desc_hi), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 // kind::tf32: FP32 operands in shared memory enter the product as TF32.
 __device__ __forceinline__ void tc_mma_tf32(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                             uint32_t idesc, uint32_t accumulate) {
