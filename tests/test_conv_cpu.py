@@ -99,3 +99,56 @@ def test_argument_checks():
                 dict(X=264), dict(Wt=520)]:
         assert plan(**bad)[0] == UNSUPPORTED, bad
     assert plan(C=8)[0] == OK and plan(stride=(8, 8))[0] == OK
+
+
+def test_whole_row_plan_invariants_on_random_layers():
+    """Seeded random stride-1 and strided layers: every whole-row plan keeps
+    its tile inside 256 rows at its pitch, covers each image's output rows
+    exactly once with the rows split evenly, and is a halo plan (pitch Q
+    rounded up to 8, k_blocks = S ceil(C / 64), a box of at most 256 rows)
+    or a box-per-tap plan (pitch Q); layers without whole-row tiles are
+    strided, have rows wider than 256 pixels, or run other tiles."""
+    import random
+    rng = random.Random(20261202)
+    seen_halo = seen_tap = seen_none = 0
+    for _ in range(400):
+        R = rng.choice([1, 3, 5, 7])
+        S = rng.choice([1, 3, 5])
+        dil = (rng.choice([1, 1, 2]), rng.choice([1, 1, 2]))
+        stride = (1, 1) if rng.random() < 0.8 else (rng.choice([1, 2]), 2)
+        H = rng.randint((R - 1) * dil[0] + 1, 80)
+        W = rng.choice([rng.randint((S - 1) * dil[1] + 1, 64), rng.randint(200, 300)])
+        C = 8 * rng.randint(1, 40)
+        K = rng.choice([16, 40, 64, 96, 128, 256])
+        N = rng.randint(1, 6)
+        pad = (rng.randint(0, R // 2 * dil[0]), rng.randint(0, S // 2 * dil[1]))
+        st, p = plan(N=N, H=H, W=W, C=C, K=K, R=R, S=S, pad=pad, stride=stride, dil=dil)
+        if st != OK or p["path_name"] in ("noop", "scale"):
+            continue
+        P = (H + 2 * pad[0] - dil[0] * (R - 1) - 1) // stride[0] + 1
+        Q = (W + 2 * pad[1] - dil[1] * (S - 1) - 1) // stride[1] + 1
+        rows, pitch = p["conv_rows"], p["conv_pitch"]
+        if rows == 0:
+            assert pitch == 0
+            assert stride != (1, 1) or Q > 256 or p["block_m"] != 256 or \
+                p["path_name"] != "tiled_1sm", (N, H, W, C, K, R, S, pad, stride, dil, p)
+            seen_none += 1
+            continue
+        assert stride == (1, 1) and p["path_name"] == "tiled_1sm" and p["block_m"] == 256
+        assert p["block_n"] <= 128 and rows * pitch <= 256 and pitch in (Q, -(-Q // 8) * 8)
+        tpi = p["tiles_m"] // N
+        assert p["tiles_m"] == N * tpi and (tpi - 1) * rows < P <= tpi * rows
+        assert rows == -(-P // tpi)
+        cb = -(-C // 64)
+        kc = 2 if C % 64 == 0 else 1
+        tap_blocks = -(-R * S * cb // kc)
+        if pitch != Q or (p["k_blocks"] != tap_blocks and p["k_blocks"] == S * cb):
+            # halo units: one step per filter column and channel block
+            assert pitch == -(-Q // 8) * 8 and p["k_blocks"] == S * cb
+            assert rows + (R - 1) * dil[0] <= 256 and p["stages"] >= 2
+            seen_halo += 1
+        else:
+            # a box per tap (or a halo plan that no count tells apart)
+            assert p["k_blocks"] in (tap_blocks, S * cb)
+            seen_tap += 1
+    assert seen_halo > 50 and seen_none > 20
