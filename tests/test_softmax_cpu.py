@@ -171,3 +171,53 @@ def test_vector_rule_and_grid():
     assert plan(100, 65536)[1]["grid"] == 100
     assert plan(100000, 65536, x=260, per_sm=10)[1]["grid"] == 10 * 152  # two passes, a CTA per row
     assert plan(100000, 1 << 20, per_sm=10)[1]["grid"] == 8 * 10  # 10 clusters of 8
+
+
+def test_plan_invariants_on_random_rows():
+    """Seeded random shapes, types and alignments: each plan's kind follows
+    from the row (staged when 16-byte aligned, 256 B to 64 KB and at most
+    16 x 32 x 8 vectors; long rows streamed twice when aligned and longer,
+    on clusters that keep 152 slices within 64 MB of L2; register kernels
+    otherwise), its threads hold the whole row, its slots fit the 200 KB
+    budget, and its HBM bytes count X twice exactly when it reads X twice."""
+    import random
+    rng = random.Random(7919)
+    kinds = {"staged": 0, "long": 0, "register": 0}
+    for _ in range(600):
+        xdt, ydt = rng.choice([DT_F32, DT_F16, DT_BF16]), rng.choice([DT_F32, DT_F16, DT_BF16])
+        ex, ey = (4 if xdt == DT_F32 else 2), (4 if ydt == DT_F32 else 2)
+        cols = rng.choice([rng.randint(1, 4096), rng.randint(4096, 40000), rng.randint(40000, 400000)])
+        rows = rng.randint(1, 3000)
+        aligned = rng.random() < 0.7
+        ldx = cols + (-cols) % 8 if aligned else cols + rng.randint(0, 3)
+        ldy = cols + (-cols) % 8 if aligned else cols
+        x = 256 if aligned else 256 + rng.choice([0, ex])
+        st, p = plan(rows, cols, x=x, ldx=ldx, xdt=xdt, ldy=ldy, ydt=ydt)
+        assert st == OK
+        vec = (x % 16 == 0) and (ldx * ex) % 16 == 0 and (ldy * ey) % 16 == 0
+        assert p["vec"] == (1 if vec else 0)
+        b = cols * ex
+        staged = vec and 256 <= b <= 64 * 1024 and b // 16 <= 16 * 32 * 8
+        if staged:
+            kinds["staged"] += 1
+            assert p["depth"] > 0 and p["mode_name"] in ("warp", "cta") and p["threads"] == 544
+            gw, unit, kv = p["group_warps"], p["unit_rows"], p["kv"]
+            assert gw in (1, 2, 4, 8, 16) and kv in (1, 2, 4, 8)
+            nvec = b // 16
+            holders = 32 if unit > 1 else 32 * gw
+            assert kv * holders >= nvec and (kv == 1 or (kv // 2) * holders < nvec)
+            assert p["hbm_bytes"] == rows * cols * (ex + ey)
+        elif vec and cols > 16384 and p["cluster"] <= 8 and p["depth"] > 0:
+            kinds["long"] += 1
+            cl, sl = p["cluster"], p["slice"]
+            assert p["mode_name"] == "stream" and p["depth"] == 6 and p["kv"] == 4
+            assert sl % 8 == 0 and sl * cl >= cols and (sl - 8) * cl < cols
+            assert cl == 1 or 152 * -(-cols // (cl // 2)) * ex > 64 << 20
+            assert p["hbm_bytes"] == rows * cols * (2 * ex + ey)
+        else:
+            kinds["register"] += 1
+            assert p["depth"] == 0
+            assert not vec or cols <= 16384 or b < 256, (rows, cols, xdt, ydt, p)
+            reads = 2 if p["mode_name"] == "stream" else 1
+            assert p["hbm_bytes"] == rows * cols * (reads * ex + ey)
+    assert min(kinds.values()) > 30, kinds
