@@ -457,3 +457,56 @@ def test_layernorm_plan_rejects():
     assert _ln_plan(-1, 64, 64)[0] == 1
     st, p = _ln_plan(0, 64, 64)
     assert st == 0 and p["path_name"] == "noop"
+
+
+def test_plan_invariants_on_random_problems():
+    """Seeded random GEMMs (shape, transposes, types, pointer and pitch
+    alignment, beta, SM count): every plan's tiles cover the (possibly
+    swapped) output once, the grid fits the SMs, the K loop is whole, operands
+    whose rows TMA cannot address are packed, the workspace holds what the
+    plan stores there, and every stream-K schedule covers each (tile,
+    k-block) exactly once."""
+    import random
+    rng = random.Random(4242)
+    seen = {}
+    for _ in range(500):
+        dt = rng.choice([(DT_BF16, DT_BF16, DT_BF16), (DT_F16, DT_F16, DT_F32),
+                         (DT_BF16, DT_BF16, DT_F32), TF32])
+        es = 4 if dt[0] == DT_F32 else 2
+        M = rng.choice([rng.randint(1, 64), rng.randint(65, 512), rng.randint(513, 6000)])
+        N = rng.choice([rng.randint(1, 256), rng.randint(257, 8192)])
+        K = rng.choice([rng.randint(1, 128), rng.randint(129, 8192)])
+        ta, tb = rng.choice("NT"), rng.choice("NT")
+        rows_a, cols_a = (M, K) if ta == "N" else (K, M)
+        rows_b, cols_b = (K, N) if tb == "N" else (N, K)
+        lda = cols_a + rng.choice([0, 0, (-cols_a) % 8, 1])
+        ldb = cols_b + rng.choice([0, 0, (-cols_b) % 8, 3])
+        ldc = N + rng.choice([0, (-N) % 8])
+        pa = 256 + rng.choice([0, 0, es])
+        sms = rng.choice([152, 148, 132, 7])
+        beta = rng.choice([0.0, 1.0])
+        st, p = lib.gemm_plan_query(ta, tb, M, N, K, 1.0, pa, lda, 256, ldb, beta, 256, ldc, dt,
+                                    num_sms=sms)
+        assert st == 0, (ta, tb, M, N, K, lda, ldb, ldc, dt)
+        path = p["path_name"]
+        seen[path] = seen.get(path, 0) + 1
+        if path not in ("tiled_1sm", "tiled_2sm", "skinny"):
+            continue
+        Mk, Nk = (N, M) if p["swap_ab"] else (M, N)
+        assert p["tiles_m"] == -(-Mk // p["block_m"]) and p["tiles_n"] == -(-Nk // p["block_n"])
+        assert p["num_tiles"] == p["tiles_m"] * p["tiles_n"]
+        assert 1 <= p["grid"] <= sms and (path != "tiled_2sm" or p["grid"] % 2 == 0)
+        assert p["k_blocks"] == -(-K // p["block_k"])
+        # TMA needs 16-byte row pitches and bases: otherwise the operand is packed
+        # (FP32 operands stored M/N-contiguous are transposed instead)
+        a_ok = (lda * es) % 16 == 0 and pa % 16 == 0
+        b_ok = (ldb * es) % 16 == 0
+        if not a_ok:
+            assert p["pack_a"] or p["transpose_ab"] or p["swap_ab"] and p["pack_b"], p
+        if not b_ok:
+            assert p["pack_b"] or p["transpose_ab"] or p["swap_ab"] and p["pack_a"], p
+        if p["sk_len"] > 0:
+            simulate_stream_k(p)
+        else:
+            assert p["sk_max_seg"] == 0 or p["sk_len"] == 0
+    assert seen.get("tiled_2sm", 0) > 20 and seen.get("tiled_1sm", 0) > 20 and seen.get("skinny", 0) > 10, seen
