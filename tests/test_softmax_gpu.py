@@ -205,7 +205,10 @@ def test_dominant_entry_everywhere(lib, orc, cols):
 
 
 def test_in_place_and_deterministic(lib, orc):
-    for cols in (1000, 10000, 100000, 200000):
+    """Y = X in place and three runs bitwise equal, in every split: warp
+    rows, a staged CTA row, long rows on one CTA and (400000 elements) long
+    rows on a cluster of 2."""
+    for cols in (1000, 10000, 100000, 200000, 400000):
         g = torch.Generator().manual_seed(cols)
         Xs = stored(torch.randn((7, cols), generator=g), cols, DT_BF16)
         Y = run(lib, Xs, cols, DT_BF16, inplace=True)
